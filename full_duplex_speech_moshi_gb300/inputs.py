@@ -1,0 +1,239 @@
+"""Seeded synthetic inputs for the Moshi/PersonaPlex per-frame decode step.
+
+This module is the only code shared by the GPU path's tests and bench and by the
+oracle's tests.  It holds shapes, seeds and random draws, and none of the decode
+step's arithmetic.
+
+Model shapes follow "PersonaPlex native LM audit" (clockless-atlas personaplex-research
+page), sections 3-5 (temporal block, depth block, parameter inventory).  Random-init
+distributions follow the workload statement of the decode benchmark: linear weights
+~N(0, 0.02) in bf16, embedding tables ~N(0, 1) in bf16, RMSNorm scales 1 + 0.1*N(0, 1)
+(so that scale application is exercised), per-frame IDs with text = pad ID 3 with
+probability 0.65 (else uniform 0..31999) and audio uniform 0..2047 with 10% set to -1.
+
+Draws are bf16 bit patterns (uint16).  A normal draw is made by an inverse-CDF table:
+a uniform 16-bit index picks one of 65536 equiprobable quantiles of N(mean, std), each
+rounded to nearest-even bf16.  Every tensor is cut into fixed chunks, each with its own
+PCG64 stream keyed by (seed, chunk), so results do not depend on the thread count.
+"""
+from __future__ import annotations
+
+import os
+import statistics
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, field, asdict
+from typing import Dict, List, Tuple
+
+import numpy as np
+
+# ----------------------------------------------------------------------------
+# configurations
+# ----------------------------------------------------------------------------
+
+DELAYS_17 = [0, 0, 1, 1, 1, 1, 1, 1, 1, 0, 1, 1, 1, 1, 1, 1, 1]
+
+
+@dataclass
+class ModelShape:
+    """Dimensions of the temporal stack and depformer (all integers are element counts)."""
+    D: int = 4096
+    H: int = 32
+    dh: int = 128
+    ffn: int = 11264          # gated hidden width (2*16896/3)
+    n_layers: int = 32
+    ctx: int = 3000
+    text_in: int = 32001      # text embedding rows (32000 = initial text ID)
+    text_out: int = 32000     # text head rows
+    audio_in: int = 2049      # audio embedding rows (2048 = initial audio ID)
+    n_streams: int = 17
+    delays: List[int] = field(default_factory=lambda: list(DELAYS_17))
+    init_text: int = 32000
+    init_audio: int = 2048
+    eps: float = 1e-8
+    rope_theta: float = 1e4
+    # depformer
+    dep_D: int = 1024
+    dep_H: int = 16
+    dep_dh: int = 64
+    dep_ffn: int = 2816       # gated hidden width (2*4224/3)
+    dep_layers: int = 6
+    dep_steps: int = 16
+    dep_ctx: int = 8
+    dep_card: int = 2048      # depth head rows
+    dep_text_in: int = 32001
+    dep_audio_in: int = 2049
+
+    def asdict(self) -> dict:
+        return asdict(self)
+
+
+FULL = ModelShape()
+
+
+def tiny_shape(**over) -> ModelShape:
+    """A small model with the same structure, used by fast parity tests."""
+    base = dict(D=256, H=2, dh=128, ffn=512, n_layers=2, ctx=16, text_in=301, text_out=300,
+                audio_in=65, init_text=300, init_audio=64, dep_D=256, dep_H=4, dep_dh=64,
+                dep_ffn=256, dep_layers=2, dep_steps=16, dep_ctx=8, dep_card=64,
+                dep_text_in=301, dep_audio_in=65)
+    base.update(over)
+    return ModelShape(**base)
+
+
+# ----------------------------------------------------------------------------
+# tensor inventory (names, shapes, distributions)
+# ----------------------------------------------------------------------------
+
+EMB, LINEAR, NORM = "emb", "linear", "norm"
+
+
+def tensor_specs(s: ModelShape, depformer: bool = True) -> List[Tuple[str, Tuple[int, ...], str]]:
+    """Canonical tensor order; weights are [out, in] as stored by PyTorch.
+
+    The order is the layout contract used by the oracle's C API and by the tests that
+    build the GPU context: index i of this list gets seed 1000 + i.
+    """
+    out: List[Tuple[str, Tuple[int, ...], str]] = []
+    out.append(("text_emb", (s.text_in, s.D), EMB))
+    for i in range(s.n_streams - 1):
+        out.append((f"emb.{i}", (s.audio_in, s.D), EMB))
+    for l in range(s.n_layers):
+        out.append((f"layers.{l}.norm1", (s.D,), NORM))
+        out.append((f"layers.{l}.in_proj", (3 * s.D, s.D), LINEAR))
+        out.append((f"layers.{l}.out_proj", (s.D, s.D), LINEAR))
+        out.append((f"layers.{l}.norm2", (s.D,), NORM))
+        out.append((f"layers.{l}.linear_in", (2 * s.ffn, s.D), LINEAR))
+        out.append((f"layers.{l}.linear_out", (s.D, s.ffn), LINEAR))
+    out.append(("out_norm", (s.D,), NORM))
+    out.append(("text_linear", (s.text_out, s.D), LINEAR))
+    if depformer:
+        Q = s.dep_steps
+        for q in range(Q):
+            out.append((f"depformer_in.{q}", (s.dep_D, s.D), LINEAR))
+        out.append(("depformer_text_emb", (s.dep_text_in, s.dep_D), EMB))
+        for q in range(Q - 1):
+            out.append((f"depformer_emb.{q}", (s.dep_audio_in, s.dep_D), EMB))
+        for j in range(s.dep_layers):
+            out.append((f"depformer.{j}.norm1", (s.dep_D,), NORM))
+            out.append((f"depformer.{j}.in_proj", (Q * 3 * s.dep_D, s.dep_D), LINEAR))
+            out.append((f"depformer.{j}.out_proj", (Q * s.dep_D, s.dep_D), LINEAR))
+            out.append((f"depformer.{j}.norm2", (s.dep_D,), NORM))
+            for q in range(Q):
+                out.append((f"depformer.{j}.gating.{q}.linear_in", (2 * s.dep_ffn, s.dep_D), LINEAR))
+            for q in range(Q):
+                out.append((f"depformer.{j}.gating.{q}.linear_out", (s.dep_D, s.dep_ffn), LINEAR))
+        for q in range(Q):
+            out.append((f"linears.{q}", (s.dep_card, s.dep_D), LINEAR))
+    return out
+
+
+# ----------------------------------------------------------------------------
+# random draws
+# ----------------------------------------------------------------------------
+
+_CHUNK = 1 << 22
+_TABLES: Dict[Tuple[float, float], np.ndarray] = {}
+
+
+def _f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round float32 to nearest-even bf16 and return the 16-bit patterns."""
+    b = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    r = (b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _normal_table(mean: float, std: float) -> np.ndarray:
+    key = (mean, std)
+    if key not in _TABLES:
+        nd = statistics.NormalDist(mean, std)
+        q = np.array([nd.inv_cdf((i + 0.5) / 65536.0) for i in range(65536)], dtype=np.float64)
+        _TABLES[key] = _f32_to_bf16_bits(q.astype(np.float32))
+    return _TABLES[key]
+
+
+def _fill_chunk(out: np.ndarray, table: np.ndarray, seed: int, chunk: int) -> None:
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, chunk])))
+    lo = chunk * _CHUNK
+    hi = min(out.size, lo + _CHUNK)
+    idx = g.integers(0, 65536, size=hi - lo, dtype=np.uint16)
+    out[lo:hi] = table[idx]
+
+
+def normal_bf16(shape, mean: float, std: float, seed: int, pool: ThreadPoolExecutor | None = None) -> np.ndarray:
+    """bf16 bits of a seeded N(mean, std) draw of the given shape."""
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    table = _normal_table(mean, std)
+    nchunks = (n + _CHUNK - 1) // _CHUNK
+    if pool is None or nchunks == 1:
+        for c in range(nchunks):
+            _fill_chunk(out, table, seed, c)
+    else:
+        list(pool.map(lambda c: _fill_chunk(out, table, seed, c), range(nchunks)))
+    return out.reshape(shape)
+
+
+_DIST = {EMB: (0.0, 1.0), LINEAR: (0.0, 0.02), NORM: (1.0, 0.1)}
+
+
+def make_weights(s: ModelShape, depformer: bool = True, base_seed: int = 1000,
+                 threads: int | None = None) -> Dict[str, np.ndarray]:
+    """All tensors of `tensor_specs(s)` as bf16 bit arrays (uint16), keyed by name."""
+    specs = tensor_specs(s, depformer)
+    threads = threads or min(32, os.cpu_count() or 1)
+    out: Dict[str, np.ndarray] = {}
+    with ThreadPoolExecutor(threads) as pool:
+        for i, (name, shape, kind) in enumerate(specs):
+            mean, std = _DIST[kind]
+            out[name] = normal_bf16(shape, mean, std, base_seed + i, pool)
+    return out
+
+
+def make_ids(s: ModelShape, T: int, B: int = 1, seed: int = 2000, pad_id: int = 3,
+             pad_prob: float = 0.65, audio_card: int = 2048, drop_prob: float = 0.10) -> np.ndarray:
+    """Per-frame undelayed token IDs, int32 [T, B, n_streams].
+
+    Stream 0 is text: `pad_id` with probability `pad_prob`, else uniform over the text
+    vocabulary below the initial ID.  Streams 1.. are audio: uniform 0..audio_card-1,
+    each replaced by -1 (no input) with probability `drop_prob`.
+    """
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, B, T])))
+    ids = np.empty((T, B, s.n_streams), dtype=np.int32)
+    text_hi = min(s.init_text, s.text_in - 1)
+    is_pad = g.random((T, B)) < pad_prob
+    txt = g.integers(0, text_hi, size=(T, B))
+    ids[:, :, 0] = np.where(is_pad, min(pad_id, text_hi - 1), txt)
+    card = min(audio_card, s.init_audio)
+    aud = g.integers(0, card, size=(T, B, s.n_streams - 1))
+    drop = g.random((T, B, s.n_streams - 1)) < drop_prob
+    ids[:, :, 1:] = np.where(drop, -1, aud)
+    return ids
+
+
+def make_supplied_codes(s: ModelShape, T: int, B: int = 1, seed: int = 4000, n_generated: int = 8) -> np.ndarray:
+    """Depformer supplied codes, int32 [T, B, dep_steps]: -1 (generate) for the first
+    `n_generated` positions, uniform 0..dep_card-1 for the rest."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, B, T])))
+    sup = g.integers(0, s.dep_card, size=(T, B, s.dep_steps)).astype(np.int32)
+    sup[:, :, :n_generated] = -1
+    return sup
+
+
+def make_cache_lengths(B: int, lo: int = 64, hi: int = 3000, seed: int = 3000) -> np.ndarray:
+    """Per-stream prefilled cache lengths, uniform lo..hi inclusive."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, B])))
+    return g.integers(lo, hi + 1, size=B).astype(np.int32)
+
+
+def make_kv_history(s: ModelShape, n_pos: int, seed: int, layer: int, stream: int,
+                    pool: ThreadPoolExecutor | None = None) -> Tuple[np.ndarray, np.ndarray]:
+    """Seeded stand-in K/V history for one (layer, stream): bf16 bits [H, n_pos, dh] each,
+    ~N(0, 1).  Attention cost does not depend on cache contents, and both sides read
+    the same bits."""
+    k = normal_bf16((s.H, n_pos, s.dh), 0.0, 1.0, seed * 1000003 + layer * 1009 + stream * 2 + 0, pool)
+    v = normal_bf16((s.H, n_pos, s.dh), 0.0, 1.0, seed * 1000003 + layer * 1009 + stream * 2 + 1, pool)
+    return k, v
