@@ -1,0 +1,98 @@
+// Delay assembly, ID validation and the 17-stream embedding gather-sum
+// ("PersonaPlex native LM audit": section 3 "Input embedding sum" -- x is the sum of the
+// 17 table rows, ID -1 is an exact zero vector, -2 never a valid input; section 7 "One
+// exact generator step" -- stream delays and initial IDs).
+//
+// Grid (ceil(D / 1024), B), 128 threads; thread t of CTA (cx, b) sums columns
+// cx*1024 + 8t .. +7 of the 17 selected rows with 16-byte loads.
+//
+// Per stream k of batch row b at position p = pos[b]:
+//   id_k    = ids[b][k], or the stream's last selected token when ids[b][k] == -3;
+//   in[k]   = id_k                          if delay_k == 0,
+//             resolved id of frame p-delay_k (ring slot (p - delay_k) & 3)
+//                                           if p - delay_k >= first_pos[b],
+//             the stream's initial ID       otherwise.
+// If any resolved ID of any row is outside -1..rows-1 the frame is aborted: the status
+// word records PM_DEV_ERR_INVALID_ID, the abort flag is raised for the rest of the frame,
+// and no state changes.
+#include "pm_kernels.h"
+
+namespace pm {
+namespace {
+
+__global__ void __launch_bounds__(128) k_embed(const EmbedParams p) {
+    __shared__ int s_in[PM_MAX_STREAMS_DEV];
+    pdl_trigger();
+    pdl_wait();
+    const int b = blockIdx.y;
+    const int tid = threadIdx.x;
+    const int S = p.n_streams;
+
+    // validate every row's IDs (cheap: B * 17 values) so all CTAs agree on the abort
+    int bad = 0;
+    for (int i = tid; i < p.B * S; i += blockDim.x) {
+        const int bb = i / S, k = i % S;
+        int id = p.io->ids[i];
+        if (id == -3) id = p.st.sel[(size_t)bb * PM_MAX_STREAMS_DEV + k];
+        if (id < -1 || id >= p.rows[k]) bad = 1;
+    }
+    bad = __syncthreads_or(bad);
+
+    if (tid < S) {
+        const int k = tid;
+        int id = p.io->ids[(size_t)b * S + k];
+        if (id == -3) id = p.st.sel[(size_t)b * PM_MAX_STREAMS_DEV + k];
+        const int pos = p.st.pos[b];
+        const int src = pos - p.delays[k];
+        int in;
+        if (p.delays[k] == 0)
+            in = id;
+        else if (src >= p.st.first_pos[b])
+            in = p.st.ring[((size_t)b * 4 + (src & 3)) * PM_MAX_STREAMS_DEV + k];
+        else
+            in = p.init_id[k];
+        s_in[k] = in;
+        if (!bad && blockIdx.x == 0) p.st.ring[((size_t)b * 4 + (pos & 3)) * PM_MAX_STREAMS_DEV + k] = id;
+    }
+    if (blockIdx.x == 0 && b == 0 && tid == 0) {
+        p.st.status[1] = bad ? 1u : 0u;
+        if (bad) set_status(p.st.status, PM_DEV_ERR_INVALID_ID);
+    }
+    __syncthreads();
+    if (bad) return;
+
+    const int col = blockIdx.x * 1024 + 8 * tid;
+    if (col >= p.D) return;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int k = 0; k < S; ++k) {
+        const int id = s_in[k];
+        if (id < 0) continue;  // -1: exact zero contribution
+        const uint4 w = *reinterpret_cast<const uint4*>(p.tables[k] + (size_t)id * p.D + col);
+        acc[0] += bf16lo(w.x); acc[1] += bf16hi(w.x);
+        acc[2] += bf16lo(w.y); acc[3] += bf16hi(w.y);
+        acc[4] += bf16lo(w.z); acc[5] += bf16hi(w.z);
+        acc[6] += bf16lo(w.w); acc[7] += bf16hi(w.w);
+    }
+    float4* dst = reinterpret_cast<float4*>(p.x + (size_t)b * p.D + col);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+}  // namespace
+
+cudaError_t launch_embed(const EmbedParams& p, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((p.D + 1023) / 1024), (unsigned)p.B);
+    cfg.blockDim = dim3(128);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, k_embed, p);
+}
+
+}  // namespace pm

@@ -1,0 +1,413 @@
+// Weight-streaming GEMV for the batch-1 decode step: y = W x with W bf16 [rows][K]
+// (PyTorch [out, in]), x fp32, fp32 accumulation.  Every projection of the temporal
+// block and of the depformer runs through this kernel ("PersonaPlex native LM audit",
+// sections 3 and 4: fused QKV, W_O, SwiGLU linear_in / linear_out, text head, depth
+// projections and heads).
+//
+// Design (HBM-bound: each weight byte is read once, ~1 flop per byte):
+//  * One CTA per SM per batch row.  CTA c owns a contiguous, balanced range of units
+//    (rows, or row pairs when the epilogue needs two rows together), so its weights are
+//    one or two contiguous byte ranges.
+//  * A producer thread streams the range through a ring of shared-memory stages with 1-D
+//    bulk copies (cp.async.bulk, TMA engine, L2 evict-first).  It issues the first ring's
+//    worth of copies before griddepcontrol.wait, so with programmatic dependent launch the
+//    weights of kernel i+1 are already in flight while kernel i finishes.
+//  * Consumer warps split each row's K dimension P ways; each lane keeps its fixed slice
+//    of the (normalised) input vector in registers, so shared memory carries only weights.
+//    Per stage a warp reduces its row slice with shuffles and leaves one partial per
+//    (row, slice) in shared memory; the epilogue adds the P partials per row.
+//  * Prologue: optional RMSNorm of x (fp32 arithmetic, eps inside the sqrt, learned
+//    scale), computed per CTA from the full vector.  Epilogues fuse what follows the
+//    projection: residual add, SwiGLU, RoPE + KV-ring append, text-head argmax, ...
+#include <math.h>
+
+#include "pm_kernels.h"
+
+namespace pm {
+
+namespace {
+
+__device__ __forceinline__ void consumer_bar(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+template <int CH, int PRO, int EPI, int UNIT>
+__global__ void __launch_bounds__(544, 1) k_gemv(const GemvParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int RPU = (UNIT == U_ROW) ? 1 : 2;
+    const int W = p.warps;
+    const int P = p.P;
+    const int K = p.K;
+    const uint32_t row_bytes = (uint32_t)K * 2u;
+    uint8_t* stages = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)p.nst * p.stage_bytes);
+    uint64_t* empty = full + p.nst;
+    float* partial = reinterpret_cast<float*>(empty + p.nst);
+    float* red = partial + (size_t)p.units_cta_max * RPU * P;  // [32] scratch
+    __shared__ int s_flags[4];  // [0] timeout seen, [1] abort, [2] stages issued
+
+    const int b = blockIdx.x % p.B;
+    const int c = blockIdx.x / p.B;
+    const int u0 = (int)((long long)c * p.n_units / p.grid_per_b);
+    const int u1 = (int)((long long)(c + 1) * p.n_units / p.grid_per_b);
+    const int nu = u1 - u0;
+    const int nstages = (nu + p.upst - 1) / p.upst;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.nst; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], (uint32_t)W);
+        }
+        fence_barrier_init();
+        s_flags[0] = 0;
+        s_flags[1] = 0;
+        s_flags[2] = 0;
+    }
+    __syncthreads();
+    pdl_trigger();
+
+    if (warp == W) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            for (int k = 0; k < nstages; ++k) {
+                const int slot = k % p.nst;
+                if (k >= p.nst) {
+                    if (!mbar_wait(&empty[slot], (uint32_t)((k / p.nst) - 1) & 1u)) {
+                        s_flags[0] = 1;
+                        set_status(p.st.status, PM_DEV_ERR_TIMEOUT);
+                        break;
+                    }
+                }
+                const int ua = u0 + k * p.upst;
+                const int n = min(p.upst, u1 - ua);
+                uint8_t* dst = stages + (size_t)slot * p.stage_bytes;
+                if (UNIT == U_PAIR_SPLIT) {
+                    const uint32_t bytes = (uint32_t)n * row_bytes;
+                    mbar_arrive_expect_tx(&full[slot], 2u * bytes);
+                    bulk_g2s(dst, p.W + (size_t)ua * K, bytes, &full[slot], pol);
+                    bulk_g2s(dst + (size_t)p.upst * row_bytes, p.W + (size_t)(ua + p.split_rows) * K, bytes,
+                             &full[slot], pol);
+                } else {
+                    const uint32_t bytes = (uint32_t)(n * RPU) * row_bytes;
+                    mbar_arrive_expect_tx(&full[slot], bytes);
+                    bulk_g2s(dst, p.W + (size_t)ua * RPU * K, bytes, &full[slot], pol);
+                }
+                s_flags[2] = k + 1;
+            }
+        }
+    } else {
+        // ------------------------------ consumers ------------------------------
+        pdl_wait();
+        const bool abort_frame = *(volatile uint32_t*)&p.st.status[1] != 0u;
+        if (threadIdx.x == 0) s_flags[1] = abort_frame ? 1 : 0;
+        const int r = warp / P;   // stage row this warp reduces
+        const int pp = warp % P;  // K slice
+        const int kslice = K / P;
+        float xr[CH * 8];
+        const float* xb = p.x + (size_t)b * p.x_stride + (size_t)pp * kslice;
+#pragma unroll
+        for (int ci = 0; ci < CH; ++ci) {
+            const float4* src = reinterpret_cast<const float4*>(xb + 8 * (lane + 32 * ci));
+            float4 a = src[0], bb = src[1];
+            xr[8 * ci + 0] = a.x; xr[8 * ci + 1] = a.y; xr[8 * ci + 2] = a.z; xr[8 * ci + 3] = a.w;
+            xr[8 * ci + 4] = bb.x; xr[8 * ci + 5] = bb.y; xr[8 * ci + 6] = bb.z; xr[8 * ci + 7] = bb.w;
+        }
+        if (PRO == PRO_RMSNORM) {
+            // warps of stage row 0 cover every column exactly once
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < CH * 8; ++i) ss = fmaf(xr[i], xr[i], ss);
+            ss = warp_sum(ss);
+            if (r == 0 && lane == 0) red[pp] = ss;
+            consumer_bar(32 * W);
+            float tot = 0.f;
+            for (int i = 0; i < P; ++i) tot += red[i];
+            const float inv = 1.0f / sqrtf(tot / (float)K + p.eps);
+            const uint16_t* al = p.alpha + (size_t)pp * kslice;
+#pragma unroll
+            for (int ci = 0; ci < CH; ++ci) {
+                const uint4 av = *reinterpret_cast<const uint4*>(al + 8 * (lane + 32 * ci));
+                xr[8 * ci + 0] *= inv * bf16lo(av.x); xr[8 * ci + 1] *= inv * bf16hi(av.x);
+                xr[8 * ci + 2] *= inv * bf16lo(av.y); xr[8 * ci + 3] *= inv * bf16hi(av.y);
+                xr[8 * ci + 4] *= inv * bf16lo(av.z); xr[8 * ci + 5] *= inv * bf16hi(av.z);
+                xr[8 * ci + 6] *= inv * bf16lo(av.w); xr[8 * ci + 7] *= inv * bf16hi(av.w);
+            }
+            if (EPI == E_HEAD && c == 0 && r == 0) {
+                // the normalised vector is the hidden state h: publish it once per batch row
+                float* dsts[2] = {p.h_internal ? p.h_internal + (size_t)b * K : nullptr,
+                                  p.io->hidden ? p.io->hidden + (size_t)b * K : nullptr};
+                for (int t = 0; t < 2; ++t) {
+                    if (!dsts[t] || abort_frame) continue;
+                    float* hb = dsts[t] + (size_t)pp * kslice;
+#pragma unroll
+                    for (int ci = 0; ci < CH; ++ci) {
+                        float4* d4 = reinterpret_cast<float4*>(hb + 8 * (lane + 32 * ci));
+                        d4[0] = make_float4(xr[8 * ci + 0], xr[8 * ci + 1], xr[8 * ci + 2], xr[8 * ci + 3]);
+                        d4[1] = make_float4(xr[8 * ci + 4], xr[8 * ci + 5], xr[8 * ci + 6], xr[8 * ci + 7]);
+                    }
+                }
+            }
+        }
+        int i_unit, j_row;
+        if (UNIT == U_PAIR_SPLIT) {
+            j_row = r / p.upst;
+            i_unit = r % p.upst;
+        } else {
+            i_unit = r / RPU;
+            j_row = r % RPU;
+        }
+        for (int k = 0; k < nstages; ++k) {
+            const int slot = k % p.nst;
+            if (!mbar_wait(&full[slot], (uint32_t)(k / p.nst) & 1u)) {
+                s_flags[0] = 1;
+                set_status(p.st.status, PM_DEV_ERR_TIMEOUT);
+                break;
+            }
+            const int n = min(p.upst, u1 - (u0 + k * p.upst));
+            if (i_unit < n) {
+                const uint4* wrow = reinterpret_cast<const uint4*>(stages + (size_t)slot * p.stage_bytes +
+                                                                   (size_t)r * row_bytes + (size_t)pp * kslice * 2);
+                float acc = 0.f;
+#pragma unroll
+                for (int ci = 0; ci < CH; ++ci) acc += dot8(wrow[lane + 32 * ci], xr + 8 * ci);
+                acc = warp_sum(acc);
+                if (lane == 0) partial[((size_t)(k * p.upst + i_unit) * RPU + j_row) * P + pp] = acc;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+    }
+    __syncthreads();
+
+    if (s_flags[0]) {
+        // a wait ran out: let any copy still in flight land before the CTA exits
+        if (threadIdx.x == 0) {
+            const int issued = s_flags[2];
+            for (int k = issued - p.nst < 0 ? 0 : issued - p.nst; k < issued; ++k)
+                (void)mbar_wait(&full[k % p.nst], (uint32_t)(k / p.nst) & 1u);
+        }
+        return;
+    }
+    const bool aborted = s_flags[1] != 0;
+    const int nthr = 32 * W;
+    const int tid = threadIdx.x;
+
+    // ------------------------------ epilogues ------------------------------
+    auto rowsum = [&](int lu, int j) -> float {
+        const float* pr = partial + ((size_t)lu * RPU + j) * P;
+        float s = 0.f;
+        for (int i = 0; i < P; ++i) s += pr[i];
+        return s;
+    };
+
+    if (EPI == E_STORE || EPI == E_RESIDUAL || EPI == E_EMB_ADD) {
+        if (aborted || tid >= nthr) return;
+        float* yb = p.y + (size_t)b * p.y_stride;
+        int tok = 0;
+        if (EPI == E_EMB_ADD) tok = (p.q == 0) ? p.st.dep_tok[b] : p.st.dep_codes[(size_t)b * p.Q + p.q - 1];
+        for (int lu = tid; lu < nu; lu += nthr) {
+            const int row = u0 + lu;
+            float v = rowsum(lu, 0);
+            if (EPI == E_RESIDUAL) v += yb[row];
+            if (EPI == E_EMB_ADD) {
+                const uint16_t e = p.emb[(size_t)tok * p.y_stride + row];
+                v += __uint_as_float((uint32_t)e << 16);
+            }
+            yb[row] = v;
+        }
+    } else if (EPI == E_SWIGLU) {
+        if (aborted || tid >= nthr) return;
+        float* yb = p.y + (size_t)b * p.y_stride;
+        for (int lu = tid; lu < nu; lu += nthr) {
+            const float g = rowsum(lu, 0);
+            const float z = rowsum(lu, 1);
+            yb[u0 + lu] = g / (1.0f + expf(-g)) * z;
+        }
+    } else if (EPI == E_QKV_ROPE) {
+        if (aborted || tid >= nthr) return;
+        const int pos = p.st.pos[b];
+        const int slot = pos % p.ctx;
+        for (int lu = tid; lu < nu; lu += nthr) {
+            const int row = 2 * (u0 + lu);
+            float a = rowsum(lu, 0), bb = rowsum(lu, 1);
+            const int sec = row / p.D;
+            const int idx = row - sec * p.D;
+            const int h = idx / p.dh, d = idx % p.dh;
+            if (sec < 2) {
+                double sn, cs;
+                sincos((double)pos * p.rope_freq[d >> 1], &sn, &cs);
+                const float c = (float)cs, s = (float)sn;
+                const float ra = a * c - bb * s;
+                const float rb = a * s + bb * c;
+                a = ra;
+                bb = rb;
+            }
+            if (sec == 0) {
+                *reinterpret_cast<float2*>(p.y + (size_t)b * p.y_stride + idx) = make_float2(a, bb);
+            } else {
+                uint16_t* cache = (sec == 1) ? p.kc : p.vc;
+                const size_t off = (((size_t)b * p.H + h) * p.ctx + slot) * p.dh + d;
+                const uint32_t packed = (uint32_t)f32_to_bf16_rne(a) | ((uint32_t)f32_to_bf16_rne(bb) << 16);
+                *reinterpret_cast<uint32_t*>(cache + off) = packed;
+            }
+        }
+    } else if (EPI == E_DEP_QKV) {
+        if (aborted || tid >= nthr) return;
+        const int Dd = p.D, dhd = p.dh;
+        for (int lu = tid; lu < nu; lu += nthr) {
+            const int row = u0 + lu;
+            const float v = rowsum(lu, 0);
+            const int sec = row / Dd;
+            const int idx = row - sec * Dd;
+            if (sec == 0) {
+                p.y[(size_t)b * p.y_stride + idx] = v;
+            } else {
+                const int h = idx / dhd, d = idx % dhd;
+                uint16_t* cache = (sec == 1) ? p.dkc : p.dvc;
+                cache[(((size_t)b * p.H + h) * p.Q + p.q) * dhd + d] = f32_to_bf16_rne(v);
+            }
+        }
+    } else if (EPI == E_HEAD || EPI == E_DEP_HEAD) {
+        if (aborted) return;
+        float* out = nullptr;
+        if (EPI == E_HEAD) {
+            if (p.io->logits) out = p.io->logits + (size_t)b * p.y_stride;
+        } else {
+            if (p.dio->logits) out = p.dio->logits + ((size_t)b * p.Q + p.q) * p.y_stride;
+        }
+        unsigned long long best = 0ull;
+        if (tid < nthr) {
+            for (int lu = tid; lu < nu; lu += nthr) {
+                const int row = u0 + lu;
+                const float v = rowsum(lu, 0);
+                if (out) out[row] = v;
+                best = umax64(best, pack_argmax(v, (uint32_t)row));
+            }
+        }
+        // CTA max of the packed keys
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xffffffffu, best, o));
+        __shared__ unsigned long long s_best[32];
+        if (lane == 0) s_best[warp] = best;
+        __syncthreads();
+        if (tid == 0) {
+            unsigned long long m = 0ull;
+            for (int i = 0; i < W + 1; ++i) m = umax64(m, s_best[i]);
+            unsigned long long* acc = (EPI == E_HEAD) ? &p.st.amax[b] : &p.st.dep_amax[b];
+            uint32_t* cnt = (EPI == E_HEAD) ? &p.st.head_count[b] : &p.st.dep_count[b];
+            atomicMax(acc, m);
+            __threadfence();
+            const uint32_t done = atomicAdd(cnt, 1u);
+            if (done == (uint32_t)p.grid_per_b - 1u) {
+                __threadfence();
+                const unsigned long long key = atomicExch(acc, 0ull);
+                *cnt = 0u;
+                const int32_t am = (int32_t)unpack_argmax_index(key);
+                if (EPI == E_HEAD) {
+                    if (p.io->token) p.io->token[b] = am;
+                    p.st.sel[(size_t)b * PM_MAX_STREAMS_DEV + 0] = am;
+                    p.st.pos[b] += 1;
+                } else {
+                    const int32_t sup = p.st.dep_sup[(size_t)b * p.Q + p.q];
+                    const int32_t code = sup >= 0 ? sup : am;
+                    p.st.dep_codes[(size_t)b * p.Q + p.q] = code;
+                    if (p.dio->codes) p.dio->codes[(size_t)b * p.Q + p.q] = code;
+                    if (p.q == p.Q - 1) {
+                        // feedback slots: stream k = 1 + q' takes depth code q'
+                        for (int qq = 0; qq < p.Q && 1 + qq < p.n_streams; ++qq)
+                            p.st.sel[(size_t)b * PM_MAX_STREAMS_DEV + 1 + qq] =
+                                p.st.dep_codes[(size_t)b * p.Q + qq];
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <int PRO, int EPI, int UNIT>
+cudaError_t launch_t(const GemvParams& p, cudaStream_t s, bool pdl) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.grid_per_b * p.B));
+    cfg.blockDim = dim3((unsigned)(32 * (p.warps + 1)));
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    switch (p.CH) {
+        case 4: return cudaLaunchKernelEx(&cfg, k_gemv<4, PRO, EPI, UNIT>, p);
+        case 2: return cudaLaunchKernelEx(&cfg, k_gemv<2, PRO, EPI, UNIT>, p);
+        case 1: return cudaLaunchKernelEx(&cfg, k_gemv<1, PRO, EPI, UNIT>, p);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int PRO, int EPI, int UNIT>
+cudaError_t prepare_t() {
+    const int mx = 220 * 1024;  // opt-in limit minus room for static shared memory
+    cudaError_t e = cudaFuncSetAttribute(k_gemv<4, PRO, EPI, UNIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_gemv<2, PRO, EPI, UNIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_gemv<1, PRO, EPI, UNIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, mx);
+    return e;
+}
+
+#define PM_GEMV_VARIANTS(X)                      \
+    X(PRO_RMSNORM, E_QKV_ROPE, U_PAIR_ADJ)       \
+    X(PRO_PLAIN, E_RESIDUAL, U_ROW)              \
+    X(PRO_RMSNORM, E_SWIGLU, U_PAIR_SPLIT)       \
+    X(PRO_RMSNORM, E_HEAD, U_ROW)                \
+    X(PRO_PLAIN, E_EMB_ADD, U_ROW)               \
+    X(PRO_RMSNORM, E_DEP_QKV, U_ROW)             \
+    X(PRO_PLAIN, E_DEP_HEAD, U_ROW)              \
+    X(PRO_PLAIN, E_STORE, U_ROW)
+
+}  // namespace
+
+bool plan_gemv(GemvParams& p, int rpu, int num_sms) {
+    const int K = p.K;
+    if (K <= 0 || K % 256 != 0 || p.n_units <= 0) return false;
+    p.CH = (K % 1024 == 0) ? 4 : (K % 512 == 0) ? 2 : 1;
+    p.P = K / (256 * p.CH);
+    if (rpu * p.P > 16) return false;
+    const int row_bytes = 2 * K;
+    int upst = 16384 / (row_bytes * rpu);
+    if (upst < 1) upst = 1;
+    while (upst > 1 && upst * rpu * p.P > 16) --upst;
+    p.upst = upst;
+    p.warps = upst * rpu * p.P;
+    p.stage_bytes = (uint32_t)(upst * rpu * row_bytes);
+    int nst = (int)(98304u / p.stage_bytes);
+    if (nst < 2) nst = 2;
+    if (nst > 16) nst = 16;
+    p.nst = nst;
+    p.grid_per_b = p.n_units < num_sms ? p.n_units : num_sms;
+    p.units_cta_max = (p.n_units + p.grid_per_b - 1) / p.grid_per_b;
+    p.smem = (size_t)nst * p.stage_bytes + 16u * (size_t)nst + (size_t)p.units_cta_max * rpu * p.P * 4u + 32u * 4u;
+    if (p.smem > 220u * 1024u) return false;
+    return true;
+}
+
+cudaError_t gemv_prepare() {
+    cudaError_t e = cudaSuccess;
+#define PM_PREP(PR, EP, UN) \
+    if (e == cudaSuccess) e = prepare_t<PR, EP, UN>();
+    PM_GEMV_VARIANTS(PM_PREP)
+#undef PM_PREP
+    return e;
+}
+
+cudaError_t launch_gemv(int pro, int epi, int unit, const GemvParams& p, cudaStream_t s, bool pdl) {
+#define PM_CASE(PR, EP, UN) \
+    if (pro == PR && epi == EP && unit == UN) return launch_t<PR, EP, UN>(p, s, pdl);
+    PM_GEMV_VARIANTS(PM_CASE)
+#undef PM_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace pm

@@ -1,0 +1,834 @@
+// C ABI of the decode step (declared in include/pm.h): context set-up, argument
+// validation, and one CUDA graph per (call kind, batch size) in which every kernel after
+// the first is a programmatic dependent launch.
+//
+// Per-call inputs and output pointers travel through small device-side structs (FrameIO,
+// DepIO) refreshed by one host-to-device copy before each graph launch, so a graph is
+// captured once per batch size and replayed for every frame.  Positions, the delay ring
+// and the last selected tokens live in device memory and are advanced by the kernels.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/pm.h"
+#include "pm_kernels.h"
+
+using namespace pm;
+
+namespace {
+
+constexpr int kMaxB = 64;
+constexpr int kAttnSplitMax = 16;
+constexpr int kStagingSlots = 8;
+
+struct Staging {
+    uint8_t* host = nullptr;  // pinned
+    cudaEvent_t done = nullptr;
+};
+
+}  // namespace
+
+struct pm_ctx {
+    pm_config cfg{};
+    int device = 0;
+    int num_sms = 0;
+    cudaStream_t stream = nullptr;   // caller's stream: every launch goes here
+    cudaStream_t cap = nullptr;      // private stream used only for graph capture
+    bool has_dep = false;
+    // weights (device)
+    const uint16_t* tables[PM_MAX_STREAMS_DEV] = {};
+    std::vector<const uint16_t*> norm1, in_proj, out_proj, norm2, lin_in, lin_out;
+    const uint16_t* out_norm = nullptr;
+    const uint16_t* text_linear = nullptr;
+    std::vector<const uint16_t*> d_in, d_aemb, d_norm1, d_qkv, d_o, d_norm2, d_lin_in, d_lin_out, d_heads;
+    const uint16_t* d_temb = nullptr;
+    uint16_t* kv = nullptr;
+    // owned device memory
+    void* block = nullptr;
+    size_t block_bytes = 0;
+    DevState st{};
+    uint8_t* io_region = nullptr;      // FrameIO + ids
+    uint8_t* dio_region = nullptr;     // DepIO + text_tok + supplied
+    float *x = nullptr, *q = nullptr, *o = nullptr, *s = nullptr, *h = nullptr;
+    float* att_part = nullptr;
+    uint32_t* att_count = nullptr;
+    double* rope_freq = nullptr;
+    float *dz = nullptr, *dq = nullptr, *dout = nullptr, *ds = nullptr;
+    uint16_t* dkv = nullptr;
+    // staging
+    Staging slots[kStagingSlots];
+    int next_slot = 0;
+    // graphs
+    std::map<int, cudaGraphExec_t> frame_graphs, dep_graphs;
+    std::string err;
+};
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// message of the last pm_create failure on this thread (pm_last_error(NULL) returns it)
+static thread_local std::string g_create_err;
+
+static pm_status fail(pm_ctx* c, pm_status st, const std::string& msg) {
+    if (c) c->err = msg;
+    return st;
+}
+
+static pm_status cuda_fail(pm_ctx* c, cudaError_t e, const char* where) {
+    return fail(c, PM_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+#define PM_CUDA(call)                                          \
+    do {                                                       \
+        cudaError_t e_ = (call);                               \
+        if (e_ != cudaSuccess) return cuda_fail(c, e_, #call); \
+    } while (0)
+
+extern "C" size_t pm_kv_cache_bytes(const pm_config* cfg) {
+    if (!cfg) return 0;
+    return (size_t)cfg->n_layers * 2u * (size_t)cfg->B_max * (size_t)cfg->H * (size_t)cfg->ctx * (size_t)cfg->dh *
+           2u;
+}
+
+static const char* check_config(const pm_config* c) {
+    if (c->B_max < 1 || c->B_max > kMaxB) return "B_max must be 1..64";
+    if (c->dh != 128) return "temporal head width dh must be 128";
+    if (c->H < 1 || c->D != c->H * c->dh) return "D must equal H * dh";
+    if (c->D % 256 != 0 || c->ffn % 256 != 0) return "D and ffn must be multiples of 256";
+    if (c->n_layers < 1 || c->ctx < 1) return "n_layers and ctx must be positive";
+    if (c->n_streams < 1 || c->n_streams > PM_MAX_STREAMS) return "n_streams must be 1..32";
+    if (c->text_in < 1 || c->audio_in < 1 || c->text_out < 1) return "table sizes must be positive";
+    for (int k = 0; k < c->n_streams; ++k)
+        if (c->delays[k] < 0 || c->delays[k] > 3) return "delays must be 0..3";
+    if (c->init_text < 0 || c->init_text >= c->text_in) return "init_text outside the text table";
+    if (c->init_audio < 0 || c->init_audio >= c->audio_in) return "init_audio outside the audio tables";
+    if (!(c->eps > 0.f) || !(c->rope_theta > 0.f)) return "eps and rope_theta must be positive";
+    if (c->dep_layers > 0) {
+        if (c->dep_dh != 64 || c->dep_D != c->dep_H * c->dep_dh) return "depformer needs dep_dh 64 and dep_D = dep_H * 64";
+        if (c->dep_D % 256 != 0 || c->dep_ffn % 256 != 0) return "dep_D and dep_ffn must be multiples of 256";
+        if (c->dep_steps < 1 || c->dep_steps > 32) return "dep_steps must be 1..32";
+        if (c->dep_ctx < 1 || c->dep_ctx > 16) return "dep_ctx must be 1..16";
+        if (c->dep_card < 1 || c->dep_text_in < 1 || c->dep_audio_in < c->dep_card) return "bad depformer table sizes";
+    }
+    return nullptr;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// ------------------------------------------------------------------------------------
+// small state kernel (reset / position set)
+// ------------------------------------------------------------------------------------
+struct SetStateArgs {
+    DevState st;
+    int n;
+    int32_t pos[kMaxB];
+    int32_t apply[kMaxB];
+};
+
+__global__ void k_set_state(const SetStateArgs a) {
+    const int b = blockIdx.x;
+    if (b >= a.n || !a.apply[b]) return;
+    if (threadIdx.x == 0) {
+        a.st.pos[b] = a.pos[b];
+        a.st.first_pos[b] = a.pos[b];
+        a.st.amax[b] = 0ull;
+        a.st.head_count[b] = 0u;
+        a.st.dep_amax[b] = 0ull;
+        a.st.dep_count[b] = 0u;
+    }
+    if (threadIdx.x < PM_MAX_STREAMS_DEV) a.st.sel[(size_t)b * PM_MAX_STREAMS_DEV + threadIdx.x] = -2;
+}
+
+// ------------------------------------------------------------------------------------
+// graph construction
+// ------------------------------------------------------------------------------------
+static GemvParams base_params(pm_ctx* c) {
+    GemvParams p;
+    memset(&p, 0, sizeof p);
+    p.st = c->st;
+    p.eps = c->cfg.eps;
+    p.io = reinterpret_cast<const FrameIO*>(c->io_region);
+    p.dio = reinterpret_cast<const DepIO*>(c->dio_region);
+    p.n_streams = c->cfg.n_streams;
+    return p;
+}
+
+static pm_status plan(pm_ctx* c, GemvParams& p, int rpu, const char* what) {
+    if (!plan_gemv(p, rpu, c->num_sms)) return fail(c, PM_ERR_UNSUPPORTED, std::string("no GEMV plan for ") + what);
+    return PM_OK;
+}
+
+static int attn_splits(const pm_ctx* c, int B) {
+    int want = (2 * c->num_sms + B * c->cfg.H - 1) / (B * c->cfg.H);
+    if (want < 1) want = 1;
+    if (want > kAttnSplitMax) want = kAttnSplitMax;
+    return want;
+}
+
+static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
+    const pm_config& f = c->cfg;
+    const int D = f.D, F = f.ffn;
+    EmbedParams ep;
+    memset(&ep, 0, sizeof ep);
+    for (int k = 0; k < f.n_streams; ++k) {
+        ep.tables[k] = c->tables[k];
+        ep.rows[k] = (k == 0) ? f.text_in : f.audio_in;
+        ep.init_id[k] = (k == 0) ? f.init_text : f.init_audio;
+        ep.delays[k] = f.delays[k];
+    }
+    ep.io = reinterpret_cast<const FrameIO*>(c->io_region);
+    ep.st = c->st;
+    ep.x = c->x;
+    ep.D = D;
+    ep.B = B;
+    ep.n_streams = f.n_streams;
+    PM_CUDA(launch_embed(ep, s, false));
+
+    const size_t layer_elems = (size_t)f.B_max * f.H * f.ctx * f.dh;
+    for (int l = 0; l < f.n_layers; ++l) {
+        uint16_t* kc = c->kv + (size_t)(2 * l + 0) * layer_elems;
+        uint16_t* vc = c->kv + (size_t)(2 * l + 1) * layer_elems;
+        // RMSNorm1 + fused QKV + RoPE + KV append
+        GemvParams p = base_params(c);
+        p.W = c->in_proj[l];
+        p.K = D;
+        p.n_units = 3 * D / 2;
+        p.B = B;
+        p.x = c->x;
+        p.x_stride = D;
+        p.alpha = c->norm1[l];
+        p.y = c->q;
+        p.y_stride = D;
+        p.D = D;
+        p.H = f.H;
+        p.dh = f.dh;
+        p.ctx = f.ctx;
+        p.B_max = f.B_max;
+        p.kc = kc;
+        p.vc = vc;
+        p.rope_freq = c->rope_freq;
+        pm_status ps = plan(c, p, 2, "in_proj");
+        if (ps) return ps;
+        PM_CUDA(launch_gemv(PRO_RMSNORM, E_QKV_ROPE, U_PAIR_ADJ, p, s, true));
+        // attention
+        AttnParams ap;
+        memset(&ap, 0, sizeof ap);
+        ap.q = c->q;
+        ap.kc = kc;
+        ap.vc = vc;
+        ap.o = c->o;
+        ap.part = c->att_part;
+        ap.count = c->att_count;
+        ap.st = c->st;
+        ap.B = B;
+        ap.H = f.H;
+        ap.ctx = f.ctx;
+        ap.S = attn_splits(c, B);
+        ap.D = D;
+        ap.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dh));
+        PM_CUDA(launch_attn(ap, s, true));
+        // W_O + residual
+        p = base_params(c);
+        p.W = c->out_proj[l];
+        p.K = D;
+        p.n_units = D;
+        p.B = B;
+        p.x = c->o;
+        p.x_stride = D;
+        p.y = c->x;
+        p.y_stride = D;
+        ps = plan(c, p, 1, "out_proj");
+        if (ps) return ps;
+        PM_CUDA(launch_gemv(PRO_PLAIN, E_RESIDUAL, U_ROW, p, s, true));
+        // RMSNorm2 + linear_in + SwiGLU
+        p = base_params(c);
+        p.W = c->lin_in[l];
+        p.K = D;
+        p.n_units = F;
+        p.split_rows = F;
+        p.B = B;
+        p.x = c->x;
+        p.x_stride = D;
+        p.alpha = c->norm2[l];
+        p.y = c->s;
+        p.y_stride = F;
+        ps = plan(c, p, 2, "linear_in");
+        if (ps) return ps;
+        PM_CUDA(launch_gemv(PRO_RMSNORM, E_SWIGLU, U_PAIR_SPLIT, p, s, true));
+        // linear_out + residual
+        p = base_params(c);
+        p.W = c->lin_out[l];
+        p.K = F;
+        p.n_units = D;
+        p.B = B;
+        p.x = c->s;
+        p.x_stride = F;
+        p.y = c->x;
+        p.y_stride = D;
+        ps = plan(c, p, 1, "linear_out");
+        if (ps) return ps;
+        PM_CUDA(launch_gemv(PRO_PLAIN, E_RESIDUAL, U_ROW, p, s, true));
+    }
+    // final RMSNorm + text head + argmax + frame finalisation
+    GemvParams p = base_params(c);
+    p.W = c->text_linear;
+    p.K = D;
+    p.n_units = f.text_out;
+    p.B = B;
+    p.x = c->x;
+    p.x_stride = D;
+    p.alpha = c->out_norm;
+    p.y_stride = f.text_out;
+    p.h_internal = c->h;
+    pm_status ps = plan(c, p, 1, "text_linear");
+    if (ps) return ps;
+    PM_CUDA(launch_gemv(PRO_RMSNORM, E_HEAD, U_ROW, p, s, true));
+    return PM_OK;
+}
+
+static pm_status record_depformer(pm_ctx* c, int B, cudaStream_t s) {
+    const pm_config& f = c->cfg;
+    const int D = f.D, Dd = f.dep_D, Fd = f.dep_ffn, Q = f.dep_steps;
+    DepBeginParams bp;
+    memset(&bp, 0, sizeof bp);
+    bp.dio = reinterpret_cast<const DepIO*>(c->dio_region);
+    bp.st = c->st;
+    bp.h_internal = c->h;
+    bp.dep_sup = c->st.dep_sup;
+    bp.B = B;
+    bp.D = D;
+    bp.Q = Q;
+    bp.card = f.dep_card;
+    bp.text_rows = f.dep_text_in;
+    PM_CUDA(launch_dep_begin(bp, s, false));
+    const size_t dl_elems = (size_t)f.B_max * f.dep_H * Q * f.dep_dh;
+    for (int q = 0; q < Q; ++q) {
+        GemvParams p = base_params(c);
+        p.W = c->d_in[q];
+        p.K = D;
+        p.n_units = Dd;
+        p.B = B;
+        p.x = c->h;
+        p.x_stride = D;
+        p.y = c->dz;
+        p.y_stride = Dd;
+        p.emb = (q == 0) ? c->d_temb : c->d_aemb[q - 1];
+        p.q = q;
+        p.Q = Q;
+        pm_status ps = plan(c, p, 1, "depformer_in");
+        if (ps) return ps;
+        PM_CUDA(launch_gemv(PRO_PLAIN, E_EMB_ADD, U_ROW, p, s, true));
+        for (int j = 0; j < f.dep_layers; ++j) {
+            uint16_t* dkc = c->dkv + (size_t)(2 * j + 0) * dl_elems;
+            uint16_t* dvc = c->dkv + (size_t)(2 * j + 1) * dl_elems;
+            p = base_params(c);
+            p.W = c->d_qkv[j] + (size_t)q * 3 * Dd * Dd;
+            p.K = Dd;
+            p.n_units = 3 * Dd;
+            p.B = B;
+            p.x = c->dz;
+            p.x_stride = Dd;
+            p.alpha = c->d_norm1[j];
+            p.y = c->dq;
+            p.y_stride = Dd;
+            p.D = Dd;
+            p.H = f.dep_H;
+            p.dh = f.dep_dh;
+            p.Q = Q;
+            p.q = q;
+            p.dkc = dkc;
+            p.dvc = dvc;
+            ps = plan(c, p, 1, "depformer in_proj");
+            if (ps) return ps;
+            PM_CUDA(launch_gemv(PRO_RMSNORM, E_DEP_QKV, U_ROW, p, s, true));
+            DepAttnParams ap;
+            memset(&ap, 0, sizeof ap);
+            ap.q = c->dq;
+            ap.kc = dkc;
+            ap.vc = dvc;
+            ap.o = c->dout;
+            ap.st = c->st;
+            ap.B = B;
+            ap.Hd = f.dep_H;
+            ap.dhd = f.dep_dh;
+            ap.Q = Q;
+            ap.q_pos = q;
+            ap.dep_ctx = f.dep_ctx;
+            ap.Dd = Dd;
+            ap.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dep_dh));
+            PM_CUDA(launch_dep_attn(ap, s, true));
+            p = base_params(c);
+            p.W = c->d_o[j] + (size_t)q * Dd * Dd;
+            p.K = Dd;
+            p.n_units = Dd;
+            p.B = B;
+            p.x = c->dout;
+            p.x_stride = Dd;
+            p.y = c->dz;
+            p.y_stride = Dd;
+            ps = plan(c, p, 1, "depformer out_proj");
+            if (ps) return ps;
+            PM_CUDA(launch_gemv(PRO_PLAIN, E_RESIDUAL, U_ROW, p, s, true));
+            p = base_params(c);
+            p.W = c->d_lin_in[(size_t)j * Q + q];
+            p.K = Dd;
+            p.n_units = Fd;
+            p.split_rows = Fd;
+            p.B = B;
+            p.x = c->dz;
+            p.x_stride = Dd;
+            p.alpha = c->d_norm2[j];
+            p.y = c->ds;
+            p.y_stride = Fd;
+            ps = plan(c, p, 2, "depformer linear_in");
+            if (ps) return ps;
+            PM_CUDA(launch_gemv(PRO_RMSNORM, E_SWIGLU, U_PAIR_SPLIT, p, s, true));
+            p = base_params(c);
+            p.W = c->d_lin_out[(size_t)j * Q + q];
+            p.K = Fd;
+            p.n_units = Dd;
+            p.B = B;
+            p.x = c->ds;
+            p.x_stride = Fd;
+            p.y = c->dz;
+            p.y_stride = Dd;
+            ps = plan(c, p, 1, "depformer linear_out");
+            if (ps) return ps;
+            PM_CUDA(launch_gemv(PRO_PLAIN, E_RESIDUAL, U_ROW, p, s, true));
+        }
+        p = base_params(c);
+        p.W = c->d_heads[q];
+        p.K = Dd;
+        p.n_units = f.dep_card;
+        p.B = B;
+        p.x = c->dz;
+        p.x_stride = Dd;
+        p.y_stride = f.dep_card;
+        p.q = q;
+        p.Q = Q;
+        ps = plan(c, p, 1, "depformer head");
+        if (ps) return ps;
+        PM_CUDA(launch_gemv(PRO_PLAIN, E_DEP_HEAD, U_ROW, p, s, true));
+    }
+    return PM_OK;
+}
+
+typedef pm_status (*record_fn)(pm_ctx*, int, cudaStream_t);
+
+static pm_status get_graph(pm_ctx* c, std::map<int, cudaGraphExec_t>& cache, int B, record_fn rec,
+                           cudaGraphExec_t* out) {
+    auto it = cache.find(B);
+    if (it != cache.end()) {
+        *out = it->second;
+        return PM_OK;
+    }
+    PM_CUDA(cudaStreamBeginCapture(c->cap, cudaStreamCaptureModeThreadLocal));
+    pm_status st = rec(c, B, c->cap);
+    cudaGraph_t g = nullptr;
+    cudaError_t e = cudaStreamEndCapture(c->cap, &g);
+    if (st != PM_OK) {
+        if (g) cudaGraphDestroy(g);
+        return st;
+    }
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaStreamEndCapture");
+    cudaGraphExec_t ex = nullptr;
+    e = cudaGraphInstantiate(&ex, g, 0);
+    cudaGraphDestroy(g);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cudaGraphInstantiate");
+    cache[B] = ex;
+    *out = ex;
+    return PM_OK;
+}
+
+// pinned staging slot for one host->device copy; waits for the slot's previous copy
+static pm_status take_slot(pm_ctx* c, uint8_t** host, cudaEvent_t* ev) {
+    Staging& sl = c->slots[c->next_slot];
+    c->next_slot = (c->next_slot + 1) % kStagingSlots;
+    PM_CUDA(cudaEventSynchronize(sl.done));
+    *host = sl.host;
+    *ev = sl.done;
+    return PM_OK;
+}
+
+static bool is_device_ptr(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+// ------------------------------------------------------------------------------------
+// ABI
+// ------------------------------------------------------------------------------------
+static void free_ctx(pm_ctx* c) {
+    if (!c) return;
+    cudaSetDevice(c->device);
+    for (auto& kv : c->frame_graphs) cudaGraphExecDestroy(kv.second);
+    for (auto& kv : c->dep_graphs) cudaGraphExecDestroy(kv.second);
+    for (int i = 0; i < kStagingSlots; ++i) {
+        if (c->slots[i].done) cudaEventDestroy(c->slots[i].done);
+        if (c->slots[i].host) cudaFreeHost(c->slots[i].host);
+    }
+    if (c->cap) cudaStreamDestroy(c->cap);
+    if (c->block) cudaFree(c->block);
+    delete c;
+}
+
+extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* tw, const pm_depformer_weights* dw,
+                               void* kv_cache, void* cuda_stream, pm_ctx** out) {
+    if (!out) return PM_ERR_ARG;
+    *out = nullptr;
+    if (!cfg || !tw || !kv_cache) {
+        g_create_err = "pm_create: null config, weights or cache";
+        return PM_ERR_ARG;
+    }
+    if (const char* why = check_config(cfg)) {
+        g_create_err = std::string("pm_create: ") + why;
+        return PM_ERR_UNSUPPORTED;
+    }
+    pm_ctx* c = new pm_ctx();
+    c->cfg = *cfg;
+    const pm_config& f = c->cfg;
+    c->has_dep = dw != nullptr && f.dep_layers > 0;
+    c->stream = reinterpret_cast<cudaStream_t>(cuda_stream);
+    c->kv = reinterpret_cast<uint16_t*>(kv_cache);
+    cudaError_t last = cudaSuccess;
+    auto bail = [&](pm_status st, const char* what) {
+        g_create_err = std::string("pm_create: ") + what;
+        if (last != cudaSuccess) g_create_err += std::string(": ") + cudaGetErrorString(last);
+        cudaGetLastError();
+        free_ctx(c);
+        return st;
+    };
+    auto ck = [&](cudaError_t e) {
+        last = e;
+        return e != cudaSuccess;
+    };
+    if (ck(cudaGetDevice(&c->device))) return bail(PM_ERR_CUDA, "cudaGetDevice");
+    if (ck(cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device)))
+        return bail(PM_ERR_CUDA, "CUDA call failed");
+    if (!aligned16(kv_cache)) return bail(PM_ERR_ARG, "kv_cache not 16-byte aligned");
+
+    // weights
+    auto W = [](const void* p) { return reinterpret_cast<const uint16_t*>(p); };
+    bool ok = tw->text_emb && tw->out_norm && tw->text_linear && tw->norm1 && tw->in_proj && tw->out_proj &&
+              tw->norm2 && tw->linear_in && tw->linear_out;
+    if (!ok) return bail(PM_ERR_ARG, "null temporal weight pointer");
+    c->tables[0] = W(tw->text_emb);
+    for (int k = 1; k < f.n_streams; ++k) {
+        if (!tw->audio_emb[k - 1]) return bail(PM_ERR_ARG, "null audio embedding pointer");
+        c->tables[k] = W(tw->audio_emb[k - 1]);
+    }
+    for (int l = 0; l < f.n_layers; ++l) {
+        c->norm1.push_back(W(tw->norm1[l]));
+        c->in_proj.push_back(W(tw->in_proj[l]));
+        c->out_proj.push_back(W(tw->out_proj[l]));
+        c->norm2.push_back(W(tw->norm2[l]));
+        c->lin_in.push_back(W(tw->linear_in[l]));
+        c->lin_out.push_back(W(tw->linear_out[l]));
+    }
+    c->out_norm = W(tw->out_norm);
+    c->text_linear = W(tw->text_linear);
+    std::vector<const void*> all = {tw->text_emb, tw->out_norm, tw->text_linear};
+    for (int k = 1; k < f.n_streams; ++k) all.push_back(tw->audio_emb[k - 1]);
+    for (int l = 0; l < f.n_layers; ++l)
+        for (const void* p : {tw->norm1[l], tw->in_proj[l], tw->out_proj[l], tw->norm2[l], tw->linear_in[l],
+                              tw->linear_out[l]})
+            all.push_back(p);
+    if (c->has_dep) {
+        const int Q = f.dep_steps, J = f.dep_layers;
+        if (!dw->dep_in || !dw->text_emb || (Q > 1 && !dw->audio_emb) || !dw->norm1 || !dw->in_proj ||
+            !dw->out_proj || !dw->norm2 || !dw->linear_in || !dw->linear_out || !dw->heads)
+            return bail(PM_ERR_ARG, "missing depformer weight array");
+        c->d_temb = W(dw->text_emb);
+        all.push_back(dw->text_emb);
+        for (int q = 0; q < Q; ++q) {
+            c->d_in.push_back(W(dw->dep_in[q]));
+            c->d_heads.push_back(W(dw->heads[q]));
+            all.push_back(dw->dep_in[q]);
+            all.push_back(dw->heads[q]);
+            if (q < Q - 1) {
+                c->d_aemb.push_back(W(dw->audio_emb[q]));
+                all.push_back(dw->audio_emb[q]);
+            }
+        }
+        for (int j = 0; j < J; ++j) {
+            c->d_norm1.push_back(W(dw->norm1[j]));
+            c->d_qkv.push_back(W(dw->in_proj[j]));
+            c->d_o.push_back(W(dw->out_proj[j]));
+            c->d_norm2.push_back(W(dw->norm2[j]));
+            all.insert(all.end(), {dw->norm1[j], dw->in_proj[j], dw->out_proj[j], dw->norm2[j]});
+            for (int q = 0; q < Q; ++q) {
+                c->d_lin_in.push_back(W(dw->linear_in[(size_t)j * Q + q]));
+                c->d_lin_out.push_back(W(dw->linear_out[(size_t)j * Q + q]));
+                all.push_back(dw->linear_in[(size_t)j * Q + q]);
+                all.push_back(dw->linear_out[(size_t)j * Q + q]);
+            }
+        }
+    }
+    for (const void* p : all)
+        if (!p || !aligned16(p)) return bail(PM_ERR_ARG, "weight pointer null or not 16-byte aligned");
+
+    // owned device memory: one allocation carved into buffers
+    const int BM = f.B_max, S = f.n_streams;
+    const int Dd = c->has_dep ? f.dep_D : 0, Fd = c->has_dep ? f.dep_ffn : 0, Q = c->has_dep ? f.dep_steps : 1;
+    struct Item {
+        void** dst;
+        size_t bytes;
+    };
+    void* p_pos; void* p_first; void* p_ring; void* p_sel; void* p_amax; void* p_hc; void* p_status;
+    void* p_damax; void* p_dcount; void* p_dcodes; void* p_dtok; void* p_dsup;
+    void* p_io; void* p_dio; void *p_x, *p_q, *p_o, *p_s, *p_h, *p_part, *p_cnt, *p_freq, *p_dz, *p_dq, *p_dout,
+        *p_ds, *p_dkv;
+    std::vector<Item> items = {
+        {&p_pos, 4u * BM}, {&p_first, 4u * BM}, {&p_ring, 4u * BM * 4 * PM_MAX_STREAMS_DEV},
+        {&p_sel, 4u * BM * PM_MAX_STREAMS_DEV}, {&p_amax, 8u * BM}, {&p_hc, 4u * BM}, {&p_status, 16u},
+        {&p_damax, 8u * BM}, {&p_dcount, 4u * BM}, {&p_dcodes, 4u * BM * Q}, {&p_dtok, 4u * BM},
+        {&p_dsup, 4u * BM * Q},
+        {&p_io, 64u + 4u * BM * S}, {&p_dio, 64u + 4u * BM + 4u * BM * Q},
+        {&p_x, 4u * BM * f.D}, {&p_q, 4u * BM * f.D}, {&p_o, 4u * BM * f.D}, {&p_s, 4u * BM * f.ffn},
+        {&p_h, 4u * BM * f.D}, {&p_part, 4u * BM * f.H * kAttnSplitMax * (f.dh + 2)}, {&p_cnt, 4u * BM * f.H},
+        {&p_freq, 8u * (f.dh / 2)},
+        {&p_dz, 4u * BM * (Dd ? Dd : 1)}, {&p_dq, 4u * BM * (Dd ? Dd : 1)}, {&p_dout, 4u * BM * (Dd ? Dd : 1)},
+        {&p_ds, 4u * BM * (Fd ? Fd : 1)},
+        {&p_dkv, c->has_dep ? 2u * 2u * f.dep_layers * BM * f.dep_H * Q * f.dep_dh : 16u},
+    };
+    size_t total = 0;
+    for (auto& it : items) total = align_up(total, 256) + align_up(it.bytes, 16);
+    total = align_up(total, 256);
+    if (ck(cudaMalloc(&c->block, total))) {
+        cudaGetLastError();
+        return bail(PM_ERR_OOM, "allocation failed");
+    }
+    c->block_bytes = total;
+    if (ck(cudaMemset(c->block, 0, total))) return bail(PM_ERR_CUDA, "cudaMemset");
+    size_t off = 0;
+    for (auto& it : items) {
+        off = align_up(off, 256);
+        *it.dst = static_cast<uint8_t*>(c->block) + off;
+        off += align_up(it.bytes, 16);
+    }
+    c->st.pos = (int32_t*)p_pos;
+    c->st.first_pos = (int32_t*)p_first;
+    c->st.ring = (int32_t*)p_ring;
+    c->st.sel = (int32_t*)p_sel;
+    c->st.amax = (unsigned long long*)p_amax;
+    c->st.head_count = (uint32_t*)p_hc;
+    c->st.status = (uint32_t*)p_status;
+    c->st.dep_amax = (unsigned long long*)p_damax;
+    c->st.dep_count = (uint32_t*)p_dcount;
+    c->st.dep_codes = (int32_t*)p_dcodes;
+    c->st.dep_tok = (int32_t*)p_dtok;
+    c->st.dep_sup = (int32_t*)p_dsup;
+    c->io_region = (uint8_t*)p_io;
+    c->dio_region = (uint8_t*)p_dio;
+    c->x = (float*)p_x;
+    c->q = (float*)p_q;
+    c->o = (float*)p_o;
+    c->s = (float*)p_s;
+    c->h = (float*)p_h;
+    c->att_part = (float*)p_part;
+    c->att_count = (uint32_t*)p_cnt;
+    c->rope_freq = (double*)p_freq;
+    c->dz = (float*)p_dz;
+    c->dq = (float*)p_dq;
+    c->dout = (float*)p_dout;
+    c->ds = (float*)p_ds;
+    c->dkv = (uint16_t*)p_dkv;
+
+    // RoPE frequencies f_j = exp(-ln(theta) * 2j / dh), in double
+    std::vector<double> freq(f.dh / 2);
+    for (int j = 0; j < f.dh / 2; ++j) freq[j] = exp(-log((double)f.rope_theta) * (2.0 * j) / (double)f.dh);
+    if (ck(cudaMemcpy(c->rope_freq, freq.data(), 8u * freq.size(), cudaMemcpyHostToDevice)))
+        return bail(PM_ERR_CUDA, "CUDA call failed");
+    // no prior selection anywhere
+    std::vector<int32_t> sel((size_t)BM * PM_MAX_STREAMS_DEV, -2);
+    if (ck(cudaMemcpy(c->st.sel, sel.data(), 4u * sel.size(), cudaMemcpyHostToDevice)))
+        return bail(PM_ERR_CUDA, "CUDA call failed");
+
+    if (ck(cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking))) return bail(PM_ERR_CUDA, "cudaStreamCreateWithFlags");
+    const size_t slot_bytes = 64u + 4u * (size_t)BM * (S + 1 + Q);
+    for (int i = 0; i < kStagingSlots; ++i) {
+        if (cudaHostAlloc((void**)&c->slots[i].host, align_up(slot_bytes, 64), cudaHostAllocDefault) !=
+            cudaSuccess)
+            return bail(PM_ERR_OOM, "allocation failed");
+        if (ck(cudaEventCreateWithFlags(&c->slots[i].done, cudaEventDisableTiming)))
+            return bail(PM_ERR_CUDA, "CUDA call failed");
+    }
+    // verify every GEMV of the configuration has a plan before accepting it
+    {
+        GemvParams t;
+        memset(&t, 0, sizeof t);
+        auto chk = [&](int K, int units, int rpu) {
+            t.K = K;
+            t.n_units = units;
+            return plan_gemv(t, rpu, c->num_sms);
+        };
+        bool good = chk(f.D, 3 * f.D / 2, 2) && chk(f.D, f.D, 1) && chk(f.D, f.ffn, 2) && chk(f.ffn, f.D, 1) &&
+                    chk(f.D, f.text_out, 1);
+        if (c->has_dep)
+            good = good && chk(f.D, f.dep_D, 1) && chk(f.dep_D, 3 * f.dep_D, 1) && chk(f.dep_D, f.dep_D, 1) &&
+                   chk(f.dep_D, f.dep_ffn, 2) && chk(f.dep_ffn, f.dep_D, 1) && chk(f.dep_D, f.dep_card, 1);
+        if (!good) return bail(PM_ERR_UNSUPPORTED, "a GEMV shape has no plan");
+    }
+    if (ck(gemv_prepare())) return bail(PM_ERR_CUDA, "gemv_prepare()");
+    if (ck(cudaDeviceSynchronize())) return bail(PM_ERR_CUDA, "cudaDeviceSynchronize()");
+    *out = c;
+    return PM_OK;
+}
+
+extern "C" void pm_destroy(pm_ctx* c) {
+    if (!c) return;
+    cudaSetDevice(c->device);
+    cudaStreamSynchronize(c->stream);
+    free_ctx(c);
+}
+
+extern "C" const char* pm_last_error(const pm_ctx* c) { return c ? c->err.c_str() : g_create_err.c_str(); }
+
+static pm_status set_state(pm_ctx* c, const int32_t* pos, const int32_t* apply, int n) {
+    SetStateArgs a;
+    memset(&a, 0, sizeof a);
+    a.st = c->st;
+    a.n = n;
+    for (int b = 0; b < n; ++b) {
+        a.pos[b] = pos[b];
+        a.apply[b] = apply[b];
+    }
+    k_set_state<<<n, 32, 0, c->stream>>>(a);
+    PM_CUDA(cudaGetLastError());
+    return PM_OK;
+}
+
+extern "C" pm_status pm_reset(pm_ctx* c, const int32_t* mask) {
+    if (!c) return PM_ERR_ARG;
+    PM_CUDA(cudaSetDevice(c->device));
+    int32_t pos[kMaxB] = {0}, apply[kMaxB];
+    for (int b = 0; b < c->cfg.B_max; ++b) apply[b] = mask ? (mask[b] != 0) : 1;
+    return set_state(c, pos, apply, c->cfg.B_max);
+}
+
+extern "C" pm_status pm_set_positions(pm_ctx* c, int B, const int32_t* pos) {
+    if (!c) return PM_ERR_ARG;
+    if (B < 1 || B > c->cfg.B_max || !pos) return fail(c, PM_ERR_ARG, "pm_set_positions: bad B or pos");
+    for (int b = 0; b < B; ++b)
+        if (pos[b] < 0) return fail(c, PM_ERR_ARG, "pm_set_positions: negative position");
+    PM_CUDA(cudaSetDevice(c->device));
+    int32_t apply[kMaxB];
+    for (int b = 0; b < B; ++b) apply[b] = 1;
+    return set_state(c, pos, apply, B);
+}
+
+extern "C" pm_status pm_get_positions(pm_ctx* c, int32_t* pos_out) {
+    if (!c || !pos_out) return PM_ERR_ARG;
+    PM_CUDA(cudaSetDevice(c->device));
+    PM_CUDA(cudaMemcpyAsync(pos_out, c->st.pos, 4u * c->cfg.B_max, cudaMemcpyDeviceToHost, c->stream));
+    PM_CUDA(cudaStreamSynchronize(c->stream));
+    return PM_OK;
+}
+
+extern "C" pm_status pm_device_status(pm_ctx* c) {
+    if (!c) return PM_ERR_ARG;
+    PM_CUDA(cudaSetDevice(c->device));
+    uint32_t st[4] = {0, 0, 0, 0};
+    PM_CUDA(cudaStreamSynchronize(c->stream));
+    PM_CUDA(cudaMemcpy(st, c->st.status, sizeof st, cudaMemcpyDeviceToHost));
+    PM_CUDA(cudaMemset(c->st.status, 0, 4));
+    if (st[0] & PM_DEV_ERR_TIMEOUT) return fail(c, PM_ERR_TIMEOUT, "a device-side wait ran out");
+    if (st[0] & PM_DEV_ERR_INVALID_ID) return fail(c, PM_ERR_INVALID_ID, "an ID given in device memory was invalid");
+    return PM_OK;
+}
+
+extern "C" pm_status pm_frame_step(pm_ctx* c, int B, const int32_t* ids, float* text_logits, float* hidden,
+                                   int32_t* text_token) {
+    if (!c) return PM_ERR_ARG;
+    const pm_config& f = c->cfg;
+    if (B < 1 || B > f.B_max) return fail(c, PM_ERR_ARG, "pm_frame_step: B outside 1..B_max");
+    if (!ids) return fail(c, PM_ERR_ARG, "pm_frame_step: ids is null");
+    PM_CUDA(cudaSetDevice(c->device));
+    const int S = f.n_streams;
+    const bool dev_ids = is_device_ptr(ids);
+    if (!dev_ids) {
+        for (int b = 0; b < B; ++b)
+            for (int k = 0; k < S; ++k) {
+                const int32_t id = ids[(size_t)b * S + k];
+                const int rows = (k == 0) ? f.text_in : f.audio_in;
+                if (!(id == PM_ID_FEEDBACK || (id >= -1 && id < rows)))
+                    return fail(c, PM_ERR_INVALID_ID, "pm_frame_step: ID " + std::to_string(id) + " at batch " +
+                                                          std::to_string(b) + " stream " + std::to_string(k));
+            }
+    }
+    cudaGraphExec_t ex;
+    pm_status st = get_graph(c, c->frame_graphs, B, record_frame, &ex);
+    if (st) return st;
+    uint8_t* host;
+    cudaEvent_t ev;
+    st = take_slot(c, &host, &ev);
+    if (st) return st;
+    FrameIO io;
+    io.ids = dev_ids ? ids : reinterpret_cast<const int32_t*>(c->io_region + 64);
+    io.logits = text_logits;
+    io.hidden = hidden;
+    io.token = text_token;
+    memcpy(host, &io, sizeof io);
+    size_t bytes = 64;
+    if (!dev_ids) {
+        memcpy(host + 64, ids, 4u * B * S);
+        bytes += 4u * B * S;
+    }
+    PM_CUDA(cudaMemcpyAsync(c->io_region, host, bytes, cudaMemcpyHostToDevice, c->stream));
+    PM_CUDA(cudaEventRecord(ev, c->stream));
+    PM_CUDA(cudaGraphLaunch(ex, c->stream));
+    return PM_OK;
+}
+
+extern "C" pm_status pm_depformer_step(pm_ctx* c, int B, const float* hidden, const int32_t* text_tok,
+                                       const int32_t* supplied, float* logits, int32_t* codes) {
+    if (!c) return PM_ERR_ARG;
+    const pm_config& f = c->cfg;
+    if (!c->has_dep) return fail(c, PM_ERR_STATE, "pm_depformer_step: context has no depformer");
+    if (B < 1 || B > f.B_max) return fail(c, PM_ERR_ARG, "pm_depformer_step: B outside 1..B_max");
+    PM_CUDA(cudaSetDevice(c->device));
+    const int Q = f.dep_steps;
+    if (hidden && !is_device_ptr(hidden)) return fail(c, PM_ERR_ARG, "pm_depformer_step: hidden must be device memory");
+    const bool dev_tok = text_tok && is_device_ptr(text_tok);
+    const bool dev_sup = supplied && is_device_ptr(supplied);
+    if (text_tok && !dev_tok)
+        for (int b = 0; b < B; ++b)
+            if (text_tok[b] < 0 || text_tok[b] >= f.dep_text_in)
+                return fail(c, PM_ERR_INVALID_ID, "pm_depformer_step: text token out of range");
+    if (supplied && !dev_sup)
+        for (int i = 0; i < B * Q; ++i)
+            if (supplied[i] < -1 || supplied[i] >= f.dep_card)
+                return fail(c, PM_ERR_INVALID_ID, "pm_depformer_step: supplied code out of range");
+    cudaGraphExec_t ex;
+    pm_status st = get_graph(c, c->dep_graphs, B, record_depformer, &ex);
+    if (st) return st;
+    uint8_t* host;
+    cudaEvent_t ev;
+    st = take_slot(c, &host, &ev);
+    if (st) return st;
+    uint8_t* dev_tok_buf = c->dio_region + 64;
+    uint8_t* dev_sup_buf = c->dio_region + 64 + 4u * f.B_max;
+    DepIO io;
+    io.hidden = hidden ? hidden : c->h;
+    io.text_tok = text_tok ? (dev_tok ? text_tok : reinterpret_cast<const int32_t*>(dev_tok_buf)) : nullptr;
+    io.supplied = supplied ? (dev_sup ? supplied : reinterpret_cast<const int32_t*>(dev_sup_buf)) : nullptr;
+    io.logits = logits;
+    io.codes = codes;
+    memcpy(host, &io, sizeof io);
+    if (text_tok && !dev_tok) memcpy(host + 64, text_tok, 4u * B);
+    if (supplied && !dev_sup) memcpy(host + 64 + 4u * f.B_max, supplied, 4u * B * Q);
+    const size_t bytes = 64u + 4u * f.B_max + 4u * (size_t)B * Q;
+    PM_CUDA(cudaMemcpyAsync(c->dio_region, host, bytes, cudaMemcpyHostToDevice, c->stream));
+    PM_CUDA(cudaEventRecord(ev, c->stream));
+    PM_CUDA(cudaGraphLaunch(ex, c->stream));
+    return PM_OK;
+}

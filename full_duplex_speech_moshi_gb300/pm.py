@@ -1,0 +1,242 @@
+"""Thin ctypes binding of `libpm.so` (declared in include/pm.h).
+
+Argument marshalling only: every step of the decode path runs in the library's CUDA
+kernels.  There is no fallback: if the library cannot be loaded, importing fails.
+PyTorch tensors are accepted wherever the C ABI takes a pointer (`.data_ptr()` is
+passed); the caller keeps the tensors alive.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Dict, List, Optional, Sequence
+
+from . import build as _build
+
+PM_OK, PM_ERR_ARG, PM_ERR_INVALID_ID, PM_ERR_CUDA, PM_ERR_TIMEOUT, PM_ERR_STATE, PM_ERR_OOM, PM_ERR_UNSUPPORTED = range(8)
+PM_ID_NONE, PM_ID_UNGENERATED, PM_ID_FEEDBACK = -1, -2, -3
+PM_MAX_STREAMS = 32
+STATUS_NAMES = {0: "PM_OK", 1: "PM_ERR_ARG", 2: "PM_ERR_INVALID_ID", 3: "PM_ERR_CUDA", 4: "PM_ERR_TIMEOUT",
+                5: "PM_ERR_STATE", 6: "PM_ERR_OOM", 7: "PM_ERR_UNSUPPORTED"}
+
+# every symbol include/pm.h declares
+EXPORTS = ["pm_kv_cache_bytes", "pm_create", "pm_reset", "pm_set_positions", "pm_get_positions",
+           "pm_frame_step", "pm_depformer_step", "pm_device_status", "pm_last_error", "pm_destroy"]
+
+
+class pm_config(C.Structure):
+    _fields_ = [("B_max", C.c_int), ("D", C.c_int), ("H", C.c_int), ("dh", C.c_int), ("ffn", C.c_int),
+                ("n_layers", C.c_int), ("ctx", C.c_int), ("text_in", C.c_int), ("text_out", C.c_int),
+                ("audio_in", C.c_int), ("n_streams", C.c_int), ("delays", C.c_int * PM_MAX_STREAMS),
+                ("init_text", C.c_int), ("init_audio", C.c_int), ("eps", C.c_float), ("rope_theta", C.c_float),
+                ("dep_D", C.c_int), ("dep_H", C.c_int), ("dep_dh", C.c_int), ("dep_ffn", C.c_int),
+                ("dep_layers", C.c_int), ("dep_steps", C.c_int), ("dep_ctx", C.c_int), ("dep_card", C.c_int),
+                ("dep_text_in", C.c_int), ("dep_audio_in", C.c_int)]
+
+
+_PP = C.POINTER(C.c_void_p)
+
+
+class pm_temporal_weights(C.Structure):
+    _fields_ = [("text_emb", C.c_void_p), ("audio_emb", C.c_void_p * (PM_MAX_STREAMS - 1)),
+                ("norm1", _PP), ("in_proj", _PP), ("out_proj", _PP), ("norm2", _PP), ("linear_in", _PP),
+                ("linear_out", _PP), ("out_norm", C.c_void_p), ("text_linear", C.c_void_p)]
+
+
+class pm_depformer_weights(C.Structure):
+    _fields_ = [("dep_in", _PP), ("text_emb", C.c_void_p), ("audio_emb", _PP), ("norm1", _PP), ("in_proj", _PP),
+                ("out_proj", _PP), ("norm2", _PP), ("linear_in", _PP), ("linear_out", _PP), ("heads", _PP)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libpm.so (compiling it first if the sources are newer)."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = C.CDLL(path)
+        vp, i32p, fp = C.c_void_p, C.POINTER(C.c_int32), C.c_void_p
+        L.pm_kv_cache_bytes.restype = C.c_size_t
+        L.pm_kv_cache_bytes.argtypes = [C.POINTER(pm_config)]
+        L.pm_create.restype = C.c_int
+        L.pm_create.argtypes = [C.POINTER(pm_config), C.POINTER(pm_temporal_weights),
+                                C.POINTER(pm_depformer_weights), vp, vp, C.POINTER(C.c_void_p)]
+        L.pm_reset.restype = C.c_int
+        L.pm_reset.argtypes = [vp, vp]
+        L.pm_set_positions.restype = C.c_int
+        L.pm_set_positions.argtypes = [vp, C.c_int, vp]
+        L.pm_get_positions.restype = C.c_int
+        L.pm_get_positions.argtypes = [vp, vp]
+        L.pm_frame_step.restype = C.c_int
+        L.pm_frame_step.argtypes = [vp, C.c_int, vp, vp, vp, vp]
+        L.pm_depformer_step.restype = C.c_int
+        L.pm_depformer_step.argtypes = [vp, C.c_int, vp, vp, vp, vp, vp]
+        L.pm_device_status.restype = C.c_int
+        L.pm_device_status.argtypes = [vp]
+        L.pm_last_error.restype = C.c_char_p
+        L.pm_last_error.argtypes = [vp]
+        L.pm_destroy.restype = None
+        L.pm_destroy.argtypes = [vp]
+        _lib = L
+    return _lib
+
+
+class PMError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def _ptr(x) -> Optional[int]:
+    """Pointer of a torch tensor / numpy array / int / None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError(type(x))
+
+
+def make_config(shape: dict, B_max: int, depformer: bool = True) -> pm_config:
+    c = pm_config()
+    c.B_max = int(B_max)
+    for k in ("D", "H", "dh", "ffn", "n_layers", "ctx", "text_in", "text_out", "audio_in", "n_streams",
+              "init_text", "init_audio", "dep_D", "dep_H", "dep_dh", "dep_ffn", "dep_steps", "dep_ctx",
+              "dep_card", "dep_text_in", "dep_audio_in"):
+        setattr(c, k, int(shape[k]))
+    c.dep_layers = int(shape["dep_layers"]) if depformer else 0
+    c.eps = float(shape["eps"])
+    c.rope_theta = float(shape["rope_theta"])
+    for i, d in enumerate(shape["delays"]):
+        c.delays[i] = int(d)
+    return c
+
+
+def pm_kv_cache_bytes(cfg: pm_config) -> int:
+    return int(lib().pm_kv_cache_bytes(C.byref(cfg)))
+
+
+class Context:
+    """Owns one pm_ctx.  `weights` maps the PyTorch parameter names of the inventory
+    (see inputs.tensor_specs) to device tensors; `kv_cache` is a device tensor of
+    pm_kv_cache_bytes bytes."""
+
+    def __init__(self, shape: dict, weights: Dict[str, object], kv_cache, B_max: int = 1,
+                 depformer: bool = True, stream: int = 0):
+        L = lib()
+        self.L = L
+        self.shape = dict(shape)
+        self.cfg = make_config(shape, B_max, depformer)
+        s = self.shape
+        self._keep: List[object] = []
+
+        def arr(names: Sequence[str]):
+            a = (C.c_void_p * max(1, len(names)))(*[_ptr(weights[n]) for n in names])
+            self._keep.append(a)
+            return C.cast(a, _PP)
+
+        tw = pm_temporal_weights()
+        tw.text_emb = _ptr(weights["text_emb"])
+        for i in range(s["n_streams"] - 1):
+            tw.audio_emb[i] = _ptr(weights[f"emb.{i}"])
+        Lr = range(s["n_layers"])
+        tw.norm1 = arr([f"layers.{l}.norm1" for l in Lr])
+        tw.in_proj = arr([f"layers.{l}.in_proj" for l in Lr])
+        tw.out_proj = arr([f"layers.{l}.out_proj" for l in Lr])
+        tw.norm2 = arr([f"layers.{l}.norm2" for l in Lr])
+        tw.linear_in = arr([f"layers.{l}.linear_in" for l in Lr])
+        tw.linear_out = arr([f"layers.{l}.linear_out" for l in Lr])
+        tw.out_norm = _ptr(weights["out_norm"])
+        tw.text_linear = _ptr(weights["text_linear"])
+        dwp = None
+        if depformer:
+            Q, J = s["dep_steps"], s["dep_layers"]
+            dw = pm_depformer_weights()
+            dw.dep_in = arr([f"depformer_in.{q}" for q in range(Q)])
+            dw.text_emb = _ptr(weights["depformer_text_emb"])
+            dw.audio_emb = arr([f"depformer_emb.{q}" for q in range(Q - 1)])
+            dw.norm1 = arr([f"depformer.{j}.norm1" for j in range(J)])
+            dw.in_proj = arr([f"depformer.{j}.in_proj" for j in range(J)])
+            dw.out_proj = arr([f"depformer.{j}.out_proj" for j in range(J)])
+            dw.norm2 = arr([f"depformer.{j}.norm2" for j in range(J)])
+            dw.linear_in = arr([f"depformer.{j}.gating.{q}.linear_in" for j in range(J) for q in range(Q)])
+            dw.linear_out = arr([f"depformer.{j}.gating.{q}.linear_out" for j in range(J) for q in range(Q)])
+            dw.heads = arr([f"linears.{q}" for q in range(Q)])
+            self._dw = dw
+            dwp = C.byref(dw)
+        self._tw = tw
+        self.kv_cache = kv_cache
+        h = C.c_void_p()
+        st = L.pm_create(C.byref(self.cfg), C.byref(tw), dwp, _ptr(kv_cache), stream or None, C.byref(h))
+        if st != PM_OK:
+            raise PMError(st, L.pm_last_error(None).decode())
+        self.h = h
+
+    def _check(self, st: int):
+        if st != PM_OK:
+            raise PMError(st, self.L.pm_last_error(self.h).decode())
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.L.pm_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def reset(self, mask=None):
+        m = None
+        if mask is not None:
+            m = (C.c_int32 * self.cfg.B_max)(*[int(v) for v in mask])
+        self._check(self.L.pm_reset(self.h, m))
+
+    def set_positions(self, pos: Sequence[int]):
+        a = (C.c_int32 * len(pos))(*[int(p) for p in pos])
+        self._check(self.L.pm_set_positions(self.h, len(pos), a))
+
+    def get_positions(self) -> List[int]:
+        a = (C.c_int32 * self.cfg.B_max)()
+        self._check(self.L.pm_get_positions(self.h, a))
+        return list(a)
+
+    def frame_step(self, B: int, ids, text_logits=None, hidden=None, text_token=None) -> None:
+        self._check(self.L.pm_frame_step(self.h, int(B), _ptr(ids), _ptr(text_logits), _ptr(hidden),
+                                         _ptr(text_token)))
+
+    def depformer_step(self, B: int, hidden=None, text_tok=None, supplied=None, logits=None, codes=None) -> None:
+        self._check(self.L.pm_depformer_step(self.h, int(B), _ptr(hidden), _ptr(text_tok), _ptr(supplied),
+                                             _ptr(logits), _ptr(codes)))
+
+    def device_status(self) -> int:
+        return int(self.L.pm_device_status(self.h))
+
+
+def upload_weights(weights: Dict[str, object], device: str = "cuda") -> Dict[str, object]:
+    """Copy bf16 bit arrays (numpy uint16) to device tensors of dtype bfloat16."""
+    import numpy as np
+    import torch
+    out = {}
+    for k, v in weights.items():
+        t = torch.from_numpy(np.ascontiguousarray(v).view(np.int16))
+        out[k] = t.to(device, non_blocking=False).view(torch.bfloat16)
+    return out
+
+
+def alloc_kv_cache(cfg: pm_config, device: str = "cuda"):
+    """A zeroed device buffer of pm_kv_cache_bytes(cfg) bytes, viewed as bf16
+    [n_layers, 2, B_max, H, ctx, dh]."""
+    import torch
+    shape = (cfg.n_layers, 2, cfg.B_max, cfg.H, cfg.ctx, cfg.dh)
+    return torch.zeros(shape, dtype=torch.bfloat16, device=device)

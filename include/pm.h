@@ -1,0 +1,177 @@
+/*
+ * pm.h -- C ABI of the GB300 (sm_103a) per-frame streaming decode step of the
+ * Moshi/PersonaPlex temporal transformer and its depformer.
+ *
+ * What the calls compute is defined on the page "PersonaPlex native LM audit"
+ * (clockless-atlas personaplex-research):
+ *   pm_frame_step      section 3 "Native temporal computation" (embedding sum, 32 blocks
+ *                      of RMSNorm32 -> fused QKV -> RoPE -> causal windowed attention ->
+ *                      W_O + residual -> RMSNorm32 -> SwiGLU FFN + residual, final
+ *                      RMSNorm32, untied text head) with the stream delays of section 7
+ *                      "One exact generator step" and the KV cache of section 6;
+ *   pm_depformer_step  section 4 "Native depth computation" (sixteen sequential
+ *                      positions, six blocks with per-position weights and shared norm
+ *                      scales, fresh depth context per frame, supplied codes replace the
+ *                      sampled ones).
+ * Selection is greedy (argmax, lowest index on ties).
+ *
+ * Conventions.
+ *  - Every call is asynchronous on the CUDA stream given to pm_create; outputs are valid
+ *    once that stream has synchronised.  Calls on one context must not overlap.
+ *  - Weights are caller-owned device memory, bf16, PyTorch [out, in] row-major.
+ *    Norm scales are bf16 vectors.  They must stay valid until pm_destroy.
+ *  - The temporal KV cache is caller-owned device memory, bf16, laid out
+ *    [n_layers][2 (K, V)][B_max][H][ctx][dh]; keys are stored after RoPE.  Position p of
+ *    stream b lives in slot p mod ctx.  Size: pm_kv_cache_bytes().
+ *  - Everything else (positions, delay ring, activations, depth cache, CUDA graphs) is
+ *    owned by the context and allocated in pm_create; no call after pm_create allocates
+ *    device memory.
+ *  - Errors: every call validates its host-visible arguments before launching anything
+ *    and returns a pm_status; on error no state changes and pm_last_error() says why.
+ *    IDs given in device memory are validated on the device: an invalid one makes the
+ *    whole frame a no-op (no KV write, no position advance) and is reported by the next
+ *    pm_device_status().
+ */
+#ifndef PM_H
+#define PM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct pm_ctx pm_ctx;
+
+typedef enum {
+    PM_OK = 0,
+    PM_ERR_ARG = 1,          /* bad pointer, size or configuration */
+    PM_ERR_INVALID_ID = 2,   /* a token ID outside -1..rows-1 (or -2), or a feedback ID with no prior selection */
+    PM_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+    PM_ERR_TIMEOUT = 4,      /* a bounded device-side wait ran out (reported by pm_device_status) */
+    PM_ERR_STATE = 5,        /* call not valid in the context's current state */
+    PM_ERR_OOM = 6,          /* device allocation in pm_create failed */
+    PM_ERR_UNSUPPORTED = 7   /* shape not supported by this build's kernels */
+} pm_status;
+
+/* Special token IDs (section 3 of the audit: -1 embeds to an exact zero vector; -2 is the
+ * ungenerated-cache sentinel and is never a valid input). */
+#define PM_ID_NONE (-1)
+#define PM_ID_UNGENERATED (-2)
+/* Library extension: the token this context selected for the same stream on the stream's
+ * previous frame (text: the greedy text token of the previous pm_frame_step; audio stream
+ * k = 1..16: depformer code q = k-1 of the previous pm_depformer_step).  Lets greedy
+ * feedback stay on the device. */
+#define PM_ID_FEEDBACK (-3)
+
+#define PM_MAX_STREAMS 32
+
+typedef struct {
+    int B_max;            /* largest batch the context serves (1..64) */
+    /* temporal transformer */
+    int D, H, dh, ffn;    /* 4096, 32, 128, 11264 (gated hidden width) */
+    int n_layers, ctx;    /* 32, 3000 */
+    int text_in;          /* text embedding rows, 32001 (32000 = initial text ID) */
+    int text_out;         /* text head rows, 32000 */
+    int audio_in;         /* audio embedding rows, 2049 (2048 = initial audio ID) */
+    int n_streams;        /* 17: text, 8 agent audio, 8 user audio */
+    int delays[PM_MAX_STREAMS];  /* per stream, 0..3: {0,0,1,1,1,1,1,1,1,0,1,1,1,1,1,1,1} */
+    int init_text, init_audio;   /* 32000, 2048 */
+    float eps;            /* 1e-8 */
+    float rope_theta;     /* 1e4 */
+    /* depformer (dep_layers = 0: none) */
+    int dep_D, dep_H, dep_dh, dep_ffn;  /* 1024, 16, 64, 2816 */
+    int dep_layers, dep_steps, dep_ctx; /* 6, 16, 8 (or 16) */
+    int dep_card;                       /* depth head rows, 2048 */
+    int dep_text_in, dep_audio_in;      /* 32001, 2049 */
+} pm_config;
+
+/* Temporal weights: device pointers.  Per-layer members point to host arrays of
+ * n_layers device pointers (copied by pm_create). */
+typedef struct {
+    const void* text_emb;                      /* [text_in][D] */
+    const void* audio_emb[PM_MAX_STREAMS - 1]; /* n_streams-1 tables [audio_in][D] */
+    const void* const* norm1;                  /* [D] attention-norm scale per layer */
+    const void* const* in_proj;                /* [3D][D] fused Q,K,V (rows Q 0..D-1, K D..2D-1, V 2D..3D-1) */
+    const void* const* out_proj;               /* [D][D] */
+    const void* const* norm2;                  /* [D] FFN-norm scale per layer */
+    const void* const* linear_in;              /* [2F][D]: rows 0..F-1 gate (SiLU), F..2F-1 value */
+    const void* const* linear_out;             /* [D][F] */
+    const void* out_norm;                      /* [D] */
+    const void* text_linear;                   /* [text_out][D] */
+} pm_temporal_weights;
+
+/* Depformer weights (section 4 of the audit, parameter names of section 5). */
+typedef struct {
+    const void* const* dep_in;      /* dep_steps pointers, [dep_D][D] */
+    const void* text_emb;           /* [dep_text_in][dep_D] */
+    const void* const* audio_emb;   /* dep_steps-1 pointers, [dep_audio_in][dep_D] */
+    const void* const* norm1;       /* dep_layers pointers, [dep_D], shared by all positions */
+    const void* const* in_proj;     /* dep_layers pointers, [dep_steps*3*dep_D][dep_D]; position q uses rows q*3*dep_D.. */
+    const void* const* out_proj;    /* dep_layers pointers, [dep_steps*dep_D][dep_D]; position q uses rows q*dep_D.. */
+    const void* const* norm2;       /* dep_layers pointers, [dep_D] */
+    const void* const* linear_in;   /* dep_layers*dep_steps pointers (index j*dep_steps+q), [2*dep_ffn][dep_D] */
+    const void* const* linear_out;  /* same indexing, [dep_D][dep_ffn] */
+    const void* const* heads;       /* dep_steps pointers, [dep_card][dep_D] */
+} pm_depformer_weights;
+
+/* Bytes of the caller-owned temporal KV cache for this configuration. */
+size_t pm_kv_cache_bytes(const pm_config* cfg);
+
+/* Create a context on the current CUDA device.  `dw` may be NULL (no depformer).
+ * `kv_cache`: device pointer, pm_kv_cache_bytes(cfg) bytes, 256-byte aligned.
+ * `cuda_stream`: a cudaStream_t (NULL = legacy default stream).  All positions start
+ * at 0 (reset).  Returns PM_ERR_UNSUPPORTED for shapes the kernels do not cover. */
+pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* tw, const pm_depformer_weights* dw,
+                    void* kv_cache, void* cuda_stream, pm_ctx** out);
+
+/* Reset streams (host mask [B_max], nonzero = reset; NULL = all): position 0, empty
+ * delay history, no prior selection.  Cache bytes are not cleared (the mask hides them). */
+pm_status pm_reset(pm_ctx* ctx, const int32_t* stream_mask);
+
+/* Set the positions of streams 0..B-1 (host array [B], each >= 0).  Used when the caller
+ * has written the KV history of positions < pos itself.  Delayed streams read their
+ * initial IDs on the first frame after a position set. */
+pm_status pm_set_positions(pm_ctx* ctx, int B, const int32_t* pos);
+
+/* Read back the positions of streams 0..B_max-1 (synchronises the stream). */
+pm_status pm_get_positions(pm_ctx* ctx, int32_t* pos_out);
+
+/* One temporal frame for streams 0..B-1.
+ *  ids         [B][n_streams] int32, host or device memory: the undelayed token of each
+ *              stream at this frame (-1 none, PM_ID_FEEDBACK allowed).  Host memory is
+ *              copied before the call returns.
+ *  text_logits [B][text_out] fp32 device memory, or NULL.
+ *  hidden      [B][D] fp32 device memory: h after the final RMSNorm, or NULL.
+ *  text_token  [B] int32, device or host-mapped memory: greedy text token, or NULL.
+ * Advances each stream's position by one. */
+pm_status pm_frame_step(pm_ctx* ctx, int B, const int32_t* ids, float* text_logits, float* hidden,
+                        int32_t* text_token);
+
+/* One depformer frame (sixteen positions) for streams 0..B-1.
+ *  hidden    [B][D] fp32 device memory, or NULL = the h of this context's last frame.
+ *  text_tok  [B] int32 host or device memory, or NULL = the greedy text token of this
+ *            context's last frame.
+ *  supplied  [B][dep_steps] int32 host or device memory, or NULL = all greedy:
+ *            -1 = take the argmax, otherwise the code to use (0..dep_card-1).
+ *  logits    [B][dep_steps][dep_card] fp32 device memory, or NULL.
+ *  codes     [B][dep_steps] int32 device or host-mapped memory, or NULL. */
+pm_status pm_depformer_step(pm_ctx* ctx, int B, const float* hidden, const int32_t* text_tok,
+                            const int32_t* supplied, float* logits, int32_t* codes);
+
+/* Synchronise the stream and return (and clear) any device-side error: an invalid ID
+ * given in device memory (PM_ERR_INVALID_ID) or a bounded wait that ran out
+ * (PM_ERR_TIMEOUT). */
+pm_status pm_device_status(pm_ctx* ctx);
+
+/* Message of the last failed call on this context (empty string if none). */
+const char* pm_last_error(const pm_ctx* ctx);
+
+/* Free everything the context owns (not the weights or the KV cache). */
+void pm_destroy(pm_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PM_H */
