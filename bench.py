@@ -1,0 +1,377 @@
+"""Throughput of the Moshi/PersonaPlex per-frame temporal decode step on GB300.
+
+Workload (one JSON line): the full 32-block temporal stack (D 4096, 32 heads x 128,
+SwiGLU 11264, 3000-frame KV ring, text head 32000), batch 1, random-init bf16 weights.
+Prime 256 frames by sequential decode with seeded IDs, then decode with the greedy text
+token fed back on the device (text ID -3) and seeded audio IDs.  A step is one frame:
+delay assembly + embedding sum, 32 blocks, final norm + text head + greedy token.
+
+  value     frames/s over K timed frames, inputs resident in HBM, CUDA events on the
+            launching stream, max over ranks (replicas only: one independent model per GPU)
+  e2e       the same through the C ABI with host IDs copied in and the greedy token read
+            back to the host every frame (the host feeds it as the next text ID)
+  roofline  the dominant kernel (RMSNorm + linear_in + SwiGLU GEMV, 184,549,376 bytes of
+            weights per launch): algorithmic bytes / mean launch time from per-launch
+            CUDA events (pm_profile_frame), against the measured HBM copy peak
+
+`--impl reference` times the float64 CPU oracle on the same workload unit instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from full_duplex_speech_moshi_gb300 import inputs as I  # noqa: E402
+
+METRIC = "temporal frames/s (B=1, 32-block stack, greedy text feedback)"
+PRIME = 256
+W_IN_BYTES = 2 * 11264 * 4096 * 2          # linear_in weights per launch: 184,549,376
+# algorithmic bytes of one B=1 frame that do not depend on the cache length:
+#   32 blocks x (in_proj 100,663,296 + out_proj 33,554,432 + linear_in 184,549,376
+#   + linear_out 92,274,688) + text head 262,144,000 + 17 embedding rows 139,264
+#   + 65 bf16 norm scales 532,480
+FRAME_FIXED_BYTES = 32 * 411_041_792 + 262_144_000 + 139_264 + 532_480
+BLOCK_BYTES = 411_041_792
+KV_BYTES_PER_POS = 32 * 2 * 4096 * 2       # K and V of one position, all layers: 524,288
+
+REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc:
+            time.sleep(0.2)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(REASONS, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        loaded = sorted(sm)[len(sm) // 4:] or sm  # drop the idle tail before the first launch
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_reference(args):
+    """The float64 CPU oracle on the same workload unit (one frame per step)."""
+    from oracle import oracle as O
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    s = I.FULL
+    t0 = time.time()
+    W = I.make_weights(s, depformer=False)
+    M = O.Oracle(s.asdict(), [W[n] for n, _, _ in I.tensor_specs(s, False)], depformer=False)
+    st = M.new_stream()
+    ids = I.make_ids(s, args.warmup + args.steps, seed=2000)[:, 0]
+    prev = None
+    for t in range(args.warmup):
+        _, _, _, prev = st.step(ids[t])
+    t1 = time.time()
+    for t in range(args.warmup, args.warmup + args.steps):
+        x = ids[t].copy()
+        if prev is not None:
+            x[0] = prev
+        _, _, _, prev = st.step(x)
+    dt = time.time() - t1
+    fps = args.steps / dt
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": fps, "unit": "frames/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "32-block temporal stack, B=1, frames from reset with greedy text feedback",
+                   "global_batch": 1, "seq_len": args.warmup + args.steps, "parallelism": "replicas"},
+        "cpu_baseline": {"value": fps, "unit": "frames/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} frames after {args.warmup} warm-up frames from reset "
+                                   f"(setup {t1 - t0:.0f} s not timed)"},
+        "e2e": {"value": fps, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_sample(budget_s: float = 15.0, max_frames: int = 64):
+    """The oracle as it stands on the host cores: consecutive frames of the 32-block B=1
+    stack from reset until about `budget_s` seconds of CPU work."""
+    from oracle import oracle as O
+    s = I.FULL
+    W = I.make_weights(s, depformer=False)
+    M = O.Oracle(s.asdict(), [W[n] for n, _, _ in I.tensor_specs(s, False)], depformer=False)
+    st = M.new_stream()
+    ids = I.make_ids(s, max_frames + 1, seed=2000)[:, 0]
+    st.step(ids[0])
+    t0 = time.time()
+    n = 0
+    while n < max_frames and (n < 3 or time.time() - t0 < budget_s):
+        n += 1
+        st.step(ids[n])
+    dt = time.time() - t0
+    return {"value": n / dt, "unit": "frames/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} frames (positions 1..{n}) of the 32-block B=1 stack, float64, OpenMP over all "
+                      f"host cores, {dt:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extras", type=int, default=1, help="also time B=8 and the depformer")
+    ap.add_argument("--prime", type=int, default=PRIME, help="frames decoded before warm-up")
+    ap.add_argument("--layers", type=int, default=32,
+                    help="temporal blocks (32 = the workload; fewer only for small profiler captures)")
+    args = ap.parse_args()
+    assert args.warmup >= 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    from full_duplex_speech_moshi_gb300 import pm
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    s = I.FULL if args.layers == 32 else I.ModelShape(n_layers=args.layers)
+    PR = args.prime
+    dev = "cuda"
+    stream = torch.cuda.current_stream()
+    W = I.make_weights_device(s, depformer=True, seed=1000 + 7919 * rank, device=dev)
+    cfg1 = pm.make_config(s.asdict(), 1, True)
+    kv1 = pm.alloc_kv_cache(cfg1)
+    ctx = pm.Context(s.asdict(), W, kv1, B_max=1, depformer=True, stream=stream.cuda_stream)
+    T = PR + args.warmup + args.steps
+    ids_h = I.make_ids(s, T + 64, seed=2000 + rank)[:, :1]     # [T, 1, 17]
+    ids_fb = ids_h.copy()
+    ids_fb[PR:, 0, 0] = pm.PM_ID_FEEDBACK
+    ids_d = torch.from_numpy(ids_fb).to(dev)
+    logits = torch.empty((1, s.text_out), dtype=torch.float32, device=dev)
+    hidden = torch.empty((1, s.D), dtype=torch.float32, device=dev)
+    token = torch.empty((1,), dtype=torch.int32, device=dev)
+
+    # prime + warm-up
+    for t in range(PR + args.warmup):
+        ctx.frame_step(1, ids_d[t], logits, hidden, token)
+    torch.cuda.synchronize()
+    p0 = PR + args.warmup
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for t in range(args.steps):
+            ctx.frame_step(1, ids_d[p0 + t], logits, hidden, token)
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = start.elapsed_time(end)
+    if dist is not None:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    fps = args.steps / (ms / 1000.0) * world
+    ms_step = ms / args.steps
+    # keys read per frame = min(pos + 1, ctx); one new K/V row written
+    mean_keys = statistics.mean(min(p + 1, s.ctx) for p in range(p0, p0 + args.steps))
+    nl = s.n_layers
+    bytes_per_frame = (FRAME_FIXED_BYTES - (32 - nl) * (BLOCK_BYTES + 16384)
+                       + KV_BYTES_PER_POS // 32 * nl * (mean_keys + 1))
+    frame_gbs = bytes_per_frame / (ms_step / 1000.0) / 1e9
+
+    # per-launch device times (dominant kernel) from eager frames with events
+    prof = []
+    for t in range(16):
+        prof.append(ctx.profile_frame(1, ids_d[p0 + args.steps + t], logits, hidden, token))
+    by_kind = {}
+    for fr in prof[4:]:
+        for kind, kms in fr:
+            by_kind.setdefault(kind, []).append(kms)
+    w_in_ms = statistics.mean(by_kind["linear_in_swiglu"])
+    peak, peak_src = load_peaks()
+    achieved = W_IN_BYTES / (w_in_ms / 1000.0) / 1e9
+
+    # end to end: host IDs in, greedy token out and fed back, every frame
+    ctx.reset()
+    ids_pin = torch.from_numpy(ids_h[:T, 0].copy()).pin_memory()
+    tok_host = torch.zeros((1,), dtype=torch.int32).pin_memory()
+    for t in range(PR + args.warmup):
+        ctx.frame_step(1, ids_pin[t], logits, hidden, token)
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    nxt = None
+    for t in range(args.steps):
+        row = ids_pin[p0 + t]
+        if nxt is not None:
+            row[0] = nxt
+        ctx.frame_step(1, row, logits, hidden, token)
+        tok_host.copy_(token, non_blocking=True)
+        stream.synchronize()
+        nxt = int(tok_host[0])
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    e2e_ms = max(e_start.elapsed_time(e_end), wall * 1000.0)
+    if dist is not None:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    e2e_fps = args.steps / (e2e_ms / 1000.0) * world
+
+    extras = {}
+    if args.extras:
+        # depformer after every frame (greedy agent codes, supplied user codes)
+        sup = torch.from_numpy(I.make_supplied_codes(s, 64, seed=4000)[:, 0].copy()).to(dev)
+        dl = torch.empty((1, s.dep_steps, s.dep_card), dtype=torch.float32, device=dev)
+        dc = torch.empty((1, s.dep_steps), dtype=torch.int32, device=dev)
+        for t in range(8):
+            ctx.frame_step(1, ids_d[PR + t], logits, hidden, token)
+            ctx.depformer_step(1, None, None, sup[t], dl, dc)
+        torch.cuda.synchronize()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n4 = 48
+        a.record(stream)
+        for t in range(n4):
+            ctx.frame_step(1, ids_d[PR + 8 + t], logits, hidden, token)
+            ctx.depformer_step(1, None, None, sup[t % 64], dl, dc)
+        b_.record(stream)
+        torch.cuda.synchronize()
+        f4 = n4 / (a.elapsed_time(b_) / 1000.0)
+        a2, b2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a2.record(stream)
+        for t in range(n4):
+            ctx.depformer_step(1, None, None, sup[t % 64], dl, dc)
+        b2.record(stream)
+        torch.cuda.synchronize()
+        extras["with_depformer_frames_per_s"] = f4
+        extras["depformer_ms"] = a2.elapsed_time(b2) / n4
+    ctx.close()
+    del kv1
+    torch.cuda.empty_cache()
+    if args.extras:
+        B8 = 8
+        cfg8 = pm.make_config(s.asdict(), B8, False)
+        kv8 = pm.alloc_kv_cache(cfg8)
+        ctx8 = pm.Context(s.asdict(), W, kv8, B_max=B8, depformer=False, stream=stream.cuda_stream)
+        ids8 = torch.from_numpy(I.make_ids(s, 96, B=B8, seed=2100)).to(dev)
+        ids8[16:, :, 0] = pm.PM_ID_FEEDBACK
+        lg8 = torch.empty((B8, s.text_out), dtype=torch.float32, device=dev)
+        for t in range(16):
+            ctx8.frame_step(B8, ids8[t], lg8, None, None)
+        torch.cuda.synchronize()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for t in range(64):
+            ctx8.frame_step(B8, ids8[16 + t], lg8, None, None)
+        b_.record(stream)
+        torch.cuda.synchronize()
+        steps8 = 64 / (a.elapsed_time(b_) / 1000.0)
+        extras["B8_steps_per_s"] = steps8
+        extras["B8_stream_frames_per_s"] = steps8 * B8
+        ctx8.close()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample()
+
+    if rank == 0:
+        launches_per_frame = 2 + 5 * s.n_layers
+        traffic = None
+        tp = os.path.join(ROOT, "profiles", "traffic.json")
+        if os.path.exists(tp):
+            traffic = json.load(open(tp)).get("linear_in_swiglu_bytes_per_launch")
+        line = {
+            "metric": METRIC, "value": fps, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init bf16 weights, seeded IDs)",
+            "config": {"workload": "32-block temporal stack (D 4096, 32x128 heads, SwiGLU 11264, ctx 3000, "
+                                   "text head 32000), B=1, 256 primed frames then greedy text feedback",
+                       "global_batch": world, "seq_len": p0 + args.steps, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: 13.4 GB of weights streamed per frame",
+                       "frame_bytes": bytes_per_frame, "frame_gbs": frame_gbs,
+                       "frame_frac_of_peak": frame_gbs / peak},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "RMSNorm + linear_in [22528,4096] + SwiGLU GEMV",
+                         "kernel_ms": w_in_ms, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
+            "kernel_ms_mean": {k: statistics.mean(v) for k, v in by_kind.items()},
+            "e2e": {"value": e2e_fps, "unit": "frames/s", "h2d_bytes_per_step": 64 + 4 * s.n_streams,
+                    "d2h_bytes_per_step": 4},
+            "gpu_launches": launches_per_frame * args.steps,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        line.update(extras)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -48,6 +48,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
                     "--expt-relaxed-constexpr"]
     if ptxas_info:
         flags += ["-Xptxas", "-v"]
+    flags += os.environ.get("PM_NVCC_EXTRA", "").split()
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")

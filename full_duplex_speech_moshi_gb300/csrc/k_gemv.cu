@@ -23,6 +23,24 @@
 
 #include "pm_kernels.h"
 
+// Tiling policy (compile-time tuning constants, chosen by measurement on GB300):
+//  stage bytes   - target size of one shared-memory stage (whole rows, rounded down)
+//  ring bytes    - target size of the stage ring per CTA
+//  CTAs per SM   - resident GEMV CTAs per SM for one kernel
+//  max warps     - consumer warps per CTA (each reduces one K-slice of one row per stage)
+#ifndef PM_GEMV_STAGE_BYTES
+#define PM_GEMV_STAGE_BYTES 16384
+#endif
+#ifndef PM_GEMV_RING_BYTES
+#define PM_GEMV_RING_BYTES 98304
+#endif
+#ifndef PM_GEMV_CTAS_PER_SM
+#define PM_GEMV_CTAS_PER_SM 2
+#endif
+#ifndef PM_GEMV_MAX_WARPS
+#define PM_GEMV_MAX_WARPS 16
+#endif
+
 namespace pm {
 
 namespace {
@@ -32,7 +50,7 @@ __device__ __forceinline__ void consumer_bar(int nthreads) {
 }
 
 template <int CH, int PRO, int EPI, int UNIT>
-__global__ void __launch_bounds__(544, 1) k_gemv(const GemvParams p) {
+__global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int RPU = (UNIT == U_ROW) ? 1 : 2;
     const int W = p.warps;
@@ -374,19 +392,20 @@ bool plan_gemv(GemvParams& p, int rpu, int num_sms) {
     if (K <= 0 || K % 256 != 0 || p.n_units <= 0) return false;
     p.CH = (K % 1024 == 0) ? 4 : (K % 512 == 0) ? 2 : 1;
     p.P = K / (256 * p.CH);
-    if (rpu * p.P > 16) return false;
+    if (rpu * p.P > PM_GEMV_MAX_WARPS) return false;
     const int row_bytes = 2 * K;
-    int upst = 16384 / (row_bytes * rpu);
+    int upst = PM_GEMV_STAGE_BYTES / (row_bytes * rpu);
     if (upst < 1) upst = 1;
-    while (upst > 1 && upst * rpu * p.P > 16) --upst;
+    while (upst > 1 && upst * rpu * p.P > PM_GEMV_MAX_WARPS) --upst;
     p.upst = upst;
     p.warps = upst * rpu * p.P;
     p.stage_bytes = (uint32_t)(upst * rpu * row_bytes);
-    int nst = (int)(98304u / p.stage_bytes);
+    int nst = (int)(PM_GEMV_RING_BYTES / p.stage_bytes);
     if (nst < 2) nst = 2;
     if (nst > 16) nst = 16;
     p.nst = nst;
-    p.grid_per_b = p.n_units < num_sms ? p.n_units : num_sms;
+    const int ctas = PM_GEMV_CTAS_PER_SM * num_sms;
+    p.grid_per_b = p.n_units < ctas ? p.n_units : ctas;
     p.units_cta_max = (p.n_units + p.grid_per_b - 1) / p.grid_per_b;
     p.smem = (size_t)nst * p.stage_bytes + 16u * (size_t)nst + (size_t)p.units_cta_max * rpu * p.P * 4u + 32u * 4u;
     if (p.smem > 220u * 1024u) return false;

@@ -24,7 +24,6 @@ using namespace pm;
 namespace {
 
 constexpr int kMaxB = 64;
-constexpr int kAttnSplitMax = 16;
 constexpr int kStagingSlots = 8;
 
 struct Staging {
@@ -67,6 +66,9 @@ struct pm_ctx {
     // graphs
     std::map<int, cudaGraphExec_t> frame_graphs, dep_graphs;
     std::string err;
+    // set while pm_profile_frame records a frame eagerly
+    std::vector<cudaEvent_t>* prof_ev = nullptr;
+    std::vector<int>* prof_kind = nullptr;
 };
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -163,11 +165,17 @@ static pm_status plan(pm_ctx* c, GemvParams& p, int rpu, const char* what) {
     return PM_OK;
 }
 
-static int attn_splits(const pm_ctx* c, int B) {
-    int want = (2 * c->num_sms + B * c->cfg.H - 1) / (B * c->cfg.H);
-    if (want < 1) want = 1;
-    if (want > kAttnSplitMax) want = kAttnSplitMax;
-    return want;
+typedef pm_status (*record_fn)(pm_ctx*, int, cudaStream_t);
+
+// profiling mark: an event after the launch just issued (only inside pm_profile_frame)
+static pm_status mark(pm_ctx* c, cudaStream_t s, int kind) {
+    if (!c->prof_ev) return PM_OK;
+    cudaEvent_t e;
+    PM_CUDA(cudaEventCreate(&e));
+    c->prof_ev->push_back(e);
+    c->prof_kind->push_back(kind);
+    PM_CUDA(cudaEventRecord(e, s));
+    return PM_OK;
 }
 
 static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
@@ -187,7 +195,11 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
     ep.D = D;
     ep.B = B;
     ep.n_streams = f.n_streams;
+    const bool pdl = c->prof_ev == nullptr;  // eager profiling runs each kernel alone
+    pm_status ms = mark(c, s, -1);
+    if (ms) return ms;
     PM_CUDA(launch_embed(ep, s, false));
+    if ((ms = mark(c, s, PM_KERNEL_EMBED))) return ms;
 
     const size_t layer_elems = (size_t)f.B_max * f.H * f.ctx * f.dh;
     for (int l = 0; l < f.n_layers; ++l) {
@@ -214,7 +226,8 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
         p.rope_freq = c->rope_freq;
         pm_status ps = plan(c, p, 2, "in_proj");
         if (ps) return ps;
-        PM_CUDA(launch_gemv(PRO_RMSNORM, E_QKV_ROPE, U_PAIR_ADJ, p, s, true));
+        PM_CUDA(launch_gemv(PRO_RMSNORM, E_QKV_ROPE, U_PAIR_ADJ, p, s, pdl));
+        if ((ms = mark(c, s, PM_KERNEL_QKV))) return ms;
         // attention
         AttnParams ap;
         memset(&ap, 0, sizeof ap);
@@ -228,10 +241,11 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
         ap.B = B;
         ap.H = f.H;
         ap.ctx = f.ctx;
-        ap.S = attn_splits(c, B);
+        ap.S = attn_max_splits(f.ctx);
         ap.D = D;
         ap.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dh));
-        PM_CUDA(launch_attn(ap, s, true));
+        PM_CUDA(launch_attn(ap, s, pdl));
+        if ((ms = mark(c, s, PM_KERNEL_ATTENTION))) return ms;
         // W_O + residual
         p = base_params(c);
         p.W = c->out_proj[l];
@@ -244,7 +258,8 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
         p.y_stride = D;
         ps = plan(c, p, 1, "out_proj");
         if (ps) return ps;
-        PM_CUDA(launch_gemv(PRO_PLAIN, E_RESIDUAL, U_ROW, p, s, true));
+        PM_CUDA(launch_gemv(PRO_PLAIN, E_RESIDUAL, U_ROW, p, s, pdl));
+        if ((ms = mark(c, s, PM_KERNEL_OUT_PROJ))) return ms;
         // RMSNorm2 + linear_in + SwiGLU
         p = base_params(c);
         p.W = c->lin_in[l];
@@ -259,7 +274,8 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
         p.y_stride = F;
         ps = plan(c, p, 2, "linear_in");
         if (ps) return ps;
-        PM_CUDA(launch_gemv(PRO_RMSNORM, E_SWIGLU, U_PAIR_SPLIT, p, s, true));
+        PM_CUDA(launch_gemv(PRO_RMSNORM, E_SWIGLU, U_PAIR_SPLIT, p, s, pdl));
+        if ((ms = mark(c, s, PM_KERNEL_LINEAR_IN))) return ms;
         // linear_out + residual
         p = base_params(c);
         p.W = c->lin_out[l];
@@ -272,7 +288,8 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
         p.y_stride = D;
         ps = plan(c, p, 1, "linear_out");
         if (ps) return ps;
-        PM_CUDA(launch_gemv(PRO_PLAIN, E_RESIDUAL, U_ROW, p, s, true));
+        PM_CUDA(launch_gemv(PRO_PLAIN, E_RESIDUAL, U_ROW, p, s, pdl));
+        if ((ms = mark(c, s, PM_KERNEL_LINEAR_OUT))) return ms;
     }
     // final RMSNorm + text head + argmax + frame finalisation
     GemvParams p = base_params(c);
@@ -287,7 +304,8 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
     p.h_internal = c->h;
     pm_status ps = plan(c, p, 1, "text_linear");
     if (ps) return ps;
-    PM_CUDA(launch_gemv(PRO_RMSNORM, E_HEAD, U_ROW, p, s, true));
+    PM_CUDA(launch_gemv(PRO_RMSNORM, E_HEAD, U_ROW, p, s, pdl));
+    if ((ms = mark(c, s, PM_KERNEL_HEAD))) return ms;
     return PM_OK;
 }
 
@@ -418,7 +436,7 @@ static pm_status record_depformer(pm_ctx* c, int B, cudaStream_t s) {
     return PM_OK;
 }
 
-typedef pm_status (*record_fn)(pm_ctx*, int, cudaStream_t);
+
 
 static pm_status get_graph(pm_ctx* c, std::map<int, cudaGraphExec_t>& cache, int B, record_fn rec,
                            cudaGraphExec_t* out) {
@@ -594,7 +612,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
         {&p_dsup, 4u * BM * Q},
         {&p_io, 64u + 4u * BM * S}, {&p_dio, 64u + 4u * BM + 4u * BM * Q},
         {&p_x, 4u * BM * f.D}, {&p_q, 4u * BM * f.D}, {&p_o, 4u * BM * f.D}, {&p_s, 4u * BM * f.ffn},
-        {&p_h, 4u * BM * f.D}, {&p_part, 4u * BM * f.H * kAttnSplitMax * (f.dh + 2)}, {&p_cnt, 4u * BM * f.H},
+        {&p_h, 4u * BM * f.D}, {&p_part, 4u * BM * f.H * attn_max_splits(f.ctx) * (f.dh + 2)}, {&p_cnt, 4u * BM * f.H},
         {&p_freq, 8u * (f.dh / 2)},
         {&p_dz, 4u * BM * (Dd ? Dd : 1)}, {&p_dq, 4u * BM * (Dd ? Dd : 1)}, {&p_dout, 4u * BM * (Dd ? Dd : 1)},
         {&p_ds, 4u * BM * (Fd ? Fd : 1)},
@@ -830,5 +848,63 @@ extern "C" pm_status pm_depformer_step(pm_ctx* c, int B, const float* hidden, co
     PM_CUDA(cudaMemcpyAsync(c->dio_region, host, bytes, cudaMemcpyHostToDevice, c->stream));
     PM_CUDA(cudaEventRecord(ev, c->stream));
     PM_CUDA(cudaGraphLaunch(ex, c->stream));
+    return PM_OK;
+}
+
+extern "C" pm_status pm_profile_frame(pm_ctx* c, int B, const int32_t* ids, float* text_logits, float* hidden,
+                                      int32_t* text_token, float* kernel_ms, int32_t* kernel_kind, int max_launches,
+                                      int* n_launches) {
+    if (!c) return PM_ERR_ARG;
+    if (!kernel_ms || !kernel_kind || !n_launches || max_launches < 0)
+        return fail(c, PM_ERR_ARG, "pm_profile_frame: null output array");
+    const pm_config& f = c->cfg;
+    if (B < 1 || B > f.B_max || !ids) return fail(c, PM_ERR_ARG, "pm_profile_frame: bad B or ids");
+    PM_CUDA(cudaSetDevice(c->device));
+    const int S = f.n_streams;
+    const bool dev_ids = is_device_ptr(ids);
+    if (!dev_ids)
+        for (int i = 0; i < B * S; ++i) {
+            const int rows = (i % S == 0) ? f.text_in : f.audio_in;
+            if (!(ids[i] == PM_ID_FEEDBACK || (ids[i] >= -1 && ids[i] < rows)))
+                return fail(c, PM_ERR_INVALID_ID, "pm_profile_frame: invalid ID");
+        }
+    uint8_t* host;
+    cudaEvent_t ev;
+    pm_status st = take_slot(c, &host, &ev);
+    if (st) return st;
+    FrameIO io;
+    io.ids = dev_ids ? ids : reinterpret_cast<const int32_t*>(c->io_region + 64);
+    io.logits = text_logits;
+    io.hidden = hidden;
+    io.token = text_token;
+    memcpy(host, &io, sizeof io);
+    size_t bytes = 64;
+    if (!dev_ids) {
+        memcpy(host + 64, ids, 4u * B * S);
+        bytes += 4u * B * S;
+    }
+    PM_CUDA(cudaMemcpyAsync(c->io_region, host, bytes, cudaMemcpyHostToDevice, c->stream));
+    PM_CUDA(cudaEventRecord(ev, c->stream));
+    std::vector<cudaEvent_t> evs;
+    std::vector<int> kinds;
+    c->prof_ev = &evs;
+    c->prof_kind = &kinds;
+    st = record_frame(c, B, c->stream);
+    c->prof_ev = nullptr;
+    c->prof_kind = nullptr;
+    cudaError_t e = cudaStreamSynchronize(c->stream);
+    int n = 0;
+    if (st == PM_OK && e == cudaSuccess) {
+        for (size_t i = 1; i < evs.size() && n < max_launches; ++i, ++n) {
+            float ms = 0.f;
+            cudaEventElapsedTime(&ms, evs[i - 1], evs[i]);
+            kernel_ms[n] = ms;
+            kernel_kind[n] = kinds[i];
+        }
+    }
+    for (cudaEvent_t x : evs) cudaEventDestroy(x);
+    *n_launches = n;
+    if (st) return st;
+    if (e != cudaSuccess) return cuda_fail(c, e, "pm_profile_frame");
     return PM_OK;
 }

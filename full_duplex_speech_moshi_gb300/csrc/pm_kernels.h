@@ -99,13 +99,16 @@ struct AttnParams {
     const uint16_t* kc;    // [B_max][H][ctx][dh]
     const uint16_t* vc;
     float* o;              // [B][D]
-    float* part;           // [B][H][S][dh + 2]
+    float* part;           // [B][H][S][dh + 2] chunk partials
     uint32_t* count;       // [B][H], zero between launches
     DevState st;
     int B, H, ctx, S, D;
     float scale_log2;      // log2(e) / sqrt(dh)
 };
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl);
+// chunks (CTAs per head) the attention grid needs for a window of ctx keys; AttnParams.S
+// must be at least this and `part` must hold S chunks per head
+int attn_max_splits(int ctx);
 
 // ----------------------------------------------------------------------------------
 // depformer helpers

@@ -237,3 +237,20 @@ def make_kv_history(s: ModelShape, n_pos: int, seed: int, layer: int, stream: in
     k = normal_bf16((s.H, n_pos, s.dh), 0.0, 1.0, seed * 1000003 + layer * 1009 + stream * 2 + 0, pool)
     v = normal_bf16((s.H, n_pos, s.dh), 0.0, 1.0, seed * 1000003 + layer * 1009 + stream * 2 + 1, pool)
     return k, v
+
+
+def make_weights_device(s: ModelShape, depformer: bool = True, seed: int = 1000, device: str = "cuda"):
+    """Seeded weights of the same shapes and distributions drawn directly on the device
+    with torch's generator (bf16 by nearest-even rounding of fp32 draws).  Used where only
+    timing matters and host copies would cost more than the measurement (the bench)."""
+    import torch
+    g = torch.Generator(device=device)
+    out = {}
+    for i, (name, shape, kind) in enumerate(tensor_specs(s, depformer)):
+        mean, std = _DIST[kind]
+        g.manual_seed(seed + i)
+        t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        t.mul_(std).add_(mean)
+        out[name] = t.to(torch.bfloat16)
+        del t
+    return out

@@ -21,7 +21,10 @@ STATUS_NAMES = {0: "PM_OK", 1: "PM_ERR_ARG", 2: "PM_ERR_INVALID_ID", 3: "PM_ERR_
 
 # every symbol include/pm.h declares
 EXPORTS = ["pm_kv_cache_bytes", "pm_create", "pm_reset", "pm_set_positions", "pm_get_positions",
-           "pm_frame_step", "pm_depformer_step", "pm_device_status", "pm_last_error", "pm_destroy"]
+           "pm_frame_step", "pm_depformer_step", "pm_profile_frame", "pm_device_status", "pm_last_error",
+           "pm_destroy"]
+KERNEL_KINDS = {0: "embed", 1: "qkv_rope", 2: "attention", 3: "out_proj", 4: "linear_in_swiglu",
+                5: "linear_out", 6: "text_head"}
 
 
 class pm_config(C.Structure):
@@ -77,6 +80,8 @@ def lib():
         L.pm_frame_step.argtypes = [vp, C.c_int, vp, vp, vp, vp]
         L.pm_depformer_step.restype = C.c_int
         L.pm_depformer_step.argtypes = [vp, C.c_int, vp, vp, vp, vp, vp]
+        L.pm_profile_frame.restype = C.c_int
+        L.pm_profile_frame.argtypes = [vp, C.c_int, vp, vp, vp, vp, vp, vp, C.c_int, C.POINTER(C.c_int)]
         L.pm_device_status.restype = C.c_int
         L.pm_device_status.argtypes = [vp]
         L.pm_last_error.restype = C.c_char_p
@@ -218,6 +223,16 @@ class Context:
     def depformer_step(self, B: int, hidden=None, text_tok=None, supplied=None, logits=None, codes=None) -> None:
         self._check(self.L.pm_depformer_step(self.h, int(B), _ptr(hidden), _ptr(text_tok), _ptr(supplied),
                                              _ptr(logits), _ptr(codes)))
+
+    def profile_frame(self, B: int, ids, text_logits=None, hidden=None, text_token=None):
+        """One frame with per-launch device times: list of (kind name, ms)."""
+        n_max = 2 + 5 * self.shape["n_layers"]
+        ms = (C.c_float * n_max)()
+        kind = (C.c_int32 * n_max)()
+        n = C.c_int(0)
+        self._check(self.L.pm_profile_frame(self.h, int(B), _ptr(ids), _ptr(text_logits), _ptr(hidden),
+                                            _ptr(text_token), ms, kind, n_max, C.byref(n)))
+        return [(KERNEL_KINDS[kind[i]], float(ms[i])) for i in range(n.value)]
 
     def device_status(self) -> int:
         return int(self.L.pm_device_status(self.h))

@@ -160,12 +160,34 @@ pm_status pm_frame_step(pm_ctx* ctx, int B, const int32_t* ids, float* text_logi
 pm_status pm_depformer_step(pm_ctx* ctx, int B, const float* hidden, const int32_t* text_tok,
                             const int32_t* supplied, float* logits, int32_t* codes);
 
+/* Kernel families of a temporal frame, as reported by pm_profile_frame. */
+typedef enum {
+    PM_KERNEL_EMBED = 0,       /* delay assembly + embedding gather-sum */
+    PM_KERNEL_QKV = 1,         /* RMSNorm + fused QKV + RoPE + KV append */
+    PM_KERNEL_ATTENTION = 2,   /* split-KV decode attention */
+    PM_KERNEL_OUT_PROJ = 3,    /* W_O + residual */
+    PM_KERNEL_LINEAR_IN = 4,   /* RMSNorm + linear_in + SwiGLU */
+    PM_KERNEL_LINEAR_OUT = 5,  /* linear_out + residual */
+    PM_KERNEL_HEAD = 6         /* final RMSNorm + text head + greedy token */
+} pm_kernel_kind;
+
+/* Same computation and state change as pm_frame_step, but the frame's kernels are
+ * launched one at a time (no graph, no overlap between kernels) with a CUDA event after
+ * each on the context's stream.  Writes each launch's device time in milliseconds to
+ * kernel_ms[i] and its pm_kernel_kind to kernel_kind[i] (host arrays of max_launches
+ * entries; a frame has 2 + 5 * n_layers launches), the count to *n_launches, and
+ * synchronises the stream.  For measurement only. */
+pm_status pm_profile_frame(pm_ctx* ctx, int B, const int32_t* ids, float* text_logits, float* hidden,
+                           int32_t* text_token, float* kernel_ms, int32_t* kernel_kind, int max_launches,
+                           int* n_launches);
+
 /* Synchronise the stream and return (and clear) any device-side error: an invalid ID
  * given in device memory (PM_ERR_INVALID_ID) or a bounded wait that ran out
  * (PM_ERR_TIMEOUT). */
 pm_status pm_device_status(pm_ctx* ctx);
 
-/* Message of the last failed call on this context (empty string if none). */
+/* Message of the last failed call on this context (empty string if none); with a NULL
+ * context, the reason the last pm_create on this thread failed. */
 const char* pm_last_error(const pm_ctx* ctx);
 
 /* Free everything the context owns (not the weights or the KV cache). */
