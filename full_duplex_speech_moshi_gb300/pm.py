@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "PM_OK", 1: "PM_ERR_ARG", 2: "PM_ERR_INVALID_ID", 3: "PM_ERR_
 # every symbol include/pm.h declares
 EXPORTS = ["pm_kv_cache_bytes", "pm_create", "pm_reset", "pm_set_positions", "pm_get_positions",
            "pm_frame_step", "pm_depformer_step", "pm_profile_frame", "pm_device_status", "pm_last_error",
-           "pm_destroy"]
+           "pm_destroy", "pm_text_head_noalloc"]
 KERNEL_KINDS = {0: "embed", 1: "qkv_rope", 2: "attention", 3: "out_proj", 4: "linear_in_swiglu",
                 5: "linear_out", 6: "text_head"}
 
@@ -86,6 +86,8 @@ def lib():
         L.pm_device_status.argtypes = [vp]
         L.pm_last_error.restype = C.c_char_p
         L.pm_last_error.argtypes = [vp]
+        L.pm_text_head_noalloc.restype = C.c_int
+        L.pm_text_head_noalloc.argtypes = [C.c_int, C.c_int, C.c_int, vp, vp, vp, C.c_float, vp, vp, vp, vp]
         L.pm_destroy.restype = None
         L.pm_destroy.argtypes = [vp]
         _lib = L
@@ -236,6 +238,15 @@ class Context:
 
     def device_status(self) -> int:
         return int(self.L.pm_device_status(self.h))
+
+
+def pm_text_head_noalloc(B: int, D: int, V: int, residual, out_norm, text_linear, eps: float,
+                         hidden=None, logits=None, token=None, stream: int = 0) -> int:
+    """Final RMSNorm + text head + greedy token without a context or any device
+    allocation (scratch in a static device array; B <= 64).  Returns the pm_status."""
+    return int(lib().pm_text_head_noalloc(int(B), int(D), int(V), _ptr(residual), _ptr(out_norm),
+                                          _ptr(text_linear), float(eps), _ptr(hidden), _ptr(logits), _ptr(token),
+                                          stream or None))
 
 
 def upload_weights(weights: Dict[str, object], device: str = "cuda") -> Dict[str, object]:

@@ -186,6 +186,24 @@ pm_status pm_profile_frame(pm_ctx* ctx, int B, const int32_t* ids, float* text_l
  * (PM_ERR_TIMEOUT). */
 pm_status pm_device_status(pm_ctx* ctx);
 
+/* Final RMSNorm + text head + greedy token with no context and no device allocation.
+ * The paper has no counterpart: this is a library entry point for callers that cannot
+ * allocate device memory (code running during CUDA stream capture, real-time threads
+ * that must not block on the allocator, hosts that own all device memory).
+ *  residual  [B][D] fp32 device memory: the residual stream after the last block.
+ *  out_norm  bf16 [D]; text_linear bf16 [V][D] (device, 16-byte aligned).
+ *  hidden    [B][D] fp32 (normalised state h) or NULL; logits [B][V] fp32 or NULL;
+ *  token     [B] int32 greedy token (lowest index on ties) or NULL.
+ * Same arithmetic as the head of pm_frame_step.  Scratch is a 10,240-byte static device
+ * array in the library, so B may be at most 64 (PM_ERR_UNSUPPORTED beyond, or if D is
+ * not a multiple of 256).  The first call on each device resolves that array's address
+ * and clears it (synchronous); make it before any stream capture.  Later calls only
+ * launch kernels on `cuda_stream` (NULL = legacy default stream).  All calls share the
+ * array: calls that overlap on the GPU race. */
+pm_status pm_text_head_noalloc(int B, int D, int V, const float* residual, const void* out_norm,
+                               const void* text_linear, float eps, float* hidden, float* logits, int32_t* token,
+                               void* cuda_stream);
+
 /* Message of the last failed call on this context (empty string if none); with a NULL
  * context, the reason the last pm_create on this thread failed. */
 const char* pm_last_error(const pm_ctx* ctx);

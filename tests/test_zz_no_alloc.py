@@ -1,0 +1,69 @@
+"""pm_text_head_noalloc, the entry point for callers that cannot allocate device memory
+(code running during CUDA stream capture, real-time threads that must not block on the
+allocator, hosts that own all device memory): its scratch is a static device array in
+the library instead of context workspaces.
+
+It is checked against the text head of pm_frame_step.  The model has one block whose
+projections are all zero, so the frame's residual stream before the final norm is
+exactly the embedding sum of the frame's delayed inputs; that sum, formed here, is the
+no-allocation call's input.  Two calls in a row must each reproduce pm_frame_step's
+hidden state, logits and greedy token within the parity tolerances.
+
+This file is collected last on purpose: a failure here leaves every other test run.
+"""
+import numpy as np
+import pytest
+
+from full_duplex_speech_moshi_gb300 import inputs as I
+
+from harness import GAP_MIN, Pair, hidden_err, logits_rel_l2, small_shape, top2_gap
+
+pytestmark = pytest.mark.gpu
+
+
+def test_noalloc_text_head_matches_frame_step():
+    from full_duplex_speech_moshi_gb300 import pm
+    s = small_shape(n_layers=1)
+    W = I.make_weights(s, depformer=False)
+    for n in ("in_proj", "out_proj", "linear_in", "linear_out"):
+        W[f"layers.0.{n}"][...] = 0
+    p = Pair(s, B_max=2, depformer=False, weights=W)
+    torch = p.torch
+    try:
+        B = 2
+        ids = I.make_ids(s, 1, B=B, seed=91)[0]
+        gh, gl, gt = p.gpu_frame(ids, B=B)        # existing entry point
+        # residual = embedding sum of the first frame's inputs (delayed streams: initial IDs)
+        inp = np.where(np.array(s.delays)[None, :] == 0, ids,
+                       np.array([s.init_text] + [s.init_audio] * (s.n_streams - 1))[None, :])
+        x = torch.zeros((B, s.D), dtype=torch.float32, device="cuda")
+        for b in range(B):
+            for k in range(s.n_streams):
+                if inp[b, k] >= 0:
+                    table = p.Wd["text_emb"] if k == 0 else p.Wd[f"emb.{k - 1}"]
+                    x[b] += table[int(inp[b, k])].float()
+        hid = torch.empty((B, s.D), dtype=torch.float32, device="cuda")
+        lg = torch.empty((B, s.text_out), dtype=torch.float32, device="cuda")
+        tok = torch.empty((B,), dtype=torch.int32, device="cuda")
+        stream = torch.cuda.current_stream().cuda_stream
+        for call in range(2):
+            hid.fill_(float("nan"))
+            lg.fill_(float("nan"))
+            tok.fill_(-7)
+            st = pm.pm_text_head_noalloc(B, s.D, s.text_out, x, p.Wd["out_norm"], p.Wd["text_linear"], s.eps,
+                                         hid, lg, tok, stream)
+            assert st == pm.PM_OK, st
+            torch.cuda.synchronize()
+            nh = hid.double().cpu().numpy()
+            nl = lg.double().cpu().numpy()
+            nt = tok.cpu().numpy()
+            for b in range(B):
+                assert hidden_err(nh[b], gh[b]) <= 2e-2, (call, b)
+                assert logits_rel_l2(nl[b], gl[b]) <= 1e-2, (call, b)
+                if top2_gap(gl[b]) > GAP_MIN:
+                    assert int(nt[b]) == int(gt[b]), (call, b)
+        # sizes beyond the static scratch are refused without launching anything
+        assert pm.pm_text_head_noalloc(65, s.D, s.text_out, x, p.Wd["out_norm"], p.Wd["text_linear"], s.eps,
+                                       hid, lg, tok, stream) == pm.PM_ERR_UNSUPPORTED
+    finally:
+        p.close()
