@@ -171,8 +171,10 @@ __global__ void __launch_bounds__(128) k_attn(const AttnParams p) {
         A += s_acc[w][t] * f;
     }
     float* ob = p.o + (size_t)b * p.D + h * DH;
+    uint16_t* obb = p.ob ? p.ob + (size_t)b * p.D + h * DH : nullptr;
     if (n_split == 1) {
         ob[t] = A / L;
+        if (obb) obb[t] = f32_to_bf16_rne(A / L);
         return;
     }
     float* part = p.part + (((size_t)b * p.H + h) * p.S + s) * (DH + 2);
@@ -201,6 +203,7 @@ __global__ void __launch_bounds__(128) k_attn(const AttnParams p) {
         A2 += __ldcg(pb + (size_t)i * (DH + 2) + t) * f;
     }
     ob[t] = A2 / L2;
+    if (obb) obb[t] = f32_to_bf16_rne(A2 / L2);
     if (t == 0) p.count[(size_t)b * p.H + h] = 0u;
 }
 

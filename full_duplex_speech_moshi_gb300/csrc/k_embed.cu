@@ -60,13 +60,19 @@ __global__ void __launch_bounds__(128) k_embed(const EmbedParams p) {
     }
     __syncthreads();
     if (bad) return;
+    if (blockIdx.x == 0 && tid < p.dh / 2) {
+        // RoPE angles of this frame: position (integer) times frequency, in double
+        double sn, cs;
+        sincos((double)p.st.pos[b] * p.rope_freq[tid], &sn, &cs);
+        p.rope_tab[(size_t)b * (p.dh / 2) + tid] = make_float2((float)cs, (float)sn);
+    }
 
     const int col = blockIdx.x * 1024 + 8 * tid;
-    if (col >= p.D) return;
+    __shared__ float s_ss[4];
     float acc[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-    for (int k = 0; k < S; ++k) {
+    for (int k = 0; k < S && col < p.D; ++k) {
         const int id = s_in[k];
         if (id < 0) continue;  // -1: exact zero contribution
         const uint4 w = *reinterpret_cast<const uint4*>(p.tables[k] + (size_t)id * p.D + col);
@@ -75,9 +81,33 @@ __global__ void __launch_bounds__(128) k_embed(const EmbedParams p) {
         acc[4] += bf16lo(w.z); acc[5] += bf16hi(w.z);
         acc[6] += bf16lo(w.w); acc[7] += bf16hi(w.w);
     }
-    float4* dst = reinterpret_cast<float4*>(p.x + (size_t)b * p.D + col);
-    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    if (col < p.D) {
+        float4* dst = reinterpret_cast<float4*>(p.x + (size_t)b * p.D + col);
+        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    if (p.xb) {
+        // tensor-core operand bf16(alpha * x) and this CTA's share of sum(x^2)
+        float ss = 0.f;
+        if (col < p.D) {
+            const uint4 av = *reinterpret_cast<const uint4*>(p.alpha + col);
+            const float al[8] = {bf16lo(av.x), bf16hi(av.x), bf16lo(av.y), bf16hi(av.y),
+                                 bf16lo(av.z), bf16hi(av.z), bf16lo(av.w), bf16hi(av.w)};
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                w[e] = (uint32_t)f32_to_bf16_rne(acc[2 * e] * al[2 * e]) |
+                       ((uint32_t)f32_to_bf16_rne(acc[2 * e + 1] * al[2 * e + 1]) << 16);
+                ss = fmaf(acc[2 * e], acc[2 * e], ss);
+                ss = fmaf(acc[2 * e + 1], acc[2 * e + 1], ss);
+            }
+            *reinterpret_cast<uint4*>(p.xb + (size_t)b * p.D + col) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        ss = warp_sum(ss);
+        if ((tid & 31) == 0) s_ss[tid >> 5] = ss;
+        __syncthreads();
+        if (tid == 0) p.ss[(size_t)blockIdx.x * p.npad + b] = s_ss[0] + s_ss[1] + s_ss[2] + s_ss[3];
+    }
 }
 
 }  // namespace

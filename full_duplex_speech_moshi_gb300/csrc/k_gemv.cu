@@ -254,9 +254,8 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
             const int idx = row - sec * p.D;
             const int h = idx / p.dh, d = idx % p.dh;
             if (sec < 2) {
-                double sn, cs;
-                sincos((double)pos * p.rope_freq[d >> 1], &sn, &cs);
-                const float c = (float)cs, s = (float)sn;
+                const float2 t2 = p.rope_tab[(size_t)b * (p.dh / 2) + (d >> 1)];
+                const float c = t2.x, s = t2.y;
                 const float ra = a * c - bb * s;
                 const float rb = a * s + bb * c;
                 a = ra;

@@ -58,6 +58,13 @@ struct pm_ctx {
     float* att_part = nullptr;
     uint32_t* att_count = nullptr;
     double* rope_freq = nullptr;
+    float2* rope_tab = nullptr;        // [B_max][dh/2]
+    // tensor-core path (B >= 2): bf16 operands, sums of squares, stream-K scratch
+    int npad_max = 0;
+    uint16_t *xb = nullptr, *ob = nullptr, *sb = nullptr;
+    float* ss = nullptr;               // [D/128][npad_max]
+    float* tc_part = nullptr;
+    uint32_t* tc_count = nullptr;
     float *dz = nullptr, *dq = nullptr, *dout = nullptr, *ds = nullptr;
     uint16_t* dkv = nullptr;
     // staging
@@ -66,6 +73,8 @@ struct pm_ctx {
     // graphs
     std::map<int, cudaGraphExec_t> frame_graphs, dep_graphs;
     std::string err;
+    size_t tc_part_floats = 0;
+    int tc_count_max = 0;
     // set while pm_profile_frame records a frame eagerly
     std::vector<cudaEvent_t>* prof_ev = nullptr;
     std::vector<int>* prof_kind = nullptr;
@@ -195,6 +204,9 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
     ep.D = D;
     ep.B = B;
     ep.n_streams = f.n_streams;
+    ep.rope_tab = c->rope_tab;
+    ep.rope_freq = c->rope_freq;
+    ep.dh = f.dh;
     const bool pdl = c->prof_ev == nullptr;  // eager profiling runs each kernel alone
     pm_status ms = mark(c, s, -1);
     if (ms) return ms;
@@ -223,7 +235,7 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
         p.B_max = f.B_max;
         p.kc = kc;
         p.vc = vc;
-        p.rope_freq = c->rope_freq;
+        p.rope_tab = c->rope_tab;
         pm_status ps = plan(c, p, 2, "in_proj");
         if (ps) return ps;
         PM_CUDA(launch_gemv(PRO_RMSNORM, E_QKV_ROPE, U_PAIR_ADJ, p, s, pdl));
@@ -307,6 +319,148 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
     PM_CUDA(launch_gemv(PRO_RMSNORM, E_HEAD, U_ROW, p, s, pdl));
     if ((ms = mark(c, s, PM_KERNEL_HEAD))) return ms;
     return PM_OK;
+}
+
+
+static int npad_for(int B) { return B <= 16 ? 16 : (B <= 32 ? 32 : 64); }
+
+// B >= 2: every projection on the tensor cores (k_gemm_tc), same kernel families and order
+static pm_status record_frame_tc(pm_ctx* c, int B, cudaStream_t s) {
+    const pm_config& f = c->cfg;
+    const int D = f.D, F = f.ffn, npad = npad_for(B);
+    if (npad > c->npad_max) return fail(c, PM_ERR_UNSUPPORTED, "batch larger than the tensor-core buffers");
+    const bool pdl = c->prof_ev == nullptr;
+    EmbedParams ep;
+    memset(&ep, 0, sizeof ep);
+    for (int k = 0; k < f.n_streams; ++k) {
+        ep.tables[k] = c->tables[k];
+        ep.rows[k] = (k == 0) ? f.text_in : f.audio_in;
+        ep.init_id[k] = (k == 0) ? f.init_text : f.init_audio;
+        ep.delays[k] = f.delays[k];
+    }
+    ep.io = reinterpret_cast<const FrameIO*>(c->io_region);
+    ep.st = c->st;
+    ep.x = c->x;
+    ep.D = D;
+    ep.B = B;
+    ep.n_streams = f.n_streams;
+    ep.rope_tab = c->rope_tab;
+    ep.rope_freq = c->rope_freq;
+    ep.dh = f.dh;
+    ep.xb = c->xb;
+    ep.alpha = c->norm1[0];
+    ep.ss = c->ss;
+    ep.npad = npad;
+    pm_status ms = mark(c, s, -1);
+    if (ms) return ms;
+    PM_CUDA(launch_embed(ep, s, false));
+    if ((ms = mark(c, s, PM_KERNEL_EMBED))) return ms;
+
+    CUtensorMap mx, mo, msb;
+    if (!make_tmap_bf16(&mx, c->xb, D, npad, npad) || !make_tmap_bf16(&mo, c->ob, D, npad, npad) ||
+        !make_tmap_bf16(&msb, c->sb, F, npad, npad))
+        return fail(c, PM_ERR_CUDA, "tensor map encoding failed (activations)");
+    auto base = [&](int epi, int K, int n_mtiles, int n_rows) {
+        TcParams p;
+        memset(&p, 0, sizeof p);
+        p.epi = epi;
+        p.K = K;
+        p.n_mtiles = n_mtiles;
+        p.n_rows = n_rows;
+        p.B = B;
+        p.npad = npad;
+        p.eps = f.eps;
+        p.part = c->tc_part;
+        p.count = c->tc_count;
+        p.st = c->st;
+        p.io = reinterpret_cast<const FrameIO*>(c->io_region);
+        p.D = D;
+        return p;
+    };
+    auto go = [&](const CUtensorMap& A, const CUtensorMap& X, TcParams& p, int kind, const char* what) -> pm_status {
+        if (!plan_tc(p, c->num_sms)) return fail(c, PM_ERR_UNSUPPORTED, std::string("no tensor-core plan for ") + what);
+        if ((size_t)p.n_mtiles * p.maxseg * p.npad * 128 > c->tc_part_floats || p.n_mtiles > c->tc_count_max)
+            return fail(c, PM_ERR_UNSUPPORTED, std::string("tensor-core scratch too small for ") + what);
+        PM_CUDA(launch_tc(A, X, p, s, pdl));
+        return mark(c, s, kind);
+    };
+    const size_t layer_elems = (size_t)f.B_max * f.H * f.ctx * f.dh;
+    for (int l = 0; l < f.n_layers; ++l) {
+        uint16_t* kc = c->kv + (size_t)(2 * l + 0) * layer_elems;
+        uint16_t* vc = c->kv + (size_t)(2 * l + 1) * layer_elems;
+        CUtensorMap mq, mwo, mwi, mwt;
+        if (!make_tmap_bf16(&mq, c->in_proj[l], D, 3 * D, 128) || !make_tmap_bf16(&mwo, c->out_proj[l], D, D, 128) ||
+            !make_tmap_bf16(&mwi, c->lin_in[l], D, 2 * F, 64) || !make_tmap_bf16(&mwt, c->lin_out[l], F, D, 128))
+            return fail(c, PM_ERR_CUDA, "tensor map encoding failed (weights)");
+        // RMSNorm1 (folded) + fused QKV + RoPE + KV append
+        TcParams p = base(TE_QKV_ROPE, D, 3 * D / 128, 3 * D);
+        p.ss_in = c->ss;
+        p.ss_parts = (l == 0) ? (D + 1023) / 1024 : D / 128;
+        p.y = c->q;
+        p.y_stride = D;
+        p.H = f.H;
+        p.dh = f.dh;
+        p.ctx = f.ctx;
+        p.kc = kc;
+        p.vc = vc;
+        p.rope_tab = c->rope_tab;
+        pm_status ps = go(mq, mx, p, PM_KERNEL_QKV, "in_proj");
+        if (ps) return ps;
+        AttnParams ap;
+        memset(&ap, 0, sizeof ap);
+        ap.ob = c->ob;
+        ap.q = c->q;
+        ap.kc = kc;
+        ap.vc = vc;
+        ap.o = c->o;
+        ap.part = c->att_part;
+        ap.count = c->att_count;
+        ap.st = c->st;
+        ap.B = B;
+        ap.H = f.H;
+        ap.ctx = f.ctx;
+        ap.S = attn_max_splits(f.ctx);
+        ap.D = D;
+        ap.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dh));
+        PM_CUDA(launch_attn(ap, s, pdl));
+        if ((ms = mark(c, s, PM_KERNEL_ATTENTION))) return ms;
+        // W_O + residual; emits bf16(norm2 alpha * y) and per-tile sums of y^2
+        p = base(TE_RESIDUAL, D, D / 128, D);
+        p.y = c->x;
+        p.y_stride = D;
+        p.yb = c->xb;
+        p.yb_stride = D;
+        p.alpha_next = c->norm2[l];
+        p.ss_out = c->ss;
+        if ((ps = go(mwo, mo, p, PM_KERNEL_OUT_PROJ, "out_proj"))) return ps;
+        // RMSNorm2 (folded) + linear_in + SwiGLU -> bf16 s
+        p = base(TE_SWIGLU, D, F / 64, F);
+        p.ss_in = c->ss;
+        p.ss_parts = D / 128;
+        p.split_rows = F;
+        p.yb = c->sb;
+        p.yb_stride = F;
+        if ((ps = go(mwi, mx, p, PM_KERNEL_LINEAR_IN, "linear_in"))) return ps;
+        // linear_out + residual; emits the next norm's operand
+        p = base(TE_RESIDUAL, F, D / 128, D);
+        p.y = c->x;
+        p.y_stride = D;
+        p.yb = c->xb;
+        p.yb_stride = D;
+        p.alpha_next = (l + 1 < f.n_layers) ? c->norm1[l + 1] : c->out_norm;
+        p.ss_out = c->ss;
+        if ((ps = go(mwt, msb, p, PM_KERNEL_LINEAR_OUT, "linear_out"))) return ps;
+    }
+    CUtensorMap mh;
+    if (!make_tmap_bf16(&mh, c->text_linear, D, f.text_out, 128))
+        return fail(c, PM_ERR_CUDA, "tensor map encoding failed (text head)");
+    TcParams p = base(TE_HEAD, D, (f.text_out + 127) / 128, f.text_out);
+    p.ss_in = c->ss;
+    p.ss_parts = D / 128;
+    p.h_internal = c->h;
+    p.x_resid = c->x;
+    p.alpha = c->out_norm;
+    return go(mh, mx, p, PM_KERNEL_HEAD, "text_linear");
 }
 
 static pm_status record_depformer(pm_ctx* c, int B, cudaStream_t s) {
@@ -604,7 +758,30 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     void* p_pos; void* p_first; void* p_ring; void* p_sel; void* p_amax; void* p_hc; void* p_status;
     void* p_damax; void* p_dcount; void* p_dcodes; void* p_dtok; void* p_dsup;
     void* p_io; void* p_dio; void *p_x, *p_q, *p_o, *p_s, *p_h, *p_part, *p_cnt, *p_freq, *p_dz, *p_dq, *p_dout,
-        *p_ds, *p_dkv;
+        *p_ds, *p_dkv, *p_rtab, *p_xb, *p_ob, *p_sb, *p_ss, *p_tcp, *p_tcc;
+    // tensor-core path scratch, sized from the plans of this configuration's projections
+    const int NP = BM >= 2 ? (BM <= 16 ? 16 : (BM <= 32 ? 32 : 64)) : 16;
+    size_t tc_part_floats = 16;
+    int tc_count_max = 1;
+    if (BM >= 2) {
+        const int shapes[5][2] = {{f.D, 3 * f.D / 128}, {f.D, f.D / 128}, {f.D, f.ffn / 64}, {f.ffn, f.D / 128},
+                                  {f.D, (f.text_out + 127) / 128}};
+        for (auto& sh : shapes) {
+            TcParams t;
+            memset(&t, 0, sizeof t);
+            t.K = sh[0];
+            t.n_mtiles = sh[1];
+            t.B = 1;
+            t.npad = NP;
+            if (!plan_tc(t, c->num_sms)) return bail(PM_ERR_UNSUPPORTED, "a tensor-core projection has no plan");
+            const size_t need = (size_t)t.n_mtiles * t.maxseg * NP * 128;
+            if (need > tc_part_floats) tc_part_floats = need;
+            if (t.n_mtiles > tc_count_max) tc_count_max = t.n_mtiles;
+        }
+    }
+    c->npad_max = BM >= 2 ? NP : 0;
+    c->tc_part_floats = tc_part_floats;
+    c->tc_count_max = tc_count_max;
     std::vector<Item> items = {
         {&p_pos, 4u * BM}, {&p_first, 4u * BM}, {&p_ring, 4u * BM * 4 * PM_MAX_STREAMS_DEV},
         {&p_sel, 4u * BM * PM_MAX_STREAMS_DEV}, {&p_amax, 8u * BM}, {&p_hc, 4u * BM}, {&p_status, 16u},
@@ -613,7 +790,9 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
         {&p_io, 64u + 4u * BM * S}, {&p_dio, 64u + 4u * BM + 4u * BM * Q},
         {&p_x, 4u * BM * f.D}, {&p_q, 4u * BM * f.D}, {&p_o, 4u * BM * f.D}, {&p_s, 4u * BM * f.ffn},
         {&p_h, 4u * BM * f.D}, {&p_part, 4u * BM * f.H * attn_max_splits(f.ctx) * (f.dh + 2)}, {&p_cnt, 4u * BM * f.H},
-        {&p_freq, 8u * (f.dh / 2)},
+        {&p_freq, 8u * (f.dh / 2)}, {&p_rtab, 8u * BM * (f.dh / 2)},
+        {&p_xb, 2u * NP * f.D}, {&p_ob, 2u * NP * f.D}, {&p_sb, 2u * NP * f.ffn}, {&p_ss, 4u * (f.D / 128) * NP},
+        {&p_tcp, 4u * tc_part_floats}, {&p_tcc, 4u * (size_t)tc_count_max},
         {&p_dz, 4u * BM * (Dd ? Dd : 1)}, {&p_dq, 4u * BM * (Dd ? Dd : 1)}, {&p_dout, 4u * BM * (Dd ? Dd : 1)},
         {&p_ds, 4u * BM * (Fd ? Fd : 1)},
         {&p_dkv, c->has_dep ? 2u * 2u * f.dep_layers * BM * f.dep_H * Q * f.dep_dh : 16u},
@@ -655,6 +834,13 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     c->att_part = (float*)p_part;
     c->att_count = (uint32_t*)p_cnt;
     c->rope_freq = (double*)p_freq;
+    c->rope_tab = (float2*)p_rtab;
+    c->xb = (uint16_t*)p_xb;
+    c->ob = (uint16_t*)p_ob;
+    c->sb = (uint16_t*)p_sb;
+    c->ss = (float*)p_ss;
+    c->tc_part = (float*)p_tcp;
+    c->tc_count = (uint32_t*)p_tcc;
     c->dz = (float*)p_dz;
     c->dq = (float*)p_dq;
     c->dout = (float*)p_dout;
@@ -697,6 +883,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
         if (!good) return bail(PM_ERR_UNSUPPORTED, "a GEMV shape has no plan");
     }
     if (ck(gemv_prepare())) return bail(PM_ERR_CUDA, "gemv_prepare()");
+    if (BM >= 2 && ck(tc_prepare())) return bail(PM_ERR_CUDA, "tc_prepare");
     if (ck(cudaDeviceSynchronize())) return bail(PM_ERR_CUDA, "cudaDeviceSynchronize()");
     *out = c;
     return PM_OK;
@@ -784,7 +971,7 @@ extern "C" pm_status pm_frame_step(pm_ctx* c, int B, const int32_t* ids, float* 
             }
     }
     cudaGraphExec_t ex;
-    pm_status st = get_graph(c, c->frame_graphs, B, record_frame, &ex);
+    pm_status st = get_graph(c, c->frame_graphs, B, B >= 2 ? record_frame_tc : record_frame, &ex);
     if (st) return st;
     uint8_t* host;
     cudaEvent_t ev;
@@ -889,7 +1076,7 @@ extern "C" pm_status pm_profile_frame(pm_ctx* c, int B, const int32_t* ids, floa
     std::vector<int> kinds;
     c->prof_ev = &evs;
     c->prof_kind = &kinds;
-    st = record_frame(c, B, c->stream);
+    st = (B >= 2 ? record_frame_tc : record_frame)(c, B, c->stream);
     c->prof_ev = nullptr;
     c->prof_kind = nullptr;
     cudaError_t e = cudaStreamSynchronize(c->stream);

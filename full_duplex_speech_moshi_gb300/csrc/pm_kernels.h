@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cuda.h>
+
 #include "pm_common.cuh"
 
 namespace pm {
@@ -52,7 +54,7 @@ struct GemvParams {
     int D, H, dh, ctx, B_max;
     uint16_t* kc;          // K cache of this layer: [B_max][H][ctx][dh]
     uint16_t* vc;          // V cache of this layer
-    const double* rope_freq;  // [dh/2]
+    const float2* rope_tab;   // [B][dh/2] (cos, sin) of this frame's positions
     // E_HEAD
     const FrameIO* io;
     float* h_internal;     // [B][K] normalised input copy (the hidden state), written by CTA 0
@@ -88,6 +90,15 @@ struct EmbedParams {
     int rows[PM_MAX_STREAMS_DEV];
     int init_id[PM_MAX_STREAMS_DEV];
     int delays[PM_MAX_STREAMS_DEV];
+    // RoPE table of this frame: rope_tab[b][j] = (cos, sin)(pos_b * freq[j]), j < dh/2
+    float2* rope_tab;
+    const double* rope_freq;
+    int dh;
+    // tensor-core path (B >= 2): bf16(alpha * x) operand [npad][D] and per-CTA sums of x^2
+    uint16_t* xb;
+    const uint16_t* alpha;
+    float* ss;       // [D/1024][npad]
+    int npad;
 };
 cudaError_t launch_embed(const EmbedParams& p, cudaStream_t s, bool pdl);
 
@@ -95,6 +106,7 @@ cudaError_t launch_embed(const EmbedParams& p, cudaStream_t s, bool pdl);
 // split-KV decode attention over the temporal ring (dh = 128)
 // ----------------------------------------------------------------------------------
 struct AttnParams {
+    uint16_t* ob;          // [npad][D] bf16 copy of o for the tensor-core W_O, or null
     const float* q;        // [B][D] rotated queries
     const uint16_t* kc;    // [B_max][H][ctx][dh]
     const uint16_t* vc;
@@ -132,5 +144,58 @@ struct DepAttnParams {
     float scale_log2;
 };
 cudaError_t launch_dep_attn(const DepAttnParams& p, cudaStream_t s, bool pdl);
+
+// ----------------------------------------------------------------------------------
+// batched projections on the tensor cores (tcgen05, accumulators in TMEM), B >= 2
+// ----------------------------------------------------------------------------------
+enum TcEpilogue {
+    TE_STORE = 0,     // y[b][row] = acc
+    TE_RESIDUAL = 1,  // y[b][row] += acc; yb = bf16(alpha_next * y); per-tile sum of y^2
+    TE_SWIGLU = 2,    // tile = 64 gate rows + 64 value rows: yb[b][j] = bf16(SiLU(g) * z)
+    TE_QKV_ROPE = 3,  // RoPE on q, k rows; q to y (fp32), k, v to the KV ring (bf16)
+    TE_HEAD = 4       // text head logits + greedy token, frame finalisation, hidden state
+};
+
+struct TcParams {
+    int epi;
+    int K, nk;               // row length, 64-element k tiles
+    int n_rows;              // rows that are real outputs (guards the last tile)
+    int n_mtiles;            // 128-row tiles (TE_SWIGLU: 64 gate/value row pairs per tile)
+    int split_rows;          // TE_SWIGLU: value rows start here
+    int B, npad;             // batch rows, MMA N (16, 32 or 64)
+    int grid, nst, maxseg;   // plan (plan_tc)
+    size_t smem;
+    // RMSNorm of the input: inv[b] = 1 / sqrt(sum(ss_in[part][b]) / K + eps)
+    const float* ss_in;      // [ss_parts][npad] or null (no norm)
+    int ss_parts;
+    float eps;
+    // outputs
+    float* y;                // fp32 [B][y_stride]
+    int y_stride;
+    uint16_t* yb;            // bf16 [npad][yb_stride] operand of the next projection, or null
+    int yb_stride;
+    const uint16_t* alpha_next;  // TE_RESIDUAL: scale folded into yb (next RMSNorm's alpha)
+    float* ss_out;           // TE_RESIDUAL: [n_mtiles][npad] per-tile sum of squares of y
+    // stream-K partials and per-tile completion counters (zero between launches)
+    float* part;             // [n_mtiles][maxseg][npad][128]
+    uint32_t* count;         // [n_mtiles]
+    DevState st;
+    // TE_QKV_ROPE
+    int D, H, dh, ctx;
+    uint16_t* kc;
+    uint16_t* vc;
+    const float2* rope_tab;  // [B][dh/2] (cos, sin) of this frame's positions
+    // TE_HEAD
+    const FrameIO* io;
+    float* h_internal;       // [B][D] hidden state
+    const float* x_resid;    // [B][D] residual before the final norm
+    const uint16_t* alpha;   // final norm scale [D]
+};
+
+bool plan_tc(TcParams& p, int num_sms);
+cudaError_t launch_tc(const CUtensorMap& A, const CUtensorMap& Bop, const TcParams& p, cudaStream_t s, bool pdl);
+cudaError_t tc_prepare();
+// 2-D bf16 tensor map, 128-byte swizzle, box {64, box_rows}; false if the driver refuses it
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
 
 }  // namespace pm
