@@ -172,6 +172,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--extras", type=int, default=1, help="also time B=8 and the depformer")
     ap.add_argument("--prime", type=int, default=PRIME, help="frames decoded before warm-up")
+    ap.add_argument("--batch", type=int, default=1,
+                    help="conversations per step (1 = the workload; 8 = the metric's batched case)")
     ap.add_argument("--layers", type=int, default=32,
                     help="temporal blocks (32 = the workload; fewer only for small profiler captures)")
     args = ap.parse_args()
@@ -200,21 +202,22 @@ def main():
     dev = "cuda"
     stream = torch.cuda.current_stream()
     W = I.make_weights_device(s, depformer=True, seed=1000 + 7919 * rank, device=dev)
-    cfg1 = pm.make_config(s.asdict(), 1, True)
+    BB = args.batch
+    cfg1 = pm.make_config(s.asdict(), BB, True)
     kv1 = pm.alloc_kv_cache(cfg1)
-    ctx = pm.Context(s.asdict(), W, kv1, B_max=1, depformer=True, stream=stream.cuda_stream)
+    ctx = pm.Context(s.asdict(), W, kv1, B_max=BB, depformer=True, stream=stream.cuda_stream)
     T = PR + args.warmup + args.steps
-    ids_h = I.make_ids(s, T + 64, seed=2000 + rank)[:, :1]     # [T, 1, 17]
+    ids_h = I.make_ids(s, T + 64, B=BB, seed=2000 + rank)      # [T, B, 17]
     ids_fb = ids_h.copy()
-    ids_fb[PR:, 0, 0] = pm.PM_ID_FEEDBACK
+    ids_fb[PR:, :, 0] = pm.PM_ID_FEEDBACK
     ids_d = torch.from_numpy(ids_fb).to(dev)
-    logits = torch.empty((1, s.text_out), dtype=torch.float32, device=dev)
-    hidden = torch.empty((1, s.D), dtype=torch.float32, device=dev)
-    token = torch.empty((1,), dtype=torch.int32, device=dev)
+    logits = torch.empty((BB, s.text_out), dtype=torch.float32, device=dev)
+    hidden = torch.empty((BB, s.D), dtype=torch.float32, device=dev)
+    token = torch.empty((BB,), dtype=torch.int32, device=dev)
 
     # prime + warm-up
     for t in range(PR + args.warmup):
-        ctx.frame_step(1, ids_d[t], logits, hidden, token)
+        ctx.frame_step(BB, ids_d[t], logits, hidden, token)
     torch.cuda.synchronize()
     p0 = PR + args.warmup
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -223,7 +226,7 @@ def main():
     with ClockSampler(local) as clk:
         start.record(stream)
         for t in range(args.steps):
-            ctx.frame_step(1, ids_d[p0 + t], logits, hidden, token)
+            ctx.frame_step(BB, ids_d[p0 + t], logits, hidden, token)
         end.record(stream)
         torch.cuda.synchronize()
     barrier()
@@ -232,19 +235,19 @@ def main():
         tt = torch.tensor([ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         ms = float(tt.item())
-    fps = args.steps / (ms / 1000.0) * world
+    fps = args.steps / (ms / 1000.0) * world * BB
     ms_step = ms / args.steps
     # keys read per frame = min(pos + 1, ctx); one new K/V row written
     mean_keys = statistics.mean(min(p + 1, s.ctx) for p in range(p0, p0 + args.steps))
     nl = s.n_layers
     bytes_per_frame = (FRAME_FIXED_BYTES - (32 - nl) * (BLOCK_BYTES + 16384)
-                       + KV_BYTES_PER_POS // 32 * nl * (mean_keys + 1))
+                       + KV_BYTES_PER_POS // 32 * nl * (mean_keys + 1) * BB)
     frame_gbs = bytes_per_frame / (ms_step / 1000.0) / 1e9
 
     # per-launch device times (dominant kernel) from eager frames with events
     prof = []
     for t in range(16):
-        prof.append(ctx.profile_frame(1, ids_d[p0 + args.steps + t], logits, hidden, token))
+        prof.append(ctx.profile_frame(BB, ids_d[p0 + args.steps + t], logits, hidden, token))
     by_kind = {}
     for fr in prof[4:]:
         for kind, kms in fr:
@@ -255,10 +258,10 @@ def main():
 
     # end to end: host IDs in, greedy token out and fed back, every frame
     ctx.reset()
-    ids_pin = torch.from_numpy(ids_h[:T, 0].copy()).pin_memory()
-    tok_host = torch.zeros((1,), dtype=torch.int32).pin_memory()
+    ids_pin = torch.from_numpy(ids_h[:T].copy()).pin_memory()
+    tok_host = torch.zeros((BB,), dtype=torch.int32).pin_memory()
     for t in range(PR + args.warmup):
-        ctx.frame_step(1, ids_pin[t], logits, hidden, token)
+        ctx.frame_step(BB, ids_pin[t], logits, hidden, token)
     torch.cuda.synchronize()
     barrier()
     t0 = time.perf_counter()
@@ -269,11 +272,11 @@ def main():
     for t in range(args.steps):
         row = ids_pin[p0 + t]
         if nxt is not None:
-            row[0] = nxt
-        ctx.frame_step(1, row, logits, hidden, token)
+            row[:, 0] = nxt
+        ctx.frame_step(BB, row, logits, hidden, token)
         tok_host.copy_(token, non_blocking=True)
         stream.synchronize()
-        nxt = int(tok_host[0])
+        nxt = tok_host.clone()
     e_end.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
@@ -282,10 +285,10 @@ def main():
         tt = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         e2e_ms = float(tt.item())
-    e2e_fps = args.steps / (e2e_ms / 1000.0) * world
+    e2e_fps = args.steps / (e2e_ms / 1000.0) * world * BB
 
     extras = {}
-    if args.extras:
+    if args.extras and BB == 1:
         # depformer after every frame (greedy agent codes, supplied user codes)
         sup = torch.from_numpy(I.make_supplied_codes(s, 64, seed=4000)[:, 0].copy()).to(dev)
         dl = torch.empty((1, s.dep_steps, s.dep_card), dtype=torch.float32, device=dev)
@@ -314,7 +317,7 @@ def main():
     ctx.close()
     del kv1
     torch.cuda.empty_cache()
-    if args.extras:
+    if args.extras and BB == 1:
         B8 = 8
         cfg8 = pm.make_config(s.asdict(), B8, False)
         kv8 = pm.alloc_kv_cache(cfg8)
@@ -337,32 +340,34 @@ def main():
         ctx8.close()
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and BB == 1:
         cpu = cpu_baseline_sample()
 
     if rank == 0:
         launches_per_frame = 2 + 5 * s.n_layers
+        metric = METRIC if BB == 1 else f"temporal stream-frames/s (B={BB}, 32-block stack, greedy text feedback)"
         traffic = None
         tp = os.path.join(ROOT, "profiles", "traffic.json")
         if os.path.exists(tp):
             traffic = json.load(open(tp)).get("linear_in_swiglu_bytes_per_launch")
         line = {
-            "metric": METRIC, "value": fps, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
+            "metric": metric, "value": fps, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init bf16 weights, seeded IDs)",
             "config": {"workload": "32-block temporal stack (D 4096, 32x128 heads, SwiGLU 11264, ctx 3000, "
                                    "text head 32000), B=1, 256 primed frames then greedy text feedback",
-                       "global_batch": world, "seq_len": p0 + args.steps, "parallelism": f"replicas x{world}",
+                       "global_batch": world * BB, "seq_len": p0 + args.steps, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2: 13.4 GB of weights streamed per frame",
                        "frame_bytes": bytes_per_frame, "frame_gbs": frame_gbs,
                        "frame_frac_of_peak": frame_gbs / peak},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "RMSNorm + linear_in [22528,4096] + SwiGLU GEMV",
+                         "frac": achieved / peak, "traffic": traffic if BB == 1 else None,
+                         "kernel": ("RMSNorm + linear_in [22528,4096] + SwiGLU GEMV" if BB == 1 else
+                                    f"RMSNorm + linear_in [22528,4096] + SwiGLU, tcgen05 GEMM N={16 if BB <= 16 else 64}"),
                          "kernel_ms": w_in_ms, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
             "kernel_ms_mean": {k: statistics.mean(v) for k, v in by_kind.items()},
-            "e2e": {"value": e2e_fps, "unit": "frames/s", "h2d_bytes_per_step": 64 + 4 * s.n_streams,
-                    "d2h_bytes_per_step": 4},
+            "e2e": {"value": e2e_fps, "unit": "frames/s", "h2d_bytes_per_step": 64 + 4 * s.n_streams * BB,
+                    "d2h_bytes_per_step": 4 * BB},
             "gpu_launches": launches_per_frame * args.steps,
             "clocks": clk.summary(),
             "cpu_baseline": cpu,

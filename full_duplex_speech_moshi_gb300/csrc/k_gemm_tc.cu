@@ -26,6 +26,18 @@
 #include "pm_kernels.h"
 #include "tc_common.cuh"
 
+// Tiling policy (compile-time tuning constants): CTAs per SM, fewest k-units per CTA
+// (bounds how many ways a tile is split), bytes of the stage ring per CTA.
+#ifndef PM_TC_CTAS_PER_SM
+#define PM_TC_CTAS_PER_SM 2
+#endif
+#ifndef PM_TC_MIN_UNITS
+#define PM_TC_MIN_UNITS 1
+#endif
+#ifndef PM_TC_RING_BYTES
+#define PM_TC_RING_BYTES (96u * 1024u)
+#endif
+
 namespace pm {
 namespace {
 
@@ -104,7 +116,9 @@ __global__ void __launch_bounds__(192, 1)
                 const long long u = w0 + i;
                 const int m = (int)(u / p.nk), kt = (int)(u % p.nk);
                 uint8_t* dst = smem + (size_t)(i % nst) * ST_BYTES;
-                if (EPI == TE_SWIGLU) {
+                if (p.a_tiled) {
+                    tma_load_2d(dst, &tmA, 0, (int)(u * 128), &full[i % nst], pol_w);
+                } else if (EPI == TE_SWIGLU) {
                     tma_load_2d(dst, &tmA, kt * KT, m * 64, &full[i % nst], pol_w);
                     tma_load_2d(dst + A_BYTES / 2, &tmA, kt * KT, p.split_rows + m * 64, &full[i % nst], pol_w);
                 } else {
@@ -114,7 +128,10 @@ __global__ void __launch_bounds__(192, 1)
             auto load_b = [&](int i) {
                 const long long u = w0 + i;
                 const int kt = (int)(u % p.nk);
-                tma_load_2d(smem + (size_t)(i % nst) * ST_BYTES + A_BYTES, &tmB, kt * KT, 0, &full[i % nst], pol_x);
+                if (p.b_tiled)
+                    tma_load_2d(smem + (size_t)(i % nst) * ST_BYTES + A_BYTES, &tmB, 0, kt * NPAD, &full[i % nst], pol_x);
+                else
+                    tma_load_2d(smem + (size_t)(i % nst) * ST_BYTES + A_BYTES, &tmB, kt * KT, 0, &full[i % nst], pol_x);
             };
             const int pre = n < nst ? n : nst;
             for (int i = 0; i < pre; ++i) {
@@ -426,11 +443,13 @@ bool plan_tc(TcParams& p, int num_sms) {
     if (!(p.npad == 16 || p.npad == 32 || p.npad == 64) || p.B < 1 || p.B > p.npad) return false;
     p.nk = p.K / KT;
     const long long U = (long long)p.n_mtiles * p.nk;
-    int G = 2 * num_sms;
-    if (U < G) G = (int)U;
+    const int min_units = p.min_units > 0 ? p.min_units : PM_TC_MIN_UNITS;
+    int G = PM_TC_CTAS_PER_SM * num_sms;
+    if ((long long)G * min_units > U) G = (int)((U + min_units - 1) / min_units);
+    if (G < 1) G = 1;
     p.grid = G;
     const uint32_t st_bytes = A_BYTES + (uint32_t)p.npad * 128u;
-    p.nst = (int)((96u * 1024u) / st_bytes);
+    p.nst = (int)((PM_TC_RING_BYTES) / st_bytes);
     if (p.nst < 2) p.nst = 2;
     int maxseg = 1;
     for (int m = 0; m < p.n_mtiles; ++m) {

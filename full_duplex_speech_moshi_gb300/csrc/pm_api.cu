@@ -254,6 +254,7 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
         ap.H = f.H;
         ap.ctx = f.ctx;
         ap.S = attn_max_splits(f.ctx);
+        ap.grid = (B == 1 ? 4 : 16) * c->num_sms;
         ap.D = D;
         ap.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dh));
         PM_CUDA(launch_attn(ap, s, pdl));
@@ -420,6 +421,7 @@ static pm_status record_frame_tc(pm_ctx* c, int B, cudaStream_t s) {
         ap.H = f.H;
         ap.ctx = f.ctx;
         ap.S = attn_max_splits(f.ctx);
+        ap.grid = (B == 1 ? 4 : 16) * c->num_sms;
         ap.D = D;
         ap.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dh));
         PM_CUDA(launch_attn(ap, s, pdl));

@@ -15,6 +15,8 @@
 
 // streams a frame may carry (text + audio codebooks)
 #define PM_MAX_STREAMS_DEV 32
+// largest batch a context serves
+#define PM_MAX_B_DEV 64
 
 // status bits written by kernels (read back by pm_device_status)
 #define PM_DEV_ERR_INVALID_ID 1u

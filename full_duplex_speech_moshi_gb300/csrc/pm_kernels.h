@@ -115,6 +115,7 @@ struct AttnParams {
     uint32_t* count;       // [B][H], zero between launches
     DevState st;
     int B, H, ctx, S, D;
+    int grid;              // CTAs walking the work list
     float scale_log2;      // log2(e) / sqrt(dh)
 };
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl);
@@ -164,6 +165,9 @@ struct TcParams {
     int split_rows;          // TE_SWIGLU: value rows start here
     int B, npad;             // batch rows, MMA N (16, 32 or 64)
     int grid, nst, maxseg;   // plan (plan_tc)
+    int min_units;           // plan input: fewest (tile, k-tile) units per CTA (0 = default)
+    int a_tiled;             // A is pre-tiled: unit u is rows u*128 .. +127 of a [units*128][64] tensor
+    int b_tiled;             // B is pre-tiled: k tile kt is rows kt*npad .. of a [nk*npad][64] tensor
     size_t smem;
     // RMSNorm of the input: inv[b] = 1 / sqrt(sum(ss_in[part][b]) / K + eps)
     const float* ss_in;      // [ss_parts][npad] or null (no norm)
