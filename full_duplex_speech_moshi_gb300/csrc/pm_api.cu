@@ -75,6 +75,12 @@ struct pm_ctx {
     std::string err;
     size_t tc_part_floats = 0;
     int tc_count_max = 0;
+    // persistent batch-1 frame program (null when the shape or device does not allow it)
+    bool prog = false;
+    FPhase* d_phases = nullptr;
+    uint32_t* prog_bar = nullptr;
+    size_t prog_smem = 0;
+    FrameProgParams prog_params{};
     // set while pm_profile_frame records a frame eagerly
     std::vector<cudaEvent_t>* prof_ev = nullptr;
     std::vector<int>* prof_kind = nullptr;
@@ -190,6 +196,12 @@ static pm_status mark(pm_ctx* c, cudaStream_t s, int kind) {
 static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
     const pm_config& f = c->cfg;
     const int D = f.D, F = f.ffn;
+    if (B == 1 && c->prog) {
+        pm_status ms = mark(c, s, -1);
+        if (ms) return ms;
+        PM_CUDA(launch_frame_prog(c->prog_params, c->num_sms, c->prog_smem, s));
+        return mark(c, s, PM_KERNEL_FRAME);
+    }
     EmbedParams ep;
     memset(&ep, 0, sizeof ep);
     for (int k = 0; k < f.n_streams; ++k) {
@@ -652,6 +664,7 @@ static void free_ctx(pm_ctx* c) {
     }
     if (c->cap) cudaStreamDestroy(c->cap);
     if (c->block) cudaFree(c->block);
+    if (c->d_phases) cudaFree(c->d_phases);
     delete c;
 }
 
@@ -883,6 +896,108 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
             good = good && chk(f.D, f.dep_D, 1) && chk(f.dep_D, 3 * f.dep_D, 1) && chk(f.dep_D, f.dep_D, 1) &&
                    chk(f.dep_D, f.dep_ffn, 2) && chk(f.dep_ffn, f.dep_D, 1) && chk(f.dep_D, f.dep_card, 1);
         if (!good) return bail(PM_ERR_UNSUPPORTED, "a GEMV shape has no plan");
+    }
+    // persistent batch-1 frame program: phases of the whole frame, built once
+    if ((f.flags & PM_FLAG_FRAME_PROGRAM) && frame_prog_supported(f.D, f.ffn, f.dh)) {
+        int coop = 0;
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device);
+        std::vector<FPhase> ph;
+        int partial_floats = 1;
+        const int G = c->num_sms;
+        auto gemv = [&](int epi, int unit, int K, int n_units, int split, const uint16_t* W, const float* x,
+                        const uint16_t* alpha, float* y, uint16_t* kc, uint16_t* vc) {
+            FPhase q;
+            memset(&q, 0, sizeof q);
+            q.type = PH_GEMV;
+            q.epi = epi;
+            q.unit = unit;
+            q.K = K;
+            q.n_units = n_units;
+            q.split_rows = split;
+            const int rpu = unit == U_ROW ? 1 : 2;
+            q.upst = frame_prog_stage_rows(K) / rpu;
+            q.W = W;
+            q.x = x;
+            q.alpha = alpha;
+            q.y = y;
+            q.kc = kc;
+            q.vc = vc;
+            const int need = ((n_units + G - 1) / G) * rpu * (K / 1024);
+            if (need > partial_floats) partial_floats = need;
+            ph.push_back(q);
+            return q.upst >= 1;
+        };
+        bool good = coop != 0;
+        FPhase e;
+        memset(&e, 0, sizeof e);
+        e.type = PH_EMBED;
+        ph.push_back(e);
+        const size_t layer_elems = (size_t)f.B_max * f.H * f.ctx * f.dh;
+        for (int l = 0; l < f.n_layers; ++l) {
+            uint16_t* kc = c->kv + (size_t)(2 * l + 0) * layer_elems;
+            uint16_t* vc = c->kv + (size_t)(2 * l + 1) * layer_elems;
+            good = good && gemv(E_QKV_ROPE, U_PAIR_ADJ, f.D, 3 * f.D / 2, 0, c->in_proj[l], c->x, c->norm1[l], c->q,
+                                kc, vc);
+            FPhase a;
+            memset(&a, 0, sizeof a);
+            a.type = PH_ATTN;
+            a.kc = kc;
+            a.vc = vc;
+            ph.push_back(a);
+            good = good && gemv(E_RESIDUAL, U_ROW, f.D, f.D, 0, c->out_proj[l], c->o, nullptr, c->x, kc, vc);
+            good = good && gemv(E_SWIGLU, U_PAIR_SPLIT, f.D, f.ffn, f.ffn, c->lin_in[l], c->x, c->norm2[l], c->s,
+                                kc, vc);
+            good = good && gemv(E_RESIDUAL, U_ROW, f.ffn, f.D, 0, c->lin_out[l], c->s, nullptr, c->x, kc, vc);
+        }
+        good = good && gemv(E_HEAD, U_ROW, f.D, f.text_out, 0, c->text_linear, c->x, c->out_norm, nullptr,
+                            nullptr, nullptr);
+        const int S = attn_max_splits(f.ctx);
+        const size_t smem = frame_prog_smem(partial_floats, S);
+        int occ = 0;
+        good = good && S <= 64 && smem <= 226u * 1024u && frame_prog_prepare(smem) == cudaSuccess &&
+               frame_prog_occupancy(smem, &occ) == cudaSuccess && occ >= 1;
+        cudaGetLastError();
+        if (good) {
+            if (ck(cudaMalloc(&c->d_phases, sizeof(FPhase) * ph.size() + 4u * ph.size())))
+                return bail(PM_ERR_OOM, "device allocation (frame program)");
+            c->prog_bar = reinterpret_cast<uint32_t*>(c->d_phases + ph.size());
+            if (ck(cudaMemcpy(c->d_phases, ph.data(), sizeof(FPhase) * ph.size(), cudaMemcpyHostToDevice)) ||
+                ck(cudaMemset(c->prog_bar, 0, 4u * ph.size())))
+                return bail(PM_ERR_CUDA, "frame program upload");
+            FrameProgParams& pp = c->prog_params;
+            memset(&pp, 0, sizeof pp);
+            pp.ph = c->d_phases;
+            pp.n_phases = (int)ph.size();
+            pp.st = c->st;
+            pp.io = reinterpret_cast<const FrameIO*>(c->io_region);
+            for (int k = 0; k < f.n_streams; ++k) {
+                pp.tables[k] = c->tables[k];
+                pp.rows[k] = (k == 0) ? f.text_in : f.audio_in;
+                pp.init_id[k] = (k == 0) ? f.init_text : f.init_audio;
+                pp.delays[k] = f.delays[k];
+            }
+            pp.n_streams = f.n_streams;
+            pp.rope_freq = c->rope_freq;
+            pp.rope_tab = c->rope_tab;
+            pp.x = c->x;
+            pp.q = c->q;
+            pp.o = c->o;
+            pp.h = c->h;
+            pp.D = f.D;
+            pp.H = f.H;
+            pp.dh = f.dh;
+            pp.ctx = f.ctx;
+            pp.eps = f.eps;
+            pp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dh));
+            pp.part = c->att_part;
+            pp.att_count = c->att_count;
+            pp.S = S;
+            pp.max_chunks = S;
+            pp.partial_floats = partial_floats;
+            pp.bar = c->prog_bar;
+            c->prog_smem = smem;
+            c->prog = true;
+        }
     }
     if (ck(gemv_prepare())) return bail(PM_ERR_CUDA, "gemv_prepare()");
     if (BM >= 2 && ck(tc_prepare())) return bail(PM_ERR_CUDA, "tc_prepare");

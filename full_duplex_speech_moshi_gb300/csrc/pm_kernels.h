@@ -202,4 +202,57 @@ cudaError_t tc_prepare();
 // 2-D bf16 tensor map, 128-byte swizzle, box {64, box_rows}; false if the driver refuses it
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);
 
+// ----------------------------------------------------------------------------------
+// persistent frame program (B = 1): one cooperative launch runs the whole frame
+// ----------------------------------------------------------------------------------
+enum PhaseType { PH_EMBED = 0, PH_GEMV = 1, PH_ATTN = 2 };
+
+struct FPhase {
+    int type;
+    int epi;            // PH_GEMV: E_QKV_ROPE, E_RESIDUAL, E_SWIGLU, E_HEAD
+    int unit;           // U_ROW, U_PAIR_ADJ, U_PAIR_SPLIT
+    int K;              // row length (multiple of 1024)
+    int n_units;
+    int split_rows;     // U_PAIR_SPLIT
+    int upst;           // units per shared-memory stage
+    const uint16_t* W;  // [rows][K] bf16
+    const float* x;     // input vector [K]
+    const uint16_t* alpha;  // RMSNorm scale of the input, or null
+    float* y;           // output vector
+    uint16_t* kc;       // QKV / attention: this layer's K cache [H][ctx][dh] (batch row 0)
+    uint16_t* vc;
+};
+
+struct FrameProgParams {
+    const FPhase* ph;
+    int n_phases;
+    DevState st;
+    const FrameIO* io;
+    const uint16_t* tables[PM_MAX_STREAMS_DEV];
+    int rows[PM_MAX_STREAMS_DEV];
+    int init_id[PM_MAX_STREAMS_DEV];
+    int delays[PM_MAX_STREAMS_DEV];
+    int n_streams;
+    const double* rope_freq;
+    float2* rope_tab;
+    float* x;
+    float* q;
+    float* o;
+    float* h;
+    int D, H, dh, ctx;
+    float eps, scale_log2;
+    float* part;        // [H][S][dh + 2] attention chunk partials
+    uint32_t* att_count;  // [H]
+    int S, max_chunks;
+    int partial_floats; // shared-memory row partials (max over GEMV phases)
+    uint32_t* bar;      // [n_phases] grid-barrier arrival counters, zero between frames
+};
+
+bool frame_prog_supported(int D, int F, int dh);
+int frame_prog_stage_rows(int K);
+size_t frame_prog_smem(int partial_floats, int max_chunks);
+cudaError_t frame_prog_prepare(size_t smem);
+cudaError_t launch_frame_prog(const FrameProgParams& p, int grid, size_t smem, cudaStream_t s);
+cudaError_t frame_prog_occupancy(size_t smem, int* blocks_per_sm);
+
 }  // namespace pm

@@ -24,7 +24,7 @@ EXPORTS = ["pm_kv_cache_bytes", "pm_create", "pm_reset", "pm_set_positions", "pm
            "pm_frame_step", "pm_depformer_step", "pm_profile_frame", "pm_device_status", "pm_last_error",
            "pm_destroy", "pm_text_head_noalloc"]
 KERNEL_KINDS = {0: "embed", 1: "qkv_rope", 2: "attention", 3: "out_proj", 4: "linear_in_swiglu",
-                5: "linear_out", 6: "text_head"}
+                5: "linear_out", 6: "text_head", 7: "frame_program"}
 
 
 class pm_config(C.Structure):
@@ -34,7 +34,9 @@ class pm_config(C.Structure):
                 ("init_text", C.c_int), ("init_audio", C.c_int), ("eps", C.c_float), ("rope_theta", C.c_float),
                 ("dep_D", C.c_int), ("dep_H", C.c_int), ("dep_dh", C.c_int), ("dep_ffn", C.c_int),
                 ("dep_layers", C.c_int), ("dep_steps", C.c_int), ("dep_ctx", C.c_int), ("dep_card", C.c_int),
-                ("dep_text_in", C.c_int), ("dep_audio_in", C.c_int)]
+                ("dep_text_in", C.c_int), ("dep_audio_in", C.c_int), ("flags", C.c_uint)]
+
+PM_FLAG_FRAME_PROGRAM = 1
 
 
 _PP = C.POINTER(C.c_void_p)
@@ -113,9 +115,10 @@ def _ptr(x) -> Optional[int]:
     raise TypeError(type(x))
 
 
-def make_config(shape: dict, B_max: int, depformer: bool = True) -> pm_config:
+def make_config(shape: dict, B_max: int, depformer: bool = True, flags: int = 0) -> pm_config:
     c = pm_config()
     c.B_max = int(B_max)
+    c.flags = int(flags)
     for k in ("D", "H", "dh", "ffn", "n_layers", "ctx", "text_in", "text_out", "audio_in", "n_streams",
               "init_text", "init_audio", "dep_D", "dep_H", "dep_dh", "dep_ffn", "dep_steps", "dep_ctx",
               "dep_card", "dep_text_in", "dep_audio_in"):
@@ -138,11 +141,11 @@ class Context:
     pm_kv_cache_bytes bytes."""
 
     def __init__(self, shape: dict, weights: Dict[str, object], kv_cache, B_max: int = 1,
-                 depformer: bool = True, stream: int = 0):
+                 depformer: bool = True, stream: int = 0, flags: int = 0):
         L = lib()
         self.L = L
         self.shape = dict(shape)
-        self.cfg = make_config(shape, B_max, depformer)
+        self.cfg = make_config(shape, B_max, depformer, flags)
         s = self.shape
         self._keep: List[object] = []
 

@@ -85,7 +85,14 @@ typedef struct {
     int dep_layers, dep_steps, dep_ctx; /* 6, 16, 8 (or 16) */
     int dep_card;                       /* depth head rows, 2048 */
     int dep_text_in, dep_audio_in;      /* 32001, 2049 */
+    unsigned flags;                     /* PM_FLAG_* */
 } pm_config;
+
+/* pm_config.flags: run batch-1 frames as one persistent cooperative launch (a phase
+ * program with grid-wide barriers) instead of the default chain of one kernel per step.
+ * Needs D and ffn multiples of 1024 and cooperative launch; otherwise the chain runs.
+ * Measured on GB300 at 2.75 ms per 32-block frame against 2.51 ms for the chain. */
+#define PM_FLAG_FRAME_PROGRAM 1u
 
 /* Temporal weights: device pointers.  Per-layer members point to host arrays of
  * n_layers device pointers (copied by pm_create). */
@@ -168,7 +175,8 @@ typedef enum {
     PM_KERNEL_OUT_PROJ = 3,    /* W_O + residual */
     PM_KERNEL_LINEAR_IN = 4,   /* RMSNorm + linear_in + SwiGLU */
     PM_KERNEL_LINEAR_OUT = 5,  /* linear_out + residual */
-    PM_KERNEL_HEAD = 6         /* final RMSNorm + text head + greedy token */
+    PM_KERNEL_HEAD = 6,        /* final RMSNorm + text head + greedy token */
+    PM_KERNEL_FRAME = 7        /* the whole batch-1 frame as one persistent launch */
 } pm_kernel_kind;
 
 /* Same computation and state change as pm_frame_step, but the frame's kernels are

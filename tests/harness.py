@@ -43,7 +43,7 @@ def top2_gap(ref: np.ndarray) -> float:
 class Pair:
     """The same model on the GPU (through the C ABI) and in the oracle."""
 
-    def __init__(self, shape: I.ModelShape, B_max: int = 1, depformer: bool = True, weights=None):
+    def __init__(self, shape: I.ModelShape, B_max: int = 1, depformer: bool = True, weights=None, flags: int = 0):
         import torch
         from full_duplex_speech_moshi_gb300 import pm
         from oracle import oracle as O
@@ -54,10 +54,10 @@ class Pair:
         specs = I.tensor_specs(shape, depformer)
         self.orc = O.Oracle(shape.asdict(), [self.W[n] for n, _, _ in specs], depformer=depformer)
         self.Wd = pm.upload_weights({n: self.W[n] for n, _, _ in specs})
-        self.cfg = pm.make_config(shape.asdict(), B_max, depformer)
+        self.cfg = pm.make_config(shape.asdict(), B_max, depformer, flags)
         self.kv = pm.alloc_kv_cache(self.cfg)
         self.ctx = pm.Context(shape.asdict(), self.Wd, self.kv, B_max=B_max, depformer=depformer,
-                              stream=torch.cuda.current_stream().cuda_stream)
+                              stream=torch.cuda.current_stream().cuda_stream, flags=flags)
         self.B_max = B_max
         self.streams = [self.orc.new_stream() for _ in range(B_max)]
         dev = "cuda"

@@ -33,6 +33,6 @@ def test_kv_cache_bytes_matches_page():
 
 
 def test_config_struct_layout():
-    # the ctypes mirror must match the C struct: 11 ints, 32 delays, 2 ints, 2 floats, 10 ints
+    # the ctypes mirror must match the C struct: 11 ints, 32 delays, 2 ints, 2 floats, 10 ints, flags
     import ctypes as C
-    assert C.sizeof(pm.pm_config) == 4 * (11 + 32 + 2 + 2 + 10)
+    assert C.sizeof(pm.pm_config) == 4 * (11 + 32 + 2 + 2 + 10 + 1)

@@ -91,6 +91,18 @@ def test_config1_full_stack_greedy_feedback(full):
         prev = rt
 
 
+def test_config1_frame_program(full):
+    """The 32-block stack through the persistent single-launch frame program."""
+    from full_duplex_speech_moshi_gb300 import pm
+    p = Pair(I.FULL, B_max=1, depformer=False, flags=pm.PM_FLAG_FRAME_PROGRAM, weights=full.W)
+    try:
+        ids = I.make_ids(p.shape, 8, seed=2005)[:, 0]
+        for t in range(8):
+            p.check_frame(p.gpu_frame(ids[t:t + 1]), p.oracle_frame(ids[t:t + 1]), f"t={t}")
+    finally:
+        p.close()
+
+
 def test_config2_long_context_wrap(full):
     s = full.shape
     full.ctx.reset()

@@ -196,3 +196,66 @@ def test_single_block_tiny_shapes():
             assert logits_rel_l2(gl[q], oc_l[q]) <= 1e-2, q
     finally:
         p.close()
+
+
+def test_frame_program_small_shapes():
+    """The persistent single-launch frame program (D, ffn multiples of 1024) against the
+    oracle: ring wrap, device-side greedy feedback, invalid device IDs as a no-op."""
+    from full_duplex_speech_moshi_gb300 import pm
+    s = small_shape(ffn=3072, ctx=96)
+    p = Pair(s, B_max=1, depformer=False, flags=pm.PM_FLAG_FRAME_PROGRAM)
+    try:
+        T = 2 * s.ctx + 7
+        ids = I.make_ids(s, T, seed=31)[:, 0]
+        for t in range(T):
+            p.check_frame(p.gpu_frame(ids[t:t + 1]), p.oracle_frame(ids[t:t + 1]), f"t={t}")
+        assert p.ctx.get_positions()[0] == T
+        # an invalid ID in device memory leaves the state unchanged
+        bd = p.torch.from_numpy(ids[0:1].copy()).cuda()
+        bd[0, 2] = -2
+        p.ctx.frame_step(1, bd, p.logits, p.hidden, p.token)
+        assert p.ctx.device_status() == pm.PM_ERR_INVALID_ID
+        assert p.ctx.get_positions()[0] == T
+        # greedy feedback on the device continues the same stream
+        st = p.streams[0]
+        more = I.make_ids(s, 6, seed=32)[:, 0]
+        prev = None
+        for t in range(6):
+            gids = more[t:t + 1].copy()
+            rids = more[t].copy()
+            if t > 0:
+                gids[0, 0] = -3
+                rids[0] = prev
+            gh, gl, gt = p.gpu_frame(gids)
+            rh, _, rl, rt = st.step(rids)
+            assert hidden_err(gh[0], rh) <= 2e-2 and logits_rel_l2(gl[0], rl) <= 1e-2, t
+            if int(gt[0]) != rt:
+                assert top2_gap(rl) <= GAP_MIN
+                break
+            prev = rt
+    finally:
+        p.close()
+
+
+def test_frame_program_matches_kernel_chain():
+    """Both batch-1 implementations (one persistent launch, one kernel per step) on the
+    same inputs agree to the parity tolerances at every frame."""
+    from full_duplex_speech_moshi_gb300 import pm
+    s = small_shape(ffn=3072, ctx=48)
+    a = Pair(s, B_max=1, depformer=False, flags=pm.PM_FLAG_FRAME_PROGRAM)
+    try:
+        b_kv = pm.alloc_kv_cache(a.cfg)
+        b = pm.Context(s.asdict(), a.Wd, b_kv, B_max=1, depformer=False,
+                       stream=a.torch.cuda.current_stream().cuda_stream)
+        ids = I.make_ids(s, 60, seed=33)[:, 0]
+        lg = a.torch.zeros_like(a.logits)
+        hd = a.torch.zeros_like(a.hidden)
+        for t in range(60):
+            ga = a.gpu_frame(ids[t:t + 1])
+            b.frame_step(1, np.ascontiguousarray(ids[t:t + 1]), lg, hd, None)
+            a.torch.cuda.synchronize()
+            assert hidden_err(ga[0][0], hd[0].double().cpu().numpy()) <= 1e-3, t
+            assert logits_rel_l2(ga[1][0], lg[0].double().cpu().numpy()) <= 1e-3, t
+        b.close()
+    finally:
+        a.close()
