@@ -1,5 +1,6 @@
-// Depformer helpers ("PersonaPlex native LM audit", section 4 "Native depth
-// computation"): the per-frame set-up kernel and the depth self-attention.
+// Depformer set-up ("PersonaPlex native LM audit", section 4 "Native depth
+// computation").  The depth self-attention itself runs in the prologue of the W_o
+// projection (k_gemv, PRO_DEPATTN).
 //
 // k_dep_begin resolves and validates the conditioning text token (caller's, or the
 // context's last greedy text token) and the supplied codes (-1 = greedy), copies the
@@ -7,9 +8,6 @@
 // an invalid value.  Invalid values are replaced by 0 / -1 so that every later index
 // stays in range; an aborted frame writes no feedback tokens.
 //
-// k_dep_attn: one warp per (head, batch row).  Position q attends to depth positions
-// max(0, q - dep_ctx + 1) .. q of this frame (no positional encoding); lane l owns
-// coordinates 2l, 2l+1 of the 64-wide head.
 #include <math.h>
 
 #include "pm_kernels.h"
@@ -50,43 +48,6 @@ __global__ void __launch_bounds__(256) k_dep_begin(const DepBeginParams p) {
     }
 }
 
-__global__ void __launch_bounds__(32) k_dep_attn(const DepAttnParams p) {
-    pdl_trigger();
-    pdl_wait();
-    const int h = blockIdx.x, b = blockIdx.y, lane = threadIdx.x;
-    const int qpos = p.q_pos;
-    const int lo = max(0, qpos - p.dep_ctx + 1);
-    const int n = qpos - lo + 1;
-    const float2 qv = *reinterpret_cast<const float2*>(p.q + (size_t)b * p.Dd + h * p.dhd + 2 * lane);
-    const size_t hb = ((size_t)b * p.Hd + h) * p.Q * p.dhd;
-    float sc[16];
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        sc[i] = -INFINITY;
-        if (i < n) {
-            const uint32_t kk = *reinterpret_cast<const uint32_t*>(p.kc + hb + (size_t)(lo + i) * p.dhd + 2 * lane);
-            float d = qv.x * bf16lo(kk) + qv.y * bf16hi(kk);
-            d = warp_sum(d) * p.scale_log2;
-            sc[i] = d;
-            m = fmaxf(m, d);
-        }
-    }
-    float l = 0.f, o0 = 0.f, o1 = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        if (i < n) {
-            const float e = exp2f(sc[i] - m);
-            l += e;
-            const uint32_t vv = *reinterpret_cast<const uint32_t*>(p.vc + hb + (size_t)(lo + i) * p.dhd + 2 * lane);
-            o0 += e * bf16lo(vv);
-            o1 += e * bf16hi(vv);
-        }
-    }
-    if (*(volatile uint32_t*)&p.st.status[1] != 0u) return;
-    *reinterpret_cast<float2*>(p.o + (size_t)b * p.Dd + h * p.dhd + 2 * lane) = make_float2(o0 / l, o1 / l);
-}
-
 cudaLaunchConfig_t make_cfg(dim3 grid, dim3 block, cudaStream_t s, bool pdl, cudaLaunchAttribute* attr) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -107,11 +68,5 @@ cudaError_t launch_dep_begin(const DepBeginParams& p, cudaStream_t s, bool pdl) 
     return cudaLaunchKernelEx(&cfg, k_dep_begin, p);
 }
 
-cudaError_t launch_dep_attn(const DepAttnParams& p, cudaStream_t s, bool pdl) {
-    if (p.dhd != 64 || p.dep_ctx > 16) return cudaErrorInvalidValue;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = make_cfg(dim3((unsigned)p.Hd, (unsigned)p.B), dim3(32), s, pdl, attr);
-    return cudaLaunchKernelEx(&cfg, k_dep_attn, p);
-}
 
 }  // namespace pm

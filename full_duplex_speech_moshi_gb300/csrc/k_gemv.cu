@@ -125,6 +125,53 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
         const int kslice = K / P;
         float xr[CH * 8];
         const float* xb = p.x + (size_t)b * p.x_stride + (size_t)pp * kslice;
+        if (PRO == PRO_DEPATTN) {
+            // Depth self-attention of position q over positions max(0, q-ctx+1)..q of this
+            // frame (no positional encoding), recomputed by every CTA from q and the depth
+            // cache: warp w takes heads w, w + W, ...; lane l coordinates 2l, 2l+1 of 64.
+            float* xs = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(red + 32) + 15) & ~(uintptr_t)15);
+            const int lo = max(0, p.q - p.dep_ctx + 1), nk = p.q - lo + 1;
+            for (int hh = warp; hh < p.H; hh += W) {
+                const size_t hb = ((size_t)b * p.H + hh) * p.Q * 64 + 2 * lane;
+                // all loads first (q, then every K and V row of the window), then arithmetic
+                const float2 qv = __ldcg(reinterpret_cast<const float2*>(p.x + (size_t)b * p.x_stride + hh * 64 +
+                                                                        2 * lane));
+                uint32_t kr[16], vr[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    kr[i] = vr[i] = 0u;
+                    if (i < nk) {
+                        kr[i] = __ldcg(reinterpret_cast<const unsigned int*>(p.dkc + hb + (size_t)(lo + i) * 64));
+                        vr[i] = __ldcg(reinterpret_cast<const unsigned int*>(p.dvc + hb + (size_t)(lo + i) * 64));
+                    }
+                }
+                float sc[16];
+                float m = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    sc[i] = -INFINITY;
+                    if (i < nk) {
+                        const float d = warp_sum(qv.x * bf16lo(kr[i]) + qv.y * bf16hi(kr[i])) * p.dep_scale_log2;
+                        sc[i] = d;
+                        m = fmaxf(m, d);
+                    }
+                }
+                float l = 0.f, o0 = 0.f, o1 = 0.f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    if (i < nk) {
+                        const float e = exp2f(sc[i] - m);
+                        l += e;
+                        o0 = fmaf(e, bf16lo(vr[i]), o0);
+                        o1 = fmaf(e, bf16hi(vr[i]), o1);
+                    }
+                }
+                xs[hh * 64 + 2 * lane] = o0 / l;
+                xs[hh * 64 + 2 * lane + 1] = o1 / l;
+            }
+            consumer_bar(32 * W);
+            xb = xs + (size_t)pp * kslice;
+        }
 #pragma unroll
         for (int ci = 0; ci < CH; ++ci) {
             const float4* src = reinterpret_cast<const float4*>(xb + 8 * (lane + 32 * ci));
@@ -382,7 +429,8 @@ cudaError_t prepare_t() {
     X(PRO_PLAIN, E_EMB_ADD, U_ROW)               \
     X(PRO_RMSNORM, E_DEP_QKV, U_ROW)             \
     X(PRO_PLAIN, E_DEP_HEAD, U_ROW)              \
-    X(PRO_PLAIN, E_STORE, U_ROW)
+    X(PRO_PLAIN, E_STORE, U_ROW)                 \
+    X(PRO_DEPATTN, E_RESIDUAL, U_ROW)
 
 }  // namespace
 
@@ -407,6 +455,7 @@ bool plan_gemv(GemvParams& p, int rpu, int num_sms) {
     p.grid_per_b = p.n_units < ctas ? p.n_units : ctas;
     p.units_cta_max = (p.n_units + p.grid_per_b - 1) / p.grid_per_b;
     p.smem = (size_t)nst * p.stage_bytes + 16u * (size_t)nst + (size_t)p.units_cta_max * rpu * p.P * 4u + 32u * 4u;
+    if (p.x_in_smem) p.smem += 4u * (size_t)K + 16u;  // the input vector built by the prologue
     if (p.smem > 220u * 1024u) return false;
     return true;
 }

@@ -65,7 +65,7 @@ struct pm_ctx {
     float* ss = nullptr;               // [D/128][npad_max]
     float* tc_part = nullptr;
     uint32_t* tc_count = nullptr;
-    float *dz = nullptr, *dq = nullptr, *dout = nullptr, *ds = nullptr;
+    float *dz = nullptr, *dq = nullptr, *ds = nullptr;
     uint16_t* dkv = nullptr;
     // staging
     Staging slots[kStagingSlots];
@@ -532,34 +532,27 @@ static pm_status record_depformer(pm_ctx* c, int B, cudaStream_t s) {
             ps = plan(c, p, 1, "depformer in_proj");
             if (ps) return ps;
             PM_CUDA(launch_gemv(PRO_RMSNORM, E_DEP_QKV, U_ROW, p, s, true));
-            DepAttnParams ap;
-            memset(&ap, 0, sizeof ap);
-            ap.q = c->dq;
-            ap.kc = dkc;
-            ap.vc = dvc;
-            ap.o = c->dout;
-            ap.st = c->st;
-            ap.B = B;
-            ap.Hd = f.dep_H;
-            ap.dhd = f.dep_dh;
-            ap.Q = Q;
-            ap.q_pos = q;
-            ap.dep_ctx = f.dep_ctx;
-            ap.Dd = Dd;
-            ap.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dep_dh));
-            PM_CUDA(launch_dep_attn(ap, s, true));
+            // W_o + residual, with the depth attention computed in its prologue
             p = base_params(c);
             p.W = c->d_o[j] + (size_t)q * Dd * Dd;
             p.K = Dd;
             p.n_units = Dd;
             p.B = B;
-            p.x = c->dout;
+            p.x = c->dq;
             p.x_stride = Dd;
             p.y = c->dz;
             p.y_stride = Dd;
+            p.H = f.dep_H;
+            p.Q = Q;
+            p.q = q;
+            p.dkc = dkc;
+            p.dvc = dvc;
+            p.dep_ctx = f.dep_ctx;
+            p.dep_scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dep_dh));
+            p.x_in_smem = 1;
             ps = plan(c, p, 1, "depformer out_proj");
             if (ps) return ps;
-            PM_CUDA(launch_gemv(PRO_PLAIN, E_RESIDUAL, U_ROW, p, s, true));
+            PM_CUDA(launch_gemv(PRO_DEPATTN, E_RESIDUAL, U_ROW, p, s, true));
             p = base_params(c);
             p.W = c->d_lin_in[(size_t)j * Q + q];
             p.K = Dd;
@@ -772,7 +765,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     };
     void* p_pos; void* p_first; void* p_ring; void* p_sel; void* p_amax; void* p_hc; void* p_status;
     void* p_damax; void* p_dcount; void* p_dcodes; void* p_dtok; void* p_dsup;
-    void* p_io; void* p_dio; void *p_x, *p_q, *p_o, *p_s, *p_h, *p_part, *p_cnt, *p_freq, *p_dz, *p_dq, *p_dout,
+    void* p_io; void* p_dio; void *p_x, *p_q, *p_o, *p_s, *p_h, *p_part, *p_cnt, *p_freq, *p_dz, *p_dq,
         *p_ds, *p_dkv, *p_rtab, *p_xb, *p_ob, *p_sb, *p_ss, *p_tcp, *p_tcc;
     // tensor-core path scratch, sized from the plans of this configuration's projections
     const int NP = BM >= 2 ? (BM <= 16 ? 16 : (BM <= 32 ? 32 : 64)) : 16;
@@ -808,7 +801,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
         {&p_freq, 8u * (f.dh / 2)}, {&p_rtab, 8u * BM * (f.dh / 2)},
         {&p_xb, 2u * NP * f.D}, {&p_ob, 2u * NP * f.D}, {&p_sb, 2u * NP * f.ffn}, {&p_ss, 4u * (f.D / 128) * NP},
         {&p_tcp, 4u * tc_part_floats}, {&p_tcc, 4u * (size_t)tc_count_max},
-        {&p_dz, 4u * BM * (Dd ? Dd : 1)}, {&p_dq, 4u * BM * (Dd ? Dd : 1)}, {&p_dout, 4u * BM * (Dd ? Dd : 1)},
+        {&p_dz, 4u * BM * (Dd ? Dd : 1)}, {&p_dq, 4u * BM * (Dd ? Dd : 1)},
         {&p_ds, 4u * BM * (Fd ? Fd : 1)},
         {&p_dkv, c->has_dep ? 2u * 2u * f.dep_layers * BM * f.dep_H * Q * f.dep_dh : 16u},
     };
@@ -858,7 +851,6 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     c->tc_count = (uint32_t*)p_tcc;
     c->dz = (float*)p_dz;
     c->dq = (float*)p_dq;
-    c->dout = (float*)p_dout;
     c->ds = (float*)p_ds;
     c->dkv = (uint16_t*)p_dkv;
 

@@ -18,7 +18,11 @@ namespace pm {
 // weight-streaming GEMV  y = W x  (bf16 W [rows][K], fp32 x), B = 1 row of x per CTA
 // ----------------------------------------------------------------------------------
 enum Unit { U_ROW = 0, U_PAIR_ADJ = 1, U_PAIR_SPLIT = 2 };
-enum Prologue { PRO_PLAIN = 0, PRO_RMSNORM = 1 };
+enum Prologue {
+    PRO_PLAIN = 0,    // x as given
+    PRO_RMSNORM = 1,  // x normalised (fp32 RMSNorm, learned scale)
+    PRO_DEPATTN = 2   // x = depth attention output, computed by every CTA from q and the depth cache
+};
 enum Epilogue {
     E_STORE = 0,      // y[row] = dot
     E_RESIDUAL = 1,   // y[row] += dot
@@ -64,8 +68,11 @@ struct GemvParams {
     int Q;                 // depth positions per frame
     const uint16_t* emb;   // E_EMB_ADD table [rows_emb][y dim]
     int emb_rows;
-    uint16_t* dkc;         // E_DEP_QKV: depth K cache of this layer [B_max][Hd][Q][dhd]
+    uint16_t* dkc;         // E_DEP_QKV / PRO_DEPATTN: depth K cache of this layer [B_max][Hd][Q][dhd]
     uint16_t* dvc;
+    int dep_ctx;           // PRO_DEPATTN: attention window (x = q of depth position q)
+    int x_in_smem;         // plan input: the prologue builds x in shared memory (PRO_DEPATTN)
+    float dep_scale_log2;
     int n_streams;
 };
 
@@ -135,16 +142,7 @@ struct DepBeginParams {
 };
 cudaError_t launch_dep_begin(const DepBeginParams& p, cudaStream_t s, bool pdl);
 
-struct DepAttnParams {
-    const float* q;        // [B][Dd]
-    const uint16_t* kc;    // depth K cache of this layer [B_max][Hd][Q][dhd]
-    const uint16_t* vc;
-    float* o;              // [B][Dd]
-    DevState st;
-    int B, Hd, dhd, Q, q_pos, dep_ctx, Dd;
-    float scale_log2;
-};
-cudaError_t launch_dep_attn(const DepAttnParams& p, cudaStream_t s, bool pdl);
+
 
 // ----------------------------------------------------------------------------------
 // batched projections on the tensor cores (tcgen05, accumulators in TMEM), B >= 2
