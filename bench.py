@@ -347,6 +347,34 @@ def main():
         extras["B8_steps_per_s"] = steps8
         extras["B8_stream_frames_per_s"] = steps8 * B8
         ctx8.close()
+        del kv8
+        torch.cuda.empty_cache()
+        # batched serving with ragged histories: 16 streams, cache lengths uniform 64..3000
+        # (positions set directly; attention cost does not depend on the cached values)
+        B16 = 16
+        cfg16 = pm.make_config(s.asdict(), B16, False)
+        kv16 = pm.alloc_kv_cache(cfg16)
+        ctx16 = pm.Context(s.asdict(), W, kv16, B_max=B16, depformer=False, stream=stream.cuda_stream)
+        L16 = I.make_cache_lengths(B16, 64, s.ctx, seed=3000)
+        ctx16.set_positions([int(v) for v in L16])
+        ids16 = torch.from_numpy(I.make_ids(s, 80, B=B16, seed=2200)).to(dev)
+        lg16 = torch.empty((B16, s.text_out), dtype=torch.float32, device=dev)
+        for t in range(8):
+            ctx16.frame_step(B16, ids16[t], lg16, None, None)
+        torch.cuda.synchronize()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for t in range(64):
+            ctx16.frame_step(B16, ids16[8 + t], lg16, None, None)
+        b_.record(stream)
+        torch.cuda.synchronize()
+        steps16 = 64 / (a.elapsed_time(b_) / 1000.0)
+        mean_keys16 = float(np.mean([min(int(v) + 8 + 32, s.ctx) for v in L16]))
+        bytes16 = FRAME_FIXED_BYTES + KV_BYTES_PER_POS * (mean_keys16 + 1) * B16
+        extras["B16_ragged_steps_per_s"] = steps16
+        extras["B16_ragged_stream_frames_per_s"] = steps16 * B16
+        extras["B16_ragged_gbs"] = bytes16 * steps16 / 1e9
+        ctx16.close()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and BB == 1:
