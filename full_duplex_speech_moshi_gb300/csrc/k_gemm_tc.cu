@@ -264,9 +264,21 @@ __global__ void __launch_bounds__(192, 1)
                     __threadfence();
 #pragma unroll
                     for (int b = 0; b < NPAD; ++b) v[b] = 0.f;
-                    for (int sidx = 0; sidx < nseg; ++sidx)
+                    // partials summed in slot order; MSEG slots' loads are issued before any add
+                    constexpr int MSEG = NPAD <= 16 ? 4 : (NPAD <= 32 ? 2 : 1);
+                    for (int s0 = 0; s0 < nseg; s0 += MSEG) {
+                        float tmp[MSEG][NPAD];
 #pragma unroll
-                        for (int b = 0; b < NPAD; ++b) v[b] += __ldcg(pm_ + ((size_t)sidx * NPAD + b) * 128 + t);
+                        for (int j = 0; j < MSEG; ++j)
+#pragma unroll
+                            for (int b = 0; b < NPAD; ++b)
+                                tmp[j][b] = (s0 + j < nseg) ? __ldcg(pm_ + ((size_t)(s0 + j) * NPAD + b) * 128 + t) : 0.f;
+#pragma unroll
+                        for (int j = 0; j < MSEG; ++j)
+                            if (s0 + j < nseg)
+#pragma unroll
+                                for (int b = 0; b < NPAD; ++b) v[b] += tmp[j][b];
+                    }
                     if (t == 0) p.count[m] = 0u;
                 }
                 // v[b] is the full dot product of row (tile m, lane t) with input row b
@@ -284,11 +296,23 @@ __global__ void __launch_bounds__(192, 1)
                     for (int b = 0; b < NPAD; ++b) ss[b] = 0.f;
                     if (!aborted) {
                         const float an = p.alpha_next ? __uint_as_float((uint32_t)p.alpha_next[r] << 16) : 1.0f;
-                        for (int b = 0; b < p.B; ++b) {
-                            const float xo = p.y[(size_t)b * p.y_stride + r] + v[b];
-                            p.y[(size_t)b * p.y_stride + r] = xo;
-                            if (p.yb) p.yb[(size_t)b * p.yb_stride + r] = f32_to_bf16_rne(xo * an);
-                            ss[b] = xo * xo;
+#pragma unroll
+                        for (int b0 = 0; b0 < NPAD; b0 += 16) {
+                            if (b0 >= p.B) break;
+                            float xr[16];  // 16 residual rows loaded before the first store
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                xr[j] = (b0 + j < p.B) ? p.y[(size_t)(b0 + j) * p.y_stride + r] : 0.f;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int b = b0 + j;
+                                if (b < p.B) {
+                                    const float xo = xr[j] + v[b];
+                                    p.y[(size_t)b * p.y_stride + r] = xo;
+                                    if (p.yb) p.yb[(size_t)b * p.yb_stride + r] = f32_to_bf16_rne(xo * an);
+                                    ss[b] = xo * xo;
+                                }
+                            }
                         }
                     }
 #pragma unroll
@@ -321,21 +345,34 @@ __global__ void __launch_bounds__(192, 1)
                     const int idx = r - sec * p.D;
                     const int h = idx / p.dh, d = idx % p.dh;
                     const bool even = (t & 1) == 0;
-                    for (int b = 0; b < p.B; ++b) {
-                        const float mine = v[b];
-                        const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-                        float o = mine;
-                        if (sec < 2) {
-                            const float2 cs = p.rope_tab[(size_t)b * (p.dh / 2) + (d >> 1)];
-                            o = even ? (mine * cs.x - other * cs.y) : (other * cs.y + mine * cs.x);
+#pragma unroll
+                    for (int b0 = 0; b0 < NPAD; b0 += 16) {
+                        if (b0 >= p.B) break;
+                        // rotation factors and ring slots of 16 streams, loaded before the first store
+                        float2 cs[16];
+                        int slot[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int b = b0 + j;
+                            cs[j] = (sec < 2 && b < p.B) ? p.rope_tab[(size_t)b * (p.dh / 2) + (d >> 1)]
+                                                         : make_float2(1.f, 0.f);
+                            slot[j] = (sec > 0 && b < p.B) ? p.st.pos[b] % p.ctx : 0;
                         }
-                        if (aborted) continue;
-                        if (sec == 0) {
-                            p.y[(size_t)b * p.y_stride + idx] = o;
-                        } else {
-                            const int slot = p.st.pos[b] % p.ctx;
-                            uint16_t* cache = (sec == 1) ? p.kc : p.vc;
-                            cache[(((size_t)b * p.H + h) * p.ctx + slot) * p.dh + d] = f32_to_bf16_rne(o);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int b = b0 + j;
+                            if (b >= p.B) break;
+                            const float mine = v[b];
+                            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+                            float o = mine;
+                            if (sec < 2) o = even ? (mine * cs[j].x - other * cs[j].y) : (other * cs[j].y + mine * cs[j].x);
+                            if (aborted) continue;
+                            if (sec == 0) {
+                                p.y[(size_t)b * p.y_stride + idx] = o;
+                            } else {
+                                uint16_t* cache = (sec == 1) ? p.kc : p.vc;
+                                cache[(((size_t)b * p.H + h) * p.ctx + slot[j]) * p.dh + d] = f32_to_bf16_rne(o);
+                            }
                         }
                     }
                 } else if (EPI == TE_HEAD) {
