@@ -11,7 +11,8 @@
 //    counter, no waiting);
 //  * warp 4 streams A (weights, 2-D TMA, 128-byte swizzle, L2 evict-first) and B (the
 //    bf16 activations, L2 evict-last: every CTA reads them) through a ring of stages;
-//    the A copies of the first ring are issued before griddepcontrol.wait;
+//    the A copies of the first ring are issued before griddepcontrol.wait, and once its
+//    own copies are out it prefetches the head of the next projection's weights to L2;
 //  * warp 5 owns the tensor memory and issues tcgen05.mma (4 x K=16 per stage), freeing
 //    each stage with tcgen05.commit; two accumulator buffers let the epilogue of one
 //    tile overlap the MMAs of the next;
@@ -56,9 +57,29 @@ __host__ __device__ __forceinline__ int cta_of(long long u, long long U, int G) 
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
+// L2 prefetch of the first units (tile boxes) that CTA c of the next tensor-core
+// projection streams, through that projection's tensor map
+__device__ __forceinline__ void prefetch_next_tc(const CUtensorMap* tmN, const NextPrefetch& nx, int c) {
+    const long long U = (long long)nx.n_mtiles * nx.nk;
+    const long long u0 = unit_begin(c, U, nx.grid), u1 = unit_begin(c + 1, U, nx.grid);
+    long long n = (long long)(nx.bytes / A_BYTES);
+    if (n > u1 - u0) n = u1 - u0;
+    for (long long i = 0; i < n; ++i) {
+        const long long u = u0 + i;
+        const int m = (int)(u / nx.nk), kt = (int)(u % nx.nk);
+        if (nx.split_rows) {
+            tma_prefetch_2d(tmN, kt * KT, m * 64);
+            tma_prefetch_2d(tmN, kt * KT, nx.split_rows + m * 64);
+        } else {
+            tma_prefetch_2d(tmN, kt * KT, m * 128);
+        }
+    }
+}
+
 template <int EPI, int NPAD>
 __global__ void __launch_bounds__(192, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmN, const TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     constexpr uint32_t B_BYTES = NPAD * 128u;
@@ -153,6 +174,7 @@ __global__ void __launch_bounds__(192, 1)
                 load_b(i);
                 flags[2] = i + 1;
             }
+            if (p.nx.n_mtiles > 0 && c < p.nx.grid) prefetch_next_tc(&tmN, p.nx, c);
         }
     } else if (warp == 5) {
         // ------------------------------ MMA issuer ------------------------------
@@ -432,7 +454,8 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 template <int EPI, int NPAD>
-cudaError_t launch_t(const CUtensorMap& A, const CUtensorMap& Bop, const TcParams& p, cudaStream_t s, bool pdl) {
+cudaError_t launch_t(const CUtensorMap& A, const CUtensorMap& Bop, const CUtensorMap& N, const TcParams& p,
+                     cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3(192);
@@ -443,17 +466,18 @@ cudaError_t launch_t(const CUtensorMap& A, const CUtensorMap& Bop, const TcParam
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, k_gemm_tc<EPI, NPAD>, A, Bop, p);
+    return cudaLaunchKernelEx(&cfg, k_gemm_tc<EPI, NPAD>, A, Bop, N, p);
 }
 
 template <int NPAD>
-cudaError_t launch_n(const CUtensorMap& A, const CUtensorMap& Bop, const TcParams& p, cudaStream_t s, bool pdl) {
+cudaError_t launch_n(const CUtensorMap& A, const CUtensorMap& Bop, const CUtensorMap& N, const TcParams& p,
+                     cudaStream_t s, bool pdl) {
     switch (p.epi) {
-        case TE_STORE: return launch_t<TE_STORE, NPAD>(A, Bop, p, s, pdl);
-        case TE_RESIDUAL: return launch_t<TE_RESIDUAL, NPAD>(A, Bop, p, s, pdl);
-        case TE_SWIGLU: return launch_t<TE_SWIGLU, NPAD>(A, Bop, p, s, pdl);
-        case TE_QKV_ROPE: return launch_t<TE_QKV_ROPE, NPAD>(A, Bop, p, s, pdl);
-        case TE_HEAD: return launch_t<TE_HEAD, NPAD>(A, Bop, p, s, pdl);
+        case TE_STORE: return launch_t<TE_STORE, NPAD>(A, Bop, N, p, s, pdl);
+        case TE_RESIDUAL: return launch_t<TE_RESIDUAL, NPAD>(A, Bop, N, p, s, pdl);
+        case TE_SWIGLU: return launch_t<TE_SWIGLU, NPAD>(A, Bop, N, p, s, pdl);
+        case TE_QKV_ROPE: return launch_t<TE_QKV_ROPE, NPAD>(A, Bop, N, p, s, pdl);
+        case TE_HEAD: return launch_t<TE_HEAD, NPAD>(A, Bop, N, p, s, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -499,11 +523,12 @@ bool plan_tc(TcParams& p, int num_sms) {
     return p.smem <= 220u * 1024u;
 }
 
-cudaError_t launch_tc(const CUtensorMap& A, const CUtensorMap& Bop, const TcParams& p, cudaStream_t s, bool pdl) {
+cudaError_t launch_tc(const CUtensorMap& A, const CUtensorMap& Bop, const CUtensorMap& next, const TcParams& p,
+                      cudaStream_t s, bool pdl) {
     switch (p.npad) {
-        case 16: return launch_n<16>(A, Bop, p, s, pdl);
-        case 32: return launch_n<32>(A, Bop, p, s, pdl);
-        case 64: return launch_n<64>(A, Bop, p, s, pdl);
+        case 16: return launch_n<16>(A, Bop, next, p, s, pdl);
+        case 32: return launch_n<32>(A, Bop, next, p, s, pdl);
+        case 64: return launch_n<64>(A, Bop, next, p, s, pdl);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -180,6 +180,30 @@ static pm_status plan(pm_ctx* c, GemvParams& p, int rpu, const char* what) {
     return PM_OK;
 }
 
+// Bytes per CTA of the next projection's weights that a tensor-core projection prefetches
+// into L2 after issuing its own copies (tuning constant; 0 disables).
+#ifndef PM_PF_TC_BYTES
+#define PM_PF_TC_BYTES 262144u
+#endif
+
+static NextPrefetch next_tc(pm_ctx* c, int K, int n_mtiles, int split_rows, int npad) {
+    NextPrefetch nx;
+    memset(&nx, 0, sizeof nx);
+    TcParams t;
+    memset(&t, 0, sizeof t);
+    t.K = K;
+    t.n_mtiles = n_mtiles;
+    t.npad = npad;
+    t.B = 1;
+    if (PM_PF_TC_BYTES == 0u || !plan_tc(t, c->num_sms)) return nx;
+    nx.n_mtiles = n_mtiles;
+    nx.nk = t.nk;
+    nx.grid = t.grid;
+    nx.split_rows = split_rows;
+    nx.bytes = PM_PF_TC_BYTES;
+    return nx;
+}
+
 typedef pm_status (*record_fn)(pm_ctx*, int, cudaStream_t);
 
 // profiling mark: an event after the launch just issued (only inside pm_profile_frame)
@@ -390,21 +414,29 @@ static pm_status record_frame_tc(pm_ctx* c, int B, cudaStream_t s) {
         p.D = D;
         return p;
     };
-    auto go = [&](const CUtensorMap& A, const CUtensorMap& X, TcParams& p, int kind, const char* what) -> pm_status {
+    auto go = [&](const CUtensorMap& A, const CUtensorMap& X, const CUtensorMap& N, TcParams& p, int kind,
+                  const char* what) -> pm_status {
         if (!plan_tc(p, c->num_sms)) return fail(c, PM_ERR_UNSUPPORTED, std::string("no tensor-core plan for ") + what);
         if ((size_t)p.n_mtiles * p.maxseg * p.npad * 128 > c->tc_part_floats || p.n_mtiles > c->tc_count_max)
             return fail(c, PM_ERR_UNSUPPORTED, std::string("tensor-core scratch too small for ") + what);
-        PM_CUDA(launch_tc(A, X, p, s, pdl));
+        PM_CUDA(launch_tc(A, X, N, p, s, pdl));
         return mark(c, s, kind);
     };
+    // weight tensor maps of every projection (each kernel also prefetches the next one's head)
+    std::vector<CUtensorMap> mq(f.n_layers), mwo(f.n_layers), mwi(f.n_layers), mwt(f.n_layers);
+    for (int l = 0; l < f.n_layers; ++l)
+        if (!make_tmap_bf16(&mq[l], c->in_proj[l], D, 3 * D, 128) ||
+            !make_tmap_bf16(&mwo[l], c->out_proj[l], D, D, 128) ||
+            !make_tmap_bf16(&mwi[l], c->lin_in[l], D, 2 * F, 64) || !make_tmap_bf16(&mwt[l], c->lin_out[l], F, D, 128))
+            return fail(c, PM_ERR_CUDA, "tensor map encoding failed (weights)");
+    CUtensorMap mh;
+    if (!make_tmap_bf16(&mh, c->text_linear, D, f.text_out, 128))
+        return fail(c, PM_ERR_CUDA, "tensor map encoding failed (text head)");
+    const int head_tiles = (f.text_out + 127) / 128;
     const size_t layer_elems = (size_t)f.B_max * f.H * f.ctx * f.dh;
     for (int l = 0; l < f.n_layers; ++l) {
         uint16_t* kc = c->kv + (size_t)(2 * l + 0) * layer_elems;
         uint16_t* vc = c->kv + (size_t)(2 * l + 1) * layer_elems;
-        CUtensorMap mq, mwo, mwi, mwt;
-        if (!make_tmap_bf16(&mq, c->in_proj[l], D, 3 * D, 128) || !make_tmap_bf16(&mwo, c->out_proj[l], D, D, 128) ||
-            !make_tmap_bf16(&mwi, c->lin_in[l], D, 2 * F, 64) || !make_tmap_bf16(&mwt, c->lin_out[l], F, D, 128))
-            return fail(c, PM_ERR_CUDA, "tensor map encoding failed (weights)");
         // RMSNorm1 (folded) + fused QKV + RoPE + KV append
         TcParams p = base(TE_QKV_ROPE, D, 3 * D / 128, 3 * D);
         p.ss_in = c->ss;
@@ -417,7 +449,8 @@ static pm_status record_frame_tc(pm_ctx* c, int B, cudaStream_t s) {
         p.kc = kc;
         p.vc = vc;
         p.rope_tab = c->rope_tab;
-        pm_status ps = go(mq, mx, p, PM_KERNEL_QKV, "in_proj");
+        p.nx = next_tc(c, D, D / 128, 0, npad);
+        pm_status ps = go(mq[l], mx, mwo[l], p, PM_KERNEL_QKV, "in_proj");
         if (ps) return ps;
         AttnParams ap;
         memset(&ap, 0, sizeof ap);
@@ -446,7 +479,8 @@ static pm_status record_frame_tc(pm_ctx* c, int B, cudaStream_t s) {
         p.yb_stride = D;
         p.alpha_next = c->norm2[l];
         p.ss_out = c->ss;
-        if ((ps = go(mwo, mo, p, PM_KERNEL_OUT_PROJ, "out_proj"))) return ps;
+        p.nx = next_tc(c, D, F / 64, F, npad);
+        if ((ps = go(mwo[l], mo, mwi[l], p, PM_KERNEL_OUT_PROJ, "out_proj"))) return ps;
         // RMSNorm2 (folded) + linear_in + SwiGLU -> bf16 s
         p = base(TE_SWIGLU, D, F / 64, F);
         p.ss_in = c->ss;
@@ -454,7 +488,8 @@ static pm_status record_frame_tc(pm_ctx* c, int B, cudaStream_t s) {
         p.split_rows = F;
         p.yb = c->sb;
         p.yb_stride = F;
-        if ((ps = go(mwi, mx, p, PM_KERNEL_LINEAR_IN, "linear_in"))) return ps;
+        p.nx = next_tc(c, F, D / 128, 0, npad);
+        if ((ps = go(mwi[l], mx, mwt[l], p, PM_KERNEL_LINEAR_IN, "linear_in"))) return ps;
         // linear_out + residual; emits the next norm's operand
         p = base(TE_RESIDUAL, F, D / 128, D);
         p.y = c->x;
@@ -463,18 +498,18 @@ static pm_status record_frame_tc(pm_ctx* c, int B, cudaStream_t s) {
         p.yb_stride = D;
         p.alpha_next = (l + 1 < f.n_layers) ? c->norm1[l + 1] : c->out_norm;
         p.ss_out = c->ss;
-        if ((ps = go(mwt, msb, p, PM_KERNEL_LINEAR_OUT, "linear_out"))) return ps;
+        const bool last = l + 1 == f.n_layers;
+        p.nx = last ? next_tc(c, D, head_tiles, 0, npad) : next_tc(c, D, 3 * D / 128, 0, npad);
+        if ((ps = go(mwt[l], msb, last ? mh : mq[l + 1], p, PM_KERNEL_LINEAR_OUT, "linear_out"))) return ps;
     }
-    CUtensorMap mh;
-    if (!make_tmap_bf16(&mh, c->text_linear, D, f.text_out, 128))
-        return fail(c, PM_ERR_CUDA, "tensor map encoding failed (text head)");
-    TcParams p = base(TE_HEAD, D, (f.text_out + 127) / 128, f.text_out);
+    TcParams p = base(TE_HEAD, D, head_tiles, f.text_out);
     p.ss_in = c->ss;
     p.ss_parts = D / 128;
     p.h_internal = c->h;
     p.x_resid = c->x;
     p.alpha = c->out_norm;
-    return go(mh, mx, p, PM_KERNEL_HEAD, "text_linear");
+    p.nx = next_tc(c, D, 3 * D / 128, 0, npad);  // the next frame's first projection
+    return go(mh, mx, mq[0], p, PM_KERNEL_HEAD, "text_linear");
 }
 
 static pm_status record_depformer(pm_ctx* c, int B, cudaStream_t s) {

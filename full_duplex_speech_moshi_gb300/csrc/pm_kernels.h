@@ -155,6 +155,18 @@ enum TcEpilogue {
     TE_HEAD = 4       // text head logits + greedy token, frame finalisation, hidden state
 };
 
+// The head of the next projection's weights, fetched into L2 by this kernel's producer
+// once its own copies are issued: while this kernel drains (last stages, split-K merges,
+// epilogue), HBM already serves the first tiles that the next projection's CTA with the
+// same index will stream, so that kernel's first loads hit L2.
+struct NextPrefetch {
+    int n_mtiles;          // next projection's 128-row tiles (0 = nothing to prefetch)
+    int nk;                // its 64-element k tiles per row
+    int grid;              // its CTAs
+    int split_rows;        // TE_SWIGLU: value rows start here (two 64-row boxes per unit), else 0
+    uint32_t bytes;        // bytes per CTA to prefetch
+};
+
 struct TcParams {
     int epi;
     int K, nk;               // row length, 64-element k tiles
@@ -192,10 +204,13 @@ struct TcParams {
     float* h_internal;       // [B][D] hidden state
     const float* x_resid;    // [B][D] residual before the final norm
     const uint16_t* alpha;   // final norm scale [D]
+    NextPrefetch nx;         // read through the `next` tensor map
 };
 
 bool plan_tc(TcParams& p, int num_sms);
-cudaError_t launch_tc(const CUtensorMap& A, const CUtensorMap& Bop, const TcParams& p, cudaStream_t s, bool pdl);
+// `next`: tensor map of the next projection's weights (read when p.nx.n_mtiles > 0)
+cudaError_t launch_tc(const CUtensorMap& A, const CUtensorMap& Bop, const CUtensorMap& next, const TcParams& p,
+                      cudaStream_t s, bool pdl);
 cudaError_t tc_prepare();
 // 2-D bf16 tensor map, 128-byte swizzle, box {64, box_rows}; false if the driver refuses it
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows);

@@ -93,6 +93,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// L2 prefetch of the box at (x0, x1) of a 2-D tensor map (x0 128-byte aligned)
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x0, int x1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x0), "r"(x1)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_evict_last_policy() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
