@@ -32,6 +32,10 @@ class orc_config(C.Structure):
                                "dep_card", "dep_text_in", "dep_audio_in")]
 
 
+class orc_sampling(C.Structure):
+    _fields_ = [("temperature", C.c_double), ("top_k", C.c_int), ("seed", C.c_uint64)]
+
+
 def build(force: bool = False) -> str:
     """Compile the oracle to a shared library (plain C11, -O2, OpenMP)."""
     newest = max(os.path.getmtime(p) for p in _SRC + [_HDR])
@@ -85,6 +89,15 @@ def lib():
             L.orc_full_sequence.argtypes = [C.c_void_p, i, i32p, dp, dp, i32p]
             L.orc_depformer_step.restype = i
             L.orc_depformer_step.argtypes = [C.c_void_p, dp, C.c_int32, i32p, dp, i32p]
+            u64p = C.POINTER(C.c_uint64)
+            L.orc_philox4x64.argtypes = [u64p, u64p, u64p]
+            L.orc_uniform24.restype = d
+            L.orc_uniform24.argtypes = [C.c_uint64, C.c_uint64, C.c_uint64, C.c_uint64]
+            L.orc_sample_topk.restype = i
+            L.orc_sample_topk.argtypes = [dp, i, d, i, C.c_uint64, C.c_uint64, C.c_uint64, C.c_uint64, dp, dp]
+            L.orc_depformer_step_sampled.restype = i
+            L.orc_depformer_step_sampled.argtypes = [C.c_void_p, dp, C.c_int32, i32p, C.POINTER(orc_sampling),
+                                                     C.c_uint64, C.c_uint64, dp, i32p, dp]
             _lib = L
     return _lib
 
@@ -169,6 +182,21 @@ class Oracle:
         if rc != ORC_OK:
             raise ValueError(f"orc_depformer_step rc={rc}")
         return lg, codes
+
+    def depformer_step_sampled(self, hidden: np.ndarray, text_tok: int, supplied: np.ndarray, temperature: float,
+                               top_k: int, seed: int, pos: int, row: int):
+        """Codes sampled where none is supplied; returns logits, codes and pick margins."""
+        Q, V = self.shape["dep_steps"], self.shape["dep_card"]
+        lg = np.zeros((Q, V), np.float64)
+        codes = np.zeros(Q, np.int32)
+        margins = np.zeros(Q, np.float64)
+        smp = orc_sampling(float(temperature), int(top_k), int(seed) & (2**64 - 1))
+        rc = self.L.orc_depformer_step_sampled(self.h, _dp(np.ascontiguousarray(hidden, np.float64)), int(text_tok),
+                                               _i32p(np.ascontiguousarray(supplied, np.int32)), C.byref(smp),
+                                               int(pos), int(row), _dp(lg), _i32p(codes), _dp(margins))
+        if rc != ORC_OK:
+            raise ValueError(f"orc_depformer_step_sampled rc={rc}")
+        return lg, codes, margins
 
 
 class OracleStream:
@@ -261,3 +289,28 @@ def attend(q: np.ndarray, keys: np.ndarray, vals: np.ndarray) -> np.ndarray:
 def argmax(v: np.ndarray) -> int:
     v = np.ascontiguousarray(v, np.float64)
     return int(lib().orc_argmax(_dp(v), v.size))
+
+
+# --- sampling ----------------------------------------------------------------
+
+def philox4x64(counter, key) -> list:
+    """Philox4x64-10 block of a 4-word counter under a 2-word key."""
+    ctr = (C.c_uint64 * 4)(*[int(v) & (2**64 - 1) for v in counter])
+    k = (C.c_uint64 * 2)(*[int(v) & (2**64 - 1) for v in key])
+    out = (C.c_uint64 * 4)()
+    lib().orc_philox4x64(ctr, k, out)
+    return [int(v) for v in out]
+
+
+def uniform24(seed: int, c0: int, c1: int, c2: int) -> float:
+    return float(lib().orc_uniform24(int(seed) & (2**64 - 1), int(c0), int(c1), int(c2)))
+
+
+def sample_topk(logits: np.ndarray, temperature: float, top_k: int, seed: int, c0: int, c1: int, c2: int):
+    """Returns (token, margin, cut_gap) of temperature / top-k sampling of one row."""
+    lg = np.ascontiguousarray(logits, np.float64)
+    mg = C.c_double()
+    gap = C.c_double()
+    tok = lib().orc_sample_topk(_dp(lg), lg.size, float(temperature), int(top_k), int(seed) & (2**64 - 1), int(c0),
+                                int(c1), int(c2), C.byref(mg), C.byref(gap))
+    return int(tok), float(mg.value), float(gap.value)

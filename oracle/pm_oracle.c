@@ -28,6 +28,17 @@
  *     position p-d; positions before the first frame since reset or position set read
  *     the initial ID of that stream.
  *
+ * Sampling (same page, section 7: the generator samples the text token and each depth
+ * position's code, released defaults text temperature 0.7 / top-k 25, audio 0.8 / 250):
+ *   - the page names temperature and top-k and nothing finer; the reading taken: keep the
+ *     k largest logits (ties at the cut to the lower index), weights exp((l - l_max) / T)
+ *     over those, and the first candidate, in descending-logit order, whose running sum
+ *     of weights exceeds u * total; T <= 0 or k <= 1 is greedy (the argmax);
+ *   - u comes from Philox4x64-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers:
+ *     as easy as 1, 2, 3", SC'11) with key (seed, 0) and counter (frame position, batch
+ *     row, substep, 0), substep 0 for the text token and 1 + q for depth position q:
+ *     u = (first output word >> 40) * 2^-24.
+ *
  * Arithmetic is float64 throughout.  Weights are bf16 bit patterns, widened exactly.
  * Nothing is blocked, fused or reordered beyond the definitions above.  Loops over
  * output rows run under OpenMP; each row's sum is a plain serial loop.
@@ -115,6 +126,95 @@ int orc_argmax(const double* v, int n) {
     for (int i = 1; i < n; ++i)
         if (v[i] > v[best]) best = i;
     return best;
+}
+
+/* ------------------------------------------------------------------------- */
+/* sampling                                                                   */
+/* ------------------------------------------------------------------------- */
+
+/* Philox4x64-10: ten rounds of the 4x64 S-box (two 64x64 -> 128-bit multiplies per
+ * round with the paper's multipliers), the key bumped by the two Weyl constants between
+ * rounds. */
+void orc_philox4x64(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]) {
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+    uint64_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint64_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += W0;
+            k1 += W1;
+        }
+        const unsigned __int128 p0 = (unsigned __int128)M0 * c0;
+        const unsigned __int128 p1 = (unsigned __int128)M1 * c2;
+        const uint64_t hi0 = (uint64_t)(p0 >> 64), lo0 = (uint64_t)p0;
+        const uint64_t hi1 = (uint64_t)(p1 >> 64), lo1 = (uint64_t)p1;
+        const uint64_t n0 = hi1 ^ c1 ^ k0, n1 = lo1, n2 = hi0 ^ c3 ^ k1, n3 = lo0;
+        c0 = n0;
+        c1 = n1;
+        c2 = n2;
+        c3 = n3;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+double orc_uniform24(uint64_t seed, uint64_t c0, uint64_t c1, uint64_t c2) {
+    const uint64_t ctr[4] = {c0, c1, c2, 0}, key[2] = {seed, 0};
+    uint64_t out[4];
+    orc_philox4x64(ctr, key, out);
+    return (double)(out[0] >> 40) * (1.0 / 16777216.0);
+}
+
+/* order for the top-k cut: larger logit first, then lower index */
+static const double* g_sort_logits;
+static int by_logit_desc(const void* a, const void* b) {
+    const int i = *(const int*)a, j = *(const int*)b;
+    const double li = g_sort_logits[i], lj = g_sort_logits[j];
+    if (li > lj) return -1;
+    if (li < lj) return 1;
+    return (i < j) ? -1 : (i > j) ? 1 : 0;
+}
+
+int orc_sample_topk(const double* logits, int V, double temperature, int top_k, uint64_t seed, uint64_t c0,
+                    uint64_t c1, uint64_t c2, double* margin, double* cut_gap) {
+    if (margin) *margin = INFINITY;
+    if (cut_gap) *cut_gap = INFINITY;
+    if (temperature <= 0.0 || top_k <= 1) return orc_argmax(logits, V);
+    const int k = top_k < V ? top_k : V;
+    int* idx = (int*)malloc(sizeof(int) * (size_t)V);
+    for (int i = 0; i < V; ++i) idx[i] = i;
+    g_sort_logits = logits;
+    qsort(idx, (size_t)V, sizeof(int), by_logit_desc);
+    if (cut_gap && k < V) *cut_gap = logits[idx[k - 1]] - logits[idx[k]];
+    double* w = (double*)malloc(sizeof(double) * (size_t)k);
+    const double lmax = logits[idx[0]];
+    double total = 0.0;
+    for (int j = 0; j < k; ++j) {
+        w[j] = exp((logits[idx[j]] - lmax) / temperature);
+        total += w[j];
+    }
+    const double target = orc_uniform24(seed, c0, c1, c2) * total;
+    int pick = k - 1;
+    double run = 0.0, below = 0.0;
+    for (int j = 0; j < k; ++j) {
+        below = run;
+        run += w[j];
+        if (run > target) {
+            pick = j;
+            break;
+        }
+    }
+    if (margin) {
+        const double d0 = target - below, d1 = run - target;
+        *margin = (d0 < d1 ? d0 : d1) / total;
+    }
+    const int token = idx[pick];
+    free(w);
+    free(idx);
+    return token;
 }
 
 /* ------------------------------------------------------------------------- */
@@ -506,6 +606,12 @@ int orc_full_sequence(const orc_model* m, int T, const int32_t* ids, double* hid
 
 int orc_depformer_step(const orc_model* m, const double* hidden, int32_t text_tok, const int32_t* supplied,
                        double* logits, int32_t* codes) {
+    return orc_depformer_step_sampled(m, hidden, text_tok, supplied, NULL, 0, 0, logits, codes, NULL);
+}
+
+int orc_depformer_step_sampled(const orc_model* m, const double* hidden, int32_t text_tok, const int32_t* supplied,
+                               const orc_sampling* smp, uint64_t pos, uint64_t row, double* logits, int32_t* codes,
+                               double* margins) {
     const orc_config* c = &m->c;
     if (c->dep_layers <= 0) return ORC_ERR_ARG;
     const int Dd = c->dep_D, Hd = c->dep_H, dd = c->dep_dh, Fd = c->dep_ffn, Q = c->dep_steps;
@@ -559,7 +665,16 @@ int orc_depformer_step(const orc_model* m, const double* hidden, int32_t text_to
         }
         double* lg = logits + (size_t)q * V;
         orc_matvec(m->dep_head[q], V, Dd, z, lg); /* no final depth norm */
-        int32_t code = supplied[q] >= 0 ? supplied[q] : orc_argmax(lg, V);
+        int32_t code;
+        double mg = INFINITY;
+        if (supplied[q] >= 0)
+            code = supplied[q];
+        else if (smp)
+            code = orc_sample_topk(lg, V, smp->temperature, smp->top_k, smp->seed, pos, row, 1u + (uint64_t)q, &mg,
+                                   NULL);
+        else
+            code = orc_argmax(lg, V);
+        if (margins) margins[q] = mg;
         codes[q] = code;
         prev = code;
     }

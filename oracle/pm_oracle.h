@@ -75,6 +75,27 @@ int orc_full_sequence(const orc_model* m, int T, const int32_t* ids, double* hid
 int orc_depformer_step(const orc_model* m, const double* hidden, int32_t text_tok, const int32_t* supplied,
                        double* logits, int32_t* codes);
 
+/* sampling: Philox4x64-10 block (counter ctr, key), the 24-bit uniform of the counter
+ * (c0, c1, c2, 0) under key (seed, 0), and temperature / top-k sampling of one row of
+ * logits with that uniform.  margin (may be NULL): distance of u * total from the nearest
+ * cumulative boundary of the pick, relative to the total; cut_gap (may be NULL): logit
+ * gap between the k-th and (k+1)-th largest (INFINITY when k >= V or greedy). */
+typedef struct {
+    double temperature;
+    int top_k;
+    uint64_t seed;
+} orc_sampling;
+void orc_philox4x64(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]);
+double orc_uniform24(uint64_t seed, uint64_t c0, uint64_t c1, uint64_t c2);
+int orc_sample_topk(const double* logits, int V, double temperature, int top_k, uint64_t seed, uint64_t c0,
+                    uint64_t c1, uint64_t c2, double* margin, double* cut_gap);
+/* Depformer with sampled codes where none is supplied (smp NULL = greedy): position q's
+ * counter is (pos, row, 1 + q).  margins [Q] (may be NULL): the pick margins (INFINITY
+ * where supplied or greedy). */
+int orc_depformer_step_sampled(const orc_model* m, const double* hidden, int32_t text_tok, const int32_t* supplied,
+                               const orc_sampling* smp, uint64_t pos, uint64_t row, double* logits, int32_t* codes,
+                               double* margins);
+
 #ifdef __cplusplus
 }
 #endif
