@@ -355,18 +355,21 @@ struct orc_stream {
     double** K;
     double** V;
     long kv_cap;
+    int n_layers;    /* so that freeing needs no model (it may be gone at teardown) */
 };
 
 orc_stream* orc_stream_new(const orc_model* m) {
     orc_stream* s = (orc_stream*)calloc(1, sizeof *s);
+    s->n_layers = m->c.n_layers;
     s->K = (double**)calloc((size_t)m->c.n_layers, sizeof(double*));
     s->V = (double**)calloc((size_t)m->c.n_layers, sizeof(double*));
     return s;
 }
 
 void orc_stream_free(const orc_model* m, orc_stream* s) {
+    (void)m;
     if (!s) return;
-    for (int l = 0; l < m->c.n_layers; ++l) { free(s->K[l]); free(s->V[l]); }
+    for (int l = 0; l < s->n_layers; ++l) { free(s->K[l]); free(s->V[l]); }
     free(s->K); free(s->V); free(s->id_hist);
     free(s);
 }
