@@ -405,6 +405,7 @@ __global__ void __launch_bounds__(192, 1)
                         unsigned long long key = 0ull;
                         if (b < p.B && r < p.n_rows) {
                             if (out && !aborted) out[(size_t)b * p.n_rows + r] = v[b];
+                            if (p.logits_copy && !aborted) p.logits_copy[(size_t)b * p.n_rows + r] = v[b];
                             key = pack_argmax(v[b], (uint32_t)r);
                         }
 #pragma unroll

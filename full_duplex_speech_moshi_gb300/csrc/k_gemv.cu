@@ -347,6 +347,7 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
                 const int row = u0 + lu;
                 const float v = rowsum(lu, 0);
                 if (out) out[row] = v;
+                if (p.logits_copy) p.logits_copy[(size_t)b * p.y_stride + row] = v;
                 best = umax64(best, pack_argmax(v, (uint32_t)row));
             }
         }

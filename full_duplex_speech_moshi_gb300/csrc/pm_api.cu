@@ -67,6 +67,12 @@ struct pm_ctx {
     uint32_t* tc_count = nullptr;
     float *dz = nullptr, *dq = nullptr, *ds = nullptr;
     uint16_t* dkv = nullptr;
+    // sampling: device-resident settings, the logits the samplers read, which kinds sample
+    SampleCfg* scfg = nullptr;
+    SampleCfg scfg_host{};
+    float* slog = nullptr;    // [B_max][text_out]
+    float* dslog = nullptr;   // [B_max][dep_card]
+    bool text_smp = false, audio_smp = false;
     // staging
     Staging slots[kStagingSlots];
     int next_slot = 0;
@@ -217,10 +223,29 @@ static pm_status mark(pm_ctx* c, cudaStream_t s, int kind) {
     return PM_OK;
 }
 
+// the drawn text token replaces the head's greedy one (when text sampling is on)
+static pm_status record_text_sample(pm_ctx* c, int B, cudaStream_t s, bool pdl) {
+    if (!c->text_smp) return PM_OK;
+    SampleParams sp;
+    memset(&sp, 0, sizeof sp);
+    sp.mode = SM_TEXT;
+    sp.logits = c->slog;
+    sp.ld = c->cfg.text_out;
+    sp.V = c->cfg.text_out;
+    sp.B = B;
+    sp.cfg = c->scfg;
+    sp.st = c->st;
+    sp.io = reinterpret_cast<const FrameIO*>(c->io_region);
+    sp.dio = reinterpret_cast<const DepIO*>(c->dio_region);
+    sp.n_streams = c->cfg.n_streams;
+    PM_CUDA(launch_sample(sp, s, pdl));
+    return mark(c, s, PM_KERNEL_SAMPLE);
+}
+
 static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
     const pm_config& f = c->cfg;
     const int D = f.D, F = f.ffn;
-    if (B == 1 && c->prog) {
+    if (B == 1 && c->prog && !c->text_smp) {
         pm_status ms = mark(c, s, -1);
         if (ms) return ms;
         PM_CUDA(launch_frame_prog(c->prog_params, c->num_sms, c->prog_smem, s));
@@ -351,11 +376,12 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
     p.alpha = c->out_norm;
     p.y_stride = f.text_out;
     p.h_internal = c->h;
+    if (c->text_smp) p.logits_copy = c->slog;
     pm_status ps = plan(c, p, 1, "text_linear");
     if (ps) return ps;
     PM_CUDA(launch_gemv(PRO_RMSNORM, E_HEAD, U_ROW, p, s, pdl));
     if ((ms = mark(c, s, PM_KERNEL_HEAD))) return ms;
-    return PM_OK;
+    return record_text_sample(c, B, s, pdl);
 }
 
 
@@ -509,7 +535,10 @@ static pm_status record_frame_tc(pm_ctx* c, int B, cudaStream_t s) {
     p.x_resid = c->x;
     p.alpha = c->out_norm;
     p.nx = next_tc(c, D, 3 * D / 128, 0, npad);  // the next frame's first projection
-    return go(mh, mx, mq[0], p, PM_KERNEL_HEAD, "text_linear");
+    if (c->text_smp) p.logits_copy = c->slog;
+    pm_status hs = go(mh, mx, mq[0], p, PM_KERNEL_HEAD, "text_linear");
+    if (hs) return hs;
+    return record_text_sample(c, B, s, pdl);
 }
 
 static pm_status record_depformer(pm_ctx* c, int B, cudaStream_t s) {
@@ -625,9 +654,29 @@ static pm_status record_depformer(pm_ctx* c, int B, cudaStream_t s) {
         p.y_stride = f.dep_card;
         p.q = q;
         p.Q = Q;
+        if (c->audio_smp) p.logits_copy = c->dslog;
         ps = plan(c, p, 1, "depformer head");
         if (ps) return ps;
         PM_CUDA(launch_gemv(PRO_PLAIN, E_DEP_HEAD, U_ROW, p, s, true));
+        if (c->audio_smp) {
+            // the drawn code replaces the argmax where none is supplied, before position
+            // q + 1 embeds it
+            SampleParams sp;
+            memset(&sp, 0, sizeof sp);
+            sp.mode = SM_DEPTH;
+            sp.logits = c->dslog;
+            sp.ld = f.dep_card;
+            sp.V = f.dep_card;
+            sp.B = B;
+            sp.cfg = c->scfg;
+            sp.st = c->st;
+            sp.io = reinterpret_cast<const FrameIO*>(c->io_region);
+            sp.dio = reinterpret_cast<const DepIO*>(c->dio_region);
+            sp.q = q;
+            sp.Q = Q;
+            sp.n_streams = f.n_streams;
+            PM_CUDA(launch_sample(sp, s, true));
+        }
     }
     return PM_OK;
 }
@@ -801,7 +850,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     void* p_pos; void* p_first; void* p_ring; void* p_sel; void* p_amax; void* p_hc; void* p_status;
     void* p_damax; void* p_dcount; void* p_dcodes; void* p_dtok; void* p_dsup;
     void* p_io; void* p_dio; void *p_x, *p_q, *p_o, *p_s, *p_h, *p_part, *p_cnt, *p_freq, *p_dz, *p_dq,
-        *p_ds, *p_dkv, *p_rtab, *p_xb, *p_ob, *p_sb, *p_ss, *p_tcp, *p_tcc;
+        *p_ds, *p_dkv, *p_rtab, *p_xb, *p_ob, *p_sb, *p_ss, *p_tcp, *p_tcc, *p_scfg, *p_slog, *p_dslog;
     // tensor-core path scratch, sized from the plans of this configuration's projections
     const int NP = BM >= 2 ? (BM <= 16 ? 16 : (BM <= 32 ? 32 : 64)) : 16;
     size_t tc_part_floats = 16;
@@ -839,6 +888,8 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
         {&p_dz, 4u * BM * (Dd ? Dd : 1)}, {&p_dq, 4u * BM * (Dd ? Dd : 1)},
         {&p_ds, 4u * BM * (Fd ? Fd : 1)},
         {&p_dkv, c->has_dep ? 2u * 2u * f.dep_layers * BM * f.dep_H * Q * f.dep_dh : 16u},
+        {&p_scfg, sizeof(SampleCfg)}, {&p_slog, 4u * BM * f.text_out},
+        {&p_dslog, c->has_dep ? 4u * BM * f.dep_card : 16u},
     };
     size_t total = 0;
     for (auto& it : items) total = align_up(total, 256) + align_up(it.bytes, 16);
@@ -888,6 +939,9 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     c->dq = (float*)p_dq;
     c->ds = (float*)p_ds;
     c->dkv = (uint16_t*)p_dkv;
+    c->scfg = (SampleCfg*)p_scfg;
+    c->slog = (float*)p_slog;
+    c->dslog = (float*)p_dslog;
 
     // RoPE frequencies f_j = exp(-ln(theta) * 2j / dh), in double
     std::vector<double> freq(f.dh / 2);
@@ -1027,6 +1081,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
         }
     }
     if (ck(gemv_prepare())) return bail(PM_ERR_CUDA, "gemv_prepare()");
+    if (ck(sample_prepare())) return bail(PM_ERR_CUDA, "sample_prepare()");
     if (BM >= 2 && ck(tc_prepare())) return bail(PM_ERR_CUDA, "tc_prepare");
     if (ck(cudaDeviceSynchronize())) return bail(PM_ERR_CUDA, "cudaDeviceSynchronize()");
     *out = c;
@@ -1179,6 +1234,62 @@ extern "C" pm_status pm_depformer_step(pm_ctx* c, int B, const float* hidden, co
     PM_CUDA(cudaMemcpyAsync(c->dio_region, host, bytes, cudaMemcpyHostToDevice, c->stream));
     PM_CUDA(cudaEventRecord(ev, c->stream));
     PM_CUDA(cudaGraphLaunch(ex, c->stream));
+    return PM_OK;
+}
+
+extern "C" pm_status pm_set_sampling(pm_ctx* c, float text_temperature, int text_top_k, float audio_temperature,
+                                     int audio_top_k, unsigned long long seed) {
+    if (!c) return PM_ERR_ARG;
+    const bool ton = text_temperature > 0.0f && text_top_k > 1;
+    const bool aon = audio_temperature > 0.0f && audio_top_k > 1;
+    if ((ton && text_top_k > PM_SAMPLE_MAX_TOP_K) || (aon && audio_top_k > PM_SAMPLE_MAX_TOP_K))
+        return fail(c, PM_ERR_ARG, "pm_set_sampling: top_k above 1024");
+    if (!(text_temperature == text_temperature) || !(audio_temperature == audio_temperature))
+        return fail(c, PM_ERR_ARG, "pm_set_sampling: temperature is NaN");
+    PM_CUDA(cudaSetDevice(c->device));
+    c->scfg_host.text_temperature = text_temperature;
+    c->scfg_host.text_top_k = text_top_k;
+    c->scfg_host.audio_temperature = audio_temperature;
+    c->scfg_host.audio_top_k = audio_top_k;
+    c->scfg_host.seed = seed;
+    // pageable source: the copy is staged before the call returns, ordered on the stream
+    PM_CUDA(cudaMemcpyAsync(c->scfg, &c->scfg_host, sizeof(SampleCfg), cudaMemcpyHostToDevice, c->stream));
+    if (ton != c->text_smp || aon != c->audio_smp) {
+        // the set of launches changes: drop the captured graphs (re-captured on next use)
+        PM_CUDA(cudaStreamSynchronize(c->stream));
+        for (auto& kv : c->frame_graphs) cudaGraphExecDestroy(kv.second);
+        for (auto& kv : c->dep_graphs) cudaGraphExecDestroy(kv.second);
+        c->frame_graphs.clear();
+        c->dep_graphs.clear();
+        c->text_smp = ton;
+        c->audio_smp = aon;
+    }
+    return PM_OK;
+}
+
+extern "C" pm_status pm_sample(pm_ctx* c, int B, const float* logits, int V, int ld, float temperature, int top_k,
+                               unsigned long long seed, long long position, int substep, int32_t* tokens) {
+    if (!c) return PM_ERR_ARG;
+    if (B < 1 || V < 1 || ld < V) return fail(c, PM_ERR_ARG, "pm_sample: need B >= 1, V >= 1, ld >= V");
+    if (!logits || !tokens) return fail(c, PM_ERR_ARG, "pm_sample: null pointer");
+    if (!(temperature == temperature)) return fail(c, PM_ERR_ARG, "pm_sample: temperature is NaN");
+    if (temperature > 0.0f && top_k > PM_SAMPLE_MAX_TOP_K) return fail(c, PM_ERR_ARG, "pm_sample: top_k above 1024");
+    PM_CUDA(cudaSetDevice(c->device));
+    if (!is_device_ptr(logits)) return fail(c, PM_ERR_ARG, "pm_sample: logits must be device memory");
+    SampleParams sp;
+    memset(&sp, 0, sizeof sp);
+    sp.mode = SM_PLAIN;
+    sp.logits = logits;
+    sp.ld = ld;
+    sp.V = V;
+    sp.B = B;
+    sp.temperature = temperature;
+    sp.top_k = top_k;
+    sp.seed = seed;
+    sp.position = position;
+    sp.substep = substep;
+    sp.tokens = tokens;
+    PM_CUDA(launch_sample(sp, c->stream, false));
     return PM_OK;
 }
 

@@ -42,6 +42,16 @@ struct DevState {
     int32_t* dep_sup;              // [B_max][dep_steps] validated supplied codes (-1 = greedy)
 };
 
+// Sampling settings of a context, device-resident so that a captured graph follows
+// pm_set_sampling without re-capture (temperature <= 0 or top_k <= 1: greedy).
+struct SampleCfg {
+    float text_temperature;
+    int text_top_k;
+    float audio_temperature;
+    int audio_top_k;
+    unsigned long long seed;
+};
+
 // Pointers the caller supplies per call, read by the kernels from device memory so that a
 // captured graph serves every call.
 struct FrameIO {

@@ -74,6 +74,7 @@ struct GemvParams {
     int x_in_smem;         // plan input: the prologue builds x in shared memory (PRO_DEPATTN)
     float dep_scale_log2;
     int n_streams;
+    float* logits_copy;    // E_HEAD / E_DEP_HEAD: also write the logits here ([B][y_stride]), or null
 };
 
 // Choose the tiling for a GEMV of row length K over n_units units of rows_per_unit rows.
@@ -145,6 +146,40 @@ cudaError_t launch_dep_begin(const DepBeginParams& p, cudaStream_t s, bool pdl);
 
 
 // ----------------------------------------------------------------------------------
+// temperature / top-k sampling (one CTA per row)
+// ----------------------------------------------------------------------------------
+enum SampleMode {
+    SM_PLAIN = 0,  // given rows, settings and counter; tokens to `tokens`
+    SM_TEXT = 1,   // the frame's text token from the head's logits (context settings)
+    SM_DEPTH = 2   // depth position q's code where none is supplied (context settings)
+};
+// rows of up to this many logits are staged in shared memory (192 KB)
+#define PM_SAMPLE_STAGE_MAX 49152
+// largest top-k the sampler serves (one survivor per thread)
+#define PM_SAMPLE_MAX_TOP_K 1024
+struct SampleParams {
+    int mode;
+    const float* logits;   // row b at logits + b * ld
+    int ld, V, B;
+    int stage;             // set by launch_sample
+    // SM_PLAIN settings; counter (position, row, substep, 0)
+    float temperature;
+    int top_k;
+    unsigned long long seed;
+    long long position;
+    int substep;
+    int32_t* tokens;       // SM_PLAIN output [B]
+    // SM_TEXT / SM_DEPTH: settings, state, outputs; counter (pos - 1, row, 0 or 1 + q, 0)
+    const SampleCfg* cfg;
+    DevState st;
+    const FrameIO* io;
+    const DepIO* dio;
+    int q, Q, n_streams;
+};
+cudaError_t launch_sample(const SampleParams& p, cudaStream_t s, bool pdl);
+cudaError_t sample_prepare();
+
+// ----------------------------------------------------------------------------------
 // batched projections on the tensor cores (tcgen05, accumulators in TMEM), B >= 2
 // ----------------------------------------------------------------------------------
 enum TcEpilogue {
@@ -204,6 +239,7 @@ struct TcParams {
     float* h_internal;       // [B][D] hidden state
     const float* x_resid;    // [B][D] residual before the final norm
     const uint16_t* alpha;   // final norm scale [D]
+    float* logits_copy;      // also write the logits here ([B][n_rows]), or null
     NextPrefetch nx;         // read through the `next` tensor map
 };
 

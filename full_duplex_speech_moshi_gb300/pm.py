@@ -22,9 +22,9 @@ STATUS_NAMES = {0: "PM_OK", 1: "PM_ERR_ARG", 2: "PM_ERR_INVALID_ID", 3: "PM_ERR_
 # every symbol include/pm.h declares
 EXPORTS = ["pm_kv_cache_bytes", "pm_create", "pm_reset", "pm_set_positions", "pm_get_positions",
            "pm_frame_step", "pm_depformer_step", "pm_profile_frame", "pm_device_status", "pm_last_error",
-           "pm_destroy", "pm_text_head_noalloc"]
+           "pm_destroy", "pm_text_head_noalloc", "pm_set_sampling", "pm_sample"]
 KERNEL_KINDS = {0: "embed", 1: "qkv_rope", 2: "attention", 3: "out_proj", 4: "linear_in_swiglu",
-                5: "linear_out", 6: "text_head", 7: "frame_program"}
+                5: "linear_out", 6: "text_head", 7: "frame_program", 8: "text_sample"}
 
 
 class pm_config(C.Structure):
@@ -90,6 +90,11 @@ def lib():
         L.pm_last_error.argtypes = [vp]
         L.pm_text_head_noalloc.restype = C.c_int
         L.pm_text_head_noalloc.argtypes = [C.c_int, C.c_int, C.c_int, vp, vp, vp, C.c_float, vp, vp, vp, vp]
+        L.pm_set_sampling.restype = C.c_int
+        L.pm_set_sampling.argtypes = [vp, C.c_float, C.c_int, C.c_float, C.c_int, C.c_ulonglong]
+        L.pm_sample.restype = C.c_int
+        L.pm_sample.argtypes = [vp, C.c_int, vp, C.c_int, C.c_int, C.c_float, C.c_int, C.c_ulonglong,
+                                C.c_longlong, C.c_int, vp]
         L.pm_destroy.restype = None
         L.pm_destroy.argtypes = [vp]
         _lib = L
@@ -229,9 +234,23 @@ class Context:
         self._check(self.L.pm_depformer_step(self.h, int(B), _ptr(hidden), _ptr(text_tok), _ptr(supplied),
                                              _ptr(logits), _ptr(codes)))
 
+    def set_sampling(self, text_temperature: float, text_top_k: int, audio_temperature: float, audio_top_k: int,
+                     seed: int) -> None:
+        """Temperature / top-k sampling of the text token and the depth codes (<= 0 / <= 1:
+        greedy)."""
+        self._check(self.L.pm_set_sampling(self.h, float(text_temperature), int(text_top_k),
+                                           float(audio_temperature), int(audio_top_k),
+                                           int(seed) & (2**64 - 1)))
+
+    def sample(self, B: int, logits, V: int, ld: int, temperature: float, top_k: int, seed: int, position: int,
+               substep: int, tokens) -> None:
+        """Standalone sampling of B rows of device logits into `tokens` (device int32)."""
+        self._check(self.L.pm_sample(self.h, int(B), _ptr(logits), int(V), int(ld), float(temperature), int(top_k),
+                                     int(seed) & (2**64 - 1), int(position), int(substep), _ptr(tokens)))
+
     def profile_frame(self, B: int, ids, text_logits=None, hidden=None, text_token=None):
         """One frame with per-launch device times: list of (kind name, ms)."""
-        n_max = 2 + 5 * self.shape["n_layers"]
+        n_max = 3 + 5 * self.shape["n_layers"]
         ms = (C.c_float * n_max)()
         kind = (C.c_int32 * n_max)()
         n = C.c_int(0)

@@ -151,17 +151,19 @@ pm_status pm_get_positions(pm_ctx* ctx, int32_t* pos_out);
  *              copied before the call returns.
  *  text_logits [B][text_out] fp32 device memory, or NULL.
  *  hidden      [B][D] fp32 device memory: h after the final RMSNorm, or NULL.
- *  text_token  [B] int32, device or host-mapped memory: greedy text token, or NULL.
+ *  text_token  [B] int32, device or host-mapped memory: the selected text token (greedy,
+ *              or drawn after pm_set_sampling), or NULL.
  * Advances each stream's position by one. */
 pm_status pm_frame_step(pm_ctx* ctx, int B, const int32_t* ids, float* text_logits, float* hidden,
                         int32_t* text_token);
 
 /* One depformer frame (sixteen positions) for streams 0..B-1.
  *  hidden    [B][D] fp32 device memory, or NULL = the h of this context's last frame.
- *  text_tok  [B] int32 host or device memory, or NULL = the greedy text token of this
- *            context's last frame.
+ *  text_tok  [B] int32 host or device memory, or NULL = the text token this context
+ *            selected on its last frame.
  *  supplied  [B][dep_steps] int32 host or device memory, or NULL = all greedy:
- *            -1 = take the argmax, otherwise the code to use (0..dep_card-1).
+ *            -1 = select (argmax, or drawn after pm_set_sampling), otherwise the code
+ *            to use (0..dep_card-1).
  *  logits    [B][dep_steps][dep_card] fp32 device memory, or NULL.
  *  codes     [B][dep_steps] int32 device or host-mapped memory, or NULL. */
 pm_status pm_depformer_step(pm_ctx* ctx, int B, const float* hidden, const int32_t* text_tok,
@@ -176,18 +178,47 @@ typedef enum {
     PM_KERNEL_LINEAR_IN = 4,   /* RMSNorm + linear_in + SwiGLU */
     PM_KERNEL_LINEAR_OUT = 5,  /* linear_out + residual */
     PM_KERNEL_HEAD = 6,        /* final RMSNorm + text head + greedy token */
-    PM_KERNEL_FRAME = 7        /* the whole batch-1 frame as one persistent launch */
+    PM_KERNEL_FRAME = 7,       /* the whole batch-1 frame as one persistent launch */
+    PM_KERNEL_SAMPLE = 8       /* temperature / top-k sampling of the text token */
 } pm_kernel_kind;
 
 /* Same computation and state change as pm_frame_step, but the frame's kernels are
  * launched one at a time (no graph, no overlap between kernels) with a CUDA event after
  * each on the context's stream.  Writes each launch's device time in milliseconds to
  * kernel_ms[i] and its pm_kernel_kind to kernel_kind[i] (host arrays of max_launches
- * entries; a frame has 2 + 5 * n_layers launches), the count to *n_launches, and
+ * entries; a frame has 2 + 5 * n_layers launches, one more with text sampling), the
+ * count to *n_launches, and
  * synchronises the stream.  For measurement only. */
 pm_status pm_profile_frame(pm_ctx* ctx, int B, const int32_t* ids, float* text_logits, float* hidden,
                            int32_t* text_token, float* kernel_ms, int32_t* kernel_kind, int max_launches,
                            int* n_launches);
+
+/* Sampling ("PersonaPlex native LM audit", section 7: the generator samples the text
+ * token and every depth code; released defaults text temperature 0.7 / top-k 25, audio
+ * 0.8 / top-k 250).  Greedy (the argmax, lowest index on ties) until this is called.
+ * With temperature > 0 and top_k > 1 a token is drawn from the top_k largest logits
+ * (ties at the cut kept by lower index) with weights exp((l - l_max) / temperature),
+ * scanning them in descending order for the first running weight above u * total, where
+ * u = (first word of Philox4x64-10 >> 40) * 2^-24 under key (seed, 0) and counter
+ * (frame position, batch row, substep, 0): substep 0 for the text token, 1 + q for depth
+ * position q; the frame position is the stream's position before the frame.  The drawn
+ * text token replaces the greedy one everywhere (text_token output, PM_ID_FEEDBACK, the
+ * depformer's default conditioning token); drawn depth codes replace the greedy ones
+ * where no code is supplied.  temperature <= 0 or top_k <= 1 selects greedy for that
+ * stream kind; top_k above 1024 is PM_ERR_ARG (it is clamped to the vocabulary size).
+ * Ordered with the context's other calls on its stream; the next frame after a switch
+ * between greedy and sampled captures new graphs. */
+pm_status pm_set_sampling(pm_ctx* ctx, float text_temperature, int text_top_k, float audio_temperature,
+                          int audio_top_k, unsigned long long seed);
+
+/* Standalone sampling of B rows of logits with the rule of pm_set_sampling (counter
+ * (position, row, substep, 0) for row b).
+ *  logits  fp32 device memory, row b at logits + b * ld (ld >= V), V >= 1.
+ *  tokens  [B] int32 device or host-mapped memory.
+ * temperature <= 0 or top_k <= 1: the argmax.  top_k above 1024 is PM_ERR_ARG.  One
+ * launch on the context's stream; touches no context state. */
+pm_status pm_sample(pm_ctx* ctx, int B, const float* logits, int V, int ld, float temperature, int top_k,
+                    unsigned long long seed, long long position, int substep, int32_t* tokens);
 
 /* Synchronise the stream and return (and clear) any device-side error: an invalid ID
  * given in device memory (PM_ERR_INVALID_ID) or a bounded wait that ran out
