@@ -323,6 +323,27 @@ def main():
         torch.cuda.synchronize()
         extras["with_depformer_frames_per_s"] = f4
         extras["depformer_ms"] = a2.elapsed_time(b2) / n4
+        # the released sampling defaults (text 0.7 / top-k 25, audio 0.8 / top-k 250)
+        ctx.set_sampling(0.7, 25, 0.8, 250, 20251)
+        for t in range(4):
+            ctx.frame_step(1, ids_d[PR + t], logits, hidden, token)
+            ctx.depformer_step(1, None, None, sup[t], dl, dc)
+        torch.cuda.synchronize()
+        a3, b3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a3.record(stream)
+        for t in range(n4):
+            ctx.frame_step(1, ids_d[PR + 8 + t], logits, hidden, token)
+        b3.record(stream)
+        a4, b4 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a4.record(stream)
+        for t in range(n4):
+            ctx.frame_step(1, ids_d[PR + 8 + t], logits, hidden, token)
+            ctx.depformer_step(1, None, None, sup[t % 64], dl, dc)
+        b4.record(stream)
+        torch.cuda.synchronize()
+        ctx.set_sampling(0.0, 1, 0.0, 1, 0)
+        extras["sampled_frames_per_s"] = n4 / (a3.elapsed_time(b3) / 1000.0)
+        extras["sampled_with_depformer_frames_per_s"] = n4 / (a4.elapsed_time(b4) / 1000.0)
     ctx.close()
     del kv1
     torch.cuda.empty_cache()
