@@ -62,6 +62,9 @@ class ModelShape:
     dep_card: int = 2048      # depth head rows
     dep_text_in: int = 32001
     dep_audio_in: int = 2049
+    # 1: attention windows follow the pinned ring's position labels instead of the declared
+    # mask (a full ring hides its oldest key)
+    pinned_ring: int = 0
 
     def asdict(self) -> dict:
         return asdict(self)

@@ -29,7 +29,7 @@ class orc_config(C.Structure):
         ("delays", C.c_int * 64), ("init_text", C.c_int), ("init_audio", C.c_int),
         ("eps", C.c_double), ("rope_theta", C.c_double)] + [
         (n, C.c_int) for n in ("dep_D", "dep_H", "dep_dh", "dep_ffn", "dep_layers", "dep_steps", "dep_ctx",
-                               "dep_card", "dep_text_in", "dep_audio_in")]
+                               "dep_card", "dep_text_in", "dep_audio_in", "pinned_ring")]
 
 
 class orc_sampling(C.Structure):
@@ -89,6 +89,9 @@ def lib():
             L.orc_full_sequence.argtypes = [C.c_void_p, i, i32p, dp, dp, i32p]
             L.orc_depformer_step.restype = i
             L.orc_depformer_step.argtypes = [C.c_void_p, dp, C.c_int32, i32p, dp, i32p]
+            L.orc_ring_labels.argtypes = [C.c_long, C.c_long, C.POINTER(C.c_long)]
+            L.orc_visible_positions.restype = i
+            L.orc_visible_positions.argtypes = [C.c_long, C.c_long, i, C.POINTER(C.c_long)]
             u64p = C.POINTER(C.c_uint64)
             L.orc_philox4x64.argtypes = [u64p, u64p, u64p]
             L.orc_uniform24.restype = d
@@ -124,6 +127,7 @@ def make_config(shape: dict, depformer: bool = True) -> orc_config:
               "dep_card", "dep_text_in", "dep_audio_in"):
         setattr(c, k, int(shape[k]))
     c.dep_layers = int(shape["dep_layers"]) if depformer else 0
+    c.pinned_ring = int(shape.get("pinned_ring", 0))
     c.eps = float(shape["eps"])
     c.rope_theta = float(shape["rope_theta"])
     for i, d in enumerate(shape["delays"]):
@@ -314,3 +318,17 @@ def sample_topk(logits: np.ndarray, temperature: float, top_k: int, seed: int, c
     tok = lib().orc_sample_topk(_dp(lg), lg.size, float(temperature), int(top_k), int(seed) & (2**64 - 1), int(c0),
                                 int(c1), int(c2), C.byref(mg), C.byref(gap))
     return int(tok), float(mg.value), float(gap.value)
+
+
+# --- ring position labels ----------------------------------------------------
+
+def ring_labels(capacity: int, end_offset: int) -> list:
+    out = (C.c_long * int(capacity))()
+    lib().orc_ring_labels(int(capacity), int(end_offset), out)
+    return [int(v) for v in out]
+
+
+def visible_positions(pos: int, capacity: int, pinned: bool) -> list:
+    out = (C.c_long * int(capacity))()
+    n = lib().orc_visible_positions(int(pos), int(capacity), int(bool(pinned)), out)
+    return [int(out[i]) for i in range(n)]

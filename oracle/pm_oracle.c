@@ -39,6 +39,13 @@
  *     row, substep, 0), substep 0 for the text token and 1 + q for depth position q:
  *     u = (first output word >> 40) * 2^-24.
  *
+ * Pinned ring mode (same page, section 6, "Observed source-level boundary"): the ring
+ * labels slot i, with end_index = end_offset mod capacity and delta = i - end_index, as
+ * position end_offset + delta when delta <= 0 and end_offset + delta - capacity otherwise;
+ * a key is attended to when its label lies in 0..query position.  After the current
+ * key's write (end_offset = position + 1) a full ring therefore hides its oldest key.  The
+ * depth cache uses the same mapping with capacity dep_ctx (the pages show it for 16).
+ *
  * Arithmetic is float64 throughout.  Weights are bf16 bit patterns, widened exactly.
  * Nothing is blocked, fused or reordered beyond the definitions above.  Loops over
  * output rows run under OpenMP; each row's sum is a plain serial loop.
@@ -118,6 +125,36 @@ void orc_attend(const double* q, const double* const* keys, const double* const*
     for (int i = 0; i < n; ++i)
         for (int c = 0; c < dh; ++c) o[c] += (s[i] / den) * vals[i][c];
     free(s);
+}
+
+void orc_ring_labels(long capacity, long end_offset, long* labels) {
+    const long end_index = end_offset % capacity;
+    for (long i = 0; i < capacity; ++i) {
+        const long delta = i - end_index;
+        labels[i] = (delta <= 0) ? end_offset + delta : end_offset + delta - capacity;
+    }
+}
+
+static int cmp_long(const void* a, const void* b) {
+    const long x = *(const long*)a, y = *(const long*)b;
+    return (x > y) - (x < y);
+}
+
+int orc_visible_positions(long pos, long capacity, int pinned, long* vis) {
+    int n = 0;
+    if (!pinned) {
+        long lo = pos - capacity + 1;
+        if (lo < 0) lo = 0;
+        for (long p = lo; p <= pos; ++p) vis[n++] = p;
+        return n;
+    }
+    long* labels = (long*)malloc(sizeof(long) * (size_t)capacity);
+    orc_ring_labels(capacity, pos + 1, labels);
+    for (long i = 0; i < capacity; ++i)
+        if (labels[i] >= 0 && labels[i] <= pos) vis[n++] = labels[i];
+    free(labels);
+    qsort(vis, (size_t)n, sizeof(long), cmp_long);
+    return n;
 }
 
 /* lowest index among the maxima */
@@ -464,20 +501,19 @@ static void temporal_block(const orc_model* m, orc_stream* s, int l, double* x) 
     memcpy(s->K[l] + (size_t)pos * (size_t)D, k, sizeof(double) * (size_t)D);
     memcpy(s->V[l] + (size_t)pos * (size_t)D, v, sizeof(double) * (size_t)D);
 
-    /* keys allowed where 0 <= pos - key_pos < ctx */
-    long lo = pos - c->ctx + 1;
-    if (lo < 0) lo = 0;
-    int n = (int)(pos - lo + 1);
+    /* keys allowed where 0 <= pos - key_pos < ctx (or the pinned ring's labels) */
+    long* vis = (long*)malloc(sizeof(long) * (size_t)c->ctx);
+    const int n = orc_visible_positions(pos, c->ctx, c->pinned_ring, vis);
     const double** kp = (const double**)malloc(sizeof(void*) * (size_t)n);
     const double** vp = (const double**)malloc(sizeof(void*) * (size_t)n);
     for (int h = 0; h < H; ++h) {
         for (int i = 0; i < n; ++i) {
-            kp[i] = s->K[l] + (size_t)(lo + i) * (size_t)D + (size_t)h * (size_t)dh;
-            vp[i] = s->V[l] + (size_t)(lo + i) * (size_t)D + (size_t)h * (size_t)dh;
+            kp[i] = s->K[l] + (size_t)vis[i] * (size_t)D + (size_t)h * (size_t)dh;
+            vp[i] = s->V[l] + (size_t)vis[i] * (size_t)D + (size_t)h * (size_t)dh;
         }
         orc_attend(q + h * dh, kp, vp, n, dh, o + h * dh);
     }
-    free(kp); free(vp);
+    free(kp); free(vp); free(vis);
 
     orc_matvec(m->w_o[l], D, D, o, a);
     for (int i = 0; i < D; ++i) x[i] += a[i]; /* y = x + a */
@@ -551,12 +587,20 @@ int orc_full_sequence(const orc_model* m, int T, const int32_t* ids, double* hid
                 orc_rope(QKV + (size_t)t * 3 * D + D + h * dh, dh, t, c->rope_theta);
             }
         }
+        /* mask matrix M[t][s] = 0 if key s is visible to query t (0 <= t - s < ctx, or the
+         * pinned ring's labels with end_offset t + 1), else -inf */
+        char* allow = (char*)calloc((size_t)T * T, 1);
+        long* vis = (long*)malloc(sizeof(long) * (size_t)c->ctx);
+        for (int t = 0; t < T; ++t) {
+            const int nv = orc_visible_positions(t, c->ctx, c->pinned_ring, vis);
+            for (int i = 0; i < nv; ++i) allow[(size_t)t * T + vis[i]] = 1;
+        }
+        free(vis);
         for (int h = 0; h < H; ++h) {
-            /* scores with the mask matrix M[t][s] = 0 if 0 <= t - s < ctx, else -inf */
             for (int t = 0; t < T; ++t) {
                 double mx = -INFINITY;
                 for (int s2 = 0; s2 < T; ++s2) {
-                    int allowed = (t - s2 >= 0) && (t - s2 < c->ctx);
+                    int allowed = allow[(size_t)t * T + s2];
                     double d = 0.0;
                     for (int e = 0; e < dh; ++e)
                         d += QKV[(size_t)t * 3 * D + h * dh + e] * QKV[(size_t)s2 * 3 * D + D + h * dh + e];
@@ -577,6 +621,7 @@ int orc_full_sequence(const orc_model* m, int T, const int32_t* ids, double* hid
                 }
             }
         }
+        free(allow);
         for (int t = 0; t < T; ++t) {
             double* x = X + (size_t)t * D;
             orc_matvec(m->w_o[l], D, D, O + (size_t)t * D, A + (size_t)t * D);
@@ -635,6 +680,7 @@ int orc_depformer_step_sampled(const orc_model* m, const double* hidden, int32_t
     double* Vd = (double*)calloc((size_t)J * Q * Dd, sizeof(double));
     const double** kp = (const double**)malloc(sizeof(void*) * (size_t)Q);
     const double** vp = (const double**)malloc(sizeof(void*) * (size_t)Q);
+    long* dvis = (long*)malloc(sizeof(long) * (size_t)(c->dep_ctx > Q ? c->dep_ctx : Q));
 
     int32_t prev = text_tok;
     for (int q = 0; q < Q; ++q) {
@@ -648,13 +694,11 @@ int orc_depformer_step_sampled(const orc_model* m, const double* hidden, int32_t
             orc_matvec(m->dep_qkv[j] + (size_t)q * 3 * Dd * Dd, 3 * Dd, Dd, u, qkv);
             memcpy(Kd + ((size_t)j * Q + q) * Dd, qkv + Dd, sizeof(double) * (size_t)Dd);
             memcpy(Vd + ((size_t)j * Q + q) * Dd, qkv + 2 * Dd, sizeof(double) * (size_t)Dd);
-            int lo = q - c->dep_ctx + 1;
-            if (lo < 0) lo = 0;
-            int n = q - lo + 1;
+            const int n = orc_visible_positions(q, c->dep_ctx, c->pinned_ring, dvis);
             for (int h = 0; h < Hd; ++h) {
                 for (int i = 0; i < n; ++i) {
-                    kp[i] = Kd + ((size_t)j * Q + lo + i) * Dd + (size_t)h * dd;
-                    vp[i] = Vd + ((size_t)j * Q + lo + i) * Dd + (size_t)h * dd;
+                    kp[i] = Kd + ((size_t)j * Q + dvis[i]) * Dd + (size_t)h * dd;
+                    vp[i] = Vd + ((size_t)j * Q + dvis[i]) * Dd + (size_t)h * dd;
                 }
                 orc_attend(qkv + h * dd, kp, vp, n, dd, o + h * dd);
             }
@@ -682,6 +726,6 @@ int orc_depformer_step_sampled(const orc_model* m, const double* hidden, int32_t
         prev = code;
     }
     free(z); free(u); free(qkv); free(o); free(a); free(gz); free(sg); free(Kd); free(Vd);
-    free(kp); free(vp);
+    free(kp); free(vp); free(dvis);
     return ORC_OK;
 }

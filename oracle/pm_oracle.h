@@ -33,6 +33,7 @@ typedef struct {
     int init_text, init_audio;
     double eps, rope_theta;
     int dep_D, dep_H, dep_dh, dep_ffn, dep_layers, dep_steps, dep_ctx, dep_card, dep_text_in, dep_audio_in;
+    int pinned_ring; /* 0: the declared mask; 1: the pinned ring's position labels (both caches) */
 } orc_config;
 
 typedef struct orc_model orc_model;
@@ -46,6 +47,12 @@ void orc_rope(double* v, int dh, long pos, double theta);
 double orc_silu(double g);
 void orc_attend(const double* q, const double* const* keys, const double* const* vals, int n, int dh, double* o);
 int orc_argmax(const double* v, int n);
+/* position labels of a ring of `capacity` slots after `end_offset` writes, as the pinned
+ * implementation reports them; and the positions a query at `pos` may attend to (its own
+ * key written, so end_offset = pos + 1), ascending, into vis[] (capacity entries); returns
+ * their count.  pinned = 0 gives the declared mask 0 <= pos - p < capacity. */
+void orc_ring_labels(long capacity, long end_offset, long* labels);
+int orc_visible_positions(long pos, long capacity, int pinned, long* vis);
 
 int orc_tensor_count(const orc_config* c);
 orc_model* orc_create(const orc_config* c, const uint16_t* const* tensors, int n_tensors);
