@@ -3,8 +3,9 @@
 // keys allowed where 0 <= query_position - key_position < 3000; section 6: the cache
 // holds keys after RoPE, values without).
 //
-// For batch row b at position p the visible keys are positions max(0, p-ctx+1) .. p,
-// stored at ring slots position mod ctx.  Work item (b, h, c) is the 64 keys
+// For batch row b at position p the visible keys are positions max(0, p-win+1) .. p,
+// stored at ring slots position mod ctx (win = ctx for the declared mask, ctx - 1 for the
+// pinned ring's labels, which hide the oldest key of a full ring).  Work item (b, h, c) is the 64 keys
 // lo + 64c .. lo + 64c + 63 of row b's window for head h.  The items of all rows form one
 // list whose length follows the device-resident positions; a fixed grid of CTAs walks it
 // with a grid stride, so the launch does not grow with the context.  128 threads = 4
@@ -54,7 +55,7 @@ __global__ void __launch_bounds__(128) k_attn(const AttnParams p) {
         int acc = 0;
         for (int bb = 0; bb < p.B; ++bb) {
             s_first[bb] = acc;
-            acc += p.H * n_chunks(p.st.pos[bb], p.ctx);
+            acc += p.H * n_chunks(p.st.pos[bb], p.win);
         }
         s_first[p.B] = acc;
     }
@@ -69,7 +70,7 @@ __global__ void __launch_bounds__(128) k_attn(const AttnParams p) {
         int b = 0;
         while (item >= s_first[b + 1]) ++b;
         const int pos = p.st.pos[b];
-        const int n = min(pos + 1, p.ctx);
+        const int n = min(pos + 1, p.win);
         const int lo = pos - n + 1;
         const int nc = (n + KPC - 1) / KPC;
         const int h = (item - s_first[b]) / nc;
@@ -239,7 +240,8 @@ __global__ void __launch_bounds__(128) k_attn(const AttnParams p) {
 int attn_max_splits(int ctx) { return (ctx + KPC - 1) / KPC; }
 
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
-    if (p.S < attn_max_splits(p.ctx) || p.S > MAX_CHUNKS || p.B > PM_MAX_B_DEV || p.grid < 1)
+    if (p.S < attn_max_splits(p.ctx) || p.S > MAX_CHUNKS || p.B > PM_MAX_B_DEV || p.grid < 1 || p.win < 1 ||
+        p.win > p.ctx)
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);

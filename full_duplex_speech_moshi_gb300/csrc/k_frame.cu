@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(NTH, 1) k_frame(const FrameProgParams p) {
                         }
                     }
                 } else if (f.type == PH_ATTN) {
-                    const int n = min(pos + 1, p.ctx), lo = pos - n + 1, nc = attn_nc(pos, p.ctx);
+                    const int n = min(pos + 1, p.win), lo = pos - n + 1, nc = attn_nc(pos, p.win);
                     for (int item = c; item < p.H * nc && ok; item += G) {
                         const int h = item / nc, ci = item % nc;
                         const int k0 = lo + ci * KPC;
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(NTH, 1) k_frame(const FrameProgParams p) {
                     }
                 }
             } else if (f.type == PH_ATTN) {
-                const int n = min(pos + 1, p.ctx), lo = pos - n + 1, nc = attn_nc(pos, p.ctx);
+                const int n = min(pos + 1, p.win), lo = pos - n + 1, nc = attn_nc(pos, p.win);
                 const int ng = warp >> 2, wq = warp & 3;  // group, warp in group
                 const int g = lane >> 3, sub = lane & 7;
                 float* myacc = gacc + (size_t)ng * 4 * (DH + 2);

@@ -131,11 +131,13 @@ static const char* check_config(const pm_config* c) {
     if (c->init_text < 0 || c->init_text >= c->text_in) return "init_text outside the text table";
     if (c->init_audio < 0 || c->init_audio >= c->audio_in) return "init_audio outside the audio tables";
     if (!(c->eps > 0.f) || !(c->rope_theta > 0.f)) return "eps and rope_theta must be positive";
+    if ((c->flags & PM_FLAG_PINNED_RING) && c->ctx < 2) return "the pinned ring needs ctx >= 2";
     if (c->dep_layers > 0) {
         if (c->dep_dh != 64 || c->dep_D != c->dep_H * c->dep_dh) return "depformer needs dep_dh 64 and dep_D = dep_H * 64";
         if (c->dep_D % 256 != 0 || c->dep_ffn % 256 != 0) return "dep_D and dep_ffn must be multiples of 256";
         if (c->dep_steps < 1 || c->dep_steps > 32) return "dep_steps must be 1..32";
         if (c->dep_ctx < 1 || c->dep_ctx > 16) return "dep_ctx must be 1..16";
+        if ((c->flags & PM_FLAG_PINNED_RING) && c->dep_ctx < 2) return "the pinned ring needs dep_ctx >= 2";
         if (c->dep_card < 1 || c->dep_text_in < 1 || c->dep_audio_in < c->dep_card) return "bad depformer table sizes";
     }
     return nullptr;
@@ -315,6 +317,7 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
         ap.H = f.H;
         ap.ctx = f.ctx;
         ap.S = attn_max_splits(f.ctx);
+        ap.win = f.ctx - ((f.flags & PM_FLAG_PINNED_RING) ? 1 : 0);
         ap.grid = (B == 1 ? 4 : 16) * c->num_sms;
         ap.D = D;
         ap.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dh));
@@ -492,6 +495,7 @@ static pm_status record_frame_tc(pm_ctx* c, int B, cudaStream_t s) {
         ap.H = f.H;
         ap.ctx = f.ctx;
         ap.S = attn_max_splits(f.ctx);
+        ap.win = f.ctx - ((f.flags & PM_FLAG_PINNED_RING) ? 1 : 0);
         ap.grid = (B == 1 ? 4 : 16) * c->num_sms;
         ap.D = D;
         ap.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dh));
@@ -611,7 +615,7 @@ static pm_status record_depformer(pm_ctx* c, int B, cudaStream_t s) {
             p.q = q;
             p.dkc = dkc;
             p.dvc = dvc;
-            p.dep_ctx = f.dep_ctx;
+            p.dep_ctx = f.dep_ctx - ((f.flags & PM_FLAG_PINNED_RING) ? 1 : 0);  // keys a position sees
             p.dep_scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dep_dh));
             p.x_in_smem = 1;
             ps = plan(c, p, 1, "depformer out_proj");
@@ -1068,6 +1072,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
             pp.H = f.H;
             pp.dh = f.dh;
             pp.ctx = f.ctx;
+            pp.win = f.ctx - ((f.flags & PM_FLAG_PINNED_RING) ? 1 : 0);
             pp.eps = f.eps;
             pp.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dh));
             pp.part = c->att_part;

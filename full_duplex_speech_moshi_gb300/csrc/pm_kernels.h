@@ -123,6 +123,7 @@ struct AttnParams {
     uint32_t* count;       // [B][H], zero between launches
     DevState st;
     int B, H, ctx, S, D;
+    int win;               // most keys a query sees (ctx, or ctx - 1 for the pinned ring)
     int grid;              // CTAs walking the work list
     float scale_log2;      // log2(e) / sqrt(dh)
 };
@@ -289,6 +290,7 @@ struct FrameProgParams {
     float* o;
     float* h;
     int D, H, dh, ctx;
+    int win;                 // most keys a query sees (ctx, or ctx - 1 for the pinned ring)
     float eps, scale_log2;
     float* part;        // [H][S][dh + 2] attention chunk partials
     uint32_t* att_count;  // [H]

@@ -37,6 +37,7 @@ class pm_config(C.Structure):
                 ("dep_text_in", C.c_int), ("dep_audio_in", C.c_int), ("flags", C.c_uint)]
 
 PM_FLAG_FRAME_PROGRAM = 1
+PM_FLAG_PINNED_RING = 2
 
 
 _PP = C.POINTER(C.c_void_p)
@@ -123,7 +124,7 @@ def _ptr(x) -> Optional[int]:
 def make_config(shape: dict, B_max: int, depformer: bool = True, flags: int = 0) -> pm_config:
     c = pm_config()
     c.B_max = int(B_max)
-    c.flags = int(flags)
+    c.flags = int(flags) | (PM_FLAG_PINNED_RING if shape.get("pinned_ring") else 0)
     for k in ("D", "H", "dh", "ffn", "n_layers", "ctx", "text_in", "text_out", "audio_in", "n_streams",
               "init_text", "init_audio", "dep_D", "dep_H", "dep_dh", "dep_ffn", "dep_steps", "dep_ctx",
               "dep_card", "dep_text_in", "dep_audio_in"):

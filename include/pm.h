@@ -94,6 +94,13 @@ typedef struct {
  * Measured on GB300 at 2.75 ms per 32-block frame against 2.51 ms for the chain. */
 #define PM_FLAG_FRAME_PROGRAM 1u
 
+/* pm_config.flags: attention windows of the pinned ring cache ("PersonaPlex native LM
+ * audit", section 6, "Observed source-level boundary"): its position labels hide the
+ * oldest key of a full ring, so a query sees min(pos + 1, ctx - 1) temporal keys and
+ * min(q + 1, dep_ctx - 1) depth keys instead of the declared mask's ctx / dep_ctx.
+ * Off by default (the declared mask).  Needs ctx >= 2 and dep_ctx >= 2. */
+#define PM_FLAG_PINNED_RING 2u
+
 /* Temporal weights: device pointers.  Per-layer members point to host arrays of
  * n_layers device pointers (copied by pm_create). */
 typedef struct {

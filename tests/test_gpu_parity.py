@@ -259,3 +259,40 @@ def test_frame_program_matches_kernel_chain():
         b.close()
     finally:
         a.close()
+
+
+def test_pinned_ring_mode_parity():
+    """PM_FLAG_PINNED_RING: the attention windows of the pinned ring cache (a full ring
+    hides its oldest key; "PersonaPlex native LM audit", section 6), temporal (B = 1 GEMV
+    path and B = 2 tensor-core path, through two ring wraps) and depth, against the
+    oracle's pinned-ring mode."""
+    s = small_shape(pinned_ring=1)
+    p = Pair(s, B_max=2)
+    try:
+        for B in (1, 2):
+            p.ctx.reset()
+            streams = [p.orc.new_stream() for _ in range(B)]
+            T = 2 * s.ctx + 3
+            ids = I.make_ids(s, T, B=B, seed=71 + B)
+            for t in range(T):
+                g = p.gpu_frame(ids[t], B=B)
+                outs = [streams[b].step(ids[t, b]) for b in range(B)]
+                r = (np.stack([o[0] for o in outs]), np.stack([o[2] for o in outs]), np.array([o[3] for o in outs]))
+                p.check_frame(g, r, f"B={B} t={t}")
+        # depth: the oracle's codes supplied everywhere, so every position's logits compare
+        p.ctx.reset()
+        st = p.orc.new_stream()
+        ids = I.make_ids(s, 2, seed=75)[:, 0]
+        for t in range(2):
+            gh, _, _ = p.gpu_frame(ids[t:t + 1])
+            rh, _, _, rt = st.step(ids[t])
+            sup = np.full(s.dep_steps, -1, np.int32)
+            ol, oc = p.orc.depformer_step(rh, int(rt), sup)
+            p.ctx.depformer_step(1, hidden=p.hidden, text_tok=np.array([int(rt)], np.int32),
+                                 supplied=oc.astype(np.int32)[None].copy(), logits=p.dlogits, codes=p.dcodes)
+            p.torch.cuda.synchronize()
+            gl = p.dlogits[0].double().cpu().numpy()
+            for q in range(s.dep_steps):
+                assert logits_rel_l2(gl[q], ol[q]) <= 1e-2, (t, q)
+    finally:
+        p.close()
