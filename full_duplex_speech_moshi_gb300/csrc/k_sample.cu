@@ -7,10 +7,16 @@
 //  * every logit gets the unique 64-bit key (order-preserving bits of the fp32 value,
 //    then the complement of its index), so "larger logit, then lower index" is plain key
 //    order and the top-k set has no ties;
-//  * the k-th largest key is found exactly by an 8-pass radix select (8 bits per pass,
-//    one shared histogram, warp-aggregated increments); the row is staged in shared
-//    memory when it fits (text head: 32000 logits = 125 KB);
-//  * the k survivors are sorted (bitonic, descending), weighted exp((l - l_max) / T) and
+//  * a short list surely holding the top k: with M the largest logit, the keys within
+//    DELTA of M outrank all others, so the smallest DELTA of a geometric ladder
+//    (0.25 * 2^j) admitting at least k (and at most 4096) keys gives it, in three
+//    cheap passes over the row (max, ladder counts, gather); a list of at most 1024 keys
+//    is ranked directly (each key counts the larger ones);
+//  * otherwise (many near-equal logits) the k-th largest key is found exactly by an
+//    8-pass radix select (8 bits per pass, per-warp histograms) over the list or the
+//    row, and the k survivors are ranked;
+//  * the row is staged in shared memory when it fits (text head: 32000 logits = 125 KB);
+//  * the k survivors, in descending order, are weighted exp((l - l_max) / T) and
 //    prefix-summed; u = (first word of Philox4x64-10 >> 40) * 2^-24 with key (seed, 0)
 //    and counter (frame position, row, substep, 0) -- Salmon, Moraes, Dror, Shaw,
 //    "Parallel random numbers: as easy as 1, 2, 3" (SC'11); the pick is the first
@@ -23,9 +29,24 @@
 namespace pm {
 namespace {
 
-constexpr int NT = 1024;  // threads per CTA (also the largest top-k)
+constexpr int NT = 1024;        // threads per CTA (also the largest top-k)
+constexpr int KEY_LIST = 4096;  // keys the selection gathers into its shared list
+constexpr int NLAD = 13;        // ladder of logit distances below the maximum
+
+// rung j of the distance ladder: 0.25 * 2^j, the last rung unbounded
+__device__ __forceinline__ float ladder(int j) { return j == NLAD - 1 ? INFINITY : ldexpf(0.25f, j); }
 
 __device__ __forceinline__ unsigned long long logit_key(float v, int i) { return pack_argmax(v, (uint32_t)i); }
+
+// slot for this lane in a shared list when `take`: one atomic per warp on the list count
+__device__ __forceinline__ int warp_append_slot(bool take, int* count) {
+    const unsigned int m = __ballot_sync(0xffffffffu, take);
+    const int lane = threadIdx.x & 31;
+    int base = 0;
+    if (m && lane == __ffs(m) - 1) base = atomicAdd(count, __popc(m));
+    base = __shfl_sync(0xffffffffu, base, m ? __ffs(m) - 1 : 0);
+    return base + __popc(m & ((1u << lane) - 1u));
+}
 
 // Philox4x64-10 block; returns the first output word
 __device__ __forceinline__ unsigned long long philox4x64_w0(unsigned long long c0, unsigned long long c1,
@@ -52,12 +73,17 @@ __device__ __forceinline__ unsigned long long philox4x64_w0(unsigned long long c
 
 __global__ void __launch_bounds__(NT) k_sample(const SampleParams p) {
     extern __shared__ float s_row[];  // staged logits (when p.stage)
+    __shared__ unsigned int s_whist[NT / 32][256];  // one histogram per warp (no cross-warp contention)
     __shared__ unsigned int s_hist[256];
     __shared__ unsigned long long s_cand[NT];
     __shared__ float s_scan[NT / 32];
     __shared__ unsigned long long s_red[NT / 32];
-    __shared__ int s_bin, s_above, s_cnt, s_pick, s_skip;
-    __shared__ float s_u, s_total;
+    __shared__ unsigned long long s_keys[KEY_LIST];
+    __shared__ int s_bin, s_above, s_inbin, s_cnt, s_pick, s_skip;
+    __shared__ float s_u, s_total, s_maxv;
+    __shared__ float s_redf[NT / 32];
+    __shared__ unsigned int s_lad[NLAD];
+    __shared__ int s_rung;
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -120,93 +146,179 @@ __global__ void __launch_bounds__(NT) k_sample(const SampleParams p) {
         __syncthreads();
         tok = s_pick;
     } else {
-        // ---- exact k-th largest key: 8-pass radix select ----
-        unsigned long long prefix = 0ull, mask = 0ull;
-        int kk = k;  // rank still to find among the keys matching the prefix
-        for (int pass = 0; pass < 8; ++pass) {
-            const int shift = 56 - 8 * pass;
-            for (int i = tid; i < 256; i += NT) s_hist[i] = 0u;
-            __syncthreads();
+        // ---- a short list that surely holds the top k ----
+        // With M the largest logit, every key whose logit is within DELTA of M outranks
+        // every key outside, so the smallest DELTA of a geometric ladder that admits at
+        // least k keys (and at most the list capacity) gives a list containing the top k.
+        float mx = -INFINITY;
+        for (int i = tid; i < V; i += NT) mx = fmaxf(mx, row[i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) s_redf[warp] = mx;
+        __syncthreads();
+        if (tid < 32) {
+            float v = s_redf[tid];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (tid == 0) s_maxv = v;
+        }
+        for (int j = tid; j < NLAD; j += NT) s_lad[j] = 0u;
+        __syncthreads();
+        const float M = s_maxv;
+        unsigned int cnt[NLAD];
+#pragma unroll
+        for (int j = 0; j < NLAD; ++j) cnt[j] = 0u;
+        for (int i = tid; i < V; i += NT) {
+            const float d = M - row[i];
+#pragma unroll
+            for (int j = 0; j < NLAD; ++j) cnt[j] += (d <= ladder(j)) ? 1u : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < NLAD; ++j) {
+            unsigned int c = cnt[j];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+            if (lane == 0) atomicAdd(&s_lad[j], c);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int pick = -1;
+            for (int j = 0; j < NLAD; ++j)
+                if (s_lad[j] >= (unsigned int)k) {
+                    if (s_lad[j] <= (unsigned int)KEY_LIST) pick = j;
+                    break;
+                }
+            s_rung = pick;
+            s_cnt = 0;
+        }
+        __syncthreads();
+        int listed = -1;  // keys in s_keys (-1: the radix select scans the row)
+        if (s_rung >= 0) {
+            const float delta = ladder(s_rung);
             for (int i0 = 0; i0 < V; i0 += NT) {
                 const int i = i0 + tid;
-                bool in = false;
-                unsigned int bin = 0u;
-                if (i < V) {
-                    const unsigned long long key = logit_key(row[i], i);
-                    in = (key & mask) == prefix;
-                    bin = (unsigned int)(key >> shift) & 255u;
-                }
-                const unsigned int act = __ballot_sync(0xffffffffu, in);
-                if (in) {
-                    const unsigned int same = __match_any_sync(act, bin);
-                    if ((__ffs(same) - 1) == lane) atomicAdd(&s_hist[bin], (unsigned int)__popc(same));
-                }
+                const float v = i < V ? row[i] : 0.0f;
+                const bool take = i < V && (M - v) <= delta;
+                const int slot = warp_append_slot(take, &s_cnt);
+                if (take) s_keys[slot] = logit_key(v, i);
             }
             __syncthreads();
-            if (warp == 0) {
-                // bins from the top: lane l holds bins 255 - 8l .. 248 - 8l
-                unsigned int c[8], sum = 0u;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    c[j] = s_hist[255 - (lane * 8 + j)];
-                    sum += c[j];
-                }
-                unsigned int incl = sum;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned int t = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += t;
-                }
-                const unsigned int excl = incl - sum;
-                if (excl < (unsigned int)kk && (unsigned int)kk <= incl) {
-                    unsigned int run = excl;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (run + c[j] >= (unsigned int)kk) {
-                            s_bin = 255 - (lane * 8 + j);
-                            s_above = (int)run;
-                            break;
-                        }
-                        run += c[j];
+            listed = s_cnt;
+        }
+        if (listed >= 0 && listed <= NT) {
+            // ---- rank the list directly: key ranks are unique ----
+            if (tid < listed) {
+                const unsigned long long key = s_keys[tid];
+                int rank = 0;
+                for (int i = 0; i < listed; ++i) rank += (s_keys[i] > key) ? 1 : 0;
+                if (rank < k) s_cand[rank] = key;
+            }
+            __syncthreads();
+        } else {
+            // ---- exact k-th largest key: 8-pass radix select (over the list, or over the
+            // row until few enough keys match the prefix to gather them) ----
+            unsigned long long prefix = 0ull, mask = 0ull;
+            int kk = k;  // rank still to find among the keys matching the prefix
+            for (int pass = 0; pass < 8; ++pass) {
+                const int shift = 56 - 8 * pass;
+                for (int i = lane; i < 256; i += 32) s_whist[warp][i] = 0u;
+                __syncthreads();
+                const int n_scan = listed < 0 ? V : listed;
+                for (int i0 = 0; i0 < n_scan; i0 += NT) {
+                    const int i = i0 + tid;
+                    bool in = false;
+                    unsigned int bin = 0u;
+                    if (i < n_scan) {
+                        const unsigned long long key = listed < 0 ? logit_key(row[i], i) : s_keys[i];
+                        in = (key & mask) == prefix;
+                        bin = (unsigned int)(key >> shift) & 255u;
                     }
-                }
-            }
-            __syncthreads();
-            prefix |= (unsigned long long)s_bin << shift;
-            mask |= 0xFFull << shift;
-            kk -= s_above;
-            __syncthreads();
-        }
-        // ---- the k survivors (keys >= the k-th largest), sorted descending ----
-        if (tid == 0) s_cnt = 0;
-        __syncthreads();
-        for (int i = tid; i < V; i += NT) {
-            const unsigned long long key = logit_key(row[i], i);
-            if (key >= prefix) {
-                const int slot = atomicAdd(&s_cnt, 1);
-                if (slot < NT) s_cand[slot] = key;
-            }
-        }
-        __syncthreads();
-        int P = 1;
-        while (P < k) P <<= 1;
-        for (int i = k + tid; i < P; i += NT) s_cand[i] = 0ull;
-        __syncthreads();
-        for (int size = 2; size <= P; size <<= 1) {
-            for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                for (int i = tid; i < P; i += NT) {
-                    const int j = i ^ stride;
-                    if (j > i) {
-                        const bool desc = (i & size) == 0;
-                        const unsigned long long a = s_cand[i], c = s_cand[j];
-                        if (desc ? (a < c) : (a > c)) {
-                            s_cand[i] = c;
-                            s_cand[j] = a;
+                    const unsigned int act = __ballot_sync(0xffffffffu, in);
+                    if (in) {
+                        // one add when the warp's keys share the bin, else one per key
+                        const unsigned int b0 = __shfl_sync(act, bin, __ffs(act) - 1);
+                        if (__all_sync(act, bin == b0)) {
+                            if ((__ffs(act) - 1) == lane) s_whist[warp][b0] += (unsigned int)__popc(act);
+                        } else {
+                            atomicAdd(&s_whist[warp][bin], 1u);
                         }
                     }
                 }
                 __syncthreads();
+                for (int i = tid; i < 256; i += NT) {
+                    unsigned int t = 0u;
+                    for (int w = 0; w < NT / 32; ++w) t += s_whist[w][i];
+                    s_hist[i] = t;
+                }
+                __syncthreads();
+                if (warp == 0) {
+                    // bins from the top: lane l holds bins 255 - 8l .. 248 - 8l
+                    unsigned int c[8], sum = 0u;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        c[j] = s_hist[255 - (lane * 8 + j)];
+                        sum += c[j];
+                    }
+                    unsigned int incl = sum;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const unsigned int t = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += t;
+                    }
+                    const unsigned int excl = incl - sum;
+                    if (excl < (unsigned int)kk && (unsigned int)kk <= incl) {
+                        unsigned int run = excl;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            if (run + c[j] >= (unsigned int)kk) {
+                                s_bin = 255 - (lane * 8 + j);
+                                s_above = (int)run;
+                                s_inbin = (int)c[j];
+                                break;
+                            }
+                            run += c[j];
+                        }
+                    }
+                }
+                __syncthreads();
+                prefix |= (unsigned long long)s_bin << shift;
+                mask |= 0xFFull << shift;
+                kk -= s_above;
+                if (listed < 0 && pass < 7 && s_inbin <= KEY_LIST) {
+                    // gather the keys matching the new prefix (their order is irrelevant)
+                    if (tid == 0) s_cnt = 0;
+                    __syncthreads();
+                    for (int i0 = 0; i0 < V; i0 += NT) {
+                        const int i = i0 + tid;
+                        const unsigned long long key = i < V ? logit_key(row[i], i) : 0ull;
+                        const bool take = i < V && (key & mask) == prefix;
+                        const int slot = warp_append_slot(take, &s_cnt);
+                        if (take) s_keys[slot] = key;
+                    }
+                    __syncthreads();
+                    listed = s_cnt;
+                }
+                __syncthreads();
             }
+            // ---- the k survivors (keys >= the k-th largest), ranked into order: every key
+            // above the prefix's bins is one, wherever it was scanned from ----
+            if (tid == 0) s_cnt = 0;
+            __syncthreads();
+            for (int i0 = 0; i0 < V; i0 += NT) {
+                const int i = i0 + tid;
+                const unsigned long long key = i < V ? logit_key(row[i], i) : 0ull;
+                const bool take = i < V && key >= prefix;
+                const int slot = warp_append_slot(take, &s_cnt);
+                if (take && slot < NT) s_keys[slot] = key;
+            }
+            __syncthreads();
+            if (tid < k) {
+                const unsigned long long key = s_keys[tid];
+                int rank = 0;
+                for (int i = 0; i < k; ++i) rank += (s_keys[i] > key) ? 1 : 0;
+                s_cand[rank] = key;
+            }
+            __syncthreads();
         }
         // ---- weights, running sums, the draw ----
         const int top_idx = (int)unpack_argmax_index(s_cand[0]);

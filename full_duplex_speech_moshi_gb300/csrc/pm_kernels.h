@@ -154,8 +154,9 @@ enum SampleMode {
     SM_TEXT = 1,   // the frame's text token from the head's logits (context settings)
     SM_DEPTH = 2   // depth position q's code where none is supplied (context settings)
 };
-// rows of up to this many logits are staged in shared memory (192 KB)
-#define PM_SAMPLE_STAGE_MAX 49152
+// rows of up to this many logits are staged in shared memory (128 KB; the kernel's
+// static shared memory takes another 75 KB)
+#define PM_SAMPLE_STAGE_MAX 32768
 // largest top-k the sampler serves (one survivor per thread)
 #define PM_SAMPLE_MAX_TOP_K 1024
 struct SampleParams {
