@@ -65,6 +65,24 @@ def test_sampler_matches_oracle_on_random_logits(pair, V, k, T):
     assert compared >= B - 2
 
 
+def test_sampler_flat_rows_take_the_radix_path(pair):
+    """Thousands of logits within a quarter of the maximum: the short-list rule cannot
+    apply and the exact radix select over the whole row runs."""
+    rng = np.random.default_rng(77)
+    B, V, k, T = 16, 32000, 25, 0.7
+    lg = (1.0 + rng.standard_normal((B, V)) * 1e-3).astype(np.float32)
+    got = _gpu_sample(pair, lg, T, k, 99, 5, 0)
+    compared = 0
+    for b in range(B):
+        tok, margin, gap = O.sample_topk(lg[b].astype(np.float64), T, k, 99, 5, b, 0)
+        keep = set(np.lexsort((np.arange(V), -lg[b].astype(np.float64)))[:k].tolist())
+        assert int(got[b]) in keep
+        if margin > MARGIN_SAME_LOGITS and gap > 0:
+            assert int(got[b]) == tok
+            compared += 1
+    assert compared >= B - 2
+
+
 def test_sampler_greedy_limits_and_ties(pair):
     lg = np.zeros((4, 300), np.float32)
     lg[:, 17] = 2.0
