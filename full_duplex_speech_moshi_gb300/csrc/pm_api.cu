@@ -1143,6 +1143,110 @@ extern "C" pm_status pm_get_positions(pm_ctx* c, int32_t* pos_out) {
     return PM_OK;
 }
 
+// ------------------------------------------------------------------------------------
+// stream snapshots
+// ------------------------------------------------------------------------------------
+namespace {
+constexpr uint32_t kSnapMagic = 0x4E534D50u;  // "PMSN"
+constexpr uint32_t kSnapVersion = 1u;
+constexpr size_t kSnapHeader = 1024;          // header bytes before the KV rows
+// header layout (bytes): [0, 64) identity and shape, 64 pos, 68 first_pos, 72 n_slots,
+// [128, 128 + 4 * 4 * PM_MAX_STREAMS_DEV) delay ring, then PM_MAX_STREAMS_DEV selections
+constexpr size_t kSnapRing = 128;
+constexpr size_t kSnapSel = kSnapRing + 4u * 4u * PM_MAX_STREAMS_DEV;
+struct SnapIdent {
+    uint32_t magic, version;
+    int32_t n_layers, H, dh, ctx, n_streams, D;
+};
+static_assert(kSnapSel + 4u * PM_MAX_STREAMS_DEV <= kSnapHeader, "snapshot header overflow");
+}  // namespace
+
+extern "C" size_t pm_snapshot_bytes(const pm_config* f) {
+    if (!f) return 0;
+    return kSnapHeader + (size_t)f->n_layers * 2u * f->H * f->ctx * f->dh * 2u;
+}
+
+// one stream's KV rows of slots [0, n) <-> the snapshot's [layer][K/V][head][slot][dh]
+static pm_status snap_kv(pm_ctx* c, int b, uint8_t* snap, int n, bool to_snap) {
+    const pm_config& f = c->cfg;
+    const size_t row = (size_t)f.dh * 2u;
+    for (int l = 0; l < f.n_layers; ++l)
+        for (int kv = 0; kv < 2; ++kv) {
+            uint8_t* cache = reinterpret_cast<uint8_t*>(c->kv) +
+                             ((((size_t)(2 * l + kv) * f.B_max + b) * f.H) * f.ctx) * row;
+            uint8_t* s = snap + kSnapHeader + ((size_t)(2 * l + kv) * f.H) * n * row;
+            if (to_snap)
+                PM_CUDA(cudaMemcpy2DAsync(s, n * row, cache, f.ctx * row, n * row, f.H, cudaMemcpyDeviceToDevice,
+                                          c->stream));
+            else
+                PM_CUDA(cudaMemcpy2DAsync(cache, f.ctx * row, s, n * row, n * row, f.H, cudaMemcpyDeviceToDevice,
+                                          c->stream));
+        }
+    return PM_OK;
+}
+
+extern "C" pm_status pm_snapshot(pm_ctx* c, int b, void* dst) {
+    if (!c) return PM_ERR_ARG;
+    const pm_config& f = c->cfg;
+    if (b < 0 || b >= f.B_max || !dst || !aligned16(dst)) return fail(c, PM_ERR_ARG, "pm_snapshot: bad stream or dst");
+    PM_CUDA(cudaSetDevice(c->device));
+    if (!is_device_ptr(dst)) return fail(c, PM_ERR_ARG, "pm_snapshot: dst must be device memory");
+    int32_t pf[2];
+    PM_CUDA(cudaStreamSynchronize(c->stream));
+    PM_CUDA(cudaMemcpy(&pf[0], c->st.pos + b, 4, cudaMemcpyDeviceToHost));
+    PM_CUDA(cudaMemcpy(&pf[1], c->st.first_pos + b, 4, cudaMemcpyDeviceToHost));
+    const int n = pf[0] < f.ctx ? pf[0] : f.ctx;
+    uint8_t hdr[128];
+    memset(hdr, 0, sizeof hdr);
+    SnapIdent id{kSnapMagic, kSnapVersion, f.n_layers, f.H, f.dh, f.ctx, f.n_streams, f.D};
+    memcpy(hdr, &id, sizeof id);
+    const int32_t st3[3] = {pf[0], pf[1], n};
+    memcpy(hdr + 64, st3, sizeof st3);
+    uint8_t* d = static_cast<uint8_t*>(dst);
+    PM_CUDA(cudaMemcpyAsync(d, hdr, sizeof hdr, cudaMemcpyHostToDevice, c->stream));
+    PM_CUDA(cudaMemcpyAsync(d + kSnapRing, c->st.ring + (size_t)b * 4 * PM_MAX_STREAMS_DEV,
+                            4u * 4u * PM_MAX_STREAMS_DEV, cudaMemcpyDeviceToDevice, c->stream));
+    PM_CUDA(cudaMemcpyAsync(d + kSnapSel, c->st.sel + (size_t)b * PM_MAX_STREAMS_DEV, 4u * PM_MAX_STREAMS_DEV,
+                            cudaMemcpyDeviceToDevice, c->stream));
+    pm_status st = snap_kv(c, b, d, n, true);
+    if (st) return st;
+    PM_CUDA(cudaStreamSynchronize(c->stream));
+    return PM_OK;
+}
+
+extern "C" pm_status pm_restore(pm_ctx* c, int b, const void* src) {
+    if (!c) return PM_ERR_ARG;
+    const pm_config& f = c->cfg;
+    if (b < 0 || b >= f.B_max || !src || !aligned16(src)) return fail(c, PM_ERR_ARG, "pm_restore: bad stream or src");
+    PM_CUDA(cudaSetDevice(c->device));
+    if (!is_device_ptr(src)) return fail(c, PM_ERR_ARG, "pm_restore: src must be device memory");
+    PM_CUDA(cudaStreamSynchronize(c->stream));
+    uint8_t hdr[128];
+    PM_CUDA(cudaMemcpy(hdr, src, sizeof hdr, cudaMemcpyDeviceToHost));
+    SnapIdent id;
+    memcpy(&id, hdr, sizeof id);
+    int32_t st3[3];
+    memcpy(st3, hdr + 64, sizeof st3);
+    if (id.magic != kSnapMagic || id.version != kSnapVersion)
+        return fail(c, PM_ERR_ARG, "pm_restore: not a snapshot");
+    if (id.n_layers != f.n_layers || id.H != f.H || id.dh != f.dh || id.ctx != f.ctx || id.n_streams != f.n_streams ||
+        id.D != f.D)
+        return fail(c, PM_ERR_ARG, "pm_restore: snapshot of another configuration");
+    if (st3[0] < 0 || st3[1] < 0 || st3[1] > st3[0] || st3[2] != (st3[0] < f.ctx ? st3[0] : f.ctx))
+        return fail(c, PM_ERR_ARG, "pm_restore: inconsistent snapshot header");
+    const uint8_t* s = static_cast<const uint8_t*>(src);
+    PM_CUDA(cudaMemcpyAsync(c->st.pos + b, s + 64, 4, cudaMemcpyDeviceToDevice, c->stream));
+    PM_CUDA(cudaMemcpyAsync(c->st.first_pos + b, s + 68, 4, cudaMemcpyDeviceToDevice, c->stream));
+    PM_CUDA(cudaMemcpyAsync(c->st.ring + (size_t)b * 4 * PM_MAX_STREAMS_DEV, s + kSnapRing,
+                            4u * 4u * PM_MAX_STREAMS_DEV, cudaMemcpyDeviceToDevice, c->stream));
+    PM_CUDA(cudaMemcpyAsync(c->st.sel + (size_t)b * PM_MAX_STREAMS_DEV, s + kSnapSel, 4u * PM_MAX_STREAMS_DEV,
+                            cudaMemcpyDeviceToDevice, c->stream));
+    pm_status st = snap_kv(c, b, const_cast<uint8_t*>(s), st3[2], false);
+    if (st) return st;
+    PM_CUDA(cudaStreamSynchronize(c->stream));
+    return PM_OK;
+}
+
 extern "C" pm_status pm_device_status(pm_ctx* c) {
     if (!c) return PM_ERR_ARG;
     PM_CUDA(cudaSetDevice(c->device));

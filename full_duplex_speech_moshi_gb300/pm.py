@@ -22,7 +22,8 @@ STATUS_NAMES = {0: "PM_OK", 1: "PM_ERR_ARG", 2: "PM_ERR_INVALID_ID", 3: "PM_ERR_
 # every symbol include/pm.h declares
 EXPORTS = ["pm_kv_cache_bytes", "pm_create", "pm_reset", "pm_set_positions", "pm_get_positions",
            "pm_frame_step", "pm_depformer_step", "pm_profile_frame", "pm_device_status", "pm_last_error",
-           "pm_destroy", "pm_text_head_noalloc", "pm_set_sampling", "pm_sample"]
+           "pm_destroy", "pm_text_head_noalloc", "pm_set_sampling", "pm_sample", "pm_snapshot_bytes",
+           "pm_snapshot", "pm_restore"]
 KERNEL_KINDS = {0: "embed", 1: "qkv_rope", 2: "attention", 3: "out_proj", 4: "linear_in_swiglu",
                 5: "linear_out", 6: "text_head", 7: "frame_program", 8: "text_sample"}
 
@@ -96,6 +97,12 @@ def lib():
         L.pm_sample.restype = C.c_int
         L.pm_sample.argtypes = [vp, C.c_int, vp, C.c_int, C.c_int, C.c_float, C.c_int, C.c_ulonglong,
                                 C.c_longlong, C.c_int, vp]
+        L.pm_snapshot_bytes.restype = C.c_size_t
+        L.pm_snapshot_bytes.argtypes = [C.POINTER(pm_config)]
+        L.pm_snapshot.restype = C.c_int
+        L.pm_snapshot.argtypes = [vp, C.c_int, vp]
+        L.pm_restore.restype = C.c_int
+        L.pm_restore.argtypes = [vp, C.c_int, vp]
         L.pm_destroy.restype = None
         L.pm_destroy.argtypes = [vp]
         _lib = L
@@ -248,6 +255,16 @@ class Context:
         """Standalone sampling of B rows of device logits into `tokens` (device int32)."""
         self._check(self.L.pm_sample(self.h, int(B), _ptr(logits), int(V), int(ld), float(temperature), int(top_k),
                                      int(seed) & (2**64 - 1), int(position), int(substep), _ptr(tokens)))
+
+    def snapshot_bytes(self) -> int:
+        return int(self.L.pm_snapshot_bytes(C.byref(self.cfg)))
+
+    def snapshot(self, stream: int, dst) -> None:
+        """Stream `stream`'s decode state into the device buffer `dst`."""
+        self._check(self.L.pm_snapshot(self.h, int(stream), _ptr(dst)))
+
+    def restore(self, stream: int, src) -> None:
+        self._check(self.L.pm_restore(self.h, int(stream), _ptr(src)))
 
     def profile_frame(self, B: int, ids, text_logits=None, hidden=None, text_token=None):
         """One frame with per-launch device times: list of (kind name, ms)."""

@@ -227,6 +227,25 @@ pm_status pm_set_sampling(pm_ctx* ctx, float text_temperature, int text_top_k, f
 pm_status pm_sample(pm_ctx* ctx, int B, const float* logits, int V, int ld, float temperature, int top_k,
                     unsigned long long seed, long long position, int substep, int32_t* tokens);
 
+/* Stream snapshots (the startup voice prompt is replayed once and its state reused:
+ * "PersonaPlex native LM audit", section 9, cached voice prompts restore temporal history
+ * and the token ring).  A snapshot holds one stream's position, first position since
+ * reset, delay history, last selections and the KV rows of every ring slot that holds a
+ * position (min(position, ctx) slots).  pm_snapshot_bytes: the buffer a snapshot of this
+ * configuration needs at most (header + all ctx slots). */
+size_t pm_snapshot_bytes(const pm_config* cfg);
+
+/* Copy stream `stream`'s decode state into `dst` (device memory, pm_snapshot_bytes bytes,
+ * 16-byte aligned).  Synchronises the context's stream (the position decides how many
+ * slots are copied). */
+pm_status pm_snapshot(pm_ctx* ctx, int stream, void* dst);
+
+/* Make stream `stream` continue exactly as the snapshotted stream would: state and KV rows
+ * from `src` (device memory written by pm_snapshot of a context with the same n_layers,
+ * H, dh, ctx and n_streams; PM_ERR_ARG otherwise).  The next frame is bit-identical to the
+ * snapshotted stream's next frame on the same path.  Synchronises the context's stream. */
+pm_status pm_restore(pm_ctx* ctx, int stream, const void* src);
+
 /* Synchronise the stream and return (and clear) any device-side error: an invalid ID
  * given in device memory (PM_ERR_INVALID_ID) or a bounded wait that ran out
  * (PM_ERR_TIMEOUT). */
