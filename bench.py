@@ -344,6 +344,19 @@ def main():
         ctx.set_sampling(0.0, 1, 0.0, 1, 0)
         extras["sampled_frames_per_s"] = n4 / (a3.elapsed_time(b3) / 1000.0)
         extras["sampled_with_depformer_frames_per_s"] = n4 / (a4.elapsed_time(b4) / 1000.0)
+        # prefill of a 3000-frame history (the long-context workload's priming) in passes of
+        # 64 frames, from reset
+        ctx.reset()
+        ids_pf = torch.from_numpy(I.make_ids(s, s.ctx, seed=2003)[:, 0].copy()).to(dev)
+        ctx.prefill(0, 128, ids_pf[:128], logits, hidden, token)  # capture the pass graphs
+        ctx.reset()
+        torch.cuda.synchronize()
+        a5, b5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a5.record(stream)
+        ctx.prefill(0, s.ctx, ids_pf, logits, hidden, token)
+        b5.record(stream)
+        torch.cuda.synchronize()
+        extras["prefill_frames_per_s"] = s.ctx / (a5.elapsed_time(b5) / 1000.0)
     ctx.close()
     del kv1
     torch.cuda.empty_cache()

@@ -27,18 +27,25 @@ __global__ void __launch_bounds__(128) k_embed(const EmbedParams p) {
     const int b = blockIdx.y;
     const int tid = threadIdx.x;
     const int S = p.n_streams;
+    const bool seq = p.resolved != nullptr;  // prefill: rows are frames of one stream
 
-    // validate every row's IDs (cheap: B * 17 values) so all CTAs agree on the abort
     int bad = 0;
-    for (int i = tid; i < p.B * S; i += blockDim.x) {
-        const int bb = i / S, k = i % S;
-        int id = p.io->ids[i];
-        if (id == -3) id = p.st.sel[(size_t)bb * PM_MAX_STREAMS_DEV + k];
-        if (id < -1 || id >= p.rows[k]) bad = 1;
+    if (seq) {
+        bad = *(volatile uint32_t*)&p.st.status[1] != 0u;  // set by k_seq_prepare
+    } else {
+        // validate every row's IDs (cheap: B * 17 values) so all CTAs agree on the abort
+        for (int i = tid; i < p.B * S; i += blockDim.x) {
+            const int bb = i / S, k = i % S;
+            int id = p.io->ids[i];
+            if (id == -3) id = p.st.sel[(size_t)bb * PM_MAX_STREAMS_DEV + k];
+            if (id < -1 || id >= p.rows[k]) bad = 1;
+        }
+        bad = __syncthreads_or(bad);
     }
-    bad = __syncthreads_or(bad);
 
-    if (tid < S) {
+    if (seq) {
+        if (tid < S) s_in[tid] = p.resolved[(size_t)b * S + tid];
+    } else if (tid < S) {
         const int k = tid;
         int id = p.io->ids[(size_t)b * S + k];
         if (id == -3) id = p.st.sel[(size_t)b * PM_MAX_STREAMS_DEV + k];
@@ -54,7 +61,7 @@ __global__ void __launch_bounds__(128) k_embed(const EmbedParams p) {
         s_in[k] = in;
         if (!bad && blockIdx.x == 0) p.st.ring[((size_t)b * 4 + (pos & 3)) * PM_MAX_STREAMS_DEV + k] = id;
     }
-    if (blockIdx.x == 0 && b == 0 && tid == 0) {
+    if (!seq && blockIdx.x == 0 && b == 0 && tid == 0) {
         p.st.status[1] = bad ? 1u : 0u;
         if (bad) set_status(p.st.status, PM_DEV_ERR_INVALID_ID);
     }
@@ -62,8 +69,9 @@ __global__ void __launch_bounds__(128) k_embed(const EmbedParams p) {
     if (bad) return;
     if (blockIdx.x == 0 && tid < p.dh / 2) {
         // RoPE angles of this frame: position (integer) times frequency, in double
+        const int pos = seq ? p.st.pos[p.io->seq_stream] + b : p.st.pos[b];
         double sn, cs;
-        sincos((double)p.st.pos[b] * p.rope_freq[tid], &sn, &cs);
+        sincos((double)pos * p.rope_freq[tid], &sn, &cs);
         p.rope_tab[(size_t)b * (p.dh / 2) + tid] = make_float2((float)cs, (float)sn);
     }
 

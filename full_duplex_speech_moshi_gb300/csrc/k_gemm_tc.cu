@@ -236,15 +236,18 @@ __global__ void __launch_bounds__(192, 1)
         }
         epi_bar();
         if (EPI == TE_HEAD) {
-            // hidden state h = alpha * x * inv for this CTA's share of the columns
+            // hidden state h = alpha * x * inv for this CTA's share of the columns (a
+            // prefill: its last frame's, as stream seq_stream's)
             const int c0 = (int)((long long)c * p.D / G), c1 = (int)((long long)(c + 1) * p.D / G);
-            for (int b = 0; b < p.B && !aborted; ++b)
+            for (int b = p.seq ? p.B - 1 : 0; b < p.B && !aborted; ++b) {
+                const int bs = p.seq ? p.io->seq_stream : b, bo = p.seq ? 0 : b;
                 for (int i = c0 + t; i < c1; i += 128) {
                     const float hv = p.x_resid[(size_t)b * p.D + i] * inv[b] *
                                      __uint_as_float((uint32_t)p.alpha[i] << 16);
-                    if (p.h_internal) p.h_internal[(size_t)b * p.D + i] = hv;
-                    if (p.io->hidden) p.io->hidden[(size_t)b * p.D + i] = hv;
+                    if (p.h_internal) p.h_internal[(size_t)bs * p.D + i] = hv;
+                    if (p.io->hidden) p.io->hidden[(size_t)bo * p.D + i] = hv;
                 }
+            }
         }
         if (n > 0) {
             const int m_first = (int)(w0 / p.nk), m_last = (int)((w1 - 1) / p.nk);
@@ -378,7 +381,10 @@ __global__ void __launch_bounds__(192, 1)
                             const int b = b0 + j;
                             cs[j] = (sec < 2 && b < p.B) ? p.rope_tab[(size_t)b * (p.dh / 2) + (d >> 1)]
                                                          : make_float2(1.f, 0.f);
-                            slot[j] = (sec > 0 && b < p.B) ? p.st.pos[b] % p.ctx : 0;
+                            // a prefill's row b is frame pos + b of stream seq_stream
+                            slot[j] = (sec > 0 && b < p.B)
+                                          ? (p.seq ? p.st.pos[p.io->seq_stream] + b : p.st.pos[b]) % p.ctx
+                                          : 0;
                         }
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
@@ -391,6 +397,9 @@ __global__ void __launch_bounds__(192, 1)
                             if (aborted) continue;
                             if (sec == 0) {
                                 p.y[(size_t)b * p.y_stride + idx] = o;
+                            } else if (p.seq) {
+                                // a prefill's K/V stay out of the ring until its attention ran
+                                p.kv_new[(((size_t)(sec - 1) * p.B + b) * p.H + h) * p.dh + d] = f32_to_bf16_rne(o);
                             } else {
                                 uint16_t* cache = (sec == 1) ? p.kc : p.vc;
                                 cache[(((size_t)b * p.H + h) * p.ctx + slot[j]) * p.dh + d] = f32_to_bf16_rne(o);
@@ -400,12 +409,16 @@ __global__ void __launch_bounds__(192, 1)
                 } else if (EPI == TE_HEAD) {
                     const int r = m * 128 + t;
                     float* out = p.io->logits;
+                    // a prefill reports only its last frame, as stream seq_stream's
+                    const int b_lo = p.seq ? p.B - 1 : 0;
+                    const int s_seq = p.seq ? p.io->seq_stream : 0;
 #pragma unroll
                     for (int b = 0; b < NPAD; ++b) {
                         unsigned long long key = 0ull;
-                        if (b < p.B && r < p.n_rows) {
-                            if (out && !aborted) out[(size_t)b * p.n_rows + r] = v[b];
-                            if (p.logits_copy && !aborted) p.logits_copy[(size_t)b * p.n_rows + r] = v[b];
+                        if (b >= b_lo && b < p.B && r < p.n_rows) {
+                            const int bo = p.seq ? 0 : b, bs = p.seq ? s_seq : b;
+                            if (out && !aborted) out[(size_t)bo * p.n_rows + r] = v[b];
+                            if (p.logits_copy && !aborted) p.logits_copy[(size_t)bs * p.n_rows + r] = v[b];
                             key = pack_argmax(v[b], (uint32_t)r);
                         }
 #pragma unroll
@@ -413,10 +426,10 @@ __global__ void __launch_bounds__(192, 1)
                         if (lane == 0) red64[warp * NPAD + b] = key;
                     }
                     epi_bar();
-                    if (t < p.B) {
+                    if (t >= b_lo && t < p.B) {
                         unsigned long long k4 = umax64(umax64(red64[t], red64[NPAD + t]),
                                                        umax64(red64[2 * NPAD + t], red64[3 * NPAD + t]));
-                        atomicMax(&p.st.amax[t], k4);
+                        atomicMax(&p.st.amax[p.seq ? s_seq : t], k4);
                     }
                     __threadfence();
                     epi_bar();
@@ -427,13 +440,14 @@ __global__ void __launch_bounds__(192, 1)
                     epi_bar();
                     if (flags[1]) {
                         __threadfence();
-                        if (t < p.B) {
-                            const unsigned long long key = atomicExch(&p.st.amax[t], 0ull);
+                        if (t >= b_lo && t < p.B) {
+                            const int bs = p.seq ? s_seq : t;
+                            const unsigned long long key = atomicExch(&p.st.amax[bs], 0ull);
                             const int32_t am = (int32_t)unpack_argmax_index(key);
                             if (!aborted) {
-                                if (p.io->token) p.io->token[t] = am;
-                                p.st.sel[(size_t)t * PM_MAX_STREAMS_DEV + 0] = am;
-                                p.st.pos[t] += 1;
+                                if (p.io->token) p.io->token[p.seq ? 0 : t] = am;
+                                p.st.sel[(size_t)bs * PM_MAX_STREAMS_DEV + 0] = am;
+                                p.st.pos[bs] += p.seq ? p.B : 1;
                             }
                         }
                         if (t == 0) p.st.head_count[0] = 0u;

@@ -85,7 +85,8 @@ __global__ void __launch_bounds__(NT) k_sample(const SampleParams p) {
     __shared__ unsigned int s_lad[NLAD];
     __shared__ int s_rung;
 
-    const int b = blockIdx.x;
+    // a prefill's text token is stream seq_stream's (one row)
+    const int b = p.seq ? p.io->seq_stream : (int)blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_trigger();
     pdl_wait();
@@ -370,7 +371,7 @@ __global__ void __launch_bounds__(NT) k_sample(const SampleParams p) {
     if (p.mode == SM_PLAIN) {
         p.tokens[b] = tok;
     } else if (p.mode == SM_TEXT) {
-        if (p.io->token) p.io->token[b] = tok;
+        if (p.io->token) p.io->token[p.seq ? 0 : b] = tok;
         p.st.sel[(size_t)b * PM_MAX_STREAMS_DEV + 0] = tok;
     } else {
         p.st.dep_codes[(size_t)b * p.Q + p.q] = tok;

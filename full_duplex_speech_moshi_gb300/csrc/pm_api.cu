@@ -73,6 +73,12 @@ struct pm_ctx {
     float* slog = nullptr;    // [B_max][text_out]
     float* dslog = nullptr;   // [B_max][dep_card]
     bool text_smp = false, audio_smp = false;
+    // prefill: resolved inputs of a pass, attention partials and counters, graphs per T
+    int32_t* seq_resolved = nullptr;
+    float* seq_part = nullptr;
+    uint32_t* seq_count = nullptr;
+    uint16_t* seq_kv = nullptr;        // [2][PM_SEQ_MAX_ROWS][H][dh] a pass's K/V before commit
+    std::map<int, cudaGraphExec_t> prefill_graphs;
     // staging
     Staging slots[kStagingSlots];
     int next_slot = 0;
@@ -226,15 +232,16 @@ static pm_status mark(pm_ctx* c, cudaStream_t s, int kind) {
 }
 
 // the drawn text token replaces the head's greedy one (when text sampling is on)
-static pm_status record_text_sample(pm_ctx* c, int B, cudaStream_t s, bool pdl) {
+static pm_status record_text_sample(pm_ctx* c, int B, cudaStream_t s, bool pdl, bool seq = false) {
     if (!c->text_smp) return PM_OK;
     SampleParams sp;
     memset(&sp, 0, sizeof sp);
     sp.mode = SM_TEXT;
+    sp.seq = seq ? 1 : 0;  // a prefill draws only its last frame's token
     sp.logits = c->slog;
     sp.ld = c->cfg.text_out;
     sp.V = c->cfg.text_out;
-    sp.B = B;
+    sp.B = seq ? 1 : B;
     sp.cfg = c->scfg;
     sp.st = c->st;
     sp.io = reinterpret_cast<const FrameIO*>(c->io_region);
@@ -391,11 +398,27 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
 static int npad_for(int B) { return B <= 16 ? 16 : (B <= 32 ? 32 : 64); }
 
 // B >= 2: every projection on the tensor cores (k_gemm_tc), same kernel families and order
-static pm_status record_frame_tc(pm_ctx* c, int B, cudaStream_t s) {
+// `seq`: a prefill pass -- the B rows are frames pos .. pos+B-1 of stream io->seq_stream
+static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq) {
     const pm_config& f = c->cfg;
     const int D = f.D, F = f.ffn, npad = npad_for(B);
     if (npad > c->npad_max) return fail(c, PM_ERR_UNSUPPORTED, "batch larger than the tensor-core buffers");
     const bool pdl = c->prof_ev == nullptr;
+    if (seq) {
+        SeqPrepParams sp;
+        memset(&sp, 0, sizeof sp);
+        sp.io = reinterpret_cast<const FrameIO*>(c->io_region);
+        sp.st = c->st;
+        sp.resolved = c->seq_resolved;
+        sp.T = B;
+        sp.n_streams = f.n_streams;
+        for (int k = 0; k < f.n_streams; ++k) {
+            sp.rows[k] = (k == 0) ? f.text_in : f.audio_in;
+            sp.init_id[k] = (k == 0) ? f.init_text : f.init_audio;
+            sp.delays[k] = f.delays[k];
+        }
+        PM_CUDA(launch_seq_prepare(sp, s, false));
+    }
     EmbedParams ep;
     memset(&ep, 0, sizeof ep);
     for (int k = 0; k < f.n_streams; ++k) {
@@ -417,9 +440,10 @@ static pm_status record_frame_tc(pm_ctx* c, int B, cudaStream_t s) {
     ep.alpha = c->norm1[0];
     ep.ss = c->ss;
     ep.npad = npad;
+    ep.resolved = seq ? c->seq_resolved : nullptr;
     pm_status ms = mark(c, s, -1);
     if (ms) return ms;
-    PM_CUDA(launch_embed(ep, s, false));
+    PM_CUDA(launch_embed(ep, s, seq && pdl));
     if ((ms = mark(c, s, PM_KERNEL_EMBED))) return ms;
 
     CUtensorMap mx, mo, msb;
@@ -479,8 +503,33 @@ static pm_status record_frame_tc(pm_ctx* c, int B, cudaStream_t s) {
         p.vc = vc;
         p.rope_tab = c->rope_tab;
         p.nx = next_tc(c, D, D / 128, 0, npad);
+        p.seq = seq ? 1 : 0;
+        p.kv_new = c->seq_kv;
         pm_status ps = go(mq[l], mx, mwo[l], p, PM_KERNEL_QKV, "in_proj");
         if (ps) return ps;
+        if (seq) {
+            AttnSeqParams aq;
+            memset(&aq, 0, sizeof aq);
+            aq.q = c->q;
+            aq.kc = kc;
+            aq.vc = vc;
+            aq.kv_new = c->seq_kv;
+            aq.o = c->o;
+            aq.ob = c->ob;
+            aq.part = c->seq_part;
+            aq.count = c->seq_count;
+            aq.st = c->st;
+            aq.io = reinterpret_cast<const FrameIO*>(c->io_region);
+            aq.T = B;
+            aq.H = f.H;
+            aq.ctx = f.ctx;
+            aq.win = f.ctx - ((f.flags & PM_FLAG_PINNED_RING) ? 1 : 0);
+            aq.D = D;
+            aq.grid = 2 * c->num_sms;
+            aq.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dh));
+            PM_CUDA(launch_attn_seq(aq, s, pdl));
+            PM_CUDA(launch_seq_commit(aq, s, pdl));
+        }
         AttnParams ap;
         memset(&ap, 0, sizeof ap);
         ap.ob = c->ob;
@@ -499,7 +548,7 @@ static pm_status record_frame_tc(pm_ctx* c, int B, cudaStream_t s) {
         ap.grid = (B == 1 ? 4 : 16) * c->num_sms;
         ap.D = D;
         ap.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dh));
-        PM_CUDA(launch_attn(ap, s, pdl));
+        if (!seq) PM_CUDA(launch_attn(ap, s, pdl));
         if ((ms = mark(c, s, PM_KERNEL_ATTENTION))) return ms;
         // W_O + residual; emits bf16(norm2 alpha * y) and per-tile sums of y^2
         p = base(TE_RESIDUAL, D, D / 128, D);
@@ -540,10 +589,14 @@ static pm_status record_frame_tc(pm_ctx* c, int B, cudaStream_t s) {
     p.alpha = c->out_norm;
     p.nx = next_tc(c, D, 3 * D / 128, 0, npad);  // the next frame's first projection
     if (c->text_smp) p.logits_copy = c->slog;
+    p.seq = seq ? 1 : 0;
     pm_status hs = go(mh, mx, mq[0], p, PM_KERNEL_HEAD, "text_linear");
     if (hs) return hs;
-    return record_text_sample(c, B, s, pdl);
+    return record_text_sample(c, B, s, pdl, seq);
 }
+
+static pm_status record_frame_tc(pm_ctx* c, int B, cudaStream_t s) { return record_frame_tc_impl(c, B, s, false); }
+static pm_status record_prefill(pm_ctx* c, int T, cudaStream_t s) { return record_frame_tc_impl(c, T, s, true); }
 
 static pm_status record_depformer(pm_ctx* c, int B, cudaStream_t s) {
     const pm_config& f = c->cfg;
@@ -739,6 +792,7 @@ static void free_ctx(pm_ctx* c) {
     cudaSetDevice(c->device);
     for (auto& kv : c->frame_graphs) cudaGraphExecDestroy(kv.second);
     for (auto& kv : c->dep_graphs) cudaGraphExecDestroy(kv.second);
+    for (auto& kv : c->prefill_graphs) cudaGraphExecDestroy(kv.second);
     for (int i = 0; i < kStagingSlots; ++i) {
         if (c->slots[i].done) cudaEventDestroy(c->slots[i].done);
         if (c->slots[i].host) cudaFreeHost(c->slots[i].host);
@@ -854,28 +908,35 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     void* p_pos; void* p_first; void* p_ring; void* p_sel; void* p_amax; void* p_hc; void* p_status;
     void* p_damax; void* p_dcount; void* p_dcodes; void* p_dtok; void* p_dsup;
     void* p_io; void* p_dio; void *p_x, *p_q, *p_o, *p_s, *p_h, *p_part, *p_cnt, *p_freq, *p_dz, *p_dq,
-        *p_ds, *p_dkv, *p_rtab, *p_xb, *p_ob, *p_sb, *p_ss, *p_tcp, *p_tcc, *p_scfg, *p_slog, *p_dslog;
-    // tensor-core path scratch, sized from the plans of this configuration's projections
-    const int NP = BM >= 2 ? (BM <= 16 ? 16 : (BM <= 32 ? 32 : 64)) : 16;
+        *p_ds, *p_dkv, *p_rtab, *p_xb, *p_ob, *p_sb, *p_ss, *p_tcp, *p_tcc, *p_scfg, *p_slog, *p_dslog,
+        *p_sres, *p_apart, *p_acnt, *p_skv;
+    // rows of the activation buffers: the batch, or a prefill pass of PM_SEQ_MAX_ROWS frames
+    const int RM = BM > PM_SEQ_MAX_ROWS ? BM : PM_SEQ_MAX_ROWS;
+    // tensor-core path scratch (batches and prefill passes), sized from the plans of this
+    // configuration's projections at every N the path uses
+    const int NP = 64;
     size_t tc_part_floats = 16;
     int tc_count_max = 1;
-    if (BM >= 2) {
+    {
         const int shapes[5][2] = {{f.D, 3 * f.D / 128}, {f.D, f.D / 128}, {f.D, f.ffn / 64}, {f.ffn, f.D / 128},
                                   {f.D, (f.text_out + 127) / 128}};
-        for (auto& sh : shapes) {
-            TcParams t;
-            memset(&t, 0, sizeof t);
-            t.K = sh[0];
-            t.n_mtiles = sh[1];
-            t.B = 1;
-            t.npad = NP;
-            if (!plan_tc(t, c->num_sms)) return bail(PM_ERR_UNSUPPORTED, "a tensor-core projection has no plan");
-            const size_t need = (size_t)t.n_mtiles * t.maxseg * NP * 128;
-            if (need > tc_part_floats) tc_part_floats = need;
-            if (t.n_mtiles > tc_count_max) tc_count_max = t.n_mtiles;
-        }
+        for (int np : {16, 32, 64})
+            for (auto& sh : shapes) {
+                TcParams t;
+                memset(&t, 0, sizeof t);
+                t.K = sh[0];
+                t.n_mtiles = sh[1];
+                t.B = 1;
+                t.npad = np;
+                if (!plan_tc(t, c->num_sms)) return bail(PM_ERR_UNSUPPORTED, "a tensor-core projection has no plan");
+                const size_t need = (size_t)t.n_mtiles * t.maxseg * np * 128;
+                if (need > tc_part_floats) tc_part_floats = need;
+                if (t.n_mtiles > tc_count_max) tc_count_max = t.n_mtiles;
+            }
     }
-    c->npad_max = BM >= 2 ? NP : 0;
+    if (attn_seq_max_chunks(f.ctx) > PM_SEQ_MAX_CHUNKS)
+        return bail(PM_ERR_UNSUPPORTED, "ctx too long for the prefill attention");
+    c->npad_max = NP;
     c->tc_part_floats = tc_part_floats;
     c->tc_count_max = tc_count_max;
     std::vector<Item> items = {
@@ -883,10 +944,10 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
         {&p_sel, 4u * BM * PM_MAX_STREAMS_DEV}, {&p_amax, 8u * BM}, {&p_hc, 4u * BM}, {&p_status, 16u},
         {&p_damax, 8u * BM}, {&p_dcount, 4u * BM}, {&p_dcodes, 4u * BM * Q}, {&p_dtok, 4u * BM},
         {&p_dsup, 4u * BM * Q},
-        {&p_io, 64u + 4u * BM * S}, {&p_dio, 64u + 4u * BM + 4u * BM * Q},
-        {&p_x, 4u * BM * f.D}, {&p_q, 4u * BM * f.D}, {&p_o, 4u * BM * f.D}, {&p_s, 4u * BM * f.ffn},
+        {&p_io, 64u + 4u * RM * S}, {&p_dio, 64u + 4u * BM + 4u * BM * Q},
+        {&p_x, 4u * RM * f.D}, {&p_q, 4u * RM * f.D}, {&p_o, 4u * RM * f.D}, {&p_s, 4u * RM * f.ffn},
         {&p_h, 4u * BM * f.D}, {&p_part, 4u * BM * f.H * attn_max_splits(f.ctx) * (f.dh + 2)}, {&p_cnt, 4u * BM * f.H},
-        {&p_freq, 8u * (f.dh / 2)}, {&p_rtab, 8u * BM * (f.dh / 2)},
+        {&p_freq, 8u * (f.dh / 2)}, {&p_rtab, 8u * RM * (f.dh / 2)},
         {&p_xb, 2u * NP * f.D}, {&p_ob, 2u * NP * f.D}, {&p_sb, 2u * NP * f.ffn}, {&p_ss, 4u * (f.D / 128) * NP},
         {&p_tcp, 4u * tc_part_floats}, {&p_tcc, 4u * (size_t)tc_count_max},
         {&p_dz, 4u * BM * (Dd ? Dd : 1)}, {&p_dq, 4u * BM * (Dd ? Dd : 1)},
@@ -894,6 +955,9 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
         {&p_dkv, c->has_dep ? 2u * 2u * f.dep_layers * BM * f.dep_H * Q * f.dep_dh : 16u},
         {&p_scfg, sizeof(SampleCfg)}, {&p_slog, 4u * BM * f.text_out},
         {&p_dslog, c->has_dep ? 4u * BM * f.dep_card : 16u},
+        {&p_sres, 4u * PM_SEQ_MAX_ROWS * S},
+        {&p_apart, 4u * PM_SEQ_MAX_ROWS * f.H * PM_SEQ_MAX_CHUNKS * PM_SEQ_PART_STRIDE}, {&p_acnt, 4u * f.H},
+        {&p_skv, 2u * 2u * PM_SEQ_MAX_ROWS * f.H * f.dh},
     };
     size_t total = 0;
     for (auto& it : items) total = align_up(total, 256) + align_up(it.bytes, 16);
@@ -946,6 +1010,10 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     c->scfg = (SampleCfg*)p_scfg;
     c->slog = (float*)p_slog;
     c->dslog = (float*)p_dslog;
+    c->seq_resolved = (int32_t*)p_sres;
+    c->seq_part = (float*)p_apart;
+    c->seq_count = (uint32_t*)p_acnt;
+    c->seq_kv = (uint16_t*)p_skv;
 
     // RoPE frequencies f_j = exp(-ln(theta) * 2j / dh), in double
     std::vector<double> freq(f.dh / 2);
@@ -958,7 +1026,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
         return bail(PM_ERR_CUDA, "CUDA call failed");
 
     if (ck(cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking))) return bail(PM_ERR_CUDA, "cudaStreamCreateWithFlags");
-    const size_t slot_bytes = 64u + 4u * (size_t)BM * (S + 1 + Q);
+    const size_t slot_bytes = 64u + 4u * (size_t)RM * (S + 1 + Q);
     for (int i = 0; i < kStagingSlots; ++i) {
         if (cudaHostAlloc((void**)&c->slots[i].host, align_up(slot_bytes, 64), cudaHostAllocDefault) !=
             cudaSuccess)
@@ -1087,7 +1155,8 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     }
     if (ck(gemv_prepare())) return bail(PM_ERR_CUDA, "gemv_prepare()");
     if (ck(sample_prepare())) return bail(PM_ERR_CUDA, "sample_prepare()");
-    if (BM >= 2 && ck(tc_prepare())) return bail(PM_ERR_CUDA, "tc_prepare");
+    if (ck(attn_seq_prepare())) return bail(PM_ERR_CUDA, "attn_seq_prepare()");
+    if (ck(tc_prepare())) return bail(PM_ERR_CUDA, "tc_prepare");
     if (ck(cudaDeviceSynchronize())) return bail(PM_ERR_CUDA, "cudaDeviceSynchronize()");
     *out = c;
     return PM_OK;
@@ -1302,6 +1371,53 @@ extern "C" pm_status pm_frame_step(pm_ctx* c, int B, const int32_t* ids, float* 
     return PM_OK;
 }
 
+extern "C" pm_status pm_prefill(pm_ctx* c, int stream, int T, const int32_t* ids, float* text_logits, float* hidden,
+                                int32_t* text_token) {
+    if (!c) return PM_ERR_ARG;
+    const pm_config& f = c->cfg;
+    if (stream < 0 || stream >= f.B_max) return fail(c, PM_ERR_ARG, "pm_prefill: stream outside 0..B_max-1");
+    if (T < 1 || !ids) return fail(c, PM_ERR_ARG, "pm_prefill: need T >= 1 and ids");
+    PM_CUDA(cudaSetDevice(c->device));
+    const int S = f.n_streams;
+    const bool dev_ids = is_device_ptr(ids);
+    if (!dev_ids)
+        for (int t = 0; t < T; ++t)
+            for (int k = 0; k < S; ++k) {
+                const int32_t id = ids[(size_t)t * S + k];
+                const int rows = (k == 0) ? f.text_in : f.audio_in;
+                if (id < -1 || id >= rows)
+                    return fail(c, PM_ERR_INVALID_ID, "pm_prefill: ID " + std::to_string(id) + " at frame " +
+                                                          std::to_string(t) + " stream " + std::to_string(k));
+            }
+    for (int t0 = 0; t0 < T; t0 += PM_SEQ_MAX_ROWS) {
+        const int n = T - t0 < PM_SEQ_MAX_ROWS ? T - t0 : PM_SEQ_MAX_ROWS;
+        cudaGraphExec_t ex;
+        pm_status st = get_graph(c, c->prefill_graphs, n, record_prefill, &ex);
+        if (st) return st;
+        uint8_t* host;
+        cudaEvent_t ev;
+        st = take_slot(c, &host, &ev);
+        if (st) return st;
+        FrameIO io;
+        memset(&io, 0, sizeof io);
+        io.ids = dev_ids ? ids + (size_t)t0 * S : reinterpret_cast<const int32_t*>(c->io_region + 64);
+        io.logits = text_logits;
+        io.hidden = hidden;
+        io.token = text_token;
+        io.seq_stream = stream;
+        memcpy(host, &io, sizeof io);
+        size_t bytes = 64;
+        if (!dev_ids) {
+            memcpy(host + 64, ids + (size_t)t0 * S, 4u * n * S);
+            bytes += 4u * n * S;
+        }
+        PM_CUDA(cudaMemcpyAsync(c->io_region, host, bytes, cudaMemcpyHostToDevice, c->stream));
+        PM_CUDA(cudaEventRecord(ev, c->stream));
+        PM_CUDA(cudaGraphLaunch(ex, c->stream));
+    }
+    return PM_OK;
+}
+
 extern "C" pm_status pm_depformer_step(pm_ctx* c, int B, const float* hidden, const int32_t* text_tok,
                                        const int32_t* supplied, float* logits, int32_t* codes) {
     if (!c) return PM_ERR_ARG;
@@ -1368,8 +1484,10 @@ extern "C" pm_status pm_set_sampling(pm_ctx* c, float text_temperature, int text
         PM_CUDA(cudaStreamSynchronize(c->stream));
         for (auto& kv : c->frame_graphs) cudaGraphExecDestroy(kv.second);
         for (auto& kv : c->dep_graphs) cudaGraphExecDestroy(kv.second);
+        for (auto& kv : c->prefill_graphs) cudaGraphExecDestroy(kv.second);
         c->frame_graphs.clear();
         c->dep_graphs.clear();
+        c->prefill_graphs.clear();
         c->text_smp = ton;
         c->audio_smp = aon;
     }

@@ -55,10 +55,11 @@ struct SampleCfg {
 // Pointers the caller supplies per call, read by the kernels from device memory so that a
 // captured graph serves every call.
 struct FrameIO {
-    const int32_t* ids;   // [B][n_streams]
-    float* logits;        // [B][text_out] or null
-    float* hidden;        // [B][D] or null
-    int32_t* token;       // [B] or null
+    const int32_t* ids;   // [B][n_streams] (a prefill: [T][n_streams], frames of one stream)
+    float* logits;        // [B][text_out] or null (a prefill: its last frame's, [1][text_out])
+    float* hidden;        // [B][D] or null (a prefill: its last frame's)
+    int32_t* token;       // [B] or null (a prefill: its last frame's)
+    int32_t seq_stream;   // a prefill: the stream whose frames the rows are
 };
 
 struct DepIO {

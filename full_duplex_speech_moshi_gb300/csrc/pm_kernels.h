@@ -102,6 +102,9 @@ struct EmbedParams {
     float2* rope_tab;
     const double* rope_freq;
     int dh;
+    // prefill: rows are frames pos .. pos+B-1 of stream io->seq_stream with these inputs
+    // (delays already applied and IDs validated by k_seq_prepare), or null
+    const int32_t* resolved;  // [B][n_streams]
     // tensor-core path (B >= 2): bf16(alpha * x) operand [npad][D] and per-CTA sums of x^2
     uint16_t* xb;
     const uint16_t* alpha;
@@ -131,6 +134,43 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl);
 // chunks (CTAs per head) the attention grid needs for a window of ctx keys; AttnParams.S
 // must be at least this and `part` must hold S chunks per head
 int attn_max_splits(int ctx);
+
+// ----------------------------------------------------------------------------------
+// prefill (T frames of one stream as one batched pass)
+// ----------------------------------------------------------------------------------
+#define PM_SEQ_MAX_ROWS 64       // frames per prefill pass
+#define PM_SEQ_KPC 256           // keys per attention work item
+#define PM_SEQ_MAX_CHUNKS 16     // work items per head (window + rows up to 4096 keys)
+#define PM_SEQ_PART_STRIDE 132   // floats per attention partial (128 values, max, sum, pad)
+struct SeqPrepParams {
+    const FrameIO* io;
+    DevState st;
+    int32_t* resolved;       // [T][n_streams] out
+    int T, n_streams;
+    int rows[PM_MAX_STREAMS_DEV];
+    int init_id[PM_MAX_STREAMS_DEV];
+    int delays[PM_MAX_STREAMS_DEV];
+};
+cudaError_t launch_seq_prepare(const SeqPrepParams& p, cudaStream_t s, bool pdl);
+struct AttnSeqParams {
+    const float* q;          // [T][D] rotated queries
+    const uint16_t* kc;      // this layer's K cache [B_max][H][ctx][dh] (positions < pos)
+    const uint16_t* vc;
+    const uint16_t* kv_new;  // [2][T][H][dh] this pass's K and V (positions pos .. pos+T-1)
+    float* o;                // [T][D]
+    uint16_t* ob;            // [npad][D] bf16 copy of o, or null
+    float* part;             // [T][H][PM_SEQ_MAX_CHUNKS][PM_SEQ_PART_STRIDE]
+    uint32_t* count;         // [H], zero between launches
+    DevState st;
+    const FrameIO* io;
+    int T, H, ctx, win, D, grid;
+    float scale_log2;
+};
+cudaError_t launch_attn_seq(const AttnSeqParams& p, cudaStream_t s, bool pdl);
+// the pass's K/V rows into the ring (the last row of each slot), after its attention
+cudaError_t launch_seq_commit(const AttnSeqParams& p, cudaStream_t s, bool pdl);
+cudaError_t attn_seq_prepare();
+int attn_seq_max_chunks(int win);
 
 // ----------------------------------------------------------------------------------
 // depformer helpers
@@ -177,8 +217,10 @@ struct SampleParams {
     const FrameIO* io;
     const DepIO* dio;
     int q, Q, n_streams;
+    int seq;
 };
 cudaError_t launch_sample(const SampleParams& p, cudaStream_t s, bool pdl);
+// (SampleParams.seq: SM_TEXT for a prefill -- one row, stream io->seq_stream)
 cudaError_t sample_prepare();
 
 // ----------------------------------------------------------------------------------
@@ -243,6 +285,11 @@ struct TcParams {
     const uint16_t* alpha;   // final norm scale [D]
     float* logits_copy;      // also write the logits here ([B][n_rows]), or null
     NextPrefetch nx;         // read through the `next` tensor map
+    // prefill: rows are frames pos .. pos+B-1 of stream io->seq_stream (TE_QKV_ROPE: their
+    // K/V go to kv_new, committed to the ring after the attention; TE_HEAD: only the last
+    // row's outputs, positions advance by B)
+    int seq;
+    uint16_t* kv_new;        // [2][B][H][dh] bf16 (K rows, then V rows)
 };
 
 bool plan_tc(TcParams& p, int num_sms);

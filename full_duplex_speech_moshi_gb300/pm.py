@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "PM_OK", 1: "PM_ERR_ARG", 2: "PM_ERR_INVALID_ID", 3: "PM_ERR_
 EXPORTS = ["pm_kv_cache_bytes", "pm_create", "pm_reset", "pm_set_positions", "pm_get_positions",
            "pm_frame_step", "pm_depformer_step", "pm_profile_frame", "pm_device_status", "pm_last_error",
            "pm_destroy", "pm_text_head_noalloc", "pm_set_sampling", "pm_sample", "pm_snapshot_bytes",
-           "pm_snapshot", "pm_restore"]
+           "pm_snapshot", "pm_restore", "pm_prefill"]
 KERNEL_KINDS = {0: "embed", 1: "qkv_rope", 2: "attention", 3: "out_proj", 4: "linear_in_swiglu",
                 5: "linear_out", 6: "text_head", 7: "frame_program", 8: "text_sample"}
 
@@ -97,6 +97,8 @@ def lib():
         L.pm_sample.restype = C.c_int
         L.pm_sample.argtypes = [vp, C.c_int, vp, C.c_int, C.c_int, C.c_float, C.c_int, C.c_ulonglong,
                                 C.c_longlong, C.c_int, vp]
+        L.pm_prefill.restype = C.c_int
+        L.pm_prefill.argtypes = [vp, C.c_int, C.c_int, vp, vp, vp, vp]
         L.pm_snapshot_bytes.restype = C.c_size_t
         L.pm_snapshot_bytes.argtypes = [C.POINTER(pm_config)]
         L.pm_snapshot.restype = C.c_int
@@ -237,6 +239,11 @@ class Context:
     def frame_step(self, B: int, ids, text_logits=None, hidden=None, text_token=None) -> None:
         self._check(self.L.pm_frame_step(self.h, int(B), _ptr(ids), _ptr(text_logits), _ptr(hidden),
                                          _ptr(text_token)))
+
+    def prefill(self, stream: int, T: int, ids, text_logits=None, hidden=None, text_token=None) -> None:
+        """T frames of one stream in batched passes (ids [T][n_streams], host or device)."""
+        self._check(self.L.pm_prefill(self.h, int(stream), int(T), _ptr(ids), _ptr(text_logits), _ptr(hidden),
+                                      _ptr(text_token)))
 
     def depformer_step(self, B: int, hidden=None, text_tok=None, supplied=None, logits=None, codes=None) -> None:
         self._check(self.L.pm_depformer_step(self.h, int(B), _ptr(hidden), _ptr(text_tok), _ptr(supplied),

@@ -164,6 +164,21 @@ pm_status pm_get_positions(pm_ctx* ctx, int32_t* pos_out);
 pm_status pm_frame_step(pm_ctx* ctx, int B, const int32_t* ids, float* text_logits, float* hidden,
                         int32_t* text_token);
 
+/* Prefill: T frames of stream `stream` from its current position, as if pm_frame_step
+ * ran T times with these IDs for that stream alone ("PersonaPlex native LM audit",
+ * section 9: the startup voice prompt, silence frames and system text prompt each advance
+ * one model step), computed as passes of up to 64 frames whose projections are 64-row
+ * tensor-core GEMMs and whose attention is causal within the pass.
+ *  ids         [T][n_streams] int32, host or device memory: each frame's undelayed tokens
+ *              (-1 none; no PM_ID_FEEDBACK).  Host memory is copied before the call returns.
+ *  text_logits [1][text_out] fp32 device memory, hidden [1][D], text_token [1]: the last
+ *              frame's outputs (greedy or drawn token), or NULL.
+ * Advances the stream's position by T; its selection slot holds the last frame's text
+ * token (so PM_ID_FEEDBACK and the depformer's default token continue from it).  Results
+ * equal T single frames up to the tensor-core path's rounding (bf16 activation operands). */
+pm_status pm_prefill(pm_ctx* ctx, int stream, int T, const int32_t* ids, float* text_logits, float* hidden,
+                     int32_t* text_token);
+
 /* One depformer frame (sixteen positions) for streams 0..B-1.
  *  hidden    [B][D] fp32 device memory, or NULL = the h of this context's last frame.
  *  text_tok  [B] int32 host or device memory, or NULL = the text token this context

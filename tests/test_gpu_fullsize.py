@@ -116,6 +116,29 @@ def test_config2_long_context_wrap(full):
     assert full.ctx.get_positions()[0] == s.ctx + 3
 
 
+def test_prefill_pass_on_a_full_ring(full):
+    """The startup-prompt path at full size: 3000 cached positions (seeded K/V), then one
+    64-frame prefill pass whose rows reuse 64 slots of the full ring, then decode frames
+    reading what it left; against the oracle stepping the same frames."""
+    s = full.shape
+    full.ctx.reset()
+    _gpu_history(full, 0, s.ctx, seed=33)
+    st = _oracle_history(full, 0, s.ctx, seed=33)
+    full.ctx.set_positions([s.ctx])
+    T = 64
+    ids = I.make_ids(s, T + 2, seed=2005)[:, 0]
+    full.ctx.prefill(0, T, np.ascontiguousarray(ids[:T]), full.logits, full.hidden, full.token)
+    full.torch.cuda.synchronize()
+    g = (full.hidden[:1].double().cpu().numpy(), full.logits[:1].double().cpu().numpy(), full.token[:1].cpu().numpy())
+    for t in range(T):
+        h, _, lg, a = st.step(ids[t])
+    full.check_frame(g, (h[None], lg[None], np.array([a])), "prefill")
+    assert full.ctx.get_positions()[0] == s.ctx + T
+    for t in range(T, T + 2):
+        h, _, lg, a = st.step(ids[t])
+        full.check_frame(full.gpu_frame(ids[t:t + 1]), (h[None], lg[None], np.array([a])), f"t={t}")
+
+
 def test_config3_batched_ragged(full):
     s = full.shape
     B = 16
