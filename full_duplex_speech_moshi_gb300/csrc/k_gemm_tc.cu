@@ -24,6 +24,10 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "pm_kernels.h"
 #include "tc_common.cuh"
 
@@ -514,27 +518,77 @@ cudaError_t prepare_n() {
 
 }  // namespace
 
+namespace {
+
+typedef void (*tc_kernel_t)(CUtensorMap, CUtensorMap, CUtensorMap, TcParams);
+
+template <int NPAD>
+tc_kernel_t kernel_n(int epi) {
+    switch (epi) {
+        case TE_STORE: return k_gemm_tc<TE_STORE, NPAD>;
+        case TE_RESIDUAL: return k_gemm_tc<TE_RESIDUAL, NPAD>;
+        case TE_SWIGLU: return k_gemm_tc<TE_SWIGLU, NPAD>;
+        case TE_QKV_ROPE: return k_gemm_tc<TE_QKV_ROPE, NPAD>;
+        case TE_HEAD: return k_gemm_tc<TE_HEAD, NPAD>;
+        default: return nullptr;
+    }
+}
+
+// CTAs of this kernel variant that fit on one SM at `smem` dynamic bytes (registers are
+// allocated per warp in units of 256), at most PM_TC_CTAS_PER_SM
+int resident_per_sm(int epi, int npad, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, size_t>, int> memo;
+    std::lock_guard<std::mutex> lock(mu);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, epi, npad, smem);
+    auto it = memo.find(key);
+    if (it != memo.end()) return it->second;
+    tc_kernel_t k = npad == 16 ? kernel_n<16>(epi) : npad == 32 ? kernel_n<32>(epi) : kernel_n<64>(epi);
+    cudaFuncAttributes fa;
+    int smem_sm = 0, reserved = 0, n = 1;
+    if (k && cudaFuncGetAttributes(&fa, k) == cudaSuccess &&
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) == cudaSuccess) {
+        const int regs_warp = ((fa.numRegs * 32 + 255) / 256) * 256;
+        const int by_regs = 65536 / (6 * regs_warp);
+        const int by_smem = smem_sm / (int)(smem + fa.sharedSizeBytes + reserved);
+        n = by_regs < by_smem ? by_regs : by_smem;
+    } else {
+        cudaGetLastError();
+    }
+    if (n > PM_TC_CTAS_PER_SM) n = PM_TC_CTAS_PER_SM;
+    if (n < 1) n = 1;
+    memo[key] = n;
+    return n;
+}
+
+}  // namespace
+
 bool plan_tc(TcParams& p, int num_sms) {
     if (p.K <= 0 || p.K % KT != 0 || p.n_mtiles <= 0) return false;
     if (!(p.npad == 16 || p.npad == 32 || p.npad == 64) || p.B < 1 || p.B > p.npad) return false;
     p.nk = p.K / KT;
     const long long U = (long long)p.n_mtiles * p.nk;
     const int min_units = p.min_units > 0 ? p.min_units : PM_TC_MIN_UNITS;
-    int G = PM_TC_CTAS_PER_SM * num_sms;
-    if ((long long)G * min_units > U) G = (int)((U + min_units - 1) / min_units);
-    if (G < 1) G = 1;
-    p.grid = G;
     const uint32_t st_bytes = A_BYTES + (uint32_t)p.npad * 128u;
     p.nst = (int)((PM_TC_RING_BYTES) / st_bytes);
     if (p.nst < 2) p.nst = 2;
+    const size_t smem = 1024 + (size_t)p.nst * st_bytes + 8u * (2 * p.nst + 5) + 16 + 16 + 4u * p.npad +
+                        4u * p.npad * 64 + 8u * 4 * p.npad;
+    // one wave: as many CTAs as fit on the GPU at once
+    int G = resident_per_sm(p.epi, p.npad, smem) * num_sms;
+    if ((long long)G * min_units > U) G = (int)((U + min_units - 1) / min_units);
+    if (G < 1) G = 1;
+    p.grid = G;
     int maxseg = 1;
     for (int m = 0; m < p.n_mtiles; ++m) {
         const int cf = cta_of((long long)m * p.nk, U, G), cl = cta_of((long long)m * p.nk + p.nk - 1, U, G);
         if (cl - cf + 1 > maxseg) maxseg = cl - cf + 1;
     }
     p.maxseg = maxseg;
-    p.smem = 1024 + (size_t)p.nst * st_bytes + 8u * (2 * p.nst + 5) + 16 + 16 + 4u * p.npad +
-             4u * p.npad * 64 + 8u * 4 * p.npad;
+    p.smem = smem;
     return p.smem <= 220u * 1024u;
 }
 

@@ -200,11 +200,12 @@ static pm_status plan(pm_ctx* c, GemvParams& p, int rpu, const char* what) {
 #define PM_PF_TC_BYTES 262144u
 #endif
 
-static NextPrefetch next_tc(pm_ctx* c, int K, int n_mtiles, int split_rows, int npad) {
+static NextPrefetch next_tc(pm_ctx* c, int epi, int K, int n_mtiles, int split_rows, int npad) {
     NextPrefetch nx;
     memset(&nx, 0, sizeof nx);
     TcParams t;
     memset(&t, 0, sizeof t);
+    t.epi = epi;
     t.K = K;
     t.n_mtiles = n_mtiles;
     t.npad = npad;
@@ -502,7 +503,7 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         p.kc = kc;
         p.vc = vc;
         p.rope_tab = c->rope_tab;
-        p.nx = next_tc(c, D, D / 128, 0, npad);
+        p.nx = next_tc(c, TE_RESIDUAL, D, D / 128, 0, npad);
         p.seq = seq ? 1 : 0;
         p.kv_new = c->seq_kv;
         pm_status ps = go(mq[l], mx, mwo[l], p, PM_KERNEL_QKV, "in_proj");
@@ -558,7 +559,7 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         p.yb_stride = D;
         p.alpha_next = c->norm2[l];
         p.ss_out = c->ss;
-        p.nx = next_tc(c, D, F / 64, F, npad);
+        p.nx = next_tc(c, TE_SWIGLU, D, F / 64, F, npad);
         if ((ps = go(mwo[l], mo, mwi[l], p, PM_KERNEL_OUT_PROJ, "out_proj"))) return ps;
         // RMSNorm2 (folded) + linear_in + SwiGLU -> bf16 s
         p = base(TE_SWIGLU, D, F / 64, F);
@@ -567,7 +568,7 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         p.split_rows = F;
         p.yb = c->sb;
         p.yb_stride = F;
-        p.nx = next_tc(c, F, D / 128, 0, npad);
+        p.nx = next_tc(c, TE_RESIDUAL, F, D / 128, 0, npad);
         if ((ps = go(mwi[l], mx, mwt[l], p, PM_KERNEL_LINEAR_IN, "linear_in"))) return ps;
         // linear_out + residual; emits the next norm's operand
         p = base(TE_RESIDUAL, F, D / 128, D);
@@ -578,7 +579,8 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         p.alpha_next = (l + 1 < f.n_layers) ? c->norm1[l + 1] : c->out_norm;
         p.ss_out = c->ss;
         const bool last = l + 1 == f.n_layers;
-        p.nx = last ? next_tc(c, D, head_tiles, 0, npad) : next_tc(c, D, 3 * D / 128, 0, npad);
+        p.nx = last ? next_tc(c, TE_HEAD, D, head_tiles, 0, npad)
+                    : next_tc(c, TE_QKV_ROPE, D, 3 * D / 128, 0, npad);
         if ((ps = go(mwt[l], msb, last ? mh : mq[l + 1], p, PM_KERNEL_LINEAR_OUT, "linear_out"))) return ps;
     }
     TcParams p = base(TE_HEAD, D, head_tiles, f.text_out);
@@ -587,7 +589,7 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
     p.h_internal = c->h;
     p.x_resid = c->x;
     p.alpha = c->out_norm;
-    p.nx = next_tc(c, D, 3 * D / 128, 0, npad);  // the next frame's first projection
+    p.nx = next_tc(c, TE_QKV_ROPE, D, 3 * D / 128, 0, npad);  // the next frame's first projection
     if (c->text_smp) p.logits_copy = c->slog;
     p.seq = seq ? 1 : 0;
     pm_status hs = go(mh, mx, mq[0], p, PM_KERNEL_HEAD, "text_linear");
@@ -918,14 +920,16 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     size_t tc_part_floats = 16;
     int tc_count_max = 1;
     {
-        const int shapes[5][2] = {{f.D, 3 * f.D / 128}, {f.D, f.D / 128}, {f.D, f.ffn / 64}, {f.ffn, f.D / 128},
-                                  {f.D, (f.text_out + 127) / 128}};
+        const int shapes[5][3] = {{TE_QKV_ROPE, f.D, 3 * f.D / 128}, {TE_RESIDUAL, f.D, f.D / 128},
+                                  {TE_SWIGLU, f.D, f.ffn / 64}, {TE_RESIDUAL, f.ffn, f.D / 128},
+                                  {TE_HEAD, f.D, (f.text_out + 127) / 128}};
         for (int np : {16, 32, 64})
             for (auto& sh : shapes) {
                 TcParams t;
                 memset(&t, 0, sizeof t);
-                t.K = sh[0];
-                t.n_mtiles = sh[1];
+                t.epi = sh[0];
+                t.K = sh[1];
+                t.n_mtiles = sh[2];
                 t.B = 1;
                 t.npad = np;
                 if (!plan_tc(t, c->num_sms)) return bail(PM_ERR_UNSUPPORTED, "a tensor-core projection has no plan");
