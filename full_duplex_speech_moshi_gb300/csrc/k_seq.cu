@@ -14,10 +14,12 @@
 // keys they can see (positions max(0, p0 - win + 1) .. p0 + T - 1): positions before p0
 // from the ring, the pass's own from the kv_new rows its QKV projection wrote (a full
 // ring's slots are reused by the pass's positions, so they are committed only afterwards
-// by k_seq_commit: the last row of each slot).  Work item = (head,
-// 256-key chunk): the chunk's K and V rows are staged once in shared memory (64 keys at a
-// time) and used by every row; per row a running (max, sum, weighted values) is kept in
-// registers; chunks merge in the CTA that finishes a head last (completion counter).
+// by k_seq_commit: the last row of each slot).  Work item = (head, 256-key chunk): 64 keys
+// at a time are staged in shared memory (K as rows, V transposed) and every warp -- 16
+// query rows -- computes its scores and weighted values with warp-wide m16n8k16 tensor
+// core MMAs (bf16 operands, fp32 accumulation), keeping the running (max, sum, weighted
+// values) of its rows in registers; chunks merge in the CTA that finishes a head last
+// (completion counter).
 #include <math.h>
 
 #include "pm_kernels.h"
@@ -27,8 +29,7 @@ namespace {
 
 constexpr int DH = 128;
 constexpr int KSUB = 64;                   // keys staged at a time
-constexpr int SEQ_NT = 256;                // threads of k_attn_seq (8 warps)
-constexpr int ROWS_PER_WARP = PM_SEQ_MAX_ROWS / (SEQ_NT / 32);
+constexpr int SEQ_NT = 128;                // threads of k_attn_seq: 4 warps x 16 query rows
 constexpr int PSTRIDE = PM_SEQ_PART_STRIDE;  // floats per partial: DH values, max, sum (16-byte rows)
 
 __global__ void __launch_bounds__(32) k_seq_prepare(const SeqPrepParams p) {
@@ -71,131 +72,191 @@ __global__ void __launch_bounds__(32) k_seq_prepare(const SeqPrepParams p) {
     }
 }
 
+// D += A * B on the tensor cores, warp-wide m16n8k16 (bf16 in, fp32 accumulate).
+// Fragments (g = lane / 4, t = lane % 4): a[0] = A[g][2t..2t+1], a[1] = A[g+8][2t..],
+// a[2] = A[g][2t+8..], a[3] = A[g+8][2t+8..]; b[0] = B[2t..2t+1][g], b[1] = B[2t+8..][g];
+// d[0..1] = D[g][2t..2t+1], d[2..3] = D[g+8][2t..2t+1].
+__device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    return (uint32_t)f32_to_bf16_rne(lo) | ((uint32_t)f32_to_bf16_rne(hi) << 16);
+}
+
+constexpr int KS_STRIDE = DH + 8;    // bf16 per staged key row (conflict-free fragment loads)
+constexpr int VT_STRIDE = KSUB + 8;  // bf16 per staged value column
+
 __global__ void __launch_bounds__(SEQ_NT) k_attn_seq(const AttnSeqParams p) {
-    extern __shared__ float sm[];
-    float* s_q = sm;                                   // [T][DH]
-    float* s_kt = s_q + (size_t)PM_SEQ_MAX_ROWS * DH;   // [DH][KSUB + 1] keys, transposed
-    float* s_v = s_kt + (size_t)DH * (KSUB + 1);        // [KSUB][DH]
+    __shared__ __align__(16) uint16_t s_k[KSUB * KS_STRIDE];  // [key][dim]
+    __shared__ __align__(16) uint16_t s_vt[DH * VT_STRIDE];   // [dim][key]
     __shared__ int s_last;
     __shared__ float s_pm[SEQ_NT / 32][PM_SEQ_MAX_CHUNKS], s_pl[SEQ_NT / 32][PM_SEQ_MAX_CHUNKS];
     pdl_trigger();
     pdl_wait();
     if (*(volatile uint32_t*)&p.st.status[1] != 0u) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int g = lane >> 2, tq = lane & 3;
     const int s = p.io->seq_stream;
     const int p0 = p.st.pos[s];
     const int T = p.T;
     const int lo_all = max(0, p0 - p.win + 1), hi_all = p0 + T - 1;
     const int C = (hi_all - lo_all + 1 + PM_SEQ_KPC - 1) / PM_SEQ_KPC;
     const int items = p.H * C;
+    // this thread's two query rows (the warp owns rows 16 * warp .. 16 * warp + 15)
+    const int r0 = 16 * warp + g, r1 = r0 + 8;
 
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
         const int h = item / C, c = item % C;
         const int c0 = lo_all + c * PM_SEQ_KPC;
         const int c1 = min(c0 + PM_SEQ_KPC, hi_all + 1);
-        for (int i = tid; i < T * DH; i += SEQ_NT)
-            s_q[i] = p.q[(size_t)(i / DH) * p.D + h * DH + (i % DH)] * p.scale_log2;
-        float m[ROWS_PER_WARP], l[ROWS_PER_WARP], acc[ROWS_PER_WARP][4];
+        // query fragments, pre-scaled by log2(e) / sqrt(dh), bf16
+        uint32_t qf[DH / 16][4];
+        {
+            const float* q0 = p.q + (size_t)r0 * p.D + h * DH;
+            const float* q1 = p.q + (size_t)r1 * p.D + h * DH;
+            const bool v0 = r0 < T, v1 = r1 < T;
 #pragma unroll
-        for (int r = 0; r < ROWS_PER_WARP; ++r) {
-            m[r] = -INFINITY;
-            l[r] = 0.f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[r][e] = 0.f;
+            for (int ks = 0; ks < DH / 16; ++ks) {
+                const int d = 16 * ks + 2 * tq;
+                const float2 a = v0 ? *reinterpret_cast<const float2*>(q0 + d) : make_float2(0.f, 0.f);
+                const float2 b = v1 ? *reinterpret_cast<const float2*>(q1 + d) : make_float2(0.f, 0.f);
+                const float2 a8 = v0 ? *reinterpret_cast<const float2*>(q0 + d + 8) : make_float2(0.f, 0.f);
+                const float2 b8 = v1 ? *reinterpret_cast<const float2*>(q1 + d + 8) : make_float2(0.f, 0.f);
+                qf[ks][0] = pack_bf16(a.x * p.scale_log2, a.y * p.scale_log2);
+                qf[ks][1] = pack_bf16(b.x * p.scale_log2, b.y * p.scale_log2);
+                qf[ks][2] = pack_bf16(a8.x * p.scale_log2, a8.y * p.scale_log2);
+                qf[ks][3] = pack_bf16(b8.x * p.scale_log2, b8.y * p.scale_log2);
+            }
         }
+        float o[DH / 8][4];
+#pragma unroll
+        for (int d = 0; d < DH / 8; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
+        float m_0 = -INFINITY, m_1 = -INFINITY, l_0 = 0.f, l_1 = 0.f;
         const size_t head_base = ((size_t)s * p.H + h) * (size_t)p.ctx * DH;
         for (int k0 = c0; k0 < c1; k0 += KSUB) {
             const int nk = min(KSUB, c1 - k0);
-            __syncthreads();  // previous sub-chunk (and q) fully used / written
-            // stage K (transposed) and V of keys k0 .. k0+nk-1 as fp32
+            __syncthreads();  // the previous sub-chunk's K / V fully used
             for (int i = tid; i < KSUB * (DH / 8); i += SEQ_NT) {
                 const int j = i / (DH / 8), d0 = (i % (DH / 8)) * 8;
-                float kv[8], vv[8];
+                uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
                 if (j < nk) {
                     const int kp = k0 + j;
-                    const uint16_t *ksrc, *vsrc;
                     if (kp >= p0) {
                         const size_t off = ((size_t)(kp - p0) * p.H + h) * DH + d0;
-                        ksrc = p.kv_new + off;
-                        vsrc = p.kv_new + (size_t)T * p.H * DH + off;
+                        kv = *reinterpret_cast<const uint4*>(p.kv_new + off);
+                        vv = *reinterpret_cast<const uint4*>(p.kv_new + (size_t)T * p.H * DH + off);
                     } else {
                         const size_t off = head_base + (size_t)(kp % p.ctx) * DH + d0;
-                        ksrc = p.kc + off;
-                        vsrc = p.vc + off;
+                        kv = *reinterpret_cast<const uint4*>(p.kc + off);
+                        vv = *reinterpret_cast<const uint4*>(p.vc + off);
                     }
-                    const uint4 a = *reinterpret_cast<const uint4*>(ksrc);
-                    const uint4 bv = *reinterpret_cast<const uint4*>(vsrc);
-                    kv[0] = bf16lo(a.x); kv[1] = bf16hi(a.x); kv[2] = bf16lo(a.y); kv[3] = bf16hi(a.y);
-                    kv[4] = bf16lo(a.z); kv[5] = bf16hi(a.z); kv[6] = bf16lo(a.w); kv[7] = bf16hi(a.w);
-                    vv[0] = bf16lo(bv.x); vv[1] = bf16hi(bv.x); vv[2] = bf16lo(bv.y); vv[3] = bf16hi(bv.y);
-                    vv[4] = bf16lo(bv.z); vv[5] = bf16hi(bv.z); vv[6] = bf16lo(bv.w); vv[7] = bf16hi(bv.w);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) kv[e] = vv[e] = 0.f;
                 }
+                *reinterpret_cast<uint4*>(s_k + (size_t)j * KS_STRIDE + d0) = kv;
+                const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    s_kt[(size_t)(d0 + e) * (KSUB + 1) + j] = kv[e];
-                    s_v[(size_t)j * DH + d0 + e] = vv[e];
+                for (int e = 0; e < 4; ++e) {
+                    s_vt[(size_t)(d0 + 2 * e) * VT_STRIDE + j] = (uint16_t)(vw[e] & 0xFFFFu);
+                    s_vt[(size_t)(d0 + 2 * e + 1) * VT_STRIDE + j] = (uint16_t)(vw[e] >> 16);
                 }
             }
             __syncthreads();
+            // S = Q K^T for the warp's 16 rows and the 64 staged keys (8 tiles of 8 keys)
+            float sc[KSUB / 8][4];
 #pragma unroll
-            for (int r = 0; r < ROWS_PER_WARP; ++r) {
-                const int t = warp + r * (SEQ_NT / 32);
-                if (t >= T) break;
-                const int qpos = p0 + t, klo = qpos - p.win + 1;
-                // scores of keys lane and lane + 32 (base-2 scaled)
-                const float* qr = s_q + (size_t)t * DH;
-                float d0 = 0.f, d1 = 0.f;
-#pragma unroll 16
-                for (int d = 0; d < DH; ++d) {
-                    const float qv = qr[d];
-                    d0 = fmaf(qv, s_kt[(size_t)d * (KSUB + 1) + lane], d0);
-                    d1 = fmaf(qv, s_kt[(size_t)d * (KSUB + 1) + lane + 32], d1);
+            for (int j = 0; j < KSUB / 8; ++j) {
+                sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+                const uint16_t* kr = s_k + (size_t)(8 * j + g) * KS_STRIDE + 2 * tq;
+#pragma unroll
+                for (int ks = 0; ks < DH / 16; ++ks) {
+                    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr + 16 * ks);
+                    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + 16 * ks + 8);
+                    mma16816(sc[j], qf[ks], b0, b1);
                 }
-                const int kp0 = k0 + lane, kp1 = k0 + lane + 32;
-                const bool v0 = lane < nk && kp0 >= klo && kp0 <= qpos;
-                const bool v1 = lane + 32 < nk && kp1 >= klo && kp1 <= qpos;
-                float sc0 = v0 ? d0 : -INFINITY, sc1 = v1 ? d1 : -INFINITY;
-                float mx = fmaxf(sc0, sc1);
+            }
+            // mask (window, causality, pass rows) and the running softmax of both rows
+            const int qp0 = p0 + r0, qp1 = p0 + r1;
+            float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                if (mx == -INFINITY) continue;  // no visible key in this sub-chunk
-                const float mn = fmaxf(m[r], mx);
-                const float fo = (m[r] == -INFINITY) ? 0.f : exp2f(m[r] - mn);
-                const float w0 = v0 ? exp2f(sc0 - mn) : 0.f, w1 = v1 ? exp2f(sc1 - mn) : 0.f;
-                float ws = w0 + w1;
+            for (int j = 0; j < KSUB / 8; ++j)
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
-                l[r] = l[r] * fo + ws;
-                m[r] = mn;
-                float a[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) a[e] = acc[r][e] * fo;
-                // weighted values: lane owns coordinates 4*lane .. 4*lane+3
-                for (int j = 0; j < nk; ++j) {
-                    const float w = __shfl_sync(0xffffffffu, j < 32 ? w0 : w1, j & 31);
-                    const float4 vv = *reinterpret_cast<const float4*>(s_v + (size_t)j * DH + 4 * lane);
-                    a[0] = fmaf(w, vv.x, a[0]);
-                    a[1] = fmaf(w, vv.y, a[1]);
-                    a[2] = fmaf(w, vv.z, a[2]);
-                    a[3] = fmaf(w, vv.w, a[3]);
+                for (int e = 0; e < 2; ++e) {
+                    const int kp = k0 + 8 * j + 2 * tq + e;
+                    const bool in = kp < k0 + nk;
+                    const bool ok0 = in && r0 < T && kp <= qp0 && kp > qp0 - p.win;
+                    const bool ok1 = in && r1 < T && kp <= qp1 && kp > qp1 - p.win;
+                    sc[j][e] = ok0 ? sc[j][e] : -INFINITY;
+                    sc[j][2 + e] = ok1 ? sc[j][2 + e] : -INFINITY;
+                    mx0 = fmaxf(mx0, sc[j][e]);
+                    mx1 = fmaxf(mx1, sc[j][2 + e]);
                 }
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[r][e] = a[e];
+            for (int off = 1; off <= 2; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m_0, mx0), mn1 = fmaxf(m_1, mx1);
+            const float f0 = (m_0 == -INFINITY) ? 0.f : exp2f(m_0 - mn0);
+            const float f1 = (m_1 == -INFINITY) ? 0.f : exp2f(m_1 - mn1);
+            float sum0 = 0.f, sum1 = 0.f;
+            uint32_t pf[KSUB / 16][4];
+#pragma unroll
+            for (int j = 0; j < KSUB / 8; ++j) {
+                const float e0 = sc[j][0] == -INFINITY ? 0.f : exp2f(sc[j][0] - mn0);
+                const float e1 = sc[j][1] == -INFINITY ? 0.f : exp2f(sc[j][1] - mn0);
+                const float e2 = sc[j][2] == -INFINITY ? 0.f : exp2f(sc[j][2] - mn1);
+                const float e3 = sc[j][3] == -INFINITY ? 0.f : exp2f(sc[j][3] - mn1);
+                sum0 += e0 + e1;
+                sum1 += e2 + e3;
+                // P as the A operand of P V: keys 16 kk .. 16 kk + 15 are tiles 2 kk, 2 kk + 1
+                const int kk = j >> 1, hi = j & 1;
+                pf[kk][hi ? 2 : 0] = pack_bf16(e0, e1);
+                pf[kk][hi ? 3 : 1] = pack_bf16(e2, e3);
+            }
+#pragma unroll
+            for (int off = 1; off <= 2; off <<= 1) {
+                sum0 += __shfl_xor_sync(0xffffffffu, sum0, off);
+                sum1 += __shfl_xor_sync(0xffffffffu, sum1, off);
+            }
+            l_0 = l_0 * f0 + sum0;
+            l_1 = l_1 * f1 + sum1;
+            m_0 = mn0;
+            m_1 = mn1;
+#pragma unroll
+            for (int d = 0; d < DH / 8; ++d) {
+                o[d][0] *= f0;
+                o[d][1] *= f0;
+                o[d][2] *= f1;
+                o[d][3] *= f1;
+            }
+            // O += P V (16 tiles of 8 output coordinates)
+#pragma unroll
+            for (int d = 0; d < DH / 8; ++d) {
+                const uint16_t* vr = s_vt + (size_t)(8 * d + g) * VT_STRIDE + 2 * tq;
+#pragma unroll
+                for (int kk = 0; kk < KSUB / 16; ++kk) {
+                    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(vr + 16 * kk);
+                    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(vr + 16 * kk + 8);
+                    mma16816(o[d], pf[kk], b0, b1);
+                }
             }
         }
-        // this chunk's partial of every row
+        // this chunk's partial of the thread's rows
 #pragma unroll
-        for (int r = 0; r < ROWS_PER_WARP; ++r) {
-            const int t = warp + r * (SEQ_NT / 32);
-            if (t >= T) break;
-            float* part = p.part + (((size_t)t * p.H + h) * PM_SEQ_MAX_CHUNKS + c) * PSTRIDE;
-            *reinterpret_cast<float4*>(part + 4 * lane) = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-            if (lane == 0) {
-                part[DH] = m[r];
-                part[DH + 1] = l[r];
+        for (int hr = 0; hr < 2; ++hr) {
+            const int r = hr ? r1 : r0;
+            if (r >= T) continue;
+            float* part = p.part + (((size_t)r * p.H + h) * PM_SEQ_MAX_CHUNKS + c) * PSTRIDE;
+#pragma unroll
+            for (int d = 0; d < DH / 8; ++d)
+                *reinterpret_cast<float2*>(part + 8 * d + 2 * tq) = make_float2(o[d][2 * hr], o[d][2 * hr + 1]);
+            if (tq == 0) {
+                part[DH] = hr ? m_1 : m_0;
+                part[DH + 1] = hr ? l_1 : l_0;
             }
         }
         __threadfence();
@@ -292,11 +353,7 @@ cudaError_t launch_seq_prepare(const SeqPrepParams& p, cudaStream_t s, bool pdl)
     return cudaLaunchKernelEx(&cfg, k_seq_prepare, p);
 }
 
-size_t attn_seq_smem() { return sizeof(float) * ((size_t)PM_SEQ_MAX_ROWS * DH + (size_t)DH * (KSUB + 1) + (size_t)KSUB * DH); }
-
-cudaError_t attn_seq_prepare() {
-    return cudaFuncSetAttribute(k_attn_seq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_seq_smem());
-}
+cudaError_t attn_seq_prepare() { return cudaSuccess; }
 
 int attn_seq_max_chunks(int win) { return (win + PM_SEQ_MAX_ROWS - 1 + PM_SEQ_KPC - 1) / PM_SEQ_KPC; }
 
@@ -307,7 +364,6 @@ cudaError_t launch_attn_seq(const AttnSeqParams& p, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3(SEQ_NT);
-    cfg.dynamicSmemBytes = attn_seq_smem();
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
