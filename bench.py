@@ -163,6 +163,77 @@ def cpu_baseline_sample(budget_s: float = 15.0, max_frames: int = 64):
                       f"host cores, {dt:.1f} s"}
 
 
+def run_case(args):
+    """Secondary workloads, one JSON line each (not the headline step):
+
+    prefill  one stream's history in passes of 64 frames (pm_prefill): ms per pass at
+             positions 0 and 2000 (--warmup untimed then --steps timed passes each), and,
+             with --full 1, a 3000-frame history primed from reset
+    sample   the standalone sampler (pm_sample) at the released text / audio settings and
+             a wide top-k, 1 / 8 / 64 rows of N(0, 3^2) logits
+    """
+    import torch
+    from full_duplex_speech_moshi_gb300 import pm
+
+    torch.cuda.set_device(0)
+    s = I.FULL if args.layers == 32 else I.ModelShape(n_layers=args.layers)
+    dev = "cuda"
+    stream = torch.cuda.current_stream()
+    W = I.make_weights_device(s, depformer=False, seed=1000, device=dev)
+    cfg = pm.make_config(s.asdict(), 1, False)
+    kv = pm.alloc_kv_cache(cfg)
+    ctx = pm.Context(s.asdict(), W, kv, B_max=1, depformer=False, stream=stream.cuda_stream)
+    lg = torch.empty((1, s.text_out), dtype=torch.float32, device=dev)
+    hid = torch.empty((1, s.D), dtype=torch.float32, device=dev)
+    tok = torch.empty((1,), dtype=torch.int32, device=dev)
+
+    def timed(fn, n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for i in range(n):
+            fn(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    line = {"case": args.case, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "data": "synthetic (random-init bf16 weights, seeded IDs)",
+            "config": {"layers": s.n_layers, "D": s.D, "heads": s.H, "ctx": s.ctx}}
+    if args.case == "prefill":
+        ids = torch.from_numpy(I.make_ids(s, s.ctx, seed=2003)[:, 0].copy()).to(dev)
+        ctx.prefill(0, 128, ids[:128], lg, hid, tok)   # captures the pass graphs
+        ctx.reset()
+        pass_ms = {}
+        for start in (0, 2000):
+            def one(i, start=start):
+                ctx.set_positions([start])
+                ctx.prefill(0, 64, ids[start:start + 64], lg, hid, tok)
+            timed(one, args.warmup)
+            pass_ms[str(start)] = timed(one, args.steps)
+        line.update({"metric": "prefill pass ms (64 frames of one stream)", "pass_ms": pass_ms,
+                     "unit": "ms", "higher_is_better": False, "value": pass_ms["2000"]})
+        if args.full:
+            ctx.reset()
+            ms = timed(lambda i: ctx.prefill(0, s.ctx, ids, lg, hid, tok), 1)
+            line.update({"metric": f"prefill frames/s ({s.ctx}-frame history from reset, B=1)",
+                         "value": s.ctx / (ms / 1000.0), "unit": "frames/s", "higher_is_better": True})
+    else:
+        x = torch.randn(64, 32000, device=dev, generator=torch.Generator(dev).manual_seed(5)) * 3.0
+        out = torch.empty(64, dtype=torch.int32, device=dev)
+        us = {}
+        for V, k, T in ((32000, 25, 0.7), (2048, 250, 0.8), (32000, 1024, 0.7)):
+            for rows in (1, 8, 64):
+                def one(i, V=V, k=k, T=T, rows=rows):
+                    ctx.sample(rows, x, V, 32000, T, k, 1, i, 0, out)
+                timed(one, args.warmup)
+                us[f"V{V}_k{k}_rows{rows}"] = 1000.0 * timed(one, args.steps)
+        line.update({"metric": "sampler us per call", "us": us, "unit": "us", "higher_is_better": False,
+                     "value": us["V32000_k25_rows1"]})
+    ctx.close()
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -176,10 +247,15 @@ def main():
                     help="conversations per step (1 = the workload; 8 = the metric's batched case)")
     ap.add_argument("--layers", type=int, default=32,
                     help="temporal blocks (32 = the workload; fewer only for small profiler captures)")
+    ap.add_argument("--case", default="frame", choices=["frame", "prefill", "sample"],
+                    help="frame = the headline decode step; prefill / sample = secondary workloads")
+    ap.add_argument("--full", type=int, default=1, help="prefill case: also prime a full history")
     args = ap.parse_args()
     assert args.warmup >= 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.case != "frame":
+        return run_case(args)
 
     import torch
     from full_duplex_speech_moshi_gb300 import pm
