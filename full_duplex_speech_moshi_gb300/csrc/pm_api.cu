@@ -87,6 +87,7 @@ struct pm_ctx {
     std::string err;
     size_t tc_part_floats = 0;
     int tc_count_max = 0;
+    int ss_parts_max = 0;              // sum-of-squares partials the ss buffer holds (batched GEMV)
     // persistent batch-1 frame program (null when the shape or device does not allow it)
     bool prog = false;
     FPhase* d_phases = nullptr;
@@ -476,6 +477,24 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         PM_CUDA(launch_tc(A, X, N, p, s, pdl));
         return mark(c, s, kind);
     };
+    // 2 <= B <= 16 decode: the batched GEMV on warp-level MMAs (k_gemv_mma); its residual
+    // epilogues leave one sum-of-squares partial per CTA instead of one per 128-row tile
+    const bool mg = !seq && npad == 16;
+    int ss_parts = (D + 1023) / 1024;  // partials of the operand the next normed projection reads
+    auto go_mg = [&](TcParams& p, const uint16_t* w, uint64_t w_rows, const uint16_t* xop, int kind,
+                     const char* what) -> pm_status {
+        p.w = w;
+        p.xop = xop;
+        if (!plan_mg(p, c->num_sms)) return fail(c, PM_ERR_UNSUPPORTED, std::string("no batched GEMV plan for ") + what);
+        if (p.epi == TE_RESIDUAL && p.grid > c->ss_parts_max)
+            return fail(c, PM_ERR_UNSUPPORTED, std::string("sum-of-squares scratch too small for ") + what);
+        CUtensorMap maps[4];
+        if (!mg_tensor_maps(p, w, w_rows, xop, maps))
+            return fail(c, PM_ERR_CUDA, std::string("tensor map encoding failed for ") + what);
+        PM_CUDA(launch_mg(maps, p, s, pdl));
+        if (p.epi == TE_RESIDUAL) ss_parts = p.grid;
+        return mark(c, s, kind);
+    };
     // weight tensor maps of every projection (each kernel also prefetches the next one's head)
     std::vector<CUtensorMap> mq(f.n_layers), mwo(f.n_layers), mwi(f.n_layers), mwt(f.n_layers);
     for (int l = 0; l < f.n_layers; ++l)
@@ -494,7 +513,7 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         // RMSNorm1 (folded) + fused QKV + RoPE + KV append
         TcParams p = base(TE_QKV_ROPE, D, 3 * D / 128, 3 * D);
         p.ss_in = c->ss;
-        p.ss_parts = (l == 0) ? (D + 1023) / 1024 : D / 128;
+        p.ss_parts = ss_parts;
         p.y = c->q;
         p.y_stride = D;
         p.H = f.H;
@@ -506,7 +525,8 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         p.nx = next_tc(c, TE_RESIDUAL, D, D / 128, 0, npad);
         p.seq = seq ? 1 : 0;
         p.kv_new = c->seq_kv;
-        pm_status ps = go(mq[l], mx, mwo[l], p, PM_KERNEL_QKV, "in_proj");
+        pm_status ps = mg ? go_mg(p, c->in_proj[l], 3u * D, c->xb, PM_KERNEL_QKV, "in_proj")
+                          : go(mq[l], mx, mwo[l], p, PM_KERNEL_QKV, "in_proj");
         if (ps) return ps;
         if (seq) {
             AttnSeqParams aq;
@@ -560,16 +580,21 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         p.alpha_next = c->norm2[l];
         p.ss_out = c->ss;
         p.nx = next_tc(c, TE_SWIGLU, D, F / 64, F, npad);
-        if ((ps = go(mwo[l], mo, mwi[l], p, PM_KERNEL_OUT_PROJ, "out_proj"))) return ps;
+        ps = mg ? go_mg(p, c->out_proj[l], D, c->ob, PM_KERNEL_OUT_PROJ, "out_proj")
+                : go(mwo[l], mo, mwi[l], p, PM_KERNEL_OUT_PROJ, "out_proj");
+        if (ps) return ps;
+        if (!mg) ss_parts = D / 128;
         // RMSNorm2 (folded) + linear_in + SwiGLU -> bf16 s
         p = base(TE_SWIGLU, D, F / 64, F);
         p.ss_in = c->ss;
-        p.ss_parts = D / 128;
+        p.ss_parts = ss_parts;
         p.split_rows = F;
         p.yb = c->sb;
         p.yb_stride = F;
         p.nx = next_tc(c, TE_RESIDUAL, F, D / 128, 0, npad);
-        if ((ps = go(mwi[l], mx, mwt[l], p, PM_KERNEL_LINEAR_IN, "linear_in"))) return ps;
+        ps = mg ? go_mg(p, c->lin_in[l], 2u * F, c->xb, PM_KERNEL_LINEAR_IN, "linear_in")
+                : go(mwi[l], mx, mwt[l], p, PM_KERNEL_LINEAR_IN, "linear_in");
+        if (ps) return ps;
         // linear_out + residual; emits the next norm's operand
         p = base(TE_RESIDUAL, F, D / 128, D);
         p.y = c->x;
@@ -581,18 +606,22 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         const bool last = l + 1 == f.n_layers;
         p.nx = last ? next_tc(c, TE_HEAD, D, head_tiles, 0, npad)
                     : next_tc(c, TE_QKV_ROPE, D, 3 * D / 128, 0, npad);
-        if ((ps = go(mwt[l], msb, last ? mh : mq[l + 1], p, PM_KERNEL_LINEAR_OUT, "linear_out"))) return ps;
+        ps = mg ? go_mg(p, c->lin_out[l], D, c->sb, PM_KERNEL_LINEAR_OUT, "linear_out")
+                : go(mwt[l], msb, last ? mh : mq[l + 1], p, PM_KERNEL_LINEAR_OUT, "linear_out");
+        if (ps) return ps;
+        if (!mg) ss_parts = D / 128;
     }
     TcParams p = base(TE_HEAD, D, head_tiles, f.text_out);
     p.ss_in = c->ss;
-    p.ss_parts = D / 128;
+    p.ss_parts = ss_parts;
     p.h_internal = c->h;
     p.x_resid = c->x;
     p.alpha = c->out_norm;
     p.nx = next_tc(c, TE_QKV_ROPE, D, 3 * D / 128, 0, npad);  // the next frame's first projection
     if (c->text_smp) p.logits_copy = c->slog;
     p.seq = seq ? 1 : 0;
-    pm_status hs = go(mh, mx, mq[0], p, PM_KERNEL_HEAD, "text_linear");
+    pm_status hs = mg ? go_mg(p, c->text_linear, f.text_out, c->xb, PM_KERNEL_HEAD, "text_linear")
+                      : go(mh, mx, mq[0], p, PM_KERNEL_HEAD, "text_linear");
     if (hs) return hs;
     return record_text_sample(c, B, s, pdl, seq);
 }
@@ -938,6 +967,21 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
                 if (t.n_mtiles > tc_count_max) tc_count_max = t.n_mtiles;
             }
     }
+    // batched GEMV: one sum-of-squares partial per CTA of its residual projections
+    int ss_parts_max = 0;
+    for (int K : {f.D, f.ffn}) {
+        TcParams t;
+        memset(&t, 0, sizeof t);
+        t.epi = TE_RESIDUAL;
+        t.K = K;
+        t.n_rows = f.D;
+        t.B = 1;
+        t.npad = 16;
+        if (!plan_mg(t, c->num_sms)) return bail(PM_ERR_UNSUPPORTED, "a batched GEMV projection has no plan");
+        if (t.grid > ss_parts_max) ss_parts_max = t.grid;
+    }
+    c->ss_parts_max = ss_parts_max;
+    const size_t ss_floats = std::max((size_t)(f.D / 128) * NP, (size_t)ss_parts_max * 16);
     if (attn_seq_max_chunks(f.ctx) > PM_SEQ_MAX_CHUNKS)
         return bail(PM_ERR_UNSUPPORTED, "ctx too long for the prefill attention");
     c->npad_max = NP;
@@ -952,7 +996,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
         {&p_x, 4u * RM * f.D}, {&p_q, 4u * RM * f.D}, {&p_o, 4u * RM * f.D}, {&p_s, 4u * RM * f.ffn},
         {&p_h, 4u * BM * f.D}, {&p_part, 4u * BM * f.H * attn_max_splits(f.ctx) * (f.dh + 2)}, {&p_cnt, 4u * BM * f.H},
         {&p_freq, 8u * (f.dh / 2)}, {&p_rtab, 8u * RM * (f.dh / 2)},
-        {&p_xb, 2u * NP * f.D}, {&p_ob, 2u * NP * f.D}, {&p_sb, 2u * NP * f.ffn}, {&p_ss, 4u * (f.D / 128) * NP},
+        {&p_xb, 2u * NP * f.D}, {&p_ob, 2u * NP * f.D}, {&p_sb, 2u * NP * f.ffn}, {&p_ss, 4u * ss_floats},
         {&p_tcp, 4u * tc_part_floats}, {&p_tcc, 4u * (size_t)tc_count_max},
         {&p_dz, 4u * BM * (Dd ? Dd : 1)}, {&p_dq, 4u * BM * (Dd ? Dd : 1)},
         {&p_ds, 4u * BM * (Fd ? Fd : 1)},
@@ -1161,6 +1205,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     if (ck(sample_prepare())) return bail(PM_ERR_CUDA, "sample_prepare()");
     if (ck(attn_seq_prepare())) return bail(PM_ERR_CUDA, "attn_seq_prepare()");
     if (ck(tc_prepare())) return bail(PM_ERR_CUDA, "tc_prepare");
+    if (ck(mg_prepare())) return bail(PM_ERR_CUDA, "mg_prepare");
     if (ck(cudaDeviceSynchronize())) return bail(PM_ERR_CUDA, "cudaDeviceSynchronize()");
     *out = c;
     return PM_OK;

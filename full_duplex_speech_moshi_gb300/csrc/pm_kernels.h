@@ -290,9 +290,28 @@ struct TcParams {
     // row's outputs, positions advance by B)
     int seq;
     uint16_t* kv_new;        // [2][B][H][dh] bf16 (K rows, then V rows)
+    // batched GEMV path (k_gemv_mma, 2 <= B <= 16): plain pointers instead of tensor maps
+    const uint16_t* w;       // weights [rows][K] bf16
+    const uint16_t* xop;     // activation operand [16][K] bf16 (rows >= B are ignored)
+    int pre_stride;          // plan: floats per batch row of the staged epilogue operands
+    int h0;                  // plan: units of the smaller CTAs (the others own h0 + 1)
+    int kchunk;              // plan: k elements per stage
+    uint32_t stage_bytes;    // plan: bytes of one weight stage
+    int xm;                  // plan: stages per activation chunk
 };
 
 bool plan_tc(TcParams& p, int num_sms);
+
+// Batched decode projections, 2 <= B <= 16, as a weight-streaming GEMV on warp-level MMAs
+// (k_gemv_mma): same epilogues as the tensor-core path except TE_STORE; the sums of
+// squares it writes (TE_RESIDUAL) are per CTA: ss_out[c][npad] for c < grid.
+#define PM_MG_MAX_TILES 8    // 16-row tiles per CTA
+bool plan_mg(TcParams& p, int num_sms);
+// tensor maps of a planned projection: the weights [w_rows][K] with boxes of a full tile
+// and of the two last-tile remainders, and the activation operand [16][K]
+bool mg_tensor_maps(const TcParams& p, const uint16_t* w, uint64_t w_rows, const uint16_t* xop, CUtensorMap* m);
+cudaError_t launch_mg(const CUtensorMap* m, const TcParams& p, cudaStream_t s, bool pdl);
+cudaError_t mg_prepare();
 // `next`: tensor map of the next projection's weights (read when p.nx.n_mtiles > 0)
 cudaError_t launch_tc(const CUtensorMap& A, const CUtensorMap& Bop, const CUtensorMap& next, const TcParams& p,
                       cudaStream_t s, bool pdl);

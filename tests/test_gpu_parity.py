@@ -128,6 +128,34 @@ def test_batched_ragged_history(pair):
     assert pair.ctx.get_positions()[:B] == list(L + 4)
 
 
+@pytest.mark.parametrize("B", [12, 20])
+def test_batched_paths_by_batch_size(B):
+    """B = 12: the batched GEMV with two 8-column MMA groups (B <= 16); B = 20: the
+    tensor-core path (N = 32).  Streams start at staggered positions with seeded K/V
+    history and run past the ring's wrap."""
+    s = small_shape()
+    p = Pair(s, B_max=B, depformer=False)
+    try:
+        torch = p.torch
+        L = 1 + (np.arange(B, dtype=np.int32) * 7) % (s.ctx + 9)
+        for b in range(B):
+            for l in range(s.n_layers):
+                k, v = I.make_kv_history(s, int(L[b]), seed=31, layer=l, stream=b)
+                p.streams[b].load_kv(l, 0, k, v)
+                for p0 in range(int(L[b])):
+                    slot = p0 % s.ctx
+                    p.kv[l, 0, b, :, slot, :] = torch.from_numpy(k[:, p0, :].astype(np.int16)).view(torch.bfloat16).cuda()
+                    p.kv[l, 1, b, :, slot, :] = torch.from_numpy(v[:, p0, :].astype(np.int16)).view(torch.bfloat16).cuda()
+            p.streams[b].set_position(int(L[b]))
+        p.ctx.set_positions(list(L))
+        ids = I.make_ids(s, 3, B=B, seed=32)
+        for t in range(3):
+            p.check_frame(p.gpu_frame(ids[t], B=B), p.oracle_frame(ids[t]), f"B={B} t={t}")
+        assert p.ctx.get_positions()[:B] == list(L + 3)
+    finally:
+        p.close()
+
+
 def test_invalid_ids_leave_state_unchanged(pair):
     from full_duplex_speech_moshi_gb300 import pm
     s = pair.shape
