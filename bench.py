@@ -337,7 +337,9 @@ def main():
     else:
         dom_kind, dom_bytes = "linear_in_swiglu", W_IN_BYTES
         dom_name = ("RMSNorm + linear_in [22528,4096] + SwiGLU GEMV" if BB == 1 else
-                    f"RMSNorm + linear_in [22528,4096] + SwiGLU, tcgen05 GEMM N={16 if BB <= 16 else 64}")
+                    f"RMSNorm + linear_in [22528,4096] + SwiGLU, batched GEMV on warp-level bf16 MMAs, {BB} rows"
+                    if BB <= 16 else
+                    f"RMSNorm + linear_in [22528,4096] + SwiGLU, tcgen05 GEMM N={32 if BB <= 32 else 64}")
     dom_ms = statistics.mean(by_kind[dom_kind])
     achieved = dom_bytes / (dom_ms / 1000.0) / 1e9
 

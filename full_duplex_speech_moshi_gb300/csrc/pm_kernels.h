@@ -295,9 +295,6 @@ struct TcParams {
     const uint16_t* xop;     // activation operand [16][K] bf16 (rows >= B are ignored)
     int pre_stride;          // plan: floats per batch row of the staged epilogue operands
     int h0;                  // plan: units of the smaller CTAs (the others own h0 + 1)
-    int kchunk;              // plan: k elements per stage
-    uint32_t stage_bytes;    // plan: bytes of one weight stage
-    int xm;                  // plan: stages per activation chunk
 };
 
 bool plan_tc(TcParams& p, int num_sms);
