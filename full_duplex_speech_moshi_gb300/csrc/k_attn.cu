@@ -5,22 +5,28 @@
 //
 // For batch row b at position p the visible keys are positions max(0, p-win+1) .. p,
 // stored at ring slots position mod ctx (win = ctx for the declared mask, ctx - 1 for the
-// pinned ring's labels, which hide the oldest key of a full ring).  Work item (b, h, c) is the 64 keys
-// lo + 64c .. lo + 64c + 63 of row b's window for head h.  The items of all rows form one
-// list whose length follows the device-resident positions; a fixed grid of CTAs walks it
-// with a grid stride, so the launch does not grow with the context.  128 threads = 4
-// warps; in a warp, lane group g (8 lanes) takes 4 keys and lane i of the group 16 of
-// the 128 coordinates, so a key row is one coalesced 256-byte read.
+// pinned ring's labels, which hide the oldest key of a full ring).  A unit is the 64 keys
+// lo + 64c .. lo + 64c + 63 of row b's window for head h; the units of all rows, ordered
+// (row, head, chunk), are split into one contiguous, balanced range per CTA, derived on
+// the device from the positions, so a fixed grid serves any batch and cache length.
 //
-// Keys and values of positions before p were written by earlier frames, so each lane
-// loads its first item's K and V rows into registers before griddepcontrol.wait: with
-// programmatic dependent launch this overlaps the fused-QKV kernel that writes the
-// current position's K/V and the query.  Scores use the base-2 exponential with the
-// query pre-scaled by log2(e)/sqrt(128) (the same softmax).  Running (max, sum, weighted
-// values) merge across lane groups (shuffles), warps (shared memory) and finally across
-// the chunks of a (b, h) in the CTA that finishes last (completion counter, nothing
-// waits), which stages the chunk maxima in shared memory and reads the partial vectors
-// with independent loads.
+// The kernel streams K/V like the projections stream weights:
+//  * a producer thread copies each unit's K rows and V rows (16 KB each, contiguous
+//    ring slots; two copies where the chunk wraps) into a ring of 32 KB shared-memory
+//    stages with 1-D bulk copies.  Every key but the current position was written by
+//    earlier frames, so the first ring is issued before griddepcontrol.wait and overlaps
+//    the fused-QKV kernel that is still writing the current K/V and the query;
+//  * four consumer warps take a unit at a time: the current position's K/V row (written by
+//    the kernel this one waited for) is loaded into its slot after the wait; scores with
+//    two lanes per key (64 dims each, reads staggered across the 16-byte columns so a
+//    quarter-warp touches 32 distinct banks), the base-2 exponential with the query
+//    pre-scaled by log2(e)/sqrt(128) (the same softmax), a running max / sum / weighted
+//    value (thread t owns coordinate t) carried across the CTA's units of one head;
+//  * a head whose units all fall in one CTA is written out directly; a head cut between
+//    CTAs leaves one partial (weighted values, max, sum) per piece, and the CTA that
+//    finishes last merges them in piece order (completion counter, nothing waits);
+//  * stages are handed back to the copy engine after a proxy fence (generic-proxy reads
+//    before the async-proxy refill).
 #include <math.h>
 
 #include "pm_kernels.h"
@@ -29,209 +35,300 @@ namespace pm {
 namespace {
 
 constexpr int DH = 128;
-constexpr int KPC = 64;    // keys per CTA item
-constexpr int KPG = 4;     // keys per lane group (4 warps x 4 groups x 4 keys = 64)
-constexpr int MAX_CHUNKS = 64;  // chunks per (b, h) the merge stages in shared memory (ctx <= 4096)
+constexpr int KPC = 64;                     // keys per unit
+constexpr int NST = 3;                      // stages per CTA
+constexpr int ROWB = DH * 2;                // bytes per K or V row
+constexpr int STAGE = 2 * KPC * ROWB;       // K rows then V rows: 32 KB
+constexpr int THREADS = 160;                // 4 consumer warps + producer warp
+constexpr int MAX_PIECES = 64;              // pieces a head can be cut into (>= chunks per head)
 
-__device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float* v) {
-    v[0] = bf16lo(a.x); v[1] = bf16hi(a.x); v[2] = bf16lo(a.y); v[3] = bf16hi(a.y);
-    v[4] = bf16lo(a.z); v[5] = bf16hi(a.z); v[6] = bf16lo(a.w); v[7] = bf16hi(a.w);
-    v[8] = bf16lo(b.x); v[9] = bf16hi(b.x); v[10] = bf16lo(b.y); v[11] = bf16hi(b.y);
-    v[12] = bf16lo(b.z); v[13] = bf16hi(b.z); v[14] = bf16lo(b.w); v[15] = bf16hi(b.w);
+__device__ __forceinline__ int n_chunks(int pos, int win) { return (min(pos + 1, win) + KPC - 1) / KPC; }
+
+__host__ __device__ __forceinline__ long long unit_begin(int c, long long U, int G) { return (long long)c * U / G; }
+
+// CTA whose unit range contains unit u
+__device__ __forceinline__ int cta_of(long long u, long long U, int G) {
+    int c = (int)(u * G / U);
+    while (c + 1 < G && unit_begin(c + 1, U, G) <= u) ++c;
+    while (c > 0 && unit_begin(c, U, G) > u) --c;
+    return c;
 }
 
-__device__ __forceinline__ int n_chunks(int pos, int ctx) { return (min(pos + 1, ctx) + KPC - 1) / KPC; }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
-__global__ void __launch_bounds__(128) k_attn(const AttnParams p) {
-    __shared__ int s_first[PM_MAX_B_DEV + 1];  // prefix of chunk counts over batch rows
-    __shared__ float s_m[4], s_l[4];
-    __shared__ float s_acc[4][DH];
-    __shared__ float s_pm[MAX_CHUNKS], s_pl[MAX_CHUNKS];
-    __shared__ int s_last;
+__device__ __forceinline__ void cons_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+struct UnitPos {
+    int b, h, ci, nc;     // row, head, chunk index, chunks of the head
+    int pos, key0, key1;  // query position, first key, one past the last key of the chunk
+};
+
+__device__ __forceinline__ UnitPos decode_unit(long long u, const int* s_first, const int* s_nc, const int* s_pos,
+                                               int B, int H, int win) {
+    UnitPos r;
+    int b = 0;
+    while (b + 1 < B && u >= s_first[b + 1]) ++b;
+    const int nc = s_nc[b];
+    const int rel = (int)(u - s_first[b]);
+    r.b = b;
+    r.h = rel / nc;
+    r.ci = rel % nc;
+    r.nc = nc;
+    r.pos = s_pos[b];
+    const int n = min(r.pos + 1, win), lo = r.pos - n + 1;
+    r.key0 = lo + KPC * r.ci;
+    r.key1 = min(r.key0 + KPC, r.pos + 1);
+    return r;
+}
+
+__global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
+    extern __shared__ __align__(128) uint8_t ring[];  // [NST][STAGE]
+    __shared__ int s_first[PM_MAX_B_DEV + 1], s_nc[PM_MAX_B_DEV], s_pos[PM_MAX_B_DEV];
+    __shared__ __align__(8) uint64_t full[NST], empty[NST];
+    __shared__ __align__(16) float s_q[DH];
+    __shared__ __align__(16) float s_p[KPC];
+    __shared__ float s_wm[4], s_wl[4];
+    __shared__ float s_pm[MAX_PIECES], s_pl[MAX_PIECES];
+    __shared__ int s_flags[4];  // [0] timeout, [1] last piece of a head, [2] units issued
+
     pdl_trigger();
-    // positions do not change within a frame (only the final text-head kernel advances
-    // them), so every row's window, and the whole work list, is known before the wait
-    if (threadIdx.x == 0) {
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    // positions change only in the frame's last kernel, so every row's window, and the
+    // whole unit list, is known before the wait
+    if (t < p.B) {
+        const int pos = p.st.pos[t];
+        s_pos[t] = pos;
+        s_nc[t] = p.H * n_chunks(pos, p.win);
+    }
+    if (t == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 4);
+        }
+        fence_barrier_init();
+        s_flags[0] = 0;
+        s_flags[1] = 0;
+        s_flags[2] = 0;
+    }
+    __syncthreads();
+    if (t == 0) {
         int acc = 0;
         for (int bb = 0; bb < p.B; ++bb) {
             s_first[bb] = acc;
-            acc += p.H * n_chunks(p.st.pos[bb], p.win);
+            acc += s_nc[bb];
+            s_nc[bb] /= p.H;  // chunks per head
         }
         s_first[p.B] = acc;
     }
     __syncthreads();
-    const int total = s_first[p.B];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 3, sub = lane & 7;
-    const int t = threadIdx.x;
-    bool waited = false;
+    const long long U = s_first[p.B];
+    const int G = gridDim.x, c = blockIdx.x;
+    const long long u0 = unit_begin(c, U, G), u1 = unit_begin(c + 1, U, G);
+    const int nu = (int)(u1 - u0);
+    if (nu <= 0) return;
 
-    for (int item = blockIdx.x; item < total; item += gridDim.x) {
-        int b = 0;
-        while (item >= s_first[b + 1]) ++b;
-        const int pos = p.st.pos[b];
-        const int n = min(pos + 1, p.win);
-        const int lo = pos - n + 1;
-        const int nc = (n + KPC - 1) / KPC;
-        const int h = (item - s_first[b]) / nc;
-        const int ci = (item - s_first[b]) % nc;
-        const int k0 = lo + ci * KPC + warp * 16 + g * KPG;  // this lane group's first key
-        const int k1 = pos + 1;
+    if (warp == 4) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            for (int k = 0; k < nu; ++k) {
+                const int slot = k % NST;
+                if (k >= NST && !mbar_wait(&empty[slot], (uint32_t)((k / NST) - 1) & 1u)) {
+                    s_flags[0] = 1;
+                    set_status(p.st.status, PM_DEV_ERR_TIMEOUT);
+                    break;
+                }
+                const UnitPos up = decode_unit(u0 + k, s_first, s_nc, s_pos, p.B, p.H, p.win);
+                // keys before the current position only: that row is written by the kernel
+                // this one overlaps
+                const int nk = max(0, min(up.key1, up.pos) - up.key0);
+                mbar_arrive_expect_tx(&full[slot], 2u * (uint32_t)nk * ROWB);
+                if (nk > 0) {
+                    const size_t head = ((size_t)up.b * p.H + up.h) * (size_t)p.ctx * DH;
+                    const int s0 = up.key0 % p.ctx;
+                    const int n1 = min(nk, p.ctx - s0), n2 = nk - n1;
+                    uint8_t* dk = ring + (size_t)slot * STAGE;
+                    uint8_t* dv = dk + KPC * ROWB;
+                    bulk_g2s(dk, p.kc + head + (size_t)s0 * DH, (uint32_t)n1 * ROWB, &full[slot], pol);
+                    bulk_g2s(dv, p.vc + head + (size_t)s0 * DH, (uint32_t)n1 * ROWB, &full[slot], pol);
+                    if (n2 > 0) {
+                        bulk_g2s(dk + n1 * ROWB, p.kc + head, (uint32_t)n2 * ROWB, &full[slot], pol);
+                        bulk_g2s(dv + n1 * ROWB, p.vc + head, (uint32_t)n2 * ROWB, &full[slot], pol);
+                    }
+                }
+                s_flags[2] = k + 1;
+            }
+        }
+    } else {
+        // ------------------------------ consumers ------------------------------
+        pdl_wait();
+        const bool aborted = *(volatile uint32_t*)&p.st.status[1] != 0u;
+        float m_run = -INFINITY, l_run = 0.f, acc = 0.f;
+        int seg_ci0 = 0;  // first chunk of the current piece of a head
+        bool ok = true;
+        for (int k = 0; k < nu; ++k) {
+            const int slot = k % NST;
+            const UnitPos up = decode_unit(u0 + k, s_first, s_nc, s_pos, p.B, p.H, p.win);
+            const bool first = (k == 0) || up.ci == 0;
+            if (first && !aborted) {
+                // this piece's query, pre-scaled for the base-2 exponential
+                s_q[t] = __ldcg(p.q + (size_t)up.b * p.D + up.h * DH + t) * p.scale_log2;
+                m_run = -INFINITY;
+                l_run = 0.f;
+                acc = 0.f;
+                seg_ci0 = up.ci;
+            }
+            if (!mbar_wait(&full[slot], (uint32_t)(k / NST) & 1u)) {
+                ok = false;
+                break;
+            }
+            uint8_t* st = ring + (size_t)slot * STAGE;
+            const int nvalid = up.key1 - up.key0;
+            if (!aborted) {
+                if (up.key1 == up.pos + 1 || first) {
+                    if (up.key1 == up.pos + 1) {
+                        // the current position's K and V rows, written by the kernel waited for
+                        const size_t row = (((size_t)up.b * p.H + up.h) * p.ctx + up.pos % p.ctx) * DH + t;
+                        const int r = up.pos - up.key0;
+                        reinterpret_cast<uint16_t*>(st + r * ROWB)[t] = __ldcg(p.kc + row);
+                        reinterpret_cast<uint16_t*>(st + KPC * ROWB + r * ROWB)[t] = __ldcg(p.vc + row);
+                    }
+                    cons_bar();  // that row, and a new piece's query, are in place
+                }
+                // scores: lanes 2j, 2j+1 of warp w take key 16w + j, 64 coordinates each
+                const int kk = 16 * warp + (lane >> 1), half = lane & 1;
+                float d0 = 0.f, d1 = 0.f;
+                if (kk < nvalid) {
+                    const uint8_t* kr = st + kk * ROWB + half * 128;
+                    const float* qh = s_q + half * 64;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int jc = (j + lane) & 7;  // staggered 16-byte column
+                        const uint4 kv = *reinterpret_cast<const uint4*>(kr + jc * 16);
+                        const float4 qa = *reinterpret_cast<const float4*>(qh + jc * 8);
+                        const float4 qb = *reinterpret_cast<const float4*>(qh + jc * 8 + 4);
+                        d0 = fmaf(qa.x, bf16lo(kv.x), d0);
+                        d1 = fmaf(qa.y, bf16hi(kv.x), d1);
+                        d0 = fmaf(qa.z, bf16lo(kv.y), d0);
+                        d1 = fmaf(qa.w, bf16hi(kv.y), d1);
+                        d0 = fmaf(qb.x, bf16lo(kv.z), d0);
+                        d1 = fmaf(qb.y, bf16hi(kv.z), d1);
+                        d0 = fmaf(qb.z, bf16lo(kv.w), d0);
+                        d1 = fmaf(qb.w, bf16hi(kv.w), d1);
+                    }
+                }
+                const float d = d0 + d1;
+                float sc = d + __shfl_xor_sync(0xffffffffu, d, 1);
+                if (kk >= nvalid) sc = -INFINITY;
+                // chunk maximum across the 4 warps, then weights against the running maximum
+                float wm = sc;
+#pragma unroll
+                for (int o = 2; o <= 16; o <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+                if (lane == 0) s_wm[warp] = wm;
+                cons_bar();
+                const float cm = fmaxf(fmaxf(s_wm[0], s_wm[1]), fmaxf(s_wm[2], s_wm[3]));
+                const float m_new = fmaxf(m_run, cm);
+                const float alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
+                const float pk = (kk < nvalid) ? exp2f(sc - m_new) : 0.f;
+                if (half == 0 && kk < KPC) s_p[kk] = pk;
+                float ws = half == 0 ? pk : 0.f;
+#pragma unroll
+                for (int o = 1; o <= 16; o <<= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+                if (lane == 0) s_wl[warp] = ws;
+                cons_bar();
+                // weighted values: thread t owns coordinate t
+                // (rows past nvalid hold stale data: they are skipped, never multiplied by 0)
+                const uint16_t* vcol = reinterpret_cast<const uint16_t*>(st + KPC * ROWB) + t;
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                const int n4 = nvalid & ~3;
+#pragma unroll 4
+                for (int j = 0; j < n4; j += 4) {
+                    const float4 pj = *reinterpret_cast<const float4*>(s_p + j);
+                    a0 = fmaf(pj.x, __uint_as_float((uint32_t)vcol[(j + 0) * DH] << 16), a0);
+                    a1 = fmaf(pj.y, __uint_as_float((uint32_t)vcol[(j + 1) * DH] << 16), a1);
+                    a2 = fmaf(pj.z, __uint_as_float((uint32_t)vcol[(j + 2) * DH] << 16), a2);
+                    a3 = fmaf(pj.w, __uint_as_float((uint32_t)vcol[(j + 3) * DH] << 16), a3);
+                }
+                for (int j = n4; j < nvalid; ++j) a0 = fmaf(s_p[j], __uint_as_float((uint32_t)vcol[j * DH] << 16), a0);
+                acc = acc * alpha + ((a0 + a1) + (a2 + a3));
+                l_run = l_run * alpha + ((s_wl[0] + s_wl[1]) + (s_wl[2] + s_wl[3]));
+                m_run = m_new;
+            }
+            // the stage goes back to the copy engine once every warp is done with it: order
+            // these reads before its refill
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            if (aborted) continue;
 
-        const size_t head_base = ((size_t)b * p.H + h) * (size_t)p.ctx * DH;
-        const uint16_t* kbase = p.kc + head_base + 16 * sub;
-        const uint16_t* vbase = p.vc + head_base + 16 * sub;
-        uint4 kr[KPG][2], vr[KPG][2];
-#pragma unroll
-        for (int it = 0; it < KPG; ++it) {
-            const int kk = k0 + it;
-            kr[it][0] = kr[it][1] = vr[it][0] = vr[it][1] = make_uint4(0, 0, 0, 0);
-            if (kk < k1 && kk != pos) {
-                const int slot = kk % p.ctx;
-                const uint4* kp = reinterpret_cast<const uint4*>(kbase + (size_t)slot * DH);
-                const uint4* vp = reinterpret_cast<const uint4*>(vbase + (size_t)slot * DH);
-                kr[it][0] = __ldg(kp);
-                kr[it][1] = __ldg(kp + 1);
-                vr[it][0] = __ldg(vp);
-                vr[it][1] = __ldg(vp + 1);
+            const bool last = (k == nu - 1) || up.ci == up.nc - 1;
+            if (!last) continue;
+            float* ob = p.o + (size_t)up.b * p.D + up.h * DH;
+            uint16_t* obb = p.ob ? p.ob + (size_t)up.b * p.D + up.h * DH : nullptr;
+            if (seg_ci0 == 0 && up.ci == up.nc - 1) {
+                // the whole head was this CTA's
+                const float v = acc / l_run;
+                ob[t] = v;
+                if (obb) obb[t] = f32_to_bf16_rne(v);
+                continue;
             }
-        }
-        if (!waited) {
-            pdl_wait();
-            waited = true;
-            if (*(volatile uint32_t*)&p.st.status[1] != 0u) return;
-        }
-        float q[16];
-        {
-            const float4* qp = reinterpret_cast<const float4*>(p.q + (size_t)b * p.D + h * DH + 16 * sub);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const float4 tq = qp[v];
-                q[4 * v + 0] = tq.x * p.scale_log2;
-                q[4 * v + 1] = tq.y * p.scale_log2;
-                q[4 * v + 2] = tq.z * p.scale_log2;
-                q[4 * v + 3] = tq.w * p.scale_log2;
+            // a piece of a head cut between CTAs: deposit, the last piece to arrive merges
+            const size_t hb = ((size_t)up.b * p.H + up.h) * p.S;
+            float* part = p.part + (hb + seg_ci0) * (DH + 2);
+            part[t] = acc;
+            if (t == 0) {
+                part[DH] = m_run;
+                part[DH + 1] = l_run;
             }
-        }
-        // the current position's row is written by the kernel this one waited for
-#pragma unroll
-        for (int it = 0; it < KPG; ++it)
-            if (k0 + it == pos) {
-                const int slot = pos % p.ctx;
-                const uint4* kp = reinterpret_cast<const uint4*>(kbase + (size_t)slot * DH);
-                const uint4* vp = reinterpret_cast<const uint4*>(vbase + (size_t)slot * DH);
-                kr[it][0] = __ldcg(kp);
-                kr[it][1] = __ldcg(kp + 1);
-                vr[it][0] = __ldcg(vp);
-                vr[it][1] = __ldcg(vp + 1);
+            __threadfence();
+            cons_bar();
+            const long long hs = (u0 + k) - up.ci;  // the head's first unit
+            const int cf = cta_of(hs, U, G), cl = cta_of(hs + up.nc - 1, U, G);
+            if (t == 0) {
+                const uint32_t done = atomicAdd(&p.count[(size_t)up.b * p.H + up.h], 1u);
+                s_flags[1] = (done == (uint32_t)(cl - cf)) ? 1 : 0;
             }
-
-        float sc[KPG];
-        float m = -INFINITY;
-#pragma unroll
-        for (int it = 0; it < KPG; ++it) {
-            float kv[16];
-            unpack16(kr[it][0], kr[it][1], kv);
-            float d = 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; ++e) d = fmaf(q[e], kv[e], d);
-            d += __shfl_xor_sync(0xffffffffu, d, 1);
-            d += __shfl_xor_sync(0xffffffffu, d, 2);
-            d += __shfl_xor_sync(0xffffffffu, d, 4);
-            sc[it] = (k0 + it < k1) ? d : -INFINITY;
-            m = fmaxf(m, sc[it]);
-        }
-        float l = 0.f, acc[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-        if (m != -INFINITY) {
-#pragma unroll
-            for (int it = 0; it < KPG; ++it) {
-                const float w = exp2f(sc[it] - m);  // exp2(-inf) = 0 for keys past the window
-                l += w;
-                float vv[16];
-                unpack16(vr[it][0], vr[it][1], vv);
-#pragma unroll
-                for (int e = 0; e < 16; ++e) acc[e] = fmaf(w, vv[e], acc[e]);
+            cons_bar();
+            if (!s_flags[1]) continue;
+            __threadfence();
+            // pieces in order: piece i starts at the head's first unit in CTA cf + i
+            const int np = cl - cf + 1;
+            for (int i = t; i < np; i += 128) {
+                const long long st_u = unit_begin(cf + i, U, G);
+                const int ci = (int)((st_u > hs ? st_u : hs) - hs);
+                s_pm[i] = __ldcg(p.part + (hb + ci) * (DH + 2) + DH);
+                s_pl[i] = __ldcg(p.part + (hb + ci) * (DH + 2) + DH + 1);
             }
-        }
-        // merge the 4 lane groups of the warp (lanes with equal `sub` hold the same coordinates)
-#pragma unroll
-        for (int off = 8; off <= 16; off <<= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-            const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
-            const float mn = fmaxf(m, m2);
-            const float fa = (m == -INFINITY) ? 0.f : exp2f(m - mn);
-            const float fb = (m2 == -INFINITY) ? 0.f : exp2f(m2 - mn);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const float a2 = __shfl_xor_sync(0xffffffffu, acc[e], off);
-                acc[e] = acc[e] * fa + a2 * fb;
+            cons_bar();
+            float M = -INFINITY;
+            for (int i = 0; i < np; ++i) M = fmaxf(M, s_pm[i]);
+            float L = 0.f, A = 0.f;
+            for (int i = 0; i < np; ++i) {
+                const long long st_u = unit_begin(cf + i, U, G);
+                const int ci = (int)((st_u > hs ? st_u : hs) - hs);
+                const float f = (s_pm[i] == -INFINITY) ? 0.f : exp2f(s_pm[i] - M);
+                L += s_pl[i] * f;
+                A += __ldcg(p.part + (hb + ci) * (DH + 2) + t) * f;
             }
-            l = l * fa + l2 * fb;
-            m = mn;
+            const float v = A / L;
+            ob[t] = v;
+            if (obb) obb[t] = f32_to_bf16_rne(v);
+            if (t == 0) p.count[(size_t)up.b * p.H + up.h] = 0u;
+            cons_bar();
         }
-        // merge the 4 warps in shared memory; thread t owns coordinate t
-        if (g == 0) {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) s_acc[warp][16 * sub + e] = acc[e];
-            if (sub == 0) {
-                s_m[warp] = m;
-                s_l[warp] = l;
-            }
+        if (!ok) {
+            s_flags[0] = 1;
+            set_status(p.st.status, PM_DEV_ERR_TIMEOUT);
         }
-        __syncthreads();
-        float M = -INFINITY;
-        for (int w = 0; w < 4; ++w) M = fmaxf(M, s_m[w]);
-        float L = 0.f, A = 0.f;
-        for (int w = 0; w < 4; ++w) {
-            const float f = (s_m[w] == -INFINITY) ? 0.f : exp2f(s_m[w] - M);
-            L += s_l[w] * f;
-            A += s_acc[w][t] * f;
-        }
-        float* ob = p.o + (size_t)b * p.D + h * DH;
-        uint16_t* obb = p.ob ? p.ob + (size_t)b * p.D + h * DH : nullptr;
-        if (nc == 1) {
-            ob[t] = A / L;
-            if (obb) obb[t] = f32_to_bf16_rne(A / L);
-            __syncthreads();  // shared partials are reused by the next item
-            continue;
-        }
-        float* part = p.part + (((size_t)b * p.H + h) * p.S + ci) * (DH + 2);
-        part[t] = A;
-        if (t == 0) {
-            part[DH] = M;
-            part[DH + 1] = L;
-        }
-        __threadfence();
-        __syncthreads();
-        if (t == 0) {
-            const uint32_t done = atomicAdd(&p.count[(size_t)b * p.H + h], 1u);
-            s_last = (done == (uint32_t)nc - 1u) ? 1 : 0;
-        }
-        __syncthreads();
-        if (!s_last) continue;
-        // last chunk of (b, h): merge every chunk in slot order with loads in parallel
-        __threadfence();
-        const float* pb = p.part + ((size_t)b * p.H + h) * p.S * (DH + 2);
-        for (int i = t; i < nc; i += 128) {
-            s_pm[i] = __ldcg(pb + (size_t)i * (DH + 2) + DH);
-            s_pl[i] = __ldcg(pb + (size_t)i * (DH + 2) + DH + 1);
-        }
-        __syncthreads();
-        float Mx = -INFINITY;
-        for (int i = 0; i < nc; ++i) Mx = fmaxf(Mx, s_pm[i]);
-        float Lx = 0.f, Ax = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < nc; ++i) {
-            const float f = (s_pm[i] == -INFINITY) ? 0.f : exp2f(s_pm[i] - Mx);
-            Lx += s_pl[i] * f;
-            Ax += __ldcg(pb + (size_t)i * (DH + 2) + t) * f;
-        }
-        ob[t] = Ax / Lx;
-        if (obb) obb[t] = f32_to_bf16_rne(Ax / Lx);
-        if (t == 0) p.count[(size_t)b * p.H + h] = 0u;
-        __syncthreads();
+    }
+    __syncthreads();
+    if (s_flags[0] && t == 128) {
+        // a wait ran out: let the copies already issued land before the CTA exits
+        const int issued = s_flags[2];
+        for (int i = issued - NST < 0 ? 0 : issued - NST; i < issued; ++i)
+            (void)mbar_wait(&full[i % NST], (uint32_t)(i / NST) & 1u);
     }
 }
 
@@ -239,13 +336,18 @@ __global__ void __launch_bounds__(128) k_attn(const AttnParams p) {
 
 int attn_max_splits(int ctx) { return (ctx + KPC - 1) / KPC; }
 
+cudaError_t attn_prepare() {
+    return cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, NST * STAGE);
+}
+
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
-    if (p.S < attn_max_splits(p.ctx) || p.S > MAX_CHUNKS || p.B > PM_MAX_B_DEV || p.grid < 1 || p.win < 1 ||
-        p.win > p.ctx)
+    if (p.S < attn_max_splits(p.ctx) || p.S > MAX_PIECES || p.B > PM_MAX_B_DEV || p.grid < 1 || p.win < 1 ||
+        p.win > p.ctx || p.D != p.H * DH)
         return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = NST * STAGE;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

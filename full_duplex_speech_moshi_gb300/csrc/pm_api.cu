@@ -327,7 +327,7 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
         ap.ctx = f.ctx;
         ap.S = attn_max_splits(f.ctx);
         ap.win = f.ctx - ((f.flags & PM_FLAG_PINNED_RING) ? 1 : 0);
-        ap.grid = (B == 1 ? 4 : 16) * c->num_sms;
+        ap.grid = 2 * c->num_sms;
         ap.D = D;
         ap.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dh));
         PM_CUDA(launch_attn(ap, s, pdl));
@@ -566,7 +566,7 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         ap.ctx = f.ctx;
         ap.S = attn_max_splits(f.ctx);
         ap.win = f.ctx - ((f.flags & PM_FLAG_PINNED_RING) ? 1 : 0);
-        ap.grid = (B == 1 ? 4 : 16) * c->num_sms;
+        ap.grid = 2 * c->num_sms;
         ap.D = D;
         ap.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dh));
         if (!seq) PM_CUDA(launch_attn(ap, s, pdl));
@@ -1206,6 +1206,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     if (ck(attn_seq_prepare())) return bail(PM_ERR_CUDA, "attn_seq_prepare()");
     if (ck(tc_prepare())) return bail(PM_ERR_CUDA, "tc_prepare");
     if (ck(mg_prepare())) return bail(PM_ERR_CUDA, "mg_prepare");
+    if (ck(attn_prepare())) return bail(PM_ERR_CUDA, "attn_prepare");
     if (ck(cudaDeviceSynchronize())) return bail(PM_ERR_CUDA, "cudaDeviceSynchronize()");
     *out = c;
     return PM_OK;

@@ -127,10 +127,11 @@ struct AttnParams {
     DevState st;
     int B, H, ctx, S, D;
     int win;               // most keys a query sees (ctx, or ctx - 1 for the pinned ring)
-    int grid;              // CTAs walking the work list
+    int grid;              // CTAs sharing the unit list (2 per SM)
     float scale_log2;      // log2(e) / sqrt(dh)
 };
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl);
+cudaError_t attn_prepare();  // opt-in shared memory of the attention kernel
 // chunks (CTAs per head) the attention grid needs for a window of ctx keys; AttnParams.S
 // must be at least this and `part` must hold S chunks per head
 int attn_max_splits(int ctx);
