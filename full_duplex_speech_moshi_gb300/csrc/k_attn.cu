@@ -6,9 +6,14 @@
 // For batch row b at position p the visible keys are positions max(0, p-win+1) .. p,
 // stored at ring slots position mod ctx (win = ctx for the declared mask, ctx - 1 for the
 // pinned ring's labels, which hide the oldest key of a full ring).  A unit is the 64 keys
-// lo + 64c .. lo + 64c + 63 of row b's window for head h; the units of all rows, ordered
-// (row, head, chunk), are split into one contiguous, balanced range per CTA, derived on
-// the device from the positions, so a fixed grid serves any batch and cache length.
+// lo + 64c .. lo + 64c + 63 of row b's window for head h.  Two ways to share them out,
+// both derived on the device from the positions so a captured graph serves any cache
+// length: when the batch's heads fit one wave, each head gets a cluster of CS CTAs
+// (CS = 8 at B = 1, 4 at B = 2, 2 at B = 4, 1 at B = 8), each taking a contiguous share of
+// the head's units, and the pieces meet in the leader CTA's shared memory through
+// distributed shared memory and a cluster barrier (no global round trip); otherwise the
+// units of all rows, ordered (row, head, chunk), are split into one contiguous, balanced
+// range per CTA (ragged and large batches).
 //
 // The kernel streams K/V like the projections stream weights:
 //  * a producer thread copies each unit's K rows and V rows (16 KB each, contiguous
@@ -22,9 +27,10 @@
 //    quarter-warp touches 32 distinct banks), the base-2 exponential with the query
 //    pre-scaled by log2(e)/sqrt(128) (the same softmax), a running max / sum / weighted
 //    value (thread t owns coordinate t) carried across the CTA's units of one head;
-//  * a head whose units all fall in one CTA is written out directly; a head cut between
-//    CTAs leaves one partial (weighted values, max, sum) per piece, and the CTA that
-//    finishes last merges them in piece order (completion counter, nothing waits);
+//  * a head whose units all fall in one CTA is written out directly; in the balanced split a
+//    head cut between CTAs leaves one partial (weighted values, max, sum) per piece in
+//    global memory and the CTA that finishes last merges them in piece order (completion
+//    counter, nothing waits);
 //  * stages are handed back to the copy engine after a proxy fence (generic-proxy reads
 //    before the async-proxy refill).
 #include <math.h>
@@ -36,11 +42,16 @@ namespace {
 
 constexpr int DH = 128;
 constexpr int KPC = 64;                     // keys per unit
-constexpr int NST = 3;                      // stages per CTA
+#ifndef PM_ATTN_NST
+#define PM_ATTN_NST 3
+#endif
+constexpr int NST = PM_ATTN_NST;            // stages per CTA (tuning: fewer let the CTAs share
+                                            // an SM with the projection kernels around them)
 constexpr int ROWB = DH * 2;                // bytes per K or V row
 constexpr int STAGE = 2 * KPC * ROWB;       // K rows then V rows: 32 KB
 constexpr int THREADS = 160;                // 4 consumer warps + producer warp
 constexpr int MAX_PIECES = 64;              // pieces a head can be cut into (>= chunks per head)
+constexpr int MAX_CLUSTER = 8;              // CTAs per head in head-per-cluster mode
 
 __device__ __forceinline__ int n_chunks(int pos, int win) { return (min(pos + 1, win) + KPC - 1) / KPC; }
 
@@ -59,6 +70,18 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 __device__ __forceinline__ void cons_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// every thread of every CTA of the cluster; stores before it are visible after it
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// store to the same shared-memory variable of CTA `rank` of this cluster
+__device__ __forceinline__ void dsmem_store(const void* local, uint32_t rank, float v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
 
 struct UnitPos {
     int b, h, ci, nc;     // row, head, chunk index, chunks of the head
@@ -92,6 +115,7 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
     __shared__ float s_wm[4], s_wl[4];
     __shared__ float s_pm[MAX_PIECES], s_pl[MAX_PIECES];
     __shared__ int s_flags[4];  // [0] timeout, [1] last piece of a head, [2] units issued
+    __shared__ float s_cpart[MAX_CLUSTER][DH + 2];  // head-per-cluster: the leader's inbox
 
     pdl_trigger();
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -125,9 +149,23 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
     __syncthreads();
     const long long U = s_first[p.B];
     const int G = gridDim.x, c = blockIdx.x;
-    const long long u0 = unit_begin(c, U, G), u1 = unit_begin(c + 1, U, G);
+    const int CS = p.cluster;
+    long long u0, u1;
+    int crank = 0, chd = 0;
+    if (CS > 0) {
+        // head-per-cluster: head chd owns CTAs chd*CS .. chd*CS+CS-1, each a contiguous share
+        chd = c / CS;
+        crank = c % CS;
+        const int b = chd / p.H, h = chd % p.H, nc = s_nc[b];
+        const long long hs = s_first[b] + (long long)h * nc;
+        u0 = hs + (long long)crank * nc / CS;
+        u1 = hs + (long long)(crank + 1) * nc / CS;
+    } else {
+        u0 = unit_begin(c, U, G);
+        u1 = unit_begin(c + 1, U, G);
+    }
     const int nu = (int)(u1 - u0);
-    if (nu <= 0) return;
+    if (nu <= 0 && CS == 0) return;  // a cluster's CTAs all reach its barrier
 
     if (warp == 4) {
         // ------------------------------ producer ------------------------------
@@ -264,7 +302,7 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
             if (aborted) continue;
 
             const bool last = (k == nu - 1) || up.ci == up.nc - 1;
-            if (!last) continue;
+            if (!last || CS > 1) continue;  // pieces of a cluster's head meet in its leader
             float* ob = p.o + (size_t)up.b * p.D + up.h * DH;
             uint16_t* obb = p.ob ? p.ob + (size_t)up.b * p.D + up.h * DH : nullptr;
             if (seg_ci0 == 0 && up.ci == up.nc - 1) {
@@ -305,12 +343,26 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
             float M = -INFINITY;
             for (int i = 0; i < np; ++i) M = fmaxf(M, s_pm[i]);
             float L = 0.f, A = 0.f;
-            for (int i = 0; i < np; ++i) {
-                const long long st_u = unit_begin(cf + i, U, G);
-                const int ci = (int)((st_u > hs ? st_u : hs) - hs);
-                const float f = (s_pm[i] == -INFINITY) ? 0.f : exp2f(s_pm[i] - M);
-                L += s_pl[i] * f;
-                A += __ldcg(p.part + (hb + ci) * (DH + 2) + t) * f;
+            for (int i0 = 0; i0 < np; i0 += 8) {
+                // eight pieces' values loaded before any is combined (one round trip, not eight)
+                float v[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    v[j] = 0.f;
+                    if (i0 + j < np) {
+                        const long long st_u = unit_begin(cf + i0 + j, U, G);
+                        const int ci = (int)((st_u > hs ? st_u : hs) - hs);
+                        v[j] = __ldcg(p.part + (hb + ci) * (DH + 2) + t);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (i0 + j < np) {
+                        const float f = (s_pm[i0 + j] == -INFINITY) ? 0.f : exp2f(s_pm[i0 + j] - M);
+                        L += s_pl[i0 + j] * f;
+                        A += v[j] * f;
+                    }
+                }
             }
             const float v = A / L;
             ob[t] = v;
@@ -321,6 +373,31 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
         if (!ok) {
             s_flags[0] = 1;
             set_status(p.st.status, PM_DEV_ERR_TIMEOUT);
+        }
+        if (CS > 1 && !aborted) {
+            // this CTA's piece of the head (empty pieces: max -inf, sum 0) into the leader
+            dsmem_store(&s_cpart[crank][t], 0, acc);
+            if (t == 0) {
+                dsmem_store(&s_cpart[crank][DH], 0, m_run);
+                dsmem_store(&s_cpart[crank][DH + 1], 0, l_run);
+            }
+        }
+    }
+    if (CS > 1) {
+        cluster_sync_all();
+        if (crank == 0 && t < DH && *(volatile uint32_t*)&p.st.status[1] == 0u) {
+            float M = -INFINITY;
+            for (int i = 0; i < CS; ++i) M = fmaxf(M, s_cpart[i][DH]);
+            float L = 0.f, A = 0.f;
+            for (int i = 0; i < CS; ++i) {
+                const float f = (s_cpart[i][DH] == -INFINITY) ? 0.f : exp2f(s_cpart[i][DH] - M);
+                L += s_cpart[i][DH + 1] * f;
+                A += s_cpart[i][t] * f;
+            }
+            const int b = chd / p.H, h = chd % p.H;
+            const float v = A / L;
+            p.o[(size_t)b * p.D + h * DH + t] = v;
+            if (p.ob) p.ob[(size_t)b * p.D + h * DH + t] = f32_to_bf16_rne(v);
         }
     }
     __syncthreads();
@@ -336,6 +413,19 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
 
 int attn_max_splits(int ctx) { return (ctx + KPC - 1) / KPC; }
 
+void attn_plan(AttnParams& p, int num_sms) {
+    const int slots = 2 * num_sms;  // resident CTAs
+    if (p.B * p.H <= slots) {
+        int cs = 1;
+        while (cs < MAX_CLUSTER && p.B * p.H * cs * 2 <= slots) cs *= 2;
+        p.cluster = cs;
+        p.grid = p.B * p.H * cs;
+    } else {
+        p.cluster = 0;
+        p.grid = slots;
+    }
+}
+
 cudaError_t attn_prepare() {
     return cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, NST * STAGE);
 }
@@ -344,16 +434,29 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
     if (p.S < attn_max_splits(p.ctx) || p.S > MAX_PIECES || p.B > PM_MAX_B_DEV || p.grid < 1 || p.win < 1 ||
         p.win > p.ctx || p.D != p.H * DH)
         return cudaErrorInvalidValue;
+    if (p.cluster < 0 || p.cluster > MAX_CLUSTER || (p.cluster > 0 && p.grid != p.B * p.H * p.cluster))
+        return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = NST * STAGE;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (p.cluster > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)p.cluster;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = (unsigned)na;
     return cudaLaunchKernelEx(&cfg, k_attn, p);
 }
 

@@ -327,7 +327,7 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
         ap.ctx = f.ctx;
         ap.S = attn_max_splits(f.ctx);
         ap.win = f.ctx - ((f.flags & PM_FLAG_PINNED_RING) ? 1 : 0);
-        ap.grid = 2 * c->num_sms;
+        attn_plan(ap, c->num_sms);
         ap.D = D;
         ap.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dh));
         PM_CUDA(launch_attn(ap, s, pdl));
@@ -566,7 +566,7 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         ap.ctx = f.ctx;
         ap.S = attn_max_splits(f.ctx);
         ap.win = f.ctx - ((f.flags & PM_FLAG_PINNED_RING) ? 1 : 0);
-        ap.grid = 2 * c->num_sms;
+        attn_plan(ap, c->num_sms);
         ap.D = D;
         ap.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dh));
         if (!seq) PM_CUDA(launch_attn(ap, s, pdl));

@@ -127,11 +127,14 @@ struct AttnParams {
     DevState st;
     int B, H, ctx, S, D;
     int win;               // most keys a query sees (ctx, or ctx - 1 for the pinned ring)
-    int grid;              // CTAs sharing the unit list (2 per SM)
+    int grid;              // CTAs (attn_plan)
+    int cluster;           // CTAs per head in head-per-cluster mode (1..8), 0 = balanced split
     float scale_log2;      // log2(e) / sqrt(dh)
 };
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl);
 cudaError_t attn_prepare();  // opt-in shared memory of the attention kernel
+// grid and mode for B rows of H heads (sets p.grid, p.cluster)
+void attn_plan(AttnParams& p, int num_sms);
 // chunks (CTAs per head) the attention grid needs for a window of ctx keys; AttnParams.S
 // must be at least this and `part` must hold S chunks per head
 int attn_max_splits(int ctx);
