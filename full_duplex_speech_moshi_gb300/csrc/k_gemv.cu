@@ -85,6 +85,9 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
     __syncthreads();
     pdl_trigger();
 
+    float ep_res = 0.f;                          // E_RESIDUAL: y of the first row
+    int ep_pos = 0;                              // E_QKV_ROPE: position and (cos, sin) of the first pair
+    float2 ep_cs = make_float2(1.f, 0.f);
     if (warp == W) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
@@ -117,12 +120,27 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
         }
     } else {
         // ------------------------------ consumers ------------------------------
-        pdl_wait();
-        const bool abort_frame = *(volatile uint32_t*)&p.st.status[1] != 0u;
-        if (threadIdx.x == 0) s_flags[1] = abort_frame ? 1 : 0;
         const int r = warp / P;   // stage row this warp reduces
         const int pp = warp % P;  // K slice
         const int kslice = K / P;
+        // the norm scale does not depend on the previous kernel: in flight before the wait
+        uint4 alv[CH];
+        if (PRO == PRO_RMSNORM) {
+            const uint16_t* al = p.alpha + (size_t)pp * kslice;
+#pragma unroll
+            for (int ci = 0; ci < CH; ++ci) alv[ci] = *reinterpret_cast<const uint4*>(al + 8 * (lane + 32 * ci));
+        }
+        pdl_wait();
+        const bool abort_frame = *(volatile uint32_t*)&p.st.status[1] != 0u;
+        if (threadIdx.x == 0) s_flags[1] = abort_frame ? 1 : 0;
+        // epilogue operands of this thread's first row, loaded with the input vector rather
+        // than after the last stage
+        if (EPI == E_RESIDUAL && (int)threadIdx.x < nu) ep_res = p.y[(size_t)b * p.y_stride + u0 + threadIdx.x];
+        if (EPI == E_QKV_ROPE && (int)threadIdx.x < nu) {
+            ep_pos = p.st.pos[b];
+            const int row = 2 * (u0 + (int)threadIdx.x), sec = row / p.D;
+            if (sec < 2) ep_cs = p.rope_tab[(size_t)b * (p.dh / 2) + (((row - sec * p.D) % p.dh) >> 1)];
+        }
         float xr[CH * 8];
         const float* xb = p.x + (size_t)b * p.x_stride + (size_t)pp * kslice;
         if (PRO == PRO_DEPATTN) {
@@ -190,10 +208,9 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
             float tot = 0.f;
             for (int i = 0; i < P; ++i) tot += red[i];
             const float inv = 1.0f / sqrtf(tot / (float)K + p.eps);
-            const uint16_t* al = p.alpha + (size_t)pp * kslice;
 #pragma unroll
             for (int ci = 0; ci < CH; ++ci) {
-                const uint4 av = *reinterpret_cast<const uint4*>(al + 8 * (lane + 32 * ci));
+                const uint4 av = alv[ci];
                 xr[8 * ci + 0] *= inv * bf16lo(av.x); xr[8 * ci + 1] *= inv * bf16hi(av.x);
                 xr[8 * ci + 2] *= inv * bf16lo(av.y); xr[8 * ci + 3] *= inv * bf16hi(av.y);
                 xr[8 * ci + 4] *= inv * bf16lo(av.z); xr[8 * ci + 5] *= inv * bf16hi(av.z);
@@ -275,7 +292,7 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
         for (int lu = tid; lu < nu; lu += nthr) {
             const int row = u0 + lu;
             float v = rowsum(lu, 0);
-            if (EPI == E_RESIDUAL) v += yb[row];
+            if (EPI == E_RESIDUAL) v += (lu == tid) ? ep_res : yb[row];
             if (EPI == E_EMB_ADD) {
                 const uint16_t e = p.emb[(size_t)tok * p.y_stride + row];
                 v += __uint_as_float((uint32_t)e << 16);
@@ -292,7 +309,7 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
         }
     } else if (EPI == E_QKV_ROPE) {
         if (aborted || tid >= nthr) return;
-        const int pos = p.st.pos[b];
+        const int pos = tid < nu ? ep_pos : p.st.pos[b];
         const int slot = pos % p.ctx;
         for (int lu = tid; lu < nu; lu += nthr) {
             const int row = 2 * (u0 + lu);
@@ -301,7 +318,7 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
             const int idx = row - sec * p.D;
             const int h = idx / p.dh, d = idx % p.dh;
             if (sec < 2) {
-                const float2 t2 = p.rope_tab[(size_t)b * (p.dh / 2) + (d >> 1)];
+                const float2 t2 = (lu == tid) ? ep_cs : p.rope_tab[(size_t)b * (p.dh / 2) + (d >> 1)];
                 const float c = t2.x, s = t2.y;
                 const float ra = a * c - bb * s;
                 const float rb = a * s + bb * c;
