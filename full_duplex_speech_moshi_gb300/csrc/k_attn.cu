@@ -23,8 +23,8 @@
 //    the fused-QKV kernel that is still writing the current K/V and the query;
 //  * four consumer warps take a unit at a time: the current position's K/V row (written by
 //    the kernel this one waited for) is loaded into its slot after the wait; scores with
-//    two lanes per key (64 dims each, reads staggered across the 16-byte columns so a
-//    quarter-warp touches 32 distinct banks), the base-2 exponential with the query
+//    128 / KPC x 2 lanes per key (reads staggered across the 16-byte columns of a row so a
+//    key's lanes touch distinct banks), the base-2 exponential with the query
 //    pre-scaled by log2(e)/sqrt(128) (the same softmax), a running max / sum / weighted
 //    value (thread t owns coordinate t) carried across the CTA's units of one head;
 //  * a head whose units all fall in one CTA is written out directly; in the balanced split a
@@ -41,7 +41,12 @@ namespace pm {
 namespace {
 
 constexpr int DH = 128;
-constexpr int KPC = 64;                     // keys per unit
+#ifndef PM_ATTN_KPC
+#define PM_ATTN_KPC 64
+#endif
+constexpr int KPC = PM_ATTN_KPC;            // keys per unit (32 or 64)
+constexpr int LPK = 2 * 64 / KPC;           // lanes per key in the scores (4 warps x 32 lanes = KPC x LPK)
+constexpr int NCOL = 128 / LPK / 8;         // 16-byte columns of a key row per lane
 #ifndef PM_ATTN_NST
 #define PM_ATTN_NST 3
 #endif
@@ -50,7 +55,7 @@ constexpr int NST = PM_ATTN_NST;            // stages per CTA (tuning: fewer let
 constexpr int ROWB = DH * 2;                // bytes per K or V row
 constexpr int STAGE = 2 * KPC * ROWB;       // K rows then V rows: 32 KB
 constexpr int THREADS = 160;                // 4 consumer warps + producer warp
-constexpr int MAX_PIECES = 64;              // pieces a head can be cut into (>= chunks per head)
+constexpr int MAX_PIECES = 128;             // pieces a head can be cut into (>= chunks per head)
 constexpr int MAX_CLUSTER = 8;              // CTAs per head in head-per-cluster mode
 
 __device__ __forceinline__ int n_chunks(int pos, int win) { return (min(pos + 1, win) + KPC - 1) / KPC; }
@@ -235,15 +240,17 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
                     }
                     cons_bar();  // that row, and a new piece's query, are in place
                 }
-                // scores: lanes 2j, 2j+1 of warp w take key 16w + j, 64 coordinates each
-                const int kk = 16 * warp + (lane >> 1), half = lane & 1;
+                // scores: LPK lanes per key (128 / LPK coordinates each); warp w takes keys
+                // w*KPC/4 .. w*KPC/4 + KPC/4 - 1
+                const int kk = (KPC / 4) * warp + lane / LPK, part = lane % LPK;
+                const int half = part;  // lanes with part 0 publish the key's weight
                 float d0 = 0.f, d1 = 0.f;
                 if (kk < nvalid) {
-                    const uint8_t* kr = st + kk * ROWB + half * 128;
-                    const float* qh = s_q + half * 64;
+                    const uint8_t* kr = st + kk * ROWB + part * (ROWB / LPK);
+                    const float* qh = s_q + part * (DH / LPK);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int jc = (j + lane) & 7;  // staggered 16-byte column
+                    for (int j = 0; j < NCOL; ++j) {
+                        const int jc = (j + lane) % NCOL;  // staggered 16-byte column
                         const uint4 kv = *reinterpret_cast<const uint4*>(kr + jc * 16);
                         const float4 qa = *reinterpret_cast<const float4*>(qh + jc * 8);
                         const float4 qb = *reinterpret_cast<const float4*>(qh + jc * 8 + 4);
@@ -257,13 +264,14 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
                         d1 = fmaf(qb.w, bf16hi(kv.w), d1);
                     }
                 }
-                const float d = d0 + d1;
-                float sc = d + __shfl_xor_sync(0xffffffffu, d, 1);
+                float sc = d0 + d1;
+#pragma unroll
+                for (int o = 1; o < LPK; o <<= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
                 if (kk >= nvalid) sc = -INFINITY;
                 // chunk maximum across the 4 warps, then weights against the running maximum
                 float wm = sc;
 #pragma unroll
-                for (int o = 2; o <= 16; o <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+                for (int o = LPK; o <= 16; o <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
                 if (lane == 0) s_wm[warp] = wm;
                 cons_bar();
                 const float cm = fmaxf(fmaxf(s_wm[0], s_wm[1]), fmaxf(s_wm[2], s_wm[3]));

@@ -32,7 +32,7 @@
 #define PM_GEMV_STAGE_BYTES 16384
 #endif
 #ifndef PM_GEMV_RING_BYTES
-#define PM_GEMV_RING_BYTES 98304
+#define PM_GEMV_RING_BYTES 81920
 #endif
 #ifndef PM_GEMV_CTAS_PER_SM
 #define PM_GEMV_CTAS_PER_SM 2
