@@ -324,3 +324,26 @@ def test_pinned_ring_mode_parity():
                 assert logits_rel_l2(gl[q], ol[q]) <= 1e-2, (t, q)
     finally:
         p.close()
+
+
+@pytest.mark.parametrize("B", [2, 8, 16])
+def test_batched_replays_bit_identical(B):
+    """The batched paths (batched GEMV on warp MMAs, head-per-cluster or balanced-split
+    attention) merge partial sums in a fixed order: replaying the same frames from the same
+    state reproduces every bit.  A missing ordering between a slot's reads and the bulk copy
+    that refills it shows up here as replays that differ."""
+    s = small_shape()
+    p = Pair(s, B_max=B, depformer=False)
+    try:
+        pos = [int(v) for v in (np.arange(B) * 5 % 40 + 3)]
+        ids = I.make_ids(s, 3, B=B, seed=51)
+        runs = []
+        for _ in range(3):
+            p.ctx.reset()
+            p.ctx.set_positions(pos)
+            runs.append([p.gpu_frame(ids[t], B=B) for t in range(3)])
+        for other in runs[1:]:
+            for a, b in zip(runs[0], other):
+                assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
+    finally:
+        p.close()
