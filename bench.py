@@ -283,7 +283,7 @@ def main():
     kv1 = pm.alloc_kv_cache(cfg1)
     ctx = pm.Context(s.asdict(), W, kv1, B_max=BB, depformer=True, stream=stream.cuda_stream)
     T = PR + args.warmup + args.steps
-    ids_h = I.make_ids(s, T + 64, B=BB, seed=2000 + rank)      # [T, B, 17]
+    ids_h = I.make_ids(s, T + 96, B=BB, seed=2000 + rank)      # [T, B, 17]
     ids_fb = ids_h.copy()
     ids_fb[PR:, :, 0] = pm.PM_ID_FEEDBACK
     ids_d = torch.from_numpy(ids_fb).to(dev)
@@ -342,6 +342,16 @@ def main():
                     f"RMSNorm + linear_in [22528,4096] + SwiGLU, tcgen05 GEMM N={32 if BB <= 32 else 64}")
     dom_ms = statistics.mean(by_kind[dom_kind])
     achieved = dom_bytes / (dom_ms / 1000.0) / 1e9
+
+    # per-frame times (median and p90 of 64 frames, each between its own events)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(65)]
+    evs[0].record(stream)
+    for t in range(64):
+        ctx.frame_step(BB, ids_d[p0 + args.steps + 16 + t], logits, hidden, token)
+        evs[t + 1].record(stream)
+    torch.cuda.synchronize()
+    per_frame = sorted(evs[t].elapsed_time(evs[t + 1]) for t in range(64))
+    frame_p50, frame_p90 = per_frame[31], per_frame[57]
 
     # end to end: host IDs in, greedy token out and fed back, every frame
     ctx.reset()
@@ -435,6 +445,20 @@ def main():
         b5.record(stream)
         torch.cuda.synchronize()
         extras["prefill_frames_per_s"] = s.ctx / (a5.elapsed_time(b5) / 1000.0)
+        # decode with a full 3000-frame window right after that prefill: every frame reads
+        # 3000 keys per layer and overwrites the oldest slot of the ring
+        ids_l = torch.from_numpy(I.make_ids(s, 72, seed=2004)).to(dev)
+        ids_l[:, :, 0] = pm.PM_ID_FEEDBACK
+        for t in range(8):
+            ctx.frame_step(1, ids_l[t], logits, hidden, token)
+        torch.cuda.synchronize()
+        a6, b6 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a6.record(stream)
+        for t in range(64):
+            ctx.frame_step(1, ids_l[8 + t], logits, hidden, token)
+        b6.record(stream)
+        torch.cuda.synchronize()
+        extras["L3000_frames_per_s"] = 64 / (a6.elapsed_time(b6) / 1000.0)
     ctx.close()
     del kv1
     torch.cuda.empty_cache()
@@ -518,6 +542,7 @@ def main():
                          "kernel_ms": dom_ms, "algorithmic_bytes_per_launch": dom_bytes,
                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"},
             "kernel_ms_mean": {k: statistics.mean(v) for k, v in by_kind.items()},
+            "frame_ms_p50": frame_p50, "frame_ms_p90": frame_p90,
             "e2e": {"value": e2e_fps, "unit": "frames/s", "h2d_bytes_per_step": 64 + 4 * s.n_streams * BB,
                     "d2h_bytes_per_step": 4 * BB},
             "gpu_launches": launches_per_frame * args.steps,

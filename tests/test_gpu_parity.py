@@ -339,6 +339,9 @@ def test_batched_replays_bit_identical(B):
         ids = I.make_ids(s, 3, B=B, seed=51)
         runs = []
         for _ in range(3):
+            # same state every time: the ring is cleared too (streams past the 32-slot
+            # wrap would otherwise read the slots the previous replay wrote)
+            p.kv.zero_()
             p.ctx.reset()
             p.ctx.set_positions(pos)
             runs.append([p.gpu_frame(ids[t], B=B) for t in range(3)])
