@@ -111,6 +111,10 @@ __device__ __forceinline__ UnitPos decode_unit(long long u, const int* s_first, 
     return r;
 }
 
+// PV2: the query in registers and weighted values over key halves x coordinate pairs (one
+// 32-bit V load per key) -- fewer shared loads per unit, a combine per piece; pays when a
+// CTA streams many units (one or two CTAs per head, or the balanced split)
+template <bool PV2>
 __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
     extern __shared__ __align__(128) uint8_t ring[];  // [NST][STAGE]
     __shared__ int s_first[PM_MAX_B_DEV + 1], s_nc[PM_MAX_B_DEV], s_pos[PM_MAX_B_DEV];
@@ -121,6 +125,7 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
     __shared__ float s_pm[MAX_PIECES], s_pl[MAX_PIECES];
     __shared__ int s_flags[4];  // [0] timeout, [1] last piece of a head, [2] units issued
     __shared__ float s_cpart[MAX_CLUSTER][DH + 2];  // head-per-cluster: the leader's inbox
+    __shared__ float s_comb[2][DH];                  // the two key halves of a piece
 
     pdl_trigger();
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -208,7 +213,14 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
         // ------------------------------ consumers ------------------------------
         pdl_wait();
         const bool aborted = *(volatile uint32_t*)&p.st.status[1] != 0u;
-        float m_run = -INFINITY, l_run = 0.f, acc = 0.f;
+        // running softmax of the current piece of a head.  Weighted values: thread t takes
+        // coordinates 2(t mod 64), 2(t mod 64)+1 over the key half t / 64 of each unit
+        // (one 32-bit load of V per key); the halves meet once per piece, into `acc`
+        // (coordinate t)
+        float m_run = -INFINITY, l_run = 0.f, acc = 0.f, ax = 0.f, ay = 0.f;
+        const int kh = t >> 6, dp = t & 63;
+        // this lane's query columns in the order its staggered K reads visit them
+        float qr[NCOL][8];
         int seg_ci0 = 0;  // first chunk of the current piece of a head
         bool ok = true;
         for (int k = 0; k < nu; ++k) {
@@ -220,6 +232,8 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
                 s_q[t] = __ldcg(p.q + (size_t)up.b * p.D + up.h * DH + t) * p.scale_log2;
                 m_run = -INFINITY;
                 l_run = 0.f;
+                ax = 0.f;
+                ay = 0.f;
                 acc = 0.f;
                 seg_ci0 = up.ci;
             }
@@ -240,6 +254,17 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
                     }
                     cons_bar();  // that row, and a new piece's query, are in place
                 }
+                if (PV2 && first) {
+                    const int part0 = (lane % LPK) * (DH / LPK);
+#pragma unroll
+                    for (int j = 0; j < NCOL; ++j) {
+                        const int jc = (j + lane) % NCOL;
+                        const float4 qa = *reinterpret_cast<const float4*>(s_q + part0 + jc * 8);
+                        const float4 qb = *reinterpret_cast<const float4*>(s_q + part0 + jc * 8 + 4);
+                        qr[j][0] = qa.x; qr[j][1] = qa.y; qr[j][2] = qa.z; qr[j][3] = qa.w;
+                        qr[j][4] = qb.x; qr[j][5] = qb.y; qr[j][6] = qb.z; qr[j][7] = qb.w;
+                    }
+                }
                 // scores: LPK lanes per key (128 / LPK coordinates each); warp w takes keys
                 // w*KPC/4 .. w*KPC/4 + KPC/4 - 1
                 const int kk = (KPC / 4) * warp + lane / LPK, part = lane % LPK;
@@ -252,16 +277,24 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
                     for (int j = 0; j < NCOL; ++j) {
                         const int jc = (j + lane) % NCOL;  // staggered 16-byte column
                         const uint4 kv = *reinterpret_cast<const uint4*>(kr + jc * 16);
-                        const float4 qa = *reinterpret_cast<const float4*>(qh + jc * 8);
-                        const float4 qb = *reinterpret_cast<const float4*>(qh + jc * 8 + 4);
-                        d0 = fmaf(qa.x, bf16lo(kv.x), d0);
-                        d1 = fmaf(qa.y, bf16hi(kv.x), d1);
-                        d0 = fmaf(qa.z, bf16lo(kv.y), d0);
-                        d1 = fmaf(qa.w, bf16hi(kv.y), d1);
-                        d0 = fmaf(qb.x, bf16lo(kv.z), d0);
-                        d1 = fmaf(qb.y, bf16hi(kv.z), d1);
-                        d0 = fmaf(qb.z, bf16lo(kv.w), d0);
-                        d1 = fmaf(qb.w, bf16hi(kv.w), d1);
+                        float q8[8];
+                        if (PV2) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) q8[e] = qr[j][e];
+                        } else {
+                            const float4 qa = *reinterpret_cast<const float4*>(qh + jc * 8);
+                            const float4 qb = *reinterpret_cast<const float4*>(qh + jc * 8 + 4);
+                            q8[0] = qa.x; q8[1] = qa.y; q8[2] = qa.z; q8[3] = qa.w;
+                            q8[4] = qb.x; q8[5] = qb.y; q8[6] = qb.z; q8[7] = qb.w;
+                        }
+                        d0 = fmaf(q8[0], bf16lo(kv.x), d0);
+                        d1 = fmaf(q8[1], bf16hi(kv.x), d1);
+                        d0 = fmaf(q8[2], bf16lo(kv.y), d0);
+                        d1 = fmaf(q8[3], bf16hi(kv.y), d1);
+                        d0 = fmaf(q8[4], bf16lo(kv.z), d0);
+                        d1 = fmaf(q8[5], bf16hi(kv.z), d1);
+                        d0 = fmaf(q8[6], bf16lo(kv.w), d0);
+                        d1 = fmaf(q8[7], bf16hi(kv.w), d1);
                     }
                 }
                 float sc = d0 + d1;
@@ -284,21 +317,51 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
                 for (int o = 1; o <= 16; o <<= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
                 if (lane == 0) s_wl[warp] = ws;
                 cons_bar();
-                // weighted values: thread t owns coordinate t
-                // (rows past nvalid hold stale data: they are skipped, never multiplied by 0)
-                const uint16_t* vcol = reinterpret_cast<const uint16_t*>(st + KPC * ROWB) + t;
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                const int n4 = nvalid & ~3;
-#pragma unroll 4
-                for (int j = 0; j < n4; j += 4) {
-                    const float4 pj = *reinterpret_cast<const float4*>(s_p + j);
-                    a0 = fmaf(pj.x, __uint_as_float((uint32_t)vcol[(j + 0) * DH] << 16), a0);
-                    a1 = fmaf(pj.y, __uint_as_float((uint32_t)vcol[(j + 1) * DH] << 16), a1);
-                    a2 = fmaf(pj.z, __uint_as_float((uint32_t)vcol[(j + 2) * DH] << 16), a2);
-                    a3 = fmaf(pj.w, __uint_as_float((uint32_t)vcol[(j + 3) * DH] << 16), a3);
+                if (PV2) {
+                    // weighted values over this thread's key half (rows past nvalid hold stale data:
+                    // they are skipped, never multiplied by 0)
+                    const uint32_t* vrow = reinterpret_cast<const uint32_t*>(st + KPC * ROWB) + dp;
+                    const int j0 = kh * (KPC / 2), j1 = min(nvalid, j0 + KPC / 2);
+                    float bx0 = 0.f, by0 = 0.f, bx1 = 0.f, by1 = 0.f;
+                    int j = j0;
+    #pragma unroll 2
+                    for (; j + 4 <= j1; j += 4) {
+                        const float4 pj = *reinterpret_cast<const float4*>(s_p + j);
+                        const uint32_t v0 = vrow[(j + 0) * (DH / 2)], v1 = vrow[(j + 1) * (DH / 2)];
+                        const uint32_t v2 = vrow[(j + 2) * (DH / 2)], v3 = vrow[(j + 3) * (DH / 2)];
+                        bx0 = fmaf(pj.x, bf16lo(v0), bx0);
+                        by0 = fmaf(pj.x, bf16hi(v0), by0);
+                        bx1 = fmaf(pj.y, bf16lo(v1), bx1);
+                        by1 = fmaf(pj.y, bf16hi(v1), by1);
+                        bx0 = fmaf(pj.z, bf16lo(v2), bx0);
+                        by0 = fmaf(pj.z, bf16hi(v2), by0);
+                        bx1 = fmaf(pj.w, bf16lo(v3), bx1);
+                        by1 = fmaf(pj.w, bf16hi(v3), by1);
+                    }
+                    for (; j < j1; ++j) {
+                        const uint32_t v = vrow[j * (DH / 2)];
+                        bx0 = fmaf(s_p[j], bf16lo(v), bx0);
+                        by0 = fmaf(s_p[j], bf16hi(v), by0);
+                    }
+                    ax = ax * alpha + (bx0 + bx1);
+                    ay = ay * alpha + (by0 + by1);
+                } else {
+                    // weighted values: thread t owns coordinate t
+                    // (rows past nvalid hold stale data: they are skipped, never multiplied by 0)
+                    const uint16_t* vcol = reinterpret_cast<const uint16_t*>(st + KPC * ROWB) + t;
+                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                    const int n4 = nvalid & ~3;
+    #pragma unroll 4
+                    for (int j = 0; j < n4; j += 4) {
+                        const float4 pj = *reinterpret_cast<const float4*>(s_p + j);
+                        a0 = fmaf(pj.x, __uint_as_float((uint32_t)vcol[(j + 0) * DH] << 16), a0);
+                        a1 = fmaf(pj.y, __uint_as_float((uint32_t)vcol[(j + 1) * DH] << 16), a1);
+                        a2 = fmaf(pj.z, __uint_as_float((uint32_t)vcol[(j + 2) * DH] << 16), a2);
+                        a3 = fmaf(pj.w, __uint_as_float((uint32_t)vcol[(j + 3) * DH] << 16), a3);
+                    }
+                    for (int j = n4; j < nvalid; ++j) a0 = fmaf(s_p[j], __uint_as_float((uint32_t)vcol[j * DH] << 16), a0);
+                    acc = acc * alpha + ((a0 + a1) + (a2 + a3));
                 }
-                for (int j = n4; j < nvalid; ++j) a0 = fmaf(s_p[j], __uint_as_float((uint32_t)vcol[j * DH] << 16), a0);
-                acc = acc * alpha + ((a0 + a1) + (a2 + a3));
                 l_run = l_run * alpha + ((s_wl[0] + s_wl[1]) + (s_wl[2] + s_wl[3]));
                 m_run = m_new;
             }
@@ -310,7 +373,16 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
             if (aborted) continue;
 
             const bool last = (k == nu - 1) || up.ci == up.nc - 1;
-            if (!last || CS > 1) continue;  // pieces of a cluster's head meet in its leader
+            if (!last) continue;
+            if (PV2) {
+                // the two key halves of the piece, into coordinate t
+                s_comb[kh][2 * dp] = ax;
+                s_comb[kh][2 * dp + 1] = ay;
+                cons_bar();
+                acc = s_comb[0][t] + s_comb[1][t];
+                cons_bar();
+            }
+            if (CS > 1) continue;  // pieces of a cluster's head meet in its leader
             float* ob = p.o + (size_t)up.b * p.D + up.h * DH;
             uint16_t* obb = p.ob ? p.ob + (size_t)up.b * p.D + up.h * DH : nullptr;
             if (seg_ci0 == 0 && up.ci == up.nc - 1) {
@@ -435,7 +507,9 @@ void attn_plan(AttnParams& p, int num_sms) {
 }
 
 cudaError_t attn_prepare() {
-    return cudaFuncSetAttribute(k_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, NST * STAGE);
+    cudaError_t e = cudaFuncSetAttribute(k_attn<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, NST * STAGE);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, NST * STAGE);
+    return e;
 }
 
 cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
@@ -465,7 +539,9 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
     }
     cfg.attrs = attr;
     cfg.numAttrs = (unsigned)na;
-    return cudaLaunchKernelEx(&cfg, k_attn, p);
+    // many units per CTA (one or two CTAs per head, or the balanced split): PV2
+    return (p.cluster == 0 || p.cluster <= 2) ? cudaLaunchKernelEx(&cfg, k_attn<true>, p)
+                                              : cudaLaunchKernelEx(&cfg, k_attn<false>, p);
 }
 
 }  // namespace pm
