@@ -267,7 +267,7 @@ pm_status pm_restore(pm_ctx* ctx, int stream, const void* src);
 pm_status pm_device_status(pm_ctx* ctx);
 
 /* Final RMSNorm + text head + greedy token with no context and no device allocation.
- * The paper has no counterpart: this is a library entry point for callers that cannot
+ * The model describes no such call: this is a library entry point for callers that cannot
  * allocate device memory (code running during CUDA stream capture, real-time threads
  * that must not block on the allocator, hosts that own all device memory).
  *  residual  [B][D] fp32 device memory: the residual stream after the last block.

@@ -170,8 +170,8 @@ int orc_argmax(const double* v, int n) {
 /* ------------------------------------------------------------------------- */
 
 /* Philox4x64-10: ten rounds of the 4x64 S-box (two 64x64 -> 128-bit multiplies per
- * round with the paper's multipliers), the key bumped by the two Weyl constants between
- * rounds. */
+ * round with the multipliers published for Philox by Salmon et al., 2011), the key
+ * bumped by the two Weyl constants between rounds. */
 void orc_philox4x64(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4]) {
     const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
     const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
