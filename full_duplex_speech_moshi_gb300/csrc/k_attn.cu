@@ -25,8 +25,12 @@
 //    the kernel this one waited for) is loaded into its slot after the wait; scores with
 //    128 / KPC x 2 lanes per key (reads staggered across the 16-byte columns of a row so a
 //    key's lanes touch distinct banks), the base-2 exponential with the query
-//    pre-scaled by log2(e)/sqrt(128) (the same softmax), a running max / sum / weighted
-//    value (thread t owns coordinate t) carried across the CTA's units of one head;
+//    pre-scaled by log2(e)/sqrt(128) (the same softmax).  Where a CTA streams many units
+//    each warp keeps its own running max / sum / weighted values over its 16 keys of every
+//    unit (no barrier per unit; the warps' states merge once per piece); with few units
+//    per CTA one running state spans the four warps (thread t owns coordinate t);
+//  * the issuing thread walks its units incrementally (no division per unit): its work
+//    between a stage coming free and the refill being issued is on every stage's cycle;
 //  * a head whose units all fall in one CTA is written out directly; in the balanced split a
 //    head cut between CTAs leaves one partial (weighted values, max, sum) per piece in
 //    global memory and the CTA that finishes last merges them in piece order (completion
@@ -91,10 +95,11 @@ __device__ __forceinline__ void dsmem_store(const void* local, uint32_t rank, fl
 struct UnitPos {
     int b, h, ci, nc;     // row, head, chunk index, chunks of the head
     int pos, key0, key1;  // query position, first key, one past the last key of the chunk
+    int lo, s0;           // the row's first visible key; ring slot of key0
 };
 
 __device__ __forceinline__ UnitPos decode_unit(long long u, const int* s_first, const int* s_nc, const int* s_pos,
-                                               int B, int H, int win) {
+                                               int B, int H, int win, int ctx) {
     UnitPos r;
     int b = 0;
     while (b + 1 < B && u >= s_first[b + 1]) ++b;
@@ -105,17 +110,56 @@ __device__ __forceinline__ UnitPos decode_unit(long long u, const int* s_first, 
     r.ci = rel % nc;
     r.nc = nc;
     r.pos = s_pos[b];
-    const int n = min(r.pos + 1, win), lo = r.pos - n + 1;
-    r.key0 = lo + KPC * r.ci;
+    const int n = min(r.pos + 1, win);
+    r.lo = r.pos - n + 1;
+    r.key0 = r.lo + KPC * r.ci;
     r.key1 = min(r.key0 + KPC, r.pos + 1);
+    r.s0 = r.key0 % ctx;
     return r;
 }
 
-// PV2: the query in registers and weighted values over key halves x coordinate pairs (one
-// 32-bit V load per key) -- fewer shared loads per unit, a combine per piece; pays when a
-// CTA streams many units (one or two CTAs per head, or the balanced split)
-template <bool PV2>
+// the unit after r in (row, head, chunk) order, without divisions: a CTA's units are
+// consecutive, and the issuing thread's per-unit work sits on every stage's refill path
+__device__ __forceinline__ void next_unit(UnitPos& r, const int* s_nc, const int* s_pos, int B, int H, int win,
+                                          int ctx) {
+    if (++r.ci == r.nc) {
+        r.ci = 0;
+        if (++r.h == H) {
+            r.h = 0;
+            if (r.b + 1 < B) ++r.b;  // (past a CTA's last unit the walk is not read)
+            r.nc = s_nc[r.b];
+            r.pos = s_pos[r.b];
+            r.lo = r.pos - min(r.pos + 1, win) + 1;
+        }
+        r.key0 = r.lo;
+        r.s0 = r.lo % ctx;
+    } else {
+        r.key0 += KPC;
+        r.s0 += KPC;
+        if (r.s0 >= ctx) r.s0 -= ctx;
+    }
+    r.key1 = min(r.key0 + KPC, r.pos + 1);
+}
+
+// Consumer variants (MODE):
+//  0  one running softmax per CTA: the chunk maximum and sum meet across the four warps
+//     (two consumer barriers per unit), thread t owns coordinate t of the weighted values;
+//  1  as 0, with the query in registers and the weighted values over key halves x
+//     coordinate pairs (one 32-bit V load per key), the halves combined once per piece;
+//  2  one running softmax per warp over its 16 keys of every unit (maximum and sum by warp
+//     shuffles, no barrier per unit), lane l owns coordinates 4l .. 4l+3 (one 64-bit V load
+//     per key); the four warps' states are merged once per piece.  Pays when a CTA streams
+//     many units.
+#ifndef PM_ATTN_MANY
+#define PM_ATTN_MANY 2
+#endif
+#ifndef PM_ATTN_FEW
+#define PM_ATTN_FEW 0
+#endif
+template <int MODE>
 __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
+    constexpr bool PV2 = MODE >= 1;  // query in registers
+    static_assert(MODE != 2 || KPC == 64, "per-warp softmax takes 16 keys per warp");
     extern __shared__ __align__(128) uint8_t ring[];  // [NST][STAGE]
     __shared__ int s_first[PM_MAX_B_DEV + 1], s_nc[PM_MAX_B_DEV], s_pos[PM_MAX_B_DEV];
     __shared__ __align__(8) uint64_t full[NST], empty[NST];
@@ -125,7 +169,8 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
     __shared__ float s_pm[MAX_PIECES], s_pl[MAX_PIECES];
     __shared__ int s_flags[4];  // [0] timeout, [1] last piece of a head, [2] units issued
     __shared__ float s_cpart[MAX_CLUSTER][DH + 2];  // head-per-cluster: the leader's inbox
-    __shared__ float s_comb[2][DH];                  // the two key halves of a piece
+    __shared__ __align__(16) float s_comb[4][DH];    // per-half (1) or per-warp (2) pieces
+    __shared__ __align__(16) float s_pw[4][16];      // mode 2: a warp's key weights
 
     pdl_trigger();
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -181,21 +226,22 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
             const uint64_t pol = l2_evict_first_policy();
+            UnitPos up = decode_unit(u0, s_first, s_nc, s_pos, p.B, p.H, p.win, p.ctx);
             for (int k = 0; k < nu; ++k) {
                 const int slot = k % NST;
+                if (k > 0) next_unit(up, s_nc, s_pos, p.B, p.H, p.win, p.ctx);
                 if (k >= NST && !mbar_wait(&empty[slot], (uint32_t)((k / NST) - 1) & 1u)) {
                     s_flags[0] = 1;
                     set_status(p.st.status, PM_DEV_ERR_TIMEOUT);
                     break;
                 }
-                const UnitPos up = decode_unit(u0 + k, s_first, s_nc, s_pos, p.B, p.H, p.win);
                 // keys before the current position only: that row is written by the kernel
                 // this one overlaps
                 const int nk = max(0, min(up.key1, up.pos) - up.key0);
                 mbar_arrive_expect_tx(&full[slot], 2u * (uint32_t)nk * ROWB);
                 if (nk > 0) {
                     const size_t head = ((size_t)up.b * p.H + up.h) * (size_t)p.ctx * DH;
-                    const int s0 = up.key0 % p.ctx;
+                    const int s0 = up.s0;
                     const int n1 = min(nk, p.ctx - s0), n2 = nk - n1;
                     uint8_t* dk = ring + (size_t)slot * STAGE;
                     uint8_t* dv = dk + KPC * ROWB;
@@ -218,23 +264,44 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
         // (one 32-bit load of V per key); the halves meet once per piece, into `acc`
         // (coordinate t)
         float m_run = -INFINITY, l_run = 0.f, acc = 0.f, ax = 0.f, ay = 0.f;
+        float mw = -INFINITY, lw = 0.f, w0 = 0.f, w1 = 0.f, w2 = 0.f, w3 = 0.f;  // mode 2
         const int kh = t >> 6, dp = t & 63;
         // this lane's query columns in the order its staggered K reads visit them
         float qr[NCOL][8];
         int seg_ci0 = 0;  // first chunk of the current piece of a head
         bool ok = true;
+        UnitPos up = decode_unit(u0, s_first, s_nc, s_pos, p.B, p.H, p.win, p.ctx);
         for (int k = 0; k < nu; ++k) {
             const int slot = k % NST;
-            const UnitPos up = decode_unit(u0 + k, s_first, s_nc, s_pos, p.B, p.H, p.win);
+            if (k > 0) next_unit(up, s_nc, s_pos, p.B, p.H, p.win, p.ctx);
             const bool first = (k == 0) || up.ci == 0;
             if (first && !aborted) {
-                // this piece's query, pre-scaled for the base-2 exponential
-                s_q[t] = __ldcg(p.q + (size_t)up.b * p.D + up.h * DH + t) * p.scale_log2;
+                // this piece's query, pre-scaled for the base-2 exponential; issued before the
+                // stage wait so its latency overlaps the K/V copies
+                if (MODE == 2) {
+                    // each lane's half of the query, in the order its staggered K reads visit it
+                    const float* qg = p.q + (size_t)up.b * p.D + up.h * DH + (lane & 1) * (DH / 2);
+#pragma unroll
+                    for (int j = 0; j < NCOL; ++j) {
+                        const int jc = (j + lane) % NCOL;
+                        const float4 qa = __ldcg(reinterpret_cast<const float4*>(qg + jc * 8));
+                        const float4 qb = __ldcg(reinterpret_cast<const float4*>(qg + jc * 8 + 4));
+                        qr[j][0] = qa.x * p.scale_log2; qr[j][1] = qa.y * p.scale_log2;
+                        qr[j][2] = qa.z * p.scale_log2; qr[j][3] = qa.w * p.scale_log2;
+                        qr[j][4] = qb.x * p.scale_log2; qr[j][5] = qb.y * p.scale_log2;
+                        qr[j][6] = qb.z * p.scale_log2; qr[j][7] = qb.w * p.scale_log2;
+                    }
+                } else {
+                    s_q[t] = __ldcg(p.q + (size_t)up.b * p.D + up.h * DH + t) * p.scale_log2;
+                }
                 m_run = -INFINITY;
                 l_run = 0.f;
                 ax = 0.f;
                 ay = 0.f;
                 acc = 0.f;
+                mw = -INFINITY;
+                lw = 0.f;
+                w0 = w1 = w2 = w3 = 0.f;
                 seg_ci0 = up.ci;
             }
             if (!mbar_wait(&full[slot], (uint32_t)(k / NST) & 1u)) {
@@ -244,7 +311,19 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
             uint8_t* st = ring + (size_t)slot * STAGE;
             const int nvalid = up.key1 - up.key0;
             if (!aborted) {
-                if (up.key1 == up.pos + 1 || first) {
+                if (MODE == 2) {
+                    const int r = up.pos - up.key0;
+                    if (up.key1 == up.pos + 1 && (r >> 4) == warp) {
+                        // the current position's K and V rows (written by the kernel waited for),
+                        // by the one warp whose keys include it
+                        const size_t row = (((size_t)up.b * p.H + up.h) * p.ctx + up.pos % p.ctx) * DH;
+                        reinterpret_cast<uint2*>(st + r * ROWB)[lane] =
+                            __ldcg(reinterpret_cast<const uint2*>(p.kc + row) + lane);
+                        reinterpret_cast<uint2*>(st + KPC * ROWB + r * ROWB)[lane] =
+                            __ldcg(reinterpret_cast<const uint2*>(p.vc + row) + lane);
+                        __syncwarp();
+                    }
+                } else if (up.key1 == up.pos + 1 || first) {
                     if (up.key1 == up.pos + 1) {
                         // the current position's K and V rows, written by the kernel waited for
                         const size_t row = (((size_t)up.b * p.H + up.h) * p.ctx + up.pos % p.ctx) * DH + t;
@@ -254,7 +333,7 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
                     }
                     cons_bar();  // that row, and a new piece's query, are in place
                 }
-                if (PV2 && first) {
+                if (MODE == 1 && first) {
                     const int part0 = (lane % LPK) * (DH / LPK);
 #pragma unroll
                     for (int j = 0; j < NCOL; ++j) {
@@ -301,69 +380,129 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
 #pragma unroll
                 for (int o = 1; o < LPK; o <<= 1) sc += __shfl_xor_sync(0xffffffffu, sc, o);
                 if (kk >= nvalid) sc = -INFINITY;
-                // chunk maximum across the 4 warps, then weights against the running maximum
-                float wm = sc;
+                if (MODE == 2) {
+                    // this warp's 16 keys: maximum and sum over the warp, no barrier
+                    float wm = sc;
 #pragma unroll
-                for (int o = LPK; o <= 16; o <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
-                if (lane == 0) s_wm[warp] = wm;
-                cons_bar();
-                const float cm = fmaxf(fmaxf(s_wm[0], s_wm[1]), fmaxf(s_wm[2], s_wm[3]));
-                const float m_new = fmaxf(m_run, cm);
-                const float alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
-                const float pk = (kk < nvalid) ? exp2f(sc - m_new) : 0.f;
-                if (half == 0 && kk < KPC) s_p[kk] = pk;
-                float ws = half == 0 ? pk : 0.f;
+                    for (int o = 2; o <= 16; o <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+                    const float m_new = fmaxf(mw, wm);
+                    const float alpha = (mw == -INFINITY) ? 0.f : exp2f(mw - m_new);
+                    const float pk = (kk < nvalid) ? exp2f(sc - m_new) : 0.f;
+                    float ws = pk;  // both lanes of a key hold it: the xor steps from 2 count it once
 #pragma unroll
-                for (int o = 1; o <= 16; o <<= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
-                if (lane == 0) s_wl[warp] = ws;
-                cons_bar();
-                if (PV2) {
-                    // weighted values over this thread's key half (rows past nvalid hold stale data:
-                    // they are skipped, never multiplied by 0)
-                    const uint32_t* vrow = reinterpret_cast<const uint32_t*>(st + KPC * ROWB) + dp;
-                    const int j0 = kh * (KPC / 2), j1 = min(nvalid, j0 + KPC / 2);
-                    float bx0 = 0.f, by0 = 0.f, bx1 = 0.f, by1 = 0.f;
-                    int j = j0;
-    #pragma unroll 2
-                    for (; j + 4 <= j1; j += 4) {
-                        const float4 pj = *reinterpret_cast<const float4*>(s_p + j);
-                        const uint32_t v0 = vrow[(j + 0) * (DH / 2)], v1 = vrow[(j + 1) * (DH / 2)];
-                        const uint32_t v2 = vrow[(j + 2) * (DH / 2)], v3 = vrow[(j + 3) * (DH / 2)];
-                        bx0 = fmaf(pj.x, bf16lo(v0), bx0);
-                        by0 = fmaf(pj.x, bf16hi(v0), by0);
-                        bx1 = fmaf(pj.y, bf16lo(v1), bx1);
-                        by1 = fmaf(pj.y, bf16hi(v1), by1);
-                        bx0 = fmaf(pj.z, bf16lo(v2), bx0);
-                        by0 = fmaf(pj.z, bf16hi(v2), by0);
-                        bx1 = fmaf(pj.w, bf16lo(v3), bx1);
-                        by1 = fmaf(pj.w, bf16hi(v3), by1);
+                    for (int o = 2; o <= 16; o <<= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+                    lw = lw * alpha + ws;
+                    mw = m_new;
+                    if (part == 0) s_pw[warp][lane >> 1] = pk;
+                    __syncwarp();
+                    // coordinates 4 lane .. 4 lane + 3 over the warp's valid keys (rows past
+                    // nvalid hold stale data: they are skipped, never multiplied by 0)
+                    const int nk = min(max(nvalid - 16 * warp, 0), 16);
+                    const uint8_t* vb = st + KPC * ROWB + (16 * warp) * ROWB + lane * 8;
+                    float b0 = 0.f, b1 = 0.f, b2 = 0.f, b3 = 0.f, c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+                    int j = 0;
+#pragma unroll 2
+                    for (; j + 4 <= nk; j += 4) {
+                        const float4 pj = *reinterpret_cast<const float4*>(&s_pw[warp][j]);
+                        const uint2 v0 = *reinterpret_cast<const uint2*>(vb + (j + 0) * ROWB);
+                        const uint2 v1 = *reinterpret_cast<const uint2*>(vb + (j + 1) * ROWB);
+                        const uint2 v2 = *reinterpret_cast<const uint2*>(vb + (j + 2) * ROWB);
+                        const uint2 v3 = *reinterpret_cast<const uint2*>(vb + (j + 3) * ROWB);
+                        b0 = fmaf(pj.x, bf16lo(v0.x), b0);
+                        b1 = fmaf(pj.x, bf16hi(v0.x), b1);
+                        b2 = fmaf(pj.x, bf16lo(v0.y), b2);
+                        b3 = fmaf(pj.x, bf16hi(v0.y), b3);
+                        c0 = fmaf(pj.y, bf16lo(v1.x), c0);
+                        c1 = fmaf(pj.y, bf16hi(v1.x), c1);
+                        c2 = fmaf(pj.y, bf16lo(v1.y), c2);
+                        c3 = fmaf(pj.y, bf16hi(v1.y), c3);
+                        b0 = fmaf(pj.z, bf16lo(v2.x), b0);
+                        b1 = fmaf(pj.z, bf16hi(v2.x), b1);
+                        b2 = fmaf(pj.z, bf16lo(v2.y), b2);
+                        b3 = fmaf(pj.z, bf16hi(v2.y), b3);
+                        c0 = fmaf(pj.w, bf16lo(v3.x), c0);
+                        c1 = fmaf(pj.w, bf16hi(v3.x), c1);
+                        c2 = fmaf(pj.w, bf16lo(v3.y), c2);
+                        c3 = fmaf(pj.w, bf16hi(v3.y), c3);
                     }
-                    for (; j < j1; ++j) {
-                        const uint32_t v = vrow[j * (DH / 2)];
-                        bx0 = fmaf(s_p[j], bf16lo(v), bx0);
-                        by0 = fmaf(s_p[j], bf16hi(v), by0);
+                    for (; j < nk; ++j) {
+                        const float pj = s_pw[warp][j];
+                        const uint2 v = *reinterpret_cast<const uint2*>(vb + j * ROWB);
+                        b0 = fmaf(pj, bf16lo(v.x), b0);
+                        b1 = fmaf(pj, bf16hi(v.x), b1);
+                        b2 = fmaf(pj, bf16lo(v.y), b2);
+                        b3 = fmaf(pj, bf16hi(v.y), b3);
                     }
-                    ax = ax * alpha + (bx0 + bx1);
-                    ay = ay * alpha + (by0 + by1);
+                    w0 = w0 * alpha + (b0 + c0);
+                    w1 = w1 * alpha + (b1 + c1);
+                    w2 = w2 * alpha + (b2 + c2);
+                    w3 = w3 * alpha + (b3 + c3);
+                    __syncwarp();  // s_pw is rewritten by the next unit
                 } else {
-                    // weighted values: thread t owns coordinate t
-                    // (rows past nvalid hold stale data: they are skipped, never multiplied by 0)
-                    const uint16_t* vcol = reinterpret_cast<const uint16_t*>(st + KPC * ROWB) + t;
-                    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                    const int n4 = nvalid & ~3;
-    #pragma unroll 4
-                    for (int j = 0; j < n4; j += 4) {
-                        const float4 pj = *reinterpret_cast<const float4*>(s_p + j);
-                        a0 = fmaf(pj.x, __uint_as_float((uint32_t)vcol[(j + 0) * DH] << 16), a0);
-                        a1 = fmaf(pj.y, __uint_as_float((uint32_t)vcol[(j + 1) * DH] << 16), a1);
-                        a2 = fmaf(pj.z, __uint_as_float((uint32_t)vcol[(j + 2) * DH] << 16), a2);
-                        a3 = fmaf(pj.w, __uint_as_float((uint32_t)vcol[(j + 3) * DH] << 16), a3);
+                    // chunk maximum across the 4 warps, then weights against the running maximum
+                    float wm = sc;
+#pragma unroll
+                    for (int o = LPK; o <= 16; o <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+                    if (lane == 0) s_wm[warp] = wm;
+                    cons_bar();
+                    const float cm = fmaxf(fmaxf(s_wm[0], s_wm[1]), fmaxf(s_wm[2], s_wm[3]));
+                    const float m_new = fmaxf(m_run, cm);
+                    const float alpha = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
+                    const float pk = (kk < nvalid) ? exp2f(sc - m_new) : 0.f;
+                    if (half == 0 && kk < KPC) s_p[kk] = pk;
+                    float ws = half == 0 ? pk : 0.f;
+#pragma unroll
+                    for (int o = 1; o <= 16; o <<= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
+                    if (lane == 0) s_wl[warp] = ws;
+                    cons_bar();
+                    if (PV2) {
+                        // weighted values over this thread's key half (rows past nvalid hold stale data:
+                        // they are skipped, never multiplied by 0)
+                        const uint32_t* vrow = reinterpret_cast<const uint32_t*>(st + KPC * ROWB) + dp;
+                        const int j0 = kh * (KPC / 2), j1 = min(nvalid, j0 + KPC / 2);
+                        float bx0 = 0.f, by0 = 0.f, bx1 = 0.f, by1 = 0.f;
+                        int j = j0;
+        #pragma unroll 2
+                        for (; j + 4 <= j1; j += 4) {
+                            const float4 pj = *reinterpret_cast<const float4*>(s_p + j);
+                            const uint32_t v0 = vrow[(j + 0) * (DH / 2)], v1 = vrow[(j + 1) * (DH / 2)];
+                            const uint32_t v2 = vrow[(j + 2) * (DH / 2)], v3 = vrow[(j + 3) * (DH / 2)];
+                            bx0 = fmaf(pj.x, bf16lo(v0), bx0);
+                            by0 = fmaf(pj.x, bf16hi(v0), by0);
+                            bx1 = fmaf(pj.y, bf16lo(v1), bx1);
+                            by1 = fmaf(pj.y, bf16hi(v1), by1);
+                            bx0 = fmaf(pj.z, bf16lo(v2), bx0);
+                            by0 = fmaf(pj.z, bf16hi(v2), by0);
+                            bx1 = fmaf(pj.w, bf16lo(v3), bx1);
+                            by1 = fmaf(pj.w, bf16hi(v3), by1);
+                        }
+                        for (; j < j1; ++j) {
+                            const uint32_t v = vrow[j * (DH / 2)];
+                            bx0 = fmaf(s_p[j], bf16lo(v), bx0);
+                            by0 = fmaf(s_p[j], bf16hi(v), by0);
+                        }
+                        ax = ax * alpha + (bx0 + bx1);
+                        ay = ay * alpha + (by0 + by1);
+                    } else {
+                        // weighted values: thread t owns coordinate t
+                        // (rows past nvalid hold stale data: they are skipped, never multiplied by 0)
+                        const uint16_t* vcol = reinterpret_cast<const uint16_t*>(st + KPC * ROWB) + t;
+                        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                        const int n4 = nvalid & ~3;
+        #pragma unroll 4
+                        for (int j = 0; j < n4; j += 4) {
+                            const float4 pj = *reinterpret_cast<const float4*>(s_p + j);
+                            a0 = fmaf(pj.x, __uint_as_float((uint32_t)vcol[(j + 0) * DH] << 16), a0);
+                            a1 = fmaf(pj.y, __uint_as_float((uint32_t)vcol[(j + 1) * DH] << 16), a1);
+                            a2 = fmaf(pj.z, __uint_as_float((uint32_t)vcol[(j + 2) * DH] << 16), a2);
+                            a3 = fmaf(pj.w, __uint_as_float((uint32_t)vcol[(j + 3) * DH] << 16), a3);
+                        }
+                        for (int j = n4; j < nvalid; ++j) a0 = fmaf(s_p[j], __uint_as_float((uint32_t)vcol[j * DH] << 16), a0);
+                        acc = acc * alpha + ((a0 + a1) + (a2 + a3));
                     }
-                    for (int j = n4; j < nvalid; ++j) a0 = fmaf(s_p[j], __uint_as_float((uint32_t)vcol[j * DH] << 16), a0);
-                    acc = acc * alpha + ((a0 + a1) + (a2 + a3));
+                    l_run = l_run * alpha + ((s_wl[0] + s_wl[1]) + (s_wl[2] + s_wl[3]));
+                    m_run = m_new;
                 }
-                l_run = l_run * alpha + ((s_wl[0] + s_wl[1]) + (s_wl[2] + s_wl[3]));
-                m_run = m_new;
             }
             // the stage goes back to the copy engine once every warp is done with it: order
             // these reads before its refill
@@ -374,7 +513,27 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
 
             const bool last = (k == nu - 1) || up.ci == up.nc - 1;
             if (!last) continue;
-            if (PV2) {
+            if (MODE == 2) {
+                // the four warps' running states of the piece, into coordinate t
+                if (lane == 0) {
+                    s_wm[warp] = mw;
+                    s_wl[warp] = lw;
+                }
+                *reinterpret_cast<float4*>(&s_comb[warp][4 * lane]) = make_float4(w0, w1, w2, w3);
+                cons_bar();
+                const float M = fmaxf(fmaxf(s_wm[0], s_wm[1]), fmaxf(s_wm[2], s_wm[3]));
+                float A = 0.f, L = 0.f;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    const float f = (s_wm[w] == -INFINITY) ? 0.f : exp2f(s_wm[w] - M);
+                    A = fmaf(f, s_comb[w][t], A);
+                    L = fmaf(f, s_wl[w], L);
+                }
+                acc = A;
+                l_run = L;
+                m_run = M;
+                cons_bar();
+            } else if (PV2) {
                 // the two key halves of the piece, into coordinate t
                 s_comb[kh][2 * dp] = ax;
                 s_comb[kh][2 * dp + 1] = ay;
@@ -507,8 +666,9 @@ void attn_plan(AttnParams& p, int num_sms) {
 }
 
 cudaError_t attn_prepare() {
-    cudaError_t e = cudaFuncSetAttribute(k_attn<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, NST * STAGE);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, NST * STAGE);
+    cudaError_t e = cudaFuncSetAttribute(k_attn<PM_ATTN_MANY>, cudaFuncAttributeMaxDynamicSharedMemorySize, NST * STAGE);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attn<PM_ATTN_FEW>, cudaFuncAttributeMaxDynamicSharedMemorySize, NST * STAGE);
     return e;
 }
 
@@ -539,9 +699,9 @@ cudaError_t launch_attn(const AttnParams& p, cudaStream_t s, bool pdl) {
     }
     cfg.attrs = attr;
     cfg.numAttrs = (unsigned)na;
-    // many units per CTA (one or two CTAs per head, or the balanced split): PV2
-    return (p.cluster == 0 || p.cluster <= 2) ? cudaLaunchKernelEx(&cfg, k_attn<true>, p)
-                                              : cudaLaunchKernelEx(&cfg, k_attn<false>, p);
+    // many units per CTA (one or two CTAs per head, or the balanced split) vs one or two
+    return (p.cluster == 0 || p.cluster <= 2) ? cudaLaunchKernelEx(&cfg, k_attn<PM_ATTN_MANY>, p)
+                                              : cudaLaunchKernelEx(&cfg, k_attn<PM_ATTN_FEW>, p);
 }
 
 }  // namespace pm
