@@ -53,6 +53,7 @@ template <int CH, int PRO, int EPI, int UNIT>
 __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const GemvParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int RPU = (UNIT == U_ROW) ? 1 : 2;
+    constexpr bool NORM = PRO == PRO_RMSNORM || PRO == PRO_RMSNORM_EMB;
     const int W = p.warps;
     const int P = p.P;
     const int K = p.K;
@@ -92,10 +93,18 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
             const uint64_t pol = l2_evict_first_policy();
+            // a CTA's range lies in one segment (the plan makes the grid a multiple of nseg)
+            const uint16_t* Wb = p.W;
+            int ub = 0;
+            if (p.nseg > 1) {
+                const int seg = u0 / p.seg_units;
+                Wb = p.Wseg[seg];
+                ub = seg * p.seg_units;
+            }
+            int slot = 0, round = 0;  // k % nst, k / nst without a division per stage
             for (int k = 0; k < nstages; ++k) {
-                const int slot = k % p.nst;
                 if (k >= p.nst) {
-                    if (!mbar_wait(&empty[slot], (uint32_t)((k / p.nst) - 1) & 1u)) {
+                    if (!mbar_wait(&empty[slot], (uint32_t)(round - 1) & 1u)) {
                         s_flags[0] = 1;
                         set_status(p.st.status, PM_DEV_ERR_TIMEOUT);
                         break;
@@ -107,15 +116,19 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
                 if (UNIT == U_PAIR_SPLIT) {
                     const uint32_t bytes = (uint32_t)n * row_bytes;
                     mbar_arrive_expect_tx(&full[slot], 2u * bytes);
-                    bulk_g2s(dst, p.W + (size_t)ua * K, bytes, &full[slot], pol);
-                    bulk_g2s(dst + (size_t)p.upst * row_bytes, p.W + (size_t)(ua + p.split_rows) * K, bytes,
+                    bulk_g2s(dst, Wb + (size_t)(ua - ub) * K, bytes, &full[slot], pol);
+                    bulk_g2s(dst + (size_t)p.upst * row_bytes, Wb + (size_t)(ua - ub + p.split_rows) * K, bytes,
                              &full[slot], pol);
                 } else {
                     const uint32_t bytes = (uint32_t)(n * RPU) * row_bytes;
                     mbar_arrive_expect_tx(&full[slot], bytes);
-                    bulk_g2s(dst, p.W + (size_t)ua * RPU * K, bytes, &full[slot], pol);
+                    bulk_g2s(dst, Wb + (size_t)(ua - ub) * RPU * K, bytes, &full[slot], pol);
                 }
                 s_flags[2] = k + 1;
+                if (++slot == p.nst) {
+                    slot = 0;
+                    ++round;
+                }
             }
         }
     } else {
@@ -125,7 +138,7 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
         const int kslice = K / P;
         // the norm scale does not depend on the previous kernel: in flight before the wait
         uint4 alv[CH];
-        if (PRO == PRO_RMSNORM) {
+        if (NORM) {
             const uint16_t* al = p.alpha + (size_t)pp * kslice;
 #pragma unroll
             for (int ci = 0; ci < CH; ++ci) alv[ci] = *reinterpret_cast<const uint4*>(al + 8 * (lane + 32 * ci));
@@ -197,7 +210,32 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
             xr[8 * ci + 0] = a.x; xr[8 * ci + 1] = a.y; xr[8 * ci + 2] = a.z; xr[8 * ci + 3] = a.w;
             xr[8 * ci + 4] = bb.x; xr[8 * ci + 5] = bb.y; xr[8 * ci + 6] = bb.z; xr[8 * ci + 7] = bb.w;
         }
-        if (PRO == PRO_RMSNORM) {
+        if (PRO == PRO_RMSNORM_EMB) {
+            // depformer layer 0: the input projection (computed for every position at the
+            // start of the call) plus the embedding of the previous position's code, or of
+            // the text token at position 0 -- decided by the kernel this one waited for
+            const int tok = (p.q == 0) ? p.st.dep_tok[b] : p.st.dep_codes[(size_t)b * p.Q + p.q - 1];
+            const uint16_t* eb = p.emb + (size_t)tok * K + (size_t)pp * kslice;
+#pragma unroll
+            for (int ci = 0; ci < CH; ++ci) {
+                const uint4 e = *reinterpret_cast<const uint4*>(eb + 8 * (lane + 32 * ci));
+                xr[8 * ci + 0] += bf16lo(e.x); xr[8 * ci + 1] += bf16hi(e.x);
+                xr[8 * ci + 2] += bf16lo(e.y); xr[8 * ci + 3] += bf16hi(e.y);
+                xr[8 * ci + 4] += bf16lo(e.z); xr[8 * ci + 5] += bf16hi(e.z);
+                xr[8 * ci + 6] += bf16lo(e.w); xr[8 * ci + 7] += bf16hi(e.w);
+            }
+            if (c == 0 && r == 0 && !abort_frame) {
+                // the residual stream of the position: warps of stage row 0 cover every column once
+                float* xo = p.x_out + (size_t)b * K + (size_t)pp * kslice;
+#pragma unroll
+                for (int ci = 0; ci < CH; ++ci) {
+                    float4* d4 = reinterpret_cast<float4*>(xo + 8 * (lane + 32 * ci));
+                    d4[0] = make_float4(xr[8 * ci + 0], xr[8 * ci + 1], xr[8 * ci + 2], xr[8 * ci + 3]);
+                    d4[1] = make_float4(xr[8 * ci + 4], xr[8 * ci + 5], xr[8 * ci + 6], xr[8 * ci + 7]);
+                }
+            }
+        }
+        if (NORM) {
             // warps of stage row 0 cover every column exactly once
             float ss = 0.f;
 #pragma unroll
@@ -240,9 +278,13 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
             i_unit = r / RPU;
             j_row = r % RPU;
         }
+        int slot = 0, round = 0;  // k % nst, k / nst without a division per stage
         for (int k = 0; k < nstages; ++k) {
-            const int slot = k % p.nst;
-            if (!mbar_wait(&full[slot], (uint32_t)(k / p.nst) & 1u)) {
+            if (k > 0 && ++slot == p.nst) {
+                slot = 0;
+                ++round;
+            }
+            if (!mbar_wait(&full[slot], (uint32_t)round & 1u)) {
                 s_flags[0] = 1;
                 set_status(p.st.status, PM_DEV_ERR_TIMEOUT);
                 break;
@@ -284,19 +326,13 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
         return s;
     };
 
-    if (EPI == E_STORE || EPI == E_RESIDUAL || EPI == E_EMB_ADD) {
+    if (EPI == E_STORE || EPI == E_RESIDUAL) {
         if (aborted || tid >= nthr) return;
         float* yb = p.y + (size_t)b * p.y_stride;
-        int tok = 0;
-        if (EPI == E_EMB_ADD) tok = (p.q == 0) ? p.st.dep_tok[b] : p.st.dep_codes[(size_t)b * p.Q + p.q - 1];
         for (int lu = tid; lu < nu; lu += nthr) {
             const int row = u0 + lu;
             float v = rowsum(lu, 0);
             if (EPI == E_RESIDUAL) v += (lu == tid) ? ep_res : yb[row];
-            if (EPI == E_EMB_ADD) {
-                const uint16_t e = p.emb[(size_t)tok * p.y_stride + row];
-                v += __uint_as_float((uint32_t)e << 16);
-            }
             yb[row] = v;
         }
     } else if (EPI == E_SWIGLU) {
@@ -444,7 +480,7 @@ cudaError_t prepare_t() {
     X(PRO_PLAIN, E_RESIDUAL, U_ROW)              \
     X(PRO_RMSNORM, E_SWIGLU, U_PAIR_SPLIT)       \
     X(PRO_RMSNORM, E_HEAD, U_ROW)                \
-    X(PRO_PLAIN, E_EMB_ADD, U_ROW)               \
+    X(PRO_RMSNORM_EMB, E_DEP_QKV, U_ROW)         \
     X(PRO_RMSNORM, E_DEP_QKV, U_ROW)             \
     X(PRO_PLAIN, E_DEP_HEAD, U_ROW)              \
     X(PRO_PLAIN, E_STORE, U_ROW)                 \
@@ -471,6 +507,13 @@ bool plan_gemv(GemvParams& p, int rpu, int num_sms) {
     p.nst = nst;
     const int ctas = PM_GEMV_CTAS_PER_SM * num_sms;
     p.grid_per_b = p.n_units < ctas ? p.n_units : ctas;
+    if (p.nseg > 1) {
+        // consecutive matrices of seg_units units each: a multiple of nseg CTAs keeps every
+        // CTA's range inside one of them
+        if (p.nseg > PM_GEMV_MAX_SEG || p.seg_units <= 0 || p.n_units != p.nseg * p.seg_units) return false;
+        p.grid_per_b = (p.grid_per_b / p.nseg) * p.nseg;
+        if (p.grid_per_b < p.nseg) p.grid_per_b = p.nseg;
+    }
     p.units_cta_max = (p.n_units + p.grid_per_b - 1) / p.grid_per_b;
     p.smem = (size_t)nst * p.stage_bytes + 16u * (size_t)nst + (size_t)p.units_cta_max * rpu * p.P * 4u + 32u * 4u;
     if (p.x_in_smem) p.smem += 4u * (size_t)K + 16u;  // the input vector built by the prologue

@@ -66,6 +66,7 @@ struct pm_ctx {
     float* tc_part = nullptr;
     uint32_t* tc_count = nullptr;
     float *dz = nullptr, *dq = nullptr, *ds = nullptr;
+    float* dzin = nullptr;  // [B_max][dep_steps][dep_D]: the depformer input projections of a call
     uint16_t* dkv = nullptr;
     // sampling: device-resident settings, the logits the samplers read, which kinds sample
     SampleCfg* scfg = nullptr;
@@ -645,22 +646,30 @@ static pm_status record_depformer(pm_ctx* c, int B, cudaStream_t s) {
     bp.text_rows = f.dep_text_in;
     PM_CUDA(launch_dep_begin(bp, s, false));
     const size_t dl_elems = (size_t)f.B_max * f.dep_H * Q * f.dep_dh;
-    for (int q = 0; q < Q; ++q) {
+    {
+        // the input projections of the temporal hidden state for every depth position: they
+        // depend only on h, so one launch (a segment per position) instead of one per
+        // position on the dependent chain; each position's layer-0 prologue adds the
+        // embedding of the code before it
         GemvParams p = base_params(c);
-        p.W = c->d_in[q];
+        p.W = c->d_in[0];  // (one position: a plain GEMV)
+        p.nseg = Q;
+        p.seg_units = Dd;
+        for (int q = 0; q < Q; ++q) p.Wseg[q] = c->d_in[q];
         p.K = D;
-        p.n_units = Dd;
+        p.n_units = Q * Dd;
         p.B = B;
         p.x = c->h;
         p.x_stride = D;
-        p.y = c->dz;
-        p.y_stride = Dd;
-        p.emb = (q == 0) ? c->d_temb : c->d_aemb[q - 1];
-        p.q = q;
-        p.Q = Q;
-        pm_status ps = plan(c, p, 1, "depformer_in");
+        p.y = c->dzin;
+        p.y_stride = Q * Dd;
+        pm_status ps = plan(c, p, 1, "depformer input projections");
         if (ps) return ps;
-        PM_CUDA(launch_gemv(PRO_PLAIN, E_EMB_ADD, U_ROW, p, s, true));
+        PM_CUDA(launch_gemv(PRO_PLAIN, E_STORE, U_ROW, p, s, true));
+    }
+    for (int q = 0; q < Q; ++q) {
+        GemvParams p;
+        pm_status ps;
         for (int j = 0; j < f.dep_layers; ++j) {
             uint16_t* dkc = c->dkv + (size_t)(2 * j + 0) * dl_elems;
             uint16_t* dvc = c->dkv + (size_t)(2 * j + 1) * dl_elems;
@@ -671,6 +680,13 @@ static pm_status record_depformer(pm_ctx* c, int B, cudaStream_t s) {
             p.B = B;
             p.x = c->dz;
             p.x_stride = Dd;
+            if (j == 0) {
+                // input projection + embedding of the previous code, kept as the residual
+                p.x = c->dzin + (size_t)q * Dd;
+                p.x_stride = Q * Dd;
+                p.emb = (q == 0) ? c->d_temb : c->d_aemb[q - 1];
+                p.x_out = c->dz;
+            }
             p.alpha = c->d_norm1[j];
             p.y = c->dq;
             p.y_stride = Dd;
@@ -683,7 +699,7 @@ static pm_status record_depformer(pm_ctx* c, int B, cudaStream_t s) {
             p.dvc = dvc;
             ps = plan(c, p, 1, "depformer in_proj");
             if (ps) return ps;
-            PM_CUDA(launch_gemv(PRO_RMSNORM, E_DEP_QKV, U_ROW, p, s, true));
+            PM_CUDA(launch_gemv(j == 0 ? PRO_RMSNORM_EMB : PRO_RMSNORM, E_DEP_QKV, U_ROW, p, s, true));
             // W_o + residual, with the depth attention computed in its prologue
             p = base_params(c);
             p.W = c->d_o[j] + (size_t)q * Dd * Dd;
@@ -940,7 +956,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     void* p_damax; void* p_dcount; void* p_dcodes; void* p_dtok; void* p_dsup;
     void* p_io; void* p_dio; void *p_x, *p_q, *p_o, *p_s, *p_h, *p_part, *p_cnt, *p_freq, *p_dz, *p_dq,
         *p_ds, *p_dkv, *p_rtab, *p_xb, *p_ob, *p_sb, *p_ss, *p_tcp, *p_tcc, *p_scfg, *p_slog, *p_dslog,
-        *p_sres, *p_apart, *p_acnt, *p_skv;
+        *p_sres, *p_apart, *p_acnt, *p_skv, *p_dzin;
     // rows of the activation buffers: the batch, or a prefill pass of PM_SEQ_MAX_ROWS frames
     const int RM = BM > PM_SEQ_MAX_ROWS ? BM : PM_SEQ_MAX_ROWS;
     // tensor-core path scratch (batches and prefill passes), sized from the plans of this
@@ -999,7 +1015,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
         {&p_xb, 2u * NP * f.D}, {&p_ob, 2u * NP * f.D}, {&p_sb, 2u * NP * f.ffn}, {&p_ss, 4u * ss_floats},
         {&p_tcp, 4u * tc_part_floats}, {&p_tcc, 4u * (size_t)tc_count_max},
         {&p_dz, 4u * BM * (Dd ? Dd : 1)}, {&p_dq, 4u * BM * (Dd ? Dd : 1)},
-        {&p_ds, 4u * BM * (Fd ? Fd : 1)},
+        {&p_ds, 4u * BM * (Fd ? Fd : 1)}, {&p_dzin, 4u * BM * (Dd ? Dd : 1) * Q},
         {&p_dkv, c->has_dep ? 2u * 2u * f.dep_layers * BM * f.dep_H * Q * f.dep_dh : 16u},
         {&p_scfg, sizeof(SampleCfg)}, {&p_slog, 4u * BM * f.text_out},
         {&p_dslog, c->has_dep ? 4u * BM * f.dep_card : 16u},
@@ -1052,6 +1068,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     c->tc_part = (float*)p_tcp;
     c->tc_count = (uint32_t*)p_tcc;
     c->dz = (float*)p_dz;
+    c->dzin = (float*)p_dzin;
     c->dq = (float*)p_dq;
     c->ds = (float*)p_ds;
     c->dkv = (uint16_t*)p_dkv;

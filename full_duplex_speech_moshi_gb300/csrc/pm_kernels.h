@@ -21,7 +21,9 @@ enum Unit { U_ROW = 0, U_PAIR_ADJ = 1, U_PAIR_SPLIT = 2 };
 enum Prologue {
     PRO_PLAIN = 0,    // x as given
     PRO_RMSNORM = 1,  // x normalised (fp32 RMSNorm, learned scale)
-    PRO_DEPATTN = 2   // x = depth attention output, computed by every CTA from q and the depth cache
+    PRO_DEPATTN = 2,  // x = depth attention output, computed by every CTA from q and the depth cache
+    PRO_RMSNORM_EMB = 3  // depformer layer 0: x = input projection + E[previous code], written to
+                         // x_out (the residual stream) by CTA 0, then normalised
 };
 enum Epilogue {
     E_STORE = 0,      // y[row] = dot
@@ -29,13 +31,17 @@ enum Epilogue {
     E_SWIGLU = 2,     // y[u] = SiLU(dot(row u)) * dot(row u + F)
     E_QKV_ROPE = 3,   // temporal fused QKV: RoPE on Q, K; K, V into the KV ring
     E_HEAD = 4,       // text head: logits + argmax, frame finalisation
-    E_EMB_ADD = 5,    // depformer input: y[row] = dot + E[token][row]
     E_DEP_QKV = 6,    // depth QKV: q to y, k, v into the depth cache at position q
     E_DEP_HEAD = 7    // depth head: logits + argmax or supplied code
 };
 
+// matrices one GEMV launch can take as consecutive segments of its rows
+#define PM_GEMV_MAX_SEG 32
+
 struct GemvParams {
     const uint16_t* W;     // [rows][K]
+    int nseg, seg_units;   // > 1: units s*seg_units .. are rows of Wseg[s] (W unused)
+    const uint16_t* Wseg[PM_GEMV_MAX_SEG];
     int K;
     int n_units;           // units (rows or row pairs) of the whole matrix
     int split_rows;        // U_PAIR_SPLIT: unit u = rows u and u + split_rows
@@ -66,7 +72,8 @@ struct GemvParams {
     const DepIO* dio;
     int q;                 // depth position
     int Q;                 // depth positions per frame
-    const uint16_t* emb;   // E_EMB_ADD table [rows_emb][y dim]
+    const uint16_t* emb;   // PRO_RMSNORM_EMB table [rows][K]
+    float* x_out;          // PRO_RMSNORM_EMB: the assembled (pre-norm) input [B][K], by CTA 0
     int emb_rows;
     uint16_t* dkc;         // E_DEP_QKV / PRO_DEPATTN: depth K cache of this layer [B_max][Hd][Q][dhd]
     uint16_t* dvc;
