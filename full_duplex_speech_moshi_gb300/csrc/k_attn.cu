@@ -158,7 +158,7 @@ __device__ __forceinline__ void next_unit(UnitPos& r, const int* s_nc, const int
 #endif
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
-    constexpr bool PV2 = MODE >= 1;  // query in registers
+    constexpr bool QREG = MODE >= 1;  // the query held in registers (modes 1 and 2)
     static_assert(MODE != 2 || KPC == 64, "per-warp softmax takes 16 keys per warp");
     extern __shared__ __align__(128) uint8_t ring[];  // [NST][STAGE]
     __shared__ int s_first[PM_MAX_B_DEV + 1], s_nc[PM_MAX_B_DEV], s_pos[PM_MAX_B_DEV];
@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
                         const int jc = (j + lane) % NCOL;  // staggered 16-byte column
                         const uint4 kv = *reinterpret_cast<const uint4*>(kr + jc * 16);
                         float q8[8];
-                        if (PV2) {
+                        if (QREG) {
 #pragma unroll
                             for (int e = 0; e < 8; ++e) q8[e] = qr[j][e];
                         } else {
@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
                     for (int o = 1; o <= 16; o <<= 1) ws += __shfl_xor_sync(0xffffffffu, ws, o);
                     if (lane == 0) s_wl[warp] = ws;
                     cons_bar();
-                    if (PV2) {
+                    if (MODE == 1) {
                         // weighted values over this thread's key half (rows past nvalid hold stale data:
                         // they are skipped, never multiplied by 0)
                         const uint32_t* vrow = reinterpret_cast<const uint32_t*>(st + KPC * ROWB) + dp;
@@ -533,7 +533,7 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
                 l_run = L;
                 m_run = M;
                 cons_bar();
-            } else if (PV2) {
+            } else if (MODE == 1) {
                 // the two key halves of the piece, into coordinate t
                 s_comb[kh][2 * dp] = ax;
                 s_comb[kh][2 * dp + 1] = ay;

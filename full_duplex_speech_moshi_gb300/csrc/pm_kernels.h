@@ -74,7 +74,6 @@ struct GemvParams {
     int Q;                 // depth positions per frame
     const uint16_t* emb;   // PRO_RMSNORM_EMB table [rows][K]
     float* x_out;          // PRO_RMSNORM_EMB: the assembled (pre-norm) input [B][K], by CTA 0
-    int emb_rows;
     uint16_t* dkc;         // E_DEP_QKV / PRO_DEPATTN: depth K cache of this layer [B_max][Hd][Q][dhd]
     uint16_t* dvc;
     int dep_ctx;           // PRO_DEPATTN: attention window (x = q of depth position q)
