@@ -34,6 +34,23 @@ import numpy as np  # noqa: E402
 from full_duplex_speech_moshi_gb300 import inputs as I  # noqa: E402
 
 METRIC = "temporal frames/s (B=1, 32-block stack, greedy text feedback)"
+
+
+def max_over_ranks(x: float, dist=None, device: str = "cpu") -> float:
+    """The largest x over all ranks of the process group, on every rank (x itself
+    without one).  Timed regions are reported as the slowest rank's."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(steps: int, ms: float, world: int, rows_per_rank: int) -> float:
+    """Units per second of the whole job: every rank runs `steps` steps of `rows_per_rank`
+    streams each (replicas: independent models), all within the slowest rank's `ms`."""
+    return steps / (ms / 1000.0) * world * rows_per_rank
 PRIME = 256
 W_IN_BYTES = 2 * 11264 * 4096 * 2          # linear_in weights per launch: 184,549,376
 # algorithmic bytes of one B=1 frame that do not depend on the cache length:
@@ -306,12 +323,8 @@ def main():
         end.record(stream)
         torch.cuda.synchronize()
     barrier()
-    ms = start.elapsed_time(end)
-    if dist is not None:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    fps = args.steps / (ms / 1000.0) * world * BB
+    ms = max_over_ranks(start.elapsed_time(end), dist, dev)
+    fps = whole_job_rate(args.steps, ms, world, BB)
     ms_step = ms / args.steps
     # keys read per frame = min(pos + 1, ctx); one new K/V row written
     mean_keys = statistics.mean(min(p + 1, s.ctx) for p in range(p0, p0 + args.steps))
@@ -377,12 +390,8 @@ def main():
     e_end.record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
-    e2e_ms = max(e_start.elapsed_time(e_end), wall * 1000.0)
-    if dist is not None:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e_fps = args.steps / (e2e_ms / 1000.0) * world * BB
+    e2e_ms = max_over_ranks(max(e_start.elapsed_time(e_end), wall * 1000.0), dist, dev)
+    e2e_fps = whole_job_rate(args.steps, e2e_ms, world, BB)
 
     extras = {}
     if args.extras and BB == 1:
