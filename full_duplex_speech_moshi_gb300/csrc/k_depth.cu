@@ -26,6 +26,9 @@ __global__ void __launch_bounds__(256) k_dep_begin(const DepBeginParams p) {
             tok = 0;
         }
         p.st.dep_tok[i] = tok;
+        // depth-head accumulators start cleared, also after a call whose head did not finish
+        p.st.dep_amax[i] = 0ull;
+        p.st.dep_count[i] = 0u;
     }
     for (int i = threadIdx.x; i < p.B * p.Q; i += blockDim.x) {
         int sup = p.dio->supplied ? p.dio->supplied[i] : -1;

@@ -12,7 +12,8 @@
 //             resolved id of frame p-delay_k (ring slot (p - delay_k) & 3)
 //                                           if p - delay_k >= first_pos[b],
 //             the stream's initial ID       otherwise.
-// If any resolved ID of any row is outside -1..rows-1 the frame is aborted: the status
+// If any resolved ID of any row (including one read back from the delay ring) is outside
+// -1..rows-1 the frame is aborted: the status
 // word records PM_DEV_ERR_INVALID_ID, the abort flag is raised for the rest of the frame,
 // and no state changes.
 #include "pm_kernels.h"
@@ -33,12 +34,19 @@ __global__ void __launch_bounds__(128) k_embed(const EmbedParams p) {
     if (seq) {
         bad = *(volatile uint32_t*)&p.st.status[1] != 0u;  // set by k_seq_prepare
     } else {
-        // validate every row's IDs (cheap: B * 17 values) so all CTAs agree on the abort
+        // validate every row's IDs (cheap: B * 17 values) so all CTAs agree on the abort;
+        // a delayed stream's input comes from the delay ring, which is checked the same way
+        // (the ring only ever holds validated IDs unless a restored snapshot was corrupt)
         for (int i = tid; i < p.B * S; i += blockDim.x) {
             const int bb = i / S, k = i % S;
             int id = p.io->ids[i];
             if (id == -3) id = p.st.sel[(size_t)bb * PM_MAX_STREAMS_DEV + k];
             if (id < -1 || id >= p.rows[k]) bad = 1;
+            const int src = p.st.pos[bb] - p.delays[k];
+            if (p.delays[k] != 0 && src >= p.st.first_pos[bb]) {
+                const int in = p.st.ring[((size_t)bb * 4 + (src & 3)) * PM_MAX_STREAMS_DEV + k];
+                if (in < -1 || in >= p.rows[k]) bad = 1;
+            }
         }
         bad = __syncthreads_or(bad);
     }
@@ -64,6 +72,12 @@ __global__ void __launch_bounds__(128) k_embed(const EmbedParams p) {
     if (!seq && blockIdx.x == 0 && b == 0 && tid == 0) {
         p.st.status[1] = bad ? 1u : 0u;
         if (bad) set_status(p.st.status, PM_DEV_ERR_INVALID_ID);
+    }
+    if (!seq && blockIdx.x == 0 && tid == 0) {
+        // the text head's argmax accumulator and completion counter start every frame
+        // cleared, also after a frame whose head did not finish (a wait that ran out)
+        p.st.amax[b] = 0ull;
+        p.st.head_count[b] = 0u;
     }
     __syncthreads();
     if (bad) return;

@@ -99,6 +99,11 @@ __global__ void __launch_bounds__(NTH, 1) k_frame(const FrameProgParams p) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tid = threadIdx.x;
     const int pos = p.st.pos[0];
+    // poll budget of the ring and phase waits (the drain after a timeout keeps the full one)
+    const uint32_t budget = wait_budget(p.st);
+    const unsigned long long grid_limit = (unsigned long long)budget << 4;
+    uint32_t* const exit_count = &p.bar[p.n_phases];     // CTAs done with this launch
+    uint32_t* const timeouts = &p.bar[p.n_phases + 1];  // CTAs whose wait ran out in this launch
 
     // ---------------- validation (all threads), barrier init ----------------
     if (tid == 0) {
@@ -114,6 +119,12 @@ __global__ void __launch_bounds__(NTH, 1) k_frame(const FrameProgParams p) {
         int id = p.io->ids[tid];
         if (id == -3) id = p.st.sel[tid];
         if (id < -1 || id >= p.rows[tid]) bad = 1;
+        // a delayed stream's input comes back from the delay ring: checked the same way
+        const int src = pos - p.delays[tid];
+        if (p.delays[tid] != 0 && src >= p.st.first_pos[0]) {
+            const int in = p.st.ring[(src & 3) * PM_MAX_STREAMS_DEV + tid];
+            if (in < -1 || in >= p.rows[tid]) bad = 1;
+        }
     }
     bad = __syncthreads_or(bad);
     if (bad) {
@@ -121,7 +132,7 @@ __global__ void __launch_bounds__(NTH, 1) k_frame(const FrameProgParams p) {
             p.st.status[1] = 1u;
             set_status(p.st.status, PM_DEV_ERR_INVALID_ID);
         }
-        return;  // nothing was issued; the frame is a no-op
+        return;  // nothing was issued and no counter touched; the frame is a no-op
     }
 
     if (warp == NCW) {
@@ -136,7 +147,7 @@ __global__ void __launch_bounds__(NTH, 1) k_frame(const FrameProgParams p) {
                     ok = false;
                     return -1;
                 }
-                if (seq >= NSLOT && !mbar_wait(&empty[slot], (uint32_t)((seq / NSLOT) - 1) & 1u)) {
+                if (seq >= NSLOT && !mbar_wait_n(&empty[slot], (uint32_t)((seq / NSLOT) - 1) & 1u, budget)) {
                     ok = false;
                     return -1;
                 }
@@ -197,7 +208,8 @@ __global__ void __launch_bounds__(NTH, 1) k_frame(const FrameProgParams p) {
             }
             if (!ok && !*(volatile int*)&s_flag[0]) {
                 s_flag[0] = 1;
-                set_status(p.st.status, PM_DEV_ERR_TIMEOUT);
+                timeout_abort(p.st);
+                atomicAdd(timeouts, 1u);
             }
             s_flag[1] = seq;
         }
@@ -209,11 +221,15 @@ __global__ void __launch_bounds__(NTH, 1) k_frame(const FrameProgParams p) {
         int seq = 0;
         const float eps = p.eps;
         auto timed_out = [&]() -> bool { return *(volatile int*)&s_flag[0] != 0; };
+        auto note_timeout = [&]() {
+            if (!timed_out()) atomicAdd(timeouts, 1u);
+            s_flag[0] = 1;
+            timeout_abort(p.st);
+        };
         auto wait_full = [&](int slot, uint32_t parity) -> bool {
             if (timed_out()) return false;
-            if (!mbar_wait(&full[slot], parity)) {
-                s_flag[0] = 1;
-                set_status(p.st.status, PM_DEV_ERR_TIMEOUT);
+            if (!mbar_wait_n(&full[slot], parity, budget)) {
+                note_timeout();
                 return false;
             }
             return true;
@@ -223,11 +239,10 @@ __global__ void __launch_bounds__(NTH, 1) k_frame(const FrameProgParams p) {
             // wait for every CTA to finish the previous phase
             if (ph > 0) {
                 if (tid == 0 && !timed_out()) {
-                    uint32_t it = 0;
+                    unsigned long long it = 0;
                     while (ld_acquire_u32(&p.bar[ph - 1]) < (uint32_t)G) {
-                        if (++it > (PM_SPIN_LIMIT << 4)) {
-                            s_flag[0] = 1;
-                            set_status(p.st.status, PM_DEV_ERR_TIMEOUT);
+                        if (++it > grid_limit) {
+                            note_timeout();
                             break;
                         }
                     }
@@ -579,36 +594,49 @@ __global__ void __launch_bounds__(NTH, 1) k_frame(const FrameProgParams p) {
             cons_bar();
             if (tid == 0) red_release_add(&p.bar[ph], 1u);
         }
-        // final phase: the greedy token and the frame's state advance (CTA 0)
+        // final phase: the greedy token and the frame's state advance (CTA 0), only when
+        // no CTA's wait ran out in this launch (then the frame leaves no selection and the
+        // position stays, like an aborted frame)
         if (!timed_out() && c == 0) {
             if (tid == 0) {
-                uint32_t it = 0;
+                unsigned long long it = 0;
                 bool done = true;
                 while (ld_acquire_u32(&p.bar[p.n_phases - 1]) < (uint32_t)G) {
-                    if (++it > (PM_SPIN_LIMIT << 4)) {
+                    if (++it > grid_limit) {
                         done = false;
-                        set_status(p.st.status, PM_DEV_ERR_TIMEOUT);
+                        note_timeout();
                         break;
                     }
                 }
-                if (done) {
+                if (done && ld_acquire_u32(timeouts) == 0u) {
                     __threadfence();
                     const unsigned long long key = atomicExch(&p.st.amax[0], 0ull);
                     const int32_t am = (int32_t)unpack_argmax_index(key);
                     if (p.io->token) p.io->token[0] = am;
                     p.st.sel[0] = am;
                     p.st.pos[0] = pos + 1;
-                    for (int i = 0; i < p.n_phases; ++i) p.bar[i] = 0u;
                 }
             }
         }
     }
     __syncthreads();
-    if (s_flag[0] && tid == 0) {
-        // a wait ran out: let the copies already issued land before the CTA exits
-        const int issued = s_flag[1];
-        for (int i = issued - NSLOT < 0 ? 0 : issued - NSLOT; i < issued; ++i)
-            (void)mbar_wait(&full[i % NSLOT], (uint32_t)(i / NSLOT) & 1u);
+    if (tid == 0) {
+        if (s_flag[0]) {
+            // a wait ran out: let the copies already issued land before the CTA exits
+            const int issued = s_flag[1];
+            for (int i = issued - NSLOT < 0 ? 0 : issued - NSLOT; i < issued; ++i)
+                (void)mbar_wait(&full[i % NSLOT], (uint32_t)(i / NSLOT) & 1u);
+        }
+        // The last CTA out clears what the launch counted with (phase counters, the exit and
+        // timeout counters, the head's argmax, the attention merge counters), whether or not a
+        // wait ran out: every CTA has passed its last read of them by then.
+        __threadfence();
+        if (atomicAdd(exit_count, 1u) == (uint32_t)G - 1u) {
+            __threadfence();
+            for (int i = 0; i < p.n_phases + 2; ++i) p.bar[i] = 0u;
+            p.st.amax[0] = 0ull;
+            for (int h = 0; h < p.H; ++h) p.att_count[h] = 0u;
+        }
     }
 }
 

@@ -72,6 +72,8 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
     const int nu = u1 - u0;
     const int nstages = (nu + p.upst - 1) / p.upst;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // poll budget of the ring waits (the drain after a timeout keeps the full budget)
+    const uint32_t budget = wait_budget(p.st);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.nst; ++s) {
@@ -104,9 +106,9 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
             int slot = 0, round = 0;  // k % nst, k / nst without a division per stage
             for (int k = 0; k < nstages; ++k) {
                 if (k >= p.nst) {
-                    if (!mbar_wait(&empty[slot], (uint32_t)(round - 1) & 1u)) {
+                    if (!mbar_wait_n(&empty[slot], (uint32_t)(round - 1) & 1u, budget)) {
                         s_flags[0] = 1;
-                        set_status(p.st.status, PM_DEV_ERR_TIMEOUT);
+                        timeout_abort(p.st);
                         break;
                     }
                 }
@@ -284,9 +286,9 @@ __global__ void __launch_bounds__(32 * (PM_GEMV_MAX_WARPS + 1), 1) k_gemv(const 
                 slot = 0;
                 ++round;
             }
-            if (!mbar_wait(&full[slot], (uint32_t)round & 1u)) {
+            if (!mbar_wait_n(&full[slot], (uint32_t)round & 1u, budget)) {
                 s_flags[0] = 1;
-                set_status(p.st.status, PM_DEV_ERR_TIMEOUT);
+                timeout_abort(p.st);
                 break;
             }
             const int n = min(p.upst, u1 - (u0 + k * p.upst));

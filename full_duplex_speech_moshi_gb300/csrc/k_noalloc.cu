@@ -40,9 +40,11 @@ constexpr size_t kScratchBytes = kOffSel + 4 * (size_t)kMaxB * PM_MAX_STREAMS_DE
 }  // namespace
 }  // namespace pm
 
-#define PM_NOALLOC_MAX_B 64
+#define PM_NOALLOC_MAX_B pm::kMaxB
 #define PM_NOALLOC_SCRATCH_BYTES 10240
 static_assert(pm::kScratchBytes <= PM_NOALLOC_SCRATCH_BYTES, "scratch layout exceeds the array");
+static_assert(sizeof(pm::FrameIO) <= pm::kOffStatus - pm::kOffIo, "FrameIO overruns its slot");
+static_assert(pm::kOffStatus + 16 <= pm::kOffAmax, "status words overrun their slot");
 
 // Device scratch of the no-allocation text head.  In host code this name is only a
 // host-side stand-in; the device address comes from cudaGetSymbolAddress below.
@@ -54,6 +56,26 @@ namespace {
 // per-device address of g_noalloc_scratch, resolved once with that device current
 unsigned char* g_scratch_dev[kMaxDevices] = {};
 std::mutex g_setup_mu;
+
+// Copy the call's outcome out of the shared scratch: PM_OK, or PM_ERR_TIMEOUT when a bounded
+// wait of the head ran out (its outputs are then incomplete).
+__global__ void k_noalloc_end(const unsigned char* scratch, int32_t* status) {
+    const uint32_t st = *reinterpret_cast<const volatile uint32_t*>(scratch + kOffStatus);
+    *status = (st & PM_DEV_ERR_TIMEOUT) ? (int32_t)PM_ERR_TIMEOUT : (int32_t)PM_OK;
+}
+
+// device, managed or host-mapped memory with the given alignment (null allowed when `opt`)
+bool gpu_ptr_ok(const void* p, uintptr_t align, bool opt) {
+    if (!p) return opt;
+    if ((uintptr_t)p & (align - 1)) return false;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged ||
+           (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr);
+}
 
 // Publish the output pointers and clear the accumulators the head kernel starts from.
 __global__ void k_noalloc_begin(unsigned char* scratch, int B, float* logits, float* hidden, int32_t* token) {
@@ -100,11 +122,16 @@ pm_status setup_device(int dev, unsigned char** out) {
 
 extern "C" pm_status pm_text_head_noalloc(int B, int D, int V, const float* residual, const void* out_norm,
                                           const void* text_linear, float eps, float* hidden, float* logits,
-                                          int32_t* token, void* cuda_stream) {
+                                          int32_t* token, int32_t* status, void* cuda_stream) {
     using namespace pm;
     if (B < 1 || B > PM_NOALLOC_MAX_B) return PM_ERR_UNSUPPORTED;  // beyond the static scratch
     if (!residual || !out_norm || !text_linear || V < 1 || !(eps > 0.f)) return PM_ERR_ARG;
-    if ((((uintptr_t)residual) | ((uintptr_t)out_norm) | ((uintptr_t)text_linear)) & 15u) return PM_ERR_ARG;
+    // inputs are read with 16-byte loads; hidden is written with 16-byte stores, logits,
+    // the token and the status word with 4-byte stores
+    if (!gpu_ptr_ok(residual, 16, false) || !gpu_ptr_ok(out_norm, 16, false) || !gpu_ptr_ok(text_linear, 16, false) ||
+        !gpu_ptr_ok(hidden, 16, true) || !gpu_ptr_ok(logits, 4, true) || !gpu_ptr_ok(token, 4, true) ||
+        !gpu_ptr_ok(status, 4, true))
+        return PM_ERR_ARG;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
         cudaGetLastError();
@@ -142,6 +169,10 @@ extern "C" pm_status pm_text_head_noalloc(int B, int D, int V, const float* resi
     if (launch_gemv(PRO_RMSNORM, E_HEAD, U_ROW, p, s, false) != cudaSuccess) {
         cudaGetLastError();
         return PM_ERR_CUDA;
+    }
+    if (status) {
+        k_noalloc_end<<<1, 1, 0, s>>>(scratch, status);
+        if (cudaGetLastError() != cudaSuccess) return PM_ERR_CUDA;
     }
     return PM_OK;
 }

@@ -46,7 +46,6 @@ __global__ void __launch_bounds__(32) k_seq_prepare(const SeqPrepParams p) {
             if (id < -1 || id >= p.rows[k]) bad = 1;  // no feedback ID in a prefill
         }
     }
-    bad = __any_sync(0xffffffffu, bad);
     if (k < S) {
         const int d = p.delays[k];
         for (int t = 0; t < p.T; ++t) {
@@ -60,8 +59,15 @@ __global__ void __launch_bounds__(32) k_seq_prepare(const SeqPrepParams p) {
                 in = p.io->ids[(size_t)(src - pos0) * S + k];
             else
                 in = p.st.ring[((size_t)s * 4 + (src & 3)) * PM_MAX_STREAMS_DEV + k];
+            if (in < -1 || in >= p.rows[k]) {  // a ring entry from a corrupt restored snapshot
+                bad = 1;
+                in = -1;
+            }
             p.resolved[(size_t)t * S + k] = in;
         }
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (k < S) {
         if (!bad)
             for (int t = p.T > 4 ? p.T - 4 : 0; t < p.T; ++t)
                 p.st.ring[((size_t)s * 4 + ((pos0 + t) & 3)) * PM_MAX_STREAMS_DEV + k] = p.io->ids[(size_t)t * S + k];

@@ -92,7 +92,8 @@ struct pm_ctx {
     // persistent batch-1 frame program (null when the shape or device does not allow it)
     bool prog = false;
     FPhase* d_phases = nullptr;
-    uint32_t* prog_bar = nullptr;
+    uint32_t* prog_bar = nullptr;      // [n_phases + 2]: phase counters, exit and timeout counters
+    uint32_t* wait_budget = nullptr;   // device word: poll budget of the GEMV and frame-program waits
     size_t prog_smem = 0;
     FrameProgParams prog_params{};
     // set while pm_profile_frame records a frame eagerly
@@ -831,6 +832,20 @@ static bool is_device_ptr(const void* p) {
     return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
 }
 
+// An output the kernels write: null, or device / managed / host-mapped memory with the
+// alignment of the widest store made to it.
+static bool output_ok(const void* p, uintptr_t align) {
+    if (!p) return true;
+    if ((uintptr_t)p & (align - 1)) return false;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged ||
+           (a.type == cudaMemoryTypeHost && a.devicePointer != nullptr);
+}
+
 // ------------------------------------------------------------------------------------
 // ABI
 // ------------------------------------------------------------------------------------
@@ -953,7 +968,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
         size_t bytes;
     };
     void* p_pos; void* p_first; void* p_ring; void* p_sel; void* p_amax; void* p_hc; void* p_status;
-    void* p_damax; void* p_dcount; void* p_dcodes; void* p_dtok; void* p_dsup;
+    void* p_damax; void* p_dcount; void* p_dcodes; void* p_dtok; void* p_dsup; void* p_budget;
     void* p_io; void* p_dio; void *p_x, *p_q, *p_o, *p_s, *p_h, *p_part, *p_cnt, *p_freq, *p_dz, *p_dq,
         *p_ds, *p_dkv, *p_rtab, *p_xb, *p_ob, *p_sb, *p_ss, *p_tcp, *p_tcc, *p_scfg, *p_slog, *p_dslog,
         *p_sres, *p_apart, *p_acnt, *p_skv, *p_dzin;
@@ -1007,7 +1022,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
         {&p_pos, 4u * BM}, {&p_first, 4u * BM}, {&p_ring, 4u * BM * 4 * PM_MAX_STREAMS_DEV},
         {&p_sel, 4u * BM * PM_MAX_STREAMS_DEV}, {&p_amax, 8u * BM}, {&p_hc, 4u * BM}, {&p_status, 16u},
         {&p_damax, 8u * BM}, {&p_dcount, 4u * BM}, {&p_dcodes, 4u * BM * Q}, {&p_dtok, 4u * BM},
-        {&p_dsup, 4u * BM * Q},
+        {&p_dsup, 4u * BM * Q}, {&p_budget, 4u},
         {&p_io, 64u + 4u * RM * S}, {&p_dio, 64u + 4u * BM + 4u * BM * Q},
         {&p_x, 4u * RM * f.D}, {&p_q, 4u * RM * f.D}, {&p_o, 4u * RM * f.D}, {&p_s, 4u * RM * f.ffn},
         {&p_h, 4u * BM * f.D}, {&p_part, 4u * BM * f.H * attn_max_splits(f.ctx) * (f.dh + 2)}, {&p_cnt, 4u * BM * f.H},
@@ -1050,6 +1065,8 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     c->st.dep_codes = (int32_t*)p_dcodes;
     c->st.dep_tok = (int32_t*)p_dtok;
     c->st.dep_sup = (int32_t*)p_dsup;
+    c->st.wait_budget = (const uint32_t*)p_budget;
+    c->wait_budget = (uint32_t*)p_budget;
     c->io_region = (uint8_t*)p_io;
     c->dio_region = (uint8_t*)p_dio;
     c->x = (float*)p_x;
@@ -1084,6 +1101,10 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     std::vector<double> freq(f.dh / 2);
     for (int j = 0; j < f.dh / 2; ++j) freq[j] = exp(-log((double)f.rope_theta) * (2.0 * j) / (double)f.dh);
     if (ck(cudaMemcpy(c->rope_freq, freq.data(), 8u * freq.size(), cudaMemcpyHostToDevice)))
+        return bail(PM_ERR_CUDA, "CUDA call failed");
+    // the full poll budget of the bounded waits
+    const uint32_t budget = PM_SPIN_LIMIT;
+    if (ck(cudaMemcpy(c->wait_budget, &budget, 4u, cudaMemcpyHostToDevice)))
         return bail(PM_ERR_CUDA, "CUDA call failed");
     // no prior selection anywhere
     std::vector<int32_t> sel((size_t)BM * PM_MAX_STREAMS_DEV, -2);
@@ -1176,11 +1197,13 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
                frame_prog_occupancy(smem, &occ) == cudaSuccess && occ >= 1;
         cudaGetLastError();
         if (good) {
-            if (ck(cudaMalloc(&c->d_phases, sizeof(FPhase) * ph.size() + 4u * ph.size())))
+            // counters: one per phase, then the launch's exit and timeout counters
+            const size_t n_bar = ph.size() + 2;
+            if (ck(cudaMalloc(&c->d_phases, sizeof(FPhase) * ph.size() + 4u * n_bar)))
                 return bail(PM_ERR_OOM, "device allocation (frame program)");
             c->prog_bar = reinterpret_cast<uint32_t*>(c->d_phases + ph.size());
             if (ck(cudaMemcpy(c->d_phases, ph.data(), sizeof(FPhase) * ph.size(), cudaMemcpyHostToDevice)) ||
-                ck(cudaMemset(c->prog_bar, 0, 4u * ph.size())))
+                ck(cudaMemset(c->prog_bar, 0, 4u * n_bar)))
                 return bail(PM_ERR_CUDA, "frame program upload");
             FrameProgParams& pp = c->prog_params;
             memset(&pp, 0, sizeof pp);
@@ -1371,6 +1394,31 @@ extern "C" pm_status pm_restore(pm_ctx* c, int b, const void* src) {
     if (st3[0] < 0 || st3[1] < 0 || st3[1] > st3[0] || st3[2] != (st3[0] < f.ctx ? st3[0] : f.ctx))
         return fail(c, PM_ERR_ARG, "pm_restore: inconsistent snapshot header");
     const uint8_t* s = static_cast<const uint8_t*>(src);
+    // The delay ring and the selections become row indices of the embedding tables on the
+    // next frame: every entry a later frame can read must be a valid ID, checked here on
+    // the host before anything reaches the context.
+    {
+        int32_t ring[4 * PM_MAX_STREAMS_DEV], sel[PM_MAX_STREAMS_DEV];
+        PM_CUDA(cudaMemcpy(ring, s + kSnapRing, sizeof ring, cudaMemcpyDeviceToHost));
+        PM_CUDA(cudaMemcpy(sel, s + kSnapSel, sizeof sel, cudaMemcpyDeviceToHost));
+        const int pos = st3[0], first = st3[1];
+        for (int k = 0; k < f.n_streams; ++k) {
+            const int rows = (k == 0) ? f.text_in : f.audio_in;
+            // frames pos-3..pos-1 since the first position: the ring slots a delay of up to
+            // 3 frames reads on the next frames
+            for (int q = pos - 3; q < pos; ++q) {
+                if (q < first) continue;
+                const int32_t id = ring[(q & 3) * PM_MAX_STREAMS_DEV + k];
+                if (id < -1 || id >= rows)
+                    return fail(c, PM_ERR_ARG, "pm_restore: snapshot delay ring holds ID " + std::to_string(id) +
+                                                   " for stream " + std::to_string(k));
+            }
+            // a selection is a token the stream selected (or -2: none yet)
+            if (sel[k] < -2 || sel[k] >= rows)
+                return fail(c, PM_ERR_ARG, "pm_restore: snapshot selection " + std::to_string(sel[k]) +
+                                               " for stream " + std::to_string(k));
+        }
+    }
     PM_CUDA(cudaMemcpyAsync(c->st.pos + b, s + 64, 4, cudaMemcpyDeviceToDevice, c->stream));
     PM_CUDA(cudaMemcpyAsync(c->st.first_pos + b, s + 68, 4, cudaMemcpyDeviceToDevice, c->stream));
     PM_CUDA(cudaMemcpyAsync(c->st.ring + (size_t)b * 4 * PM_MAX_STREAMS_DEV, s + kSnapRing,
@@ -1380,6 +1428,17 @@ extern "C" pm_status pm_restore(pm_ctx* c, int b, const void* src) {
     pm_status st = snap_kv(c, b, const_cast<uint8_t*>(s), st3[2], false);
     if (st) return st;
     PM_CUDA(cudaStreamSynchronize(c->stream));
+    return PM_OK;
+}
+
+// one word of device memory, written in stream order
+__global__ void k_set_word(uint32_t* dst, uint32_t v) { *dst = v; }
+
+extern "C" pm_status pm_set_wait_budget(pm_ctx* c, uint32_t polls) {
+    if (!c) return PM_ERR_ARG;
+    PM_CUDA(cudaSetDevice(c->device));
+    k_set_word<<<1, 1, 0, c->stream>>>(c->wait_budget, polls == PM_WAIT_BUDGET_DEFAULT ? (uint32_t)PM_SPIN_LIMIT : polls);
+    PM_CUDA(cudaGetLastError());
     return PM_OK;
 }
 
@@ -1402,6 +1461,10 @@ extern "C" pm_status pm_frame_step(pm_ctx* c, int B, const int32_t* ids, float* 
     if (B < 1 || B > f.B_max) return fail(c, PM_ERR_ARG, "pm_frame_step: B outside 1..B_max");
     if (!ids) return fail(c, PM_ERR_ARG, "pm_frame_step: ids is null");
     PM_CUDA(cudaSetDevice(c->device));
+    // the head writes hidden with 16-byte stores, logits and the token with 4-byte stores
+    if (!output_ok(hidden, 16) || !output_ok(text_logits, 4) || !output_ok(text_token, 4))
+        return fail(c, PM_ERR_ARG,
+                    "pm_frame_step: an output is not device or host-mapped memory, or hidden is not 16-byte aligned");
     const int S = f.n_streams;
     const bool dev_ids = is_device_ptr(ids);
     if (!dev_ids) {

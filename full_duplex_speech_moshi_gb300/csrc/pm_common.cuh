@@ -40,6 +40,7 @@ struct DevState {
     int32_t* dep_codes;            // [B_max][dep_steps] codes selected in the frame in flight
     int32_t* dep_tok;              // [B_max] text token the depformer conditions on
     int32_t* dep_sup;              // [B_max][dep_steps] validated supplied codes (-1 = greedy)
+    const uint32_t* wait_budget;   // [1] poll budget of the waits that honour it (PM_SPIN_LIMIT unless lowered)
 };
 
 // Sampling settings of a context, device-resident so that a captured graph follows
@@ -168,6 +169,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     return false;
 }
 
+// Same with a budget read at run time (a budget of 0 gives up without polling).
+__device__ __forceinline__ bool mbar_wait_n(uint64_t* bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// The context's wait budget (PM_SPIN_LIMIT where a kernel runs without a context word).
+__device__ __forceinline__ uint32_t wait_budget(const DevState& st) {
+    return st.wait_budget ? *(const volatile uint32_t*)st.wait_budget : (uint32_t)PM_SPIN_LIMIT;
+}
+
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -185,5 +198,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 }
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bits) { atomicOr(status, bits); }
+
+// A bounded wait ran out: record it and raise the frame's abort flag, so the kernels that
+// follow in the frame skip their writes and the stream's position does not advance.
+__device__ __forceinline__ void timeout_abort(const DevState& st) {
+    set_status(st.status, PM_DEV_ERR_TIMEOUT);
+    atomicExch(&st.status[1], 1u);
+}
 
 }  // namespace pm

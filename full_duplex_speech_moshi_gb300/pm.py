@@ -23,7 +23,8 @@ STATUS_NAMES = {0: "PM_OK", 1: "PM_ERR_ARG", 2: "PM_ERR_INVALID_ID", 3: "PM_ERR_
 EXPORTS = ["pm_kv_cache_bytes", "pm_create", "pm_reset", "pm_set_positions", "pm_get_positions",
            "pm_frame_step", "pm_depformer_step", "pm_profile_frame", "pm_device_status", "pm_last_error",
            "pm_destroy", "pm_text_head_noalloc", "pm_set_sampling", "pm_sample", "pm_snapshot_bytes",
-           "pm_snapshot", "pm_restore", "pm_prefill"]
+           "pm_snapshot", "pm_restore", "pm_prefill", "pm_set_wait_budget"]
+PM_WAIT_BUDGET_DEFAULT = 0xFFFFFFFF
 KERNEL_KINDS = {0: "embed", 1: "qkv_rope", 2: "attention", 3: "out_proj", 4: "linear_in_swiglu",
                 5: "linear_out", 6: "text_head", 7: "frame_program", 8: "text_sample"}
 
@@ -91,7 +92,9 @@ def lib():
         L.pm_last_error.restype = C.c_char_p
         L.pm_last_error.argtypes = [vp]
         L.pm_text_head_noalloc.restype = C.c_int
-        L.pm_text_head_noalloc.argtypes = [C.c_int, C.c_int, C.c_int, vp, vp, vp, C.c_float, vp, vp, vp, vp]
+        L.pm_text_head_noalloc.argtypes = [C.c_int, C.c_int, C.c_int, vp, vp, vp, C.c_float, vp, vp, vp, vp, vp]
+        L.pm_set_wait_budget.restype = C.c_int
+        L.pm_set_wait_budget.argtypes = [vp, C.c_uint32]
         L.pm_set_sampling.restype = C.c_int
         L.pm_set_sampling.argtypes = [vp, C.c_float, C.c_int, C.c_float, C.c_int, C.c_ulonglong]
         L.pm_sample.restype = C.c_int
@@ -286,14 +289,19 @@ class Context:
     def device_status(self) -> int:
         return int(self.L.pm_device_status(self.h))
 
+    def set_wait_budget(self, polls: int = PM_WAIT_BUDGET_DEFAULT) -> None:
+        """Poll budget of the bounded waits (0: the next frame's waits run out at once)."""
+        self._check(self.L.pm_set_wait_budget(self.h, int(polls) & 0xFFFFFFFF))
+
 
 def pm_text_head_noalloc(B: int, D: int, V: int, residual, out_norm, text_linear, eps: float,
-                         hidden=None, logits=None, token=None, stream: int = 0) -> int:
+                         hidden=None, logits=None, token=None, status=None, stream: int = 0) -> int:
     """Final RMSNorm + text head + greedy token without a context or any device
-    allocation (scratch in a static device array; B <= 64).  Returns the pm_status."""
+    allocation (scratch in a static device array; B <= 64).  Returns the pm_status of the
+    call; `status` (int32 [1], optional) receives the device-side outcome."""
     return int(lib().pm_text_head_noalloc(int(B), int(D), int(V), _ptr(residual), _ptr(out_norm),
                                           _ptr(text_linear), float(eps), _ptr(hidden), _ptr(logits), _ptr(token),
-                                          stream or None))
+                                          _ptr(status), stream or None))
 
 
 def upload_weights(weights: Dict[str, object], device: str = "cuda") -> Dict[str, object]:

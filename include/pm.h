@@ -91,7 +91,7 @@ typedef struct {
 /* pm_config.flags: run batch-1 frames as one persistent cooperative launch (a phase
  * program with grid-wide barriers) instead of the default chain of one kernel per step.
  * Needs D and ffn multiples of 1024 and cooperative launch; otherwise the chain runs.
- * Measured on GB300 at 2.75 ms per 32-block frame against 2.51 ms for the chain. */
+ * Measured on GB300 at 2.707 ms per 32-block frame against 2.374 ms for the chain. */
 #define PM_FLAG_FRAME_PROGRAM 1u
 
 /* pm_config.flags: attention windows of the pinned ring cache ("PersonaPlex native LM
@@ -157,9 +157,12 @@ pm_status pm_get_positions(pm_ctx* ctx, int32_t* pos_out);
  *              stream at this frame (-1 none, PM_ID_FEEDBACK allowed).  Host memory is
  *              copied before the call returns.
  *  text_logits [B][text_out] fp32 device memory, or NULL.
- *  hidden      [B][D] fp32 device memory: h after the final RMSNorm, or NULL.
+ *  hidden      [B][D] fp32 device memory, 16-byte aligned: h after the final RMSNorm,
+ *              or NULL.
  *  text_token  [B] int32, device or host-mapped memory: the selected text token (greedy,
  *              or drawn after pm_set_sampling), or NULL.
+ * An output that is neither device, managed nor host-mapped memory, or a hidden pointer
+ * that is not 16-byte aligned, is PM_ERR_ARG (nothing is launched).
  * Advances each stream's position by one. */
 pm_status pm_frame_step(pm_ctx* ctx, int B, const int32_t* ids, float* text_logits, float* hidden,
                         int32_t* text_token);
@@ -257,23 +260,43 @@ pm_status pm_snapshot(pm_ctx* ctx, int stream, void* dst);
 
 /* Make stream `stream` continue exactly as the snapshotted stream would: state and KV rows
  * from `src` (device memory written by pm_snapshot of a context with the same n_layers,
- * H, dh, ctx and n_streams; PM_ERR_ARG otherwise).  The next frame is bit-identical to the
- * snapshotted stream's next frame on the same path.  Synchronises the context's stream. */
+ * H, dh, ctx and n_streams; PM_ERR_ARG otherwise).  The snapshot's delay-ring entries that
+ * later frames read and its selections are checked on the host first: an ID outside
+ * -1..rows-1 (a selection outside -2..rows-1) is PM_ERR_ARG and nothing is restored.  The
+ * next frame is bit-identical to the snapshotted stream's next frame on the same path.
+ * Synchronises the context's stream. */
 pm_status pm_restore(pm_ctx* ctx, int stream, const void* src);
 
 /* Synchronise the stream and return (and clear) any device-side error: an invalid ID
  * given in device memory (PM_ERR_INVALID_ID) or a bounded wait that ran out
- * (PM_ERR_TIMEOUT). */
+ * (PM_ERR_TIMEOUT).  A frame in which a wait ran out is abandoned like a frame with an
+ * invalid ID: its later kernels skip their writes, the position does not advance and no
+ * selection is recorded, so the next frame repeats that position. */
 pm_status pm_device_status(pm_ctx* ctx);
+
+/* Fault injection for tests of the timeout path.  Sets the poll budget of the bounded
+ * waits of the batch-1 kernel chain's projections and of the persistent frame program
+ * (their shared-memory ring waits and grid-wide phase barriers), in stream order.
+ * polls = 0 makes every such wait give up at once, so the next frame times out:
+ * pm_device_status then returns PM_ERR_TIMEOUT.  PM_WAIT_BUDGET_DEFAULT restores the
+ * normal budget.  Copies already issued by a CTA whose wait ran out are still waited for
+ * with the normal budget before it exits. */
+#define PM_WAIT_BUDGET_DEFAULT 0xFFFFFFFFu
+pm_status pm_set_wait_budget(pm_ctx* ctx, uint32_t polls);
 
 /* Final RMSNorm + text head + greedy token with no context and no device allocation.
  * The model describes no such call: this is a library entry point for callers that cannot
  * allocate device memory (code running during CUDA stream capture, real-time threads
  * that must not block on the allocator, hosts that own all device memory).
- *  residual  [B][D] fp32 device memory: the residual stream after the last block.
+ *  residual  [B][D] fp32 device memory, 16-byte aligned: the residual stream after the
+ *            last block.
  *  out_norm  bf16 [D]; text_linear bf16 [V][D] (device, 16-byte aligned).
- *  hidden    [B][D] fp32 (normalised state h) or NULL; logits [B][V] fp32 or NULL;
- *  token     [B] int32 greedy token (lowest index on ties) or NULL.
+ *  hidden    [B][D] fp32, 16-byte aligned (normalised state h) or NULL;
+ *  logits    [B][V] fp32 or NULL;
+ *  token     [B] int32 greedy token (lowest index on ties) or NULL;
+ *  status    [1] int32 or NULL: once the stream reaches the end of the call, PM_OK, or
+ *            PM_ERR_TIMEOUT if a bounded wait of the head ran out (outputs incomplete).
+ * Outputs are device, managed or host-mapped memory; anything else is PM_ERR_ARG.
  * Same arithmetic as the head of pm_frame_step.  Scratch is a 10,240-byte static device
  * array in the library, so B may be at most 64 (PM_ERR_UNSUPPORTED beyond, or if D is
  * not a multiple of 256).  The first call on each device resolves that array's address
@@ -282,7 +305,7 @@ pm_status pm_device_status(pm_ctx* ctx);
  * array: calls that overlap on the GPU race. */
 pm_status pm_text_head_noalloc(int B, int D, int V, const float* residual, const void* out_norm,
                                const void* text_linear, float eps, float* hidden, float* logits, int32_t* token,
-                               void* cuda_stream);
+                               int32_t* status, void* cuda_stream);
 
 /* Message of the last failed call on this context (empty string if none); with a NULL
  * context, the reason the last pm_create on this thread failed. */

@@ -7,6 +7,9 @@ oracle's top-2 gap exceeds 1e-2 (elsewhere both sides are fed the oracle's token
 """
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 from full_duplex_speech_moshi_gb300 import inputs as I
@@ -95,3 +98,35 @@ class Pair:
             if top2_gap(rl[b]) > GAP_MIN:
                 assert int(gt[b]) == int(rt[b]), f"{where} b={b} token {gt[b]} vs oracle {rt[b]}"
         return max(hidden_err(gh[b], rh[b]) for b in range(gh.shape[0]))
+
+
+def record_parity(name: str, **values) -> None:
+    """Append one JSON line of measured parity figures (worst errors over a run) to the
+    file named by PM_PARITY_LOG, when that variable is set; print it either way."""
+    line = json.dumps({"case": name, **values})
+    print(line)
+    path = os.environ.get("PM_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(line + "\n")
+
+
+class Worst:
+    """Running worst hidden error / logits relative L2 of a parity run, and how many greedy
+    decisions the oracle's near-tie let the two sides take differently (lockstep)."""
+
+    def __init__(self):
+        self.hidden = 0.0
+        self.logits = 0.0
+        self.frames = 0
+        self.forced = 0
+
+    def add(self, he: float, le: float) -> None:
+        self.hidden = max(self.hidden, he)
+        self.logits = max(self.logits, le)
+        self.frames += 1
+
+    def asdict(self) -> dict:
+        return {"frames": self.frames, "worst_hidden_err": self.hidden, "worst_logits_rel_l2": self.logits,
+                "near_tie_tokens_fed_from_oracle": self.forced}
+

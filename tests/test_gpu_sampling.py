@@ -158,21 +158,25 @@ def test_frame_text_sampling_batched_rows(pair):
     """B = 4 runs the tensor-core path, whose bf16 activation operands leave the logits
     too far from the oracle's for the logit bound to force most draws; the drawn tokens
     are checked against the oracle where it does, are valid picks everywhere, and equal
-    the standalone sampler applied to the frame's own logits with counter (frame
-    position, batch row, 0)."""
+    the oracle's sampler applied to the frame's own logits with counter (frame position,
+    batch row, 0) wherever that draw is not within fp32 rounding of a boundary."""
     s = pair.shape
-    torch = pair.torch
     B, T_text, k_text, seed = 4, 1.1, 40, 4242
     _frames_with_sampling(pair, B, T_text, k_text, seed, 6, 42)
     pair.ctx.reset()
     pair.ctx.set_sampling(T_text, k_text, 0.0, 1, seed)
     ids = I.make_ids(s, 6, B=B, seed=46)
-    out = torch.empty(B, dtype=torch.int32, device="cuda")
+    compared = 0
     for t in range(6):
         _, gl, gt = pair.gpu_frame(ids[t], B=B)
-        pair.ctx.sample(B, pair.logits, s.text_out, s.text_out, T_text, k_text, seed, t, 0, out)
-        torch.cuda.synchronize()
-        assert np.array_equal(out.cpu().numpy(), gt), t
+        for b in range(B):
+            tok, margin, gap = O.sample_topk(gl[b], T_text, k_text, seed, t, b, 0)
+            keep = set(np.lexsort((np.arange(gl[b].size), -gl[b]))[:k_text].tolist())
+            assert int(gt[b]) in keep, (t, b)
+            if _stable(margin, gap, 0.0, T_text):
+                assert int(gt[b]) == tok, (t, b, int(gt[b]), tok, margin)
+                compared += 1
+    assert compared >= 20
     pair.ctx.set_sampling(0.0, 1, 0.0, 1, 0)
 
 

@@ -73,3 +73,43 @@ def test_restore_rejects_foreign_and_corrupt_buffers():
     finally:
         a.close()
         c.close()
+
+
+def test_restore_rejects_invalid_ids_in_the_snapshot():
+    """A snapshot whose header is intact but whose delay ring or selections hold an ID
+    outside the embedding tables is refused on the host before any copy into the context,
+    so no kernel ever sees the bad value as a table row."""
+    s = small_shape()
+    a = Pair(s, B_max=1, depformer=False)
+    torch = a.torch
+    try:
+        ids = I.make_ids(s, 6, seed=83)[:, 0]
+        _run(a, ids)
+        snap = torch.empty(a.ctx.snapshot_bytes(), dtype=torch.uint8, device="cuda")
+        a.ctx.snapshot(0, snap)
+        # header words: the delay ring [4 slots][32 streams] at byte 128, selections at 640
+        ring_word = lambda q, k: 128 // 4 + (q & 3) * pm.PM_MAX_STREAMS + k
+        rows = lambda k: s.text_in if k == 0 else s.audio_in
+        cases = [(ring_word(5, 2), 2), (ring_word(4, 0), 0), (ring_word(3, 12), 12), (640 // 4 + 0, 0),
+                 (640 // 4 + 3, 3)]
+        for w, k in cases:
+            for value in (rows(k), rows(k) + 5, -5, 1 << 30):
+                bad = snap.clone()
+                bad.view(torch.int32)[w] = value
+                a.ctx.reset()
+                with pytest.raises(pm.PMError) as e:
+                    a.ctx.restore(0, bad)
+                assert e.value.status == pm.PM_ERR_ARG, (w, value)
+                assert a.ctx.get_positions()[0] == 0, (w, value)  # nothing restored
+        # the intact snapshot still restores and continues bit-identically
+        a.ctx.reset()
+        a.ctx.restore(0, snap)
+        more = I.make_ids(s, 3, seed=84)[:, 0]
+        cont = _run(a, more)
+        b = Pair(s, B_max=1, depformer=False, weights=a.W)
+        try:
+            _same(cont, _run(b, np.concatenate([ids, more]))[6:])
+        finally:
+            b.close()
+    finally:
+        a.close()

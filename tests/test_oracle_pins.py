@@ -434,22 +434,59 @@ def test_first_frame_attention_is_value():
     assert np.allclose(res, expect, rtol=1e-13, atol=1e-13)
 
 
-def test_loaded_history_equals_computed_history():
-    # K/V loaded as bf16 history then decoded == the same K/V reached through load (the
-    # loaded path is what the seeded long-context and batched cases use)
+def _rne_bf16(x):
+    """float64 -> bf16 bits, round to nearest even (finite values)."""
+    u = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    u = u + 0x7FFF + ((u >> 16) & 1)
+    return (u >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("H,dh", [(2, 128), (4, 64)])
+def test_loaded_history_equals_computed_history(H, dh):
+    """A stream that decodes positions 0..19 and a stream that loads the bf16-rounded K/V of
+    those positions, computed from the oracle's own steps (embedding sum -> RMSNorm ->
+    fused QKV -> RoPE of the keys at their positions), continue within bf16-rounding
+    distance of each other.  All delays are 0 so that a position's input does not depend on
+    the previous frame's IDs.  The same history loaded in the transposed layout
+    [position][head][dh] instead of [head][position][dh] misses by far more, so a layout
+    error in the load would fail here."""
+    s = I.tiny_shape(n_layers=1, H=H, dh=dh, ctx=32, delays=[0] * 17)
+    s, W, M = tiny_model(s, depformer=False)
+    T0, T1 = 20, 4
+    D = s.D
+    ids = I.make_ids(s, T0 + T1, seed=9)[:, 0]
+    a = M.new_stream()
+    ha = [a.step(ids[t])[0] for t in range(T0 + T1)]
+    K = np.zeros((H, T0, dh))
+    V = np.zeros((H, T0, dh))
+    for p in range(T0):
+        u = O.rmsnorm(M.embed(ids[p]), W["layers.0.norm1"], s.eps)
+        qkv = O.matvec(W["layers.0.in_proj"], u)
+        for h in range(H):
+            K[h, p] = O.rope(qkv[D + h * dh:D + (h + 1) * dh], p, s.rope_theta)
+            V[h, p] = qkv[2 * D + h * dh:2 * D + (h + 1) * dh]
+    Kb, Vb = _rne_bf16(K), _rne_bf16(V)
+
+    def run(k, v):
+        st = M.new_stream()
+        st.load_kv(0, 0, k, v)
+        st.set_position(T0)
+        return [st.step(ids[t])[0] for t in range(T0, T0 + T1)]
+
+    def err(hs):
+        return max(float(np.max(np.abs(h - ha[T0 + i])) / np.max(np.abs(ha[T0 + i]))) for i, h in enumerate(hs))
+
+    e_load = err(run(Kb, Vb))
+    assert 0.0 < e_load <= 1e-3, e_load          # bf16 rounding of K and V only
+    e_transposed = err(run(np.ascontiguousarray(Kb.transpose(1, 0, 2)).reshape(H, T0, dh),
+                           np.ascontiguousarray(Vb.transpose(1, 0, 2)).reshape(H, T0, dh)))
+    assert e_transposed > 100 * e_load, (e_transposed, e_load)
+
+
+def test_key_outside_the_window_changes_nothing():
     s, W, M = tiny_model(I.tiny_shape(ctx=8), depformer=False)
     ids = I.make_ids(s, 3, seed=9)[:, 0]
-    a = M.new_stream()
-    b = M.new_stream()
     k_hist = [I.make_kv_history(s, 20, seed=3, layer=l, stream=0) for l in range(s.n_layers)]
-    for st in (a, b):
-        for l in range(s.n_layers):
-            st.load_kv(l, 0, *k_hist[l])
-        st.set_position(20)
-    for t in range(3):
-        ha = a.step(ids[t])[0]
-        hb = b.step(ids[t])[0]
-        assert np.array_equal(ha, hb)
     # changing a key outside the window (position 5 < 23-8+1) changes nothing; inside does
     c = M.new_stream()
     d = M.new_stream()
