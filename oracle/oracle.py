@@ -85,6 +85,8 @@ def lib():
             L.orc_delay_assemble.argtypes = [C.c_void_p, C.c_void_p, i32p, i32p]
             L.orc_frame_step.restype = i
             L.orc_frame_step.argtypes = [C.c_void_p, C.c_void_p, i32p, dp, dp, dp, i32p]
+            L.orc_frame_forward.restype = i
+            L.orc_frame_forward.argtypes = [C.c_void_p, C.c_void_p, i32p, dp, dp, dp, i32p]
             L.orc_full_sequence.restype = i
             L.orc_full_sequence.argtypes = [C.c_void_p, i, i32p, dp, dp, i32p]
             L.orc_depformer_step.restype = i
@@ -249,6 +251,21 @@ class OracleStream:
                                    _dp(res), _dp(lg) if lg is not None else None, _i32p(am))
         if rc != ORC_OK:
             raise ValueError(f"orc_frame_step rc={rc}")
+        return hid, res, lg, int(am[0])
+
+
+    def forward(self, inputs: np.ndarray, want_logits: bool = True):
+        """One frame from already-delayed inputs (no delay assembly).  Returns (hidden [D],
+        residual [D], logits [text_out] or None, argmax)."""
+        D = self.m.shape["D"]
+        hid = np.zeros(D, np.float64)
+        res = np.zeros(D, np.float64)
+        lg = np.zeros(self.m.shape["text_out"], np.float64) if want_logits else None
+        am = np.zeros(1, np.int32)
+        rc = self.L.orc_frame_forward(self.m.h, self.h, _i32p(np.ascontiguousarray(inputs, np.int32)), _dp(hid),
+                                      _dp(res), _dp(lg) if lg is not None else None, _i32p(am))
+        if rc != ORC_OK:
+            raise ValueError(f"orc_frame_forward rc={rc}")
         return hid, res, lg, int(am[0])
 
 

@@ -529,10 +529,19 @@ static void temporal_block(const orc_model* m, orc_stream* s, int l, double* x) 
 
 int orc_frame_step(const orc_model* m, orc_stream* s, const int32_t* ids, double* hidden, double* residual,
                    double* logits, int32_t* argmax) {
-    const orc_config* c = &m->c;
     int32_t in[64];
     int rc = orc_delay_assemble(m, s, ids, in);
     if (rc != ORC_OK) return rc;
+    return orc_frame_forward(m, s, in, hidden, residual, logits, argmax);
+}
+
+/* The temporal forward of one frame from its already-delayed inputs in[n_streams] (what
+ * the generator's token ring hands the model): embedding sum, the blocks at the stream's
+ * position, final norm, text head.  The stream's ID history is not touched. */
+int orc_frame_forward(const orc_model* m, orc_stream* s, const int32_t* in, double* hidden, double* residual,
+                      double* logits, int32_t* argmax) {
+    const orc_config* c = &m->c;
+    if (orc_validate_ids(c, in) != ORC_OK) return ORC_ERR_INVALID_ID;
     double* x = (double*)malloc(sizeof(double) * (size_t)c->D);
     double* h = (double*)malloc(sizeof(double) * (size_t)c->D);
     orc_embed(m, in, x);
@@ -666,7 +675,9 @@ int orc_depformer_step_sampled(const orc_model* m, const double* hidden, int32_t
     const int J = c->dep_layers, V = c->dep_card;
     if (text_tok < 0 || text_tok >= c->dep_text_in) return ORC_ERR_INVALID_ID;
     for (int q = 0; q < Q; ++q)
-        if (supplied[q] < -1 || supplied[q] >= V) return ORC_ERR_INVALID_ID;
+        /* a supplied code is a depth input row: 0..dep_audio_in-1, which includes the initial
+         * audio ID that the generator's first model step supplies at delayed positions */
+        if (supplied[q] < -1 || supplied[q] >= c->dep_audio_in) return ORC_ERR_INVALID_ID;
 
     double* z = (double*)malloc(sizeof(double) * (size_t)Dd);
     double* u = (double*)malloc(sizeof(double) * (size_t)Dd);

@@ -73,6 +73,10 @@ int orc_delay_assemble(const orc_model* m, orc_stream* s, const int32_t* ids, in
  * residual = x before it [D] (may be NULL), logits [text_out] (may be NULL), argmax. */
 int orc_frame_step(const orc_model* m, orc_stream* s, const int32_t* ids, double* hidden, double* residual,
                    double* logits, int32_t* argmax);
+/* One frame from already-delayed inputs in[n_streams] (no delay assembly, ID history
+ * untouched); same outputs as orc_frame_step, position advanced by one. */
+int orc_frame_forward(const orc_model* m, orc_stream* s, const int32_t* in, double* hidden, double* residual,
+                      double* logits, int32_t* argmax);
 /* Frames 0..T-1 from reset, every layer evaluated over all T positions with an explicit
  * mask matrix.  ids [T][n_streams]; hidden [T][D]; logits [T][text_out]; argmax [T]. */
 int orc_full_sequence(const orc_model* m, int T, const int32_t* ids, double* hidden, double* logits,
