@@ -3,7 +3,8 @@
 // projection (k_gemv, PRO_DEPATTN).
 //
 // k_dep_begin resolves and validates the conditioning text token (caller's, or the
-// context's last greedy text token) and the supplied codes (-1 = greedy), copies the
+// context's last greedy text token) and the supplied codes (-1 = greedy; a supplied code
+// is a row of the next position's depth embedding, so 0..dep_audio_in-1), copies the
 // caller's hidden state into the buffer the chain reads, and raises the abort flag on
 // an invalid value.  Invalid values are replaced by 0 / -1 so that every later index
 // stays in range; an aborted frame writes no feedback tokens.
@@ -32,7 +33,7 @@ __global__ void __launch_bounds__(256) k_dep_begin(const DepBeginParams p) {
     }
     for (int i = threadIdx.x; i < p.B * p.Q; i += blockDim.x) {
         int sup = p.dio->supplied ? p.dio->supplied[i] : -1;
-        if (sup < -1 || sup >= p.card) {
+        if (sup < -1 || sup >= p.sup_rows) {
             bad = 1;
             sup = -1;
         }

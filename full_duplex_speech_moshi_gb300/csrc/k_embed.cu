@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(128) k_embed(const EmbedParams p) {
     const bool seq = p.resolved != nullptr;  // prefill: rows are frames of one stream
 
     int bad = 0;
+    const bool direct = !seq && p.io->direct != 0;  // inputs already delayed (generator step)
     if (seq) {
         bad = *(volatile uint32_t*)&p.st.status[1] != 0u;  // set by k_seq_prepare
     } else {
@@ -43,7 +44,7 @@ __global__ void __launch_bounds__(128) k_embed(const EmbedParams p) {
             if (id == -3) id = p.st.sel[(size_t)bb * PM_MAX_STREAMS_DEV + k];
             if (id < -1 || id >= p.rows[k]) bad = 1;
             const int src = p.st.pos[bb] - p.delays[k];
-            if (p.delays[k] != 0 && src >= p.st.first_pos[bb]) {
+            if (!direct && p.delays[k] != 0 && src >= p.st.first_pos[bb]) {
                 const int in = p.st.ring[((size_t)bb * 4 + (src & 3)) * PM_MAX_STREAMS_DEV + k];
                 if (in < -1 || in >= p.rows[k]) bad = 1;
             }
@@ -60,14 +61,14 @@ __global__ void __launch_bounds__(128) k_embed(const EmbedParams p) {
         const int pos = p.st.pos[b];
         const int src = pos - p.delays[k];
         int in;
-        if (p.delays[k] == 0)
+        if (direct || p.delays[k] == 0)
             in = id;
         else if (src >= p.st.first_pos[b])
             in = p.st.ring[((size_t)b * 4 + (src & 3)) * PM_MAX_STREAMS_DEV + k];
         else
             in = p.init_id[k];
         s_in[k] = in;
-        if (!bad && blockIdx.x == 0) p.st.ring[((size_t)b * 4 + (pos & 3)) * PM_MAX_STREAMS_DEV + k] = id;
+        if (!bad && !direct && blockIdx.x == 0) p.st.ring[((size_t)b * 4 + (pos & 3)) * PM_MAX_STREAMS_DEV + k] = id;
     }
     if (!seq && blockIdx.x == 0 && b == 0 && tid == 0) {
         p.st.status[1] = bad ? 1u : 0u;

@@ -115,13 +115,14 @@ __global__ void __launch_bounds__(NTH, 1) k_frame(const FrameProgParams p) {
         s_flag[0] = 0;  // timeout
     }
     int bad = 0;
+    const bool direct = p.io->direct != 0;  // inputs already delayed (generator step)
     if (tid < p.n_streams) {
         int id = p.io->ids[tid];
         if (id == -3) id = p.st.sel[tid];
         if (id < -1 || id >= p.rows[tid]) bad = 1;
         // a delayed stream's input comes back from the delay ring: checked the same way
         const int src = pos - p.delays[tid];
-        if (p.delays[tid] != 0 && src >= p.st.first_pos[0]) {
+        if (!direct && p.delays[tid] != 0 && src >= p.st.first_pos[0]) {
             const int in = p.st.ring[(src & 3) * PM_MAX_STREAMS_DEV + tid];
             if (in < -1 || in >= p.rows[tid]) bad = 1;
         }
@@ -262,14 +263,14 @@ __global__ void __launch_bounds__(NTH, 1) k_frame(const FrameProgParams p) {
                     if (id == -3) id = p.st.sel[k];
                     const int src = pos - p.delays[k];
                     int in;
-                    if (p.delays[k] == 0)
+                    if (direct || p.delays[k] == 0)
                         in = id;
                     else if (src >= p.st.first_pos[0])
                         in = p.st.ring[(src & 3) * PM_MAX_STREAMS_DEV + k];
                     else
                         in = p.init_id[k];
                     s_in[k] = in;
-                    if (c == 0) p.st.ring[(pos & 3) * PM_MAX_STREAMS_DEV + k] = id;
+                    if (c == 0 && !direct) p.st.ring[(pos & 3) * PM_MAX_STREAMS_DEV + k] = id;
                 }
                 if (c == 0 && tid < p.dh / 2) {
                     double sn, cs;

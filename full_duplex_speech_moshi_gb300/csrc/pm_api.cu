@@ -11,6 +11,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <string>
@@ -94,6 +95,11 @@ struct pm_ctx {
     FPhase* d_phases = nullptr;
     uint32_t* prog_bar = nullptr;      // [n_phases + 2]: phase counters, exit and timeout counters
     uint32_t* wait_budget = nullptr;   // device word: poll budget of the GEMV and frame-program waits
+    // generator (token ring + provided ring per stream, offsets; device-resident) and the host's
+    // copy of the offsets (they change only through pm_generator_step, pm_reset, pm_restore)
+    int32_t *gen_ring = nullptr, *gen_prov = nullptr, *gen_off = nullptr, *gen_in = nullptr;
+    int32_t *gen_tok = nullptr, *gen_sup = nullptr, *gen_pos_save = nullptr, *gen_sel_save = nullptr;
+    std::vector<int> gen_s;
     size_t prog_smem = 0;
     FrameProgParams prog_params{};
     // set while pm_profile_frame records a frame eagerly
@@ -159,6 +165,9 @@ static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 // ------------------------------------------------------------------------------------
 struct SetStateArgs {
     DevState st;
+    int32_t* gen_ring;  // non-null: also reset the generator (ring unwritten, no flags, offset 0)
+    int32_t* gen_prov;
+    int32_t* gen_off;
     int n;
     int32_t pos[kMaxB];
     int32_t apply[kMaxB];
@@ -176,6 +185,13 @@ __global__ void k_set_state(const SetStateArgs a) {
         a.st.dep_count[b] = 0u;
     }
     if (threadIdx.x < PM_MAX_STREAMS_DEV) a.st.sel[(size_t)b * PM_MAX_STREAMS_DEV + threadIdx.x] = -2;
+    if (a.gen_ring) {
+        for (int i = threadIdx.x; i < 4 * PM_MAX_STREAMS_DEV; i += blockDim.x) {
+            a.gen_ring[(size_t)b * 4 * PM_MAX_STREAMS_DEV + i] = -2;
+            a.gen_prov[(size_t)b * 4 * PM_MAX_STREAMS_DEV + i] = 0;
+        }
+        if (threadIdx.x == 0) a.gen_off[b] = 0;
+    }
 }
 
 // ------------------------------------------------------------------------------------
@@ -643,7 +659,7 @@ static pm_status record_depformer(pm_ctx* c, int B, cudaStream_t s) {
     bp.B = B;
     bp.D = D;
     bp.Q = Q;
-    bp.card = f.dep_card;
+    bp.sup_rows = f.dep_audio_in;
     bp.text_rows = f.dep_text_in;
     PM_CUDA(launch_dep_begin(bp, s, false));
     const size_t dl_elems = (size_t)f.B_max * f.dep_H * Q * f.dep_dh;
@@ -969,6 +985,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     };
     void* p_pos; void* p_first; void* p_ring; void* p_sel; void* p_amax; void* p_hc; void* p_status;
     void* p_damax; void* p_dcount; void* p_dcodes; void* p_dtok; void* p_dsup; void* p_budget;
+    void *p_gring, *p_gprov, *p_goff, *p_gin, *p_gtok, *p_gsup, *p_gpos, *p_gsel;
     void* p_io; void* p_dio; void *p_x, *p_q, *p_o, *p_s, *p_h, *p_part, *p_cnt, *p_freq, *p_dz, *p_dq,
         *p_ds, *p_dkv, *p_rtab, *p_xb, *p_ob, *p_sb, *p_ss, *p_tcp, *p_tcc, *p_scfg, *p_slog, *p_dslog,
         *p_sres, *p_apart, *p_acnt, *p_skv, *p_dzin;
@@ -1023,6 +1040,9 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
         {&p_sel, 4u * BM * PM_MAX_STREAMS_DEV}, {&p_amax, 8u * BM}, {&p_hc, 4u * BM}, {&p_status, 16u},
         {&p_damax, 8u * BM}, {&p_dcount, 4u * BM}, {&p_dcodes, 4u * BM * Q}, {&p_dtok, 4u * BM},
         {&p_dsup, 4u * BM * Q}, {&p_budget, 4u},
+        {&p_gring, 16u * BM * PM_MAX_STREAMS_DEV}, {&p_gprov, 16u * BM * PM_MAX_STREAMS_DEV}, {&p_goff, 4u * BM},
+        {&p_gin, 4u * BM * S}, {&p_gtok, 4u * BM}, {&p_gsup, 4u * BM * Q}, {&p_gpos, 4u * BM},
+        {&p_gsel, 4u * BM * PM_MAX_STREAMS_DEV},
         {&p_io, 64u + 4u * RM * S}, {&p_dio, 64u + 4u * BM + 4u * BM * Q},
         {&p_x, 4u * RM * f.D}, {&p_q, 4u * RM * f.D}, {&p_o, 4u * RM * f.D}, {&p_s, 4u * RM * f.ffn},
         {&p_h, 4u * BM * f.D}, {&p_part, 4u * BM * f.H * attn_max_splits(f.ctx) * (f.dh + 2)}, {&p_cnt, 4u * BM * f.H},
@@ -1067,6 +1087,15 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     c->st.dep_sup = (int32_t*)p_dsup;
     c->st.wait_budget = (const uint32_t*)p_budget;
     c->wait_budget = (uint32_t*)p_budget;
+    c->gen_ring = (int32_t*)p_gring;
+    c->gen_prov = (int32_t*)p_gprov;
+    c->gen_off = (int32_t*)p_goff;
+    c->gen_in = (int32_t*)p_gin;
+    c->gen_tok = (int32_t*)p_gtok;
+    c->gen_sup = (int32_t*)p_gsup;
+    c->gen_pos_save = (int32_t*)p_gpos;
+    c->gen_sel_save = (int32_t*)p_gsel;
+    c->gen_s.assign(BM, 0);
     c->io_region = (uint8_t*)p_io;
     c->dio_region = (uint8_t*)p_dio;
     c->x = (float*)p_x;
@@ -1106,9 +1135,10 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     const uint32_t budget = PM_SPIN_LIMIT;
     if (ck(cudaMemcpy(c->wait_budget, &budget, 4u, cudaMemcpyHostToDevice)))
         return bail(PM_ERR_CUDA, "CUDA call failed");
-    // no prior selection anywhere
-    std::vector<int32_t> sel((size_t)BM * PM_MAX_STREAMS_DEV, -2);
-    if (ck(cudaMemcpy(c->st.sel, sel.data(), 4u * sel.size(), cudaMemcpyHostToDevice)))
+    // no prior selection anywhere; every generator ring slot unwritten (-2)
+    std::vector<int32_t> sel((size_t)BM * PM_MAX_STREAMS_DEV * 4, -2);
+    if (ck(cudaMemcpy(c->st.sel, sel.data(), 4u * BM * PM_MAX_STREAMS_DEV, cudaMemcpyHostToDevice)) ||
+        ck(cudaMemcpy(c->gen_ring, sel.data(), 16u * BM * PM_MAX_STREAMS_DEV, cudaMemcpyHostToDevice)))
         return bail(PM_ERR_CUDA, "CUDA call failed");
 
     if (ck(cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking))) return bail(PM_ERR_CUDA, "cudaStreamCreateWithFlags");
@@ -1261,10 +1291,17 @@ extern "C" void pm_destroy(pm_ctx* c) {
 
 extern "C" const char* pm_last_error(const pm_ctx* c) { return c ? c->err.c_str() : g_create_err.c_str(); }
 
-static pm_status set_state(pm_ctx* c, const int32_t* pos, const int32_t* apply, int n) {
+static pm_status set_state(pm_ctx* c, const int32_t* pos, const int32_t* apply, int n, bool reset_gen) {
     SetStateArgs a;
     memset(&a, 0, sizeof a);
     a.st = c->st;
+    if (reset_gen) {
+        a.gen_ring = c->gen_ring;
+        a.gen_prov = c->gen_prov;
+        a.gen_off = c->gen_off;
+        for (int b = 0; b < n; ++b)
+            if (apply[b]) c->gen_s[b] = 0;
+    }
     a.n = n;
     for (int b = 0; b < n; ++b) {
         a.pos[b] = pos[b];
@@ -1280,7 +1317,7 @@ extern "C" pm_status pm_reset(pm_ctx* c, const int32_t* mask) {
     PM_CUDA(cudaSetDevice(c->device));
     int32_t pos[kMaxB] = {0}, apply[kMaxB];
     for (int b = 0; b < c->cfg.B_max; ++b) apply[b] = mask ? (mask[b] != 0) : 1;
-    return set_state(c, pos, apply, c->cfg.B_max);
+    return set_state(c, pos, apply, c->cfg.B_max, true);
 }
 
 extern "C" pm_status pm_set_positions(pm_ctx* c, int B, const int32_t* pos) {
@@ -1291,7 +1328,7 @@ extern "C" pm_status pm_set_positions(pm_ctx* c, int B, const int32_t* pos) {
     PM_CUDA(cudaSetDevice(c->device));
     int32_t apply[kMaxB];
     for (int b = 0; b < B; ++b) apply[b] = 1;
-    return set_state(c, pos, apply, B);
+    return set_state(c, pos, apply, B, false);
 }
 
 extern "C" pm_status pm_get_positions(pm_ctx* c, int32_t* pos_out) {
@@ -1307,17 +1344,22 @@ extern "C" pm_status pm_get_positions(pm_ctx* c, int32_t* pos_out) {
 // ------------------------------------------------------------------------------------
 namespace {
 constexpr uint32_t kSnapMagic = 0x4E534D50u;  // "PMSN"
-constexpr uint32_t kSnapVersion = 1u;
-constexpr size_t kSnapHeader = 1024;          // header bytes before the KV rows
+constexpr uint32_t kSnapVersion = 2u;
+constexpr size_t kSnapHeader = 2048;          // header bytes before the KV rows
 // header layout (bytes): [0, 64) identity and shape, 64 pos, 68 first_pos, 72 n_slots,
-// [128, 128 + 4 * 4 * PM_MAX_STREAMS_DEV) delay ring, then PM_MAX_STREAMS_DEV selections
+// 76 generator offset, [128, 128 + 4 * 4 * PM_MAX_STREAMS_DEV) delay ring, then
+// PM_MAX_STREAMS_DEV selections; [1024, 1536) the generator's token ring and [1536, 2048)
+// its provided ring ([PM_MAX_STREAMS_DEV][4] each)
 constexpr size_t kSnapRing = 128;
 constexpr size_t kSnapSel = kSnapRing + 4u * 4u * PM_MAX_STREAMS_DEV;
+constexpr size_t kSnapGenRing = 1024;
+constexpr size_t kSnapGenProv = kSnapGenRing + 16u * PM_MAX_STREAMS_DEV;
 struct SnapIdent {
     uint32_t magic, version;
     int32_t n_layers, H, dh, ctx, n_streams, D;
 };
-static_assert(kSnapSel + 4u * PM_MAX_STREAMS_DEV <= kSnapHeader, "snapshot header overflow");
+static_assert(kSnapSel + 4u * PM_MAX_STREAMS_DEV <= kSnapGenRing, "snapshot header overflow");
+static_assert(kSnapGenProv + 16u * PM_MAX_STREAMS_DEV <= kSnapHeader, "snapshot header overflow");
 }  // namespace
 
 extern "C" size_t pm_snapshot_bytes(const pm_config* f) {
@@ -1359,14 +1401,18 @@ extern "C" pm_status pm_snapshot(pm_ctx* c, int b, void* dst) {
     memset(hdr, 0, sizeof hdr);
     SnapIdent id{kSnapMagic, kSnapVersion, f.n_layers, f.H, f.dh, f.ctx, f.n_streams, f.D};
     memcpy(hdr, &id, sizeof id);
-    const int32_t st3[3] = {pf[0], pf[1], n};
-    memcpy(hdr + 64, st3, sizeof st3);
+    const int32_t st4[4] = {pf[0], pf[1], n, c->gen_s[b]};
+    memcpy(hdr + 64, st4, sizeof st4);
     uint8_t* d = static_cast<uint8_t*>(dst);
     PM_CUDA(cudaMemcpyAsync(d, hdr, sizeof hdr, cudaMemcpyHostToDevice, c->stream));
     PM_CUDA(cudaMemcpyAsync(d + kSnapRing, c->st.ring + (size_t)b * 4 * PM_MAX_STREAMS_DEV,
                             4u * 4u * PM_MAX_STREAMS_DEV, cudaMemcpyDeviceToDevice, c->stream));
     PM_CUDA(cudaMemcpyAsync(d + kSnapSel, c->st.sel + (size_t)b * PM_MAX_STREAMS_DEV, 4u * PM_MAX_STREAMS_DEV,
                             cudaMemcpyDeviceToDevice, c->stream));
+    PM_CUDA(cudaMemcpyAsync(d + kSnapGenRing, c->gen_ring + (size_t)b * 4 * PM_MAX_STREAMS_DEV,
+                            16u * PM_MAX_STREAMS_DEV, cudaMemcpyDeviceToDevice, c->stream));
+    PM_CUDA(cudaMemcpyAsync(d + kSnapGenProv, c->gen_prov + (size_t)b * 4 * PM_MAX_STREAMS_DEV,
+                            16u * PM_MAX_STREAMS_DEV, cudaMemcpyDeviceToDevice, c->stream));
     pm_status st = snap_kv(c, b, d, n, true);
     if (st) return st;
     PM_CUDA(cudaStreamSynchronize(c->stream));
@@ -1384,14 +1430,14 @@ extern "C" pm_status pm_restore(pm_ctx* c, int b, const void* src) {
     PM_CUDA(cudaMemcpy(hdr, src, sizeof hdr, cudaMemcpyDeviceToHost));
     SnapIdent id;
     memcpy(&id, hdr, sizeof id);
-    int32_t st3[3];
+    int32_t st3[4];
     memcpy(st3, hdr + 64, sizeof st3);
     if (id.magic != kSnapMagic || id.version != kSnapVersion)
         return fail(c, PM_ERR_ARG, "pm_restore: not a snapshot");
     if (id.n_layers != f.n_layers || id.H != f.H || id.dh != f.dh || id.ctx != f.ctx || id.n_streams != f.n_streams ||
         id.D != f.D)
         return fail(c, PM_ERR_ARG, "pm_restore: snapshot of another configuration");
-    if (st3[0] < 0 || st3[1] < 0 || st3[1] > st3[0] || st3[2] != (st3[0] < f.ctx ? st3[0] : f.ctx))
+    if (st3[0] < 0 || st3[1] < 0 || st3[1] > st3[0] || st3[2] != (st3[0] < f.ctx ? st3[0] : f.ctx) || st3[3] < 0)
         return fail(c, PM_ERR_ARG, "pm_restore: inconsistent snapshot header");
     const uint8_t* s = static_cast<const uint8_t*>(src);
     // The delay ring and the selections become row indices of the embedding tables on the
@@ -1418,6 +1464,19 @@ extern "C" pm_status pm_restore(pm_ctx* c, int b, const void* src) {
                 return fail(c, PM_ERR_ARG, "pm_restore: snapshot selection " + std::to_string(sel[k]) +
                                                " for stream " + std::to_string(k));
         }
+        // the generator's rings: codes -2 (unwritten) .. rows-1, flags 0 / 1
+        int32_t gring[4 * PM_MAX_STREAMS_DEV], gprov[4 * PM_MAX_STREAMS_DEV];
+        PM_CUDA(cudaMemcpy(gring, s + kSnapGenRing, sizeof gring, cudaMemcpyDeviceToHost));
+        PM_CUDA(cudaMemcpy(gprov, s + kSnapGenProv, sizeof gprov, cudaMemcpyDeviceToHost));
+        for (int k = 0; k < f.n_streams; ++k) {
+            const int rows = (k == 0) ? f.text_in : f.audio_in;
+            for (int j = 0; j < 4; ++j) {
+                const int32_t v = gring[k * 4 + j], fl = gprov[k * 4 + j];
+                if (v < -2 || v >= rows || (fl != 0 && fl != 1))
+                    return fail(c, PM_ERR_ARG, "pm_restore: snapshot generator ring holds " + std::to_string(v) +
+                                                   " for stream " + std::to_string(k));
+            }
+        }
     }
     PM_CUDA(cudaMemcpyAsync(c->st.pos + b, s + 64, 4, cudaMemcpyDeviceToDevice, c->stream));
     PM_CUDA(cudaMemcpyAsync(c->st.first_pos + b, s + 68, 4, cudaMemcpyDeviceToDevice, c->stream));
@@ -1425,6 +1484,12 @@ extern "C" pm_status pm_restore(pm_ctx* c, int b, const void* src) {
                             4u * 4u * PM_MAX_STREAMS_DEV, cudaMemcpyDeviceToDevice, c->stream));
     PM_CUDA(cudaMemcpyAsync(c->st.sel + (size_t)b * PM_MAX_STREAMS_DEV, s + kSnapSel, 4u * PM_MAX_STREAMS_DEV,
                             cudaMemcpyDeviceToDevice, c->stream));
+    PM_CUDA(cudaMemcpyAsync(c->gen_ring + (size_t)b * 4 * PM_MAX_STREAMS_DEV, s + kSnapGenRing,
+                            16u * PM_MAX_STREAMS_DEV, cudaMemcpyDeviceToDevice, c->stream));
+    PM_CUDA(cudaMemcpyAsync(c->gen_prov + (size_t)b * 4 * PM_MAX_STREAMS_DEV, s + kSnapGenProv,
+                            16u * PM_MAX_STREAMS_DEV, cudaMemcpyDeviceToDevice, c->stream));
+    PM_CUDA(cudaMemcpyAsync(c->gen_off + b, s + 76, 4, cudaMemcpyDeviceToDevice, c->stream));
+    c->gen_s[b] = st3[3];
     pm_status st = snap_kv(c, b, const_cast<uint8_t*>(s), st3[2], false);
     if (st) return st;
     PM_CUDA(cudaStreamSynchronize(c->stream));
@@ -1485,6 +1550,7 @@ extern "C" pm_status pm_frame_step(pm_ctx* c, int B, const int32_t* ids, float* 
     st = take_slot(c, &host, &ev);
     if (st) return st;
     FrameIO io;
+    memset(&io, 0, sizeof io);
     io.ids = dev_ids ? ids : reinterpret_cast<const int32_t*>(c->io_region + 64);
     io.logits = text_logits;
     io.hidden = hidden;
@@ -1565,7 +1631,7 @@ extern "C" pm_status pm_depformer_step(pm_ctx* c, int B, const float* hidden, co
                 return fail(c, PM_ERR_INVALID_ID, "pm_depformer_step: text token out of range");
     if (supplied && !dev_sup)
         for (int i = 0; i < B * Q; ++i)
-            if (supplied[i] < -1 || supplied[i] >= f.dep_card)
+            if (supplied[i] < -1 || supplied[i] >= f.dep_audio_in)
                 return fail(c, PM_ERR_INVALID_ID, "pm_depformer_step: supplied code out of range");
     cudaGraphExec_t ex;
     pm_status st = get_graph(c, c->dep_graphs, B, record_depformer, &ex);
@@ -1577,6 +1643,7 @@ extern "C" pm_status pm_depformer_step(pm_ctx* c, int B, const float* hidden, co
     uint8_t* dev_tok_buf = c->dio_region + 64;
     uint8_t* dev_sup_buf = c->dio_region + 64 + 4u * f.B_max;
     DepIO io;
+    memset(&io, 0, sizeof io);
     io.hidden = hidden ? hidden : c->h;
     io.text_tok = text_tok ? (dev_tok ? text_tok : reinterpret_cast<const int32_t*>(dev_tok_buf)) : nullptr;
     io.supplied = supplied ? (dev_sup ? supplied : reinterpret_cast<const int32_t*>(dev_sup_buf)) : nullptr;
@@ -1589,6 +1656,106 @@ extern "C" pm_status pm_depformer_step(pm_ctx* c, int B, const float* hidden, co
     PM_CUDA(cudaMemcpyAsync(c->dio_region, host, bytes, cudaMemcpyHostToDevice, c->stream));
     PM_CUDA(cudaEventRecord(ev, c->stream));
     PM_CUDA(cudaGraphLaunch(ex, c->stream));
+    return PM_OK;
+}
+
+extern "C" pm_status pm_generator_step(pm_ctx* c, int B, const int32_t* provided, int32_t* out, int32_t* out_valid,
+                                       float* text_logits, float* hidden, float* depth_logits) {
+    if (!c) return PM_ERR_ARG;
+    const pm_config& f = c->cfg;
+    if (!c->has_dep) return fail(c, PM_ERR_STATE, "pm_generator_step: context has no depformer");
+    if (f.dep_steps != f.n_streams - 1)
+        return fail(c, PM_ERR_UNSUPPORTED, "pm_generator_step: needs one depth position per audio stream");
+    if (B < 1 || B > f.B_max) return fail(c, PM_ERR_ARG, "pm_generator_step: B outside 1..B_max");
+    PM_CUDA(cudaSetDevice(c->device));
+    if (!output_ok(out, 4) || !output_ok(out_valid, 4) || !output_ok(text_logits, 4) || !output_ok(hidden, 16) ||
+        !output_ok(depth_logits, 4))
+        return fail(c, PM_ERR_ARG,
+                    "pm_generator_step: an output is not device or host-mapped memory, or hidden is not 16-byte aligned");
+    const int S = f.n_streams, Q = f.dep_steps;
+    if (provided) {
+        if (is_device_ptr(provided)) return fail(c, PM_ERR_ARG, "pm_generator_step: provided must be host memory");
+        for (int b = 0; b < B; ++b)
+            for (int k = 0; k < S; ++k) {
+                // a provided code is a temporal input and a depth input (or conditioning token)
+                const int rows = (k == 0) ? std::min(f.text_in, f.dep_text_in) : std::min(f.audio_in, f.dep_audio_in);
+                const int32_t v = provided[(size_t)b * S + k];
+                if (!(v == -1 || (v >= 0 && v < rows)))
+                    return fail(c, PM_ERR_INVALID_ID, "pm_generator_step: provided code " + std::to_string(v) +
+                                                          " at batch " + std::to_string(b) + " stream " + std::to_string(k));
+            }
+    }
+    bool run = false;  // a call where every row is at offset 0 runs no model step
+    for (int b = 0; b < B; ++b)
+        if (c->gen_s[b] > 0) run = true;
+    cudaGraphExec_t fex = nullptr, dex = nullptr;
+    if (run) {
+        pm_status st = get_graph(c, c->frame_graphs, B, B >= 2 ? record_frame_tc : record_frame, &fex);
+        if (st) return st;
+        st = get_graph(c, c->dep_graphs, B, record_depformer, &dex);
+        if (st) return st;
+    }
+    GenParams g;
+    memset(&g, 0, sizeof g);
+    g.st = c->st;
+    g.ring = c->gen_ring;
+    g.prov = c->gen_prov;
+    g.off = c->gen_off;
+    g.provided = provided ? reinterpret_cast<const int32_t*>(c->io_region + 64) : nullptr;
+    g.in = c->gen_in;
+    g.dep_tok = c->gen_tok;
+    g.dep_sup = c->gen_sup;
+    g.pos_save = c->gen_pos_save;
+    g.sel_save = c->gen_sel_save;
+    g.out = out;
+    g.valid = out_valid;
+    g.B = B;
+    g.S = S;
+    g.Q = Q;
+    for (int k = 0; k < S; ++k) {
+        g.delays[k] = f.delays[k];
+        g.init[k] = (k == 0) ? f.init_text : f.init_audio;
+        g.max_delay = std::max(g.max_delay, f.delays[k]);
+    }
+    g.ran = run ? 1 : 0;
+    // the frame's I/O block, the provided codes where a frame's host IDs go
+    uint8_t* host;
+    cudaEvent_t ev;
+    pm_status st = take_slot(c, &host, &ev);
+    if (st) return st;
+    FrameIO io;
+    memset(&io, 0, sizeof io);
+    io.ids = c->gen_in;
+    io.logits = text_logits;
+    io.hidden = hidden;
+    io.direct = 1;
+    memcpy(host, &io, sizeof io);
+    size_t bytes = 64;
+    if (provided) {
+        memcpy(host + 64, provided, 4u * B * S);
+        bytes += 4u * B * S;
+    }
+    PM_CUDA(cudaMemcpyAsync(c->io_region, host, bytes, cudaMemcpyHostToDevice, c->stream));
+    PM_CUDA(cudaEventRecord(ev, c->stream));
+    PM_CUDA(launch_gen(0, g, c->stream));
+    if (run) {
+        PM_CUDA(cudaGraphLaunch(fex, c->stream));
+        PM_CUDA(launch_gen(1, g, c->stream));
+        st = take_slot(c, &host, &ev);
+        if (st) return st;
+        DepIO dio;
+        memset(&dio, 0, sizeof dio);
+        dio.hidden = c->h;
+        dio.text_tok = c->gen_tok;
+        dio.supplied = c->gen_sup;
+        dio.logits = depth_logits;
+        memcpy(host, &dio, sizeof dio);
+        PM_CUDA(cudaMemcpyAsync(c->dio_region, host, 64, cudaMemcpyHostToDevice, c->stream));
+        PM_CUDA(cudaEventRecord(ev, c->stream));
+        PM_CUDA(cudaGraphLaunch(dex, c->stream));
+    }
+    PM_CUDA(launch_gen(2, g, c->stream));
+    for (int b = 0; b < B; ++b) c->gen_s[b] += 1;
     return PM_OK;
 }
 
@@ -1672,6 +1839,7 @@ extern "C" pm_status pm_profile_frame(pm_ctx* c, int B, const int32_t* ids, floa
     pm_status st = take_slot(c, &host, &ev);
     if (st) return st;
     FrameIO io;
+    memset(&io, 0, sizeof io);
     io.ids = dev_ids ? ids : reinterpret_cast<const int32_t*>(c->io_region + 64);
     io.logits = text_logits;
     io.hidden = hidden;

@@ -61,6 +61,8 @@ struct FrameIO {
     float* hidden;        // [B][D] or null (a prefill: its last frame's)
     int32_t* token;       // [B] or null (a prefill: its last frame's)
     int32_t seq_stream;   // a prefill: the stream whose frames the rows are
+    int32_t direct;       // 1: ids are the model's inputs as given (the generator's input column,
+                          // delays already applied): no delay assembly, delay ring untouched
 };
 
 struct DepIO {

@@ -190,9 +190,33 @@ struct DepBeginParams {
     DevState st;
     float* h_internal;     // [B][D] hidden the chain reads
     int32_t* dep_sup;      // [B][Q] validated supplied codes
-    int B, D, Q, card, text_rows;
+    int B, D, Q, sup_rows, text_rows;  // sup_rows: depth audio embedding rows (supplied codes < it)
 };
 cudaError_t launch_dep_begin(const DepBeginParams& p, cudaStream_t s, bool pdl);
+
+// ----------------------------------------------------------------------------------
+// generator step (token ring + provided ring, section 7 of the audit)
+// ----------------------------------------------------------------------------------
+struct GenParams {
+    DevState st;
+    int32_t* ring;            // [B_max][PM_MAX_STREAMS_DEV][4] codes (-2: never written)
+    int32_t* prov;            // [B_max][PM_MAX_STREAMS_DEV][4] provided flags
+    int32_t* off;             // [B_max] generator offsets
+    const int32_t* provided;  // [B][S] codes handed in (-1: none), or null
+    int32_t* in;              // [B][S] the frame's inputs
+    int32_t* dep_tok;         // [B] depth conditioning token
+    int32_t* dep_sup;         // [B][Q] provided depth targets (-1: select)
+    int32_t* pos_save;        // [B_max] position before the call's frame
+    int32_t* sel_save;        // [B_max][PM_MAX_STREAMS_DEV] selections before the call's frame
+    int32_t* out;             // [B][S] aligned output codes, or null
+    int32_t* valid;           // [B] 1 where out holds a frame, or null
+    int B, S, Q, max_delay;
+    int ran;                  // the frame and the depformer ran in this call
+    int delays[PM_MAX_STREAMS_DEV];
+    int init[PM_MAX_STREAMS_DEV];
+};
+// phase 0: steps 1-3 (before the frame), 1: depth inputs (before the depformer), 2: steps 6-7
+cudaError_t launch_gen(int phase, const GenParams& p, cudaStream_t s);
 
 
 

@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "PM_OK", 1: "PM_ERR_ARG", 2: "PM_ERR_INVALID_ID", 3: "PM_ERR_
 EXPORTS = ["pm_kv_cache_bytes", "pm_create", "pm_reset", "pm_set_positions", "pm_get_positions",
            "pm_frame_step", "pm_depformer_step", "pm_profile_frame", "pm_device_status", "pm_last_error",
            "pm_destroy", "pm_text_head_noalloc", "pm_set_sampling", "pm_sample", "pm_snapshot_bytes",
-           "pm_snapshot", "pm_restore", "pm_prefill", "pm_set_wait_budget"]
+           "pm_snapshot", "pm_restore", "pm_prefill", "pm_set_wait_budget", "pm_generator_step"]
 PM_WAIT_BUDGET_DEFAULT = 0xFFFFFFFF
 KERNEL_KINDS = {0: "embed", 1: "qkv_rope", 2: "attention", 3: "out_proj", 4: "linear_in_swiglu",
                 5: "linear_out", 6: "text_head", 7: "frame_program", 8: "text_sample"}
@@ -93,6 +93,8 @@ def lib():
         L.pm_last_error.argtypes = [vp]
         L.pm_text_head_noalloc.restype = C.c_int
         L.pm_text_head_noalloc.argtypes = [C.c_int, C.c_int, C.c_int, vp, vp, vp, C.c_float, vp, vp, vp, vp, vp]
+        L.pm_generator_step.restype = C.c_int
+        L.pm_generator_step.argtypes = [vp, C.c_int, vp, vp, vp, vp, vp, vp]
         L.pm_set_wait_budget.restype = C.c_int
         L.pm_set_wait_budget.argtypes = [vp, C.c_uint32]
         L.pm_set_sampling.restype = C.c_int
@@ -288,6 +290,15 @@ class Context:
 
     def device_status(self) -> int:
         return int(self.L.pm_device_status(self.h))
+
+    def generator_step(self, B: int, provided=None, out=None, out_valid=None, text_logits=None, hidden=None,
+                       depth_logits=None) -> None:
+        """One generator step (token ring + provided ring): aligned output codes into `out`."""
+        if provided is not None and not hasattr(provided, "data_ptr"):
+            import numpy as np
+            provided = np.ascontiguousarray(provided, dtype=np.int32)
+        self._check(self.L.pm_generator_step(self.h, int(B), _ptr(provided), _ptr(out), _ptr(out_valid),
+                                             _ptr(text_logits), _ptr(hidden), _ptr(depth_logits)))
 
     def set_wait_budget(self, polls: int = PM_WAIT_BUDGET_DEFAULT) -> None:
         """Poll budget of the bounded waits (0: the next frame's waits run out at once)."""

@@ -141,7 +141,8 @@ pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* tw, const p
                     void* kv_cache, void* cuda_stream, pm_ctx** out);
 
 /* Reset streams (host mask [B_max], nonzero = reset; NULL = all): position 0, empty
- * delay history, no prior selection.  Cache bytes are not cleared (the mask hides them). */
+ * delay history, no prior selection, generator offset 0 with empty token and provided
+ * rings.  Cache bytes are not cleared (the mask hides them). */
 pm_status pm_reset(pm_ctx* ctx, const int32_t* stream_mask);
 
 /* Set the positions of streams 0..B-1 (host array [B], each >= 0).  Used when the caller
@@ -188,11 +189,43 @@ pm_status pm_prefill(pm_ctx* ctx, int stream, int T, const int32_t* ids, float* 
  *            selected on its last frame.
  *  supplied  [B][dep_steps] int32 host or device memory, or NULL = all greedy:
  *            -1 = select (argmax, or drawn after pm_set_sampling), otherwise the code
- *            to use (0..dep_card-1).
+ *            to use (0..dep_audio_in-1: a row of the next position's depth embedding,
+ *            which includes the initial audio ID the generator supplies on its first
+ *            model step).
  *  logits    [B][dep_steps][dep_card] fp32 device memory, or NULL.
  *  codes     [B][dep_steps] int32 device or host-mapped memory, or NULL. */
 pm_status pm_depformer_step(pm_ctx* ctx, int B, const float* hidden, const int32_t* text_tok,
                             const int32_t* supplied, float* logits, int32_t* codes);
+
+/* One generator step for streams 0..B-1 ("PersonaPlex native LM audit", section 7 "One
+ * exact generator step"; its token ring [B,17,4] and provided ring of section 6).  Each
+ * stream has a generator offset s (0 after pm_reset), separate from its position.
+ *  provided     [B][n_streams] int32 host memory, or NULL: per stream the code handed in
+ *               at this call (-1 = none): the user's codebooks (streams 9..16), or forced
+ *               text / agent codes.  It is placed at ring column (s + delay[k]) mod 4 and
+ *               marked provided; a provided target replaces the selection (text: also as
+ *               the depformer's conditioning token).  Codes are 0..rows-1 of both the
+ *               temporal and the depth tables of that stream; anything else is
+ *               PM_ERR_INVALID_ID (nothing runs).
+ *  out          [B][n_streams] int32 device or host-mapped memory, or NULL: the aligned
+ *               output frame, stream k from column (s - max_delay + delay[k]) mod 4 (text
+ *               and codebook 0 selected on the previous call, delayed codebooks on this
+ *               one); -1 where out_valid is 0.
+ *  out_valid    [B] int32 or NULL: 1 once the initial delay padding is over (s > max_delay).
+ *  text_logits  [B][text_out] fp32, hidden [B][D] fp32 (16-byte aligned), depth_logits
+ *               [B][dep_steps][dep_card] fp32: this call's model outputs, or NULL.
+ * Steps per call: place the provided codes; while s <= delay[k] insert stream k's initial
+ * ID at column s mod 4 (provided); at s = 0 nothing else (a batch whose rows are all at
+ * s = 0 runs no model; rows at s = 0 in a batch that runs are restored to their position
+ * and selections afterwards); otherwise run the temporal frame on column (s - 1) mod 4 as
+ * given (no delay assembly: the ring has applied the delays) and the depformer with the
+ * provided targets, write the selections into the unprovided slots of column s mod 4,
+ * clear the provided flags of column (s - 1) mod 4, emit the aligned output, advance s.
+ * Selection follows pm_set_sampling (greedy by default).  A stream driven by this call
+ * should not also be stepped with pm_frame_step (PM_ID_FEEDBACK and the delay history
+ * are that call's mechanism).  Needs a depformer with dep_steps = n_streams - 1. */
+pm_status pm_generator_step(pm_ctx* ctx, int B, const int32_t* provided, int32_t* out, int32_t* out_valid,
+                            float* text_logits, float* hidden, float* depth_logits);
 
 /* Kernel families of a temporal frame, as reported by pm_profile_frame. */
 typedef enum {
@@ -248,8 +281,9 @@ pm_status pm_sample(pm_ctx* ctx, int B, const float* logits, int V, int ld, floa
 /* Stream snapshots (the startup voice prompt is replayed once and its state reused:
  * "PersonaPlex native LM audit", section 9, cached voice prompts restore temporal history
  * and the token ring).  A snapshot holds one stream's position, first position since
- * reset, delay history, last selections and the KV rows of every ring slot that holds a
- * position (min(position, ctx) slots).  pm_snapshot_bytes: the buffer a snapshot of this
+ * reset, delay history, last selections, the generator's offset, token ring and provided
+ * ring, and the KV rows of every ring slot that holds a position (min(position, ctx)
+ * slots).  pm_snapshot_bytes: the buffer a snapshot of this
  * configuration needs at most (header + all ctx slots). */
 size_t pm_snapshot_bytes(const pm_config* cfg);
 
@@ -262,7 +296,8 @@ pm_status pm_snapshot(pm_ctx* ctx, int stream, void* dst);
  * from `src` (device memory written by pm_snapshot of a context with the same n_layers,
  * H, dh, ctx and n_streams; PM_ERR_ARG otherwise).  The snapshot's delay-ring entries that
  * later frames read and its selections are checked on the host first: an ID outside
- * -1..rows-1 (a selection outside -2..rows-1) is PM_ERR_ARG and nothing is restored.  The
+ * -1..rows-1 (a selection outside -2..rows-1, a generator ring code outside -2..rows-1 or
+ * a provided flag other than 0 / 1) is PM_ERR_ARG and nothing is restored.  The
  * next frame is bit-identical to the snapshotted stream's next frame on the same path.
  * Synchronises the context's stream. */
 pm_status pm_restore(pm_ctx* ctx, int stream, const void* src);
