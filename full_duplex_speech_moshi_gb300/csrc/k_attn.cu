@@ -544,11 +544,16 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
             if (CS > 1) continue;  // pieces of a cluster's head meet in its leader
             float* ob = p.o + (size_t)up.b * p.D + up.h * DH;
             uint16_t* obb = p.ob ? p.ob + (size_t)up.b * p.D + up.h * DH : nullptr;
+            const size_t lo_off = (size_t)p.ob_lo_rows * p.D;
             if (seg_ci0 == 0 && up.ci == up.nc - 1) {
                 // the whole head was this CTA's
                 const float v = acc / l_run;
                 ob[t] = v;
-                if (obb) obb[t] = f32_to_bf16_rne(v);
+                if (obb) {
+                    const uint16_t hi = f32_to_bf16_rne(v);
+                    obb[t] = hi;
+                    if (lo_off) obb[lo_off + t] = bf16_lo_part(v, hi);
+                }
                 continue;
             }
             // a piece of a head cut between CTAs: deposit, the last piece to arrive merges
@@ -605,7 +610,11 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
             }
             const float v = A / L;
             ob[t] = v;
-            if (obb) obb[t] = f32_to_bf16_rne(v);
+            if (obb) {
+                const uint16_t hi = f32_to_bf16_rne(v);
+                obb[t] = hi;
+                if (lo_off) obb[lo_off + t] = bf16_lo_part(v, hi);
+            }
             if (t == 0) p.count[(size_t)up.b * p.H + up.h] = 0u;
             cons_bar();
         }
@@ -636,7 +645,11 @@ __global__ void __launch_bounds__(THREADS, 2) k_attn(const AttnParams p) {
             const int b = chd / p.H, h = chd % p.H;
             const float v = A / L;
             p.o[(size_t)b * p.D + h * DH + t] = v;
-            if (p.ob) p.ob[(size_t)b * p.D + h * DH + t] = f32_to_bf16_rne(v);
+            if (p.ob) {
+                const uint16_t hi = f32_to_bf16_rne(v);
+                p.ob[(size_t)b * p.D + h * DH + t] = hi;
+                if (p.ob_lo_rows) p.ob[((size_t)b + p.ob_lo_rows) * p.D + h * DH + t] = bf16_lo_part(v, hi);
+            }
         }
     }
     __syncthreads();

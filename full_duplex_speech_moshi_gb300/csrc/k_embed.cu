@@ -116,15 +116,20 @@ __global__ void __launch_bounds__(128) k_embed(const EmbedParams p) {
             const uint4 av = *reinterpret_cast<const uint4*>(p.alpha + col);
             const float al[8] = {bf16lo(av.x), bf16hi(av.x), bf16lo(av.y), bf16hi(av.y),
                                  bf16lo(av.z), bf16hi(av.z), bf16lo(av.w), bf16hi(av.w)};
-            uint32_t w[4];
+            uint32_t w[4], wl[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                w[e] = (uint32_t)f32_to_bf16_rne(acc[2 * e] * al[2 * e]) |
-                       ((uint32_t)f32_to_bf16_rne(acc[2 * e + 1] * al[2 * e + 1]) << 16);
+                const float v0 = acc[2 * e] * al[2 * e], v1 = acc[2 * e + 1] * al[2 * e + 1];
+                const uint16_t h0 = f32_to_bf16_rne(v0), h1 = f32_to_bf16_rne(v1);
+                w[e] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+                wl[e] = (uint32_t)bf16_lo_part(v0, h0) | ((uint32_t)bf16_lo_part(v1, h1) << 16);
                 ss = fmaf(acc[2 * e], acc[2 * e], ss);
                 ss = fmaf(acc[2 * e + 1], acc[2 * e + 1], ss);
             }
             *reinterpret_cast<uint4*>(p.xb + (size_t)b * p.D + col) = make_uint4(w[0], w[1], w[2], w[3]);
+            if (p.xb_lo_rows)
+                *reinterpret_cast<uint4*>(p.xb + ((size_t)b + p.xb_lo_rows) * p.D + col) =
+                    make_uint4(wl[0], wl[1], wl[2], wl[3]);
         }
         ss = warp_sum(ss);
         if ((tid & 31) == 0) s_ss[tid >> 5] = ss;

@@ -61,12 +61,22 @@ constexpr int PIECE = 32;               // k elements per warp piece (two MMAs)
 constexpr int PPW = KC / PIECE / CW;    // pieces per warp per chunk
 constexpr int SLOT = KC * 2;            // bytes per staged row (dense: the tensor copy's box)
 constexpr int STAGE = 16 * SLOT;        // one 16-row weight tile x one chunk
-constexpr int XST = 2;                  // activation chunks in flight
-constexpr int MAXT = PM_MG_MAX_TILES;   // 16-row tiles per CTA
+constexpr int XST = 1;                  // activation chunks in flight (operand + remainder each)
+constexpr int MAXT = PM_MG_MAX_TILES;   // 16-row tiles per CTA (text head)
+constexpr int LO = 16;                  // row of the operand buffers where the remainder plane starts
 constexpr int NPX = 16;                 // batch rows of the operand buffers
 constexpr int THREADS = 32 * (CW + 3);  // consumers, weight producer, activation producer, prologue
 
 enum RowMode { M_ROW = 0, M_ADJ = 1, M_SPLIT = 2 };
+
+// 16-row tiles a CTA holds accumulators for, per epilogue and batch width (the full shapes'
+// rows per CTA at one wave of 2 CTAs per SM: text head 7, SwiGLU 5 gate/value tile pairs,
+// fused QKV 3, W_O / linear_out 1), so registers are sized for what each projection needs.
+// At 16 columns the text head's 7 tiles and both operand planes would not fit the
+// register budget: it takes 5 and a second half wave of CTAs.
+__host__ __device__ constexpr int maxt_of(int epi, int nb) {
+    return epi == TE_HEAD ? (nb == 8 ? MAXT : 5) : (epi == TE_SWIGLU ? 5 : (epi == TE_QKV_ROPE ? 3 : 2));
+}
 
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(CW * 32) : "memory"); }
 // consumers + the prologue warp: the epilogue operands are in place
@@ -105,7 +115,9 @@ __device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uin
 template <int NB>
 struct MgLayout {
     static constexpr int NST = NB == 8 ? PM_MG_NST8 : PM_MG_NST16;
-    static constexpr int XSLOT = NB * SLOT;  // one activation chunk: NB rows x 512 elements
+    // one activation chunk: NB rows x 512 elements of the bf16 operand, then NB rows of its
+    // rounding remainder
+    static constexpr int XSLOT = 2 * NB * SLOT;
     static constexpr size_t FIXED = 128u + (size_t)NST * STAGE + (size_t)XST * XSLOT + 8u * (2 * NST + 2 * XST) +
                                     4u * NPX + 4u * NPX + 4u * 4;
 };
@@ -121,6 +133,7 @@ __global__ void __launch_bounds__(THREADS, PM_MG_CTAS_PER_SM)
     constexpr int RPU = MODE == M_ROW ? 1 : 2;
     constexpr int NST = MgLayout<NB>::NST;
     constexpr int XSLOT = MgLayout<NB>::XSLOT;
+    constexpr int MT = maxt_of(EPI, NB);
     uint8_t* ring = smem;
     uint8_t* xring = smem + (size_t)NST * STAGE;
     uint64_t* full = reinterpret_cast<uint64_t*>(xring + (size_t)XST * XSLOT);
@@ -207,6 +220,7 @@ __global__ void __launch_bounds__(THREADS, PM_MG_CTAS_PER_SM)
                 }
                 mbar_arrive_expect_tx(&xfull[slot], (uint32_t)XSLOT);
                 tma_load_3d(xring + (size_t)slot * XSLOT, &tmX, 0, 2 * ch, 0, &xfull[slot], pol);
+                tma_load_3d(xring + (size_t)slot * XSLOT + NB * SLOT, &tmX, 0, 2 * ch, LO, &xfull[slot], pol);
                 flags[3] = ch + 1;
             }
         }
@@ -298,9 +312,9 @@ __global__ void __launch_bounds__(THREADS, PM_MG_CTAS_PER_SM)
     } else {
         // ------------------------------ consumers ------------------------------
         const int g = lane >> 2, t = lane & 3;
-        float acc[MAXT][NB / 8][4];
+        float acc[MT][NB / 8][4];
 #pragma unroll
-        for (int i = 0; i < MAXT; ++i)
+        for (int i = 0; i < MT; ++i)
 #pragma unroll
             for (int nb = 0; nb < NB / 8; ++nb)
 #pragma unroll
@@ -316,15 +330,19 @@ __global__ void __launch_bounds__(THREADS, PM_MG_CTAS_PER_SM)
                 ok = false;
                 break;
             }
-            uint4 xf[PPW][NB / 8];
+            // bf16 operand (hi) and its rounding remainder (lo): hi + lo carries the fp32
+            // activation to ~16 significant bits, so the products lose no more than fp32
+            uint4 xf[PPW][NB / 8], xl[PPW][NB / 8];
             const uint32_t xa = smem_u32(xring) + (uint32_t)(xs * XSLOT + g * SLOT + (warp * PIECE + 8 * t) * 2);
 #pragma unroll
             for (int j = 0; j < PPW; ++j) {
                 const int pc = warp + CW * j;
 #pragma unroll
-                for (int nb = 0; nb < NB / 8; ++nb)
-                    xf[j][nb] = pc * PIECE < len ? lds128(xa + (uint32_t)(nb * 8 * SLOT + j * CW * PIECE * 2))
-                                                 : make_uint4(0u, 0u, 0u, 0u);
+                for (int nb = 0; nb < NB / 8; ++nb) {
+                    const uint32_t a = xa + (uint32_t)(nb * 8 * SLOT + j * CW * PIECE * 2);
+                    xf[j][nb] = pc * PIECE < len ? lds128(a) : make_uint4(0u, 0u, 0u, 0u);
+                    xl[j][nb] = pc * PIECE < len ? lds128(a + NB * SLOT) : make_uint4(0u, 0u, 0u, 0u);
+                }
             }
             // the slot is refilled by the async proxy (bulk copy): order these generic-proxy
             // reads before that write
@@ -332,7 +350,7 @@ __global__ void __launch_bounds__(THREADS, PM_MG_CTAS_PER_SM)
             __syncwarp();
             if (lane == 0) mbar_arrive(&xempty[xs]);
 #pragma unroll
-            for (int i = 0; i < MAXT; ++i) {
+            for (int i = 0; i < MT; ++i) {
                 if (i < ntiles) {
                     const int slot = k % NST;
                     if (!mbar_wait(&full[slot], (uint32_t)(k / NST) & 1u)) {
@@ -350,6 +368,8 @@ __global__ void __launch_bounds__(THREADS, PM_MG_CTAS_PER_SM)
                             for (int nb = 0; nb < NB / 8; ++nb) {
                                 mma_bf16(acc[i][nb], wa.x, wb.x, wa.y, wb.y, xf[j][nb].x, xf[j][nb].y);
                                 mma_bf16(acc[i][nb], wa.z, wb.z, wa.w, wb.w, xf[j][nb].z, xf[j][nb].w);
+                                mma_bf16(acc[i][nb], wa.x, wb.x, wa.y, wb.y, xl[j][nb].x, xl[j][nb].y);
+                                mma_bf16(acc[i][nb], wa.z, wb.z, wa.w, wb.w, xl[j][nb].z, xl[j][nb].w);
                             }
                         }
                     }
@@ -366,11 +386,11 @@ __global__ void __launch_bounds__(THREADS, PM_MG_CTAS_PER_SM)
         }
         pbar();  // every consumer is done with the ring; the prologue's operands are in place
         const bool aborted = *(volatile uint32_t*)&p.st.status[1] != 0u;
-        float* scr = reinterpret_cast<float*>(ring);  // [CW][MAXT][16 slots][16 batch]
+        float* scr = reinterpret_cast<float*>(ring);  // [CW][MT][16 slots][16 batch]
 #pragma unroll
-        for (int i = 0; i < MAXT; ++i) {
+        for (int i = 0; i < MT; ++i) {
             if (i < ntiles) {
-                float* o = scr + (size_t)(warp * MAXT + i) * 256;
+                float* o = scr + (size_t)(warp * MT + i) * 256;
 #pragma unroll
                 for (int nb = 0; nb < NB / 8; ++nb) {
                     o[g * 16 + nb * 8 + 2 * t] = acc[i][nb][0];
@@ -386,7 +406,7 @@ __global__ void __launch_bounds__(THREADS, PM_MG_CTAS_PER_SM)
             const int i = e >> 8, rem = e & 255;
             float v = 0.f;
 #pragma unroll
-            for (int w = 0; w < CW; ++w) v += scr[(size_t)(w * MAXT + i) * 256 + rem];
+            for (int w = 0; w < CW; ++w) v += scr[(size_t)(w * MT + i) * 256 + rem];
             scr[(size_t)i * 256 + rem] = v * inv[rem & 15];
         }
         cbar();
@@ -400,7 +420,12 @@ __global__ void __launch_bounds__(THREADS, PM_MG_CTAS_PER_SM)
                         const int r = u0 + q;
                         const float xo = pre[b * ps + q] + yt[(q >> 4) * 256 + (q & 15) * 16 + b];
                         p.y[(size_t)b * p.y_stride + r] = xo;
-                        if (p.yb) p.yb[(size_t)b * p.yb_stride + r] = f32_to_bf16_rne(xo * pre[NPX * ps + q]);
+                        if (p.yb) {
+                            const float v = xo * pre[NPX * ps + q];
+                            const uint16_t hi = f32_to_bf16_rne(v);
+                            p.yb[(size_t)b * p.yb_stride + r] = hi;
+                            if (p.yb_lo_rows) p.yb[((size_t)b + p.yb_lo_rows) * p.yb_stride + r] = bf16_lo_part(v, hi);
+                        }
                         ss = fmaf(xo, xo, ss);
                     }
                 }
@@ -412,7 +437,10 @@ __global__ void __launch_bounds__(THREADS, PM_MG_CTAS_PER_SM)
                 for (int q = lane; q < nu; q += 32) {
                     const float gt = yt[(q >> 3) * 256 + (q & 7) * 16 + b];
                     const float z = yt[(q >> 3) * 256 + (8 + (q & 7)) * 16 + b];
-                    p.yb[(size_t)b * p.yb_stride + u0 + q] = f32_to_bf16_rne(gt / (1.0f + expf(-gt)) * z);
+                    const float v = gt / (1.0f + expf(-gt)) * z;
+                    const uint16_t hi = f32_to_bf16_rne(v);
+                    p.yb[(size_t)b * p.yb_stride + u0 + q] = hi;
+                    if (p.yb_lo_rows) p.yb[((size_t)b + p.yb_lo_rows) * p.yb_stride + u0 + q] = bf16_lo_part(v, hi);
                 }
             }
         } else if (EPI == TE_QKV_ROPE) {
@@ -571,7 +599,7 @@ bool plan_mg(TcParams& p, int num_sms) {
     for (;;) {
         umax = (n_units + G - 1) / G;
         const long long tiles = mode == M_SPLIT ? (umax + 7) / 8 : (umax * (mode == M_ADJ ? 2 : 1) + 15) / 16;
-        if (tiles <= MAXT) break;
+        if (tiles <= maxt_of(p.epi, p.B <= 8 ? 8 : 16)) break;
         G += num_sms;
     }
     p.grid = (int)G;
@@ -598,7 +626,8 @@ bool mg_tensor_maps(const TcParams& p, const uint16_t* w, uint64_t w_rows, const
     if (!make_tmap_rows(&m[0], w, (uint64_t)p.K, w_rows, (uint32_t)tile_rows)) return false;
     if (!make_tmap_rows(&m[1], w, (uint64_t)p.K, w_rows, (uint32_t)(r0 ? r0 : tile_rows))) return false;
     if (!make_tmap_rows(&m[2], w, (uint64_t)p.K, w_rows, (uint32_t)(r1 ? r1 : tile_rows))) return false;
-    return make_tmap_rows(&m[3], xop, (uint64_t)p.K, NPX, p.B <= 8 ? 8u : 16u);
+    // the operand's rows and, LO rows further, its rounding remainder
+    return make_tmap_rows(&m[3], xop, (uint64_t)p.K, LO + NPX, p.B <= 8 ? 8u : 16u);
 }
 
 cudaError_t launch_mg(const CUtensorMap* m, const TcParams& p, cudaStream_t s, bool pdl) {

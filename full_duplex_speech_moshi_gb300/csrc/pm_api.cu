@@ -457,6 +457,11 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
     ep.rope_freq = c->rope_freq;
     ep.dh = f.dh;
     ep.xb = c->xb;
+    // 2 <= B <= 16 decode runs the batched GEMV on warp-level MMAs (k_gemv_mma), which
+    // also reads each bf16 operand's rounding remainder (rows 16..31 of the operand buffers)
+    const bool mg = !seq && npad == 16;
+    const int lo_rows = mg ? 16 : 0;
+    ep.xb_lo_rows = lo_rows;
     ep.alpha = c->norm1[0];
     ep.ss = c->ss;
     ep.npad = npad;
@@ -495,9 +500,8 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         PM_CUDA(launch_tc(A, X, N, p, s, pdl));
         return mark(c, s, kind);
     };
-    // 2 <= B <= 16 decode: the batched GEMV on warp-level MMAs (k_gemv_mma); its residual
-    // epilogues leave one sum-of-squares partial per CTA instead of one per 128-row tile
-    const bool mg = !seq && npad == 16;
+    // the batched GEMV's residual epilogues leave one sum-of-squares partial per CTA instead
+    // of one per 128-row tile
     int ss_parts = (D + 1023) / 1024;  // partials of the operand the next normed projection reads
     auto go_mg = [&](TcParams& p, const uint16_t* w, uint64_t w_rows, const uint16_t* xop, int kind,
                      const char* what) -> pm_status {
@@ -572,6 +576,7 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         AttnParams ap;
         memset(&ap, 0, sizeof ap);
         ap.ob = c->ob;
+        ap.ob_lo_rows = lo_rows;
         ap.q = c->q;
         ap.kc = kc;
         ap.vc = vc;
@@ -595,6 +600,7 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         p.y_stride = D;
         p.yb = c->xb;
         p.yb_stride = D;
+        p.yb_lo_rows = lo_rows;
         p.alpha_next = c->norm2[l];
         p.ss_out = c->ss;
         p.nx = next_tc(c, TE_SWIGLU, D, F / 64, F, npad);
@@ -609,6 +615,7 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         p.split_rows = F;
         p.yb = c->sb;
         p.yb_stride = F;
+        p.yb_lo_rows = lo_rows;
         p.nx = next_tc(c, TE_RESIDUAL, F, D / 128, 0, npad);
         ps = mg ? go_mg(p, c->lin_in[l], 2u * F, c->xb, PM_KERNEL_LINEAR_IN, "linear_in")
                 : go(mwi[l], mx, mwt[l], p, PM_KERNEL_LINEAR_IN, "linear_in");
@@ -619,6 +626,7 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
         p.y_stride = D;
         p.yb = c->xb;
         p.yb_stride = D;
+        p.yb_lo_rows = lo_rows;
         p.alpha_next = (l + 1 < f.n_layers) ? c->norm1[l + 1] : c->out_norm;
         p.ss_out = c->ss;
         const bool last = l + 1 == f.n_layers;

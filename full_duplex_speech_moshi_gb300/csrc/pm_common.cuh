@@ -86,6 +86,11 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rne(float f) {
     return (uint16_t)(u >> 16);
 }
 
+// bf16 pair (hi, lo) with hi + lo = f to about 16 significant bits: hi = RNE(f), lo = RNE(f - hi)
+__device__ __forceinline__ uint16_t bf16_lo_part(float f, uint16_t hi) {
+    return f32_to_bf16_rne(f - __uint_as_float((uint32_t)hi << 16));
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

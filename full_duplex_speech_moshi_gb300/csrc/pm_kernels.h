@@ -113,6 +113,7 @@ struct EmbedParams {
     const int32_t* resolved;  // [B][n_streams]
     // tensor-core path (B >= 2): bf16(alpha * x) operand [npad][D] and per-CTA sums of x^2
     uint16_t* xb;
+    int xb_lo_rows;  // > 0: also the rounding remainder of the operand at row b + xb_lo_rows
     const uint16_t* alpha;
     float* ss;       // [D/1024][npad]
     int npad;
@@ -124,6 +125,7 @@ cudaError_t launch_embed(const EmbedParams& p, cudaStream_t s, bool pdl);
 // ----------------------------------------------------------------------------------
 struct AttnParams {
     uint16_t* ob;          // [npad][D] bf16 copy of o for the tensor-core W_O, or null
+    int ob_lo_rows;        // > 0: also the rounding remainder bf16(o - ob) at row b + ob_lo_rows
     const float* q;        // [B][D] rotated queries
     const uint16_t* kc;    // [B_max][H][ctx][dh]
     const uint16_t* vc;
@@ -301,6 +303,7 @@ struct TcParams {
     int y_stride;
     uint16_t* yb;            // bf16 [npad][yb_stride] operand of the next projection, or null
     int yb_stride;
+    int yb_lo_rows;          // > 0: also its rounding remainder at row b + yb_lo_rows (batched GEMV)
     const uint16_t* alpha_next;  // TE_RESIDUAL: scale folded into yb (next RMSNorm's alpha)
     float* ss_out;           // TE_RESIDUAL: [n_mtiles][npad] per-tile sum of squares of y
     // stream-K partials and per-tile completion counters (zero between launches)
