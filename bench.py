@@ -34,6 +34,12 @@ import numpy as np  # noqa: E402
 from full_duplex_speech_moshi_gb300 import inputs as I  # noqa: E402
 
 METRIC = "temporal frames/s (B=1, 32-block stack, greedy text feedback)"
+# depformer weight bytes per call: 16 positions x (input projection [1024,4096] + 6 blocks of
+# QKV [3072,1024], W_o [1024,1024], linear_in [5632,1024], linear_out [1024,2816] + head
+# [2048,1024]), bf16
+DEP_BYTES = 2 * 16 * (1024 * 4096 + 6 * (3072 + 1024 + 5632 + 2816) * 1024 + 2048 * 1024)
+WORKLOAD = ("32-block temporal stack (D 4096, 32x128 heads, SwiGLU 11264, ctx 3000, text head 32000), B=1, "
+            "256 primed frames then greedy text feedback")
 
 
 def max_over_ranks(x: float, dist=None, device: str = "cpu") -> float:
@@ -122,7 +128,10 @@ class ClockSampler:
 
 
 def run_reference(args):
-    """The float64 CPU oracle on the same workload unit (one frame per step)."""
+    """The float64 CPU oracle on the GPU arm's workload: the same 32-block B=1 stack primed
+    with the same number of frames from reset (untimed), then warm-up frames and the timed
+    frames with greedy text feedback -- so the timed frames attend over the same context
+    lengths as the GPU arm's."""
     from oracle import oracle as O
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -132,15 +141,18 @@ def run_reference(args):
     W = I.make_weights(s, depformer=False)
     M = O.Oracle(s.asdict(), [W[n] for n, _, _ in I.tensor_specs(s, False)], depformer=False)
     st = M.new_stream()
-    ids = I.make_ids(s, args.warmup + args.steps, seed=2000)[:, 0]
+    PR = args.prime
+    ids = I.make_ids(s, PR + args.warmup + args.steps, seed=2000)[:, 0]
     prev = None
-    for t in range(args.warmup):
-        _, _, _, prev = st.step(ids[t])
-    t1 = time.time()
-    for t in range(args.warmup, args.warmup + args.steps):
+    for t in range(PR + args.warmup):
         x = ids[t].copy()
-        if prev is not None:
+        if t >= PR and prev is not None:
             x[0] = prev
+        _, _, _, prev = st.step(x)
+    t1 = time.time()
+    for t in range(PR + args.warmup, PR + args.warmup + args.steps):
+        x = ids[t].copy()
+        x[0] = prev
         _, _, _, prev = st.step(x)
     dt = time.time() - t1
     fps = args.steps / dt
@@ -149,11 +161,12 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": fps, "unit": "frames/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * dt / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "32-block temporal stack, B=1, frames from reset with greedy text feedback",
-                   "global_batch": 1, "seq_len": args.warmup + args.steps, "parallelism": "replicas"},
+        "config": {"workload": WORKLOAD, "global_batch": 1, "seq_len": PR + args.warmup + args.steps,
+                   "parallelism": "replicas"},
         "cpu_baseline": {"value": fps, "unit": "frames/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{args.steps} frames after {args.warmup} warm-up frames from reset "
-                                   f"(setup {t1 - t0:.0f} s not timed)"},
+                         "sample": f"{args.steps} frames at positions {PR + args.warmup}.."
+                                   f"{PR + args.warmup + args.steps - 1} after {PR} primed and {args.warmup} "
+                                   f"warm-up frames from reset (set-up and priming {t1 - t0:.0f} s not timed)"},
         "e2e": {"value": fps, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -161,13 +174,14 @@ def run_reference(args):
 
 def cpu_baseline_sample(budget_s: float = 15.0, max_frames: int = 64):
     """The oracle as it stands on the host cores: consecutive frames of the 32-block B=1
-    stack from reset until about `budget_s` seconds of CPU work."""
+    stack from reset until about `budget_s` seconds of CPU work, then one more frame on a
+    single thread."""
     from oracle import oracle as O
     s = I.FULL
     W = I.make_weights(s, depformer=False)
     M = O.Oracle(s.asdict(), [W[n] for n, _, _ in I.tensor_specs(s, False)], depformer=False)
     st = M.new_stream()
-    ids = I.make_ids(s, max_frames + 1, seed=2000)[:, 0]
+    ids = I.make_ids(s, max_frames + 2, seed=2000)[:, 0]
     st.step(ids[0])
     t0 = time.time()
     n = 0
@@ -175,9 +189,16 @@ def cpu_baseline_sample(budget_s: float = 15.0, max_frames: int = 64):
         n += 1
         st.step(ids[n])
     dt = time.time() - t0
+    prev = O.set_threads(1)
+    t1 = time.time()
+    st.step(ids[n + 1])
+    dt1 = time.time() - t1
+    O.set_threads(prev)
     return {"value": n / dt, "unit": "frames/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{n} frames (positions 1..{n}) of the 32-block B=1 stack, float64, OpenMP over all "
-                      f"host cores, {dt:.1f} s"}
+                      f"host cores, {dt:.1f} s",
+            "one_thread": {"value": 1.0 / dt1, "unit": "frames/s", "cores": 1,
+                           "sample": f"frame at position {n + 1}, one OpenMP thread, {dt1:.1f} s"}}
 
 
 def run_case(args):
@@ -420,6 +441,24 @@ def main():
         torch.cuda.synchronize()
         extras["with_depformer_frames_per_s"] = f4
         extras["depformer_ms"] = a2.elapsed_time(b2) / n4
+        extras["depformer_gbs"] = DEP_BYTES / (extras["depformer_ms"] / 1000.0) / 1e9
+        # the same calls through the chain of one kernel per projection, for comparison
+        kvc = pm.alloc_kv_cache(pm.make_config(s.asdict(), 1, True, pm.PM_FLAG_DEPFORMER_CHAIN))
+        ctxc = pm.Context(s.asdict(), W, kvc, B_max=1, depformer=True, stream=stream.cuda_stream,
+                          flags=pm.PM_FLAG_DEPFORMER_CHAIN)
+        ctxc.frame_step(1, ids_d[PR], logits, hidden, token)
+        for t in range(4):
+            ctxc.depformer_step(1, None, None, sup[t], dl, dc)
+        torch.cuda.synchronize()
+        a3, b3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a3.record(stream)
+        for t in range(n4):
+            ctxc.depformer_step(1, None, None, sup[t % 64], dl, dc)
+        b3.record(stream)
+        torch.cuda.synchronize()
+        extras["depformer_chain_ms"] = a3.elapsed_time(b3) / n4
+        ctxc.close()
+        del kvc
         # the released sampling defaults (text 0.7 / top-k 25, audio 0.8 / top-k 250)
         ctx.set_sampling(0.7, 25, 0.8, 250, 20251)
         for t in range(4):
@@ -540,8 +579,7 @@ def main():
             "metric": metric, "value": fps, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random-init bf16 weights, seeded IDs)",
-            "config": {"workload": "32-block temporal stack (D 4096, 32x128 heads, SwiGLU 11264, ctx 3000, "
-                                   "text head 32000), B=1, 256 primed frames then greedy text feedback",
+            "config": {"workload": WORKLOAD if BB == 1 else WORKLOAD.replace("B=1", f"B={BB}"),
                        "global_batch": world * BB, "seq_len": p0 + args.steps, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2: 13.4 GB of weights streamed per frame",
                        "frame_bytes": bytes_per_frame, "frame_gbs": frame_gbs,

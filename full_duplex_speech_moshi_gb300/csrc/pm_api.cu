@@ -100,6 +100,11 @@ struct pm_ctx {
     int32_t *gen_ring = nullptr, *gen_prov = nullptr, *gen_off = nullptr, *gen_in = nullptr;
     int32_t *gen_tok = nullptr, *gen_sup = nullptr, *gen_pos_save = nullptr, *gen_sel_save = nullptr;
     std::vector<int> gen_s;
+    // persistent batch-1 depformer (null when the shape, the device or the flags exclude it)
+    bool dep_fused = false;
+    void* df_block = nullptr;          // re-laid W_o / linear_out copies and the call's scratch
+    DepFusedParams df{};
+    size_t df_smem = 0;
     size_t prog_smem = 0;
     FrameProgParams prog_params{};
     // set while pm_profile_frame records a frame eagerly
@@ -658,6 +663,11 @@ static pm_status record_prefill(pm_ctx* c, int T, cudaStream_t s) { return recor
 static pm_status record_depformer(pm_ctx* c, int B, cudaStream_t s) {
     const pm_config& f = c->cfg;
     const int D = f.D, Dd = f.dep_D, Fd = f.dep_ffn, Q = f.dep_steps;
+    if (B == 1 && c->dep_fused && !c->audio_smp) {
+        // batch 1, selection by argmax or supplied codes: the whole call as one launch
+        PM_CUDA(launch_depth_fused(c->df, c->df_smem, s));
+        return PM_OK;
+    }
     DepBeginParams bp;
     memset(&bp, 0, sizeof bp);
     bp.dio = reinterpret_cast<const DepIO*>(c->dio_region);
@@ -886,6 +896,7 @@ static void free_ctx(pm_ctx* c) {
     if (c->cap) cudaStreamDestroy(c->cap);
     if (c->block) cudaFree(c->block);
     if (c->d_phases) cudaFree(c->d_phases);
+    if (c->df_block) cudaFree(c->df_block);
     delete c;
 }
 
@@ -1277,6 +1288,79 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
             pp.bar = c->prog_bar;
             c->prog_smem = smem;
             c->prog = true;
+        }
+    }
+    // persistent batch-1 depformer: one cooperative launch of H clusters of 4 CTAs, its own
+    // re-laid copies of W_o (head blocks) and linear_out (transposed)
+    if (c->has_dep && !(f.flags & PM_FLAG_DEPFORMER_CHAIN) && f.dep_steps <= PM_DF_MAX_Q &&
+        f.dep_layers <= PM_DF_MAX_J &&
+        depth_fused_supported(f.D, f.dep_D, f.dep_H, f.dep_dh, f.dep_ffn, f.dep_steps, f.dep_card, c->num_sms)) {
+        int coop = 0, nclu = 0;
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device);
+        const size_t smem = depth_fused_smem();
+        const int G = 4 * f.dep_H;
+        const bool fits = coop && depth_fused_prepare(smem) == cudaSuccess &&
+                          depth_fused_max_clusters(smem, G, &nclu) == cudaSuccess && nclu >= f.dep_H;
+        cudaGetLastError();
+        if (fits) {
+            const int J = f.dep_layers, Qd = f.dep_steps;
+            const size_t wo_elems = (size_t)J * Qd * Dd * Dd, wt_elems = (size_t)J * Qd * Fd * Dd;
+            const size_t sc_bytes = 4u * ((size_t)Qd * Dd + 2u * f.dep_H * Dd) + 8u * Qd + 16u;
+            if (ck(cudaMalloc(&c->df_block, 2u * (wo_elems + wt_elems) + sc_bytes + 256)))
+                return bail(PM_ERR_OOM, "device allocation (depformer copies)");
+            if (ck(cudaMemset(c->df_block, 0, 2u * (wo_elems + wt_elems) + sc_bytes + 256)))
+                return bail(PM_ERR_CUDA, "cudaMemset");
+            uint16_t* wo = static_cast<uint16_t*>(c->df_block);
+            uint16_t* wt = wo + wo_elems;
+            uint8_t* scr = reinterpret_cast<uint8_t*>(wt + wt_elems);
+            for (int j = 0; j < J; ++j)
+                for (int q = 0; q < Qd; ++q)
+                    if (ck(depth_relayout(c->d_o[j] + (size_t)q * Dd * Dd, wo + ((size_t)j * Qd + q) * Dd * Dd,
+                                          c->d_lin_out[(size_t)j * Qd + q], wt + ((size_t)j * Qd + q) * Fd * Dd, Dd,
+                                          Fd, f.dep_H, 0)))
+                        return bail(PM_ERR_CUDA, "depformer weight re-layout");
+            DepFusedParams& d = c->df;
+            memset(&d, 0, sizeof d);
+            d.st = c->st;
+            d.dio = reinterpret_cast<const DepIO*>(c->dio_region);
+            for (int q = 0; q < Qd; ++q) {
+                d.dep_in[q] = c->d_in[q];
+                d.heads[q] = c->d_heads[q];
+                if (q > 0) d.aemb[q - 1] = c->d_aemb[q - 1];
+            }
+            d.temb = c->d_temb;
+            const size_t dl_elems = (size_t)f.B_max * f.dep_H * Qd * f.dep_dh;
+            for (int j = 0; j < J; ++j) {
+                d.norm1[j] = c->d_norm1[j];
+                d.norm2[j] = c->d_norm2[j];
+                d.qkv[j] = c->d_qkv[j];
+                for (int q = 0; q < Qd; ++q) d.lin_in[j * Qd + q] = c->d_lin_in[(size_t)j * Qd + q];
+                d.dk[j] = c->dkv + (size_t)(2 * j + 0) * dl_elems;
+                d.dv[j] = c->dkv + (size_t)(2 * j + 1) * dl_elems;
+            }
+            d.wo_packed = wo;
+            d.wout_t = wt;
+            d.dzin = reinterpret_cast<float*>(scr);
+            d.part_att = d.dzin + (size_t)Qd * Dd;
+            d.part_ffn = d.part_att + (size_t)f.dep_H * Dd;
+            d.amax = reinterpret_cast<unsigned long long*>(d.part_ffn + (size_t)f.dep_H * Dd);
+            d.bar = reinterpret_cast<uint32_t*>(d.amax + Qd);
+            d.G = G;
+            d.D = f.D;
+            d.Dd = Dd;
+            d.H = f.dep_H;
+            d.Fd = Fd;
+            d.Q = Qd;
+            d.J = J;
+            d.card = f.dep_card;
+            d.n_streams = f.n_streams;
+            d.text_rows = f.dep_text_in;
+            d.sup_rows = f.dep_audio_in;
+            d.dep_win = f.dep_ctx - ((f.flags & PM_FLAG_PINNED_RING) ? 1 : 0);
+            d.eps = f.eps;
+            d.scale_log2 = (float)(1.4426950408889634 / sqrt((double)f.dep_dh));
+            c->df_smem = smem;
+            c->dep_fused = true;
         }
     }
     if (ck(gemv_prepare())) return bail(PM_ERR_CUDA, "gemv_prepare()");

@@ -220,6 +220,44 @@ struct GenParams {
 // phase 0: steps 1-3 (before the frame), 1: depth inputs (before the depformer), 2: steps 6-7
 cudaError_t launch_gen(int phase, const GenParams& p, cudaStream_t s);
 
+// ----------------------------------------------------------------------------------
+// depformer call for batch 1 as one persistent launch (clusters of 4 CTAs per depth head)
+// ----------------------------------------------------------------------------------
+#define PM_DF_MAX_Q 16
+#define PM_DF_MAX_J 8
+struct DepFusedParams {
+    DevState st;
+    const DepIO* dio;
+    const uint16_t* dep_in[PM_DF_MAX_Q];           // [Dd][D] per position
+    const uint16_t* temb;                           // [dep_text_in][Dd]
+    const uint16_t* aemb[PM_DF_MAX_Q];              // [dep_audio_in][Dd] per position 1..Q-1
+    const uint16_t* norm1[PM_DF_MAX_J];
+    const uint16_t* norm2[PM_DF_MAX_J];
+    const uint16_t* qkv[PM_DF_MAX_J];               // [Q * 3 * Dd][Dd]
+    const uint16_t* lin_in[PM_DF_MAX_J * PM_DF_MAX_Q];  // [2 * Fd][Dd], index j * Q + q
+    const uint16_t* heads[PM_DF_MAX_Q];             // [card][Dd]
+    const uint16_t* wo_packed;                      // [J][Q][H][4][Dd / 4][64]
+    const uint16_t* wout_t;                         // [J][Q][Fd][Dd]
+    uint16_t* dk[PM_DF_MAX_J];                      // depth cache of block j, batch row 0: [H][Q][64]
+    uint16_t* dv[PM_DF_MAX_J];
+    float* dzin;                                    // [Q][Dd] input projections
+    float* part_att;                                // [H][Dd]
+    float* part_ffn;                                // [H][Dd]
+    unsigned long long* amax;                       // [Q]
+    uint32_t* bar;                                  // [3]: arrivals, exits, timeouts
+    int G, D, Dd, H, Fd, Q, J, card, n_streams, text_rows, sup_rows, dep_win;
+    float eps, scale_log2;
+};
+size_t depth_fused_smem();
+bool depth_fused_supported(int D, int Dd, int H, int dh, int Fd, int Q, int card, int G_sms);
+cudaError_t depth_fused_prepare(size_t smem);
+cudaError_t depth_fused_max_clusters(size_t smem, int G, int* n);
+cudaError_t launch_depth_fused(const DepFusedParams& p, size_t smem, cudaStream_t s);
+// one (block, position): W_o slice [Dd][Dd] into the packed head blocks, linear_out [Dd][Fd]
+// into its transpose
+cudaError_t depth_relayout(const uint16_t* wo_q, uint16_t* wo_dst, const uint16_t* wout_q, uint16_t* woutT_dst, int Dd,
+                           int Fd, int H, cudaStream_t s);
+
 
 
 // ----------------------------------------------------------------------------------

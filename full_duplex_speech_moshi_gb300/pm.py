@@ -40,6 +40,7 @@ class pm_config(C.Structure):
 
 PM_FLAG_FRAME_PROGRAM = 1
 PM_FLAG_PINNED_RING = 2
+PM_FLAG_DEPFORMER_CHAIN = 4
 
 
 _PP = C.POINTER(C.c_void_p)

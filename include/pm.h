@@ -101,6 +101,15 @@ typedef struct {
  * Off by default (the declared mask).  Needs ctx >= 2 and dep_ctx >= 2. */
 #define PM_FLAG_PINNED_RING 2u
 
+/* pm_config.flags: run batch-1 depformer calls as a chain of one kernel per projection
+ * instead of the default persistent launch (clusters of 4 CTAs per depth head, grid-wide
+ * barriers between its phases).  The persistent launch keeps re-laid copies of the
+ * depformer's W_o (per-head blocks) and linear_out (transposed), made in pm_create from
+ * the weights as they are then (2 * J * Q * (dep_D^2 + dep_ffn * dep_D) bytes: 754 MB at
+ * the full shape); it needs dep_dh = 64, dep_D = 64 * dep_H <= 1024, cooperative launch and
+ * room for dep_H clusters, and is not used while depth codes are sampled or for B > 1. */
+#define PM_FLAG_DEPFORMER_CHAIN 4u
+
 /* Temporal weights: device pointers.  Per-layer members point to host arrays of
  * n_layers device pointers (copied by pm_create). */
 typedef struct {

@@ -85,6 +85,8 @@ def lib():
             L.orc_delay_assemble.argtypes = [C.c_void_p, C.c_void_p, i32p, i32p]
             L.orc_frame_step.restype = i
             L.orc_frame_step.argtypes = [C.c_void_p, C.c_void_p, i32p, dp, dp, dp, i32p]
+            L.orc_set_threads.restype = i
+            L.orc_set_threads.argtypes = [i]
             L.orc_frame_forward.restype = i
             L.orc_frame_forward.argtypes = [C.c_void_p, C.c_void_p, i32p, dp, dp, dp, i32p]
             L.orc_full_sequence.restype = i
@@ -305,6 +307,11 @@ def attend(q: np.ndarray, keys: np.ndarray, vals: np.ndarray) -> np.ndarray:
     o = np.zeros(dh, np.float64)
     lib().orc_attend(_dp(q), kp, vp, n, dh, _dp(o))
     return o
+
+
+def set_threads(n: int) -> int:
+    """Threads of the oracle's OpenMP loops from now on; returns the previous count."""
+    return int(lib().orc_set_threads(int(n)))
 
 
 def argmax(v: np.ndarray) -> int:

@@ -54,6 +54,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #include "pm_oracle.h"
 
@@ -740,3 +743,17 @@ int orc_depformer_step_sampled(const orc_model* m, const double* hidden, int32_t
     free(kp); free(vp); free(dvis);
     return ORC_OK;
 }
+
+/* Threads of the OpenMP row loops from now on (n >= 1); returns the previous count.  Used to
+ * time the oracle on one core beside all of them; no arithmetic depends on it. */
+int orc_set_threads(int n) {
+#ifdef _OPENMP
+    const int prev = omp_get_max_threads();
+    if (n >= 1) omp_set_num_threads(n);
+    return prev;
+#else
+    (void)n;
+    return 1;
+#endif
+}
+

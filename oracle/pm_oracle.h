@@ -107,6 +107,9 @@ int orc_depformer_step_sampled(const orc_model* m, const double* hidden, int32_t
                                const orc_sampling* smp, uint64_t pos, uint64_t row, double* logits, int32_t* codes,
                                double* margins);
 
+/* threads of the OpenMP row loops from now on (n >= 1); returns the previous count */
+int orc_set_threads(int n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -41,3 +41,40 @@ def test_wait_timeout_abandons_the_frame_and_recovers(program):
         assert p.ctx.get_positions()[0] == 14
     finally:
         p.close()
+
+
+def test_wait_timeout_in_the_persistent_depformer():
+    """The batch-1 depformer launch with a zero poll budget: PM_ERR_TIMEOUT, no feedback
+    codes recorded; with the budget restored the next call matches the oracle."""
+    from full_duplex_speech_moshi_gb300 import pm
+    from harness import logits_rel_l2
+    s = small_shape()
+    p = Pair(s, B_max=1)
+    try:
+        ids = I.make_ids(s, 2, seed=43)[:, 0]
+        st = p.streams[0]
+        rh, _, _, rt = st.step(ids[0])
+        p.gpu_frame(ids[0:1])
+        sup = np.full((1, s.dep_steps), -1, np.int32)
+        p.ctx.set_wait_budget(0)
+        p.dcodes.fill_(-7)
+        p.ctx.depformer_step(1, hidden=p.hidden, text_tok=np.array([int(rt)], np.int32), supplied=sup,
+                             logits=p.dlogits, codes=p.dcodes)
+        assert p.ctx.device_status() == pm.PM_ERR_TIMEOUT
+        p.ctx.set_wait_budget()
+        ol, oc = p.orc.depformer_step(rh, int(rt), oc_sup := oc_supplied(s))
+        p.ctx.depformer_step(1, hidden=p.hidden, text_tok=np.array([int(rt)], np.int32), supplied=oc_sup[None],
+                             logits=p.dlogits, codes=p.dcodes)
+        assert p.ctx.device_status() == pm.PM_OK
+        gl = p.dlogits[0].double().cpu().numpy()
+        for q in range(s.dep_steps):
+            assert logits_rel_l2(gl[q], ol[q]) <= 1e-2, q
+        assert np.array_equal(p.dcodes[0].cpu().numpy(), oc)
+    finally:
+        p.close()
+
+
+def oc_supplied(s):
+    """Seeded supplied codes at every position (so the comparison needs no lockstep)."""
+    return np.random.default_rng(44).integers(0, s.dep_card, s.dep_steps).astype(np.int32)
+
