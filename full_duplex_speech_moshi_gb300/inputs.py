@@ -257,3 +257,75 @@ def make_weights_device(s: ModelShape, depformer: bool = True, seed: int = 1000,
         out[name] = t.to(torch.bfloat16)
         del t
     return out
+
+
+# ----------------------------------------------------------------------------
+# Mimi decoder ("PersonaPlex native LM audit", chapter "Exact Mimi codec construction")
+# ----------------------------------------------------------------------------
+
+MIMI_FULL = dict(dim=512, cb_dim=256, card=2048, n_q=8, n_layers=8, heads=8, ffn=2048, ctx=250, n_filters=64,
+                 ratios=[8, 6, 5, 4], kernel=7, last_kernel=3, res_kernel=3, compress=2, up_kernel=4,
+                 up_stride=2, ln_eps=1e-5, rope_theta=1e4)
+
+# the smallest shape the GPU kernels take (dim a multiple of 256) that still has two
+# transformer blocks, a window the test outruns in a few frames and two SEANet stages
+MIMI_SMALL = dict(MIMI_FULL, dim=256, cb_dim=32, card=64, n_layers=2, heads=4, ffn=512, ctx=6, n_filters=8,
+                  ratios=[4, 3])
+
+
+def mimi_tensor_specs(shape: dict) -> List[Tuple[str, Tuple[int, ...]]]:
+    """Names and shapes of the decoder's tensors in their canonical order (PyTorch
+    layouts: Linear [out, in], Conv1d [out, in, k], ConvTranspose1d [in, out, k])."""
+    s = dict(MIMI_FULL)
+    s.update(shape)
+    t = [(f"q.codebook.{j}", (s["card"], s["cb_dim"])) for j in range(s["n_q"])]
+    t += [("q.sem.out", (s["dim"], s["cb_dim"])), ("q.ac.out", (s["dim"], s["cb_dim"])),
+          ("up.weight", (s["dim"], 1, s["up_kernel"]))]
+    d, f = s["dim"], s["ffn"]
+    for l in range(s["n_layers"]):
+        p = f"tr.{l}."
+        t += [(p + "norm1.w", (d,)), (p + "norm1.b", (d,)), (p + "in_proj", (3 * d, d)), (p + "out_proj", (d, d)),
+              (p + "scale1", (d,)), (p + "norm2.w", (d,)), (p + "norm2.b", (d,)), (p + "lin1", (f, d)),
+              (p + "lin2", (d, f)), (p + "scale2", (d,))]
+    C = s["n_filters"] * 2 ** len(s["ratios"])
+    t += [("dec.0.w", (C, d, s["kernel"])), ("dec.0.b", (C,))]
+    for i, r in enumerate(s["ratios"]):
+        co = C // 2
+        h = co // s["compress"]
+        t += [(f"dec.up{i}.w", (C, co, 2 * r)), (f"dec.up{i}.b", (co,)), (f"dec.res{i}.w1", (h, co, s["res_kernel"])),
+              (f"dec.res{i}.b1", (h,)), (f"dec.res{i}.w2", (co, h, 1)), (f"dec.res{i}.b2", (co,))]
+        C = co
+    return t + [("dec.out.w", (1, C, s["last_kernel"])), ("dec.out.b", (1,))]
+
+
+def make_mimi_weights(shape: dict, base_seed: int = 5000, layer_scale: float = 0.05,
+                      threads: int | None = None) -> Dict[str, np.ndarray]:
+    """bf16 bits of every decoder tensor: codebooks N(0, 1); LayerNorm weights
+    1 + 0.1 N(0, 1); LayerScale layer_scale (1 + 0.1 N(0, 1)); biases (LayerNorm biases
+    included) N(0, 0.02); matrices and kernels N(0, 1 / fan), fan = the product of all
+    dimensions after the first (so activations keep their scale through the stack).
+    Tensor i of the canonical order gets seed base_seed + i."""
+    threads = threads or min(32, os.cpu_count() or 1)
+    out: Dict[str, np.ndarray] = {}
+    with ThreadPoolExecutor(threads) as pool:
+        for i, (name, sh) in enumerate(mimi_tensor_specs(shape)):
+            if name.startswith("q.codebook"):
+                mean, std = 0.0, 1.0
+            elif name.endswith(("norm1.w", "norm2.w")):
+                mean, std = 1.0, 0.1
+            elif name.endswith(("scale1", "scale2")):
+                mean, std = layer_scale, 0.1 * layer_scale
+            elif len(sh) == 1:
+                mean, std = 0.0, 0.02
+            else:
+                mean, std = 0.0, float(1.0 / np.sqrt(np.prod(sh[1:])))
+            out[name] = normal_bf16(sh, mean, std, base_seed + i, pool)
+    return out
+
+
+def make_mimi_codes(shape: dict, T: int, B: int = 1, seed: int = 6000) -> np.ndarray:
+    """Code frames [T][B][n_q], each code uniform over 0..card-1."""
+    s = dict(MIMI_FULL)
+    s.update(shape)
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, T, B])))
+    return g.integers(0, s["card"], size=(T, B, s["n_q"]), dtype=np.int64).astype(np.int32)

@@ -24,6 +24,9 @@ EXPORTS = ["pm_kv_cache_bytes", "pm_create", "pm_reset", "pm_set_positions", "pm
            "pm_frame_step", "pm_depformer_step", "pm_profile_frame", "pm_device_status", "pm_last_error",
            "pm_destroy", "pm_text_head_noalloc", "pm_set_sampling", "pm_sample", "pm_snapshot_bytes",
            "pm_snapshot", "pm_restore", "pm_prefill", "pm_set_wait_budget", "pm_generator_step"]
+# every symbol include/pm_mimi.h declares
+MIMI_EXPORTS = ["pm_mimi_tensor_count", "pm_mimi_create", "pm_mimi_decode", "pm_mimi_reset", "pm_mimi_status",
+                "pm_mimi_get_frames", "pm_mimi_last_error", "pm_mimi_destroy"]
 PM_WAIT_BUDGET_DEFAULT = 0xFFFFFFFF
 KERNEL_KINDS = {0: "embed", 1: "qkv_rope", 2: "attention", 3: "out_proj", 4: "linear_in_swiglu",
                 5: "linear_out", 6: "text_head", 7: "frame_program", 8: "text_sample"}
@@ -44,6 +47,17 @@ PM_FLAG_DEPFORMER_CHAIN = 4
 
 
 _PP = C.POINTER(C.c_void_p)
+
+PM_MIMI_MAX_B = 8
+PM_MIMI_MAX_RATIOS = 8
+
+
+class pm_mimi_config(C.Structure):
+    _fields_ = [("B_max", C.c_int), ("dim", C.c_int), ("cb_dim", C.c_int), ("card", C.c_int), ("n_q", C.c_int),
+                ("n_layers", C.c_int), ("heads", C.c_int), ("ffn", C.c_int), ("ctx", C.c_int),
+                ("n_filters", C.c_int), ("n_ratios", C.c_int), ("ratios", C.c_int * PM_MIMI_MAX_RATIOS),
+                ("kernel", C.c_int), ("last_kernel", C.c_int), ("res_kernel", C.c_int), ("compress", C.c_int),
+                ("up_kernel", C.c_int), ("up_stride", C.c_int), ("ln_eps", C.c_float), ("rope_theta", C.c_float)]
 
 
 class pm_temporal_weights(C.Structure):
@@ -113,6 +127,23 @@ def lib():
         L.pm_restore.argtypes = [vp, C.c_int, vp]
         L.pm_destroy.restype = None
         L.pm_destroy.argtypes = [vp]
+        mp = C.POINTER(pm_mimi_config)
+        L.pm_mimi_tensor_count.restype = C.c_int
+        L.pm_mimi_tensor_count.argtypes = [mp]
+        L.pm_mimi_create.restype = C.c_int
+        L.pm_mimi_create.argtypes = [mp, vp, C.c_int, vp, C.POINTER(C.c_void_p)]
+        L.pm_mimi_decode.restype = C.c_int
+        L.pm_mimi_decode.argtypes = [vp, C.c_int, vp, vp]
+        L.pm_mimi_reset.restype = C.c_int
+        L.pm_mimi_reset.argtypes = [vp, vp]
+        L.pm_mimi_status.restype = C.c_int
+        L.pm_mimi_status.argtypes = [vp]
+        L.pm_mimi_get_frames.restype = C.c_int
+        L.pm_mimi_get_frames.argtypes = [vp, vp]
+        L.pm_mimi_last_error.restype = C.c_char_p
+        L.pm_mimi_last_error.argtypes = [vp]
+        L.pm_mimi_destroy.restype = None
+        L.pm_mimi_destroy.argtypes = [vp]
         _lib = L
     return _lib
 
@@ -333,3 +364,109 @@ def alloc_kv_cache(cfg: pm_config, device: str = "cuda"):
     import torch
     shape = (cfg.n_layers, 2, cfg.B_max, cfg.H, cfg.ctx, cfg.dh)
     return torch.zeros(shape, dtype=torch.bfloat16, device=device)
+
+
+# ------------------------------------------------------------------------------------
+# streaming Mimi decoder (include/pm_mimi.h)
+# ------------------------------------------------------------------------------------
+
+MIMI_DEFAULT = dict(dim=512, cb_dim=256, card=2048, n_q=8, n_layers=8, heads=8, ffn=2048, ctx=250, n_filters=64,
+                    ratios=[8, 6, 5, 4], kernel=7, last_kernel=3, res_kernel=3, compress=2, up_kernel=4,
+                    up_stride=2, ln_eps=1e-5, rope_theta=1e4)
+
+
+def make_mimi_config(shape: dict, B_max: int) -> pm_mimi_config:
+    s = dict(MIMI_DEFAULT)
+    s.update(shape)
+    c = pm_mimi_config()
+    c.B_max = int(B_max)
+    for k in ("dim", "cb_dim", "card", "n_q", "n_layers", "heads", "ffn", "ctx", "n_filters", "kernel",
+              "last_kernel", "res_kernel", "compress", "up_kernel", "up_stride"):
+        setattr(c, k, int(s[k]))
+    c.n_ratios = len(s["ratios"])
+    for i, r in enumerate(s["ratios"]):
+        c.ratios[i] = int(r)
+    c.ln_eps = float(s["ln_eps"])
+    c.rope_theta = float(s["rope_theta"])
+    return c
+
+
+def mimi_tensor_names(shape: dict) -> List[str]:
+    """Tensor names in the canonical order of include/pm_mimi.h."""
+    s = dict(MIMI_DEFAULT)
+    s.update(shape)
+    n = [f"q.codebook.{j}" for j in range(s["n_q"])] + ["q.sem.out", "q.ac.out", "up.weight"]
+    for l in range(s["n_layers"]):
+        n += [f"tr.{l}.{k}" for k in ("norm1.w", "norm1.b", "in_proj", "out_proj", "scale1", "norm2.w", "norm2.b",
+                                      "lin1", "lin2", "scale2")]
+    n += ["dec.0.w", "dec.0.b"]
+    for i in range(len(s["ratios"])):
+        n += [f"dec.up{i}.w", f"dec.up{i}.b", f"dec.res{i}.w1", f"dec.res{i}.b1", f"dec.res{i}.w2", f"dec.res{i}.b2"]
+    return n + ["dec.out.w", "dec.out.b"]
+
+
+def mimi_frame_samples(shape: dict) -> int:
+    s = dict(MIMI_DEFAULT)
+    s.update(shape)
+    n = int(s["up_stride"])
+    for r in s["ratios"]:
+        n *= int(r)
+    return n
+
+
+class MimiDecoder:
+    """Owns one pm_mimi_ctx.  `weights` maps the canonical tensor names (mimi_tensor_names)
+    to bf16 device tensors, which the caller keeps alive."""
+
+    def __init__(self, shape: dict, weights: Dict[str, object], B_max: int = 1, stream: int = 0):
+        L = lib()
+        self.L = L
+        self.cfg = make_mimi_config(shape, B_max)
+        self.frame_samples = mimi_frame_samples(shape)
+        names = mimi_tensor_names(shape)
+        n = L.pm_mimi_tensor_count(C.byref(self.cfg))
+        if n != len(names):
+            raise PMError(PM_ERR_ARG, f"unsupported Mimi configuration (tensor count {n})")
+        self._ptrs = (C.c_void_p * len(names))(*[_ptr(weights[k]) for k in names])
+        h = C.c_void_p()
+        st = L.pm_mimi_create(C.byref(self.cfg), self._ptrs, len(names), stream or None, C.byref(h))
+        if st != PM_OK:
+            raise PMError(st, L.pm_mimi_last_error(None).decode())
+        self.h = h
+
+    def _check(self, st: int):
+        if st != PM_OK:
+            raise PMError(st, self.L.pm_mimi_last_error(self.h).decode())
+
+    def decode(self, B: int, codes, pcm) -> None:
+        """Next frame of streams 0..B-1: codes [B][n_q] int32 (host or device), pcm
+        [B][frame_samples] fp32 (device or host-mapped)."""
+        if codes is not None and not hasattr(codes, "data_ptr"):
+            import numpy as np
+            codes = np.ascontiguousarray(codes, dtype=np.int32)
+        self._check(self.L.pm_mimi_decode(self.h, int(B), _ptr(codes), _ptr(pcm)))
+
+    def reset(self, mask=None) -> None:
+        m = None
+        if mask is not None:
+            m = (C.c_int32 * self.cfg.B_max)(*[int(v) for v in mask])
+        self._check(self.L.pm_mimi_reset(self.h, m))
+
+    def status(self) -> int:
+        return int(self.L.pm_mimi_status(self.h))
+
+    def frames(self) -> List[int]:
+        a = (C.c_int32 * self.cfg.B_max)()
+        self._check(self.L.pm_mimi_get_frames(self.h, a))
+        return list(a)
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.L.pm_mimi_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

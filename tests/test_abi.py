@@ -10,17 +10,19 @@ from full_duplex_speech_moshi_gb300 import pm
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def declared_functions():
-    src = open(os.path.join(ROOT, "include", "pm.h")).read()
+def declared_functions(header="pm.h"):
+    src = open(os.path.join(ROOT, "include", header)).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(pm_[a-z_]+)\s*\(", src)))
 
 
 def test_exports_every_declared_symbol():
     L = pm.lib()
-    names = declared_functions()
-    assert set(names) == set(pm.EXPORTS)
-    for n in names:
+    headers = sorted(f for f in os.listdir(os.path.join(ROOT, "include")) if f.endswith(".h"))
+    assert headers == ["pm.h", "pm_mimi.h"]
+    assert set(declared_functions("pm.h")) == set(pm.EXPORTS)
+    assert set(declared_functions("pm_mimi.h")) == set(pm.MIMI_EXPORTS)
+    for n in pm.EXPORTS + pm.MIMI_EXPORTS:
         assert hasattr(L, n), n
 
 
