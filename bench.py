@@ -201,6 +201,157 @@ def cpu_baseline_sample(budget_s: float = 15.0, max_frames: int = 64):
                            "sample": f"frame at position {n + 1}, one OpenMP thread, {dt1:.1f} s"}}
 
 
+# ------------------------------------------------------------------------------------
+# streaming Mimi decoder (codes -> 24 kHz PCM)
+# ------------------------------------------------------------------------------------
+
+MIMI_METRIC = "Mimi decode frames/s (B=1, 80 ms code frame -> 1920 PCM samples)"
+MIMI_WORKLOAD = ("Mimi decoder (split RVQ 8 x 2048 x 256 -> dim 512, depthwise 2x upsampler, 8-block transformer "
+                 "8x64 heads ffn 2048 window 250, SEANet 1024 -> 64 ratios 8,6,5,4), B=1, streaming from reset")
+FP32_LANES = 152 * 128     # FP32 FMA lanes of the GPU (152 SMs x 128)
+
+
+def mimi_work(shape: dict, B: int):
+    """Algorithmic (bytes, flops) of each launch of one decode call, in launch order:
+    bytes = bf16 weights read once + fp32 activations in and out; flops = 2 x the
+    multiply-adds the definition needs (a transposed convolution: every input position x
+    Cin x Cout x kernel)."""
+    s = dict(I.MIMI_FULL)
+    s.update(shape)
+    d, f, cb, nq = s["dim"], s["ffn"], s["cb_dim"], s["n_q"]
+    q = 2 * B
+    out = [(2 * 2 * d * cb + 2 * nq * cb * B + 4 * 2 * d * B * 2, 2 * 2 * d * cb * B)]
+    for _ in range(s["n_layers"]):
+        out.append((2 * 3 * d * d + 4 * q * (d + 3 * d), 2 * 3 * d * d * q))
+        out.append((4 * q * 3 * d + 4 * q * d, 0))     # attention: new q/k/v in, o out (ring reads are L2-resident)
+        out.append((2 * d * d + 4 * q * 2 * d, 2 * d * d * q))
+        out.append((2 * f * d + 4 * q * (d + f), 2 * f * d * q))
+        out.append((2 * d * f + 4 * q * (f + 2 * d), 2 * d * f * q))
+    C = s["n_filters"] * 2 ** len(s["ratios"])
+    T = 2
+    out.append((2 * C * d * s["kernel"] + 4 * B * T * (d + C), 2 * C * d * s["kernel"] * T * B))
+    for r in s["ratios"]:
+        co, h = C // 2, C // 2 // s["compress"]
+        out.append((2 * C * co * 2 * r + 4 * B * (C * T + co * T * r), 2 * T * C * co * 2 * r * B))
+        T *= r
+        out.append((2 * h * co * s["res_kernel"] + 4 * B * T * (co + h), 2 * h * co * s["res_kernel"] * T * B))
+        out.append((2 * co * h + 4 * B * T * (h + 2 * co), 2 * co * h * T * B))
+        C = co
+    out.append((2 * C * s["last_kernel"] + 4 * B * T * (C + 1), 2 * C * s["last_kernel"] * T * B))
+    out.append((0, 0))
+    return out
+
+
+def mimi_measure(B: int, steps: int, warmup: int, stream, flush, profile: bool = False):
+    """Frames/s of the streaming decoder at batch B: each timed call bracketed by CUDA
+    events, L2 flushed (256 MB written) between calls, since the decoder's 90 MB of
+    weights would otherwise stay in the 129 MB L2.  With profile, also per-launch times
+    of one call (pm_mimi_profile, queued behind a spin so host launch gaps do not count)."""
+    import torch
+    from full_duplex_speech_moshi_gb300 import pm
+    shape = I.MIMI_FULL
+    W = pm.upload_weights(I.make_mimi_weights(shape))
+    dec = pm.MimiDecoder(shape, W, B_max=B, stream=stream.cuda_stream)
+    fs = pm.mimi_frame_samples(shape)
+    n = warmup + steps
+    codes = torch.from_numpy(I.make_mimi_codes(shape, n + 1, B, seed=6100)).cuda()
+    pcm = torch.empty((B, fs), dtype=torch.float32, device="cuda")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for t in range(warmup):
+        dec.decode(B, codes[t], pcm)
+    for i in range(steps):
+        flush.fill_(float(i))
+        ev[i][0].record(stream)
+        dec.decode(B, codes[warmup + i], pcm)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    res = {"ms_mean": statistics.mean(ms), "ms_p50": statistics.median(ms), "frames_per_s": B * 1000.0 / statistics.mean(ms)}
+    if profile:
+        prof = []
+        for rep in range(3):
+            flush.fill_(1.0 + rep)
+            torch.cuda._sleep(2_000_000)
+            prof.append(dec.profile(B, codes[n - 3 + rep], pcm))
+        res["profile"] = [(k, statistics.median(p[i][1] for p in prof)) for i, (k, _) in enumerate(prof[0])]
+    # end to end: host codes in, PCM out into pinned host memory, synchronised per frame
+    host_codes = I.make_mimi_codes(shape, steps, B, seed=6200)
+    host_pcm = torch.empty((B, fs), dtype=torch.float32).pin_memory()
+    dec.reset()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for t in range(steps):
+        dec.decode(B, host_codes[t], host_pcm)
+        stream.synchronize()
+    res["e2e_frames_per_s"] = B * steps / (time.perf_counter() - t0)
+    res["e2e_h2d_bytes"] = 4 * B * I.MIMI_FULL["n_q"] + 16
+    res["e2e_d2h_bytes"] = 4 * B * fs
+    dec.close()
+    return res
+
+
+def run_mimi(args):
+    """The streaming Mimi decoder as its own JSON line: value = frames/s at B=1, the
+    B=8 stream-frames/s beside it, per-kind device times of one call, the roofline of the
+    kind with the largest share (fp32 FMA work against the ALU peak at the sampled clock, or
+    bytes against HBM), e2e through host memory, and the oracle's CPU rate."""
+    import torch
+    from full_duplex_speech_moshi_gb300 import pm  # noqa: F401
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
+    with ClockSampler(0) as clk:
+        r1 = mimi_measure(1, args.steps, args.warmup, stream, flush, profile=True)
+        r8 = mimi_measure(8, args.steps, args.warmup, stream, flush, profile=True)
+    clocks = clk.summary()
+    work = mimi_work(I.MIMI_FULL, 1)
+    by_kind = {}
+    for (k, ms), (by, fl) in zip(r1["profile"], work):
+        e = by_kind.setdefault(k, [0.0, 0, 0, 0])
+        e[0] += ms
+        e[1] += by
+        e[2] += fl
+        e[3] += 1
+    total = sum(v[0] for v in by_kind.values())
+    dom = max(by_kind, key=lambda k: by_kind[k][0])
+    t_ms, by, fl, cnt = by_kind[dom]
+    mhz = clocks.get("sm_mhz") or 2070.0
+    alu_peak = FP32_LANES * 2 * mhz * 1e6 / 1e12
+    hbm_peak, src = load_peaks()
+    if fl / (t_ms * 1e-3) / 1e12 / alu_peak >= by / (t_ms * 1e-3) / 1e9 / hbm_peak:
+        roof = {"bound": "alu", "achieved": fl / (t_ms * 1e-3) / 1e12, "peak": alu_peak, "unit": "TFLOP/s",
+                "peak_source": f"152 SMs x 128 FP32 lanes x 2 x {mhz:.0f} MHz (sampled SM clock)"}
+    else:
+        roof = {"bound": "hbm", "achieved": by / (t_ms * 1e-3) / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"}
+    roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None, "kernel": dom, "launches": cnt,
+                 "kernel_ms": t_ms / cnt, "share_of_call": t_ms / total})
+    cpu = None
+    if not args.no_cpu_baseline:
+        from oracle import mimi as M
+        orc = M.MimiDecoderOracle(M.MimiShape(**I.MIMI_FULL), I.make_mimi_weights(I.MIMI_FULL))
+        codes = I.make_mimi_codes(I.MIMI_FULL, 8, 1, seed=6300)[:, 0]
+        t0 = time.perf_counter()
+        orc.decode(codes)
+        dt = time.perf_counter() - t0
+        cpu = {"value": 8 / dt, "unit": "frames/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"8 frames from reset decoded at once (non-streaming), float64 numpy, {dt:.1f} s"}
+    line = {"metric": MIMI_METRIC, "value": r1["frames_per_s"], "unit": "frames/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": r1["ms_mean"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (random-init bf16 weights, "
+            "uniform codes)", "config": {"workload": MIMI_WORKLOAD, "global_batch": 1,
+                                         "l2": "flushed between timed calls (256 MB written)"},
+            "roofline": roof,
+            "kernel_ms_by_kind": {k: v[0] for k, v in by_kind.items()},
+            "profiled_call_ms": total,
+            "B8_stream_frames_per_s": r8["frames_per_s"], "B8_ms_per_step": r8["ms_mean"],
+            "e2e": {"value": r1["e2e_frames_per_s"], "unit": "frames/s", "h2d_bytes_per_step": r1["e2e_h2d_bytes"],
+                    "d2h_bytes_per_step": r1["e2e_d2h_bytes"]},
+            "gpu_launches": len(work) * args.steps, "clocks": clocks, "cpu_baseline": cpu,
+            "realtime_factor_B1": 80.0 / r1["ms_mean"]}
+    print(json.dumps(line), flush=True)
+
+
 def run_case(args):
     """Secondary workloads, one JSON line each (not the headline step):
 
@@ -285,13 +436,15 @@ def main():
                     help="conversations per step (1 = the workload; 8 = the metric's batched case)")
     ap.add_argument("--layers", type=int, default=32,
                     help="temporal blocks (32 = the workload; fewer only for small profiler captures)")
-    ap.add_argument("--case", default="frame", choices=["frame", "prefill", "sample"],
-                    help="frame = the headline decode step; prefill / sample = secondary workloads")
+    ap.add_argument("--case", default="frame", choices=["frame", "prefill", "sample", "mimi"],
+                    help="frame = the headline decode step; prefill / sample / mimi = secondary workloads")
     ap.add_argument("--full", type=int, default=1, help="prefill case: also prime a full history")
     args = ap.parse_args()
     assert args.warmup >= 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.case == "mimi":
+        return run_mimi(args)
     if args.case != "frame":
         return run_case(args)
 

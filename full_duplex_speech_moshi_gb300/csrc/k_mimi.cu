@@ -5,16 +5,24 @@
 // every stage", and the streaming rules of "Stateful streaming, padding and dependency
 // boundaries").
 //
-// One CUDA graph per batch size B:
+// One CUDA graph per batch size B, every launch after the first with programmatic
+// dependent launch (each kernel lets its successor start at once, stages its weights -- which
+// no earlier kernel writes -- and only then waits for its predecessor's results):
 //   k_mimi_front      codes -> split-RVQ lookup -> the two output projections -> latent;
 //                     the depthwise ConvTranspose (kernel 4, stride 2) makes the frame's two
 //                     25 Hz positions from this latent and the previous one
 //   per block         LayerNorm-prologue GEMV (in_proj) -> k_mimi_attn (RoPE, ring append,
 //                     causal window) -> GEMV (out_proj) + LayerScale + residual ->
 //                     LayerNorm GEMV (lin1) + GELU -> GEMV (lin2) + LayerScale + residual
-//   SEANet decoder    causal Conv1d / ConvTranspose1d with ELU on their inputs and the
-//                     residual units; a convolution keeps its last k-1 (activated) inputs,
-//                     a transposed convolution its k-s unfinished outputs
+//   SEANet decoder    every convolution as a "phased" product: output row (phase p, channel
+//                     co), column u, = bias + sum over input channels ci and taps m of
+//                     Wt[p, co][m][ci] x[ci][u - (NT - 1) + m], with the activated input x
+//                     (ELU where the decoder applies one).  A Conv1d is one phase with NT = k
+//                     taps; a ConvTranspose1d of kernel 2s and stride s is s phases with two
+//                     taps each (output n = u s + p takes tap p of input u and tap p + s of
+//                     input u - 1).  Weights are re-laid tap-major once, in pm_mimi_create.
+//                     A convolution keeps its last k - 1 activated inputs; a transposed
+//                     convolution its column u = T (the s outputs the next frame completes).
 //   k_mimi_finish     advances each stream's frame counter and position
 // Streaming state is double-buffered by frame parity: a kernel reads the state of parity
 // (frame & 1) and writes parity (frame + 1) & 1, so no kernel waits for another's reads,
@@ -36,8 +44,8 @@
 namespace pm {
 namespace {
 
-constexpr int MDH = 64;  // transformer head width
-constexpr int TILE = 32; // positions per CTA of the tiled convolutions
+constexpr int MDH = 64;    // transformer head width
+constexpr int GW = 4;      // rows (warps) per CTA of the transformer GEMVs
 
 struct MimiIO {
     const int32_t* codes;  // [B][n_q]
@@ -59,6 +67,26 @@ __device__ __forceinline__ float gelu_f(float x) { return 0.5f * x * (1.0f + erf
 
 __device__ __forceinline__ bool aborted(const MimiState& st) { return *(volatile const uint32_t*)st.abort != 0u; }
 
+__device__ __forceinline__ uint2 ldg_u2(const uint16_t* p) { return __ldg(reinterpret_cast<const uint2*>(p)); }
+
+// copy n elements with NB loads in flight per thread: ld(i) reads element i, st(i, v) stores it
+template <int NB, typename LoadF, typename StoreF>
+__device__ __forceinline__ void batched_copy(int n, LoadF ld, StoreF st) {
+    for (int i0 = threadIdx.x; i0 < n; i0 += NB * (int)blockDim.x) {
+        decltype(ld(0)) v[NB];
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+            const int i = i0 + j * (int)blockDim.x;
+            if (i < n) v[j] = ld(i);
+        }
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+            const int i = i0 + j * (int)blockDim.x;
+            if (i < n) st(i, v[j]);
+        }
+    }
+}
+
 // ------------------------------------------------------------------------------------
 // codes -> latent -> the frame's two upsampled positions
 // ------------------------------------------------------------------------------------
@@ -74,7 +102,7 @@ struct FrontParams {
     int B_max, dim, cb_dim, card, n_q;
 };
 
-// grid (dim / 64, B), 256 threads: warp w makes channels 64 x + 8 w .. + 7
+// grid (dim / 16, B), 256 threads: warp w makes channels 16 x + 2 w, 16 x + 2 w + 1
 __global__ void __launch_bounds__(256) k_mimi_front(const FrontParams p) {
     extern __shared__ float sm[];
     float* sem = sm;              // semantic vector  [cb_dim]
@@ -82,8 +110,8 @@ __global__ void __launch_bounds__(256) k_mimi_front(const FrontParams p) {
     __shared__ int s_codes[16];
     __shared__ int s_bad;
     const int b = blockIdx.y, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    pdl_trigger();
     if (t == 0) s_bad = 0;
-    __syncthreads();
     if (t < p.n_q) {
         const int c = p.io->codes[(size_t)b * p.n_q + t];
         s_codes[t] = c;
@@ -99,40 +127,38 @@ __global__ void __launch_bounds__(256) k_mimi_front(const FrontParams p) {
         return;
     }
     for (int k = t; k < p.cb_dim; k += blockDim.x) {
-        sem[k] = bf(p.cb[0], (size_t)s_codes[0] * p.cb_dim + k);
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (j < p.n_q) v[j] = bf(p.cb[j], (size_t)s_codes[j] * p.cb_dim + k);
         float a = 0.f;
-        for (int j = 1; j < p.n_q; ++j) a += bf(p.cb[j], (size_t)s_codes[j] * p.cb_dim + k);
+#pragma unroll
+        for (int j = 1; j < 16; ++j)
+            if (j < p.n_q) a += v[j];
+        sem[k] = v[0];
         ac[k] = a;
     }
     __syncthreads();
     const int par = p.st.frame[b] & 1;
-    for (int r = 0; r < 8; ++r) {
-        const int c = blockIdx.x * 64 + warp * 8 + r;
+    for (int r = 0; r < 2; ++r) {
+        const int c = blockIdx.x * 16 + warp * 2 + r;
         if (c >= p.dim) break;
         const uint16_t* ws = p.sem_out + (size_t)c * p.cb_dim;
         const uint16_t* wa = p.ac_out + (size_t)c * p.cb_dim;
         float v = 0.f;
-        for (int k = 8 * lane; k < p.cb_dim; k += 256) {
-            const uint4 a = *reinterpret_cast<const uint4*>(ws + k);
-            const uint4 e = *reinterpret_cast<const uint4*>(wa + k);
-            const float* x = sem + k;
-            const float* y = ac + k;
-            v = fmaf(bf16lo(a.x), x[0], v);
-            v = fmaf(bf16hi(a.x), x[1], v);
-            v = fmaf(bf16lo(a.y), x[2], v);
-            v = fmaf(bf16hi(a.y), x[3], v);
-            v = fmaf(bf16lo(a.z), x[4], v);
-            v = fmaf(bf16hi(a.z), x[5], v);
-            v = fmaf(bf16lo(a.w), x[6], v);
-            v = fmaf(bf16hi(a.w), x[7], v);
-            v = fmaf(bf16lo(e.x), y[0], v);
-            v = fmaf(bf16hi(e.x), y[1], v);
-            v = fmaf(bf16lo(e.y), y[2], v);
-            v = fmaf(bf16hi(e.y), y[3], v);
-            v = fmaf(bf16lo(e.z), y[4], v);
-            v = fmaf(bf16hi(e.z), y[5], v);
-            v = fmaf(bf16lo(e.w), y[6], v);
-            v = fmaf(bf16hi(e.w), y[7], v);
+#pragma unroll 4
+        for (int k = 4 * lane; k < p.cb_dim; k += 128) {
+            const uint2 a = ldg_u2(ws + k), e = ldg_u2(wa + k);
+            const float4 x = *reinterpret_cast<const float4*>(sem + k);
+            const float4 y = *reinterpret_cast<const float4*>(ac + k);
+            v = fmaf(bf16lo(a.x), x.x, v);
+            v = fmaf(bf16hi(a.x), x.y, v);
+            v = fmaf(bf16lo(a.y), x.z, v);
+            v = fmaf(bf16hi(a.y), x.w, v);
+            v = fmaf(bf16lo(e.x), y.x, v);
+            v = fmaf(bf16hi(e.x), y.y, v);
+            v = fmaf(bf16lo(e.y), y.z, v);
+            v = fmaf(bf16hi(e.y), y.w, v);
         }
         const float lat = warp_sum(v);
         if (lane == 0) {
@@ -166,71 +192,93 @@ struct MGemvParams {
     int R, K, nq;
 };
 
-// grid ceil(R / 8), 256 threads, a warp per output row; nq <= 16, K a multiple of 128
-template <int PRO, int EPI>
-__global__ void __launch_bounds__(256) k_mimi_gemv(const MGemvParams p) {
-    extern __shared__ float xs[];  // [nq][K]
+// grid ceil(R / 4), 128 threads, a warp per output row.  The CTA's 4 weight rows (and the
+// LayerNorm parameters, the LayerScale) are staged in shared memory before the wait; lane l
+// then takes elements 4 l + 128 i .. + 3 of its row for every position.  NQ bounds the
+// call's positions 2B (nq <= NQ <= 16); K a multiple of 128.
+template <int PRO, int EPI, int NQ>
+__global__ void __launch_bounds__(128) k_mimi_gemv(const MGemvParams p) {
+    extern __shared__ __align__(16) float xs[];  // [nq][K] | LN weight [K] | LN bias [K] | W [4][K] bf16
     __shared__ float s_m[16], s_r[16];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, t = threadIdx.x;
+    const int r0 = blockIdx.x * GW, r = r0 + warp, K = p.K;
+    float* lnw = xs + p.nq * K;
+    float* lnb = lnw + K;
+    uint16_t* ws = reinterpret_cast<uint16_t*>(lnb + K);
+    pdl_trigger();
+    {
+        const int nrow = min(GW, p.R - r0), n8 = nrow * K / 8;
+        const uint4* src = reinterpret_cast<const uint4*>(p.W + (size_t)r0 * K);
+        batched_copy<4>(n8, [&](int i) { return __ldg(src + i); },
+                        [&](int i, uint4 v) { reinterpret_cast<uint4*>(ws)[i] = v; });
+    }
+    float scale = 0.f;
+    if (EPI == ME_SCALE_RES && r < p.R) scale = bf(p.scale, r);
+    if (PRO == MP_LN)
+        batched_copy<4>(K, [&](int k) { return make_float2(bf(p.ln_w, k), bf(p.ln_b, k)); },
+                        [&](int k, float2 v) {
+                            lnw[k] = v.x;
+                            lnb[k] = v.y;
+                        });
+    pdl_wait();
     if (aborted(p.st)) return;
-    for (int i = 4 * t; i < p.nq * p.K; i += 4 * blockDim.x)
-        *reinterpret_cast<float4*>(xs + i) = *reinterpret_cast<const float4*>(p.x + i);
+    batched_copy<4>(p.nq * K / 4, [&](int i) { return reinterpret_cast<const float4*>(p.x)[i]; },
+                    [&](int i, float4 v) { reinterpret_cast<float4*>(xs)[i] = v; });
     __syncthreads();
     if (PRO == MP_LN) {
         // mean and biased variance per position, then (x - m) / sqrt(v + eps) * w + b
-        for (int q = warp; q < p.nq; q += 8) {
-            float s = 0.f;
-            for (int k = lane; k < p.K; k += 32) s += xs[q * p.K + k];
-            const float m = warp_sum(s) / (float)p.K;
-            float v = 0.f;
-            for (int k = lane; k < p.K; k += 32) {
-                const float d = xs[q * p.K + k] - m;
-                v = fmaf(d, d, v);
+        for (int q = warp; q < p.nq; q += GW) {
+            const float4* xq = reinterpret_cast<const float4*>(xs + q * K);
+            float s0 = 0.f, s1 = 0.f;
+            for (int k = lane; k < K / 4; k += 32) {
+                const float4 v = xq[k];
+                s0 += v.x + v.y;
+                s1 += v.z + v.w;
             }
-            v = warp_sum(v);
+            const float m = warp_sum(s0 + s1) / (float)K;
+            float v0 = 0.f, v1 = 0.f;
+            for (int k = lane; k < K / 4; k += 32) {
+                const float4 v = xq[k];
+                const float a = v.x - m, b2 = v.y - m, c = v.z - m, d = v.w - m;
+                v0 = fmaf(a, a, fmaf(b2, b2, v0));
+                v1 = fmaf(c, c, fmaf(d, d, v1));
+            }
+            const float var = warp_sum(v0 + v1);
             if (lane == 0) {
                 s_m[q] = m;
-                s_r[q] = 1.0f / sqrtf(v / (float)p.K + p.eps);
+                s_r[q] = 1.0f / sqrtf(var / (float)K + p.eps);
             }
         }
         __syncthreads();
-        for (int i = t; i < p.nq * p.K; i += blockDim.x) {
-            const int q = i / p.K, k = i - q * p.K;
-            xs[i] = fmaf((xs[i] - s_m[q]) * s_r[q], bf(p.ln_w, k), bf(p.ln_b, k));
-        }
+        for (int q = 0; q < p.nq; ++q)
+            for (int k = t; k < K; k += blockDim.x) xs[q * K + k] = fmaf((xs[q * K + k] - s_m[q]) * s_r[q], lnw[k], lnb[k]);
         __syncthreads();
     }
-    const int r = blockIdx.x * 8 + warp;
     if (r >= p.R) return;
-    float acc[16];
+    float acc[NQ];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) acc[q] = 0.f;
-    const uint16_t* wr = p.W + (size_t)r * p.K;
-    for (int k = 4 * lane; k < p.K; k += 128) {
-        const uint2 w = *reinterpret_cast<const uint2*>(wr + k);
+    for (int q = 0; q < NQ; ++q) acc[q] = 0.f;
+    const uint16_t* wrow = ws + (size_t)warp * K;
+    for (int k = 4 * lane; k < K; k += 128) {
+        const uint2 w = *reinterpret_cast<const uint2*>(wrow + k);
         const float w0 = bf16lo(w.x), w1 = bf16hi(w.x), w2 = bf16lo(w.y), w3 = bf16hi(w.y);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < NQ; ++q) {
             if (q < p.nq) {
-                const float4 x = *reinterpret_cast<const float4*>(xs + q * p.K + k);
-                float a = acc[q];
-                a = fmaf(w0, x.x, a);
-                a = fmaf(w1, x.y, a);
-                a = fmaf(w2, x.z, a);
-                a = fmaf(w3, x.w, a);
-                acc[q] = a;
+                const float4 x = *reinterpret_cast<const float4*>(xs + q * K + k);
+                acc[q] = fmaf(w3, x.w, fmaf(w2, x.z, fmaf(w1, x.y, fmaf(w0, x.x, acc[q]))));
             }
         }
     }
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
+    for (int q = 0; q < NQ; ++q) {
         if (q < p.nq) {
             const float v = warp_sum(acc[q]);
-            if (lane == 0) {
+            if (lane == q) {
                 float* o = p.y + (size_t)q * p.R + r;
                 if (EPI == ME_STORE) *o = v;
                 if (EPI == ME_GELU) *o = gelu_f(v);
-                if (EPI == ME_SCALE_RES) *o = fmaf(v, bf(p.scale, r), *o);
+                if (EPI == ME_SCALE_RES) *o = fmaf(v, scale, *o);
             }
         }
     }
@@ -251,217 +299,364 @@ struct MAttnParams {
     float scale_log2;     // log2(e) / sqrt(64)
 };
 
+// The window holds keys base .. pos0 + 1, base = pos0 - ctx + 1: NW = ctx + 1 rows.  The
+// rows of earlier frames are final when the call starts, so they are staged into shared
+// memory before the wait; the frame's two keys and values are made after it (RoPE) and go
+// both to the ring and to the staged window.  Then a thread per key computes both queries'
+// scores, the CTA takes the softmax, and pairs of threads sum the values.
 __global__ void __launch_bounds__(256) k_mimi_attn(const MAttnParams p) {
+    extern __shared__ __align__(16) float asm_[];
+    const int NW = p.ctx + 1;
+    float* Ks = asm_;                                  // [NW][65]
+    float* Vs = Ks + (((size_t)NW * 65 + 3) & ~(size_t)3);  // [NW][64], 16-byte aligned
+    float* sc = Vs + (size_t)NW * 64;    // [2][NW] scores, then probabilities
     __shared__ float qr[2][MDH];
-    __shared__ float s_m[8][2], s_l[8][2];
-    __shared__ float s_o[8][2][MDH];
+    __shared__ float red[2][8];
+    __shared__ float s_max[2], s_sum[2];
+    __shared__ float part[2][2][MDH];
     const int b = blockIdx.x, h = blockIdx.y;
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    if (aborted(p.st)) return;
-    const int pos0 = p.st.pos[b];
     const size_t hb = ((size_t)b * p.H + h) * p.RS;
-    // RoPE on adjacent pairs (2j, 2j + 1) of q and k at the frame's two positions
+    pdl_trigger();
+    const int pos0 = p.st.pos[b];        // set by the previous call's last kernel
+    const int base = pos0 - p.ctx + 1;
+    {
+        // old rows: positions max(0, base) .. pos0 - 1, 16 float4 per row and tensor
+        const int first = max(0, base), n_old = pos0 - first;
+        const int n4 = n_old * 16;
+        for (int i0 = t; i0 < 2 * n4; i0 += 4 * blockDim.x) {
+            float4 v[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * blockDim.x;
+                if (i < 2 * n4) {
+                    const int tensor = i >= n4, ii = i - tensor * n4, row = ii >> 4, c4 = ii & 15;
+                    const int kp = first + row;
+                    v[j] = reinterpret_cast<const float4*>((tensor ? p.vc : p.kc) + (hb + (size_t)(kp % p.RS)) * MDH)[c4];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + j * blockDim.x;
+                if (i < 2 * n4) {
+                    const int tensor = i >= n4, ii = i - tensor * n4, row = ii >> 4, c4 = ii & 15;
+                    const int sr = first + row - base;
+                    if (tensor) {
+                        reinterpret_cast<float4*>(Vs + (size_t)sr * 64)[c4] = v[j];
+                    } else {
+                        float* d = Ks + (size_t)sr * 65 + 4 * c4;
+                        d[0] = v[j].x;
+                        d[1] = v[j].y;
+                        d[2] = v[j].z;
+                        d[3] = v[j].w;
+                    }
+                }
+            }
+        }
+    }
+    pdl_wait();
+    if (aborted(p.st)) return;
+    // RoPE on adjacent pairs (2j, 2j + 1) of q and k at the frame's two positions; the
+    // angle is reduced modulo 2 pi in double before the single-precision sine and cosine
     if (t < MDH) {
         const int i = t / (MDH / 2), j = t % (MDH / 2);
         const int pos = pos0 + i;
-        double sn, cs;
-        sincos((double)pos * p.freq[j], &sn, &cs);
-        const float c = (float)cs, s = (float)sn;
+        const double a = (double)pos * p.freq[j];
+        const double two_pi = 6.283185307179586476925;
+        const float ang = (float)(a - two_pi * rint(a * (1.0 / two_pi)));
+        float sn, cs;
+        sincosf(ang, &sn, &cs);
         const float* row = p.qkv + ((size_t)b * 2 + i) * 3 * p.dim + h * MDH;
         const float q0 = row[2 * j], q1 = row[2 * j + 1];
         const float k0 = row[p.dim + 2 * j], k1 = row[p.dim + 2 * j + 1];
-        qr[i][2 * j] = q0 * c - q1 * s;
-        qr[i][2 * j + 1] = q0 * s + q1 * c;
+        const float v0 = row[2 * p.dim + 2 * j], v1 = row[2 * p.dim + 2 * j + 1];
+        const float kr0 = k0 * cs - k1 * sn, kr1 = k0 * sn + k1 * cs;
+        qr[i][2 * j] = q0 * cs - q1 * sn;
+        qr[i][2 * j + 1] = q0 * sn + q1 * cs;
         float* kd = p.kc + (hb + (size_t)(pos % p.RS)) * MDH;
         float* vd = p.vc + (hb + (size_t)(pos % p.RS)) * MDH;
-        kd[2 * j] = k0 * c - k1 * s;
-        kd[2 * j + 1] = k0 * s + k1 * c;
-        vd[2 * j] = row[2 * p.dim + 2 * j];
-        vd[2 * j + 1] = row[2 * p.dim + 2 * j + 1];
+        kd[2 * j] = kr0;
+        kd[2 * j + 1] = kr1;
+        vd[2 * j] = v0;
+        vd[2 * j + 1] = v1;
+        const int sr = pos - base;  // ctx - 1 + i
+        Ks[(size_t)sr * 65 + 2 * j] = kr0;
+        Ks[(size_t)sr * 65 + 2 * j + 1] = kr1;
+        Vs[(size_t)sr * 64 + 2 * j] = v0;
+        Vs[(size_t)sr * 64 + 2 * j + 1] = v1;
     }
     __syncthreads();
-    // the query at position pos sees keys max(0, pos - ctx + 1) .. pos; warp w takes keys
-    // lo + w, lo + w + 8, ... with a running maximum and sum; lane l holds coordinates 2l, 2l+1
-    for (int i = 0; i < 2; ++i) {
-        const int pos = pos0 + i, lo = max(0, pos - p.ctx + 1);
-        const float qa = qr[i][2 * lane], qb = qr[i][2 * lane + 1];
-        float m = -INFINITY, l = 0.f, a0 = 0.f, a1 = 0.f;
-        for (int kp = lo + warp; kp <= pos; kp += 8) {
-            const float2 kv = *reinterpret_cast<const float2*>(p.kc + (hb + (size_t)(kp % p.RS)) * MDH + 2 * lane);
-            const float2 vv = *reinterpret_cast<const float2*>(p.vc + (hb + (size_t)(kp % p.RS)) * MDH + 2 * lane);
-            const float sc = warp_sum(fmaf(qa, kv.x, qb * kv.y)) * p.scale_log2;
-            const float mn = fmaxf(m, sc);
-            const float f = exp2f(m - mn), e = exp2f(sc - mn);
-            l = fmaf(l, f, e);
-            a0 = fmaf(a0, f, e * vv.x);
-            a1 = fmaf(a1, f, e * vv.y);
-            m = mn;
+    // scores: query i (position pos0 + i) sees keys max(0, pos0 + i - ctx + 1) .. pos0 + i,
+    // i.e. rows i .. ctx - 1 + i of the window, without negative positions
+    float mx[2] = {-INFINITY, -INFINITY};
+    for (int r = t; r < NW; r += blockDim.x) {
+        const float* kr = Ks + (size_t)r * 65;
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll 16
+        for (int d = 0; d < MDH; ++d) {
+            const float k = kr[d];
+            a0 = fmaf(qr[0][d], k, a0);
+            a1 = fmaf(qr[1][d], k, a1);
         }
-        if (lane == 0) {
-            s_m[warp][i] = m;
-            s_l[warp][i] = l;
-        }
-        s_o[warp][i][2 * lane] = a0;
-        s_o[warp][i][2 * lane + 1] = a1;
+        const bool live = base + r >= 0;
+        const float s0 = (live && r <= p.ctx - 1) ? a0 * p.scale_log2 : -INFINITY;
+        const float s1 = (live && r >= 1) ? a1 * p.scale_log2 : -INFINITY;
+        sc[r] = s0;
+        sc[NW + r] = s1;
+        mx[0] = fmaxf(mx[0], s0);
+        mx[1] = fmaxf(mx[1], s1);
     }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        float m = mx[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) red[i][warp] = m;
+    }
+    __syncthreads();
+    if (t < 2) {
+        float m = red[t][0];
+        for (int w = 1; w < 8; ++w) m = fmaxf(m, red[t][w]);
+        s_max[t] = m;
+    }
+    __syncthreads();
+    float sm[2] = {0.f, 0.f};
+    for (int r = t; r < NW; r += blockDim.x) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float e = exp2f(sc[i * NW + r] - s_max[i]);
+            sc[i * NW + r] = e;
+            sm[i] += e;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float v = warp_sum(sm[i]);
+        if (lane == 0) red[i][warp] = v;
+    }
+    __syncthreads();
+    if (t < 2) {
+        float v = 0.f;
+        for (int w = 0; w < 8; ++w) v += red[t][w];
+        s_sum[t] = v;
+    }
+    // values: thread (half, i, d) sums rows r_lo + half, r_lo + half + 2, ... of query i;
+    // rows of negative positions (before the stream's first frame) were never staged
+    const int d = t & 63, i = (t >> 6) & 1, half = t >> 7, r_lo = max(0, -base);
+    float a = 0.f;
+    for (int r = r_lo + half; r < NW; r += 2) a = fmaf(sc[i * NW + r], Vs[(size_t)r * 64 + d], a);
+    part[half][i][d] = a;
     __syncthreads();
     if (t < 2 * MDH) {
-        const int i = t / MDH, d = t % MDH;
-        float M = -INFINITY;
-        for (int w = 0; w < 8; ++w) M = fmaxf(M, s_m[w][i]);
-        float L = 0.f, A = 0.f;
-        for (int w = 0; w < 8; ++w) {
-            const float f = (s_m[w][i] == -INFINITY) ? 0.f : exp2f(s_m[w][i] - M);
-            L = fmaf(s_l[w][i], f, L);
-            A = fmaf(s_o[w][i][d], f, A);
-        }
-        p.o[((size_t)b * 2 + i) * p.dim + h * MDH + d] = A / L;
+        const int ii = t >> 6, dd = t & 63;
+        p.o[((size_t)b * 2 + ii) * p.dim + h * MDH + dd] = (part[0][ii][dd] + part[1][ii][dd]) / s_sum[ii];
     }
 }
 
+size_t attn_smem(int ctx) {
+    const size_t NW = (size_t)ctx + 1;
+    return 4u * (((NW * 65 + 3) & ~(size_t)3) + NW * 64 + 2 * NW);
+}
+
 // ------------------------------------------------------------------------------------
-// SEANet: causal Conv1d (stride 1) and ConvTranspose1d (kernel 2s, stride s)
+// SEANet convolutions as phased products (see the file header)
 // ------------------------------------------------------------------------------------
 struct MConvParams {
-    const float* in;        // [B][Cin][T] (or [B][T][Cin] when in_pm)
-    float* out;             // [B][Cout][T out]: written, or added to (res)
+    const float* in;        // [B][Cin][T] (or [B][T][Cin] when in_pm), already activated
+    float* out;             // the output as computed, or NULL: Conv1d [B][Cout][T],
+                            // ConvTranspose1d [B][Cout][T s]
+    float* out_act;         // ELU of the output (what the next convolution reads), or NULL
+    const float* res_in;    // residual added to the output (same layout), or NULL
     const MimiIO* io_out;   // when set, the output is the caller's PCM (io_out->pcm)
-    const uint16_t* W;      // Conv1d [Cout][Cin][k]; ConvTranspose1d [Cin][Cout][k]
+    const uint16_t* Wt;     // tap-major [R = P Cout][NT][Cin]
     const uint16_t* bias;   // [Cout]
-    float* state;           // Conv1d: [2][B_max][Cin][k-1] activated inputs;
-                            // ConvTranspose1d: [2][B_max][Cout][k-s] unfinished outputs
+    float* state;           // Conv1d: [2][B_max][Cin][NT-1] activated inputs;
+                            // ConvTranspose1d: [2][B_max][Cout][P] column T of the last call
     MimiState st;
-    int B_max, Cin, Cout, k, s, T;  // T: input positions of this call
-    int elu_in, in_pm, res;
+    int B_max, Cin, Cout, NT, P, T, U;  // P phases (1: Conv1d); U = T (Conv1d) or T + 1
+    int in_pm, rows_per_cta;
 };
 
-// input column tau of channel ci after the optional ELU; tau < 0 is the streaming state
-__device__ __forceinline__ float conv_in(const MConvParams& p, int b, int ci, int tau, const float* st_old) {
-    if (tau < 0) return st_old[((size_t)b * p.Cin + ci) * (p.k - 1) + (p.k - 1 + tau)];
-    const float v = p.in_pm ? p.in[((size_t)b * p.T + tau) * p.Cin + ci] : p.in[((size_t)b * p.Cin + ci) * p.T + tau];
-    return p.elu_in ? elu_f(v) : v;
+// (activated) input of channel ci at position src of this call: a Conv1d takes src < 0 from
+// its state, a ConvTranspose1d reads zeros outside 0..T-1 (its carried column stands in)
+__device__ __forceinline__ float conv_load(const MConvParams& p, int b, int ci, int src, const float* st_old) {
+    if (src < 0)
+        return (p.P == 1 && p.NT > 1) ? st_old[((size_t)b * p.Cin + ci) * (p.NT - 1) + (p.NT - 1 + src)] : 0.f;
+    if (src >= p.T) return 0.f;
+    return p.in_pm ? p.in[((size_t)b * p.T + src) * p.Cin + ci] : p.in[((size_t)b * p.Cin + ci) * p.T + src];
 }
 
-__device__ __forceinline__ float* conv_out(const MConvParams& p) { return p.io_out ? p.io_out->pcm : p.out; }
 
-// T <= 16: grid (ceil(Cout / 8), B), a warp per output channel, lanes split the Cin x k
-// reduction; the CTA stages the activated window [Cin][k - 1 + T] in shared memory
-__global__ void __launch_bounds__(256) k_mimi_conv_w(const MConvParams p) {
-    extern __shared__ float win[];
-    if (aborted(p.st)) return;
-    const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int par = p.st.frame[b] & 1, km = p.k - 1, WL = km + p.T;
-    const float* st_old = km ? p.state + (size_t)par * p.B_max * p.Cin * km : nullptr;
-    for (int i = threadIdx.x; i < p.Cin * WL; i += blockDim.x) {
-        const int ci = i / WL, m = i - ci * WL;
-        win[i] = conv_in(p, b, ci, m - km, st_old);
-    }
-    __syncthreads();
-    if (km && blockIdx.x == 0) {
-        float* st_new = p.state + (size_t)(par ^ 1) * p.B_max * p.Cin * km;
-        for (int i = threadIdx.x; i < p.Cin * km; i += blockDim.x) {
-            const int ci = i / km, m = i - ci * km;
-            st_new[((size_t)b * p.Cin + ci) * km + m] = win[ci * WL + p.T + m];
+// output of row (phase, co), column u: bias (+ carried column, + residual) -> the raw
+// output, its ELU, or the PCM
+__device__ __forceinline__ void conv_put(const MConvParams& p, int b, int row, int u, float acc, int par) {
+    int co = row, n = u, len = p.T;
+    float v = acc;
+    if (p.P > 1) {
+        const int ph = row / p.Cout;
+        co = row - ph * p.Cout;
+        const size_t tl = ((size_t)b * p.Cout + co) * p.P + ph;
+        if (u == p.T) {  // the column the next call completes: kept without the bias
+            p.state[(size_t)(par ^ 1) * p.B_max * p.Cout * p.P + tl] = acc;
+            return;
         }
+        if (u == 0) v += p.state[(size_t)par * p.B_max * p.Cout * p.P + tl];
+        n = u * p.P + ph;
+        len = p.T * p.P;
     }
-    const int co = blockIdx.x * 8 + warp;
-    if (co >= p.Cout) return;
-    float acc[16];
-#pragma unroll
-    for (int t = 0; t < 16; ++t) acc[t] = 0.f;
-    const uint16_t* wr = p.W + (size_t)co * p.Cin * p.k;
-    for (int idx = lane; idx < p.Cin * p.k; idx += 32) {
-        const int ci = idx / p.k, j = idx - ci * p.k;
-        const float w = bf(wr, idx);
-        const float* x = win + ci * WL + j;
-#pragma unroll
-        for (int t = 0; t < 16; ++t)
-            if (t < p.T) acc[t] = fmaf(w, x[t], acc[t]);
+    v += bf(p.bias, co);
+    const size_t o = ((size_t)b * p.Cout + co) * len + n;
+    if (p.res_in) v += p.res_in[o];
+    if (p.io_out) {
+        p.io_out->pcm[o] = v;
+        return;
     }
-    float* out = conv_out(p);
-    const float bias = bf(p.bias, co);
+    if (p.out) p.out[o] = v;
+    if (p.out_act) p.out_act[o] = elu_f(v);
+}
+
+// the next call's Conv1d state: the last NT - 1 activated inputs, from a window that holds
+// positions u0 - (NT - 1) ..
+__device__ __forceinline__ void conv_save_state(const MConvParams& p, int b, int par, const float* win, int WL,
+                                                int u0) {
+    const int km = p.NT - 1;
+    float* st_new = p.state + (size_t)(par ^ 1) * p.B_max * p.Cin * km;
+    for (int i = threadIdx.x; i < p.Cin * km; i += blockDim.x) {
+        const int ci = i / km, m = i - ci * km;
+        st_new[((size_t)b * p.Cin + ci) * km + m] = win[ci * WL + (p.T - u0) + m];
+    }
+}
+
+// U <= UMAX: grid (ceil(R / RC), B) with RC = rows_per_cta (8 or 16), a warp per row (warp w
+// takes rows w, w + 8), lanes over input channels.  The CTA stages its RC rows of weights
+// ([RC][NT][Cin], contiguous) before the wait and the window [Cin][U + NT - 1] (odd row
+// stride) after it.
+template <int UMAX>
+__global__ void __launch_bounds__(256) k_mimi_conv_rows(const MConvParams p) {
+    extern __shared__ __align__(16) uint8_t smraw[];
+    const int R = p.P * p.Cout, KR = p.NT * p.Cin, RC = p.rows_per_cta;
+    const int r0 = blockIdx.x * RC, nrow = min(RC, R - r0);
+    uint16_t* ws = reinterpret_cast<uint16_t*>(smraw);
+    float* win = reinterpret_cast<float*>(smraw + (((size_t)RC * KR * 2 + 15) & ~(size_t)15));
+    const int WL = (p.U + p.NT - 1) | 1;
+    const int b = blockIdx.y, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_trigger();
+    const uint16_t* src = p.Wt + (size_t)r0 * KR;
+    if ((KR & 7) == 0) {
+        batched_copy<4>(nrow * KR / 8, [&](int i) { return __ldg(reinterpret_cast<const uint4*>(src) + i); },
+                        [&](int i, uint4 v) { reinterpret_cast<uint4*>(ws)[i] = v; });
+    } else {
+        batched_copy<8>(nrow * KR, [&](int i) { return src[i]; }, [&](int i, uint16_t v) { ws[i] = v; });
+    }
+    pdl_wait();
+    if (aborted(p.st)) return;
+    const int par = p.st.frame[b] & 1;
+    const float* st_old = p.state + (size_t)par * p.B_max * p.Cin * (p.NT - 1);
+    const int WW = p.U + p.NT - 1;
+    batched_copy<8>(
+        p.Cin * WW,
+        [&](int i) {
+            const int ci = i / WW;
+            return conv_load(p, b, ci, i - ci * WW - (p.NT - 1), st_old);
+        },
+        [&](int i, float v) {
+            const int ci = i / WW;
+            win[ci * WL + (i - ci * WW)] = v;
+        });
+    __syncthreads();
+    if (p.P == 1 && p.NT > 1 && blockIdx.x == 0) conv_save_state(p, b, par, win, WL, 0);
+    for (int rr = warp; rr < nrow; rr += 8) {
+        float acc[UMAX];
 #pragma unroll
-    for (int t = 0; t < 16; ++t) {
-        if (t < p.T) {
-            const float v = warp_sum(acc[t]) + bias;
-            if (lane == 0) {
-                float* o = out + ((size_t)b * p.Cout + co) * p.T + t;
-                *o = p.res ? *o + v : v;
+        for (int u = 0; u < UMAX; ++u) acc[u] = 0.f;
+        const uint16_t* wrow = ws + (size_t)rr * KR;
+        for (int ci = lane; ci < p.Cin; ci += 32) {
+            const float* x = win + ci * WL;
+            for (int m = 0; m < p.NT; ++m) {
+                const float w = __uint_as_float((uint32_t)wrow[m * p.Cin + ci] << 16);
+#pragma unroll
+                for (int u = 0; u < UMAX; ++u)
+                    if (u < p.U) acc[u] = fmaf(w, x[u + m], acc[u]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UMAX; ++u) {
+            if (u < p.U) {
+                const float v = warp_sum(acc[u]);
+                if (lane == u) conv_put(p, b, r0 + rr, u, v, par);
             }
         }
     }
 }
 
-// grid (ceil(T / 32), ceil(Cout / 8), B): lane = position in the tile, warp = channel; the
-// CTA stages the activated inputs [Cin][32 + k - 1] once
-__global__ void __launch_bounds__(256) k_mimi_conv_t(const MConvParams p) {
-    extern __shared__ float win[];
-    if (aborted(p.st)) return;
-    const int b = blockIdx.z, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int par = p.st.frame[b] & 1, km = p.k - 1, WL = TILE + km;
-    const int t0 = blockIdx.x * TILE;
-    const float* st_old = km ? p.state + (size_t)par * p.B_max * p.Cin * km : nullptr;
-    for (int i = threadIdx.x; i < p.Cin * WL; i += blockDim.x) {
-        const int ci = i / WL, m = i - ci * WL, tau = t0 - km + m;
-        win[i] = tau < p.T ? conv_in(p, b, ci, tau, st_old) : 0.f;
-    }
-    __syncthreads();
-    if (km && blockIdx.y == 0 && t0 + TILE >= p.T) {
-        // the last tile's window holds the call's last k - 1 inputs
-        float* st_new = p.state + (size_t)(par ^ 1) * p.B_max * p.Cin * km;
-        for (int i = threadIdx.x; i < p.Cin * km; i += blockDim.x) {
-            const int ci = i / km, m = i - ci * km;
-            st_new[((size_t)b * p.Cin + ci) * km + m] = win[ci * WL + (p.T - t0) + m];
-        }
-    }
-    const int co = blockIdx.y * 8 + warp, t = t0 + lane;
-    if (co >= p.Cout || t >= p.T) return;
-    float acc = bf(p.bias, co);
-    const uint16_t* wr = p.W + (size_t)co * p.Cin * p.k;
-    for (int ci = 0; ci < p.Cin; ++ci) {
-        const float* x = win + ci * WL + lane;
-        for (int j = 0; j < p.k; ++j) acc = fmaf(bf(wr, ci * p.k + j), x[j], acc);
-    }
-    float* o = conv_out(p) + ((size_t)b * p.Cout + co) * p.T + t;
-    *o = p.res ? *o + acc : acc;
+// grid (ceil(U / 32), ceil(R / CO), B): lane = column u0 + lane; the 8 warps split the input
+// channels (warp w takes ci = w, w + 8, ...), each accumulating the CTA's CO rows, and the
+// partial sums meet in shared memory in a fixed order.  Weights are staged before the wait
+// as [NT Cin][CO] (a channel's CO rows adjacent), the activated window [Cin][32 + NT - 1]
+// after it.
+size_t tiled_smem(int Cin, int NT, int CO) {
+    return (((size_t)NT * Cin * CO * 2 + 15) & ~(size_t)15) + ((4u * (size_t)Cin * (32 + NT - 1) + 15) & ~(size_t)15) +
+           4u * 8 * CO * 32;
 }
 
-// ConvTranspose1d, k = 2s: output n takes tap n mod s of input n / s and tap n mod s + s of
-// input n / s - 1.  grid (ceil((T + 1) s / 32), ceil(Cout / 8), B): the call emits outputs
-// 0 .. T s - 1 (the first s completed by the previous call's tail) and keeps T s .. T s + s - 1
-__global__ void __launch_bounds__(256) k_mimi_convtr(const MConvParams p) {
-    extern __shared__ float xs[];  // [Cin][NT] activated inputs t_lo .. t_lo + NT - 1
-    if (aborted(p.st)) return;
+template <int CO>
+__global__ void __launch_bounds__(256) k_mimi_conv_tiled(const MConvParams p) {
+    extern __shared__ __align__(16) uint8_t smraw[];
+    const int R = p.P * p.Cout, KR = p.NT * p.Cin, WL = 32 + p.NT - 1;
+    uint16_t* ws = reinterpret_cast<uint16_t*>(smraw);
+    float* win = reinterpret_cast<float*>(smraw + (((size_t)KR * CO * 2 + 15) & ~(size_t)15));
+    float* red = win + ((((size_t)p.Cin * WL) + 3) & ~(size_t)3);
     const int b = blockIdx.z, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int par = p.st.frame[b] & 1, s = p.s, keep = p.k - p.s, len = p.T * s;
-    const int n0 = blockIdx.x * TILE;
-    const int t_lo = max(0, n0 / s - 1), t_hi = min(p.T - 1, (n0 + TILE - 1) / s);
-    const int NT = t_hi - t_lo + 1;
-    for (int i = threadIdx.x; i < p.Cin * NT; i += blockDim.x) {
-        const int ci = i / NT, m = i - ci * NT;
-        const float v = p.in[((size_t)b * p.Cin + ci) * p.T + t_lo + m];
-        xs[i] = p.elu_in ? elu_f(v) : v;
-    }
+    const int row0 = blockIdx.y * CO, u0 = blockIdx.x * 32;
+    pdl_trigger();
+    batched_copy<8>(
+        CO * KR,
+        [&](int i) { return row0 + i / KR < R ? p.Wt[(size_t)row0 * KR + i] : (uint16_t)0; },
+        [&](int i, uint16_t v) {
+            const int r = i / KR;
+            ws[(i - r * KR) * CO + r] = v;
+        });
+    pdl_wait();
+    if (aborted(p.st)) return;
+    const int par = p.st.frame[b] & 1;
+    const float* st_old = p.state + (size_t)par * p.B_max * p.Cin * (p.NT - 1);
+    batched_copy<8>(
+        p.Cin * WL,
+        [&](int i) {
+            const int ci = i / WL;
+            return conv_load(p, b, ci, u0 - (p.NT - 1) + (i - ci * WL), st_old);
+        },
+        [&](int i, float v) { win[i] = v; });
     __syncthreads();
-    const int co = blockIdx.y * 8 + warp, n = n0 + lane;
-    if (co >= p.Cout || n >= len + keep) return;
-    const int t1 = n / s, j1 = n - t1 * s;
-    const bool v1 = t1 < p.T, v0 = t1 >= 1;
-    const int i1 = v1 ? t1 - t_lo : 0, i0 = v0 ? t1 - 1 - t_lo : 0;
-    float acc = 0.f;
-    for (int ci = 0; ci < p.Cin; ++ci) {
-        const uint16_t* w = p.W + ((size_t)ci * p.Cout + co) * p.k;
-        const float* x = xs + ci * NT;
-        if (v1) acc = fmaf(bf(w, j1), x[i1], acc);
-        if (v0) acc = fmaf(bf(w, j1 + s), x[i0], acc);
+    if (p.P == 1 && p.NT > 1 && blockIdx.y == 0 && u0 + 32 >= p.T) conv_save_state(p, b, par, win, WL, u0);
+    float acc[CO];
+#pragma unroll
+    for (int r = 0; r < CO; ++r) acc[r] = 0.f;
+    for (int ci = warp; ci < p.Cin; ci += 8) {
+        const float* x = win + ci * WL + lane;
+        for (int m = 0; m < p.NT; ++m) {
+            const float xv = x[m];
+            const uint2* wv = reinterpret_cast<const uint2*>(ws + (size_t)(m * p.Cin + ci) * CO);
+#pragma unroll
+            for (int g = 0; g < CO / 4; ++g) {
+                const uint2 w = wv[g];
+                acc[4 * g + 0] = fmaf(bf16lo(w.x), xv, acc[4 * g + 0]);
+                acc[4 * g + 1] = fmaf(bf16hi(w.x), xv, acc[4 * g + 1]);
+                acc[4 * g + 2] = fmaf(bf16lo(w.y), xv, acc[4 * g + 2]);
+                acc[4 * g + 3] = fmaf(bf16hi(w.y), xv, acc[4 * g + 3]);
+            }
+        }
     }
-    const float* tl_old = p.state + (size_t)par * p.B_max * p.Cout * keep;
-    float* tl_new = p.state + (size_t)(par ^ 1) * p.B_max * p.Cout * keep;
-    if (n < len) {
-        if (n < keep) acc += tl_old[((size_t)b * p.Cout + co) * keep + n];
-        p.out[((size_t)b * p.Cout + co) * len + n] = acc + bf(p.bias, co);
-    } else {
-        tl_new[((size_t)b * p.Cout + co) * keep + (n - len)] = acc;
+#pragma unroll
+    for (int r = 0; r < CO; ++r) red[(warp * CO + r) * 32 + lane] = acc[r];
+    __syncthreads();
+    for (int i = threadIdx.x; i < CO * 32; i += blockDim.x) {
+        const int r = i >> 5, l = i & 31;
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) v += red[(w * CO + r) * 32 + l];
+        const int row = row0 + r, u = u0 + l;
+        if (row < R && u < p.U) conv_put(p, b, row, u, v, par);
     }
 }
 
@@ -472,6 +667,7 @@ struct FinishParams {
 };
 
 __global__ void __launch_bounds__(256) k_mimi_finish(const FinishParams p) {
+    pdl_wait();
     const bool ab = aborted(p.st);
     if (ab) {
         for (int i = threadIdx.x; i < p.B * p.frame_samples; i += blockDim.x) p.io->pcm[i] = 0.f;
@@ -483,6 +679,25 @@ __global__ void __launch_bounds__(256) k_mimi_finish(const FinishParams p) {
     if (threadIdx.x == 0) *p.st.abort = 0u;
 }
 
+// tap-major relayout, once at creation: Conv1d W [Cout][Cin][k] -> Wt [Cout][k][Cin];
+// ConvTranspose1d W [Cin][Cout][2s] -> Wt [s][Cout][2][Cin], tap m = 1 being kernel index p
+// (input u) and m = 0 kernel index p + s (input u - 1)
+__global__ void k_mimi_relayout(const uint16_t* W, uint16_t* Wt, int Cin, int Cout, int NT, int P) {
+    const size_t n = (size_t)P * Cout * NT * Cin;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const int ci = (int)(i % Cin);
+        const size_t rest = i / Cin;
+        const int m = (int)(rest % NT);
+        const size_t row = rest / NT;
+        if (P == 1) {
+            Wt[i] = W[(row * Cin + ci) * NT + m];
+        } else {
+            const int ph = (int)(row / Cout), co = (int)(row % Cout), k = 2 * P;
+            Wt[i] = W[((size_t)ci * Cout + co) * k + ph + (1 - m) * P];
+        }
+    }
+}
+
 }  // namespace
 }  // namespace pm
 
@@ -491,6 +706,17 @@ __global__ void __launch_bounds__(256) k_mimi_finish(const FinishParams p) {
 // =====================================================================================
 using namespace pm;
 
+struct MimiLayer {         // one SEANet convolution, as recorded
+    const uint16_t* Wt;    // tap-major weights
+    const uint16_t* bias;
+    float* state;
+    int Cin, Cout, NT, P, T;
+    int in_buf;            // input buffer (activated); -1: the transformer output, position-major
+    int out_raw, out_act;  // buffers for the output and for its ELU (-1: none)
+    int res_buf;           // buffer added to the output (-1: none)
+    int pcm;               // the output is the caller's PCM
+};
+
 struct pm_mimi_ctx {
     pm_mimi_config cfg{};
     int device = 0;
@@ -498,6 +724,7 @@ struct pm_mimi_ctx {
     cudaStream_t stream = nullptr, cap = nullptr;
     std::vector<const uint16_t*> w;      // canonical tensors
     void* block = nullptr;
+    uint16_t* wt_block = nullptr;        // tap-major SEANet weights
     MimiState st{};
     MimiIO* io = nullptr;                // device I/O block
     int32_t* codes_dev = nullptr;        // host codes staged here
@@ -508,6 +735,7 @@ struct pm_mimi_ctx {
     std::vector<float*> acts;            // SEANet activations
     std::vector<float*> states;          // SEANet streaming state [2][B_max][per_stream]
     std::vector<size_t> state_per_stream;
+    std::vector<MimiLayer> layers;       // SEANet convolutions in order
     std::vector<cudaGraphExec_t> graphs; // per B
     std::string err;
 };
@@ -560,43 +788,131 @@ const char* mimi_check(const pm_mimi_config* c) {
     return nullptr;
 }
 
-// per-stream element counts of the state buffers, in recording order
-std::vector<size_t> state_sizes(const pm_mimi_config& f) {
-    std::vector<size_t> v;
-    int C = mimi_channels(f);
-    v.push_back((size_t)f.dim * (f.kernel - 1));
+// the SEANet convolutions in order, with their shapes and buffers (weights filled later).
+// Every convolution after the first reads an ELU, so each producer writes its output
+// activated (the ELU computed once per element); the transposed convolution also keeps its
+// raw output, which the residual unit's second convolution adds.  Buffers: 0 = first
+// convolution (activated); stage i: 1 + 3i raw y, 2 + 3i ELU(y) -- reused for ELU of the
+// residual sum, the next stage's input, once the unit's first convolution has read it --,
+// 3 + 3i the unit's activated middle.
+std::vector<MimiLayer> seanet_layers(const pm_mimi_config& f) {
+    std::vector<MimiLayer> v;
+    auto add = [&](int Cin, int Cout, int NT, int P, int T, int in, int raw, int act, int res, int pcm) {
+        MimiLayer L;
+        memset(&L, 0, sizeof L);
+        L.Cin = Cin;
+        L.Cout = Cout;
+        L.NT = NT;
+        L.P = P;
+        L.T = T;
+        L.in_buf = in;
+        L.out_raw = raw;
+        L.out_act = act;
+        L.res_buf = res;
+        L.pcm = pcm;
+        v.push_back(L);
+    };
+    int C = mimi_channels(f), T = 2;
+    add(f.dim, C, f.kernel, 1, T, -1, -1, 0, -1, 0);
+    int cur = 0;
     for (int i = 0; i < f.n_ratios; ++i) {
-        const int co = C / 2;
-        v.push_back((size_t)co * f.ratios[i]);             // transposed-convolution tail (k - s = r)
-        v.push_back((size_t)co * (f.res_kernel - 1));      // residual unit's first convolution
+        const int r = f.ratios[i], co = C / 2, h = co / f.compress;
+        const int yraw = 1 + 3 * i, yact = 2 + 3 * i, mid = 3 + 3 * i;
+        add(C, co, 2, r, T, cur, yraw, yact, -1, 0);                // ConvTranspose1d, kernel 2r, stride r
+        T *= r;
+        add(co, h, f.res_kernel, 1, T, yact, -1, mid, -1, 0);       // residual unit
+        add(h, co, 1, 1, T, mid, -1, yact, yraw, 0);
+        cur = yact;
         C = co;
     }
-    v.push_back((size_t)C * (f.last_kernel - 1));
+    add(C, 1, f.last_kernel, 1, T, cur, -1, -1, -1, 1);
     return v;
 }
 
+// per-stream element counts of each layer's state (0: none)
+size_t layer_state(const MimiLayer& L) {
+    if (L.P > 1) return (size_t)L.Cout * L.P;
+    return (size_t)L.Cin * (L.NT - 1);
+}
+
+// the launch shape of a layer: row kernel (U <= 32) or tiled, with its shared memory
+struct ConvLaunch {
+    int rows;          // 1: k_mimi_conv_rows
+    int umax;          // rows: 4, 16 or 32
+    int rpc;           // rows: rows per CTA (8 or 16)
+    int CO;            // tiled: rows per CTA (4, 8 or 16)
+    dim3 grid;
+    size_t smem;
+};
+ConvLaunch conv_launch(const MimiLayer& L, int B) {
+    ConvLaunch c;
+    memset(&c, 0, sizeof c);
+    const int R = L.P * L.Cout, U = L.P > 1 ? L.T + 1 : L.T, KR = L.NT * L.Cin;
+    if (U <= 32) {
+        // a warp per row; two rows per warp where one would give more than two CTAs per SM,
+        // so fewer CTAs stage the same window
+        c.rows = 1;
+        c.umax = U <= 4 ? 4 : U <= 16 ? 16 : 32;
+        c.rpc = ((R + 7) / 8) * B > 2 * 152 ? 16 : 8;
+        c.grid = dim3((unsigned)((R + c.rpc - 1) / c.rpc), (unsigned)B);
+        c.smem = (((size_t)c.rpc * KR * 2 + 15) & ~(size_t)15) + 4u * (size_t)L.Cin * ((U + L.NT - 1) | 1);
+        return c;
+    }
+    // the most rows per CTA (fewest CTAs staging the same window) that still fills the SMs
+    const int tiles = (U + 31) / 32;
+    c.CO = 4;
+    for (int co = 16; co > 4; co /= 2)
+        if (tiles * ((R + co - 1) / co) * B >= 152) {
+            c.CO = co;
+            break;
+        }
+    c.grid = dim3((unsigned)tiles, (unsigned)((R + c.CO - 1) / c.CO), (unsigned)B);
+    c.smem = tiled_smem(L.Cin, L.NT, c.CO);
+    return c;
+}
+
+template <typename K, typename P>
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, const P& params) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, params);
+}
+
+size_t gemv_smem(int nq, int K) { return 4u * (size_t)(nq + 2) * K + 2u * GW * (size_t)K; }
+
 template <int PRO, int EPI>
 cudaError_t mgemv(const MGemvParams& p, cudaStream_t s) {
-    const size_t smem = 4u * (size_t)p.nq * p.K;
-    k_mimi_gemv<PRO, EPI><<<(p.R + 7) / 8, 256, smem, s>>>(p);
-    return cudaGetLastError();
+    const dim3 g((unsigned)((p.R + GW - 1) / GW)), b(32 * GW);
+    const size_t sm = gemv_smem(p.nq, p.K);
+    if (p.nq <= 2) return launch_pdl(k_mimi_gemv<PRO, EPI, 2>, g, b, sm, s, p);
+    if (p.nq <= 4) return launch_pdl(k_mimi_gemv<PRO, EPI, 4>, g, b, sm, s, p);
+    if (p.nq <= 8) return launch_pdl(k_mimi_gemv<PRO, EPI, 8>, g, b, sm, s, p);
+    return launch_pdl(k_mimi_gemv<PRO, EPI, 16>, g, b, sm, s, p);
 }
 
-size_t conv_w_smem(int Cin, int k, int T) { return 4u * (size_t)Cin * (k - 1 + T); }
-size_t conv_t_smem(int Cin, int k) { return 4u * (size_t)Cin * (TILE + k - 1); }
-size_t convtr_smem(int Cin, int s) { return 4u * (size_t)Cin * (TILE / s + 3); }
+// per-launch events of pm_mimi_profile (NULL when recording into a graph)
+struct MimiMarks {
+    std::vector<cudaEvent_t> ev;
+    std::vector<int32_t> kind;
+};
 
-pm_status launch_conv(pm_mimi_ctx* c, const MConvParams& q, int B, cudaStream_t s) {
-    if (q.T <= 16) {
-        k_mimi_conv_w<<<dim3((unsigned)((q.Cout + 7) / 8), (unsigned)B), 256, conv_w_smem(q.Cin, q.k, q.T), s>>>(q);
-    } else {
-        k_mimi_conv_t<<<dim3((unsigned)((q.T + TILE - 1) / TILE), (unsigned)((q.Cout + 7) / 8), (unsigned)B), 256,
-                        conv_t_smem(q.Cin, q.k), s>>>(q);
-    }
-    return cudaGetLastError() == cudaSuccess ? PM_OK : mfail(c, PM_ERR_CUDA, "mimi convolution launch");
-}
-
-pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s) {
+pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk = nullptr) {
+    auto mark = [&](int32_t kind) {
+        if (!mk) return;
+        cudaEvent_t e;
+        if (cudaEventCreate(&e) != cudaSuccess) return;
+        cudaEventRecord(e, s);
+        mk->ev.push_back(e);
+        mk->kind.push_back(kind);
+    };
     const pm_mimi_config& f = c->cfg;
     const MimiIdx ix = mimi_index(f);
     const int D = f.dim;
@@ -615,8 +931,10 @@ pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s) {
     fp.cb_dim = f.cb_dim;
     fp.card = f.card;
     fp.n_q = f.n_q;
-    k_mimi_front<<<dim3((unsigned)((D + 63) / 64), (unsigned)B), 256, 8u * f.cb_dim, s>>>(fp);
+    // the first launch follows the I/O copies, not a kernel: no programmatic dependency
+    k_mimi_front<<<dim3((unsigned)((D + 15) / 16), (unsigned)B), 256, 8u * f.cb_dim, s>>>(fp);
     if (cudaGetLastError() != cudaSuccess) return mfail(c, PM_ERR_CUDA, "k_mimi_front launch");
+    mark(PM_MIMI_K_FRONT);
     const int nq = 2 * B, RS = f.ctx + 1;
     const size_t kv_block = (size_t)f.B_max * f.heads * RS * MDH;
     for (int l = 0; l < f.n_layers; ++l) {
@@ -636,6 +954,7 @@ pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s) {
         g.R = 3 * D;
         g.K = D;
         if (mgemv<MP_LN, ME_STORE>(g, s) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi in_proj launch");
+        mark(PM_MIMI_K_IN_PROJ);
         MAttnParams a;
         memset(&a, 0, sizeof a);
         a.qkv = c->qkv;
@@ -649,8 +968,10 @@ pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s) {
         a.ctx = f.ctx;
         a.RS = RS;
         a.scale_log2 = (float)(1.4426950408889634 / sqrt((double)MDH));
-        k_mimi_attn<<<dim3((unsigned)B, (unsigned)f.heads), 256, 0, s>>>(a);
-        if (cudaGetLastError() != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi attention launch");
+        if (launch_pdl(k_mimi_attn, dim3((unsigned)B, (unsigned)f.heads), dim3(256), attn_smem(f.ctx), s, a) !=
+            cudaSuccess)
+            return mfail(c, PM_ERR_CUDA, "mimi attention launch");
+        mark(PM_MIMI_K_ATTN);
         g.W = c->w[w0 + 3];
         g.x = c->o;
         g.y = c->X;
@@ -658,6 +979,7 @@ pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s) {
         g.R = D;
         g.K = D;
         if (mgemv<MP_NONE, ME_SCALE_RES>(g, s) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi out_proj launch");
+        mark(PM_MIMI_K_OUT_PROJ);
         g.W = c->w[w0 + 7];
         g.x = c->X;
         g.ln_w = c->w[w0 + 5];
@@ -666,6 +988,7 @@ pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s) {
         g.R = f.ffn;
         g.K = D;
         if (mgemv<MP_LN, ME_GELU>(g, s) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi lin1 launch");
+        mark(PM_MIMI_K_LIN1);
         g.W = c->w[w0 + 8];
         g.x = c->hf;
         g.y = c->X;
@@ -673,83 +996,67 @@ pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s) {
         g.R = D;
         g.K = f.ffn;
         if (mgemv<MP_NONE, ME_SCALE_RES>(g, s) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi lin2 launch");
+        mark(PM_MIMI_K_LIN2);
     }
     // SEANet decoder
-    auto conv_params = [&](const float* in, float* out, int wi, float* state, int Cin, int Cout, int k, int T) {
+    for (size_t i = 0; i < c->layers.size(); ++i) {
+        const MimiLayer& L = c->layers[i];
         MConvParams q;
         memset(&q, 0, sizeof q);
-        q.in = in;
-        q.out = out;
-        q.W = c->w[wi];
-        q.bias = c->w[wi + 1];
-        q.state = state;
+        q.in = L.in_buf < 0 ? c->X : c->acts[L.in_buf];
+        q.in_pm = L.in_buf < 0;
+        q.out = L.out_raw < 0 ? nullptr : c->acts[L.out_raw];
+        q.out_act = L.out_act < 0 ? nullptr : c->acts[L.out_act];
+        q.res_in = L.res_buf < 0 ? nullptr : c->acts[L.res_buf];
+        q.io_out = L.pcm ? c->io : nullptr;  // the last convolution writes the caller's PCM
+        q.Wt = L.Wt;
+        q.bias = L.bias;
+        q.state = L.state;
         q.st = c->st;
         q.B_max = f.B_max;
-        q.Cin = Cin;
-        q.Cout = Cout;
-        q.k = k;
-        q.s = 1;
-        q.T = T;
-        q.elu_in = 1;
-        return q;
-    };
-    int T = 2, C = mimi_channels(f), si = 0;
-    MConvParams q = conv_params(c->X, c->acts[0], ix.dec0w, c->states[si++], D, C, f.kernel, T);
-    q.elu_in = 0;  // the first convolution takes the transformer output as it is
-    q.in_pm = 1;
-    pm_status ps = launch_conv(c, q, B, s);
-    if (ps) return ps;
-    const float* cur = c->acts[0];
-    for (int i = 0; i < f.n_ratios; ++i) {
-        const int r = f.ratios[i], co = C / 2, hd = co / f.compress, w = ix.stage0 + 6 * i;
-        float* y = c->acts[1 + 2 * i];
-        float* hmid = c->acts[2 + 2 * i];
-        q = conv_params(cur, y, w, c->states[si++], C, co, 2 * r, T);
-        q.s = r;
-        const int n_out = T * r + r;
-        k_mimi_convtr<<<dim3((unsigned)((n_out + TILE - 1) / TILE), (unsigned)((co + 7) / 8), (unsigned)B), 256,
-                        convtr_smem(C, r), s>>>(q);
-        if (cudaGetLastError() != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi transposed convolution launch");
-        T *= r;
-        // residual unit: y += conv_k1(ELU(conv_k(ELU(y))))
-        if ((ps = launch_conv(c, conv_params(y, hmid, w + 2, c->states[si++], co, hd, f.res_kernel, T), B, s))) return ps;
-        q = conv_params(hmid, y, w + 4, nullptr, hd, co, 1, T);
-        q.res = 1;
-        if ((ps = launch_conv(c, q, B, s))) return ps;
-        cur = y;
-        C = co;
+        q.Cin = L.Cin;
+        q.Cout = L.Cout;
+        q.NT = L.NT;
+        q.P = L.P;
+        q.T = L.T;
+        q.U = L.P > 1 ? L.T + 1 : L.T;
+        const ConvLaunch cl = conv_launch(L, B);
+        q.rows_per_cta = cl.rpc;
+        cudaError_t e;
+        if (cl.rows)
+            e = cl.umax == 4    ? launch_pdl(k_mimi_conv_rows<4>, cl.grid, dim3(256), cl.smem, s, q)
+                : cl.umax == 16 ? launch_pdl(k_mimi_conv_rows<16>, cl.grid, dim3(256), cl.smem, s, q)
+                                : launch_pdl(k_mimi_conv_rows<32>, cl.grid, dim3(256), cl.smem, s, q);
+        else
+            e = cl.CO == 16  ? launch_pdl(k_mimi_conv_tiled<16>, cl.grid, dim3(256), cl.smem, s, q)
+                : cl.CO == 8 ? launch_pdl(k_mimi_conv_tiled<8>, cl.grid, dim3(256), cl.smem, s, q)
+                             : launch_pdl(k_mimi_conv_tiled<4>, cl.grid, dim3(256), cl.smem, s, q);
+        if (e != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi convolution launch");
+        mark(i == 0 ? PM_MIMI_K_CONV_FIRST
+                    : i + 1 == c->layers.size() ? PM_MIMI_K_CONV_LAST
+                                                : (int32_t)(PM_MIMI_K_CONVTR + (i - 1) % 3));
     }
-    q = conv_params(cur, nullptr, ix.outw, c->states[si++], C, 1, f.last_kernel, T);
-    q.io_out = c->io;  // straight into the caller's PCM
-    if ((ps = launch_conv(c, q, B, s))) return ps;
     FinishParams fin;
     fin.st = c->st;
     fin.io = c->io;
     fin.B = B;
     fin.frame_samples = c->frame_samples;
-    k_mimi_finish<<<1, 256, 0, s>>>(fin);
-    if (cudaGetLastError() != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi finish launch");
+    if (launch_pdl(k_mimi_finish, dim3(1), dim3(256), 0, s, fin) != cudaSuccess)
+        return mfail(c, PM_ERR_CUDA, "mimi finish launch");
+    mark(PM_MIMI_K_FINISH);
     return PM_OK;
 }
 
 // largest dynamic shared memory any launch of this configuration asks for
 size_t mimi_smem_need(const pm_mimi_config& f) {
-    size_t m = 4u * 2 * f.B_max * (size_t)(f.dim > f.ffn ? f.dim : f.ffn);
-    int T = 2, C = mimi_channels(f);
-    auto conv = [&](int Cin, int k, int TT) {
-        const size_t v = TT <= 16 ? conv_w_smem(Cin, k, TT) : conv_t_smem(Cin, k);
-        if (v > m) m = v;
-    };
-    conv(f.dim, f.kernel, T);
-    for (int i = 0; i < f.n_ratios; ++i) {
-        const int r = f.ratios[i], co = C / 2;
-        if (convtr_smem(C, r) > m) m = convtr_smem(C, r);
-        T *= r;
-        conv(co, f.res_kernel, T);
-        conv(co / f.compress, 1, T);
-        C = co;
+    size_t m = gemv_smem(2 * f.B_max, f.dim > f.ffn ? f.dim : f.ffn);
+    if (attn_smem(f.ctx) > m) m = attn_smem(f.ctx);
+    for (const MimiLayer& L : seanet_layers(f)) {
+        const ConvLaunch cl = conv_launch(L, f.B_max);
+        if (cl.smem > m) m = cl.smem;
+        const ConvLaunch c1 = conv_launch(L, 1);
+        if (c1.smem > m) m = c1.smem;
     }
-    conv(C, f.last_kernel, T);
     return m;
 }
 
@@ -759,13 +1066,23 @@ cudaError_t mimi_func_attributes(size_t smem) {
     auto set = [&](const void* fn) {
         if (e == cudaSuccess) e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, v);
     };
-    set((const void*)k_mimi_gemv<MP_LN, ME_STORE>);
-    set((const void*)k_mimi_gemv<MP_LN, ME_GELU>);
-    set((const void*)k_mimi_gemv<MP_NONE, ME_SCALE_RES>);
-    set((const void*)k_mimi_conv_w);
-    set((const void*)k_mimi_conv_t);
-    set((const void*)k_mimi_convtr);
+#define PM_MIMI_SET_GEMV(NQ)                                   \
+    set((const void*)k_mimi_gemv<MP_LN, ME_STORE, NQ>);        \
+    set((const void*)k_mimi_gemv<MP_LN, ME_GELU, NQ>);         \
+    set((const void*)k_mimi_gemv<MP_NONE, ME_SCALE_RES, NQ>);
+    PM_MIMI_SET_GEMV(2)
+    PM_MIMI_SET_GEMV(4)
+    PM_MIMI_SET_GEMV(8)
+    PM_MIMI_SET_GEMV(16)
+#undef PM_MIMI_SET_GEMV
+    set((const void*)k_mimi_conv_rows<4>);
+    set((const void*)k_mimi_conv_rows<16>);
+    set((const void*)k_mimi_conv_rows<32>);
+    set((const void*)k_mimi_conv_tiled<4>);
+    set((const void*)k_mimi_conv_tiled<8>);
+    set((const void*)k_mimi_conv_tiled<16>);
     set((const void*)k_mimi_front);
+    set((const void*)k_mimi_attn);
     return e;
 }
 
@@ -817,6 +1134,7 @@ extern "C" pm_status pm_mimi_create(const pm_mimi_config* cfg, const void* const
         cudaGetLastError();
         return bail(PM_ERR_CUDA, "cudaFuncSetAttribute");
     }
+    c->layers = seanet_layers(f);
     // one allocation for state, activations and I/O
     const int BM = f.B_max, D = f.dim;
     void *p_frame, *p_pos, *p_abort, *p_status, *p_io, *p_codes, *p_prev, *p_X, *p_qkv, *p_o, *p_hf, *p_kv, *p_freq;
@@ -837,21 +1155,20 @@ extern "C" pm_status pm_mimi_create(const pm_mimi_config* cfg, const void* const
     };
     // activations: the first convolution's output, per stage the transposed convolution's
     // output (the residual stream) and the residual unit's middle
-    int T = 2, C = mimi_channels(f);
-    std::vector<size_t> act_sizes = {(size_t)BM * C * T};
-    for (int i = 0; i < f.n_ratios; ++i) {
-        const int co = C / 2;
-        T *= f.ratios[i];
-        act_sizes.push_back((size_t)BM * co * T);
-        act_sizes.push_back((size_t)BM * (co / f.compress) * T);
-        C = co;
+    std::vector<size_t> act_sizes(1 + 3 * f.n_ratios, 0);
+    for (const MimiLayer& L : c->layers) {
+        const size_t n = (size_t)BM * L.Cout * (L.P > 1 ? L.T * L.P : L.T);
+        for (int k : {L.out_raw, L.out_act})
+            if (k >= 0 && n > act_sizes[k]) act_sizes[k] = n;
     }
-    c->state_per_stream = state_sizes(f);
     c->acts.assign(act_sizes.size(), nullptr);
-    c->states.assign(c->state_per_stream.size(), nullptr);
     for (size_t i = 0; i < act_sizes.size(); ++i) items.push_back({reinterpret_cast<void**>(&c->acts[i]), 4u * act_sizes[i]});
-    for (size_t i = 0; i < c->states.size(); ++i)
+    c->states.assign(c->layers.size(), nullptr);
+    c->state_per_stream.assign(c->layers.size(), 0);
+    for (size_t i = 0; i < c->layers.size(); ++i) {
+        c->state_per_stream[i] = layer_state(c->layers[i]);
         items.push_back({reinterpret_cast<void**>(&c->states[i]), 4u * 2 * BM * c->state_per_stream[i]});
+    }
     size_t total = 0;
     for (auto& it : items) total = (total + 255) / 256 * 256 + (it.second + 15) / 16 * 16;
     if (cudaMalloc(&c->block, total) != cudaSuccess) {
@@ -878,6 +1195,33 @@ extern "C" pm_status pm_mimi_create(const pm_mimi_config* cfg, const void* const
     c->hf = (float*)p_hf;
     c->kv = (float*)p_kv;
     c->freq = (double*)p_freq;
+    // tap-major SEANet weights, re-laid from the caller's tensors once
+    std::vector<size_t> wt_off;
+    size_t wt_total = 0;
+    for (const MimiLayer& L : c->layers) {
+        wt_off.push_back(wt_total);
+        wt_total += ((size_t)L.P * L.Cout * L.NT * L.Cin + 7) / 8 * 8;
+    }
+    if (cudaMalloc((void**)&c->wt_block, 2 * wt_total) != cudaSuccess) {
+        cudaGetLastError();
+        return bail(PM_ERR_OOM, "device allocation (re-laid weights)");
+    }
+    for (size_t i = 0; i < c->layers.size(); ++i) {
+        MimiLayer& L = c->layers[i];
+        // canonical: dec.0 (w, b); per stage up (w, b), res w1, b1, w2, b2; dec.out (w, b)
+        int wi;
+        if (i == 0)
+            wi = ix.dec0w;
+        else if (i + 1 == c->layers.size())
+            wi = ix.outw;
+        else
+            wi = ix.stage0 + 6 * (int)((i - 1) / 3) + 2 * (int)((i - 1) % 3);
+        L.Wt = c->wt_block + wt_off[i];
+        L.bias = c->w[wi + 1];
+        L.state = c->states[i];
+        k_mimi_relayout<<<256, 256>>>(c->w[wi], c->wt_block + wt_off[i], L.Cin, L.Cout, L.NT, L.P);
+        if (cudaGetLastError() != cudaSuccess) return bail(PM_ERR_CUDA, "relayout launch");
+    }
     // RoPE frequency of pair j: theta^(-2j / 64)
     std::vector<double> fq(MDH / 2);
     for (int j = 0; j < MDH / 2; ++j) fq[j] = exp(-log((double)f.rope_theta) * (2.0 * j) / (double)MDH);
@@ -904,12 +1248,16 @@ extern "C" void pm_mimi_destroy(pm_mimi_ctx* c) {
     if (c->io_done) cudaEventDestroy(c->io_done);
     if (c->host_io) cudaFreeHost(c->host_io);
     if (c->cap) cudaStreamDestroy(c->cap);
+    if (c->wt_block) cudaFree(c->wt_block);
     if (c->block) cudaFree(c->block);
     delete c;
 }
 
-extern "C" pm_status pm_mimi_decode(pm_mimi_ctx* c, int B, const int32_t* codes, float* pcm) {
-    if (!c) return PM_ERR_ARG;
+namespace {
+
+// validate the call's pointers and codes, then copy the I/O block (and host codes) on the
+// context's stream; graph or eager launches follow
+pm_status mimi_stage(pm_mimi_ctx* c, int B, const int32_t* codes, float* pcm) {
     const pm_mimi_config& f = c->cfg;
     if (B < 1 || B > f.B_max || !codes || !pcm) return mfail(c, PM_ERR_ARG, "pm_mimi_decode: bad B or NULL pointer");
     if (cudaSetDevice(c->device) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "cudaSetDevice");
@@ -930,7 +1278,29 @@ extern "C" pm_status pm_mimi_decode(pm_mimi_ctx* c, int B, const int32_t* codes,
             if (codes[i] < 0 || codes[i] >= f.card)
                 return mfail(c, PM_ERR_INVALID_ID,
                              "pm_mimi_decode: code " + std::to_string(codes[i]) + " at " + std::to_string(i) + " out of range");
-    if (!c->graphs[B]) {
+    // the previous call's copies out of the pinned staging must be done before it is reused
+    if (cudaEventSynchronize(c->io_done) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "cudaEventSynchronize");
+    MimiIO io;
+    io.codes = dev_codes ? codes : c->codes_dev;
+    io.pcm = pcm_dev;
+    memcpy(c->host_io, &io, sizeof io);
+    if (!dev_codes) {
+        memcpy(c->host_io + 64, codes, 4u * B * f.n_q);
+        if (cudaMemcpyAsync(c->codes_dev, c->host_io + 64, 4u * B * f.n_q, cudaMemcpyHostToDevice, c->stream) != cudaSuccess)
+            return mfail(c, PM_ERR_CUDA, "codes copy");
+    }
+    if (cudaMemcpyAsync(c->io, c->host_io, sizeof io, cudaMemcpyHostToDevice, c->stream) != cudaSuccess ||
+        cudaEventRecord(c->io_done, c->stream) != cudaSuccess)
+        return mfail(c, PM_ERR_CUDA, "I/O block copy");
+    return PM_OK;
+}
+
+}  // namespace
+
+extern "C" pm_status pm_mimi_decode(pm_mimi_ctx* c, int B, const int32_t* codes, float* pcm) {
+    if (!c) return PM_ERR_ARG;
+    if (B >= 1 && B <= c->cfg.B_max && !c->graphs[B]) {
+        if (cudaSetDevice(c->device) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "cudaSetDevice");
         if (cudaStreamBeginCapture(c->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
             return mfail(c, PM_ERR_CUDA, "cudaStreamBeginCapture");
         pm_status st = record_mimi(c, B, c->cap);
@@ -944,21 +1314,40 @@ extern "C" pm_status pm_mimi_decode(pm_mimi_ctx* c, int B, const int32_t* codes,
         }
         cudaGraphDestroy(g);
     }
-    // the previous call's copies out of the pinned staging must be done before it is reused
-    if (cudaEventSynchronize(c->io_done) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "cudaEventSynchronize");
-    MimiIO io;
-    io.codes = dev_codes ? codes : c->codes_dev;
-    io.pcm = pcm_dev;
-    memcpy(c->host_io, &io, sizeof io);
-    if (!dev_codes) {
-        memcpy(c->host_io + 64, codes, 4u * B * f.n_q);
-        if (cudaMemcpyAsync(c->codes_dev, c->host_io + 64, 4u * B * f.n_q, cudaMemcpyHostToDevice, c->stream) != cudaSuccess)
-            return mfail(c, PM_ERR_CUDA, "codes copy");
-    }
-    if (cudaMemcpyAsync(c->io, c->host_io, sizeof io, cudaMemcpyHostToDevice, c->stream) != cudaSuccess ||
-        cudaEventRecord(c->io_done, c->stream) != cudaSuccess || cudaGraphLaunch(c->graphs[B], c->stream) != cudaSuccess)
-        return mfail(c, PM_ERR_CUDA, "mimi launch");
+    pm_status st = mimi_stage(c, B, codes, pcm);
+    if (st != PM_OK) return st;
+    if (cudaGraphLaunch(c->graphs[B], c->stream) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi launch");
     return PM_OK;
+}
+
+extern "C" pm_status pm_mimi_profile(pm_mimi_ctx* c, int B, const int32_t* codes, float* pcm, float* ms,
+                                     int32_t* kind, int n_max, int* n) {
+    if (!c) return PM_ERR_ARG;
+    if (!ms || !kind || !n || n_max < 1) return mfail(c, PM_ERR_ARG, "pm_mimi_profile: NULL output or n_max < 1");
+    pm_status st = mimi_stage(c, B, codes, pcm);
+    if (st != PM_OK) return st;
+    MimiMarks mk;
+    cudaEvent_t start;
+    if (cudaEventCreate(&start) != cudaSuccess || cudaEventRecord(start, c->stream) != cudaSuccess)
+        return mfail(c, PM_ERR_CUDA, "pm_mimi_profile: event");
+    st = record_mimi(c, B, c->stream, &mk);
+    const bool synced = cudaStreamSynchronize(c->stream) == cudaSuccess;
+    int k = 0;
+    cudaEvent_t prev = start;
+    for (size_t i = 0; i < mk.ev.size(); ++i) {
+        float t = 0.f;
+        if (synced && k < n_max && cudaEventElapsedTime(&t, prev, mk.ev[i]) == cudaSuccess) {
+            ms[k] = t;
+            kind[k] = mk.kind[i];
+            ++k;
+        }
+        prev = mk.ev[i];
+    }
+    for (auto e : mk.ev) cudaEventDestroy(e);
+    cudaEventDestroy(start);
+    *n = k;
+    if (st != PM_OK) return st;
+    return synced ? PM_OK : mfail(c, PM_ERR_CUDA, "pm_mimi_profile: synchronize");
 }
 
 extern "C" pm_status pm_mimi_reset(pm_mimi_ctx* c, const int32_t* mask) {
@@ -967,8 +1356,8 @@ extern "C" pm_status pm_mimi_reset(pm_mimi_ctx* c, const int32_t* mask) {
     const pm_mimi_config& f = c->cfg;
     const int BM = f.B_max;
     // a fresh stream: frame 0 at position 0, no previous latent, zero convolution history
-    // and zero transposed-convolution tails (the ring needs no clearing: the window only
-    // reaches positions written since the reset)
+    // and zero carried columns (the ring needs no clearing: the window only reaches
+    // positions written since the reset)
     for (int b = 0; b < BM; ++b) {
         if (mask && !mask[b]) continue;
         bool ok = cudaMemsetAsync(c->st.frame + b, 0, 4, c->stream) == cudaSuccess &&

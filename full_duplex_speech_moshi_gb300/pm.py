@@ -26,7 +26,9 @@ EXPORTS = ["pm_kv_cache_bytes", "pm_create", "pm_reset", "pm_set_positions", "pm
            "pm_snapshot", "pm_restore", "pm_prefill", "pm_set_wait_budget", "pm_generator_step"]
 # every symbol include/pm_mimi.h declares
 MIMI_EXPORTS = ["pm_mimi_tensor_count", "pm_mimi_create", "pm_mimi_decode", "pm_mimi_reset", "pm_mimi_status",
-                "pm_mimi_get_frames", "pm_mimi_last_error", "pm_mimi_destroy"]
+                "pm_mimi_get_frames", "pm_mimi_last_error", "pm_mimi_destroy", "pm_mimi_profile"]
+MIMI_KINDS = {0: "front", 1: "in_proj", 2: "attention", 3: "out_proj", 4: "lin1", 5: "lin2", 6: "conv_first",
+              7: "convtr", 8: "res_conv1", 9: "res_conv2", 10: "conv_last", 11: "finish"}
 PM_WAIT_BUDGET_DEFAULT = 0xFFFFFFFF
 KERNEL_KINDS = {0: "embed", 1: "qkv_rope", 2: "attention", 3: "out_proj", 4: "linear_in_swiglu",
                 5: "linear_out", 6: "text_head", 7: "frame_program", 8: "text_sample"}
@@ -142,6 +144,8 @@ def lib():
         L.pm_mimi_get_frames.argtypes = [vp, vp]
         L.pm_mimi_last_error.restype = C.c_char_p
         L.pm_mimi_last_error.argtypes = [vp]
+        L.pm_mimi_profile.restype = C.c_int
+        L.pm_mimi_profile.argtypes = [vp, C.c_int, vp, vp, vp, vp, C.c_int, C.POINTER(C.c_int)]
         L.pm_mimi_destroy.restype = None
         L.pm_mimi_destroy.argtypes = [vp]
         _lib = L
@@ -445,6 +449,18 @@ class MimiDecoder:
             import numpy as np
             codes = np.ascontiguousarray(codes, dtype=np.int32)
         self._check(self.L.pm_mimi_decode(self.h, int(B), _ptr(codes), _ptr(pcm)))
+
+    def profile(self, B: int, codes, pcm):
+        """One decode with per-launch device times: list of (kind name, ms)."""
+        if not hasattr(codes, "data_ptr"):
+            import numpy as np
+            codes = np.ascontiguousarray(codes, dtype=np.int32)
+        n_max = 2 + 5 * self.cfg.n_layers + 3 * self.cfg.n_ratios + 2
+        ms = (C.c_float * n_max)()
+        kind = (C.c_int32 * n_max)()
+        n = C.c_int(0)
+        self._check(self.L.pm_mimi_profile(self.h, int(B), _ptr(codes), _ptr(pcm), ms, kind, n_max, C.byref(n)))
+        return [(MIMI_KINDS[kind[i]], float(ms[i])) for i in range(n.value)]
 
     def reset(self, mask=None) -> None:
         m = None

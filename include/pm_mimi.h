@@ -111,6 +111,31 @@ pm_status pm_mimi_create(const pm_mimi_config* cfg, const void* const* tensors, 
  * captures that batch size's graph (synchronous; later calls only launch it). */
 pm_status pm_mimi_decode(pm_mimi_ctx* ctx, int B, const int32_t* codes, float* pcm);
 
+/* Kinds of the launches pm_mimi_profile times, in launch order: the front; per block
+ * in_proj, attention, out_proj, lin1, lin2; the first convolution; per stage the
+ * transposed convolution and the residual unit's two convolutions; the last convolution;
+ * the finishing kernel. */
+#define PM_MIMI_K_FRONT 0
+#define PM_MIMI_K_IN_PROJ 1
+#define PM_MIMI_K_ATTN 2
+#define PM_MIMI_K_OUT_PROJ 3
+#define PM_MIMI_K_LIN1 4
+#define PM_MIMI_K_LIN2 5
+#define PM_MIMI_K_CONV_FIRST 6
+#define PM_MIMI_K_CONVTR 7
+#define PM_MIMI_K_RES1 8
+#define PM_MIMI_K_RES2 9
+#define PM_MIMI_K_CONV_LAST 10
+#define PM_MIMI_K_FINISH 11
+
+/* pm_mimi_decode launched kernel by kernel (not from the graph) with a CUDA event after
+ * each launch, then synchronised: ms[i] is the device time between launch i's event and
+ * the previous one, kind[i] its PM_MIMI_K_* kind; *n receives the count (at most n_max;
+ * 2 + 5 n_layers + 3 n_ratios + 2 launches).  Same arguments, results and state advance
+ * as pm_mimi_decode.  For measurement, not for serving: it creates and destroys events. */
+pm_status pm_mimi_profile(pm_mimi_ctx* ctx, int B, const int32_t* codes, float* pcm, float* ms, int32_t* kind,
+                          int n_max, int* n);
+
 /* Return the streams whose mask entry is nonzero (all streams if mask is NULL; a host
  * array of B_max entries) to frame 0 with empty history, ordered on the context's stream. */
 pm_status pm_mimi_reset(pm_mimi_ctx* ctx, const int32_t* mask);
