@@ -329,3 +329,68 @@ def make_mimi_codes(shape: dict, T: int, B: int = 1, seed: int = 6000) -> np.nda
     s.update(shape)
     g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, T, B])))
     return g.integers(0, s["card"], size=(T, B, s["n_q"]), dtype=np.int64).astype(np.int32)
+
+
+def mimi_encoder_tensor_specs(shape: dict) -> List[Tuple[str, Tuple[int, ...]]]:
+    """Names and shapes of the encoder's tensors in their canonical order: the SEANet
+    encoder (stages in the reversed ratio order), the encoder transformer, the latent
+    downsampler, the quantizer input projections, then the codebooks."""
+    s = dict(MIMI_FULL)
+    s.update(shape)
+    d, f, C = s["dim"], s["ffn"], s["n_filters"]
+    t = [("enc.0.w", (C, 1, s["kernel"])), ("enc.0.b", (C,))]
+    for i, r in enumerate(reversed(s["ratios"])):
+        h = C // s["compress"]
+        t += [(f"enc.res{i}.w1", (h, C, s["res_kernel"])), (f"enc.res{i}.b1", (h,)), (f"enc.res{i}.w2", (C, h, 1)),
+              (f"enc.res{i}.b2", (C,)), (f"enc.down{i}.w", (2 * C, C, 2 * r)), (f"enc.down{i}.b", (2 * C,))]
+        C *= 2
+    t += [("enc.out.w", (d, C, s["last_kernel"])), ("enc.out.b", (d,))]
+    for l in range(s["n_layers"]):
+        p = f"etr.{l}."
+        t += [(p + "norm1.w", (d,)), (p + "norm1.b", (d,)), (p + "in_proj", (3 * d, d)), (p + "out_proj", (d, d)),
+              (p + "scale1", (d,)), (p + "norm2.w", (d,)), (p + "norm2.b", (d,)), (p + "lin1", (f, d)),
+              (p + "lin2", (d, f)), (p + "scale2", (d,))]
+    t += [("ds.weight", (d, d, s["up_kernel"])), ("q.sem.in", (s["cb_dim"], d)), ("q.ac.in", (s["cb_dim"], d))]
+    return t + [(f"q.codebook.{j}", (s["card"], s["cb_dim"])) for j in range(s["n_q"])]
+
+
+def make_mimi_encoder_weights(shape: dict, base_seed: int = 7000, codebook_seed: int = 5000,
+                              layer_scale: float = 0.05, threads: int | None = None) -> Dict[str, np.ndarray]:
+    """bf16 bits of every encoder tensor with the distributions of make_mimi_weights; tensor
+    i of the encoder order gets seed base_seed + i, except the codebooks, drawn exactly as
+    make_mimi_weights(shape, codebook_seed) draws them, so that one set of tables serves the
+    encoder and the decoder."""
+    threads = threads or min(32, os.cpu_count() or 1)
+    out: Dict[str, np.ndarray] = {}
+    with ThreadPoolExecutor(threads) as pool:
+        for i, (name, sh) in enumerate(mimi_encoder_tensor_specs(shape)):
+            if name.startswith("q.codebook"):
+                out[name] = normal_bf16(sh, 0.0, 1.0, codebook_seed + int(name.rsplit(".", 1)[1]), pool)
+                continue
+            if name.endswith(("norm1.w", "norm2.w")):
+                mean, std = 1.0, 0.1
+            elif name.endswith(("scale1", "scale2")):
+                mean, std = layer_scale, 0.1 * layer_scale
+            elif len(sh) == 1:
+                mean, std = 0.0, 0.02
+            else:
+                mean, std = 0.0, float(1.0 / np.sqrt(np.prod(sh[1:])))
+            out[name] = normal_bf16(sh, mean, std, base_seed + i, pool)
+    return out
+
+
+def make_mimi_pcm(n_samples: int, B: int = 1, seed: int = 8000, rate: int = 24000) -> np.ndarray:
+    """Seeded speech-band stand-in [B][n_samples] float32: per stream five sines (80-3000 Hz,
+    amplitudes 0.02-0.2, random phases) under a 3 Hz syllable-rate envelope, plus white noise
+    of standard deviation 0.01."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, n_samples, B])))
+    t = np.arange(n_samples) / rate
+    out = np.zeros((B, n_samples))
+    for b in range(B):
+        f = g.uniform(80.0, 3000.0, 5)
+        a = g.uniform(0.02, 0.2, 5)
+        ph = g.uniform(0.0, 2 * np.pi, 5)
+        env = 0.6 + 0.4 * np.sin(2 * np.pi * 3.0 * t + g.uniform(0.0, 2 * np.pi))
+        out[b] = env * (a[:, None] * np.sin(2 * np.pi * f[:, None] * t[None, :] + ph[:, None])).sum(0)
+        out[b] += 0.01 * g.standard_normal(n_samples)
+    return out.astype(np.float32)

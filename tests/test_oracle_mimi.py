@@ -13,7 +13,13 @@ mathematics fix:
   pos radians in pair 0;
 - attention: a one-position sequence passes v through; the window: a key ctx positions
   back has no effect;
-- the decoder is causal: decoding T + 2 frames reproduces the first T frames' samples.
+- the decoder is causal: decoding T + 2 frames reproduces the first T frames' samples;
+- encoder: the SEANet encoder, the encoder transformer and the dense downsampler sum to
+  the page's totals; the explainer's worked example quantises to its printed codes and
+  residual norms; a strided causal convolution equals the subsampled truncated
+  convolution (zero padding) and the replicate-padded downsampler repeats the first
+  position; exact ties take the lowest index; the acoustic chain does not depend on the
+  semantic branch; the encoder is causal frame by frame.
 """
 import json
 import math
@@ -38,10 +44,10 @@ def tiny_mimi_shape(**over):
     return M.MimiShape(**base)
 
 
-def random_weights(s, seed=1, ls=0.05):
+def random_weights(s, seed=1, ls=0.05, specs=None):
     rng = np.random.default_rng(seed)
     W = {}
-    for n, sh in M.tensor_specs(s):
+    for n, sh in (specs if specs is not None else M.tensor_specs(s)):
         if n.startswith("q.codebook"):
             v = rng.standard_normal(sh)
         elif n.endswith(("norm1.w", "norm2.w")):
@@ -185,3 +191,84 @@ def test_decoder_is_causal_frame_by_frame():
     assert a.shape == (3 * s.frame_samples,) and b.shape == (5 * s.frame_samples,)
     assert np.allclose(a, b[:a.size], rtol=0, atol=1e-12 * np.abs(b).max())  # (BLAS blocking may differ)
     assert np.all(np.isfinite(b)) and np.std(b) > 0
+
+
+# ------------------------------------------------------------------------------------
+# encoder
+# ------------------------------------------------------------------------------------
+
+def test_encoder_shapes_match_the_page_inventory():
+    g = json.load(open(os.path.join(GOLDEN, "mimi_inventory.json")))
+    s = M.MimiShape()
+    specs = dict(M.encoder_tensor_specs(s))
+    n = lambda pred: sum(int(np.prod(sh)) for k, sh in specs.items() if pred(k))
+    assert n(lambda k: k.startswith("enc.")) == g["seanet_encoder_params"]
+    assert n(lambda k: k.startswith("etr.")) == g["encoder_transformer_params"]
+    assert n(lambda k: k == "ds.weight") == g["dense_latent_downsampler_params"]
+    # the encoder's two input projections are the other half of the four projections
+    assert 2 * n(lambda k: k in ("q.sem.in", "q.ac.in")) == g["four_quantizer_projections_params"]
+    # the encoder downsamples by the reversed ratios: 4, 5, 6, 8
+    assert [specs[f"enc.down{i}.w"][2] // 2 for i in range(4)] == [4, 5, 6, 8]
+
+
+def test_rvq_encode_reproduces_the_worked_example():
+    g = json.load(open(os.path.join(GOLDEN, "rvq_worked_example.json")))
+    books = [np.array(c, np.float64) for c in g["codebooks"]]
+    codes, gaps, r = M.rvq_encode(books, np.array(g["x"]))
+    assert codes == g["codes_zero_based"]
+    assert np.allclose(np.array(g["x"]) - r, g["reconstruction"], atol=1e-15)
+    assert np.linalg.norm(r) < 1e-15 and all(gg > 0 for gg in gaps)
+    # a forced code replaces the choice and the chain continues from it
+    codes2, _, r2 = M.rvq_encode(books, np.array(g["x"]), forced=[1, -1, -1])
+    assert codes2[0] == 1 and np.allclose(r2, np.array(g["x"]) - books[0][1] - books[1][codes2[1]] - books[2][codes2[2]])
+
+
+def test_nearest_takes_the_lowest_index_on_an_exact_tie():
+    cb = np.array([[1.0, 0.0], [0.0, 1.0], [1.0, 0.0], [0.0, 1.0]])
+    assert M.nearest(cb, np.array([0.0, 1.0]))[0] == 1
+    i, gap = M.nearest(cb, np.array([0.5, 0.5]))   # all four at the same distance
+    assert i == 0 and gap == 0.0
+
+
+def test_strided_convolution_and_replicate_padding():
+    rng = np.random.default_rng(21)
+    for k, st in ((8, 4), (10, 5), (12, 6), (16, 8), (4, 2)):
+        x = rng.standard_normal((1, 6 * st))
+        w = rng.standard_normal((1, 1, k))
+        y = M.conv1d_causal_strided(x, w, np.array([0.25]), st)[0]
+        full = np.convolve(np.concatenate([np.zeros(k - st), x[0]]), w[0, 0][::-1], mode="valid")
+        assert y.shape == (6,) and np.allclose(y, full[::st][:6] + 0.25, rtol=1e-13, atol=1e-13)
+    # replicate: a constant input gives the constant sum of the taps everywhere
+    w = rng.standard_normal((3, 2, 4))
+    c = np.array([[1.5], [-0.5]])
+    y = M.conv1d_causal_strided(np.repeat(c, 8, axis=1), w, None, 2, replicate=True)
+    assert np.allclose(y, (w.sum(2) @ c).repeat(4, axis=1), rtol=1e-13)
+    # and the first output sees x0 three times, then x1
+    x = rng.standard_normal((2, 6))
+    y0 = M.conv1d_causal_strided(x, w, None, 2, replicate=True)[:, 0]
+    assert np.allclose(y0, (w[:, :, 0] + w[:, :, 1] + w[:, :, 2]) @ x[:, 0] + w[:, :, 3] @ x[:, 1], rtol=1e-13)
+
+
+def _tiny_encoder(seed):
+    s = tiny_mimi_shape()
+    return s, M.MimiEncoderOracle(s, random_weights(s, seed=seed, specs=M.encoder_tensor_specs(s)))
+
+
+def test_acoustic_chain_ignores_the_semantic_branch():
+    s, E = _tiny_encoder(22)
+    e = np.random.default_rng(23).standard_normal(s.dim)
+    codes, _ = E.quantize(e)
+    E.W["q.codebook.0"] = E.W["q.codebook.0"][::-1].copy()   # a different semantic table
+    E.W["q.sem.in"] = -E.W["q.sem.in"]
+    codes2, _ = E.quantize(e)
+    assert codes2[1:] == codes[1:]
+
+
+def test_encoder_is_causal_frame_by_frame():
+    s, E = _tiny_encoder(24)
+    pcm = np.random.default_rng(25).standard_normal(5 * s.frame_samples) * 0.3
+    a = E.latent(pcm[:3 * s.frame_samples])
+    b = E.latent(pcm)
+    assert a.shape == (3, s.dim) and b.shape == (5, s.dim)
+    assert np.allclose(a, b[:3], rtol=0, atol=1e-12 * np.abs(b).max())
+    assert np.array_equal(E.encode(pcm[:3 * s.frame_samples]), E.encode(pcm)[:3])
