@@ -48,8 +48,11 @@ constexpr int MDH = 64;    // transformer head width
 constexpr int GW = 4;      // rows (warps) per CTA of the transformer GEMVs
 
 struct MimiIO {
-    const int32_t* codes;  // [B][n_q]
-    float* pcm;            // [B][frame_samples]
+    const int32_t* codes;  // decoder: [B][n_q] input codes
+    float* pcm;            // decoder: [B][frame_samples] output PCM
+    const float* pcm_in;   // encoder: [B][frame_samples] input PCM
+    int32_t* codes_out;    // encoder: [B][n_q] output codes
+    float* latent_out;     // encoder: [B][dim] unquantised latent, or NULL
 };
 
 struct MimiState {
@@ -462,7 +465,10 @@ size_t attn_smem(int ctx) {
 // SEANet convolutions as phased products (see the file header)
 // ------------------------------------------------------------------------------------
 struct MConvParams {
-    const float* in;        // [B][Cin][T] (or [B][T][Cin] when in_pm), already activated
+    const float* in;        // [B][Cin][T S] (or [B][T S][Cin] when in_pm), already activated;
+                            // input channel ci' = ci S + p at position t is element t S + p of
+                            // channel ci (S = 1: plain channels)
+    const MimiIO* io_in;    // when set, the input is the caller's PCM (io_in->pcm_in)
     float* out;             // the output as computed, or NULL: Conv1d [B][Cout][T],
                             // ConvTranspose1d [B][Cout][T s]
     float* out_act;         // ELU of the output (what the next convolution reads), or NULL
@@ -473,19 +479,28 @@ struct MConvParams {
     float* state;           // Conv1d: [2][B_max][Cin][NT-1] activated inputs;
                             // ConvTranspose1d: [2][B_max][Cout][P] column T of the last call
     MimiState st;
-    int B_max, Cin, Cout, NT, P, T, U;  // P phases (1: Conv1d); U = T (Conv1d) or T + 1
+    int B_max, Cin, Cout, NT, P, T, U;  // P phases (1: Conv1d); U = T (Conv1d) or T + 1; Cin
+                                        // counts input channels ci' (S per original channel)
+    int S;                  // input positions folded into a channel (a stride-S convolution)
+    int rep;                // at a stream's first frame, positions before 0 repeat position 0
+    int no_bias, out_pm;    // no bias; output position-major [B][T][Cout]
     int in_pm, rows_per_cta;
 };
 
 // (activated) input of channel ci at position src of this call: a Conv1d takes src < 0 from
 // its state, a ConvTranspose1d reads zeros outside 0..T-1 (its carried column stands in)
 __device__ __forceinline__ float conv_load(const MConvParams& p, int b, int ci, int src, const float* st_old) {
-    if (src < 0)
+    const int c0 = ci / p.S, ph = ci - c0 * p.S, Cs = p.Cin / p.S, TS = p.T * p.S;
+    const float* in = p.io_in ? p.io_in->pcm_in : p.in;
+    if (src < 0) {
+        if (p.rep && p.st.frame[b] == 0)  // replicated left padding: the stream's first position
+            return p.in_pm ? in[(size_t)b * TS * Cs + c0] : in[((size_t)b * Cs + c0) * TS];
         return (p.P == 1 && p.NT > 1) ? st_old[((size_t)b * p.Cin + ci) * (p.NT - 1) + (p.NT - 1 + src)] : 0.f;
+    }
     if (src >= p.T) return 0.f;
-    return p.in_pm ? p.in[((size_t)b * p.T + src) * p.Cin + ci] : p.in[((size_t)b * p.Cin + ci) * p.T + src];
+    const int t = src * p.S + ph;
+    return p.in_pm ? in[((size_t)b * TS + t) * Cs + c0] : in[((size_t)b * Cs + c0) * TS + t];
 }
-
 
 // output of row (phase, co), column u: bias (+ carried column, + residual) -> the raw
 // output, its ELU, or the PCM
@@ -504,8 +519,8 @@ __device__ __forceinline__ void conv_put(const MConvParams& p, int b, int row, i
         n = u * p.P + ph;
         len = p.T * p.P;
     }
-    v += bf(p.bias, co);
-    const size_t o = ((size_t)b * p.Cout + co) * len + n;
+    if (!p.no_bias) v += bf(p.bias, co);
+    const size_t o = p.out_pm ? ((size_t)b * len + n) * p.Cout + co : ((size_t)b * p.Cout + co) * len + n;
     if (p.res_in) v += p.res_in[o];
     if (p.io_out) {
         p.io_out->pcm[o] = v;
@@ -679,10 +694,153 @@ __global__ void __launch_bounds__(256) k_mimi_finish(const FinishParams p) {
     if (threadIdx.x == 0) *p.st.abort = 0u;
 }
 
-// tap-major relayout, once at creation: Conv1d W [Cout][Cin][k] -> Wt [Cout][k][Cin];
-// ConvTranspose1d W [Cin][Cout][2s] -> Wt [s][Cout][2][Cin], tap m = 1 being kernel index p
-// (input u) and m = 0 kernel index p + s (input u - 1)
-__global__ void k_mimi_relayout(const uint16_t* W, uint16_t* Wt, int Cin, int Cout, int NT, int P) {
+// ------------------------------------------------------------------------------------
+// split residual vector quantisation of the latent: one cluster of RQ CTAs per stream
+// ------------------------------------------------------------------------------------
+constexpr int RQ = 8;
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// store to the same shared-memory variable of CTA `rank` of the cluster
+__device__ __forceinline__ void st_cluster_f32(float* local, uint32_t rank, float v) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(r), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u64(unsigned long long* local, uint32_t rank, unsigned long long v) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(r), "l"(v) : "memory");
+}
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+struct RvqParams {
+    const float* e;            // [B][dim] the latent after the downsampler
+    const uint16_t* w_sem;     // semantic input projection [cb_dim][dim]
+    const uint16_t* w_ac;      // acoustic input projection [cb_dim][dim]
+    const uint16_t* cb[16];    // codebooks [card][cb_dim]
+    const MimiIO* io;          // codes_out, latent_out
+    int dim, cb_dim, card, n_q;
+};
+
+// grid (RQ, B), clusters of RQ along x, 256 threads.  CTA k of a stream's cluster makes
+// projection rows k R2 .. (R2 = 2 cb_dim / RQ; the semantic rows first) and sends them to
+// every CTA of the cluster; then per level it scans entries k card/RQ .. of the codebook
+// (squared distance, a warp per entry), and the cluster agrees on the smallest
+// (distance, index) key through shared-memory slots and a cluster barrier.  The semantic
+// search runs beside the first acoustic level; each acoustic level subtracts the chosen
+// entry from the residual all CTAs hold.
+__global__ void __launch_bounds__(256) k_mimi_rvq(const RvqParams p) {
+    extern __shared__ __align__(16) uint8_t smraw[];
+    __shared__ unsigned long long keys[2][2][RQ];  // [phase parity][search][rank]
+    __shared__ unsigned long long wkey[2][8];
+    const int R2 = 2 * p.cb_dim / RQ;
+    uint16_t* wsm = reinterpret_cast<uint16_t*>(smraw);                  // [R2][dim]
+    float* es = reinterpret_cast<float*>(smraw + (size_t)R2 * p.dim * 2); // [dim]
+    float* z = es + p.dim;                                               // [2][cb_dim]: semantic, acoustic residual
+    const uint32_t rank = cluster_rank();
+    const int b = blockIdx.y, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int per = p.card / RQ, e0 = (int)rank * per;
+    pdl_trigger();
+    // every CTA of the cluster must be running before any stores into it: arrive now, wait
+    // before the first remote store
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    {
+        const int r0 = (int)rank * R2;  // projection rows of this CTA
+        const int n8 = R2 * p.dim / 8;
+        batched_copy<4>(
+            n8,
+            [&](int i) {
+                const int row = r0 + (i * 8) / p.dim, k = (i * 8) % p.dim;
+                const uint16_t* w = row < p.cb_dim ? p.w_sem + (size_t)row * p.dim : p.w_ac + (size_t)(row - p.cb_dim) * p.dim;
+                return __ldg(reinterpret_cast<const uint4*>(w + k));
+            },
+            [&](int i, uint4 v) { reinterpret_cast<uint4*>(wsm)[i] = v; });
+        if (t < p.n_q) prefetch_l2_bulk(p.cb[t] + (size_t)e0 * p.cb_dim, (uint32_t)(per * p.cb_dim * 2));
+    }
+    pdl_wait();
+    for (int k = t; k < p.dim; k += blockDim.x) es[k] = p.e[(size_t)b * p.dim + k];
+    __syncthreads();
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    // input projections: warp w makes rows w, w + 8, ... of this CTA's R2 and stores each
+    // into every CTA of the cluster
+    for (int rr = warp; rr < R2; rr += 8) {
+        const uint16_t* w = wsm + (size_t)rr * p.dim;
+        float a = 0.f;
+        for (int k = 4 * lane; k < p.dim; k += 128) {
+            const uint2 wv = *reinterpret_cast<const uint2*>(w + k);
+            const float4 x = *reinterpret_cast<const float4*>(es + k);
+            a = fmaf(bf16lo(wv.x), x.x, fmaf(bf16hi(wv.x), x.y, fmaf(bf16lo(wv.y), x.z, fmaf(bf16hi(wv.y), x.w, a))));
+        }
+        a = warp_sum(a);
+        const int row = (int)rank * R2 + rr;
+        if (lane < RQ) st_cluster_f32(z + row, (uint32_t)lane, a);  // row < cb_dim: semantic
+    }
+    cluster_sync();
+    for (int ph = 0; ph + 1 < p.n_q; ++ph) {
+        const int ns = ph == 0 ? 2 : 1;
+        for (int sidx = 0; sidx < ns; ++sidx) {
+            // ph 0: search 0 = semantic codebook 0 on z[0], search 1 = acoustic codebook 1
+            const int j = ph == 0 ? sidx : ph + 1;
+            const float* v = z + (j == 0 ? 0 : p.cb_dim);
+            unsigned long long best = ~0ull;
+            for (int en = warp; en < per; en += 8) {
+                const int idx = e0 + en;
+                const uint16_t* c = p.cb[j] + (size_t)idx * p.cb_dim;
+                float d = 0.f;
+                for (int k = 8 * lane; k < p.cb_dim; k += 256) {
+                    const uint4 cv = *reinterpret_cast<const uint4*>(c + k);
+                    const float4 x0 = *reinterpret_cast<const float4*>(v + k);
+                    const float4 x1 = *reinterpret_cast<const float4*>(v + k + 4);
+                    const float d0 = x0.x - bf16lo(cv.x), d1 = x0.y - bf16hi(cv.x), d2 = x0.z - bf16lo(cv.y),
+                                d3 = x0.w - bf16hi(cv.y), d4 = x1.x - bf16lo(cv.z), d5 = x1.y - bf16hi(cv.z),
+                                d6 = x1.z - bf16lo(cv.w), d7 = x1.w - bf16hi(cv.w);
+                    d = fmaf(d0, d0, fmaf(d1, d1, fmaf(d2, d2, fmaf(d3, d3, d))));
+                    d = fmaf(d4, d4, fmaf(d5, d5, fmaf(d6, d6, fmaf(d7, d7, d))));
+                }
+                d = warp_sum(d);
+                const unsigned long long key = ((unsigned long long)float_order_key(d) << 32) | (uint32_t)idx;
+                best = key < best ? key : best;
+            }
+            if (lane == 0) wkey[sidx][warp] = best;
+        }
+        __syncthreads();
+        if (t < ns) {
+            unsigned long long m = wkey[t][0];
+            for (int w = 1; w < 8; ++w) m = wkey[t][w] < m ? wkey[t][w] : m;
+            for (uint32_t r = 0; r < RQ; ++r) st_cluster_u64(&keys[ph & 1][t][rank], r, m);
+        }
+        cluster_sync();
+        for (int sidx = 0; sidx < ns; ++sidx) {
+            unsigned long long m = keys[ph & 1][sidx][0];
+            for (int r = 1; r < RQ; ++r) m = keys[ph & 1][sidx][r] < m ? keys[ph & 1][sidx][r] : m;
+            const int code = (int)(uint32_t)(m & 0xFFFFFFFFull);
+            const int j = ph == 0 ? sidx : ph + 1;
+            if (rank == 0 && t == 0) p.io->codes_out[(size_t)b * p.n_q + j] = code;
+            if (j > 0)  // the acoustic residual moves on
+                for (int k = t; k < p.cb_dim; k += blockDim.x) z[p.cb_dim + k] -= bf(p.cb[j], (size_t)code * p.cb_dim + k);
+        }
+        __syncthreads();
+    }
+    if (rank == 0 && p.io->latent_out)
+        for (int k = t; k < p.dim; k += blockDim.x) p.io->latent_out[(size_t)b * p.dim + k] = es[k];
+}
+
+size_t rvq_smem(int dim, int cb_dim) { return (size_t)(2 * cb_dim / RQ) * dim * 2 + 4u * (size_t)(dim + 2 * cb_dim); }
+
+// tap-major relayout, once at creation: Conv1d W [Cout][Cin/S][NT S] -> Wt [Cout][NT][Cin]
+// with input channel ci' = ci S + p taking kernel index m S + p (S = 1: Wt[co][m][ci] =
+// W[co][ci][m]); ConvTranspose1d W [Cin][Cout][2s] -> Wt [s][Cout][2][Cin], tap m = 1 being
+// kernel index p (input u) and m = 0 kernel index p + s (input u - 1)
+__global__ void k_mimi_relayout(const uint16_t* W, uint16_t* Wt, int Cin, int Cout, int NT, int P, int S) {
     const size_t n = (size_t)P * Cout * NT * Cin;
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const int ci = (int)(i % Cin);
@@ -690,7 +848,8 @@ __global__ void k_mimi_relayout(const uint16_t* W, uint16_t* Wt, int Cin, int Co
         const int m = (int)(rest % NT);
         const size_t row = rest / NT;
         if (P == 1) {
-            Wt[i] = W[(row * Cin + ci) * NT + m];
+            const int c0 = ci / S, ph = ci - c0 * S;
+            Wt[i] = W[(row * (Cin / S) + c0) * ((size_t)NT * S) + (size_t)m * S + ph];
         } else {
             const int ph = (int)(row / Cout), co = (int)(row % Cout), k = 2 * P;
             Wt[i] = W[((size_t)ci * Cout + co) * k + ph + (1 - m) * P];
@@ -706,36 +865,47 @@ __global__ void k_mimi_relayout(const uint16_t* W, uint16_t* Wt, int Cin, int Co
 // =====================================================================================
 using namespace pm;
 
-struct MimiLayer {         // one SEANet convolution, as recorded
+// buffer codes of a convolution's input / outputs: >= 0 an activation buffer, or
+constexpr int BUF_NONE = -100;  // no such output
+constexpr int BUF_X = -1;       // the transformer residual stream [B][2][dim] (position-major)
+constexpr int BUF_IO = -2;      // the caller's PCM (decoder output, encoder input)
+constexpr int BUF_LAT = -3;     // the encoder's latent [B][dim]
+
+struct MimiLayer {         // one SEANet (or resampling) convolution, as recorded
     const uint16_t* Wt;    // tap-major weights
     const uint16_t* bias;
     float* state;
-    int Cin, Cout, NT, P, T;
-    int in_buf;            // input buffer (activated); -1: the transformer output, position-major
-    int out_raw, out_act;  // buffers for the output and for its ELU (-1: none)
-    int res_buf;           // buffer added to the output (-1: none)
-    int pcm;               // the output is the caller's PCM
+    int Cin, Cout, NT, P, T, S;  // Cin counts folded input channels (S per original channel)
+    int rep, no_bias;
+    int in_buf;            // input buffer (activated)
+    int out_raw, out_act;  // buffers for the output and for its ELU
+    int res_buf;           // buffer added to the output
+    int wi;                // canonical index of the weight (the bias follows it)
+    int kind;              // PM_MIMI_K_* of the launch
 };
 
 struct pm_mimi_ctx {
     pm_mimi_config cfg{};
+    int encoder = 0;                     // 0: decoder context, 1: encoder context
     int device = 0;
     int frame_samples = 0;
     cudaStream_t stream = nullptr, cap = nullptr;
     std::vector<const uint16_t*> w;      // canonical tensors
     void* block = nullptr;
-    uint16_t* wt_block = nullptr;        // tap-major SEANet weights
+    uint16_t* wt_block = nullptr;        // tap-major convolution weights
     MimiState st{};
     MimiIO* io = nullptr;                // device I/O block
-    int32_t* codes_dev = nullptr;        // host codes staged here
-    uint8_t* host_io = nullptr;          // pinned: I/O block image + host codes
+    int32_t* codes_dev = nullptr;        // decoder: host codes staged here
+    float* pcm_dev = nullptr;            // encoder: host PCM staged here
+    uint8_t* host_io = nullptr;          // pinned: I/O block image + host codes / PCM
+    size_t host_io_bytes = 0;
     cudaEvent_t io_done = nullptr;
-    float *prev = nullptr, *X = nullptr, *qkv = nullptr, *o = nullptr, *hf = nullptr, *kv = nullptr;
+    float *prev = nullptr, *X = nullptr, *qkv = nullptr, *o = nullptr, *hf = nullptr, *kv = nullptr, *lat = nullptr;
     double* freq = nullptr;
     std::vector<float*> acts;            // SEANet activations
-    std::vector<float*> states;          // SEANet streaming state [2][B_max][per_stream]
+    std::vector<float*> states;          // streaming state per layer [2][B_max][per_stream]
     std::vector<size_t> state_per_stream;
-    std::vector<MimiLayer> layers;       // SEANet convolutions in order
+    std::vector<MimiLayer> layers;       // convolutions in order
     std::vector<cudaGraphExec_t> graphs; // per B
     std::string err;
 };
@@ -751,7 +921,7 @@ pm_status mfail(pm_mimi_ctx* c, pm_status s, const std::string& m) {
     return s;
 }
 
-// positions of each group in the canonical tensor order
+// positions of each group in the decoder's canonical tensor order
 struct MimiIdx {
     int cb0, sem_out, ac_out, up, layer0, dec0w, stage0, outw, total;
 };
@@ -769,6 +939,24 @@ MimiIdx mimi_index(const pm_mimi_config& c) {
     return x;
 }
 
+// positions in the encoder's canonical order
+struct MimiEncIdx {
+    int enc0w, stage0, outw, layer0, ds, sem_in, ac_in, cb0, total;
+};
+MimiEncIdx mimi_enc_index(const pm_mimi_config& c) {
+    MimiEncIdx x;
+    x.enc0w = 0;
+    x.stage0 = 2;
+    x.outw = 2 + 6 * c.n_ratios;
+    x.layer0 = x.outw + 2;
+    x.ds = x.layer0 + 10 * c.n_layers;
+    x.sem_in = x.ds + 1;
+    x.ac_in = x.ds + 2;
+    x.cb0 = x.ds + 3;
+    x.total = x.cb0 + c.n_q;
+    return x;
+}
+
 const char* mimi_check(const pm_mimi_config* c) {
     if (c->B_max < 1 || c->B_max > PM_MIMI_MAX_B) return "B_max outside 1..8";
     if (c->heads < 1 || c->dim != c->heads * MDH) return "dim must be 64 x heads";
@@ -777,7 +965,7 @@ const char* mimi_check(const pm_mimi_config* c) {
     if (c->cb_dim < 8 || c->cb_dim % 8 != 0 || c->cb_dim > 4096) return "cb_dim must be a multiple of 8 (<= 4096)";
     if (c->card < 1 || c->n_q < 2 || c->n_q > 16) return "codebooks: card >= 1, 2 <= n_q <= 16";
     if (c->n_layers < 0 || c->ctx < 2) return "transformer: n_layers >= 0, ctx >= 2";
-    if (c->up_kernel != 4 || c->up_stride != 2) return "the latent upsampler must be kernel 4, stride 2";
+    if (c->up_kernel != 4 || c->up_stride != 2) return "the latent resamplers must be kernel 4, stride 2";
     if (c->n_ratios < 1 || c->n_ratios > PM_MIMI_MAX_RATIOS || c->n_filters < 1) return "SEANet stages";
     for (int i = 0; i < c->n_ratios; ++i)
         if (c->ratios[i] < 1 || c->ratios[i] > 16) return "SEANet ratios must be 1..16";
@@ -788,44 +976,86 @@ const char* mimi_check(const pm_mimi_config* c) {
     return nullptr;
 }
 
-// the SEANet convolutions in order, with their shapes and buffers (weights filled later).
-// Every convolution after the first reads an ELU, so each producer writes its output
-// activated (the ELU computed once per element); the transposed convolution also keeps its
-// raw output, which the residual unit's second convolution adds.  Buffers: 0 = first
-// convolution (activated); stage i: 1 + 3i raw y, 2 + 3i ELU(y) -- reused for ELU of the
-// residual sum, the next stage's input, once the unit's first convolution has read it --,
-// 3 + 3i the unit's activated middle.
+// the encoder's extra constraints (the cluster search and its projection slices)
+const char* mimi_encoder_check(const pm_mimi_config* c) {
+    if (c->card % RQ != 0) return "the encoder needs card to be a multiple of 8";
+    if ((2 * c->cb_dim) % RQ != 0 || c->cb_dim % 8 != 0) return "the encoder needs cb_dim a multiple of 8";
+    if (c->dim % 128 != 0) return "the encoder needs dim a multiple of 128";
+    return nullptr;
+}
+
+MimiLayer make_layer(int Cin, int Cout, int NT, int P, int T, int S, int in, int raw, int act, int res, int wi, int kind) {
+    MimiLayer L;
+    memset(&L, 0, sizeof L);
+    L.Cin = Cin;
+    L.Cout = Cout;
+    L.NT = NT;
+    L.P = P;
+    L.T = T;
+    L.S = S;
+    L.in_buf = in;
+    L.out_raw = raw;
+    L.out_act = act;
+    L.res_buf = res;
+    L.wi = wi;
+    L.kind = kind;
+    return L;
+}
+
+// the decoder's SEANet convolutions in order.  Every convolution after the first reads an
+// ELU, so each producer writes its output activated (the ELU computed once per element);
+// the transposed convolution also keeps its raw output, which the residual unit's second
+// convolution adds.  Buffers: 0 = first convolution (activated); stage i: 1 + 3i raw y,
+// 2 + 3i ELU(y) -- reused for ELU of the residual sum, the next stage's input, once the
+// unit's first convolution has read it --, 3 + 3i the unit's activated middle.
 std::vector<MimiLayer> seanet_layers(const pm_mimi_config& f) {
+    const MimiIdx ix = mimi_index(f);
     std::vector<MimiLayer> v;
-    auto add = [&](int Cin, int Cout, int NT, int P, int T, int in, int raw, int act, int res, int pcm) {
-        MimiLayer L;
-        memset(&L, 0, sizeof L);
-        L.Cin = Cin;
-        L.Cout = Cout;
-        L.NT = NT;
-        L.P = P;
-        L.T = T;
-        L.in_buf = in;
-        L.out_raw = raw;
-        L.out_act = act;
-        L.res_buf = res;
-        L.pcm = pcm;
-        v.push_back(L);
-    };
     int C = mimi_channels(f), T = 2;
-    add(f.dim, C, f.kernel, 1, T, -1, -1, 0, -1, 0);
+    v.push_back(make_layer(f.dim, C, f.kernel, 1, T, 1, BUF_X, BUF_NONE, 0, BUF_NONE, ix.dec0w, PM_MIMI_K_CONV_FIRST));
     int cur = 0;
     for (int i = 0; i < f.n_ratios; ++i) {
-        const int r = f.ratios[i], co = C / 2, h = co / f.compress;
+        const int r = f.ratios[i], co = C / 2, h = co / f.compress, w = ix.stage0 + 6 * i;
         const int yraw = 1 + 3 * i, yact = 2 + 3 * i, mid = 3 + 3 * i;
-        add(C, co, 2, r, T, cur, yraw, yact, -1, 0);                // ConvTranspose1d, kernel 2r, stride r
+        v.push_back(make_layer(C, co, 2, r, T, 1, cur, yraw, yact, BUF_NONE, w, PM_MIMI_K_CONVTR));
         T *= r;
-        add(co, h, f.res_kernel, 1, T, yact, -1, mid, -1, 0);       // residual unit
-        add(h, co, 1, 1, T, mid, -1, yact, yraw, 0);
+        v.push_back(make_layer(co, h, f.res_kernel, 1, T, 1, yact, BUF_NONE, mid, BUF_NONE, w + 2, PM_MIMI_K_RES1));
+        v.push_back(make_layer(h, co, 1, 1, T, 1, mid, BUF_NONE, yact, yraw, w + 4, PM_MIMI_K_RES2));
         cur = yact;
         C = co;
     }
-    add(C, 1, f.last_kernel, 1, T, cur, -1, -1, -1, 1);
+    v.push_back(make_layer(C, 1, f.last_kernel, 1, T, 1, cur, BUF_IO, BUF_NONE, BUF_NONE, ix.outw, PM_MIMI_K_CONV_LAST));
+    return v;
+}
+
+// the encoder's convolutions in order: the SEANet encoder (stages in the reversed ratio
+// order, each a residual unit then a stride-r convolution of kernel 2r folded as S = r input
+// positions per channel and two taps), the last convolution into the transformer stream,
+// and, recorded after the transformer, the latent downsampler.  Buffers per stage i: 3i raw
+// x, 3i + 1 ELU(x) (reused for ELU of the residual sum), 3i + 2 the unit's activated middle;
+// the stage's strided convolution writes stage i + 1's raw and ELU.
+std::vector<MimiLayer> seanet_encoder_layers(const pm_mimi_config& f) {
+    const MimiEncIdx ix = mimi_enc_index(f);
+    std::vector<MimiLayer> v;
+    int C = f.n_filters, T = 2;
+    for (int i = 0; i < f.n_ratios; ++i) T *= f.ratios[i];
+    v.push_back(make_layer(1, C, f.kernel, 1, T, 1, BUF_IO, 0, 1, BUF_NONE, ix.enc0w, PM_MIMI_K_CONV_FIRST));
+    for (int i = 0; i < f.n_ratios; ++i) {
+        const int r = f.ratios[f.n_ratios - 1 - i], h = C / f.compress, w = ix.stage0 + 6 * i;
+        const int xraw = 3 * i, xact = 3 * i + 1, mid = 3 * i + 2;
+        v.push_back(make_layer(C, h, f.res_kernel, 1, T, 1, xact, BUF_NONE, mid, BUF_NONE, w, PM_MIMI_K_RES1));
+        v.push_back(make_layer(h, C, 1, 1, T, 1, mid, BUF_NONE, xact, xraw, w + 2, PM_MIMI_K_RES2));
+        v.push_back(make_layer(C * r, 2 * C, 2, 1, T / r, r, xact, 3 * (i + 1), 3 * (i + 1) + 1, BUF_NONE, w + 4,
+                               PM_MIMI_K_DOWN));
+        C *= 2;
+        T /= r;
+    }
+    v.push_back(make_layer(C, f.dim, f.last_kernel, 1, T, 1, 3 * f.n_ratios + 1, BUF_X, BUF_NONE, BUF_NONE, ix.outw,
+                           PM_MIMI_K_CONV_LAST));
+    MimiLayer ds = make_layer(2 * f.dim, f.dim, 2, 1, 1, 2, BUF_X, BUF_LAT, BUF_NONE, BUF_NONE, ix.ds, PM_MIMI_K_RESAMPLE);
+    ds.rep = 1;
+    ds.no_bias = 1;
+    v.push_back(ds);
     return v;
 }
 
@@ -844,18 +1074,21 @@ struct ConvLaunch {
     dim3 grid;
     size_t smem;
 };
+size_t rows_smem(const MimiLayer& L, int rpc, int U) {
+    return (((size_t)rpc * L.NT * L.Cin * 2 + 15) & ~(size_t)15) + 4u * (size_t)L.Cin * ((U + L.NT - 1) | 1);
+}
 ConvLaunch conv_launch(const MimiLayer& L, int B) {
     ConvLaunch c;
     memset(&c, 0, sizeof c);
-    const int R = L.P * L.Cout, U = L.P > 1 ? L.T + 1 : L.T, KR = L.NT * L.Cin;
+    const int R = L.P * L.Cout, U = L.P > 1 ? L.T + 1 : L.T;
     if (U <= 32) {
-        // a warp per row; two rows per warp where one would give more than two CTAs per SM,
-        // so fewer CTAs stage the same window
+        // a warp per row; two rows per warp where one would give more than two CTAs per SM
+        // (fewer CTAs stage the same window) and the weights still fit
         c.rows = 1;
         c.umax = U <= 4 ? 4 : U <= 16 ? 16 : 32;
-        c.rpc = ((R + 7) / 8) * B > 2 * 152 ? 16 : 8;
+        c.rpc = ((R + 7) / 8) * B > 2 * 152 && rows_smem(L, 16, U) <= 200u * 1024u ? 16 : 8;
         c.grid = dim3((unsigned)((R + c.rpc - 1) / c.rpc), (unsigned)B);
-        c.smem = (((size_t)c.rpc * KR * 2 + 15) & ~(size_t)15) + 4u * (size_t)L.Cin * ((U + L.NT - 1) | 1);
+        c.smem = rows_smem(L, c.rpc, U);
         return c;
     }
     // the most rows per CTA (fewest CTAs staging the same window) that still fills the SMs
@@ -898,49 +1131,28 @@ cudaError_t mgemv(const MGemvParams& p, cudaStream_t s) {
     return launch_pdl(k_mimi_gemv<PRO, EPI, 16>, g, b, sm, s, p);
 }
 
-// per-launch events of pm_mimi_profile (NULL when recording into a graph)
+// per-launch events of the profiling calls (NULL when recording into a graph)
 struct MimiMarks {
     std::vector<cudaEvent_t> ev;
     std::vector<int32_t> kind;
-};
-
-pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk = nullptr) {
-    auto mark = [&](int32_t kind) {
-        if (!mk) return;
+    void mark(cudaStream_t s, int32_t k) {
         cudaEvent_t e;
         if (cudaEventCreate(&e) != cudaSuccess) return;
         cudaEventRecord(e, s);
-        mk->ev.push_back(e);
-        mk->kind.push_back(kind);
-    };
+        ev.push_back(e);
+        kind.push_back(k);
+    }
+};
+
+// a transformer stack over the context's X: layer0 = canonical index of block 0's norm1.w
+pm_status record_transformer(pm_mimi_ctx* c, int B, cudaStream_t s, int layer0, MimiMarks* mk) {
     const pm_mimi_config& f = c->cfg;
-    const MimiIdx ix = mimi_index(f);
-    const int D = f.dim;
-    FrontParams fp;
-    memset(&fp, 0, sizeof fp);
-    fp.io = c->io;
-    fp.st = c->st;
-    for (int j = 0; j < f.n_q; ++j) fp.cb[j] = c->w[ix.cb0 + j];
-    fp.sem_out = c->w[ix.sem_out];
-    fp.ac_out = c->w[ix.ac_out];
-    fp.up = c->w[ix.up];
-    fp.prev = c->prev;
-    fp.X = c->X;
-    fp.B_max = f.B_max;
-    fp.dim = D;
-    fp.cb_dim = f.cb_dim;
-    fp.card = f.card;
-    fp.n_q = f.n_q;
-    // the first launch follows the I/O copies, not a kernel: no programmatic dependency
-    k_mimi_front<<<dim3((unsigned)((D + 15) / 16), (unsigned)B), 256, 8u * f.cb_dim, s>>>(fp);
-    if (cudaGetLastError() != cudaSuccess) return mfail(c, PM_ERR_CUDA, "k_mimi_front launch");
-    mark(PM_MIMI_K_FRONT);
-    const int nq = 2 * B, RS = f.ctx + 1;
+    const int D = f.dim, nq = 2 * B, RS = f.ctx + 1;
     const size_t kv_block = (size_t)f.B_max * f.heads * RS * MDH;
     for (int l = 0; l < f.n_layers; ++l) {
         // canonical per-block order: norm1.w, norm1.b, in_proj, out_proj, scale1, norm2.w,
         // norm2.b, lin1, lin2, scale2
-        const int w0 = ix.layer0 + 10 * l;
+        const int w0 = layer0 + 10 * l;
         MGemvParams g;
         memset(&g, 0, sizeof g);
         g.st = c->st;
@@ -954,7 +1166,7 @@ pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk = nul
         g.R = 3 * D;
         g.K = D;
         if (mgemv<MP_LN, ME_STORE>(g, s) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi in_proj launch");
-        mark(PM_MIMI_K_IN_PROJ);
+        if (mk) mk->mark(s, PM_MIMI_K_IN_PROJ);
         MAttnParams a;
         memset(&a, 0, sizeof a);
         a.qkv = c->qkv;
@@ -971,7 +1183,7 @@ pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk = nul
         if (launch_pdl(k_mimi_attn, dim3((unsigned)B, (unsigned)f.heads), dim3(256), attn_smem(f.ctx), s, a) !=
             cudaSuccess)
             return mfail(c, PM_ERR_CUDA, "mimi attention launch");
-        mark(PM_MIMI_K_ATTN);
+        if (mk) mk->mark(s, PM_MIMI_K_ATTN);
         g.W = c->w[w0 + 3];
         g.x = c->o;
         g.y = c->X;
@@ -979,7 +1191,7 @@ pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk = nul
         g.R = D;
         g.K = D;
         if (mgemv<MP_NONE, ME_SCALE_RES>(g, s) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi out_proj launch");
-        mark(PM_MIMI_K_OUT_PROJ);
+        if (mk) mk->mark(s, PM_MIMI_K_OUT_PROJ);
         g.W = c->w[w0 + 7];
         g.x = c->X;
         g.ln_w = c->w[w0 + 5];
@@ -988,7 +1200,7 @@ pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk = nul
         g.R = f.ffn;
         g.K = D;
         if (mgemv<MP_LN, ME_GELU>(g, s) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi lin1 launch");
-        mark(PM_MIMI_K_LIN1);
+        if (mk) mk->mark(s, PM_MIMI_K_LIN1);
         g.W = c->w[w0 + 8];
         g.x = c->hf;
         g.y = c->X;
@@ -996,19 +1208,33 @@ pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk = nul
         g.R = D;
         g.K = f.ffn;
         if (mgemv<MP_NONE, ME_SCALE_RES>(g, s) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi lin2 launch");
-        mark(PM_MIMI_K_LIN2);
+        if (mk) mk->mark(s, PM_MIMI_K_LIN2);
     }
-    // SEANet decoder
-    for (size_t i = 0; i < c->layers.size(); ++i) {
+    return PM_OK;
+}
+
+float* buf_ptr(pm_mimi_ctx* c, int code) {
+    if (code >= 0) return c->acts[code];
+    if (code == BUF_X) return c->X;
+    if (code == BUF_LAT) return c->lat;
+    return nullptr;
+}
+
+// convolutions first .. last - 1 of the context's plan
+pm_status record_convs(pm_mimi_ctx* c, int B, cudaStream_t s, size_t first, size_t last, MimiMarks* mk) {
+    const pm_mimi_config& f = c->cfg;
+    for (size_t i = first; i < last; ++i) {
         const MimiLayer& L = c->layers[i];
         MConvParams q;
         memset(&q, 0, sizeof q);
-        q.in = L.in_buf < 0 ? c->X : c->acts[L.in_buf];
-        q.in_pm = L.in_buf < 0;
-        q.out = L.out_raw < 0 ? nullptr : c->acts[L.out_raw];
-        q.out_act = L.out_act < 0 ? nullptr : c->acts[L.out_act];
-        q.res_in = L.res_buf < 0 ? nullptr : c->acts[L.res_buf];
-        q.io_out = L.pcm ? c->io : nullptr;  // the last convolution writes the caller's PCM
+        q.in = buf_ptr(c, L.in_buf);
+        q.io_in = L.in_buf == BUF_IO ? c->io : nullptr;  // the encoder's first convolution reads the caller's PCM
+        q.in_pm = L.in_buf == BUF_X;
+        q.out = buf_ptr(c, L.out_raw);
+        q.out_pm = L.out_raw == BUF_X;
+        q.io_out = L.out_raw == BUF_IO ? c->io : nullptr;  // the decoder's last convolution writes the caller's PCM
+        q.out_act = L.out_act == BUF_NONE ? nullptr : buf_ptr(c, L.out_act);
+        q.res_in = L.res_buf == BUF_NONE ? nullptr : buf_ptr(c, L.res_buf);
         q.Wt = L.Wt;
         q.bias = L.bias;
         q.state = L.state;
@@ -1020,6 +1246,9 @@ pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk = nul
         q.P = L.P;
         q.T = L.T;
         q.U = L.P > 1 ? L.T + 1 : L.T;
+        q.S = L.S;
+        q.rep = L.rep;
+        q.no_bias = L.no_bias;
         const ConvLaunch cl = conv_launch(L, B);
         q.rows_per_cta = cl.rpc;
         cudaError_t e;
@@ -1032,31 +1261,101 @@ pm_status record_mimi(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk = nul
                 : cl.CO == 8 ? launch_pdl(k_mimi_conv_tiled<8>, cl.grid, dim3(256), cl.smem, s, q)
                              : launch_pdl(k_mimi_conv_tiled<4>, cl.grid, dim3(256), cl.smem, s, q);
         if (e != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi convolution launch");
-        mark(i == 0 ? PM_MIMI_K_CONV_FIRST
-                    : i + 1 == c->layers.size() ? PM_MIMI_K_CONV_LAST
-                                                : (int32_t)(PM_MIMI_K_CONVTR + (i - 1) % 3));
+        if (mk) mk->mark(s, L.kind);
     }
+    return PM_OK;
+}
+
+pm_status record_finish(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk) {
     FinishParams fin;
     fin.st = c->st;
     fin.io = c->io;
     fin.B = B;
-    fin.frame_samples = c->frame_samples;
+    fin.frame_samples = c->encoder ? 0 : c->frame_samples;
     if (launch_pdl(k_mimi_finish, dim3(1), dim3(256), 0, s, fin) != cudaSuccess)
         return mfail(c, PM_ERR_CUDA, "mimi finish launch");
-    mark(PM_MIMI_K_FINISH);
+    if (mk) mk->mark(s, PM_MIMI_K_FINISH);
     return PM_OK;
 }
 
-// largest dynamic shared memory any launch of this configuration asks for
-size_t mimi_smem_need(const pm_mimi_config& f) {
+pm_status record_decoder(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk) {
+    const pm_mimi_config& f = c->cfg;
+    const MimiIdx ix = mimi_index(f);
+    FrontParams fp;
+    memset(&fp, 0, sizeof fp);
+    fp.io = c->io;
+    fp.st = c->st;
+    for (int j = 0; j < f.n_q; ++j) fp.cb[j] = c->w[ix.cb0 + j];
+    fp.sem_out = c->w[ix.sem_out];
+    fp.ac_out = c->w[ix.ac_out];
+    fp.up = c->w[ix.up];
+    fp.prev = c->prev;
+    fp.X = c->X;
+    fp.B_max = f.B_max;
+    fp.dim = f.dim;
+    fp.cb_dim = f.cb_dim;
+    fp.card = f.card;
+    fp.n_q = f.n_q;
+    // the first launch follows the I/O copies, not a kernel: no programmatic dependency
+    k_mimi_front<<<dim3((unsigned)((f.dim + 15) / 16), (unsigned)B), 256, 8u * f.cb_dim, s>>>(fp);
+    if (cudaGetLastError() != cudaSuccess) return mfail(c, PM_ERR_CUDA, "k_mimi_front launch");
+    if (mk) mk->mark(s, PM_MIMI_K_FRONT);
+    pm_status st = record_transformer(c, B, s, ix.layer0, mk);
+    if (st == PM_OK) st = record_convs(c, B, s, 0, c->layers.size(), mk);
+    if (st == PM_OK) st = record_finish(c, B, s, mk);
+    return st;
+}
+
+pm_status record_encoder(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk) {
+    const pm_mimi_config& f = c->cfg;
+    const MimiEncIdx ix = mimi_enc_index(f);
+    const size_t n = c->layers.size();  // the last one is the downsampler, after the transformer
+    pm_status st = record_convs(c, B, s, 0, n - 1, mk);
+    if (st == PM_OK) st = record_transformer(c, B, s, ix.layer0, mk);
+    if (st == PM_OK) st = record_convs(c, B, s, n - 1, n, mk);
+    if (st != PM_OK) return st;
+    RvqParams rp;
+    memset(&rp, 0, sizeof rp);
+    rp.e = c->lat;
+    rp.w_sem = c->w[ix.sem_in];
+    rp.w_ac = c->w[ix.ac_in];
+    for (int j = 0; j < f.n_q; ++j) rp.cb[j] = c->w[ix.cb0 + j];
+    rp.io = c->io;
+    rp.dim = f.dim;
+    rp.cb_dim = f.cb_dim;
+    rp.card = f.card;
+    rp.n_q = f.n_q;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(RQ, (unsigned)B);
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = rvq_smem(f.dim, f.cb_dim);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = RQ;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        if (cudaLaunchKernelEx(&cfg, k_mimi_rvq, rp) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi rvq launch");
+        if (mk) mk->mark(s, PM_MIMI_K_RVQ);
+    }
+    return record_finish(c, B, s, mk);
+}
+
+// largest dynamic shared memory any launch of this context asks for
+size_t mimi_smem_need(const pm_mimi_config& f, const std::vector<MimiLayer>& layers, int encoder) {
     size_t m = gemv_smem(2 * f.B_max, f.dim > f.ffn ? f.dim : f.ffn);
     if (attn_smem(f.ctx) > m) m = attn_smem(f.ctx);
-    for (const MimiLayer& L : seanet_layers(f)) {
-        const ConvLaunch cl = conv_launch(L, f.B_max);
-        if (cl.smem > m) m = cl.smem;
-        const ConvLaunch c1 = conv_launch(L, 1);
-        if (c1.smem > m) m = c1.smem;
-    }
+    if (encoder && rvq_smem(f.dim, f.cb_dim) > m) m = rvq_smem(f.dim, f.cb_dim);
+    for (const MimiLayer& L : layers)
+        for (int B : {1, f.B_max}) {
+            const ConvLaunch cl = conv_launch(L, B);
+            if (cl.smem > m) m = cl.smem;
+        }
     return m;
 }
 
@@ -1083,61 +1382,60 @@ cudaError_t mimi_func_attributes(size_t smem) {
     set((const void*)k_mimi_conv_tiled<16>);
     set((const void*)k_mimi_front);
     set((const void*)k_mimi_attn);
+    set((const void*)k_mimi_rvq);
     return e;
 }
 
-}  // namespace
-
-extern "C" int pm_mimi_tensor_count(const pm_mimi_config* cfg) {
-    if (!cfg || mimi_check(cfg)) return -1;
-    return mimi_index(*cfg).total;
-}
-
-extern "C" pm_status pm_mimi_create(const pm_mimi_config* cfg, const void* const* tensors, int n_tensors,
-                                    void* cuda_stream, pm_mimi_ctx** out) {
+pm_status mimi_create(const pm_mimi_config* cfg, const void* const* tensors, int n_tensors, void* cuda_stream,
+                      pm_mimi_ctx** out, int encoder) {
     g_mimi_create_error.clear();
-    auto refuse = [](pm_status s, const std::string& m) {
-        g_mimi_create_error = m;
+    const char* fn = encoder ? "pm_mimi_encoder_create: " : "pm_mimi_create: ";
+    auto refuse = [&](pm_status s, const std::string& m) {
+        g_mimi_create_error = fn + m;
         return s;
     };
-    if (!cfg || !tensors || !out) return refuse(PM_ERR_ARG, "pm_mimi_create: NULL argument");
+    if (!cfg || !tensors || !out) return refuse(PM_ERR_ARG, "NULL argument");
     *out = nullptr;
-    if (const char* why = mimi_check(cfg)) return refuse(PM_ERR_ARG, std::string("pm_mimi_create: ") + why);
-    const MimiIdx ix = mimi_index(*cfg);
-    if (n_tensors != ix.total)
-        return refuse(PM_ERR_ARG, "pm_mimi_create: expected " + std::to_string(ix.total) + " tensors");
+    if (const char* why = mimi_check(cfg)) return refuse(PM_ERR_ARG, why);
+    if (encoder)
+        if (const char* why = mimi_encoder_check(cfg)) return refuse(PM_ERR_ARG, why);
+    const int total = encoder ? mimi_enc_index(*cfg).total : mimi_index(*cfg).total;
+    if (n_tensors != total) return refuse(PM_ERR_ARG, "expected " + std::to_string(total) + " tensors");
     for (int i = 0; i < n_tensors; ++i) {
         if (!tensors[i] || (reinterpret_cast<uintptr_t>(tensors[i]) & 15u))
-            return refuse(PM_ERR_ARG, "pm_mimi_create: tensor " + std::to_string(i) + " NULL or not 16-byte aligned");
+            return refuse(PM_ERR_ARG, "tensor " + std::to_string(i) + " NULL or not 16-byte aligned");
         cudaPointerAttributes a;
         const bool dev = cudaPointerGetAttributes(&a, tensors[i]) == cudaSuccess &&
                          (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged);
         cudaGetLastError();
-        if (!dev) return refuse(PM_ERR_ARG, "pm_mimi_create: tensor " + std::to_string(i) + " is not device memory");
+        if (!dev) return refuse(PM_ERR_ARG, "tensor " + std::to_string(i) + " is not device memory");
     }
-    const size_t smem = mimi_smem_need(*cfg);
-    if (smem > 227u * 1024u) return refuse(PM_ERR_UNSUPPORTED, "pm_mimi_create: shared memory above 227 KB");
+    const std::vector<MimiLayer> layers = encoder ? seanet_encoder_layers(*cfg) : seanet_layers(*cfg);
+    const size_t smem = mimi_smem_need(*cfg, layers, encoder);
+    if (smem > 227u * 1024u) return refuse(PM_ERR_UNSUPPORTED, "shared memory above 227 KB");
     pm_mimi_ctx* c = new pm_mimi_ctx();
     c->cfg = *cfg;
+    c->encoder = encoder;
     const pm_mimi_config& f = c->cfg;
     c->frame_samples = 2;
     for (int i = 0; i < f.n_ratios; ++i) c->frame_samples *= f.ratios[i];
     cudaGetDevice(&c->device);
     c->stream = reinterpret_cast<cudaStream_t>(cuda_stream);
     for (int i = 0; i < n_tensors; ++i) c->w.push_back(static_cast<const uint16_t*>(tensors[i]));
+    c->layers = layers;
     auto bail = [&](pm_status s, const char* m) {
         pm_mimi_destroy(c);
-        g_mimi_create_error = std::string("pm_mimi_create: ") + m;
+        g_mimi_create_error = std::string(fn) + m;
         return s;
     };
     if (mimi_func_attributes(smem) != cudaSuccess) {
         cudaGetLastError();
         return bail(PM_ERR_CUDA, "cudaFuncSetAttribute");
     }
-    c->layers = seanet_layers(f);
     // one allocation for state, activations and I/O
     const int BM = f.B_max, D = f.dim;
-    void *p_frame, *p_pos, *p_abort, *p_status, *p_io, *p_codes, *p_prev, *p_X, *p_qkv, *p_o, *p_hf, *p_kv, *p_freq;
+    void *p_frame, *p_pos, *p_abort, *p_status, *p_io, *p_codes, *p_pcm, *p_prev, *p_X, *p_qkv, *p_o, *p_hf, *p_kv,
+        *p_lat, *p_freq;
     std::vector<std::pair<void**, size_t>> items = {
         {&p_frame, 4u * BM},
         {&p_pos, 4u * BM},
@@ -1145,17 +1443,20 @@ extern "C" pm_status pm_mimi_create(const pm_mimi_config* cfg, const void* const
         {&p_status, 4u},
         {&p_io, sizeof(MimiIO)},
         {&p_codes, 4u * BM * f.n_q},
+        {&p_pcm, encoder ? 4u * BM * c->frame_samples : 16u},
         {&p_prev, 4u * 2 * BM * D},
         {&p_X, 4u * BM * 2 * D},
         {&p_qkv, 4u * BM * 2 * 3 * D},
         {&p_o, 4u * BM * 2 * D},
         {&p_hf, 4u * BM * 2 * f.ffn},
         {&p_kv, 4u * (size_t)f.n_layers * 2 * BM * f.heads * (f.ctx + 1) * MDH},
+        {&p_lat, 4u * BM * D},
         {&p_freq, 8u * (MDH / 2)},
     };
-    // activations: the first convolution's output, per stage the transposed convolution's
-    // output (the residual stream) and the residual unit's middle
-    std::vector<size_t> act_sizes(1 + 3 * f.n_ratios, 0);
+    int n_act = 0;
+    for (const MimiLayer& L : c->layers)
+        for (int k : {L.in_buf, L.out_raw, L.out_act, L.res_buf}) n_act = k + 1 > n_act ? k + 1 : n_act;
+    std::vector<size_t> act_sizes(n_act, 0);
     for (const MimiLayer& L : c->layers) {
         const size_t n = (size_t)BM * L.Cout * (L.P > 1 ? L.T * L.P : L.T);
         for (int k : {L.out_raw, L.out_act})
@@ -1169,13 +1470,13 @@ extern "C" pm_status pm_mimi_create(const pm_mimi_config* cfg, const void* const
         c->state_per_stream[i] = layer_state(c->layers[i]);
         items.push_back({reinterpret_cast<void**>(&c->states[i]), 4u * 2 * BM * c->state_per_stream[i]});
     }
-    size_t total = 0;
-    for (auto& it : items) total = (total + 255) / 256 * 256 + (it.second + 15) / 16 * 16;
-    if (cudaMalloc(&c->block, total) != cudaSuccess) {
+    size_t total_bytes = 0;
+    for (auto& it : items) total_bytes = (total_bytes + 255) / 256 * 256 + (it.second + 15) / 16 * 16;
+    if (cudaMalloc(&c->block, total_bytes) != cudaSuccess) {
         cudaGetLastError();
         return bail(PM_ERR_OOM, "device allocation");
     }
-    if (cudaMemset(c->block, 0, total) != cudaSuccess) return bail(PM_ERR_CUDA, "cudaMemset");
+    if (cudaMemset(c->block, 0, total_bytes) != cudaSuccess) return bail(PM_ERR_CUDA, "cudaMemset");
     size_t off = 0;
     for (auto& it : items) {
         off = (off + 255) / 256 * 256;
@@ -1188,14 +1489,16 @@ extern "C" pm_status pm_mimi_create(const pm_mimi_config* cfg, const void* const
     c->st.status = (uint32_t*)p_status;
     c->io = (MimiIO*)p_io;
     c->codes_dev = (int32_t*)p_codes;
+    c->pcm_dev = (float*)p_pcm;
     c->prev = (float*)p_prev;
     c->X = (float*)p_X;
     c->qkv = (float*)p_qkv;
     c->o = (float*)p_o;
     c->hf = (float*)p_hf;
     c->kv = (float*)p_kv;
+    c->lat = (float*)p_lat;
     c->freq = (double*)p_freq;
-    // tap-major SEANet weights, re-laid from the caller's tensors once
+    // tap-major convolution weights, re-laid from the caller's tensors once
     std::vector<size_t> wt_off;
     size_t wt_total = 0;
     for (const MimiLayer& L : c->layers) {
@@ -1208,18 +1511,10 @@ extern "C" pm_status pm_mimi_create(const pm_mimi_config* cfg, const void* const
     }
     for (size_t i = 0; i < c->layers.size(); ++i) {
         MimiLayer& L = c->layers[i];
-        // canonical: dec.0 (w, b); per stage up (w, b), res w1, b1, w2, b2; dec.out (w, b)
-        int wi;
-        if (i == 0)
-            wi = ix.dec0w;
-        else if (i + 1 == c->layers.size())
-            wi = ix.outw;
-        else
-            wi = ix.stage0 + 6 * (int)((i - 1) / 3) + 2 * (int)((i - 1) % 3);
         L.Wt = c->wt_block + wt_off[i];
-        L.bias = c->w[wi + 1];
+        L.bias = L.no_bias ? nullptr : c->w[L.wi + 1];
         L.state = c->states[i];
-        k_mimi_relayout<<<256, 256>>>(c->w[wi], c->wt_block + wt_off[i], L.Cin, L.Cout, L.NT, L.P);
+        k_mimi_relayout<<<256, 256>>>(c->w[L.wi], c->wt_block + wt_off[i], L.Cin, L.Cout, L.NT, L.P, L.S);
         if (cudaGetLastError() != cudaSuccess) return bail(PM_ERR_CUDA, "relayout launch");
     }
     // RoPE frequency of pair j: theta^(-2j / 64)
@@ -1227,7 +1522,8 @@ extern "C" pm_status pm_mimi_create(const pm_mimi_config* cfg, const void* const
     for (int j = 0; j < MDH / 2; ++j) fq[j] = exp(-log((double)f.rope_theta) * (2.0 * j) / (double)MDH);
     if (cudaMemcpy(c->freq, fq.data(), 8u * fq.size(), cudaMemcpyHostToDevice) != cudaSuccess)
         return bail(PM_ERR_CUDA, "cudaMemcpy");
-    if (cudaHostAlloc((void**)&c->host_io, 64u + 4u * BM * f.n_q, cudaHostAllocDefault) != cudaSuccess)
+    c->host_io_bytes = 64u + (encoder ? 4u * BM * c->frame_samples : 4u * BM * f.n_q);
+    if (cudaHostAlloc((void**)&c->host_io, c->host_io_bytes, cudaHostAllocDefault) != cudaSuccess)
         return bail(PM_ERR_OOM, "pinned host allocation");
     if (cudaEventCreateWithFlags(&c->io_done, cudaEventDisableTiming) != cudaSuccess)
         return bail(PM_ERR_CUDA, "cudaEventCreate");
@@ -1239,40 +1535,38 @@ extern "C" pm_status pm_mimi_create(const pm_mimi_config* cfg, const void* const
     return PM_OK;
 }
 
-extern "C" void pm_mimi_destroy(pm_mimi_ctx* c) {
-    if (!c) return;
-    cudaSetDevice(c->device);
-    if (c->block) cudaStreamSynchronize(c->stream);
-    for (auto g : c->graphs)
-        if (g) cudaGraphExecDestroy(g);
-    if (c->io_done) cudaEventDestroy(c->io_done);
-    if (c->host_io) cudaFreeHost(c->host_io);
-    if (c->cap) cudaStreamDestroy(c->cap);
-    if (c->wt_block) cudaFree(c->wt_block);
-    if (c->block) cudaFree(c->block);
-    delete c;
-}
-
-namespace {
-
-// validate the call's pointers and codes, then copy the I/O block (and host codes) on the
-// context's stream; graph or eager launches follow
-pm_status mimi_stage(pm_mimi_ctx* c, int B, const int32_t* codes, float* pcm) {
-    const pm_mimi_config& f = c->cfg;
-    if (B < 1 || B > f.B_max || !codes || !pcm) return mfail(c, PM_ERR_ARG, "pm_mimi_decode: bad B or NULL pointer");
-    if (cudaSetDevice(c->device) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "cudaSetDevice");
+// device, managed or host-mapped memory: the pointer the kernels use, or NULL
+template <typename T>
+T* device_view(T* p) {
     cudaPointerAttributes a;
-    float* pcm_dev = nullptr;
-    if (cudaPointerGetAttributes(&a, pcm) == cudaSuccess) {
-        if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) pcm_dev = pcm;
-        if (a.type == cudaMemoryTypeHost && a.devicePointer) pcm_dev = static_cast<float*>(a.devicePointer);
+    T* d = nullptr;
+    if (p && cudaPointerGetAttributes(&a, p) == cudaSuccess) {
+        if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) d = p;
+        if (a.type == cudaMemoryTypeHost && a.devicePointer) d = static_cast<T*>(a.devicePointer);
     }
     cudaGetLastError();
+    return d;
+}
+
+bool is_device(const void* p) {
+    cudaPointerAttributes a;
+    const bool d = p && cudaPointerGetAttributes(&a, p) == cudaSuccess &&
+                   (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged);
+    cudaGetLastError();
+    return d;
+}
+
+// decoder: validate the call's pointers and codes, then copy the I/O block (and host codes)
+// on the context's stream; graph or eager launches follow
+pm_status mimi_stage(pm_mimi_ctx* c, int B, const int32_t* codes, float* pcm) {
+    const pm_mimi_config& f = c->cfg;
+    if (c->encoder) return mfail(c, PM_ERR_STATE, "pm_mimi_decode on an encoder context");
+    if (B < 1 || B > f.B_max || !codes || !pcm) return mfail(c, PM_ERR_ARG, "pm_mimi_decode: bad B or NULL pointer");
+    if (cudaSetDevice(c->device) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "cudaSetDevice");
+    float* pcm_dev = device_view(pcm);
     if (!pcm_dev || (reinterpret_cast<uintptr_t>(pcm) & 3u))
         return mfail(c, PM_ERR_ARG, "pm_mimi_decode: pcm must be 4-byte aligned device, managed or host-mapped memory");
-    const bool dev_codes = cudaPointerGetAttributes(&a, codes) == cudaSuccess &&
-                           (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged);
-    cudaGetLastError();
+    const bool dev_codes = is_device(codes);
     if (!dev_codes)
         for (int i = 0; i < B * f.n_q; ++i)
             if (codes[i] < 0 || codes[i] >= f.card)
@@ -1281,6 +1575,7 @@ pm_status mimi_stage(pm_mimi_ctx* c, int B, const int32_t* codes, float* pcm) {
     // the previous call's copies out of the pinned staging must be done before it is reused
     if (cudaEventSynchronize(c->io_done) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "cudaEventSynchronize");
     MimiIO io;
+    memset(&io, 0, sizeof io);
     io.codes = dev_codes ? codes : c->codes_dev;
     io.pcm = pcm_dev;
     memcpy(c->host_io, &io, sizeof io);
@@ -1295,42 +1590,70 @@ pm_status mimi_stage(pm_mimi_ctx* c, int B, const int32_t* codes, float* pcm) {
     return PM_OK;
 }
 
-}  // namespace
-
-extern "C" pm_status pm_mimi_decode(pm_mimi_ctx* c, int B, const int32_t* codes, float* pcm) {
-    if (!c) return PM_ERR_ARG;
-    if (B >= 1 && B <= c->cfg.B_max && !c->graphs[B]) {
-        if (cudaSetDevice(c->device) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "cudaSetDevice");
-        if (cudaStreamBeginCapture(c->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
-            return mfail(c, PM_ERR_CUDA, "cudaStreamBeginCapture");
-        pm_status st = record_mimi(c, B, c->cap);
-        cudaGraph_t g = nullptr;
-        const cudaError_t e = cudaStreamEndCapture(c->cap, &g);
-        if (st != PM_OK || e != cudaSuccess || cudaGraphInstantiate(&c->graphs[B], g, 0) != cudaSuccess) {
-            if (g) cudaGraphDestroy(g);
-            c->graphs[B] = nullptr;
-            cudaGetLastError();
-            return st != PM_OK ? st : mfail(c, PM_ERR_CUDA, "mimi graph capture");
-        }
-        cudaGraphDestroy(g);
+// encoder: the same for PCM in, codes (and the latent) out
+pm_status mimi_stage_enc(pm_mimi_ctx* c, int B, const float* pcm, int32_t* codes, float* latent) {
+    const pm_mimi_config& f = c->cfg;
+    if (!c->encoder) return mfail(c, PM_ERR_STATE, "pm_mimi_encode on a decoder context");
+    if (B < 1 || B > f.B_max || !pcm || !codes) return mfail(c, PM_ERR_ARG, "pm_mimi_encode: bad B or NULL pointer");
+    if (cudaSetDevice(c->device) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "cudaSetDevice");
+    int32_t* codes_dev = device_view(codes);
+    if (!codes_dev || (reinterpret_cast<uintptr_t>(codes) & 3u))
+        return mfail(c, PM_ERR_ARG, "pm_mimi_encode: codes must be 4-byte aligned device, managed or host-mapped memory");
+    float* lat_dev = nullptr;
+    if (latent) {
+        lat_dev = device_view(latent);
+        if (!lat_dev || (reinterpret_cast<uintptr_t>(latent) & 3u))
+            return mfail(c, PM_ERR_ARG, "pm_mimi_encode: latent must be device, managed or host-mapped memory");
     }
-    pm_status st = mimi_stage(c, B, codes, pcm);
-    if (st != PM_OK) return st;
-    if (cudaGraphLaunch(c->graphs[B], c->stream) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi launch");
+    const bool dev_pcm = is_device(pcm);
+    if (dev_pcm && (reinterpret_cast<uintptr_t>(pcm) & 3u)) return mfail(c, PM_ERR_ARG, "pm_mimi_encode: pcm not aligned");
+    if (cudaEventSynchronize(c->io_done) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "cudaEventSynchronize");
+    MimiIO io;
+    memset(&io, 0, sizeof io);
+    io.pcm_in = dev_pcm ? pcm : c->pcm_dev;
+    io.codes_out = codes_dev;
+    io.latent_out = lat_dev;
+    memcpy(c->host_io, &io, sizeof io);
+    if (!dev_pcm) {
+        const size_t n = 4u * (size_t)B * c->frame_samples;
+        memcpy(c->host_io + 64, pcm, n);
+        if (cudaMemcpyAsync(c->pcm_dev, c->host_io + 64, n, cudaMemcpyHostToDevice, c->stream) != cudaSuccess)
+            return mfail(c, PM_ERR_CUDA, "pcm copy");
+    }
+    if (cudaMemcpyAsync(c->io, c->host_io, sizeof io, cudaMemcpyHostToDevice, c->stream) != cudaSuccess ||
+        cudaEventRecord(c->io_done, c->stream) != cudaSuccess)
+        return mfail(c, PM_ERR_CUDA, "I/O block copy");
     return PM_OK;
 }
 
-extern "C" pm_status pm_mimi_profile(pm_mimi_ctx* c, int B, const int32_t* codes, float* pcm, float* ms,
-                                     int32_t* kind, int n_max, int* n) {
-    if (!c) return PM_ERR_ARG;
-    if (!ms || !kind || !n || n_max < 1) return mfail(c, PM_ERR_ARG, "pm_mimi_profile: NULL output or n_max < 1");
-    pm_status st = mimi_stage(c, B, codes, pcm);
-    if (st != PM_OK) return st;
+pm_status mimi_record(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk) {
+    return c->encoder ? record_encoder(c, B, s, mk) : record_decoder(c, B, s, mk);
+}
+
+pm_status mimi_graph(pm_mimi_ctx* c, int B) {
+    if (B < 1 || B > c->cfg.B_max || c->graphs[B]) return PM_OK;
+    if (cudaSetDevice(c->device) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "cudaSetDevice");
+    if (cudaStreamBeginCapture(c->cap, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+        return mfail(c, PM_ERR_CUDA, "cudaStreamBeginCapture");
+    pm_status st = mimi_record(c, B, c->cap, nullptr);
+    cudaGraph_t g = nullptr;
+    const cudaError_t e = cudaStreamEndCapture(c->cap, &g);
+    if (st != PM_OK || e != cudaSuccess || cudaGraphInstantiate(&c->graphs[B], g, 0) != cudaSuccess) {
+        if (g) cudaGraphDestroy(g);
+        c->graphs[B] = nullptr;
+        cudaGetLastError();
+        return st != PM_OK ? st : mfail(c, PM_ERR_CUDA, "mimi graph capture");
+    }
+    cudaGraphDestroy(g);
+    return PM_OK;
+}
+
+pm_status mimi_profile_run(pm_mimi_ctx* c, int B, float* ms, int32_t* kind, int n_max, int* n) {
     MimiMarks mk;
     cudaEvent_t start;
     if (cudaEventCreate(&start) != cudaSuccess || cudaEventRecord(start, c->stream) != cudaSuccess)
-        return mfail(c, PM_ERR_CUDA, "pm_mimi_profile: event");
-    st = record_mimi(c, B, c->stream, &mk);
+        return mfail(c, PM_ERR_CUDA, "profile: event");
+    pm_status st = mimi_record(c, B, c->stream, &mk);
     const bool synced = cudaStreamSynchronize(c->stream) == cudaSuccess;
     int k = 0;
     cudaEvent_t prev = start;
@@ -1347,7 +1670,79 @@ extern "C" pm_status pm_mimi_profile(pm_mimi_ctx* c, int B, const int32_t* codes
     cudaEventDestroy(start);
     *n = k;
     if (st != PM_OK) return st;
-    return synced ? PM_OK : mfail(c, PM_ERR_CUDA, "pm_mimi_profile: synchronize");
+    return synced ? PM_OK : mfail(c, PM_ERR_CUDA, "profile: synchronize");
+}
+
+}  // namespace
+
+extern "C" int pm_mimi_tensor_count(const pm_mimi_config* cfg) {
+    if (!cfg || mimi_check(cfg)) return -1;
+    return mimi_index(*cfg).total;
+}
+
+extern "C" int pm_mimi_encoder_tensor_count(const pm_mimi_config* cfg) {
+    if (!cfg || mimi_check(cfg) || mimi_encoder_check(cfg)) return -1;
+    return mimi_enc_index(*cfg).total;
+}
+
+extern "C" pm_status pm_mimi_create(const pm_mimi_config* cfg, const void* const* tensors, int n_tensors,
+                                    void* cuda_stream, pm_mimi_ctx** out) {
+    return mimi_create(cfg, tensors, n_tensors, cuda_stream, out, 0);
+}
+
+extern "C" pm_status pm_mimi_encoder_create(const pm_mimi_config* cfg, const void* const* tensors, int n_tensors,
+                                            void* cuda_stream, pm_mimi_ctx** out) {
+    return mimi_create(cfg, tensors, n_tensors, cuda_stream, out, 1);
+}
+
+extern "C" void pm_mimi_destroy(pm_mimi_ctx* c) {
+    if (!c) return;
+    cudaSetDevice(c->device);
+    if (c->block) cudaStreamSynchronize(c->stream);
+    for (auto g : c->graphs)
+        if (g) cudaGraphExecDestroy(g);
+    if (c->io_done) cudaEventDestroy(c->io_done);
+    if (c->host_io) cudaFreeHost(c->host_io);
+    if (c->cap) cudaStreamDestroy(c->cap);
+    if (c->wt_block) cudaFree(c->wt_block);
+    if (c->block) cudaFree(c->block);
+    delete c;
+}
+
+extern "C" pm_status pm_mimi_decode(pm_mimi_ctx* c, int B, const int32_t* codes, float* pcm) {
+    if (!c) return PM_ERR_ARG;
+    if (c->encoder) return mfail(c, PM_ERR_STATE, "pm_mimi_decode on an encoder context");
+    pm_status st = mimi_graph(c, B);
+    if (st == PM_OK) st = mimi_stage(c, B, codes, pcm);
+    if (st != PM_OK) return st;
+    if (cudaGraphLaunch(c->graphs[B], c->stream) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi launch");
+    return PM_OK;
+}
+
+extern "C" pm_status pm_mimi_encode(pm_mimi_ctx* c, int B, const float* pcm, int32_t* codes, float* latent) {
+    if (!c) return PM_ERR_ARG;
+    if (!c->encoder) return mfail(c, PM_ERR_STATE, "pm_mimi_encode on a decoder context");
+    pm_status st = mimi_graph(c, B);
+    if (st == PM_OK) st = mimi_stage_enc(c, B, pcm, codes, latent);
+    if (st != PM_OK) return st;
+    if (cudaGraphLaunch(c->graphs[B], c->stream) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "mimi launch");
+    return PM_OK;
+}
+
+extern "C" pm_status pm_mimi_profile(pm_mimi_ctx* c, int B, const int32_t* codes, float* pcm, float* ms,
+                                     int32_t* kind, int n_max, int* n) {
+    if (!c) return PM_ERR_ARG;
+    if (!ms || !kind || !n || n_max < 1) return mfail(c, PM_ERR_ARG, "pm_mimi_profile: NULL output or n_max < 1");
+    pm_status st = mimi_stage(c, B, codes, pcm);
+    return st != PM_OK ? st : mimi_profile_run(c, B, ms, kind, n_max, n);
+}
+
+extern "C" pm_status pm_mimi_encode_profile(pm_mimi_ctx* c, int B, const float* pcm, int32_t* codes, float* latent,
+                                            float* ms, int32_t* kind, int n_max, int* n) {
+    if (!c) return PM_ERR_ARG;
+    if (!ms || !kind || !n || n_max < 1) return mfail(c, PM_ERR_ARG, "pm_mimi_encode_profile: NULL output or n_max < 1");
+    pm_status st = mimi_stage_enc(c, B, pcm, codes, latent);
+    return st != PM_OK ? st : mimi_profile_run(c, B, ms, kind, n_max, n);
 }
 
 extern "C" pm_status pm_mimi_reset(pm_mimi_ctx* c, const int32_t* mask) {

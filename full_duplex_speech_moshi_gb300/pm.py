@@ -26,9 +26,11 @@ EXPORTS = ["pm_kv_cache_bytes", "pm_create", "pm_reset", "pm_set_positions", "pm
            "pm_snapshot", "pm_restore", "pm_prefill", "pm_set_wait_budget", "pm_generator_step"]
 # every symbol include/pm_mimi.h declares
 MIMI_EXPORTS = ["pm_mimi_tensor_count", "pm_mimi_create", "pm_mimi_decode", "pm_mimi_reset", "pm_mimi_status",
-                "pm_mimi_get_frames", "pm_mimi_last_error", "pm_mimi_destroy", "pm_mimi_profile"]
+                "pm_mimi_get_frames", "pm_mimi_last_error", "pm_mimi_destroy", "pm_mimi_profile",
+                "pm_mimi_encoder_tensor_count", "pm_mimi_encoder_create", "pm_mimi_encode", "pm_mimi_encode_profile"]
 MIMI_KINDS = {0: "front", 1: "in_proj", 2: "attention", 3: "out_proj", 4: "lin1", 5: "lin2", 6: "conv_first",
-              7: "convtr", 8: "res_conv1", 9: "res_conv2", 10: "conv_last", 11: "finish"}
+              7: "convtr", 8: "res_conv1", 9: "res_conv2", 10: "conv_last", 11: "finish", 12: "down",
+              13: "resample", 14: "rvq"}
 PM_WAIT_BUDGET_DEFAULT = 0xFFFFFFFF
 KERNEL_KINDS = {0: "embed", 1: "qkv_rope", 2: "attention", 3: "out_proj", 4: "linear_in_swiglu",
                 5: "linear_out", 6: "text_head", 7: "frame_program", 8: "text_sample"}
@@ -146,6 +148,14 @@ def lib():
         L.pm_mimi_last_error.argtypes = [vp]
         L.pm_mimi_profile.restype = C.c_int
         L.pm_mimi_profile.argtypes = [vp, C.c_int, vp, vp, vp, vp, C.c_int, C.POINTER(C.c_int)]
+        L.pm_mimi_encoder_tensor_count.restype = C.c_int
+        L.pm_mimi_encoder_tensor_count.argtypes = [mp]
+        L.pm_mimi_encoder_create.restype = C.c_int
+        L.pm_mimi_encoder_create.argtypes = [mp, vp, C.c_int, vp, C.POINTER(C.c_void_p)]
+        L.pm_mimi_encode.restype = C.c_int
+        L.pm_mimi_encode.argtypes = [vp, C.c_int, vp, vp, vp]
+        L.pm_mimi_encode_profile.restype = C.c_int
+        L.pm_mimi_encode_profile.argtypes = [vp, C.c_int, vp, vp, vp, vp, vp, C.c_int, C.POINTER(C.c_int)]
         L.pm_mimi_destroy.restype = None
         L.pm_mimi_destroy.argtypes = [vp]
         _lib = L
@@ -418,22 +428,42 @@ def mimi_frame_samples(shape: dict) -> int:
     return n
 
 
-class MimiDecoder:
-    """Owns one pm_mimi_ctx.  `weights` maps the canonical tensor names (mimi_tensor_names)
-    to bf16 device tensors, which the caller keeps alive."""
+def mimi_encoder_tensor_names(shape: dict) -> List[str]:
+    """Tensor names in the encoder's canonical order of include/pm_mimi.h."""
+    s = dict(MIMI_DEFAULT)
+    s.update(shape)
+    n = ["enc.0.w", "enc.0.b"]
+    for i in range(len(s["ratios"])):
+        n += [f"enc.res{i}.w1", f"enc.res{i}.b1", f"enc.res{i}.w2", f"enc.res{i}.b2", f"enc.down{i}.w", f"enc.down{i}.b"]
+    n += ["enc.out.w", "enc.out.b"]
+    for l in range(s["n_layers"]):
+        n += [f"etr.{l}.{k}" for k in ("norm1.w", "norm1.b", "in_proj", "out_proj", "scale1", "norm2.w", "norm2.b",
+                                       "lin1", "lin2", "scale2")]
+    return n + ["ds.weight", "q.sem.in", "q.ac.in"] + [f"q.codebook.{j}" for j in range(s["n_q"])]
+
+
+class _MimiContext:
+    """Owns one pm_mimi_ctx (decoder or encoder).  `weights` maps the canonical tensor
+    names to bf16 device tensors, which the caller keeps alive."""
+
+    _encoder = False
 
     def __init__(self, shape: dict, weights: Dict[str, object], B_max: int = 1, stream: int = 0):
         L = lib()
         self.L = L
         self.cfg = make_mimi_config(shape, B_max)
         self.frame_samples = mimi_frame_samples(shape)
-        names = mimi_tensor_names(shape)
-        n = L.pm_mimi_tensor_count(C.byref(self.cfg))
+        if self._encoder:
+            names, count, create = (mimi_encoder_tensor_names(shape), L.pm_mimi_encoder_tensor_count,
+                                    L.pm_mimi_encoder_create)
+        else:
+            names, count, create = mimi_tensor_names(shape), L.pm_mimi_tensor_count, L.pm_mimi_create
+        n = count(C.byref(self.cfg))
         if n != len(names):
             raise PMError(PM_ERR_ARG, f"unsupported Mimi configuration (tensor count {n})")
         self._ptrs = (C.c_void_p * len(names))(*[_ptr(weights[k]) for k in names])
         h = C.c_void_p()
-        st = L.pm_mimi_create(C.byref(self.cfg), self._ptrs, len(names), stream or None, C.byref(h))
+        st = create(C.byref(self.cfg), self._ptrs, len(names), stream or None, C.byref(h))
         if st != PM_OK:
             raise PMError(st, L.pm_mimi_last_error(None).decode())
         self.h = h
@@ -442,24 +472,12 @@ class MimiDecoder:
         if st != PM_OK:
             raise PMError(st, self.L.pm_mimi_last_error(self.h).decode())
 
-    def decode(self, B: int, codes, pcm) -> None:
-        """Next frame of streams 0..B-1: codes [B][n_q] int32 (host or device), pcm
-        [B][frame_samples] fp32 (device or host-mapped)."""
-        if codes is not None and not hasattr(codes, "data_ptr"):
-            import numpy as np
-            codes = np.ascontiguousarray(codes, dtype=np.int32)
-        self._check(self.L.pm_mimi_decode(self.h, int(B), _ptr(codes), _ptr(pcm)))
-
-    def profile(self, B: int, codes, pcm):
-        """One decode with per-launch device times: list of (kind name, ms)."""
-        if not hasattr(codes, "data_ptr"):
-            import numpy as np
-            codes = np.ascontiguousarray(codes, dtype=np.int32)
-        n_max = 2 + 5 * self.cfg.n_layers + 3 * self.cfg.n_ratios + 2
+    def _timed(self, fn, *args):
+        n_max = 8 + 5 * self.cfg.n_layers + 3 * self.cfg.n_ratios
         ms = (C.c_float * n_max)()
         kind = (C.c_int32 * n_max)()
         n = C.c_int(0)
-        self._check(self.L.pm_mimi_profile(self.h, int(B), _ptr(codes), _ptr(pcm), ms, kind, n_max, C.byref(n)))
+        self._check(fn(self.h, *args, ms, kind, n_max, C.byref(n)))
         return [(MIMI_KINDS[kind[i]], float(ms[i])) for i in range(n.value)]
 
     def reset(self, mask=None) -> None:
@@ -486,3 +504,45 @@ class MimiDecoder:
             self.close()
         except Exception:
             pass
+
+
+def _i32(a):
+    if a is not None and not hasattr(a, "data_ptr"):
+        import numpy as np
+        a = np.ascontiguousarray(a, dtype=np.int32)
+    return a
+
+
+def _f32(a):
+    if a is not None and not hasattr(a, "data_ptr"):
+        import numpy as np
+        a = np.ascontiguousarray(a, dtype=np.float32)
+    return a
+
+
+class MimiDecoder(_MimiContext):
+    """Streaming decoder: codes -> PCM (include/pm_mimi.h)."""
+
+    def decode(self, B: int, codes, pcm) -> None:
+        """Next frame of streams 0..B-1: codes [B][n_q] int32 (host or device), pcm
+        [B][frame_samples] fp32 (device or host-mapped)."""
+        self._check(self.L.pm_mimi_decode(self.h, int(B), _ptr(_i32(codes)), _ptr(pcm)))
+
+    def profile(self, B: int, codes, pcm):
+        """One decode with per-launch device times: list of (kind name, ms)."""
+        return self._timed(self.L.pm_mimi_profile, int(B), _ptr(_i32(codes)), _ptr(pcm))
+
+
+class MimiEncoder(_MimiContext):
+    """Streaming encoder: PCM -> codes (include/pm_mimi.h)."""
+
+    _encoder = True
+
+    def encode(self, B: int, pcm, codes, latent=None) -> None:
+        """Next frame of streams 0..B-1: pcm [B][frame_samples] fp32 (host or device),
+        codes [B][n_q] int32 and latent [B][dim] fp32 out (device or host-mapped)."""
+        self._check(self.L.pm_mimi_encode(self.h, int(B), _ptr(_f32(pcm)), _ptr(codes), _ptr(latent)))
+
+    def profile(self, B: int, pcm, codes, latent=None):
+        """One encode with per-launch device times: list of (kind name, ms)."""
+        return self._timed(self.L.pm_mimi_encode_profile, int(B), _ptr(_f32(pcm)), _ptr(codes), _ptr(latent))

@@ -1,6 +1,7 @@
 /*
- * pm_mimi.h -- C ABI of the GB300 (sm_103a) streaming Mimi decoder: one 80 ms frame of
- * codes per stream and call -> 1,920 samples of 24 kHz PCM.
+ * pm_mimi.h -- C ABI of the GB300 (sm_103a) streaming Mimi codec: the decoder takes one
+ * 80 ms frame of codes per stream and call to 1,920 samples of 24 kHz PCM; the encoder
+ * takes 1,920 samples to one frame of codes.
  *
  * What the calls compute is defined on the page "PersonaPlex native LM audit"
  * (clockless-atlas personaplex-research), chapter "Exact Mimi codec construction":
@@ -19,10 +20,18 @@
  *     Conv1d -> 1 channel, kernel last_kernel; every convolution with a bias);
  *   - "Stateful streaming, padding and dependency boundaries": causal convolutions pad
  *     kernel - stride on the left, causal transposed convolutions trim kernel - stride on
- *     the right; a streaming decoder emits exactly the non-streaming result frame by frame.
+ *     the right; a streaming codec emits exactly the non-streaming result frame by frame;
+ *   - ENCODE: "SEANet encoder, every stage" (Conv1d 1 -> n_filters, kernel `kernel`; per
+ *     stage, in the reversed ratio order, the residual unit then ELU -> Conv1d C -> 2C,
+ *     kernel 2r, stride r; ELU -> Conv1d -> dim, kernel last_kernel), the encoder
+ *     transformer (a separate stack), "Learned resampling around the quantizer" (Conv1d
+ *     dim -> dim, kernel 4, stride 2, no bias, the first position replicated as left
+ *     padding), and the split quantizer (semantic projection -> nearest entry of codebook
+ *     0; acoustic projection -> residual chain over codebooks 1..n_q-1).
  * Readings where the chapter is silent: RoPE turns adjacent pairs (2j, 2j+1) of each head
  * by position * rope_theta^(-2j/64); the attention scale is 1/sqrt(64); GELU is the erf
- * form; ELU has alpha 1; transformer positions count the 25 Hz grid from 0 at reset.
+ * form; ELU has alpha 1; transformer positions count the 25 Hz grid from 0 at reset;
+ * "nearest" is the smallest squared Euclidean distance (fp32), the lowest index on ties.
  *
  * Conventions (as in pm.h).
  *  - Calls are asynchronous on the CUDA stream given to pm_mimi_create; outputs are valid
@@ -91,6 +100,20 @@ typedef struct {
  * configuration is not supported. */
 int pm_mimi_tensor_count(const pm_mimi_config* cfg);
 
+/* The encoder's canonical tensor order (same layout conventions):
+ *      enc.0.w [n_filters][1][kernel], enc.0.b
+ *      per stage i (C = n_filters << i, r = ratios[n_ratios - 1 - i], h = C / compress):
+ *        res.w1 [h][C][res_kernel], res.b1 [h], res.w2 [C][h][1], res.b2 [C],
+ *        down.w [2C][C][2r], down.b [2C]
+ *      enc.out.w [dim][n_filters << n_ratios][last_kernel], enc.out.b [dim]
+ *      per block l < n_layers: the ten tensors of a decoder block (the encoder's own stack)
+ *      ds.weight [dim][dim][4] (the downsampler, no bias)
+ *      q.sem.in [cb_dim][dim], q.ac.in [cb_dim][dim] (input projections)
+ *      q.codebook.0 .. q.codebook.{n_q-1} [card][cb_dim] (the tables the decoder reads)
+ * Count, or -1 if the encoder does not support the configuration (it also needs card a
+ * multiple of 8 and dim a multiple of 128). */
+int pm_mimi_encoder_tensor_count(const pm_mimi_config* cfg);
+
 /* Create a decoder for up to cfg->B_max streams, all at frame 0.  tensors: n_tensors
  * device pointers in the canonical order above.  cuda_stream: the stream every call runs
  * on (NULL = legacy default stream).  PM_ERR_ARG for a bad configuration, pointer or
@@ -99,6 +122,23 @@ int pm_mimi_tensor_count(const pm_mimi_config* cfg);
  * pm_mimi_last_error(NULL) says why. */
 pm_status pm_mimi_create(const pm_mimi_config* cfg, const void* const* tensors, int n_tensors, void* cuda_stream,
                          pm_mimi_ctx** out);
+
+/* Create an encoder context (same conventions as pm_mimi_create; the tensors in the
+ * encoder's order).  pm_mimi_reset, pm_mimi_status, pm_mimi_get_frames, pm_mimi_last_error
+ * and pm_mimi_destroy serve both kinds; pm_mimi_decode on an encoder context, or
+ * pm_mimi_encode on a decoder context, is PM_ERR_STATE. */
+pm_status pm_mimi_encoder_create(const pm_mimi_config* cfg, const void* const* tensors, int n_tensors,
+                                 void* cuda_stream, pm_mimi_ctx** out);
+
+/* Encode the next frame of streams 0..B-1.
+ *  pcm     [B][frame_samples] fp32, host or device memory (host PCM is copied in through
+ *          pinned staging).
+ *  codes   [B][n_q] int32 out: semantic code then the acoustic codes; device, managed or
+ *          host-mapped memory, 4-byte aligned.
+ *  latent  [B][dim] fp32 out, or NULL: the unquantised latent after the downsampler.
+ * Each stream advances by one frame.  Every float input gives in-range codes (no device
+ * validation is needed); non-finite PCM gives unspecified codes. */
+pm_status pm_mimi_encode(pm_mimi_ctx* ctx, int B, const float* pcm, int32_t* codes, float* latent);
 
 /* Decode the next frame of streams 0..B-1.
  *  codes  [B][n_q] int32 code indices 0..card-1, host or device memory.  Host codes are
@@ -127,6 +167,9 @@ pm_status pm_mimi_decode(pm_mimi_ctx* ctx, int B, const int32_t* codes, float* p
 #define PM_MIMI_K_RES2 9
 #define PM_MIMI_K_CONV_LAST 10
 #define PM_MIMI_K_FINISH 11
+#define PM_MIMI_K_DOWN 12      /* encoder: a SEANet stride-r convolution */
+#define PM_MIMI_K_RESAMPLE 13  /* encoder: the latent downsampler */
+#define PM_MIMI_K_RVQ 14       /* encoder: input projections + residual quantisation */
 
 /* pm_mimi_decode launched kernel by kernel (not from the graph) with a CUDA event after
  * each launch, then synchronised: ms[i] is the device time between launch i's event and
@@ -135,6 +178,13 @@ pm_status pm_mimi_decode(pm_mimi_ctx* ctx, int B, const int32_t* codes, float* p
  * as pm_mimi_decode.  For measurement, not for serving: it creates and destroys events. */
 pm_status pm_mimi_profile(pm_mimi_ctx* ctx, int B, const int32_t* codes, float* pcm, float* ms, int32_t* kind,
                           int n_max, int* n);
+
+/* pm_mimi_encode launched kernel by kernel, timed the same way (the encoder's launches: the
+ * first convolution; per stage the residual unit's two convolutions and the strided
+ * convolution; the last convolution; the transformer; the downsampler; the quantiser; the
+ * finishing kernel). */
+pm_status pm_mimi_encode_profile(pm_mimi_ctx* ctx, int B, const float* pcm, int32_t* codes, float* latent,
+                                 float* ms, int32_t* kind, int n_max, int* n);
 
 /* Return the streams whose mask entry is nonzero (all streams if mask is NULL; a host
  * array of B_max entries) to frame 0 with empty history, ordered on the context's stream. */
@@ -151,7 +201,7 @@ pm_status pm_mimi_get_frames(pm_mimi_ctx* ctx, int32_t* frames);
  * pm_mimi_create on this thread failed. */
 const char* pm_mimi_last_error(const pm_mimi_ctx* ctx);
 
-/* Free everything the context owns (not the weights). */
+/* Free everything the context owns (not the weights); either kind. */
 void pm_mimi_destroy(pm_mimi_ctx* ctx);
 
 #ifdef __cplusplus

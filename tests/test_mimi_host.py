@@ -47,3 +47,17 @@ def test_generator_draws_are_seeded_and_scaled():
     assert abs(w.std() * (512 * 16) ** 0.5 - 1.0) < 0.01
     c = I.make_mimi_codes(I.MIMI_FULL, 50, 2)
     assert c.shape == (50, 2, 8) and c.min() >= 0 and c.max() < 2048
+
+
+def test_encoder_tensor_order_agrees():
+    for shape in (I.MIMI_SMALL, I.MIMI_FULL):
+        gen = I.mimi_encoder_tensor_specs(shape)
+        orc = [(n, tuple(s)) for n, s in M.encoder_tensor_specs(M.MimiShape(**shape))]
+        assert gen == orc
+        assert [n for n, _ in gen] == pm.mimi_encoder_tensor_names(shape)
+        cfg = pm.make_mimi_config(shape, B_max=1)
+        assert pm.lib().pm_mimi_encoder_tensor_count(C.byref(cfg)) == len(gen)
+    # the encoder's own limits: codebooks split over 8 CTAs
+    cfg = pm.make_mimi_config(dict(I.MIMI_SMALL, card=60), B_max=1)
+    assert pm.lib().pm_mimi_encoder_tensor_count(C.byref(cfg)) == -1
+    assert pm.lib().pm_mimi_tensor_count(C.byref(cfg)) > 0
