@@ -242,71 +242,83 @@ def mimi_work(shape: dict, B: int):
     return out
 
 
-def mimi_measure(B: int, steps: int, warmup: int, stream, flush, profile: bool = False):
-    """Frames/s of the streaming decoder at batch B: each timed call bracketed by CUDA
-    events, L2 flushed (256 MB written) between calls, since the decoder's 90 MB of
-    weights would otherwise stay in the 129 MB L2.  With profile, also per-launch times
-    of one call (pm_mimi_profile, queued behind a spin so host launch gaps do not count)."""
+def mimi_measure(B: int, steps: int, warmup: int, stream, flush, profile: bool = False, encoder: bool = False):
+    """Frames/s of the streaming decoder (or encoder) at batch B: each timed call bracketed
+    by CUDA events, L2 flushed (256 MB written) between calls, since the codec's 90 MB of
+    weights would otherwise stay in the 129 MB L2.  With profile, also per-launch times of
+    one call (queued behind a spin so host launch gaps do not count).  e2e: host codes (or
+    host PCM) in, PCM (or codes) out into pinned host memory, synchronised every frame."""
     import torch
     from full_duplex_speech_moshi_gb300 import pm
     shape = I.MIMI_FULL
-    W = pm.upload_weights(I.make_mimi_weights(shape))
-    dec = pm.MimiDecoder(shape, W, B_max=B, stream=stream.cuda_stream)
+    n_q, dim = shape["n_q"], shape["dim"]
     fs = pm.mimi_frame_samples(shape)
     n = warmup + steps
-    codes = torch.from_numpy(I.make_mimi_codes(shape, n + 1, B, seed=6100)).cuda()
-    pcm = torch.empty((B, fs), dtype=torch.float32, device="cuda")
+    if encoder:
+        W = pm.upload_weights(I.make_mimi_encoder_weights(shape))
+        ctx = pm.MimiEncoder(shape, W, B_max=B, stream=stream.cuda_stream)
+        x = torch.from_numpy(I.make_mimi_pcm((n + 3) * fs, B, seed=8100)).cuda()
+        inputs = [x[:, t * fs:(t + 1) * fs].contiguous() for t in range(n + 3)]
+        out = torch.empty((B, n_q), dtype=torch.int32, device="cuda")
+        call = lambda t: ctx.encode(B, inputs[t], out)
+        prof = lambda t: ctx.profile(B, inputs[t], out)
+    else:
+        W = pm.upload_weights(I.make_mimi_weights(shape))
+        ctx = pm.MimiDecoder(shape, W, B_max=B, stream=stream.cuda_stream)
+        codes = torch.from_numpy(I.make_mimi_codes(shape, n + 3, B, seed=6100)).cuda()
+        inputs = [codes[t] for t in range(n + 3)]
+        out = torch.empty((B, fs), dtype=torch.float32, device="cuda")
+        call = lambda t: ctx.decode(B, inputs[t], out)
+        prof = lambda t: ctx.profile(B, inputs[t], out)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for t in range(warmup):
-        dec.decode(B, codes[t], pcm)
+        call(t)
     for i in range(steps):
         flush.fill_(float(i))
         ev[i][0].record(stream)
-        dec.decode(B, codes[warmup + i], pcm)
+        call(warmup + i)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in ev]
     res = {"ms_mean": statistics.mean(ms), "ms_p50": statistics.median(ms), "frames_per_s": B * 1000.0 / statistics.mean(ms)}
     if profile:
-        prof = []
+        runs = []
         for rep in range(3):
             flush.fill_(1.0 + rep)
             torch.cuda._sleep(2_000_000)
-            prof.append(dec.profile(B, codes[n - 3 + rep], pcm))
-        res["profile"] = [(k, statistics.median(p[i][1] for p in prof)) for i, (k, _) in enumerate(prof[0])]
-    # end to end: host codes in, PCM out into pinned host memory, synchronised per frame
-    host_codes = I.make_mimi_codes(shape, steps, B, seed=6200)
-    host_pcm = torch.empty((B, fs), dtype=torch.float32).pin_memory()
-    dec.reset()
+            runs.append(prof(n + rep))
+        res["profile"] = [(k, statistics.median(r[i][1] for r in runs)) for i, (k, _) in enumerate(runs[0])]
+    ctx.reset()
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for t in range(steps):
-        dec.decode(B, host_codes[t], host_pcm)
-        stream.synchronize()
+    if encoder:
+        host_in = I.make_mimi_pcm(steps * fs, B, seed=8200)
+        host_out = torch.empty((B, n_q), dtype=torch.int32).pin_memory()
+        t0 = time.perf_counter()
+        for t in range(steps):
+            ctx.encode(B, host_in[:, t * fs:(t + 1) * fs], host_out)
+            stream.synchronize()
+        res["e2e_h2d_bytes"] = 4 * B * fs + 40
+        res["e2e_d2h_bytes"] = 4 * B * n_q
+    else:
+        host_in = I.make_mimi_codes(shape, steps, B, seed=6200)
+        host_out = torch.empty((B, fs), dtype=torch.float32).pin_memory()
+        t0 = time.perf_counter()
+        for t in range(steps):
+            ctx.decode(B, host_in[t], host_out)
+            stream.synchronize()
+        res["e2e_h2d_bytes"] = 4 * B * n_q + 40
+        res["e2e_d2h_bytes"] = 4 * B * fs
     res["e2e_frames_per_s"] = B * steps / (time.perf_counter() - t0)
-    res["e2e_h2d_bytes"] = 4 * B * I.MIMI_FULL["n_q"] + 16
-    res["e2e_d2h_bytes"] = 4 * B * fs
-    dec.close()
+    ctx.close()
     return res
 
 
-def run_mimi(args):
-    """The streaming Mimi decoder as its own JSON line: value = frames/s at B=1, the
-    B=8 stream-frames/s beside it, per-kind device times of one call, the roofline of the
-    kind with the largest share (fp32 FMA work against the ALU peak at the sampled clock, or
-    bytes against HBM), e2e through host memory, and the oracle's CPU rate."""
-    import torch
-    from full_duplex_speech_moshi_gb300 import pm  # noqa: F401
-    torch.cuda.set_device(0)
-    stream = torch.cuda.current_stream()
-    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
-    with ClockSampler(0) as clk:
-        r1 = mimi_measure(1, args.steps, args.warmup, stream, flush, profile=True)
-        r8 = mimi_measure(8, args.steps, args.warmup, stream, flush, profile=True)
-    clocks = clk.summary()
-    work = mimi_work(I.MIMI_FULL, 1)
+def mimi_roofline(profile, work, clocks):
+    """Roofline of the launch kind with the largest share of one profiled call: fp32 FMA work
+    against the ALU peak at the sampled clock, or bytes against HBM, whichever fraction is
+    larger."""
     by_kind = {}
-    for (k, ms), (by, fl) in zip(r1["profile"], work):
+    for (k, ms), (by, fl) in zip(profile, work):
         e = by_kind.setdefault(k, [0.0, 0, 0, 0])
         e[0] += ms
         e[1] += by
@@ -326,6 +338,59 @@ def run_mimi(args):
                 "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"}
     roof.update({"frac": roof["achieved"] / roof["peak"], "traffic": None, "kernel": dom, "launches": cnt,
                  "kernel_ms": t_ms / cnt, "share_of_call": t_ms / total})
+    return roof, {k: v[0] for k, v in by_kind.items()}, total
+
+
+def mimi_encoder_work(shape: dict, B: int):
+    """Algorithmic (bytes, flops) of each launch of one encode call, in launch order."""
+    s = dict(I.MIMI_FULL)
+    s.update(shape)
+    d, f, cb, nq, card = s["dim"], s["ffn"], s["cb_dim"], s["n_q"], s["card"]
+    T = 2
+    for r in s["ratios"]:
+        T *= r
+    C = s["n_filters"]
+    out = [(2 * C * s["kernel"] + 4 * B * T * (1 + 2 * C), 2 * C * s["kernel"] * T * B)]
+    for r in reversed(s["ratios"]):
+        h = C // s["compress"]
+        out.append((2 * h * C * s["res_kernel"] + 4 * B * T * (C + h), 2 * h * C * s["res_kernel"] * T * B))
+        out.append((2 * C * h + 4 * B * T * (h + 2 * C), 2 * C * h * T * B))
+        out.append((2 * 2 * C * C * 2 * r + 4 * B * (C * T + 2 * 2 * C * T // r), 2 * 2 * C * C * 2 * r * (T // r) * B))
+        C *= 2
+        T //= r
+    out.append((2 * d * C * s["last_kernel"] + 4 * B * T * (C + d), 2 * d * C * s["last_kernel"] * T * B))
+    q = 2 * B
+    for _ in range(s["n_layers"]):
+        out.append((2 * 3 * d * d + 4 * q * (d + 3 * d), 2 * 3 * d * d * q))
+        out.append((4 * q * 3 * d + 4 * q * d, 0))
+        out.append((2 * d * d + 4 * q * 2 * d, 2 * d * d * q))
+        out.append((2 * f * d + 4 * q * (d + f), 2 * f * d * q))
+        out.append((2 * d * f + 4 * q * (f + 2 * d), 2 * d * f * q))
+    out.append((2 * d * d * 4 + 4 * B * 3 * d, 2 * d * d * 4 * B))
+    # quantiser: projections, then every codebook row scanned once (3 flops per element)
+    out.append((2 * 2 * cb * d + 2 * nq * card * cb, (2 * 2 * cb * d + 3 * nq * card * cb) * B))
+    out.append((0, 0))
+    return out
+
+
+def run_mimi(args):
+    """The streaming Mimi codec as its own JSON line: value = decode frames/s at B=1, the
+    B=8 stream-frames/s beside it, per-kind device times of one call, the roofline of the
+    kind with the largest share, e2e through host memory, the oracle's CPU rate; and the
+    same figures for the encoder under "encoder"."""
+    import torch
+    from full_duplex_speech_moshi_gb300 import pm  # noqa: F401
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")
+    with ClockSampler(0) as clk:
+        r1 = mimi_measure(1, args.steps, args.warmup, stream, flush, profile=True)
+        r8 = mimi_measure(8, args.steps, args.warmup, stream, flush, profile=False)
+        e1 = mimi_measure(1, args.steps, args.warmup, stream, flush, profile=True, encoder=True)
+        e8 = mimi_measure(8, args.steps, args.warmup, stream, flush, profile=False, encoder=True)
+    clocks = clk.summary()
+    roof, kinds, total = mimi_roofline(r1["profile"], mimi_work(I.MIMI_FULL, 1), clocks)
+    eroof, ekinds, etotal = mimi_roofline(e1["profile"], mimi_encoder_work(I.MIMI_FULL, 1), clocks)
     cpu = None
     if not args.no_cpu_baseline:
         from oracle import mimi as M
@@ -336,19 +401,34 @@ def run_mimi(args):
         dt = time.perf_counter() - t0
         cpu = {"value": 8 / dt, "unit": "frames/s", "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"8 frames from reset decoded at once (non-streaming), float64 numpy, {dt:.1f} s"}
+        eorc = M.MimiEncoderOracle(M.MimiShape(**I.MIMI_FULL), I.make_mimi_encoder_weights(I.MIMI_FULL))
+        pcm = I.make_mimi_pcm(8 * 1920, 1, seed=8300)[0].astype(np.float64)
+        t0 = time.perf_counter()
+        eorc.encode(pcm)
+        edt = time.perf_counter() - t0
+        ecpu = {"value": 8 / edt, "unit": "frames/s", "cores": os.cpu_count(), "kind": "oracle",
+                "sample": f"8 frames from reset encoded at once (non-streaming), float64 numpy, {edt:.1f} s"}
+    n_dec = len(mimi_work(I.MIMI_FULL, 1))
+    n_enc = len(mimi_encoder_work(I.MIMI_FULL, 1))
     line = {"metric": MIMI_METRIC, "value": r1["frames_per_s"], "unit": "frames/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": r1["ms_mean"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (random-init bf16 weights, "
-            "uniform codes)", "config": {"workload": MIMI_WORKLOAD, "global_batch": 1,
-                                         "l2": "flushed between timed calls (256 MB written)"},
-            "roofline": roof,
-            "kernel_ms_by_kind": {k: v[0] for k, v in by_kind.items()},
-            "profiled_call_ms": total,
+            "uniform codes; seeded speech-band PCM for the encoder)",
+            "config": {"workload": MIMI_WORKLOAD, "global_batch": 1, "l2": "flushed between timed calls (256 MB written)"},
+            "roofline": roof, "kernel_ms_by_kind": kinds, "profiled_call_ms": total,
             "B8_stream_frames_per_s": r8["frames_per_s"], "B8_ms_per_step": r8["ms_mean"],
             "e2e": {"value": r1["e2e_frames_per_s"], "unit": "frames/s", "h2d_bytes_per_step": r1["e2e_h2d_bytes"],
                     "d2h_bytes_per_step": r1["e2e_d2h_bytes"]},
-            "gpu_launches": len(work) * args.steps, "clocks": clocks, "cpu_baseline": cpu,
-            "realtime_factor_B1": 80.0 / r1["ms_mean"]}
+            "gpu_launches": (n_dec + n_enc) * args.steps, "clocks": clocks, "cpu_baseline": cpu,
+            "realtime_factor_B1": 80.0 / r1["ms_mean"],
+            "encoder": {"metric": "Mimi encode frames/s (B=1, 1920 PCM samples -> 8 codes)",
+                        "value": e1["frames_per_s"], "ms_per_step": e1["ms_mean"],
+                        "B8_stream_frames_per_s": e8["frames_per_s"], "B8_ms_per_step": e8["ms_mean"],
+                        "roofline": eroof, "kernel_ms_by_kind": ekinds, "profiled_call_ms": etotal,
+                        "e2e": {"value": e1["e2e_frames_per_s"], "unit": "frames/s",
+                                "h2d_bytes_per_step": e1["e2e_h2d_bytes"], "d2h_bytes_per_step": e1["e2e_d2h_bytes"]},
+                        "cpu_baseline": None if args.no_cpu_baseline else ecpu,
+                        "realtime_factor_B1": 80.0 / e1["ms_mean"]}}
     print(json.dumps(line), flush=True)
 
 
@@ -715,6 +795,16 @@ def main():
         extras["B16_ragged_stream_frames_per_s"] = steps16 * B16
         extras["B16_ragged_gbs"] = bytes16 * steps16 / 1e9
         ctx16.close()
+        del kv16
+        torch.cuda.empty_cache()
+        # the Mimi codec on the same 80 ms frame (B=1, L2 flushed between calls; the full
+        # line with rooflines is --case mimi)
+        flush_m = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device=dev)
+        md = mimi_measure(1, 50, 5, stream, flush_m)
+        me = mimi_measure(1, 50, 5, stream, flush_m, encoder=True)
+        extras["mimi_decode_frames_per_s"] = md["frames_per_s"]
+        extras["mimi_encode_frames_per_s"] = me["frames_per_s"]
+        del flush_m
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and BB == 1:
