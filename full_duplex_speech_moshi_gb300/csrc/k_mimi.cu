@@ -791,24 +791,33 @@ __global__ void __launch_bounds__(256) k_mimi_rvq(const RvqParams p) {
             // ph 0: search 0 = semantic codebook 0 on z[0], search 1 = acoustic codebook 1
             const int j = ph == 0 ? sidx : ph + 1;
             const float* v = z + (j == 0 ? 0 : p.cb_dim);
+            // four entries in flight per warp: warp w takes entries 4 w .. 4 w + 3, + 32, ...
             unsigned long long best = ~0ull;
-            for (int en = warp; en < per; en += 8) {
-                const int idx = e0 + en;
-                const uint16_t* c = p.cb[j] + (size_t)idx * p.cb_dim;
-                float d = 0.f;
+            for (int en0 = 4 * warp; en0 < per; en0 += 32) {
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int k = 8 * lane; k < p.cb_dim; k += 256) {
-                    const uint4 cv = *reinterpret_cast<const uint4*>(c + k);
                     const float4 x0 = *reinterpret_cast<const float4*>(v + k);
                     const float4 x1 = *reinterpret_cast<const float4*>(v + k + 4);
-                    const float d0 = x0.x - bf16lo(cv.x), d1 = x0.y - bf16hi(cv.x), d2 = x0.z - bf16lo(cv.y),
-                                d3 = x0.w - bf16hi(cv.y), d4 = x1.x - bf16lo(cv.z), d5 = x1.y - bf16hi(cv.z),
-                                d6 = x1.z - bf16lo(cv.w), d7 = x1.w - bf16hi(cv.w);
-                    d = fmaf(d0, d0, fmaf(d1, d1, fmaf(d2, d2, fmaf(d3, d3, d))));
-                    d = fmaf(d4, d4, fmaf(d5, d5, fmaf(d6, d6, fmaf(d7, d7, d))));
+                    uint4 cv[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        cv[u] = en0 + u < per ? __ldg(reinterpret_cast<const uint4*>(p.cb[j] + (size_t)(e0 + en0 + u) * p.cb_dim + k))
+                                              : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float d0 = x0.x - bf16lo(cv[u].x), d1 = x0.y - bf16hi(cv[u].x), d2 = x0.z - bf16lo(cv[u].y),
+                                    d3 = x0.w - bf16hi(cv[u].y), d4 = x1.x - bf16lo(cv[u].z), d5 = x1.y - bf16hi(cv[u].z),
+                                    d6 = x1.z - bf16lo(cv[u].w), d7 = x1.w - bf16hi(cv[u].w);
+                        float a = fmaf(d0, d0, fmaf(d1, d1, fmaf(d2, d2, fmaf(d3, d3, d[u]))));
+                        d[u] = fmaf(d4, d4, fmaf(d5, d5, fmaf(d6, d6, fmaf(d7, d7, a))));
+                    }
                 }
-                d = warp_sum(d);
-                const unsigned long long key = ((unsigned long long)float_order_key(d) << 32) | (uint32_t)idx;
-                best = key < best ? key : best;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float du = warp_sum(d[u]);
+                    const unsigned long long key = ((unsigned long long)float_order_key(du) << 32) | (uint32_t)(e0 + en0 + u);
+                    if (en0 + u < per && key < best) best = key;
+                }
             }
             if (lane == 0) wkey[sidx][warp] = best;
         }
