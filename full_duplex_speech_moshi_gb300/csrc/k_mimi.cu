@@ -718,9 +718,6 @@ __device__ __forceinline__ void st_cluster_u64(unsigned long long* local, uint32
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
     asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(r), "l"(v) : "memory");
 }
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
 struct RvqParams {
     const float* e;            // [B][dim] the latent after the downsampler
@@ -728,31 +725,54 @@ struct RvqParams {
     const uint16_t* w_ac;      // acoustic input projection [cb_dim][dim]
     const uint16_t* cb[16];    // codebooks [card][cb_dim]
     const MimiIO* io;          // codes_out, latent_out
+    uint32_t* status;          // sticky status word (bit 2: a bounded wait ran out)
     int dim, cb_dim, card, n_q;
 };
 
 // grid (RQ, B), clusters of RQ along x, 256 threads.  CTA k of a stream's cluster makes
 // projection rows k R2 .. (R2 = 2 cb_dim / RQ; the semantic rows first) and sends them to
-// every CTA of the cluster; then per level it scans entries k card/RQ .. of the codebook
-// (squared distance, a warp per entry), and the cluster agrees on the smallest
-// (distance, index) key through shared-memory slots and a cluster barrier.  The semantic
-// search runs beside the first acoustic level; each acoustic level subtracts the chosen
-// entry from the residual all CTAs hold.
+// every CTA of the cluster.  Its slice of every codebook (entries k card/RQ .. + card/RQ)
+// streams through shared memory in halves, two buffers, by bulk copies on the copy engine
+// -- the slices do not depend on the latent, so they run a level ahead of the scan; per
+// level the CTA scans its slice (squared distance, a warp per entry, four at a time) and
+// the cluster agrees on the smallest (distance, index) key through shared-memory slots
+// and a cluster barrier.  The semantic search runs beside the first acoustic level; each
+// acoustic level subtracts the chosen entry from the residual all CTAs hold.
 __global__ void __launch_bounds__(256) k_mimi_rvq(const RvqParams p) {
     extern __shared__ __align__(16) uint8_t smraw[];
     __shared__ unsigned long long keys[2][2][RQ];  // [phase parity][search][rank]
-    __shared__ unsigned long long wkey[2][8];
-    const int R2 = 2 * p.cb_dim / RQ;
-    uint16_t* wsm = reinterpret_cast<uint16_t*>(smraw);                  // [R2][dim]
-    float* es = reinterpret_cast<float*>(smraw + (size_t)R2 * p.dim * 2); // [dim]
-    float* z = es + p.dim;                                               // [2][cb_dim]: semantic, acoustic residual
+    __shared__ unsigned long long wkey[8];
+    __shared__ __align__(8) uint64_t full[2];      // one mbarrier per codebook buffer
+    const int R2 = 2 * p.cb_dim / RQ, per = p.card / RQ, half = per / 2;
+    const uint32_t chunk = (uint32_t)half * p.cb_dim * 2;
+    uint16_t* cbuf = reinterpret_cast<uint16_t*>(smraw);                                  // [2][half][cb_dim]
+    uint16_t* wsm = reinterpret_cast<uint16_t*>(smraw + 2 * (size_t)chunk);              // [R2][dim]
+    float* es = reinterpret_cast<float*>(smraw + 2 * (size_t)chunk + (size_t)R2 * p.dim * 2);  // [dim]
+    float* z = es + p.dim;                                                               // [2][cb_dim]
     const uint32_t rank = cluster_rank();
     const int b = blockIdx.y, t = threadIdx.x, warp = t >> 5, lane = t & 31;
-    const int per = p.card / RQ, e0 = (int)rank * per;
+    const int e0 = (int)rank * per, n_chunks = 2 * p.n_q;
+    // chunk c: codebook c / 2, half c % 2 of this CTA's slice, into buffer c % 2
+    auto issue = [&](int c) {
+        uint64_t* bar = &full[c & 1];
+        mbar_arrive_expect_tx(bar, chunk);
+        bulk_g2s(cbuf + (size_t)(c & 1) * half * p.cb_dim, p.cb[c >> 1] + (size_t)(e0 + (c & 1) * half) * p.cb_dim,
+                 chunk, bar, l2_evict_first_policy());
+    };
     pdl_trigger();
     // every CTA of the cluster must be running before any stores into it: arrive now, wait
     // before the first remote store
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    if (t == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (t == 0) {
+        issue(0);
+        issue(1);
+    }
     {
         const int r0 = (int)rank * R2;  // projection rows of this CTA
         const int n8 = R2 * p.dim / 8;
@@ -764,7 +784,6 @@ __global__ void __launch_bounds__(256) k_mimi_rvq(const RvqParams p) {
                 return __ldg(reinterpret_cast<const uint4*>(w + k));
             },
             [&](int i, uint4 v) { reinterpret_cast<uint4*>(wsm)[i] = v; });
-        if (t < p.n_q) prefetch_l2_bulk(p.cb[t] + (size_t)e0 * p.cb_dim, (uint32_t)(per * p.cb_dim * 2));
     }
     pdl_wait();
     for (int k = t; k < p.dim; k += blockDim.x) es[k] = p.e[(size_t)b * p.dim + k];
@@ -785,53 +804,60 @@ __global__ void __launch_bounds__(256) k_mimi_rvq(const RvqParams p) {
         if (lane < RQ) st_cluster_f32(z + row, (uint32_t)lane, a);  // row < cb_dim: semantic
     }
     cluster_sync();
+    bool ok = true;
+    int c = 0;  // next chunk to consume
     for (int ph = 0; ph + 1 < p.n_q; ++ph) {
         const int ns = ph == 0 ? 2 : 1;
         for (int sidx = 0; sidx < ns; ++sidx) {
             // ph 0: search 0 = semantic codebook 0 on z[0], search 1 = acoustic codebook 1
             const int j = ph == 0 ? sidx : ph + 1;
             const float* v = z + (j == 0 ? 0 : p.cb_dim);
-            // four entries in flight per warp: warp w takes entries 4 w .. 4 w + 3, + 32, ...
             unsigned long long best = ~0ull;
-            for (int en0 = 4 * warp; en0 < per; en0 += 32) {
-                float d[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int k = 8 * lane; k < p.cb_dim; k += 256) {
-                    const float4 x0 = *reinterpret_cast<const float4*>(v + k);
-                    const float4 x1 = *reinterpret_cast<const float4*>(v + k + 4);
-                    uint4 cv[4];
+            for (int h = 0; h < 2; ++h, ++c) {
+                if (!mbar_wait_n(&full[c & 1], (uint32_t)(c >> 1) & 1u, PM_SPIN_LIMIT)) ok = false;
+                const uint16_t* cb = cbuf + (size_t)(c & 1) * half * p.cb_dim;
+                // four entries in flight per warp: warp w takes entries 4 w .. 4 w + 3, + 32, ...
+                for (int en0 = 4 * warp; en0 < half; en0 += 32) {
+                    float d[4] = {0.f, 0.f, 0.f, 0.f};
+                    for (int k = 8 * lane; k < p.cb_dim; k += 256) {
+                        const float4 x0 = *reinterpret_cast<const float4*>(v + k);
+                        const float4 x1 = *reinterpret_cast<const float4*>(v + k + 4);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        cv[u] = en0 + u < per ? __ldg(reinterpret_cast<const uint4*>(p.cb[j] + (size_t)(e0 + en0 + u) * p.cb_dim + k))
-                                              : make_uint4(0u, 0u, 0u, 0u);
+                        for (int u = 0; u < 4; ++u) {
+                            if (en0 + u >= half) break;
+                            const uint4 cv = *reinterpret_cast<const uint4*>(cb + (size_t)(en0 + u) * p.cb_dim + k);
+                            const float d0 = x0.x - bf16lo(cv.x), d1 = x0.y - bf16hi(cv.x), d2 = x0.z - bf16lo(cv.y),
+                                        d3 = x0.w - bf16hi(cv.y), d4 = x1.x - bf16lo(cv.z), d5 = x1.y - bf16hi(cv.z),
+                                        d6 = x1.z - bf16lo(cv.w), d7 = x1.w - bf16hi(cv.w);
+                            const float a = fmaf(d0, d0, fmaf(d1, d1, fmaf(d2, d2, fmaf(d3, d3, d[u]))));
+                            d[u] = fmaf(d4, d4, fmaf(d5, d5, fmaf(d6, d6, fmaf(d7, d7, a))));
+                        }
+                    }
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const float d0 = x0.x - bf16lo(cv[u].x), d1 = x0.y - bf16hi(cv[u].x), d2 = x0.z - bf16lo(cv[u].y),
-                                    d3 = x0.w - bf16hi(cv[u].y), d4 = x1.x - bf16lo(cv[u].z), d5 = x1.y - bf16hi(cv[u].z),
-                                    d6 = x1.z - bf16lo(cv[u].w), d7 = x1.w - bf16hi(cv[u].w);
-                        float a = fmaf(d0, d0, fmaf(d1, d1, fmaf(d2, d2, fmaf(d3, d3, d[u]))));
-                        d[u] = fmaf(d4, d4, fmaf(d5, d5, fmaf(d6, d6, fmaf(d7, d7, a))));
+                        const float du = warp_sum(d[u]);
+                        const uint32_t idx = (uint32_t)(e0 + h * half + en0 + u);
+                        const unsigned long long key = ((unsigned long long)float_order_key(du) << 32) | idx;
+                        if (en0 + u < half && key < best) best = key;
                     }
                 }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float du = warp_sum(d[u]);
-                    const unsigned long long key = ((unsigned long long)float_order_key(du) << 32) | (uint32_t)(e0 + en0 + u);
-                    if (en0 + u < per && key < best) best = key;
-                }
+                __syncthreads();  // every warp is done with this buffer
+                if (t == 0 && c + 2 < n_chunks) issue(c + 2);
             }
-            if (lane == 0) wkey[sidx][warp] = best;
-        }
-        __syncthreads();
-        if (t < ns) {
-            unsigned long long m = wkey[t][0];
-            for (int w = 1; w < 8; ++w) m = wkey[t][w] < m ? wkey[t][w] : m;
-            for (uint32_t r = 0; r < RQ; ++r) st_cluster_u64(&keys[ph & 1][t][rank], r, m);
+            if (lane == 0) wkey[warp] = best;
+            __syncthreads();
+            if (t == 0) {
+                unsigned long long m = wkey[0];
+                for (int w = 1; w < 8; ++w) m = wkey[w] < m ? wkey[w] : m;
+                for (uint32_t r = 0; r < RQ; ++r) st_cluster_u64(&keys[ph & 1][sidx][rank], r, m);
+            }
+            __syncthreads();
         }
         cluster_sync();
         for (int sidx = 0; sidx < ns; ++sidx) {
             unsigned long long m = keys[ph & 1][sidx][0];
             for (int r = 1; r < RQ; ++r) m = keys[ph & 1][sidx][r] < m ? keys[ph & 1][sidx][r] : m;
-            const int code = (int)(uint32_t)(m & 0xFFFFFFFFull);
+            const int code = (int)(uint32_t)(m & 0xFFFFFFFFull) % p.card;
             const int j = ph == 0 ? sidx : ph + 1;
             if (rank == 0 && t == 0) p.io->codes_out[(size_t)b * p.n_q + j] = code;
             if (j > 0)  // the acoustic residual moves on
@@ -839,11 +865,14 @@ __global__ void __launch_bounds__(256) k_mimi_rvq(const RvqParams p) {
         }
         __syncthreads();
     }
+    if (!ok && t == 0) atomicOr(p.status, 2u);
     if (rank == 0 && p.io->latent_out)
         for (int k = t; k < p.dim; k += blockDim.x) p.io->latent_out[(size_t)b * p.dim + k] = es[k];
 }
 
-size_t rvq_smem(int dim, int cb_dim) { return (size_t)(2 * cb_dim / RQ) * dim * 2 + 4u * (size_t)(dim + 2 * cb_dim); }
+size_t rvq_smem(int dim, int cb_dim, int card) {
+    return 2 * (size_t)(card / RQ / 2) * cb_dim * 2 + (size_t)(2 * cb_dim / RQ) * dim * 2 + 4u * (size_t)(dim + 2 * cb_dim);
+}
 
 // tap-major relayout, once at creation: Conv1d W [Cout][Cin/S][NT S] -> Wt [Cout][NT][Cin]
 // with input channel ci' = ci S + p taking kernel index m S + p (S = 1: Wt[co][m][ci] =
@@ -987,7 +1016,7 @@ const char* mimi_check(const pm_mimi_config* c) {
 
 // the encoder's extra constraints (the cluster search and its projection slices)
 const char* mimi_encoder_check(const pm_mimi_config* c) {
-    if (c->card % RQ != 0) return "the encoder needs card to be a multiple of 8";
+    if (c->card % (2 * RQ) != 0) return "the encoder needs card to be a multiple of 16";
     if ((2 * c->cb_dim) % RQ != 0 || c->cb_dim % 8 != 0) return "the encoder needs cb_dim a multiple of 8";
     if (c->dim % 128 != 0) return "the encoder needs dim a multiple of 128";
     return nullptr;
@@ -1330,6 +1359,7 @@ pm_status record_encoder(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk) {
     rp.w_ac = c->w[ix.ac_in];
     for (int j = 0; j < f.n_q; ++j) rp.cb[j] = c->w[ix.cb0 + j];
     rp.io = c->io;
+    rp.status = c->st.status;
     rp.dim = f.dim;
     rp.cb_dim = f.cb_dim;
     rp.card = f.card;
@@ -1338,7 +1368,7 @@ pm_status record_encoder(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(RQ, (unsigned)B);
         cfg.blockDim = dim3(256);
-        cfg.dynamicSmemBytes = rvq_smem(f.dim, f.cb_dim);
+        cfg.dynamicSmemBytes = rvq_smem(f.dim, f.cb_dim, f.card);
         cfg.stream = s;
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1359,7 +1389,7 @@ pm_status record_encoder(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk) {
 size_t mimi_smem_need(const pm_mimi_config& f, const std::vector<MimiLayer>& layers, int encoder) {
     size_t m = gemv_smem(2 * f.B_max, f.dim > f.ffn ? f.dim : f.ffn);
     if (attn_smem(f.ctx) > m) m = attn_smem(f.ctx);
-    if (encoder && rvq_smem(f.dim, f.cb_dim) > m) m = rvq_smem(f.dim, f.cb_dim);
+    if (encoder && rvq_smem(f.dim, f.cb_dim, f.card) > m) m = rvq_smem(f.dim, f.cb_dim, f.card);
     for (const MimiLayer& L : layers)
         for (int B : {1, f.B_max}) {
             const ConvLaunch cl = conv_launch(L, B);
@@ -1785,6 +1815,7 @@ extern "C" pm_status pm_mimi_status(pm_mimi_ctx* c) {
     uint32_t s = 0;
     if (cudaMemcpy(&s, c->st.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess || cudaMemset(c->st.status, 0, 4) != cudaSuccess)
         return mfail(c, PM_ERR_CUDA, "pm_mimi_status: read");
+    if (s & 2u) return mfail(c, PM_ERR_TIMEOUT, "a bounded wait of the quantiser ran out (that call's codes are undefined)");
     return s ? mfail(c, PM_ERR_INVALID_ID, "a code given in device memory was out of range (that call was a no-op)") : PM_OK;
 }
 
