@@ -795,6 +795,21 @@ def main():
         extras["B16_ragged_stream_frames_per_s"] = steps16 * B16
         extras["B16_ragged_gbs"] = bytes16 * steps16 / 1e9
         ctx16.close()
+        # the same frames on the tcgen05 GEMM (PM_FLAG_BATCHED_TCGEN05), for comparison
+        ctx16 = pm.Context(s.asdict(), W, kv16, B_max=B16, depformer=False, stream=stream.cuda_stream,
+                           flags=pm.PM_FLAG_BATCHED_TCGEN05)
+        ctx16.set_positions([int(v) for v in L16])
+        for t in range(8):
+            ctx16.frame_step(B16, ids16[t], lg16, None, None)
+        torch.cuda.synchronize()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for t in range(64):
+            ctx16.frame_step(B16, ids16[8 + t], lg16, None, None)
+        b_.record(stream)
+        torch.cuda.synchronize()
+        extras["B16_ragged_tcgen05_stream_frames_per_s"] = 64 / (a.elapsed_time(b_) / 1000.0) * B16
+        ctx16.close()
         del kv16
         torch.cuda.empty_cache()
         # the Mimi codec on the same 80 ms frame (B=1, L2 flushed between calls; the full

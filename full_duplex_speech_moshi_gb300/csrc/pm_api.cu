@@ -420,13 +420,18 @@ static pm_status record_frame(pm_ctx* c, int B, cudaStream_t s) {
 }
 
 
-static int npad_for(int B) { return B <= 16 ? 16 : (B <= 32 ? 32 : 64); }
+// batch columns of the batched paths: 16 = the warp-MMA GEMV (2 <= B <= 16), 32 / 64 = the
+// tcgen05 GEMM; PM_FLAG_BATCHED_TCGEN05 sends B <= 16 to the GEMM as well
+static int npad_for(const pm_ctx* c, int B) {
+    if (c->cfg.flags & PM_FLAG_BATCHED_TCGEN05) return B <= 32 ? 32 : 64;
+    return B <= 16 ? 16 : (B <= 32 ? 32 : 64);
+}
 
 // B >= 2: every projection on the tensor cores (k_gemm_tc), same kernel families and order
 // `seq`: a prefill pass -- the B rows are frames pos .. pos+B-1 of stream io->seq_stream
 static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq) {
     const pm_config& f = c->cfg;
-    const int D = f.D, F = f.ffn, npad = npad_for(B);
+    const int D = f.D, F = f.ffn, npad = npad_for(c, B);
     if (npad > c->npad_max) return fail(c, PM_ERR_UNSUPPORTED, "batch larger than the tensor-core buffers");
     const bool pdl = c->prof_ev == nullptr;
     if (seq) {

@@ -48,6 +48,7 @@ class pm_config(C.Structure):
 PM_FLAG_FRAME_PROGRAM = 1
 PM_FLAG_PINNED_RING = 2
 PM_FLAG_DEPFORMER_CHAIN = 4
+PM_FLAG_BATCHED_TCGEN05 = 8
 
 
 _PP = C.POINTER(C.c_void_p)
@@ -444,7 +445,8 @@ def mimi_encoder_tensor_names(shape: dict) -> List[str]:
 
 class _MimiContext:
     """Owns one pm_mimi_ctx (decoder or encoder).  `weights` maps the canonical tensor
-    names to bf16 device tensors, which the caller keeps alive."""
+    names to bf16 device tensors; the context holds a reference to each, since the library
+    reads them on every call."""
 
     _encoder = False
 
@@ -461,7 +463,8 @@ class _MimiContext:
         n = count(C.byref(self.cfg))
         if n != len(names):
             raise PMError(PM_ERR_ARG, f"unsupported Mimi configuration (tensor count {n})")
-        self._ptrs = (C.c_void_p * len(names))(*[_ptr(weights[k]) for k in names])
+        self._weights = [weights[k] for k in names]
+        self._ptrs = (C.c_void_p * len(names))(*[_ptr(w) for w in self._weights])
         h = C.c_void_p()
         st = create(C.byref(self.cfg), self._ptrs, len(names), stream or None, C.byref(h))
         if st != PM_OK:

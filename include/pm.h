@@ -110,6 +110,12 @@ typedef struct {
  * room for dep_H clusters, and is not used while depth codes are sampled or for B > 1. */
 #define PM_FLAG_DEPFORMER_CHAIN 4u
 
+/* pm_config.flags: run batches of 2..16 streams on the tcgen05 GEMM (32 batch columns)
+ * instead of the warp-level MMA GEMV.  For comparison only: the GEMM takes bf16 activation
+ * operands without the rounding-remainder plane, which at B = 16 moved a greedy token at a
+ * top-2 gap of 1.3e-2 (the default path carries the remainder). */
+#define PM_FLAG_BATCHED_TCGEN05 8u
+
 /* Temporal weights: device pointers.  Per-layer members point to host arrays of
  * n_layers device pointers (copied by pm_create). */
 typedef struct {

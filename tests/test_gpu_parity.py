@@ -128,13 +128,14 @@ def test_batched_ragged_history(pair):
     assert pair.ctx.get_positions()[:B] == list(L + 4)
 
 
-@pytest.mark.parametrize("B", [12, 20])
-def test_batched_paths_by_batch_size(B):
+@pytest.mark.parametrize("B,flags", [(12, 0), (20, 0), (12, 8)])
+def test_batched_paths_by_batch_size(B, flags):
     """B = 12: the batched GEMV with two 8-column MMA groups (B <= 16); B = 20: the
-    tensor-core path (N = 32).  Streams start at staggered positions with seeded K/V
-    history and run past the ring's wrap."""
+    tensor-core path (N = 32); B = 12 with PM_FLAG_BATCHED_TCGEN05 (8): the tensor-core
+    path for a batch the GEMV would take.  Streams start at staggered positions with
+    seeded K/V history and run past the ring's wrap."""
     s = small_shape()
-    p = Pair(s, B_max=B, depformer=False)
+    p = Pair(s, B_max=B, depformer=False, flags=flags)
     try:
         torch = p.torch
         L = 1 + (np.arange(B, dtype=np.int32) * 7) % (s.ctx + 9)
