@@ -432,6 +432,60 @@ def run_mimi(args):
     print(json.dumps(line), flush=True)
 
 
+def run_depformer(args):
+    """The B=1 depformer call alone (16 positions x 6 blocks after one temporal frame): ms
+    per call on the default persistent launch and on the chain of one kernel per projection
+    (PM_FLAG_DEPFORMER_CHAIN), and the weight rate against the measured HBM peak.  The
+    2.67 GB of weights per call exceed L2, so no flush is needed."""
+    import torch
+    from full_duplex_speech_moshi_gb300 import pm
+    torch.cuda.set_device(0)
+    s = I.FULL if args.layers == 32 else I.ModelShape(n_layers=args.layers)
+    dev = "cuda"
+    stream = torch.cuda.current_stream()
+    W = I.make_weights_device(s, depformer=True, seed=1000, device=dev)
+    ids = torch.from_numpy(I.make_ids(s, 4, seed=2000)[:, 0].copy()).to(dev)
+    sup = torch.from_numpy(I.make_supplied_codes(s, 64, seed=4000)[:, 0].copy()).to(dev)
+    logits = torch.empty((1, s.text_out), dtype=torch.float32, device=dev)
+    hidden = torch.empty((1, s.D), dtype=torch.float32, device=dev)
+    token = torch.empty((1,), dtype=torch.int32, device=dev)
+    dl = torch.empty((1, s.dep_steps, s.dep_card), dtype=torch.float32, device=dev)
+    dc = torch.empty((1, s.dep_steps), dtype=torch.int32, device=dev)
+    out = {}
+    with ClockSampler(0) as clk:
+        for name, flags in (("persistent", 0), ("chain", pm.PM_FLAG_DEPFORMER_CHAIN)):
+            kv = pm.alloc_kv_cache(pm.make_config(s.asdict(), 1, True, flags))
+            ctx = pm.Context(s.asdict(), W, kv, B_max=1, depformer=True, stream=stream.cuda_stream, flags=flags)
+            ctx.frame_step(1, ids[0:1], logits, hidden, token)
+            for t in range(args.warmup):
+                ctx.depformer_step(1, None, None, sup[t % 64], dl, dc)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for t in range(args.steps):
+                ctx.depformer_step(1, None, None, sup[t % 64], dl, dc)
+            b.record(stream)
+            torch.cuda.synchronize()
+            out[name] = a.elapsed_time(b) / args.steps
+            ctx.close()
+            del kv
+            torch.cuda.empty_cache()
+    peak, src = load_peaks()
+    gbs = DEP_BYTES / (out["persistent"] / 1000.0) / 1e9
+    line = {"case": "depformer", "metric": "depformer ms per call (B=1, 16 positions x 6 blocks)",
+            "value": out["persistent"], "unit": "ms", "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "chain_ms": out["chain"], "dtype": "bf16",
+            "data": "synthetic (random-init bf16 weights, seeded supplied codes)",
+            "config": {"workload": "depformer dim 1024, 6 blocks x 16 positions, 16 heads, ctx 8, FFN 2816, "
+                                   "input projection 4096 -> 1024, heads [2048,1024]",
+                       "weight_bytes_per_call": DEP_BYTES, "l2": "weights (2.67 GB) exceed L2"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "traffic": None, "kernel": "k_depth_fused (one launch per call)",
+                         "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"},
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def run_case(args):
     """Secondary workloads, one JSON line each (not the headline step):
 
@@ -516,8 +570,8 @@ def main():
                     help="conversations per step (1 = the workload; 8 = the metric's batched case)")
     ap.add_argument("--layers", type=int, default=32,
                     help="temporal blocks (32 = the workload; fewer only for small profiler captures)")
-    ap.add_argument("--case", default="frame", choices=["frame", "prefill", "sample", "mimi"],
-                    help="frame = the headline decode step; prefill / sample / mimi = secondary workloads")
+    ap.add_argument("--case", default="frame", choices=["frame", "prefill", "sample", "mimi", "depformer"],
+                    help="frame = the headline decode step; prefill / sample / mimi / depformer = secondary workloads")
     ap.add_argument("--full", type=int, default=1, help="prefill case: also prime a full history")
     args = ap.parse_args()
     assert args.warmup >= 3
@@ -525,6 +579,8 @@ def main():
         return run_reference(args)
     if args.case == "mimi":
         return run_mimi(args)
+    if args.case == "depformer":
+        return run_depformer(args)
     if args.case != "frame":
         return run_case(args)
 
