@@ -43,7 +43,7 @@
 // Tiling policy: weight stages in the ring (8-column and 16-column variants), resident
 // CTAs per SM.
 #ifndef PM_MG_NST8
-#define PM_MG_NST8 5
+#define PM_MG_NST8 4
 #endif
 #ifndef PM_MG_NST16
 #define PM_MG_NST16 4
@@ -61,7 +61,6 @@ constexpr int PIECE = 32;               // k elements per warp piece (two MMAs)
 constexpr int PPW = KC / PIECE / CW;    // pieces per warp per chunk
 constexpr int SLOT = KC * 2;            // bytes per staged row (dense: the tensor copy's box)
 constexpr int STAGE = 16 * SLOT;        // one 16-row weight tile x one chunk
-constexpr int XST = 1;                  // activation chunks in flight (operand + remainder each)
 constexpr int MAXT = PM_MG_MAX_TILES;   // 16-row tiles per CTA (text head)
 constexpr int LO = 16;                  // row of the operand buffers where the remainder plane starts
 constexpr int NPX = 16;                 // batch rows of the operand buffers
@@ -115,6 +114,10 @@ __device__ __forceinline__ void mma_bf16(float* d, uint32_t a0, uint32_t a1, uin
 template <int NB>
 struct MgLayout {
     static constexpr int NST = NB == 8 ? PM_MG_NST8 : PM_MG_NST16;
+    // activation chunks in flight: two at 8 columns, so a CTA with few tiles (W_O,
+    // linear_out) does not wait out each chunk's load; at 16 columns the second slot would
+    // cost a weight stage the ring cannot spare at two CTAs per SM
+    static constexpr int XST = NB == 8 ? 2 : 1;
     // one activation chunk: NB rows x 512 elements of the bf16 operand, then NB rows of its
     // rounding remainder
     static constexpr int XSLOT = 2 * NB * SLOT;
@@ -133,6 +136,7 @@ __global__ void __launch_bounds__(THREADS, PM_MG_CTAS_PER_SM)
     constexpr int RPU = MODE == M_ROW ? 1 : 2;
     constexpr int NST = MgLayout<NB>::NST;
     constexpr int XSLOT = MgLayout<NB>::XSLOT;
+    constexpr int XST = MgLayout<NB>::XST;
     constexpr int MT = maxt_of(EPI, NB);
     uint8_t* ring = smem;
     uint8_t* xring = smem + (size_t)NST * STAGE;
