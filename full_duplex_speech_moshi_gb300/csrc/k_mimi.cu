@@ -59,7 +59,8 @@ struct MimiState {
     int32_t* frame;     // [B_max] frames decoded since reset (state parity = frame & 1)
     int32_t* pos;       // [B_max] 25 Hz position of the frame's first position
     uint32_t* abort;    // [1] nonzero: this call's codes were invalid (nothing advances)
-    uint32_t* status;   // [1] sticky: an invalid device code was seen
+    uint32_t* status;   // [1] sticky: bit 0 an invalid device code, bit 1 a wait ran out
+    const uint32_t* wait_budget;  // [1] polls of the quantiser's copy waits
 };
 
 __device__ __forceinline__ float bf(const uint16_t* p, size_t i) { return __uint_as_float((uint32_t)p[i] << 16); }
@@ -725,7 +726,7 @@ struct RvqParams {
     const uint16_t* w_ac;      // acoustic input projection [cb_dim][dim]
     const uint16_t* cb[16];    // codebooks [card][cb_dim]
     const MimiIO* io;          // codes_out, latent_out
-    uint32_t* status;          // sticky status word (bit 2: a bounded wait ran out)
+    MimiState st;              // status word (bit 1: a bounded wait ran out) and wait budget
     int dim, cb_dim, card, n_q;
 };
 
@@ -752,9 +753,12 @@ __global__ void __launch_bounds__(256) k_mimi_rvq(const RvqParams p) {
     const uint32_t rank = cluster_rank();
     const int b = blockIdx.y, t = threadIdx.x, warp = t >> 5, lane = t & 31;
     const int e0 = (int)rank * per, n_chunks = 2 * p.n_q;
+    const uint32_t budget = *(volatile const uint32_t*)p.st.wait_budget;
+    int n_issued[2] = {0, 0};  // thread 0: copies issued into each buffer
     // chunk c: codebook c / 2, half c % 2 of this CTA's slice, into buffer c % 2
     auto issue = [&](int c) {
         uint64_t* bar = &full[c & 1];
+        ++n_issued[c & 1];
         mbar_arrive_expect_tx(bar, chunk);
         bulk_g2s(cbuf + (size_t)(c & 1) * half * p.cb_dim, p.cb[c >> 1] + (size_t)(e0 + (c & 1) * half) * p.cb_dim,
                  chunk, bar, l2_evict_first_policy());
@@ -814,7 +818,7 @@ __global__ void __launch_bounds__(256) k_mimi_rvq(const RvqParams p) {
             const float* v = z + (j == 0 ? 0 : p.cb_dim);
             unsigned long long best = ~0ull;
             for (int h = 0; h < 2; ++h, ++c) {
-                if (!mbar_wait_n(&full[c & 1], (uint32_t)(c >> 1) & 1u, PM_SPIN_LIMIT)) ok = false;
+                if (!mbar_wait_n(&full[c & 1], (uint32_t)(c >> 1) & 1u, budget)) ok = false;
                 const uint16_t* cb = cbuf + (size_t)(c & 1) * half * p.cb_dim;
                 // four entries in flight per warp: warp w takes entries 4 w .. 4 w + 3, + 32, ...
                 for (int en0 = 4 * warp; en0 < half; en0 += 32) {
@@ -842,7 +846,9 @@ __global__ void __launch_bounds__(256) k_mimi_rvq(const RvqParams p) {
                     }
                 }
                 __syncthreads();  // every warp is done with this buffer
-                if (t == 0 && c + 2 < n_chunks) issue(c + 2);
+                // after a wait ran out no copy is issued into a buffer whose last copy may
+                // still be landing
+                if (t == 0 && ok && c + 2 < n_chunks) issue(c + 2);
             }
             if (lane == 0) wkey[warp] = best;
             __syncthreads();
@@ -865,7 +871,10 @@ __global__ void __launch_bounds__(256) k_mimi_rvq(const RvqParams p) {
         }
         __syncthreads();
     }
-    if (!ok && t == 0) atomicOr(p.status, 2u);
+    if (!ok && t == 0) atomicOr(p.st.status, 2u);
+    if (t == 0)  // every copy issued has landed before the CTA exits (the full poll budget)
+        for (int bf_ = 0; bf_ < 2; ++bf_)
+            if (n_issued[bf_] > 0) (void)mbar_wait_n(&full[bf_], (uint32_t)(n_issued[bf_] - 1) & 1u, PM_SPIN_LIMIT);
     if (rank == 0 && p.io->latent_out)
         for (int k = t; k < p.dim; k += blockDim.x) p.io->latent_out[(size_t)b * p.dim + k] = es[k];
 }
@@ -1359,7 +1368,7 @@ pm_status record_encoder(pm_mimi_ctx* c, int B, cudaStream_t s, MimiMarks* mk) {
     rp.w_ac = c->w[ix.ac_in];
     for (int j = 0; j < f.n_q; ++j) rp.cb[j] = c->w[ix.cb0 + j];
     rp.io = c->io;
-    rp.status = c->st.status;
+    rp.st = c->st;
     rp.dim = f.dim;
     rp.cb_dim = f.cb_dim;
     rp.card = f.card;
@@ -1473,13 +1482,14 @@ pm_status mimi_create(const pm_mimi_config* cfg, const void* const* tensors, int
     }
     // one allocation for state, activations and I/O
     const int BM = f.B_max, D = f.dim;
-    void *p_frame, *p_pos, *p_abort, *p_status, *p_io, *p_codes, *p_pcm, *p_prev, *p_X, *p_qkv, *p_o, *p_hf, *p_kv,
-        *p_lat, *p_freq;
+    void *p_frame, *p_pos, *p_abort, *p_status, *p_budget, *p_io, *p_codes, *p_pcm, *p_prev, *p_X, *p_qkv, *p_o,
+        *p_hf, *p_kv, *p_lat, *p_freq;
     std::vector<std::pair<void**, size_t>> items = {
         {&p_frame, 4u * BM},
         {&p_pos, 4u * BM},
         {&p_abort, 4u},
         {&p_status, 4u},
+        {&p_budget, 4u},
         {&p_io, sizeof(MimiIO)},
         {&p_codes, 4u * BM * f.n_q},
         {&p_pcm, encoder ? 4u * BM * c->frame_samples : 16u},
@@ -1526,6 +1536,11 @@ pm_status mimi_create(const pm_mimi_config* cfg, const void* const* tensors, int
     c->st.pos = (int32_t*)p_pos;
     c->st.abort = (uint32_t*)p_abort;
     c->st.status = (uint32_t*)p_status;
+    c->st.wait_budget = (const uint32_t*)p_budget;
+    {
+        const uint32_t b0 = PM_SPIN_LIMIT;
+        if (cudaMemcpy(p_budget, &b0, 4, cudaMemcpyHostToDevice) != cudaSuccess) return bail(PM_ERR_CUDA, "cudaMemcpy");
+    }
     c->io = (MimiIO*)p_io;
     c->codes_dev = (int32_t*)p_codes;
     c->pcm_dev = (float*)p_pcm;
@@ -1816,7 +1831,19 @@ extern "C" pm_status pm_mimi_status(pm_mimi_ctx* c) {
     if (cudaMemcpy(&s, c->st.status, 4, cudaMemcpyDeviceToHost) != cudaSuccess || cudaMemset(c->st.status, 0, 4) != cudaSuccess)
         return mfail(c, PM_ERR_CUDA, "pm_mimi_status: read");
     if (s & 2u) return mfail(c, PM_ERR_TIMEOUT, "a bounded wait of the quantiser ran out (that call's codes are undefined)");
+    if (s & ~1u) return mfail(c, PM_ERR_CUDA, "unknown device status");
     return s ? mfail(c, PM_ERR_INVALID_ID, "a code given in device memory was out of range (that call was a no-op)") : PM_OK;
+}
+
+extern "C" pm_status pm_mimi_set_wait_budget(pm_mimi_ctx* c, uint32_t polls) {
+    if (!c) return PM_ERR_ARG;
+    if (cudaSetDevice(c->device) != cudaSuccess) return mfail(c, PM_ERR_CUDA, "cudaSetDevice");
+    const uint32_t v = polls == PM_WAIT_BUDGET_DEFAULT ? (uint32_t)PM_SPIN_LIMIT : polls;
+    // ordered on the context's stream: calls before it keep the old budget
+    if (cudaStreamSynchronize(c->stream) != cudaSuccess ||
+        cudaMemcpy((void*)c->st.wait_budget, &v, 4, cudaMemcpyHostToDevice) != cudaSuccess)
+        return mfail(c, PM_ERR_CUDA, "pm_mimi_set_wait_budget");
+    return PM_OK;
 }
 
 extern "C" pm_status pm_mimi_get_frames(pm_mimi_ctx* c, int32_t* frames) {

@@ -27,7 +27,8 @@ EXPORTS = ["pm_kv_cache_bytes", "pm_create", "pm_reset", "pm_set_positions", "pm
 # every symbol include/pm_mimi.h declares
 MIMI_EXPORTS = ["pm_mimi_tensor_count", "pm_mimi_create", "pm_mimi_decode", "pm_mimi_reset", "pm_mimi_status",
                 "pm_mimi_get_frames", "pm_mimi_last_error", "pm_mimi_destroy", "pm_mimi_profile",
-                "pm_mimi_encoder_tensor_count", "pm_mimi_encoder_create", "pm_mimi_encode", "pm_mimi_encode_profile"]
+                "pm_mimi_encoder_tensor_count", "pm_mimi_encoder_create", "pm_mimi_encode", "pm_mimi_encode_profile",
+                "pm_mimi_set_wait_budget"]
 MIMI_KINDS = {0: "front", 1: "in_proj", 2: "attention", 3: "out_proj", 4: "lin1", 5: "lin2", 6: "conv_first",
               7: "convtr", 8: "res_conv1", 9: "res_conv2", 10: "conv_last", 11: "finish", 12: "down",
               13: "resample", 14: "rvq"}
@@ -157,6 +158,8 @@ def lib():
         L.pm_mimi_encode.argtypes = [vp, C.c_int, vp, vp, vp]
         L.pm_mimi_encode_profile.restype = C.c_int
         L.pm_mimi_encode_profile.argtypes = [vp, C.c_int, vp, vp, vp, vp, vp, C.c_int, C.POINTER(C.c_int)]
+        L.pm_mimi_set_wait_budget.restype = C.c_int
+        L.pm_mimi_set_wait_budget.argtypes = [vp, C.c_uint32]
         L.pm_mimi_destroy.restype = None
         L.pm_mimi_destroy.argtypes = [vp]
         _lib = L
@@ -491,6 +494,10 @@ class _MimiContext:
 
     def status(self) -> int:
         return int(self.L.pm_mimi_status(self.h))
+
+    def set_wait_budget(self, polls: int = PM_WAIT_BUDGET_DEFAULT) -> None:
+        """Poll budget of the encoder's bounded waits (0: they give up at once)."""
+        self._check(self.L.pm_mimi_set_wait_budget(self.h, int(polls) & 0xFFFFFFFF))
 
     def frames(self) -> List[int]:
         a = (C.c_int32 * self.cfg.B_max)()

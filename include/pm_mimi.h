@@ -191,8 +191,17 @@ pm_status pm_mimi_encode_profile(pm_mimi_ctx* ctx, int B, const float* pcm, int3
 pm_status pm_mimi_reset(pm_mimi_ctx* ctx, const int32_t* mask);
 
 /* Synchronise the context's stream; PM_ERR_INVALID_ID if a call since the last
- * pm_mimi_status met an invalid device code (that call was a no-op), else PM_OK. */
+ * pm_mimi_status met an invalid device code (that call was a no-op), PM_ERR_TIMEOUT if a
+ * bounded wait ran out (pm_mimi_set_wait_budget), else PM_OK.  Reading clears both. */
 pm_status pm_mimi_status(pm_mimi_ctx* ctx);
+
+/* Poll budget of the encoder's bounded waits (the quantiser's waits for its codebook
+ * copies; PM_WAIT_BUDGET_DEFAULT restores the normal budget).  A wait that runs out makes
+ * that call's codes undefined and the next pm_mimi_status returns PM_ERR_TIMEOUT; the
+ * streaming state advances as usual (the quantiser holds none), and copies already issued
+ * are waited for with the normal budget before the kernel exits.  Synchronises the
+ * context's stream; for tests of that path. */
+pm_status pm_mimi_set_wait_budget(pm_mimi_ctx* ctx, uint32_t polls);
 
 /* Synchronise and copy the frames decoded since reset per stream ([B_max] int32, host). */
 pm_status pm_mimi_get_frames(pm_mimi_ctx* ctx, int32_t* frames);

@@ -259,9 +259,11 @@ def test_config2_stated_length_past_the_wrap(full):
 
 @pytest.mark.slow
 def test_config3_batched_sixteen_frames(full):
-    """All 16 streams (cache lengths uniform 64..3000) for 16 frames on the batched path."""
+    """All 16 streams (cache lengths uniform 64..3000) for 16 frames on the batched path
+    (PM_CONFIG3_FRAMES sets another length: the workload states 128, about 13 minutes of
+    oracle time on 16 cores)."""
     s = full.shape
-    B, T = 16, 16
+    B, T = 16, int(os.environ.get("PM_CONFIG3_FRAMES", "16"))
     full.ctx.reset()
     L = I.make_cache_lengths(B, 64, s.ctx, seed=3000)
     for b in range(B):
@@ -278,7 +280,7 @@ def test_config3_batched_sixteen_frames(full):
             _check(w, g[t][0][b], g[t][1][b], h, lg, f"b={b} L={L[b]} t={t}")
             _token(w, g[t][2][b], a, lg, f"b={b} L={L[b]} t={t}")
         del st
-    record_parity("config3_B16_ragged_16_frames", **w.asdict())
+    record_parity(f"config3_B16_ragged_{T}_frames", **w.asdict())
 
 
 def _depformer_lockstep(full, w, t, h_ref, text, sup_row):
@@ -315,9 +317,10 @@ def test_config4_stated_length_generator_loop(full):
     then on every stream is fed back, as the generator does: the text stream takes the
     previous greedy text token, audio stream k the previous frame's depth code k-1 (q0-7
     greedy, q8-15 supplied from seeded codes).  On the GPU the feedback stays on the
-    device (ID -3) wherever its selections equal the oracle's."""
+    device (ID -3) wherever its selections equal the oracle's.  PM_CONFIG4_FRAMES sets
+    another length (the workload states 1000 frames, about 8 minutes of oracle time)."""
     s = full.shape
-    N = 64
+    N = int(os.environ.get("PM_CONFIG4_FRAMES", "64"))
     full.ctx.reset()
     st = full.orc.new_stream()
     ids0 = I.make_ids(s, 1, seed=2014)[0, 0]
@@ -341,6 +344,6 @@ def test_config4_stated_length_generator_loop(full):
         # (the oracle's text token was supplied to its depformer)
         prev_r = np.concatenate([[text], oc]).astype(np.int32)
         prev_g = np.concatenate([[int(gt[0])], full.dcodes[0].cpu().numpy()]).astype(np.int32)
-    record_parity("config4_64_frames_generator_loop", **w.asdict())
+    record_parity(f"config4_{N}_frames_generator_loop", **w.asdict())
     del st
 

@@ -57,14 +57,17 @@ class EncPair:
         torch.cuda.synchronize()
         return codes.cpu().numpy(), lat.double().cpu().numpy()
 
-    def check_stream(self, pcm, codes, lats, w):
-        """pcm [F * fs] from reset, the GPU's codes [F][n_q] and latents [F][dim]."""
+    def check_stream(self, pcm, codes, lats, w, skip_codes=()):
+        """pcm [F * fs] from reset, the GPU's codes [F][n_q] and latents [F][dim]; the codes
+        of frames in skip_codes are not compared."""
         ref = self.orc.latent(pcm.astype(np.float64))
         cbs = [self.orc.W[f"q.codebook.{j}"] for j in range(self.n_q)]
         for f in range(len(codes)):
             e = _rel_l2(lats[f], ref[f])
             w["latent"] = max(w["latent"], e)
             assert e <= TOL, (f, e)
+            if f in skip_codes:
+                continue
             forced = [-1] * self.n_q
             oc, gaps = self.orc.quantize(ref[f])
             for j in range(self.n_q):
@@ -154,6 +157,31 @@ def test_host_and_device_pcm_agree_and_outputs_to_pinned_memory():
             assert np.array_equal(hc.numpy(), a[f][0])
         # the wrong direction on a context is refused before anything runs
         assert p.enc.L.pm_mimi_decode(p.enc.h, 1, hc.data_ptr(), hc.data_ptr()) == p.pm.PM_ERR_STATE
+    finally:
+        p.close()
+
+
+def test_a_quantiser_wait_that_runs_out():
+    """With a poll budget of 0 the quantiser's copy waits give up at once: that call's codes
+    are undefined and pm_mimi_status reports PM_ERR_TIMEOUT; the streaming state advances as
+    usual, so with the budget restored the next frames match the oracle again."""
+    p = EncPair(I.MIMI_SMALL, B_max=1)
+    pm = p.pm
+    try:
+        pcm = I.make_mimi_pcm(6 * p.fs, 1, seed=13)
+        frame = lambda f: pcm[:, f * p.fs:(f + 1) * p.fs]
+        got = [p.step(frame(0)), p.step(frame(1))]
+        assert p.enc.status() == pm.PM_OK
+        p.enc.set_wait_budget(0)
+        got.append(p.step(frame(2)))
+        assert p.enc.status() == pm.PM_ERR_TIMEOUT
+        assert p.enc.status() == pm.PM_OK  # reading clears it
+        p.enc.set_wait_budget()
+        got += [p.step(frame(f)) for f in range(3, 6)]
+        assert p.enc.status() == pm.PM_OK and p.enc.frames()[0] == 6
+        w = _worst()
+        p.check_stream(pcm[0], np.stack([g[0][0] for g in got]), np.stack([g[1][0] for g in got]), w,
+                       skip_codes=(2,))
     finally:
         p.close()
 
