@@ -80,6 +80,13 @@ __device__ __forceinline__ void prefetch_next_tc(const CUtensorMap* tmN, const N
     }
 }
 
+// v[i] = v[i + 16]: the next block of 16 frames moves to the front of the accumulator row
+template <int NPAD>
+__device__ __forceinline__ void shift_block(float (&v)[NPAD]) {
+#pragma unroll
+    for (int i = 0; i + 16 < NPAD; ++i) v[i] = v[i + 16];
+}
+
 template <int EPI, int NPAD>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -314,45 +321,56 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                 for (int b = 0; b < NPAD; ++b) v[b] *= inv[b];
 
+                // The per-frame epilogues run over frames in blocks of 16 in a rolled loop: a
+                // straight-line body for all NPAD frames is tens of KB of code that each CTA
+                // executes once, so nearly every instruction fetch missed.  Block k's values sit
+                // in v[0..15] and the others move down 16 places after each block, which keeps
+                // every index into v a compile-time constant (v stays in registers).
                 if (EPI == TE_STORE) {
                     const int r = m * 128 + t;
-                    if (!aborted && r < p.n_rows)
-                        for (int b = 0; b < p.B; ++b) p.y[(size_t)b * p.y_stride + r] = v[b];
-                } else if (EPI == TE_RESIDUAL) {
-                    const int r = m * 128 + t;
-                    float ss[NPAD];
-#pragma unroll
-                    for (int b = 0; b < NPAD; ++b) ss[b] = 0.f;
-                    if (!aborted) {
-                        const float an = p.alpha_next ? __uint_as_float((uint32_t)p.alpha_next[r] << 16) : 1.0f;
-#pragma unroll
-                        for (int b0 = 0; b0 < NPAD; b0 += 16) {
-                            if (b0 >= p.B) break;
-                            float xr[16];  // 16 residual rows loaded before the first store
+                    if (!aborted && r < p.n_rows) {
+#pragma unroll 1
+                        for (int b0 = 0; b0 < p.B; b0 += 16) {
 #pragma unroll
                             for (int j = 0; j < 16; ++j)
-                                xr[j] = (b0 + j < p.B) ? p.y[(size_t)(b0 + j) * p.y_stride + r] : 0.f;
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int b = b0 + j;
-                                if (b < p.B) {
-                                    const float xo = xr[j] + v[b];
-                                    p.y[(size_t)b * p.y_stride + r] = xo;
-                                    if (p.yb) p.yb[(size_t)b * p.yb_stride + r] = f32_to_bf16_rne(xo * an);
-                                    ss[b] = xo * xo;
-                                }
-                            }
+                                if (b0 + j < p.B) p.y[(size_t)(b0 + j) * p.y_stride + r] = v[j];
+                            shift_block<NPAD>(v);
                         }
                     }
+                } else if (EPI == TE_RESIDUAL) {
+                    const int r = m * 128 + t;
+                    const float an =
+                        (!aborted && p.alpha_next) ? __uint_as_float((uint32_t)p.alpha_next[r] << 16) : 1.0f;
+#pragma unroll 1
+                    for (int b0 = 0; b0 < p.B; b0 += 16) {
+                        float xr[16];  // 16 residual rows loaded before the first store
 #pragma unroll
-                    for (int b = 0; b < NPAD; ++b) {
-                        const float w = warp_sum(ss[b]);
-                        if (lane == 0) xch[warp * NPAD + b] = w;
+                        for (int j = 0; j < 16; ++j)
+                            xr[j] = (!aborted && b0 + j < p.B) ? p.y[(size_t)(b0 + j) * p.y_stride + r] : 0.f;
+                        float ss[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int b = b0 + j;
+                            ss[j] = 0.f;
+                            if (!aborted && b < p.B) {
+                                const float xo = xr[j] + v[j];
+                                p.y[(size_t)b * p.y_stride + r] = xo;
+                                if (p.yb) p.yb[(size_t)b * p.yb_stride + r] = f32_to_bf16_rne(xo * an);
+                                ss[j] = xo * xo;
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float w = warp_sum(ss[j]);
+                            if (lane == 0) xch[warp * NPAD + b0 + j] = w;
+                        }
+                        shift_block<NPAD>(v);
                     }
                     epi_bar();
                     if (t < NPAD && !aborted && p.ss_out)
                         p.ss_out[(size_t)m * NPAD + t] =
-                            xch[0 * NPAD + t] + xch[1 * NPAD + t] + xch[2 * NPAD + t] + xch[3 * NPAD + t];
+                            t < p.B ? xch[0 * NPAD + t] + xch[1 * NPAD + t] + xch[2 * NPAD + t] + xch[3 * NPAD + t]
+                                    : 0.f;
                     epi_bar();
                 } else if (EPI == TE_SWIGLU) {
                     // lanes 0-63: gate rows m*64 + t; lanes 64-127: value rows of the same j
@@ -361,23 +379,30 @@ __global__ void __launch_bounds__(192, 1)
                         for (int b = 0; b < NPAD; ++b) xch[b * 64 + (t - 64)] = v[b];
                     epi_bar();
                     if (t < 64 && !aborted) {
-                        const int j = m * 64 + t;
-                        for (int b = 0; b < p.B; ++b) {
-                            const float g = v[b], z = xch[b * 64 + t];
-                            p.yb[(size_t)b * p.yb_stride + j] = f32_to_bf16_rne(g / (1.0f + expf(-g)) * z);
+                        const int jr = m * 64 + t;
+#pragma unroll 1
+                        for (int b0 = 0; b0 < p.B; b0 += 16) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int b = b0 + j;
+                                if (b < p.B) {
+                                    const float g = v[j], z = xch[b * 64 + t];
+                                    p.yb[(size_t)b * p.yb_stride + jr] = f32_to_bf16_rne(g / (1.0f + expf(-g)) * z);
+                                }
+                            }
+                            shift_block<NPAD>(v);
                         }
                     }
                     epi_bar();
                 } else if (EPI == TE_QKV_ROPE) {
                     const int r = m * 128 + t;
-                    const int sec = r / p.D;
+                    const int sec = r / p.D;  // 0: q, 1: k, 2: v (a tile lies in one section)
                     const int idx = r - sec * p.D;
                     const int h = idx / p.dh, d = idx % p.dh;
                     const bool even = (t & 1) == 0;
-#pragma unroll
-                    for (int b0 = 0; b0 < NPAD; b0 += 16) {
-                        if (b0 >= p.B) break;
-                        // rotation factors and ring slots of 16 streams, loaded before the first store
+#pragma unroll 1
+                    for (int b0 = 0; b0 < p.B; b0 += 16) {
+                        // rotation factors and ring slots of 16 frames, loaded before the first store
                         float2 cs[16];
                         int slot[16];
 #pragma unroll
@@ -385,16 +410,13 @@ __global__ void __launch_bounds__(192, 1)
                             const int b = b0 + j;
                             cs[j] = (sec < 2 && b < p.B) ? p.rope_tab[(size_t)b * (p.dh / 2) + (d >> 1)]
                                                          : make_float2(1.f, 0.f);
-                            // a prefill's row b is frame pos + b of stream seq_stream
-                            slot[j] = (sec > 0 && b < p.B)
-                                          ? (p.seq ? p.st.pos[p.io->seq_stream] + b : p.st.pos[b]) % p.ctx
-                                          : 0;
+                            slot[j] = (sec > 0 && !p.seq && b < p.B) ? p.st.pos[b] % p.ctx : 0;
                         }
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const int b = b0 + j;
                             if (b >= p.B) break;
-                            const float mine = v[b];
+                            const float mine = v[j];
                             const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
                             float o = mine;
                             if (sec < 2) o = even ? (mine * cs[j].x - other * cs[j].y) : (other * cs[j].y + mine * cs[j].x);
@@ -409,6 +431,7 @@ __global__ void __launch_bounds__(192, 1)
                                 cache[(((size_t)b * p.H + h) * p.ctx + slot[j]) * p.dh + d] = f32_to_bf16_rne(o);
                             }
                         }
+                        shift_block<NPAD>(v);
                     }
                 } else if (EPI == TE_HEAD) {
                     const int r = m * 128 + t;
@@ -416,18 +439,25 @@ __global__ void __launch_bounds__(192, 1)
                     // a prefill reports only its last frame, as stream seq_stream's
                     const int b_lo = p.seq ? p.B - 1 : 0;
                     const int s_seq = p.seq ? p.io->seq_stream : 0;
+#pragma unroll 1
+                    for (int b0 = 0; b0 < p.B; b0 += 16) {
+                        if (b0 + 16 > b_lo) {
 #pragma unroll
-                    for (int b = 0; b < NPAD; ++b) {
-                        unsigned long long key = 0ull;
-                        if (b >= b_lo && b < p.B && r < p.n_rows) {
-                            const int bo = p.seq ? 0 : b, bs = p.seq ? s_seq : b;
-                            if (out && !aborted) out[(size_t)bo * p.n_rows + r] = v[b];
-                            if (p.logits_copy && !aborted) p.logits_copy[(size_t)bs * p.n_rows + r] = v[b];
-                            key = pack_argmax(v[b], (uint32_t)r);
+                            for (int j = 0; j < 16; ++j) {
+                                const int b = b0 + j;
+                                unsigned long long key = 0ull;
+                                if (b >= b_lo && b < p.B && r < p.n_rows) {
+                                    const int bo = p.seq ? 0 : b, bs = p.seq ? s_seq : b;
+                                    if (out && !aborted) out[(size_t)bo * p.n_rows + r] = v[j];
+                                    if (p.logits_copy && !aborted) p.logits_copy[(size_t)bs * p.n_rows + r] = v[j];
+                                    key = pack_argmax(v[j], (uint32_t)r);
+                                }
+#pragma unroll
+                                for (int o = 16; o > 0; o >>= 1) key = umax64(key, __shfl_xor_sync(0xffffffffu, key, o));
+                                if (lane == 0) red64[warp * NPAD + b] = key;
+                            }
                         }
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) key = umax64(key, __shfl_xor_sync(0xffffffffu, key, o));
-                        if (lane == 0) red64[warp * NPAD + b] = key;
+                        shift_block<NPAD>(v);
                     }
                     epi_bar();
                     if (t >= b_lo && t < p.B) {

@@ -14,12 +14,14 @@
 // keys they can see (positions max(0, p0 - win + 1) .. p0 + T - 1): positions before p0
 // from the ring, the pass's own from the kv_new rows its QKV projection wrote (a full
 // ring's slots are reused by the pass's positions, so they are committed only afterwards
-// by k_seq_commit: the last row of each slot).  Work item = (head, 256-key chunk): 64 keys
-// at a time are staged in shared memory (K as rows, V transposed) and every warp -- 16
-// query rows -- computes its scores and weighted values with warp-wide m16n8k16 tensor
-// core MMAs (bf16 operands, fp32 accumulation), keeping the running (max, sum, weighted
-// values) of its rows in registers; chunks merge in the CTA that finishes a head last
-// (completion counter).
+// by k_seq_commit: the last row of each slot).  Work item = (head, 256-key chunk): the
+// chunk's keys stream through a ring of three 64-key stages in shared memory (K and V as
+// rows, filled by cp.async while the previous stage is in use), and every warp -- 16 query
+// rows -- computes its scores and weighted values with warp-wide m16n8k16 tensor-core MMAs
+// (bf16 operands from ldmatrix, V through its transposing form; fp32 accumulation),
+// keeping the running (max, sum, weighted values) of its rows in registers.  A head whose
+// keys fit one chunk writes its output directly; otherwise every chunk leaves a partial
+// and k_seq_commit, one CTA per row, merges the row's partials of all heads.
 #include <math.h>
 
 #include "pm_kernels.h"
@@ -94,14 +96,51 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return (uint32_t)f32_to_bf16_rne(lo) | ((uint32_t)f32_to_bf16_rne(hi) << 16);
 }
 
-constexpr int KS_STRIDE = DH + 8;    // bf16 per staged key row (conflict-free fragment loads)
-constexpr int VT_STRIDE = KSUB + 8;  // bf16 per staged value column
+// shared-memory stage ring of k_attn_seq: K rows then V rows of 64 keys, 272 B per row
+// (16-byte aligned rows for cp.async and ldmatrix; 8 rows of a fragment land in 8
+// distinct 4-bank groups)
+constexpr int NSTAGE = 3;
+constexpr int KROW = DH + 8;                               // bf16 per staged row
+constexpr uint32_t HALF_BYTES = KSUB * KROW * 2;           // K (or V) of one stage
+constexpr uint32_t STAGE_BYTES = 2 * HALF_BYTES;
+constexpr size_t SEQ_SMEM = (size_t)NSTAGE * STAGE_BYTES;  // 104,448 B: two CTAs per SM
+
+// 16-byte global -> shared copy; when !valid the destination is zero-filled and nothing is read
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// four 8x8 b16 matrices; lanes 8q .. 8q+7 give the row addresses of matrix q
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// the pass's key range and its chunking (k_attn_seq and k_seq_commit agree on it)
+struct SeqChunks {
+    int lo, hi, C;
+};
+__device__ __forceinline__ SeqChunks seq_chunks(int p0, int T, int win) {
+    SeqChunks k;
+    k.lo = max(0, p0 - win + 1);
+    k.hi = p0 + T - 1;
+    k.C = (k.hi - k.lo + 1 + PM_SEQ_KPC - 1) / PM_SEQ_KPC;
+    return k;
+}
 
 __global__ void __launch_bounds__(SEQ_NT) k_attn_seq(const AttnSeqParams p) {
-    __shared__ __align__(16) uint16_t s_k[KSUB * KS_STRIDE];  // [key][dim]
-    __shared__ __align__(16) uint16_t s_vt[DH * VT_STRIDE];   // [dim][key]
-    __shared__ int s_last;
-    __shared__ float s_pm[SEQ_NT / 32][PM_SEQ_MAX_CHUNKS], s_pl[SEQ_NT / 32][PM_SEQ_MAX_CHUNKS];
+    extern __shared__ __align__(128) uint8_t seq_smem[];
     pdl_trigger();
     pdl_wait();
     if (*(volatile uint32_t*)&p.st.status[1] != 0u) return;
@@ -110,16 +149,52 @@ __global__ void __launch_bounds__(SEQ_NT) k_attn_seq(const AttnSeqParams p) {
     const int s = p.io->seq_stream;
     const int p0 = p.st.pos[s];
     const int T = p.T;
-    const int lo_all = max(0, p0 - p.win + 1), hi_all = p0 + T - 1;
-    const int C = (hi_all - lo_all + 1 + PM_SEQ_KPC - 1) / PM_SEQ_KPC;
+    const SeqChunks ch = seq_chunks(p0, T, p.win);
+    const int C = ch.C;
     const int items = p.H * C;
     // this thread's two query rows (the warp owns rows 16 * warp .. 16 * warp + 15)
     const int r0 = 16 * warp + g, r1 = r0 + 8;
+    const uint32_t sbase = smem_u32(seq_smem);
+    // ldmatrix row of this lane: matrix q = lane / 8, row lane % 8
+    const int lq = lane >> 3, lr = lane & 7;
 
     for (int item = blockIdx.x; item < items; item += gridDim.x) {
         const int h = item / C, c = item % C;
-        const int c0 = lo_all + c * PM_SEQ_KPC;
-        const int c1 = min(c0 + PM_SEQ_KPC, hi_all + 1);
+        const int c0 = ch.lo + c * PM_SEQ_KPC;
+        const int c1 = min(c0 + PM_SEQ_KPC, ch.hi + 1);
+        const int nsub = (c1 - c0 + KSUB - 1) / KSUB;
+        const size_t head_base = ((size_t)s * p.H + h) * (size_t)p.ctx * DH;
+        // K and V of keys k0 .. k0+63 into stage `buf`; keys past the chunk are zeros
+        auto stage = [&](int sub, int buf) {
+            const int k0 = c0 + sub * KSUB;
+            const uint32_t sk = sbase + (uint32_t)buf * STAGE_BYTES;
+            for (int i = tid; i < KSUB * (DH / 8); i += SEQ_NT) {
+                const int j = i >> 4, d0 = (i & 15) * 8;
+                const int kp = k0 + j;
+                const bool ok = kp < c1;
+                const uint16_t* ks = p.kv_new;
+                const uint16_t* vs = p.kv_new;
+                if (ok) {
+                    if (kp >= p0) {
+                        const size_t off = ((size_t)(kp - p0) * p.H + h) * DH + d0;
+                        ks = p.kv_new + off;
+                        vs = p.kv_new + (size_t)T * p.H * DH + off;
+                    } else {
+                        const size_t off = head_base + (size_t)(kp % p.ctx) * DH + d0;
+                        ks = p.kc + off;
+                        vs = p.vc + off;
+                    }
+                }
+                const uint32_t o = (uint32_t)(j * KROW + d0) * 2u;
+                cp_async16(sk + o, ks, ok);
+                cp_async16(sk + HALF_BYTES + o, vs, ok);
+            }
+        };
+#pragma unroll
+        for (int i = 0; i < NSTAGE - 1; ++i) {
+            if (i < nsub) stage(i, i);
+            cp_async_commit();
+        }
         // query fragments, pre-scaled by log2(e) / sqrt(dh), bf16
         uint32_t qf[DH / 16][4];
         {
@@ -143,48 +218,30 @@ __global__ void __launch_bounds__(SEQ_NT) k_attn_seq(const AttnSeqParams p) {
 #pragma unroll
         for (int d = 0; d < DH / 8; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
         float m_0 = -INFINITY, m_1 = -INFINITY, l_0 = 0.f, l_1 = 0.f;
-        const size_t head_base = ((size_t)s * p.H + h) * (size_t)p.ctx * DH;
-        for (int k0 = c0; k0 < c1; k0 += KSUB) {
-            const int nk = min(KSUB, c1 - k0);
-            __syncthreads();  // the previous sub-chunk's K / V fully used
-            for (int i = tid; i < KSUB * (DH / 8); i += SEQ_NT) {
-                const int j = i / (DH / 8), d0 = (i % (DH / 8)) * 8;
-                uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-                if (j < nk) {
-                    const int kp = k0 + j;
-                    if (kp >= p0) {
-                        const size_t off = ((size_t)(kp - p0) * p.H + h) * DH + d0;
-                        kv = *reinterpret_cast<const uint4*>(p.kv_new + off);
-                        vv = *reinterpret_cast<const uint4*>(p.kv_new + (size_t)T * p.H * DH + off);
-                    } else {
-                        const size_t off = head_base + (size_t)(kp % p.ctx) * DH + d0;
-                        kv = *reinterpret_cast<const uint4*>(p.kc + off);
-                        vv = *reinterpret_cast<const uint4*>(p.vc + off);
-                    }
-                }
-                *reinterpret_cast<uint4*>(s_k + (size_t)j * KS_STRIDE + d0) = kv;
-                const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    s_vt[(size_t)(d0 + 2 * e) * VT_STRIDE + j] = (uint16_t)(vw[e] & 0xFFFFu);
-                    s_vt[(size_t)(d0 + 2 * e + 1) * VT_STRIDE + j] = (uint16_t)(vw[e] >> 16);
-                }
-            }
-            __syncthreads();
-            // S = Q K^T for the warp's 16 rows and the 64 staged keys (8 tiles of 8 keys)
+        for (int sub = 0; sub < nsub; ++sub) {
+            cp_async_wait<NSTAGE - 2>();  // this thread's copies of stage `sub` landed
+            __syncthreads();              // everyone's did, and stage sub-1 is no longer read
+            if (sub + NSTAGE - 1 < nsub) stage(sub + NSTAGE - 1, (sub + NSTAGE - 1) % NSTAGE);
+            cp_async_commit();
+            const uint32_t sk = sbase + (uint32_t)(sub % NSTAGE) * STAGE_BYTES;
+            const uint32_t sv = sk + HALF_BYTES;
+            const int k0 = c0 + sub * KSUB;
+            // S = Q K^T for the warp's 16 rows and the 64 staged keys (8 tiles of 8 keys);
+            // matrices q = 0..3 of one ldmatrix: dims 16 ks + 8 q .. +7 of keys 8 j .. 8 j + 7
             float sc[KSUB / 8][4];
 #pragma unroll
             for (int j = 0; j < KSUB / 8; ++j) {
                 sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-                const uint16_t* kr = s_k + (size_t)(8 * j + g) * KS_STRIDE + 2 * tq;
+                const uint32_t kr = sk + (uint32_t)((8 * j + lr) * KROW + 8 * lq) * 2u;
 #pragma unroll
-                for (int ks = 0; ks < DH / 16; ++ks) {
-                    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(kr + 16 * ks);
-                    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(kr + 16 * ks + 8);
+                for (int ks = 0; ks < DH / 16; ks += 2) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kr + 32u * ks, b0, b1, b2, b3);
                     mma16816(sc[j], qf[ks], b0, b1);
+                    mma16816(sc[j], qf[ks + 1], b2, b3);
                 }
             }
-            // mask (window, causality, pass rows) and the running softmax of both rows
+            // mask (window, causality, pass rows, chunk end) and the running softmax of both rows
             const int qp0 = p0 + r0, qp1 = p0 + r1;
             float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
@@ -192,7 +249,7 @@ __global__ void __launch_bounds__(SEQ_NT) k_attn_seq(const AttnSeqParams p) {
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int kp = k0 + 8 * j + 2 * tq + e;
-                    const bool in = kp < k0 + nk;
+                    const bool in = kp < c1;
                     const bool ok0 = in && r0 < T && kp <= qp0 && kp > qp0 - p.win;
                     const bool ok1 = in && r1 < T && kp <= qp1 && kp > qp1 - p.win;
                     sc[j][e] = ok0 ? sc[j][e] : -INFINITY;
@@ -239,89 +296,128 @@ __global__ void __launch_bounds__(SEQ_NT) k_attn_seq(const AttnSeqParams p) {
                 o[d][2] *= f1;
                 o[d][3] *= f1;
             }
-            // O += P V (16 tiles of 8 output coordinates)
+            // O += P V: transposed 8x8 loads of V give the B fragments; matrices q = 0..3 are
+            // keys 16 kk + 8 (q & 1) .. +7 of dims 8 d + 8 (q >> 1) .. +7 (tiles d, d + 1)
 #pragma unroll
-            for (int d = 0; d < DH / 8; ++d) {
-                const uint16_t* vr = s_vt + (size_t)(8 * d + g) * VT_STRIDE + 2 * tq;
+            for (int kk = 0; kk < KSUB / 16; ++kk) {
+                const uint32_t vr = sv + (uint32_t)((16 * kk + 8 * (lq & 1) + lr) * KROW + 8 * (lq >> 1)) * 2u;
 #pragma unroll
-                for (int kk = 0; kk < KSUB / 16; ++kk) {
-                    const uint32_t b0 = *reinterpret_cast<const uint32_t*>(vr + 16 * kk);
-                    const uint32_t b1 = *reinterpret_cast<const uint32_t*>(vr + 16 * kk + 8);
+                for (int d = 0; d < DH / 8; d += 2) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(vr + 16u * d, b0, b1, b2, b3);
                     mma16816(o[d], pf[kk], b0, b1);
+                    mma16816(o[d + 1], pf[kk], b2, b3);
                 }
             }
         }
-        // this chunk's partial of the thread's rows
+        cp_async_wait<0>();
+        __syncthreads();  // the stages are free for the next item
 #pragma unroll
         for (int hr = 0; hr < 2; ++hr) {
             const int r = hr ? r1 : r0;
             if (r >= T) continue;
-            float* part = p.part + (((size_t)r * p.H + h) * PM_SEQ_MAX_CHUNKS + c) * PSTRIDE;
+            if (C == 1) {
+                // the whole window in one chunk: the normalised output
+                const float inv = 1.0f / (hr ? l_1 : l_0);
+                float* ob = p.o + (size_t)r * p.D + h * DH;
 #pragma unroll
-            for (int d = 0; d < DH / 8; ++d)
-                *reinterpret_cast<float2*>(part + 8 * d + 2 * tq) = make_float2(o[d][2 * hr], o[d][2 * hr + 1]);
-            if (tq == 0) {
-                part[DH] = hr ? m_1 : m_0;
-                part[DH + 1] = hr ? l_1 : l_0;
-            }
-        }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-            const uint32_t done = atomicAdd(&p.count[h], 1u);
-            s_last = (done == (uint32_t)C - 1u) ? 1 : 0;
-        }
-        __syncthreads();
-        if (!s_last) continue;
-        // last chunk of head h: merge every row's chunks in chunk order
-        __threadfence();
-        for (int t = warp; t < T; t += SEQ_NT / 32) {
-            const float* pb = p.part + ((size_t)t * p.H + h) * PM_SEQ_MAX_CHUNKS * PSTRIDE;
-            float* wm = s_pm[warp];
-            float* wl = s_pl[warp];
-            for (int i = lane; i < C; i += 32) {
-                wm[i] = __ldcg(pb + (size_t)i * PSTRIDE + DH);
-                wl[i] = __ldcg(pb + (size_t)i * PSTRIDE + DH + 1);
-            }
-            __syncwarp();
-            float M = -INFINITY;
-            for (int i = 0; i < C; ++i) M = fmaxf(M, wm[i]);
-            float L = 0.f, A[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int i = 0; i < C; ++i) {
-                const float f = (wm[i] == -INFINITY) ? 0.f : exp2f(wm[i] - M);
-                L += wl[i] * f;
-                const float4 a = __ldcg(reinterpret_cast<const float4*>(pb + (size_t)i * PSTRIDE + 4 * lane));
-                A[0] += a.x * f;
-                A[1] += a.y * f;
-                A[2] += a.z * f;
-                A[3] += a.w * f;
-            }
-            __syncwarp();
-            float* ob = p.o + (size_t)t * p.D + h * DH + 4 * lane;
+                for (int d = 0; d < DH / 8; ++d) {
+                    const float a = o[d][2 * hr] * inv, b = o[d][2 * hr + 1] * inv;
+                    *reinterpret_cast<float2*>(ob + 8 * d + 2 * tq) = make_float2(a, b);
+                    if (p.ob)
+                        *reinterpret_cast<uint32_t*>(p.ob + (size_t)r * p.D + h * DH + 8 * d + 2 * tq) = pack_bf16(a, b);
+                }
+            } else {
+                // this chunk's partial of the row: unnormalised values, max, sum
+                float* part = p.part + (((size_t)r * p.H + h) * PM_SEQ_MAX_CHUNKS + c) * PSTRIDE;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float v = A[e] / L;
-                ob[e] = v;
-                if (p.ob) p.ob[(size_t)t * p.D + h * DH + 4 * lane + e] = f32_to_bf16_rne(v);
+                for (int d = 0; d < DH / 8; ++d)
+                    *reinterpret_cast<float2*>(part + 8 * d + 2 * tq) = make_float2(o[d][2 * hr], o[d][2 * hr + 1]);
+                if (tq == 0) {
+                    part[DH] = hr ? m_1 : m_0;
+                    part[DH + 1] = hr ? l_1 : l_0;
+                }
             }
         }
-        if (tid == 0) p.count[h] = 0u;
-        __syncthreads();
     }
 }
 
 }  // namespace
 
-// CTA t copies row t's K and V (all heads) into the ring slot (p0 + t) mod ctx unless a
-// later row of the pass owns the same slot
+// CTA t: (1) copies row t's K and V (all heads) into the ring slot (p0 + t) mod ctx unless
+// a later row of the pass owns the same slot; (2) when the window took several chunks,
+// merges row t's chunk partials of every head: out = sum_c exp2(m_c - M) o_c / L with
+// M = max_c m_c and L = sum_c exp2(m_c - M) l_c.
 __global__ void __launch_bounds__(128) k_seq_commit(const AttnSeqParams p) {
+    __shared__ float s_w[PM_SEQ_MAX_HEADS * PM_SEQ_MAX_CHUNKS];
+    __shared__ float s_m[PM_SEQ_MAX_HEADS * PM_SEQ_MAX_CHUNKS];
     pdl_trigger();
     pdl_wait();
     if (*(volatile uint32_t*)&p.st.status[1] != 0u) return;
     const int t = blockIdx.x;
-    if (t + p.ctx < p.T) return;
     const int s = p.io->seq_stream;
-    const int slot = (p.st.pos[s] + t) % p.ctx;
+    const int p0 = p.st.pos[s];
+    const int C = seq_chunks(p0, p.T, p.win).C;
+    if (C > 1) {
+        const int H = p.H;
+        const float* pr = p.part + (size_t)t * H * PM_SEQ_MAX_CHUNKS * PSTRIDE;
+        for (int i = threadIdx.x; i < H * C; i += blockDim.x) {
+            const int h = i / C, c = i % C;
+            const float* pc = pr + ((size_t)h * PM_SEQ_MAX_CHUNKS + c) * PSTRIDE;
+            s_m[h * PM_SEQ_MAX_CHUNKS + c] = __ldcg(pc + DH);
+            s_w[h * PM_SEQ_MAX_CHUNKS + c] = __ldcg(pc + DH + 1);
+        }
+        __syncthreads();
+        if ((int)threadIdx.x < H) {
+            const int h = threadIdx.x;
+            float M = -INFINITY;
+            for (int c = 0; c < C; ++c) M = fmaxf(M, s_m[h * PM_SEQ_MAX_CHUNKS + c]);
+            float L = 0.f;
+            for (int c = 0; c < C; ++c) {
+                const float mc = s_m[h * PM_SEQ_MAX_CHUNKS + c];
+                const float f = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
+                s_m[h * PM_SEQ_MAX_CHUNKS + c] = f;
+                L += s_w[h * PM_SEQ_MAX_CHUNKS + c] * f;
+            }
+            const float inv = 1.0f / L;
+            for (int c = 0; c < C; ++c) s_w[h * PM_SEQ_MAX_CHUNKS + c] = s_m[h * PM_SEQ_MAX_CHUNKS + c] * inv;
+        }
+        __syncthreads();
+        // thread -> head h = i / 4, 32 consecutive dims 32 (i % 4) .. +31
+        for (int i = threadIdx.x; i < H * 4; i += blockDim.x) {
+            const int h = i >> 2, d0 = (i & 3) * 32;
+            float acc[32];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
+            const float* ph = pr + (size_t)h * PM_SEQ_MAX_CHUNKS * PSTRIDE + d0;
+#pragma unroll 2
+            for (int c = 0; c < C; ++c) {
+                const float w = s_w[h * PM_SEQ_MAX_CHUNKS + c];
+                const float4* pc = reinterpret_cast<const float4*>(ph + (size_t)c * PSTRIDE);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float4 a = __ldcg(pc + e);
+                    acc[4 * e + 0] += a.x * w;
+                    acc[4 * e + 1] += a.y * w;
+                    acc[4 * e + 2] += a.z * w;
+                    acc[4 * e + 3] += a.w * w;
+                }
+            }
+            float* ob = p.o + (size_t)t * p.D + h * DH + d0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                reinterpret_cast<float4*>(ob)[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
+            if (p.ob) {
+                uint16_t* bb = p.ob + (size_t)t * p.D + h * DH + d0;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    reinterpret_cast<uint2*>(bb)[e] = make_uint2(pack_bf16(acc[4 * e], acc[4 * e + 1]),
+                                                                 pack_bf16(acc[4 * e + 2], acc[4 * e + 3]));
+            }
+        }
+    }
+    if (t + p.ctx < p.T) return;
+    const int slot = (p0 + t) % p.ctx;
     const int n16 = p.H * DH / 8;  // 16-byte pieces per row
     for (int i = threadIdx.x; i < 2 * n16; i += blockDim.x) {
         const int kv = i / n16, j = i % n16;
@@ -333,6 +429,7 @@ __global__ void __launch_bounds__(128) k_seq_commit(const AttnSeqParams p) {
 }
 
 cudaError_t launch_seq_commit(const AttnSeqParams& p, cudaStream_t s, bool pdl) {
+    if (p.H > PM_SEQ_MAX_HEADS || p.T < 1 || p.T > PM_SEQ_MAX_ROWS) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.T);
     cfg.blockDim = dim3(128);
@@ -359,7 +456,9 @@ cudaError_t launch_seq_prepare(const SeqPrepParams& p, cudaStream_t s, bool pdl)
     return cudaLaunchKernelEx(&cfg, k_seq_prepare, p);
 }
 
-cudaError_t attn_seq_prepare() { return cudaSuccess; }
+cudaError_t attn_seq_prepare() {
+    return cudaFuncSetAttribute(k_attn_seq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SEQ_SMEM);
+}
 
 int attn_seq_max_chunks(int win) { return (win + PM_SEQ_MAX_ROWS - 1 + PM_SEQ_KPC - 1) / PM_SEQ_KPC; }
 
@@ -370,6 +469,7 @@ cudaError_t launch_attn_seq(const AttnSeqParams& p, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid);
     cfg.blockDim = dim3(SEQ_NT);
+    cfg.dynamicSmemBytes = SEQ_SMEM;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

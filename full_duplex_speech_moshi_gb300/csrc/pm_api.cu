@@ -78,7 +78,6 @@ struct pm_ctx {
     // prefill: resolved inputs of a pass, attention partials and counters, graphs per T
     int32_t* seq_resolved = nullptr;
     float* seq_part = nullptr;
-    uint32_t* seq_count = nullptr;
     uint16_t* seq_kv = nullptr;        // [2][PM_SEQ_MAX_ROWS][H][dh] a pass's K/V before commit
     std::map<int, cudaGraphExec_t> prefill_graphs;
     // staging
@@ -570,7 +569,6 @@ static pm_status record_frame_tc_impl(pm_ctx* c, int B, cudaStream_t s, bool seq
             aq.o = c->o;
             aq.ob = c->ob;
             aq.part = c->seq_part;
-            aq.count = c->seq_count;
             aq.st = c->st;
             aq.io = reinterpret_cast<const FrameIO*>(c->io_region);
             aq.T = B;
@@ -1012,7 +1010,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     void *p_gring, *p_gprov, *p_goff, *p_gin, *p_gtok, *p_gsup, *p_gpos, *p_gsel;
     void* p_io; void* p_dio; void *p_x, *p_q, *p_o, *p_s, *p_h, *p_part, *p_cnt, *p_freq, *p_dz, *p_dq,
         *p_ds, *p_dkv, *p_rtab, *p_xb, *p_ob, *p_sb, *p_ss, *p_tcp, *p_tcc, *p_scfg, *p_slog, *p_dslog,
-        *p_sres, *p_apart, *p_acnt, *p_skv, *p_dzin;
+        *p_sres, *p_apart, *p_skv, *p_dzin;
     // rows of the activation buffers: the batch, or a prefill pass of PM_SEQ_MAX_ROWS frames
     const int RM = BM > PM_SEQ_MAX_ROWS ? BM : PM_SEQ_MAX_ROWS;
     // tensor-core path scratch (batches and prefill passes), sized from the plans of this
@@ -1056,6 +1054,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     const size_t ss_floats = std::max((size_t)(f.D / 128) * NP, (size_t)ss_parts_max * 16);
     if (attn_seq_max_chunks(f.ctx) > PM_SEQ_MAX_CHUNKS)
         return bail(PM_ERR_UNSUPPORTED, "ctx too long for the prefill attention");
+    if (f.H > PM_SEQ_MAX_HEADS) return bail(PM_ERR_UNSUPPORTED, "too many heads for the prefill attention");
     c->npad_max = NP;
     c->tc_part_floats = tc_part_floats;
     c->tc_count_max = tc_count_max;
@@ -1079,7 +1078,7 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
         {&p_scfg, sizeof(SampleCfg)}, {&p_slog, 4u * BM * f.text_out},
         {&p_dslog, c->has_dep ? 4u * BM * f.dep_card : 16u},
         {&p_sres, 4u * PM_SEQ_MAX_ROWS * S},
-        {&p_apart, 4u * PM_SEQ_MAX_ROWS * f.H * PM_SEQ_MAX_CHUNKS * PM_SEQ_PART_STRIDE}, {&p_acnt, 4u * f.H},
+        {&p_apart, 4u * PM_SEQ_MAX_ROWS * f.H * PM_SEQ_MAX_CHUNKS * PM_SEQ_PART_STRIDE},
         {&p_skv, 2u * 2u * PM_SEQ_MAX_ROWS * f.H * f.dh},
     };
     size_t total = 0;
@@ -1147,7 +1146,6 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     c->dslog = (float*)p_dslog;
     c->seq_resolved = (int32_t*)p_sres;
     c->seq_part = (float*)p_apart;
-    c->seq_count = (uint32_t*)p_acnt;
     c->seq_kv = (uint16_t*)p_skv;
 
     // RoPE frequencies f_j = exp(-ln(theta) * 2j / dh), in double

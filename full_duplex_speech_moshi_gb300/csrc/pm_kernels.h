@@ -154,6 +154,7 @@ int attn_max_splits(int ctx);
 #define PM_SEQ_KPC 256           // keys per attention work item
 #define PM_SEQ_MAX_CHUNKS 16     // work items per head (window + rows up to 4096 keys)
 #define PM_SEQ_PART_STRIDE 132   // floats per attention partial (128 values, max, sum, pad)
+#define PM_SEQ_MAX_HEADS 64      // heads the prefill merge holds weights for
 struct SeqPrepParams {
     const FrameIO* io;
     DevState st;
@@ -172,14 +173,14 @@ struct AttnSeqParams {
     float* o;                // [T][D]
     uint16_t* ob;            // [npad][D] bf16 copy of o, or null
     float* part;             // [T][H][PM_SEQ_MAX_CHUNKS][PM_SEQ_PART_STRIDE]
-    uint32_t* count;         // [H], zero between launches
     DevState st;
     const FrameIO* io;
     int T, H, ctx, win, D, grid;
     float scale_log2;
 };
 cudaError_t launch_attn_seq(const AttnSeqParams& p, cudaStream_t s, bool pdl);
-// the pass's K/V rows into the ring (the last row of each slot), after its attention
+// after the pass attention: merges each row's chunk partials (windows of several chunks)
+// and copies the pass's K/V rows into the ring (the last row of each slot)
 cudaError_t launch_seq_commit(const AttnSeqParams& p, cudaStream_t s, bool pdl);
 cudaError_t attn_seq_prepare();
 int attn_seq_max_chunks(int win);

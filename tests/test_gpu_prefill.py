@@ -74,6 +74,30 @@ def test_prefill_after_wrapped_decode(pair):
         _check((gh[0], gl[0], int(gt[0])), (rh, rl, rt), f"decode t={t}")
 
 
+def test_prefill_window_of_several_chunks():
+    """A 600-position ring and 700 frames: passes of 64 rows from 0 to 640, the last one 60
+    rows; from position 256 on a pass attends over more than one 256-key chunk (three at
+    the end, past the ring's wrap), so its rows are merged from chunk partials."""
+    p = Pair(small_shape(ctx=600), B_max=1, depformer=False)
+    try:
+        s = p.shape
+        st = p.orc.new_stream()
+        T = 700
+        ids = I.make_ids(s, T + 3, seed=93)[:, 0]
+        g = _prefill(p, 0, ids[:T])
+        r = None
+        for t in range(T):
+            r = st.step(ids[t])
+        _check(g, (r[0], r[2], r[3]), "prefill of 700 frames")
+        assert p.ctx.get_positions()[0] == T
+        for t in range(T, T + 3):
+            gh, gl, gt = p.gpu_frame(ids[t:t + 1])
+            rh, _, rl, rt = st.step(ids[t])
+            _check((gh[0], gl[0], int(gt[0])), (rh, rl, rt), f"decode t={t}")
+    finally:
+        p.close()
+
+
 def test_prefill_of_one_stream_leaves_the_others(pair):
     s = pair.shape
     pair.ctx.reset()
