@@ -87,6 +87,67 @@ __device__ __forceinline__ void shift_block(float (&v)[NPAD]) {
     for (int i = 0; i + 16 < NPAD; ++i) v[i] = v[i + 16];
 }
 
+// Sum over the warp of each of 16 per-lane values in 16 shuffles (instead of 16 x 5): at
+// each step a lane keeps half of its values and adds its partner's copy of that half, so
+// lane l ends with the total of value (l >> 1) & 15 (both lanes of a pair hold it).
+__device__ __forceinline__ float warp_sum16_transposed(float (&a)[16], int lane) {
+#pragma unroll
+    for (int half = 8, mask = 16; half >= 1; half >>= 1, mask >>= 1) {
+        const bool upper = (lane & mask) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+            const float send = upper ? a[i] : a[i + half];
+            const float keep = upper ? a[i + half] : a[i];
+            a[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+        }
+    }
+    return a[0] + __shfl_xor_sync(0xffffffffu, a[0], 1);
+}
+
+// RoPE over the frames of a q or k row (lane pairs hold the two coordinates of a rotation
+// pair, the even coordinate first); frame b's value goes to put(b, o, aux(b)), with aux --
+// a ring slot, say -- evaluated for a block of 16 frames before its first store; rolled in
+// blocks of 16
+template <int NPAD, class Aux, class Put>
+__device__ __forceinline__ void rope_frames(float (&v)[NPAD], const TcParams& p, int d, int lane, Aux aux, Put put) {
+    const bool even = (lane & 1) == 0;
+    const float2* tab = p.rope_tab + (d >> 1);
+#pragma unroll 1
+    for (int b0 = 0; b0 < p.B; b0 += 16) {
+        float2 cs[16];  // the block's rotation factors
+        int ax[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const bool in = b0 + j < p.B;
+            cs[j] = in ? tab[(size_t)(b0 + j) * (p.dh / 2)] : make_float2(1.f, 0.f);
+            ax[j] = in ? aux(b0 + j) : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (b0 + j >= p.B) break;
+            const float mine = v[j];
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+            put(b0 + j, even ? (mine * cs[j].x - other * cs[j].y) : (other * cs[j].y + mine * cs[j].x), ax[j]);
+        }
+        shift_block<NPAD>(v);
+    }
+}
+
+// the frames of a row without rotation (v rows), as rope_frames
+template <int NPAD, class Aux, class Put>
+__device__ __forceinline__ void plain_frames(float (&v)[NPAD], int B, Aux aux, Put put) {
+#pragma unroll 1
+    for (int b0 = 0; b0 < B; b0 += 16) {
+        int ax[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) ax[j] = (b0 + j < B) ? aux(b0 + j) : 0;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            if (b0 + j < B) put(b0 + j, v[j], ax[j]);
+        shift_block<NPAD>(v);
+    }
+}
+
 template <int EPI, int NPAD>
 __global__ void __launch_bounds__(192, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -359,11 +420,9 @@ __global__ void __launch_bounds__(192, 1)
                                 ss[j] = xo * xo;
                             }
                         }
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const float w = warp_sum(ss[j]);
-                            if (lane == 0) xch[warp * NPAD + b0 + j] = w;
-                        }
+                        // the warp's sums of the 16 frames' squares, lane l ending with frame (l >> 1) & 15
+                        const float w = warp_sum16_transposed(ss, lane);
+                        if ((lane & 1) == 0) xch[warp * NPAD + b0 + ((lane >> 1) & 15)] = w;
                         shift_block<NPAD>(v);
                     }
                     epi_bar();
@@ -399,39 +458,34 @@ __global__ void __launch_bounds__(192, 1)
                     const int sec = r / p.D;  // 0: q, 1: k, 2: v (a tile lies in one section)
                     const int idx = r - sec * p.D;
                     const int h = idx / p.dh, d = idx % p.dh;
-                    const bool even = (t & 1) == 0;
-#pragma unroll 1
-                    for (int b0 = 0; b0 < p.B; b0 += 16) {
-                        // rotation factors and ring slots of 16 frames, loaded before the first store
-                        float2 cs[16];
-                        int slot[16];
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int b = b0 + j;
-                            cs[j] = (sec < 2 && b < p.B) ? p.rope_tab[(size_t)b * (p.dh / 2) + (d >> 1)]
-                                                         : make_float2(1.f, 0.f);
-                            slot[j] = (sec > 0 && !p.seq && b < p.B) ? p.st.pos[b] % p.ctx : 0;
+                    auto none = [](int) { return 0; };
+                    if (!aborted) {
+                        if (sec == 0) {
+                            float* dst = p.y + idx;
+                            rope_frames<NPAD>(v, p, d, lane, none,
+                                              [&](int b, float o, int) { dst[(size_t)b * p.y_stride] = o; });
+                        } else if (p.seq) {
+                            // a prefill's K/V stay out of the ring until its attention ran
+                            uint16_t* dst = p.kv_new + (((size_t)(sec - 1) * p.B) * p.H + h) * p.dh + d;
+                            const size_t st = (size_t)p.H * p.dh;
+                            auto put = [&](int b, float o, int) { dst[(size_t)b * st] = f32_to_bf16_rne(o); };
+                            if (sec == 1)
+                                rope_frames<NPAD>(v, p, d, lane, none, put);
+                            else
+                                plain_frames<NPAD>(v, p.B, none, put);
+                        } else {
+                            // frame b is stream b, written to its ring slot pos[b] mod ctx
+                            uint16_t* base = ((sec == 1) ? p.kc : p.vc) + (size_t)h * p.ctx * p.dh + d;
+                            const size_t st = (size_t)p.H * p.ctx * p.dh;
+                            auto slot = [&](int b) { return p.st.pos[b] % p.ctx; };
+                            auto put = [&](int b, float o, int sl) {
+                                base[(size_t)b * st + (size_t)sl * p.dh] = f32_to_bf16_rne(o);
+                            };
+                            if (sec == 1)
+                                rope_frames<NPAD>(v, p, d, lane, slot, put);
+                            else
+                                plain_frames<NPAD>(v, p.B, slot, put);
                         }
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int b = b0 + j;
-                            if (b >= p.B) break;
-                            const float mine = v[j];
-                            const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-                            float o = mine;
-                            if (sec < 2) o = even ? (mine * cs[j].x - other * cs[j].y) : (other * cs[j].y + mine * cs[j].x);
-                            if (aborted) continue;
-                            if (sec == 0) {
-                                p.y[(size_t)b * p.y_stride + idx] = o;
-                            } else if (p.seq) {
-                                // a prefill's K/V stay out of the ring until its attention ran
-                                p.kv_new[(((size_t)(sec - 1) * p.B + b) * p.H + h) * p.dh + d] = f32_to_bf16_rne(o);
-                            } else {
-                                uint16_t* cache = (sec == 1) ? p.kc : p.vc;
-                                cache[(((size_t)b * p.H + h) * p.ctx + slot[j]) * p.dh + d] = f32_to_bf16_rne(o);
-                            }
-                        }
-                        shift_block<NPAD>(v);
                     }
                 } else if (EPI == TE_HEAD) {
                     const int r = m * 128 + t;
