@@ -344,84 +344,93 @@ __global__ void __launch_bounds__(SEQ_NT) k_attn_seq(const AttnSeqParams p) {
 
 }  // namespace
 
-// CTA t: (1) copies row t's K and V (all heads) into the ring slot (p0 + t) mod ctx unless
-// a later row of the pass owns the same slot; (2) when the window took several chunks,
-// merges row t's chunk partials of every head: out = sum_c exp2(m_c - M) o_c / L with
-// M = max_c m_c and L = sum_c exp2(m_c - M) l_c.
+// CTA (t, j) handles row t for heads 8j .. 8j+7: (1) when the window took several chunks,
+// merges the row's chunk partials of those heads, out = sum_c exp2(m_c - M) o_c / L with
+// M = max_c m_c and L = sum_c exp2(m_c - M) l_c (chunks in order); (2) copies the row's K
+// and V of those heads into the ring slot (p0 + t) mod ctx unless a later row of the pass
+// owns the same slot.
+constexpr int CM_HEADS = 8;  // heads per k_seq_commit CTA: 16 threads per head, 8 coordinates each
+
 __global__ void __launch_bounds__(128) k_seq_commit(const AttnSeqParams p) {
-    __shared__ float s_w[PM_SEQ_MAX_HEADS * PM_SEQ_MAX_CHUNKS];
-    __shared__ float s_m[PM_SEQ_MAX_HEADS * PM_SEQ_MAX_CHUNKS];
+    __shared__ float s_w[CM_HEADS * PM_SEQ_MAX_CHUNKS];
+    __shared__ float s_m[CM_HEADS * PM_SEQ_MAX_CHUNKS];
     pdl_trigger();
     pdl_wait();
     if (*(volatile uint32_t*)&p.st.status[1] != 0u) return;
-    const int t = blockIdx.x;
+    const int t = blockIdx.x, h0 = blockIdx.y * CM_HEADS;
+    const int nh = min(CM_HEADS, p.H - h0);
+    const int tid = threadIdx.x;
     const int s = p.io->seq_stream;
     const int p0 = p.st.pos[s];
     const int C = seq_chunks(p0, p.T, p.win).C;
     if (C > 1) {
-        const int H = p.H;
-        const float* pr = p.part + (size_t)t * H * PM_SEQ_MAX_CHUNKS * PSTRIDE;
-        for (int i = threadIdx.x; i < H * C; i += blockDim.x) {
-            const int h = i / C, c = i % C;
-            const float* pc = pr + ((size_t)h * PM_SEQ_MAX_CHUNKS + c) * PSTRIDE;
-            s_m[h * PM_SEQ_MAX_CHUNKS + c] = __ldcg(pc + DH);
-            s_w[h * PM_SEQ_MAX_CHUNKS + c] = __ldcg(pc + DH + 1);
+        const float* pr = p.part + ((size_t)t * p.H + h0) * PM_SEQ_MAX_CHUNKS * PSTRIDE;
+        for (int i = tid; i < nh * C; i += blockDim.x) {
+            const int hh = i / C, c = i % C;
+            const float* pc = pr + ((size_t)hh * PM_SEQ_MAX_CHUNKS + c) * PSTRIDE;
+            s_m[hh * PM_SEQ_MAX_CHUNKS + c] = __ldcg(pc + DH);
+            s_w[hh * PM_SEQ_MAX_CHUNKS + c] = __ldcg(pc + DH + 1);
         }
         __syncthreads();
-        if ((int)threadIdx.x < H) {
-            const int h = threadIdx.x;
+        if (tid < nh) {
+            float* m = s_m + tid * PM_SEQ_MAX_CHUNKS;
+            float* w = s_w + tid * PM_SEQ_MAX_CHUNKS;
             float M = -INFINITY;
-            for (int c = 0; c < C; ++c) M = fmaxf(M, s_m[h * PM_SEQ_MAX_CHUNKS + c]);
+            for (int c = 0; c < C; ++c) M = fmaxf(M, m[c]);
             float L = 0.f;
             for (int c = 0; c < C; ++c) {
-                const float mc = s_m[h * PM_SEQ_MAX_CHUNKS + c];
-                const float f = (mc == -INFINITY) ? 0.f : exp2f(mc - M);
-                s_m[h * PM_SEQ_MAX_CHUNKS + c] = f;
-                L += s_w[h * PM_SEQ_MAX_CHUNKS + c] * f;
+                const float f = (m[c] == -INFINITY) ? 0.f : exp2f(m[c] - M);
+                m[c] = f;
+                L += w[c] * f;
             }
             const float inv = 1.0f / L;
-            for (int c = 0; c < C; ++c) s_w[h * PM_SEQ_MAX_CHUNKS + c] = s_m[h * PM_SEQ_MAX_CHUNKS + c] * inv;
+            for (int c = 0; c < C; ++c) w[c] = m[c] * inv;
         }
         __syncthreads();
-        // thread -> head h = i / 4, 32 consecutive dims 32 (i % 4) .. +31
-        for (int i = threadIdx.x; i < H * 4; i += blockDim.x) {
-            const int h = i >> 2, d0 = (i & 3) * 32;
-            float acc[32];
+        const int hh = tid >> 4, d0 = (tid & 15) * 8;
+        if (hh < nh) {
+            float acc[8];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-            const float* ph = pr + (size_t)h * PM_SEQ_MAX_CHUNKS * PSTRIDE + d0;
-#pragma unroll 2
-            for (int c = 0; c < C; ++c) {
-                const float w = s_w[h * PM_SEQ_MAX_CHUNKS + c];
-                const float4* pc = reinterpret_cast<const float4*>(ph + (size_t)c * PSTRIDE);
+            for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+            const float* ph = pr + (size_t)hh * PM_SEQ_MAX_CHUNKS * PSTRIDE + d0;
+            // eight chunks' loads in flight, then their weighted sums in chunk order
+            for (int c0 = 0; c0 < C; c0 += 8) {
+                float4 a[8][2];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float4 a = __ldcg(pc + e);
-                    acc[4 * e + 0] += a.x * w;
-                    acc[4 * e + 1] += a.y * w;
-                    acc[4 * e + 2] += a.z * w;
-                    acc[4 * e + 3] += a.w * w;
+                for (int j = 0; j < 8; ++j) {
+                    const bool in = c0 + j < C;
+                    const float4* pc = reinterpret_cast<const float4*>(ph + (size_t)(c0 + j) * PSTRIDE);
+                    a[j][0] = in ? __ldcg(pc) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    a[j][1] = in ? __ldcg(pc + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (c0 + j >= C) break;
+                    const float wt = s_w[hh * PM_SEQ_MAX_CHUNKS + c0 + j];
+                    acc[0] += a[j][0].x * wt;
+                    acc[1] += a[j][0].y * wt;
+                    acc[2] += a[j][0].z * wt;
+                    acc[3] += a[j][0].w * wt;
+                    acc[4] += a[j][1].x * wt;
+                    acc[5] += a[j][1].y * wt;
+                    acc[6] += a[j][1].z * wt;
+                    acc[7] += a[j][1].w * wt;
                 }
             }
-            float* ob = p.o + (size_t)t * p.D + h * DH + d0;
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                reinterpret_cast<float4*>(ob)[e] = make_float4(acc[4 * e], acc[4 * e + 1], acc[4 * e + 2], acc[4 * e + 3]);
-            if (p.ob) {
-                uint16_t* bb = p.ob + (size_t)t * p.D + h * DH + d0;
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    reinterpret_cast<uint2*>(bb)[e] = make_uint2(pack_bf16(acc[4 * e], acc[4 * e + 1]),
-                                                                 pack_bf16(acc[4 * e + 2], acc[4 * e + 3]));
-            }
+            const size_t ob = (size_t)t * p.D + (size_t)(h0 + hh) * DH + d0;
+            reinterpret_cast<float4*>(p.o + ob)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            reinterpret_cast<float4*>(p.o + ob)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            if (p.ob)
+                *reinterpret_cast<uint4*>(p.ob + ob) = make_uint4(pack_bf16(acc[0], acc[1]), pack_bf16(acc[2], acc[3]),
+                                                                  pack_bf16(acc[4], acc[5]), pack_bf16(acc[6], acc[7]));
         }
     }
     if (t + p.ctx < p.T) return;
     const int slot = (p0 + t) % p.ctx;
-    const int n16 = p.H * DH / 8;  // 16-byte pieces per row
-    for (int i = threadIdx.x; i < 2 * n16; i += blockDim.x) {
+    const int n16 = nh * DH / 8;  // 16-byte pieces of the CTA's heads in one row
+    for (int i = tid; i < 2 * n16; i += blockDim.x) {
         const int kv = i / n16, j = i % n16;
-        const int h = (j * 8) / DH, d = (j * 8) % DH;
+        const int h = h0 + (j * 8) / DH, d = (j * 8) % DH;
         const uint4 v = *reinterpret_cast<const uint4*>(p.kv_new + (((size_t)kv * p.T + t) * p.H + h) * DH + d);
         uint16_t* dst = const_cast<uint16_t*>(kv ? p.vc : p.kc) + (((size_t)s * p.H + h) * p.ctx + slot) * DH + d;
         *reinterpret_cast<uint4*>(dst) = v;
@@ -429,9 +438,9 @@ __global__ void __launch_bounds__(128) k_seq_commit(const AttnSeqParams p) {
 }
 
 cudaError_t launch_seq_commit(const AttnSeqParams& p, cudaStream_t s, bool pdl) {
-    if (p.H > PM_SEQ_MAX_HEADS || p.T < 1 || p.T > PM_SEQ_MAX_ROWS) return cudaErrorInvalidValue;
+    if (p.H < 1 || p.T < 1 || p.T > PM_SEQ_MAX_ROWS) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.T);
+    cfg.gridDim = dim3((unsigned)p.T, (unsigned)((p.H + CM_HEADS - 1) / CM_HEADS));
     cfg.blockDim = dim3(128);
     cfg.stream = s;
     cudaLaunchAttribute attr[1];

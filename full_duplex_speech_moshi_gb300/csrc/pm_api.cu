@@ -1054,7 +1054,6 @@ extern "C" pm_status pm_create(const pm_config* cfg, const pm_temporal_weights* 
     const size_t ss_floats = std::max((size_t)(f.D / 128) * NP, (size_t)ss_parts_max * 16);
     if (attn_seq_max_chunks(f.ctx) > PM_SEQ_MAX_CHUNKS)
         return bail(PM_ERR_UNSUPPORTED, "ctx too long for the prefill attention");
-    if (f.H > PM_SEQ_MAX_HEADS) return bail(PM_ERR_UNSUPPORTED, "too many heads for the prefill attention");
     c->npad_max = NP;
     c->tc_part_floats = tc_part_floats;
     c->tc_count_max = tc_count_max;

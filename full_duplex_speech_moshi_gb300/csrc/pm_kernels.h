@@ -154,7 +154,6 @@ int attn_max_splits(int ctx);
 #define PM_SEQ_KPC 256           // keys per attention work item
 #define PM_SEQ_MAX_CHUNKS 16     // work items per head (window + rows up to 4096 keys)
 #define PM_SEQ_PART_STRIDE 132   // floats per attention partial (128 values, max, sum, pad)
-#define PM_SEQ_MAX_HEADS 64      // heads the prefill merge holds weights for
 struct SeqPrepParams {
     const FrameIO* io;
     DevState st;
