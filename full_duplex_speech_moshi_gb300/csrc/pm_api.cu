@@ -218,9 +218,11 @@ static pm_status plan(pm_ctx* c, GemvParams& p, int rpu, const char* what) {
 }
 
 // Bytes per CTA of the next projection's weights that a tensor-core projection prefetches
-// into L2 after issuing its own copies (tuning constant; 0 disables).
+// into L2 after issuing its own copies (tuning constant; 0 disables).  Off: with the
+// epilogues rolled, 256 KB per CTA made the 64-row prefill pass and B = 40 about 2% slower
+// (the prefetch competes with the projection's own weight stream).
 #ifndef PM_PF_TC_BYTES
-#define PM_PF_TC_BYTES 262144u
+#define PM_PF_TC_BYTES 0u
 #endif
 
 static NextPrefetch next_tc(pm_ctx* c, int epi, int K, int n_mtiles, int split_rows, int npad) {
