@@ -48,14 +48,15 @@ constexpr int DH = 128;
 #ifndef PM_ATTN_KPC
 #define PM_ATTN_KPC 64
 #endif
-constexpr int KPC = PM_ATTN_KPC;            // keys per unit (32 or 64)
+constexpr int KPC = PM_ATTN_KPC;            // keys per unit (64: the per-warp softmax takes 16 keys per warp)
 constexpr int LPK = 2 * 64 / KPC;           // lanes per key in the scores (4 warps x 32 lanes = KPC x LPK)
 constexpr int NCOL = 128 / LPK / 8;         // 16-byte columns of a key row per lane
 #ifndef PM_ATTN_NST
-#define PM_ATTN_NST 3
+#define PM_ATTN_NST 2
 #endif
-constexpr int NST = PM_ATTN_NST;            // stages per CTA (tuning: fewer let the CTAs share
-                                            // an SM with the projection kernels around them)
+constexpr int NST = PM_ATTN_NST;            // stages per CTA: two (64 KB) let the CTAs share an SM
+                                            // with the projection kernels around them; B=1 frame
+                                            // +1.6% over three, four 8% slower
 constexpr int ROWB = DH * 2;                // bytes per K or V row
 constexpr int STAGE = 2 * KPC * ROWB;       // K rows then V rows: 32 KB
 constexpr int THREADS = 160;                // 4 consumer warps + producer warp
